@@ -1,0 +1,246 @@
+"""fp64 CPU oracle for the forward linear-layer family.
+
+TEST INFRASTRUCTURE ONLY. Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this module. The CUDA library and
+its Python binding never import it, and it imports nothing from them: the two
+sides share no code. The only thing both sides consume is the seeded input
+generator in ``transformer_linear_layer_tcgen05_gb300.workloads``, which holds
+none of the method's arithmetic.
+
+What is computed, and where the pages define it
+-----------------------------------------------
+Page "matmul ve matmul_residual -- Tiled Matrix Multiply (Forward)"
+(llm.istanbul/learn/tr/03_linear_forward), section "Ne Yapar?":
+
+* ``matmul``                    Y[M,N] = X[M,K] @ W[K,N]
+* ``matmul_residual``           Y = X @ W + R, R[M,N] added in the epilogue
+* ``matmul_residual_swiglu_a``  Y = (silu(GATE) * UP) @ W_down + R, the
+                                element-wise SwiGLU product feeding W_down
+* ``*_w16``                     the same three with W stored as IEEE binary16
+                                (list of forward kernels at the top of the page;
+                                "matmul_w16 -- f16 weight versiyonu")
+
+Page "ffn_gelu_backward ve ffn_swiglu_backward"
+(llm.istanbul/learn/tr/09_backward_ffn), section "SiLU'" and
+"WGSL-Spesifik Notlar" note 2: silu(x) = x * sigma(x) with the stable,
+sign-branched sigmoid -- for x >= 0 it is 1 / (1 + exp(-x)), otherwise
+e / (1 + e) with e = exp(x), so exp() never sees a positive argument and no
+clamp is applied. The same page (note 3) says the forward kernels share this
+helper.
+
+Everything is evaluated in float64. Inputs are widened exactly: float32 to
+float64 by numpy, binary16 bit patterns by ``f16_bits_to_f64`` below (an
+IEEE 754 decoder written from the format's definition). The contraction uses
+numpy's float64 matmul as a library primitive; nothing is blocked, fused or
+reordered beyond the definitions above.
+
+Acceptance metric (the normalised error) is ``normalised_error``: for every
+output element, |Y - Y_ref| / S with S[i,j] = sum_k |A[i,k] * W[k,j]|, A being
+X or silu(GATE) * UP. Where S is 0 nothing was accumulated and the element
+must equal the residual (or 0) exactly.
+
+Every function here is pinned by ``tests/test_oracle.py`` against closed forms,
+hand-computed fixtures in ``tests/golden/``, exact integer brute force,
+invariants and numpy's own binary16 type.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = [
+    "sigmoid",
+    "silu",
+    "f16_bits_to_f64",
+    "swiglu_a",
+    "matmul",
+    "matmul_residual",
+    "matmul_residual_swiglu_a",
+    "matmul_w16",
+    "matmul_residual_w16",
+    "matmul_residual_swiglu_a_w16",
+    "normaliser",
+    "normalised_error",
+    "reference",
+    "FORMS",
+]
+
+FORMS = (
+    "matmul",
+    "matmul_residual",
+    "matmul_residual_swiglu_a",
+    "matmul_w16",
+    "matmul_residual_w16",
+    "matmul_residual_swiglu_a_w16",
+)
+
+
+def _f64(a) -> np.ndarray:
+    return np.asarray(a, dtype=np.float64)
+
+
+# --------------------------------------------------------------------------
+# Activation (09_backward_ffn, "SiLU'" and "WGSL-Spesifik Notlar" note 2)
+# --------------------------------------------------------------------------
+
+def sigmoid(x) -> np.ndarray:
+    """Stable sigmoid, branched on the sign of x.
+
+    x >= 0: 1 / (1 + exp(-x));  x < 0: e / (1 + e) with e = exp(x).
+    exp() therefore only sees arguments <= 0: no overflow, and very negative
+    x underflows gracefully towards 0 (09_backward_ffn, note 2).
+    """
+    x = _f64(x)
+    out = np.empty_like(x)
+    nonneg = x >= 0.0
+    out[nonneg] = 1.0 / (1.0 + np.exp(-x[nonneg]))
+    e = np.exp(x[~nonneg])
+    out[~nonneg] = e / (1.0 + e)
+    return out
+
+
+def silu(x) -> np.ndarray:
+    """silu(x) = x * sigmoid(x) (09_backward_ffn, "SiLU'": forward)."""
+    x = _f64(x)
+    return x * sigmoid(x)
+
+
+# --------------------------------------------------------------------------
+# binary16 decoding (the f16 weights of the *_w16 forms)
+# --------------------------------------------------------------------------
+
+def f16_bits_to_f64(bits) -> np.ndarray:
+    """Decode IEEE 754 binary16 bit patterns (uint16) to float64, exactly.
+
+    Layout: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits.
+    exponent 0      -> subnormal: (-1)^s * 2^-14 * (f / 1024)
+    exponent 1..30  -> normal:    (-1)^s * 2^(e-15) * (1 + f / 1024)
+    exponent 31     -> +-inf (f == 0) or NaN (f != 0)
+    """
+    b = np.asarray(bits, dtype=np.uint16).astype(np.int64)
+    sign = np.where((b >> 15) & 1, -1.0, 1.0)
+    e = (b >> 10) & 0x1F
+    f = (b & 0x3FF).astype(np.float64)
+    normal = np.ldexp(1.0 + f / 1024.0, (e - 15).astype(np.int64))
+    subnormal = np.ldexp(f / 1024.0, -14)
+    mag = np.where(e == 0, subnormal, normal)
+    mag = np.where(e == 31, np.where(f == 0.0, np.inf, np.nan), mag)
+    return sign * mag
+
+
+# --------------------------------------------------------------------------
+# The three definitions (03_linear_forward, "Ne Yapar?")
+# --------------------------------------------------------------------------
+
+def swiglu_a(gate, up) -> np.ndarray:
+    """A[i,k] = silu(GATE[i,k]) * UP[i,k]: the SwiGLU hidden matrix that
+    matmul_residual_swiglu_a feeds into W_down (03_linear_forward, "Ne Yapar?"
+    and "Önemli Optimizasyonlar" 3)."""
+    return silu(gate) * _f64(up)
+
+
+def matmul(X, W) -> np.ndarray:
+    """Y[M,N] = X[M,K] @ W[K,N], row-major, in float64."""
+    X = _f64(X)
+    W = _f64(W)
+    if X.ndim != 2 or W.ndim != 2 or X.shape[1] != W.shape[0]:
+        raise ValueError(f"shape mismatch: X{X.shape} @ W{W.shape}")
+    return X @ W
+
+
+def matmul_residual(X, W, R) -> np.ndarray:
+    """Y = X @ W + R (R[M,N] added in the epilogue)."""
+    Y = matmul(X, W)
+    R = _f64(R)
+    if R.shape != Y.shape:
+        raise ValueError(f"residual shape {R.shape} != output shape {Y.shape}")
+    return Y + R
+
+
+def matmul_residual_swiglu_a(GATE, UP, W, R) -> np.ndarray:
+    """Y = (silu(GATE) * UP) @ W_down + R, GATE and UP [M,K], W_down [K,N]."""
+    GATE = _f64(GATE)
+    UP = _f64(UP)
+    if GATE.shape != UP.shape:
+        raise ValueError(f"GATE{GATE.shape} and UP{UP.shape} differ")
+    return matmul_residual(swiglu_a(GATE, UP), W, R)
+
+
+def matmul_w16(X, W16) -> np.ndarray:
+    """matmul with W given as binary16 bit patterns (uint16 [K,N])."""
+    return matmul(X, f16_bits_to_f64(W16))
+
+
+def matmul_residual_w16(X, W16, R) -> np.ndarray:
+    """matmul_residual with binary16 weights."""
+    return matmul_residual(X, f16_bits_to_f64(W16), R)
+
+
+def matmul_residual_swiglu_a_w16(GATE, UP, W16, R) -> np.ndarray:
+    """matmul_residual_swiglu_a with binary16 W_down."""
+    return matmul_residual_swiglu_a(GATE, UP, f16_bits_to_f64(W16), R)
+
+
+# --------------------------------------------------------------------------
+# Acceptance metric
+# --------------------------------------------------------------------------
+
+def normaliser(A, W) -> np.ndarray:
+    """S[i,j] = sum_k |A[i,k] * W[k,j]| = (|A| @ |W|)[i,j], in float64.
+
+    A is the left operand as the definition states it (X, or
+    silu(GATE) * UP), before any rounding a fast path may apply; W is the
+    weight matrix as stored (binary16 values decoded exactly).
+    """
+    return np.abs(_f64(A)) @ np.abs(_f64(W))
+
+
+def normalised_error(Y, Y_ref, S, R=None) -> float:
+    """max_ij |Y - Y_ref| / S over all elements.
+
+    Elements with S == 0 accumulated nothing: there Y must equal float32(R)
+    (or 0 without a residual) exactly, else the error is reported as inf.
+    Non-finite Y anywhere is an infinite error.
+    """
+    Y = _f64(Y)
+    Y_ref = _f64(Y_ref)
+    S = _f64(S)
+    if not (Y.shape == Y_ref.shape == S.shape):
+        raise ValueError("Y, Y_ref and S must have one shape")
+    if Y.size == 0:
+        return 0.0
+    if not np.all(np.isfinite(Y)):
+        return float("inf")
+    zero = S == 0.0
+    err = 0.0
+    if np.any(~zero):
+        err = float(np.max(np.abs(Y[~zero] - Y_ref[~zero]) / S[~zero]))
+    if np.any(zero):
+        expect = np.zeros_like(Y) if R is None else _f64(np.asarray(R, dtype=np.float32))
+        if not np.array_equal(Y[zero], expect[zero]):
+            return float("inf")
+    return err
+
+
+def reference(form: str, inputs: dict, rows=None):
+    """Evaluate ``form`` on an input dict; return (Y_ref, S).
+
+    ``inputs`` holds the arrays named by the C ABI: X or GATE/UP, W (float32)
+    or W16 (uint16 bit patterns), and R for the residual forms. ``rows`` picks
+    a subset of output rows: every output row depends only on the same row of
+    X / GATE / UP / R, so a row subset is the definition applied to those rows.
+    """
+    if form not in FORMS:
+        raise ValueError(f"unknown form {form!r}")
+    sel = (lambda a: a) if rows is None else (lambda a: np.asarray(a)[rows])
+    w16 = form.endswith("_w16")
+    W = f16_bits_to_f64(inputs["W16"]) if w16 else _f64(inputs["W"])
+    if "swiglu" in form:
+        A = swiglu_a(sel(inputs["GATE"]), sel(inputs["UP"]))
+    else:
+        A = _f64(sel(inputs["X"]))
+    if "residual" in form:
+        Y = matmul_residual(A, W, sel(inputs["R"]))
+    else:
+        Y = matmul(A, W)
+    return Y, normaliser(A, W)

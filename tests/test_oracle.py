@@ -1,0 +1,237 @@
+"""Pins for the fp64 oracle (CPU only).
+
+Each test ties the oracle to something other than itself: hand-computed
+fixtures in tests/golden/, closed forms of the sigmoid, exact integer brute
+force, numpy's own binary16 type, and invariants the definitions imply.
+Definitions: llm.istanbul 03_linear_forward ("Ne Yapar?") and
+09_backward_ffn ("SiLU'", "WGSL-Spesifik Notlar" note 2).
+"""
+
+import itertools
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from tests.golden_io import read_blocks, read_rows
+
+
+# ---------------------------------------------------------------- fixtures
+
+def test_golden_matmul_and_residual():
+    g = read_blocks("matmul_3x2x4.txt")
+    assert np.array_equal(oracle.matmul(g["X"], g["W"]), g["Y_matmul"])
+    assert np.array_equal(oracle.matmul_residual(g["X"], g["W"], g["R"]), g["Y_residual"])
+    assert np.array_equal(oracle.normaliser(g["X"], g["W"]), g["S"])
+
+
+def test_golden_swiglu():
+    g = read_blocks("swiglu_2x2x2.txt")
+    A = oracle.swiglu_a(g["GATE"], g["UP"])
+    np.testing.assert_allclose(A, g["A"], rtol=1e-15, atol=0)
+    Y = oracle.matmul_residual_swiglu_a(g["GATE"], g["UP"], g["W"], g["R"])
+    np.testing.assert_allclose(Y, g["Y"], rtol=1e-15, atol=0)
+    np.testing.assert_allclose(oracle.normaliser(A, g["W"]), g["S"], rtol=1e-15, atol=0)
+
+
+def test_golden_sigmoid_closed_forms():
+    for x, s, y in read_rows("sigmoid_closed_forms.txt"):
+        x, s, y = float(x), float(s), float(y)
+        got_s = float(oracle.sigmoid(np.array([x]))[0])
+        got_y = float(oracle.silu(np.array([x]))[0])
+        assert math.isclose(got_s, s, rel_tol=1e-15, abs_tol=0.0), (x, got_s, s)
+        assert math.isclose(got_y, y, rel_tol=1e-15, abs_tol=0.0), (x, got_y, y)
+
+
+def test_golden_f16_bits():
+    for hx, val in read_rows("f16_bits.txt"):
+        got = float(oracle.f16_bits_to_f64(np.array([int(hx, 16)], dtype=np.uint16))[0])
+        want = float(val)
+        if math.isnan(want):
+            assert math.isnan(got)
+        else:
+            assert got == want and math.copysign(1.0, got) == math.copysign(1.0, want), hx
+
+
+# ---------------------------------------------------------------- sigmoid / silu
+
+def test_sigmoid_symmetry_and_range():
+    x = np.linspace(-60.0, 60.0, 4801)
+    s = oracle.sigmoid(x)
+    np.testing.assert_allclose(s + oracle.sigmoid(-x), 1.0, rtol=0, atol=4.5e-16)  # 2 ulp of 1
+    assert np.all((s >= 0.0) & (s <= 1.0))
+    assert np.all(np.diff(s) >= 0.0)            # monotone non-decreasing
+
+
+def test_sigmoid_no_overflow_or_nan():
+    x = np.concatenate([np.linspace(-1000.0, 1000.0, 20001), [-1e300, 1e300, -745.2, 710.0]])
+    with np.errstate(over="raise", invalid="raise"):
+        s = oracle.sigmoid(x)
+        y = oracle.silu(x)
+    assert np.all(np.isfinite(s)) and np.all(np.isfinite(y[np.abs(x) <= 1e3]))
+
+
+def test_silu_identities():
+    x = np.linspace(-30.0, 30.0, 1201)
+    # x*s(x) - (-x)*s(-x) = x*(s(x) + s(-x)) = x
+    np.testing.assert_allclose(oracle.silu(x) - oracle.silu(-x), x, rtol=0, atol=1e-13)
+    assert oracle.silu(np.array([0.0]))[0] == 0.0
+    # derivative at 0 is sigma(0) = 1/2: central difference
+    h = 1e-6
+    d = (oracle.silu(np.array([h])) - oracle.silu(np.array([-h])))[0] / (2 * h)
+    assert abs(d - 0.5) < 1e-9
+
+
+def test_sigmoid_branch_matches_logistic_where_safe():
+    # In the range where exp(-x) cannot overflow, the textbook 1/(1+e^-x) is a
+    # library-independent special case of the same function.
+    x = np.linspace(-30.0, 30.0, 601)
+    np.testing.assert_allclose(oracle.sigmoid(x), 1.0 / (1.0 + np.exp(-x)), rtol=1e-14, atol=0)
+
+
+# ---------------------------------------------------------------- binary16
+
+def test_f16_decoder_all_bit_patterns():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    got = oracle.f16_bits_to_f64(bits)
+    want = bits.view(np.float16).astype(np.float64)
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(want[~nan]))
+
+
+# ---------------------------------------------------------------- contraction
+
+def _int_matrix(rng, shape, lo=-4, hi=4):
+    return rng.integers(lo, hi + 1, size=shape).astype(np.float64)
+
+
+def _brute(X, W):
+    M, K = X.shape
+    N = W.shape[1]
+    out = [[0] * N for _ in range(M)]
+    for i, j in itertools.product(range(M), range(N)):
+        out[i][j] = sum(int(X[i, k]) * int(W[k, j]) for k in range(K))
+    return np.array(out, dtype=np.float64).reshape(M, N)
+
+
+@pytest.mark.parametrize("M,K,N", [(1, 1, 1), (2, 3, 4), (5, 1, 7), (8, 8, 8), (3, 7, 2), (6, 5, 1)])
+def test_integer_brute_force(M, K, N):
+    rng = np.random.default_rng(M * 100 + K * 10 + N)
+    X, W, R = _int_matrix(rng, (M, K)), _int_matrix(rng, (K, N)), _int_matrix(rng, (M, N))
+    want = _brute(X, W)
+    assert np.array_equal(oracle.matmul(X, W), want)
+    assert np.array_equal(oracle.matmul_residual(X, W, R), want + R)
+    assert np.array_equal(oracle.normaliser(X, W), _brute(np.abs(X), np.abs(W)))
+
+
+def test_identity_and_one_hot_weights():
+    rng = np.random.default_rng(7)
+    X = rng.standard_normal((5, 6))
+    assert np.array_equal(oracle.matmul(X, np.eye(6)), X)
+    for k in range(6):
+        for j in (0, 3):
+            W = np.zeros((6, 4))
+            W[k, j] = 1.0
+            Y = oracle.matmul(X, W)
+            assert np.array_equal(Y[:, j], X[:, k])
+            assert np.count_nonzero(Y[:, [c for c in range(4) if c != j]]) == 0
+
+
+def test_residual_invariant_exact():
+    rng = np.random.default_rng(11)
+    X, W, R = _int_matrix(rng, (9, 13)), _int_matrix(rng, (13, 6)), _int_matrix(rng, (9, 6))
+    assert np.array_equal(oracle.matmul_residual(X, W, R) - oracle.matmul(X, W), R)
+
+
+def test_swiglu_reduces_to_product_for_large_gate():
+    # sigma(g) == 1.0 exactly in float64 for g >= 40 (e^-40 < 2^-53), so
+    # silu(g) = g and the fused form is the plain integer product (G*U)@W + R.
+    rng = np.random.default_rng(3)
+    G = rng.integers(40, 60, size=(4, 6)).astype(np.float64)
+    U = _int_matrix(rng, (4, 6))
+    W, R = _int_matrix(rng, (6, 5)), _int_matrix(rng, (4, 5))
+    Y = oracle.matmul_residual_swiglu_a(G, U, W, R)
+    assert np.array_equal(Y, _brute(G * U, W) + R)
+
+
+def test_swiglu_zero_gate_kills_row():
+    # silu(0) = 0, so a zero GATE row contributes nothing: Y row == R row.
+    rng = np.random.default_rng(5)
+    G = rng.standard_normal((3, 8))
+    G[1] = 0.0
+    U, W, R = rng.standard_normal((3, 8)), rng.standard_normal((8, 4)), rng.standard_normal((3, 4))
+    Y = oracle.matmul_residual_swiglu_a(G, U, W, R)
+    assert np.array_equal(Y[1], R[1])
+
+
+def test_swiglu_composition_invariant():
+    rng = np.random.default_rng(9)
+    G, U = 2 * rng.standard_normal((7, 12)), rng.standard_normal((7, 12))
+    W, R = rng.standard_normal((12, 5)), rng.standard_normal((7, 5))
+    fused = oracle.matmul_residual_swiglu_a(G, U, W, R)
+    staged = oracle.matmul_residual(oracle.swiglu_a(G, U), W, R)
+    assert np.array_equal(fused, staged)
+
+
+def test_w16_forms_match_f32_forms_on_representable_weights():
+    rng = np.random.default_rng(13)
+    Wf = rng.standard_normal((6, 8)).astype(np.float16)
+    bits = Wf.view(np.uint16)
+    W = Wf.astype(np.float64)
+    X, G, U = rng.standard_normal((3, 6)), rng.standard_normal((3, 6)), rng.standard_normal((3, 6))
+    R = rng.standard_normal((3, 8))
+    assert np.array_equal(oracle.matmul_w16(X, bits), oracle.matmul(X, W))
+    assert np.array_equal(oracle.matmul_residual_w16(X, bits, R), oracle.matmul_residual(X, W, R))
+    assert np.array_equal(oracle.matmul_residual_swiglu_a_w16(G, U, bits, R),
+                          oracle.matmul_residual_swiglu_a(G, U, W, R))
+
+
+def test_shape_errors():
+    with pytest.raises(ValueError):
+        oracle.matmul(np.zeros((2, 3)), np.zeros((2, 3)))
+    with pytest.raises(ValueError):
+        oracle.matmul_residual(np.zeros((2, 3)), np.zeros((3, 4)), np.zeros((4, 2)))
+    with pytest.raises(ValueError):
+        oracle.matmul_residual_swiglu_a(np.zeros((2, 3)), np.zeros((3, 2)), np.zeros((3, 4)),
+                                        np.zeros((2, 4)))
+
+
+# ---------------------------------------------------------------- metric
+
+def test_normalised_error_values():
+    g = read_blocks("matmul_3x2x4.txt")
+    S = g["S"]
+    Y = g["Y_matmul"].copy()
+    assert oracle.normalised_error(Y, g["Y_matmul"], S) == 0.0
+    Y[2, 3] += 0.23                   # S[2,3] = 23 -> error 0.01
+    assert math.isclose(oracle.normalised_error(Y, g["Y_matmul"], S), 0.01, rel_tol=1e-12)
+    Y[0, 0] += 0.5                    # S[0,0] = 1  -> error 0.5 dominates
+    assert math.isclose(oracle.normalised_error(Y, g["Y_matmul"], S), 0.5, rel_tol=1e-12)
+    Y[1, 1] = np.nan
+    assert oracle.normalised_error(Y, g["Y_matmul"], S) == math.inf
+
+
+def test_normalised_error_zero_rows():
+    S = np.array([[0.0, 0.0], [1.0, 2.0]])
+    R = np.array([[0.1, -2.0], [0.0, 0.0]], dtype=np.float32)
+    ref = np.array([[0.1, -2.0], [1.0, 1.0]])
+    Y = np.array([[np.float32(0.1), -2.0], [1.0, 1.0]])
+    assert oracle.normalised_error(Y, ref, S, R) == 0.0
+    Y2 = Y.copy()
+    Y2[0, 0] = 0.1 + 1e-9                # not the float32 residual
+    assert oracle.normalised_error(Y2, ref, S, R) == math.inf
+    assert oracle.normalised_error(np.zeros((2, 2)), np.zeros((2, 2)), np.zeros((2, 2))) == 0.0
+
+
+def test_reference_row_subset_equals_full():
+    from transformer_linear_layer_tcgen05_gb300.workloads import generate
+    for form in oracle.FORMS:
+        inp = generate(form, 20, 16, 12, seed=42)
+        Y, S = oracle.reference(form, inp)
+        rows = np.array([0, 3, 19, 7])
+        Yr, Sr = oracle.reference(form, inp, rows=rows)
+        assert np.array_equal(Yr, Y[rows]) and np.array_equal(Sr, S[rows])
+        assert np.all(S >= np.abs(Y - (inp["R"] if "R" in inp else 0.0)) - 1e-12)
