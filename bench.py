@@ -1,0 +1,495 @@
+#!/usr/bin/env python3
+"""Benchmark of the forward linear-layer family on one GB300 per rank.
+
+A step is one call of the fused SwiGLU down projection with binary16
+weights, ``lin_matmul_residual_swiglu_a_w16`` at M=16384 tokens, N=2048,
+K=8192 (the scaled-up workload; it runs every step of the hot path: TMA
+staging, the SwiGLU transform, binary16 rounding, the tcgen05 contraction and
+the residual epilogue). Its inputs (1.3 GB) are far larger than the 129 MB
+L2, so no flush is needed between steps.
+
+Printed: one JSON line on rank 0 with the metric (TFLOP/s = 2MNK / time),
+the roofline of the GEMM kernel, the end-to-end figure (host buffers, copies
+inside the timed region), the oracle's CPU baseline, SM clocks sampled during
+the timed region, and a per-workload table for the four small transformer
+shapes (each timed cold, after an L2 flush, and warm, back to back).
+
+``--impl reference`` times the fp64 CPU oracle instead (rank 0 only), each
+step a bounded sample of rows of the same workload.
+
+Multi-GPU: one process per GPU (torchrun); the path shards over tokens with
+no exchange, so every rank runs its own replica of the workload ("replicas
+only", weak scaling) and value = all ranks' FLOPs / the slowest rank's time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from transformer_linear_layer_tcgen05_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "TFLOP/s per linear-form GEMM on 1 GB300 and % of tensor-core roofline"
+HEADLINE = "ffn_down_swiglu_w16_16k"
+SMALL = ("attn_proj_f32", "ffn_up_residual_f32", "ffn_down_swiglu_f32", "lm_head_w16")
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# Nominal dense rates relative to bf16 (2.25 PFLOP/s): f16 1.0, tf32 1.1/2.25.
+NOMINAL_RATIO = {"f16": 1.0, "tf32": 1.1 / 2.25}
+
+
+# ----------------------------------------------------------------- helpers
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    csrc = os.path.join(ROOT, "transformer_linear_layer_tcgen05_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    want = kernel_source_hash()
+    with open(p) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 3 and not line.startswith("#") and parts[0] == workload \
+                    and parts[1] == want:
+                return int(parts[2])
+    return None
+
+
+def mma_dtype(form: str) -> str:
+    return "f16" if form.endswith("_w16") else "tf32"
+
+
+def roofline(w: wl.Workload, peaks: dict, sustained: bool = False):
+    """(bound, roofline TFLOP/s, tensor peak TFLOP/s, HBM GB/s) of workload w:
+    min(peak FLOP/s, algorithmic bytes / HBM bandwidth * FLOP/byte)."""
+    bf16 = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
+    tpeak = bf16 * NOMINAL_RATIO[mma_dtype(w.form)]
+    hbm = peaks["hbm_gbs"]
+    nbytes = wl.input_bytes(w.form, w.M, w.N, w.K)
+    mem_tflops = w.flops / nbytes * hbm / 1e3
+    if mem_tflops < tpeak:
+        return "hbm", mem_tflops, tpeak, hbm
+    return "tensor", tpeak, tpeak, hbm
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons every 200 ms in a thread."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id = gpu_id
+        self.samples = []   # (host time, fields...)
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "200"]
+        if self.gpu_id:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        inside = [s for t, s in self.samples if t0 <= t <= t1 + 0.2]
+        used = inside if inside else [s for _, s in self.samples]
+        if not used:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(s[1]) for s in used if len(s) > 8 and num(s[1]) is not None]
+        smax = [num(s[2]) for s in used if len(s) > 8 and num(s[2]) is not None]
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = set()
+        for s in used:
+            if len(s) > 8:
+                for name, v in zip(names, s[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(name)
+        power = [num(s[3]) for s in used if len(s) > 8 and num(s[3]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons),
+                "power_w_max": max(power) if power else None,
+                "samples": len(used), "samples_in_timed_region": len(inside)}
+
+
+def oracle_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        import numpy  # noqa: F401
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n and max(n) > 0:
+            return max(n)
+    except Exception:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+
+
+def cpu_baseline(w: wl.Workload, inputs: dict, budget_s: float = 12.0, chunk: int = 64):
+    """Time the fp64 oracle, as it stands, on consecutive row chunks of the
+    workload until about `budget_s` seconds of CPU work are done."""
+    import numpy as np
+    import oracle
+    rows_done = 0
+    t0 = time.perf_counter()
+    start = 0
+    while True:
+        rows = np.arange(start, min(start + chunk, w.M))
+        oracle.reference(w.form, inputs, rows=rows)
+        rows_done += len(rows)
+        start = (start + chunk) % w.M
+        if time.perf_counter() - t0 >= budget_s or rows_done >= w.M:
+            break
+    dt = time.perf_counter() - t0
+    flops = 2.0 * rows_done * w.N * w.K
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle_threads(),
+            "kind": "oracle",
+            "sample": f"{rows_done} of {w.M} rows of {w.name} ({w.describe()}), "
+                      f"fp64 numpy oracle incl. normaliser, {dt:.1f} s"}
+
+
+# ----------------------------------------------------------------- reference arm
+
+def run_reference(args, rank: int):
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    w = wl.WORKLOADS_BY_NAME[args.workload]
+    # Only the sampled rows are drawn in full size where needed: the generator
+    # draws the whole workload, then the oracle reads a row sample per step.
+    inputs = wl.generate_workload(w)
+    rows_per_step = args.ref_rows
+    starts = [(i * rows_per_step) % w.M for i in range(args.warmup + args.steps)]
+    for s in starts[:args.warmup]:
+        oracle.reference(w.form, inputs, rows=np.arange(s, min(s + rows_per_step, w.M)))
+    t0 = time.perf_counter()
+    nrows = 0
+    for s in starts[args.warmup:]:
+        rows = np.arange(s, min(s + rows_per_step, w.M))
+        oracle.reference(w.form, inputs, rows=rows)
+        nrows += len(rows)
+    dt = time.perf_counter() - t0
+    value = 2.0 * nrows * w.N * w.K / dt / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / max(args.steps, 1) * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "form": w.form, "M": w.M, "N": w.N, "K": w.K,
+                   "sample_rows_per_step": rows_per_step},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "kind": "oracle",
+                         "cores": oracle_threads(),
+                         "sample": f"{rows_per_step} rows of {w.M} per step"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------- our arm
+
+def device_inputs(inputs: dict):
+    import numpy as np
+    import torch
+    return {k: torch.from_numpy(v.view(np.int16) if v.dtype == np.uint16 else v).cuda()
+            for k, v in inputs.items()}
+
+
+def time_small(w: wl.Workload, iters: int, flush_buf):
+    """Cold (L2 flushed before each call) and warm (graph of back-to-back
+    calls) kernel times of a small workload, in microseconds, plus its error
+    is not computed here (the GPU tests cover parity)."""
+    import torch
+    from transformer_linear_layer_tcgen05_gb300 import lin
+    d = device_inputs(wl.generate_workload(w))
+    Y = torch.empty((w.M, w.N), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    for _ in range(5):
+        lin.run_form(w.form, d, Y)
+    torch.cuda.synchronize()
+    cold = []
+    for _ in range(iters):
+        flush_buf.fill_(1.0)           # evicts L2 and keeps the GPU busy while we enqueue
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        lin.run_form(w.form, d, Y)
+        e1.record(stream)
+        e1.synchronize()
+        cold.append(e0.elapsed_time(e1) * 1e3)
+    # warm: capture `reps` calls into a CUDA graph and replay it
+    reps = 20
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(stream)
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s, capture_error_mode="relaxed"):
+            for _ in range(reps):
+                lin.run_form(w.form, d, Y)
+    stream.wait_stream(s)
+    g.replay()
+    torch.cuda.synchronize()
+    warm = []
+    for _ in range(max(3, iters // 10)):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        e1.synchronize()
+        warm.append(e0.elapsed_time(e1) * 1e3 / reps)
+    assert lin.lin_get_device_status() == lin.LIN_SUCCESS
+    del g
+    return statistics.median(cold), statistics.median(warm)
+
+
+def run_ours(args, rank: int, world: int):
+    import numpy as np
+    import torch
+    from transformer_linear_layer_tcgen05_gb300 import build as _build
+    from transformer_linear_layer_tcgen05_gb300 import lin
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist  # noqa: F811
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    _build.build_library()
+    lin.lib()
+    peaks, peak_src = load_peaks()
+    w = wl.WORKLOADS_BY_NAME[args.workload]
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    # ---- inputs resident in HBM before the timed region
+    host = wl.generate_workload(w)
+    d = device_inputs(host)
+    Y = torch.empty((w.M, w.N), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        lin.run_form(w.form, d, Y)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if lin.lin_get_device_status() != lin.LIN_SUCCESS:
+        raise RuntimeError("device status after warm-up is not LIN_SUCCESS")
+
+    gpu_id = None
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
+    except Exception:
+        gpu_id = None
+    sampler = ClockSampler(gpu_id)
+    sampler.start()
+    time.sleep(0.5)
+
+    barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    h0 = time.time()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    e1.synchronize()
+    h1 = time.time()
+    torch.cuda.synchronize()
+    barrier()
+    sampler.stop()
+    ms = e0.elapsed_time(e1) / max(args.steps, 1)
+    status = lin.lin_get_device_status()
+    if status != lin.LIN_SUCCESS:
+        raise RuntimeError(f"device status {lin.STATUS.get(status, status)} after timed region")
+
+    ms_t = torch.tensor([ms], dtype=torch.float64, device="cuda")
+    if dist is not None:
+        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
+    ms_max = float(ms_t.item())
+    value = world * w.flops / (ms_max * 1e-3) / 1e12
+    kernel_tflops = w.flops / (ms * 1e-3) / 1e12
+
+    # ---- end to end through the public API: pinned host buffers, H2D of the
+    # step's inputs, the call, D2H of Y, all inside the timed region
+    e2e_steps = max(3, min(args.steps, args.e2e_steps))
+    pinned = {k: torch.from_numpy(v.view(np.int16) if v.dtype == np.uint16 else v).pin_memory()
+              for k, v in host.items()}
+    y_host = torch.empty((w.M, w.N), dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in pinned.values())
+    d2h = y_host.numel() * 4
+
+    def e2e_step():
+        for k, t in pinned.items():
+            d[k].copy_(t, non_blocking=True)
+        lin.run_form(w.form, d, Y)
+        y_host.copy_(Y, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    f0 = torch.cuda.Event(enable_timing=True)
+    f1 = torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    f1.record(stream)
+    f1.synchronize()
+    e2e_ms = f0.elapsed_time(f1) / e2e_steps
+    e2e_t = torch.tensor([e2e_ms], dtype=torch.float64, device="cuda")
+    if dist is not None:
+        dist.all_reduce(e2e_t, op=dist.ReduceOp.MAX)
+    e2e_value = world * w.flops / (float(e2e_t.item()) * 1e-3) / 1e12
+    del pinned, y_host
+
+    # ---- roofline of the GEMM kernel (one launch per step)
+    bound, roof, tpeak, hbm = roofline(w, peaks)
+    traffic = recorded_traffic(w.name)
+    roof_obj = {"bound": bound, "achieved": kernel_tflops, "peak": roof, "unit": "TFLOP/s",
+                "frac": kernel_tflops / roof, "traffic": traffic,
+                "peak_source": f"{peak_src} bf16 {'x nominal f16/bf16 ratio 1.0' if mma_dtype(w.form) == 'f16' else 'x nominal tf32/bf16 ratio 0.489'} (burst)",
+                "peak_sustained": roofline(w, peaks, sustained=True)[1],
+                "kernel": "lin_gemm_kernel<A_SWIGLU_F16,resid,128>",
+                "algorithmic_bytes": wl.input_bytes(w.form, w.M, w.N, w.K),
+                "algorithmic_flops": w.flops}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "form": w.form, "M": w.M, "N": w.N, "K": w.K,
+                   "l2": f"inputs {wl.input_bytes(w.form, w.M, w.N, w.K) / 1e9:.2f} GB > L2, no flush",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": roof_obj,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": args.steps,
+        "clocks": sampler.summary(h0, h1),
+    }
+
+    if rank == 0 and not args.no_small:
+        flush = torch.empty(int(2 * L2_BYTES // 4), dtype=torch.float32, device="cuda")
+        table = []
+        for name in SMALL:
+            sw = wl.WORKLOADS_BY_NAME[name]
+            cold_us, warm_us = time_small(sw, args.small_iters, flush)
+            b, r, tp, _ = roofline(sw, peaks)
+            table.append({"workload": name, "form": sw.form, "M": sw.M, "N": sw.N, "K": sw.K,
+                          "bound": b, "roofline_tflops": r,
+                          "cold_us": cold_us, "cold_tflops": sw.flops / cold_us / 1e6,
+                          "cold_frac": sw.flops / cold_us / 1e6 / r,
+                          "warm_us": warm_us, "warm_tflops": sw.flops / warm_us / 1e6,
+                          "warm_frac": sw.flops / warm_us / 1e6 / r})
+        line["workloads"] = table
+        del flush
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, host, budget_s=args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default=HEADLINE, choices=[w.name for w in wl.WORKLOADS])
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--small-iters", type=int, default=50)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-rows", type=int, default=16)
+    ap.add_argument("--no-small", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist.init_process_group("nccl")
+    try:
+        run_ours(args, rank, world)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,168 @@
+/*
+ * lin.h -- C ABI of the GB300 (sm_103a) forward linear-layer library.
+ *
+ * The operations are the forward kernels of the page
+ * "matmul ve matmul_residual -- Tiled Matrix Multiply (Forward)"
+ * (llm.istanbul/learn/tr/03_linear_forward):
+ *
+ *   lin_matmul                       Y = X @ W            ("Ne Yapar?")
+ *   lin_matmul_residual              Y = X @ W + R        ("Ne Yapar?": residual
+ *                                                          added in the epilogue)
+ *   lin_matmul_residual_swiglu_a     Y = (silu(GATE) * UP) @ W + R
+ *                                    ("Ne Yapar?" and "Onemli Optimizasyonlar" 3:
+ *                                     the SwiGLU product is formed while the A tile
+ *                                     is loaded; the [M, K] hidden matrix is never
+ *                                     written to memory)
+ *   lin_*_w16                        the same with W stored as IEEE binary16
+ *                                    (the page's list of forward kernels:
+ *                                     "f16 weight versiyonu")
+ *
+ * silu(x) = x * sigma(x) with the stable, sign-branched sigmoid of the page
+ * "ffn_gelu_backward ve ffn_swiglu_backward" (09_backward_ffn), section "SiLU'".
+ *
+ * Argument order follows the pages' bind-group tables ("Bind Group ABI"):
+ * inputs, then Y, then the dims (M, N, K), then the stream.
+ *
+ * Conventions shared by every compute entry point
+ * -----------------------------------------------
+ * Layout      All matrices are dense and row-major with no padding:
+ *             X, GATE, UP are [M, K]; W is [K, N] (N contiguous, the pages'
+ *             own convention); R and Y are [M, N].
+ * Types       X, GATE, UP, R, Y and the f32 W are IEEE binary32. W16 holds
+ *             IEEE binary16 bit patterns (uint16_t), so this header needs no
+ *             CUDA half type.
+ * Memory      Every pointer is device memory of the current CUDA device,
+ *             owned by the caller. The library keeps no reference after the
+ *             call returns and allocates no device memory per call.
+ * Stream      Work is enqueued on `stream` (a cudaStream_t; NULL means the
+ *             legacy default stream) and the call returns without waiting.
+ *             Inputs must stay valid, and Y must not be read, until the
+ *             stream reaches the call.
+ * Arithmetic  The f32 forms run the contraction on the tensor cores in TF32
+ *             (operands keep their 10 explicit mantissa bits) with float32
+ *             accumulation. The w16 forms round the A operand (X, or
+ *             silu(GATE) * UP) to binary16, round-to-nearest-even, and
+ *             multiply binary16 x binary16 with float32 accumulation. The
+ *             residual is added once in float32. Results satisfy
+ *             max |Y - Y_exact| / sum_k |A[i,k] W[k,j]| <= 4e-3.
+ *             Values of A beyond the binary16 range (|A| > 65504) become
+ *             +-inf in the w16 forms.
+ *
+ * Validation (synchronous, before anything is enqueued) and error behaviour
+ * ------------------------------------------------------------------------
+ *   M < 0, N < 0 or K < 0, or a required pointer NULL -> LIN_ERROR_INVALID_VALUE
+ *   M == 0 or N == 0                        -> LIN_SUCCESS, nothing enqueued
+ *                                              (pointers are not inspected)
+ *   K == 0                                  -> Y = R (or Y = 0 without a residual);
+ *                                              X/GATE/UP/W are not read and may be NULL
+ *   K % 4 != 0 or N % 4 != 0                -> LIN_ERROR_UNSUPPORTED_SHAPE
+ *                                              (the pages' vec4 rule, "Vec4 Tile Loads")
+ *   w16 forms: N % 8 != 0                   -> LIN_ERROR_UNSUPPORTED_SHAPE
+ *                                              (a binary16 W row must be a multiple of
+ *                                              16 bytes for the tensor-memory copies)
+ *   M, N or K > 2^31 - 1                    -> LIN_ERROR_UNSUPPORTED_SHAPE
+ *   any pointer not 16-byte aligned         -> LIN_ERROR_MISALIGNED
+ *   a buffer that is not device memory of the current device, or whose
+ *   allocation is smaller than its extent   -> LIN_ERROR_INVALID_VALUE
+ *   Y overlapping any input                 -> LIN_ERROR_ALIASING (in-place
+ *                                              residual included; the pages forbid a
+ *                                              buffer bound both read and read_write)
+ *   current device not sm_103               -> LIN_ERROR_UNSUPPORTED_DEVICE
+ *   a CUDA runtime/driver failure           -> LIN_ERROR_CUDA (lin_last_cuda_error()
+ *                                              returns the cudaError_t value)
+ * On any error nothing is enqueued and Y is untouched.
+ *
+ * Device-side failures. Every wait inside the kernels is bounded (about one
+ * second by default). A wait that runs out records LIN_ERROR_TIMEOUT in a
+ * per-device status word and the kernel exits cleanly; the next
+ * lin_get_device_status() call reports and clears it. This is never expected
+ * on a correct build; it exists so a scheduling bug cannot hang the GPU.
+ *
+ * Thread safety: every entry point may be called from several host threads.
+ */
+#ifndef LIN_H
+#define LIN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream; NULL is the legacy default stream. */
+typedef struct CUstream_st *lin_stream_t;
+
+typedef enum lin_status {
+  LIN_SUCCESS = 0,
+  LIN_ERROR_INVALID_VALUE = 1,
+  LIN_ERROR_UNSUPPORTED_SHAPE = 2,
+  LIN_ERROR_MISALIGNED = 3,
+  LIN_ERROR_ALIASING = 4,
+  LIN_ERROR_UNSUPPORTED_DEVICE = 5,
+  LIN_ERROR_CUDA = 6,
+  LIN_ERROR_TIMEOUT = 7
+} lin_status;
+
+/* Y[M,N] = X[M,K] @ W[K,N]; X, W, Y binary32.
+ * 03_linear_forward, "Ne Yapar?"; bind group "matmul" (X, W, Y, dims). */
+lin_status lin_matmul(const float *X, const float *W, float *Y,
+                      int64_t M, int64_t N, int64_t K, lin_stream_t stream);
+
+/* Y = X @ W + R; R[M,N] binary32, must not overlap Y.
+ * 03_linear_forward, "Ne Yapar?"; bind group "matmul_residual". */
+lin_status lin_matmul_residual(const float *X, const float *W, const float *R, float *Y,
+                               int64_t M, int64_t N, int64_t K, lin_stream_t stream);
+
+/* Y = (silu(GATE) * UP) @ W + R; GATE, UP [M,K], W [K,N] (W_down), R [M,N].
+ * K is the FFN width (d_ff). The product silu(GATE) * UP is formed on chip and
+ * never stored. 03_linear_forward, "Ne Yapar?" and "Onemli Optimizasyonlar" 3;
+ * bind group "matmul_residual_swiglu_a" (GATE, UP, W, R, Y, dims). */
+lin_status lin_matmul_residual_swiglu_a(const float *GATE, const float *UP, const float *W,
+                                        const float *R, float *Y,
+                                        int64_t M, int64_t N, int64_t K, lin_stream_t stream);
+
+/* lin_matmul with binary16 weights W16[K,N] (bit patterns). N % 8 == 0.
+ * 03_linear_forward, forward kernel list: "matmul_w16". */
+lin_status lin_matmul_w16(const float *X, const uint16_t *W16, float *Y,
+                          int64_t M, int64_t N, int64_t K, lin_stream_t stream);
+
+/* lin_matmul_residual with binary16 weights. N % 8 == 0.
+ * 03_linear_forward, forward kernel list: "matmul_residual_w16". */
+lin_status lin_matmul_residual_w16(const float *X, const uint16_t *W16, const float *R,
+                                   float *Y, int64_t M, int64_t N, int64_t K,
+                                   lin_stream_t stream);
+
+/* lin_matmul_residual_swiglu_a with binary16 W_down. N % 8 == 0.
+ * 03_linear_forward, forward kernel list: "matmul_residual_swiglu_a_w16". */
+lin_status lin_matmul_residual_swiglu_a_w16(const float *GATE, const float *UP,
+                                            const uint16_t *W16, const float *R, float *Y,
+                                            int64_t M, int64_t N, int64_t K,
+                                            lin_stream_t stream);
+
+/* Static, NUL-terminated name of a status code ("LIN_SUCCESS", ...). Never NULL. */
+const char *lin_status_string(lin_status status);
+
+/* The cudaError_t value behind the calling thread's last LIN_ERROR_CUDA (0 if none). */
+int lin_last_cuda_error(void);
+
+/* Waits for `stream`, then returns and clears the current device's status
+ * word: LIN_SUCCESS, or LIN_ERROR_TIMEOUT if a kernel gave up on a wait since
+ * the last call. Returns LIN_ERROR_CUDA if the synchronisation itself fails. */
+lin_status lin_get_device_status(lin_stream_t stream);
+
+/* Self-test of the bounded waits: enqueues one small kernel whose data
+ * producer is told never to start, so every consumer's wait runs out after
+ * `timeout_us` microseconds (1 .. 10,000,000); the kernel records
+ * LIN_ERROR_TIMEOUT and exits cleanly. Waits for `stream` and returns the
+ * status word (then cleared): LIN_ERROR_TIMEOUT when the mechanism works.
+ * No memory is touched. */
+lin_status lin_selftest_wait_timeout(int64_t timeout_us, lin_stream_t stream);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int lin_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIN_H */

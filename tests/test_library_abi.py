@@ -1,0 +1,101 @@
+"""The C-ABI library builds, loads and exports every symbol of include/lin.h
+(CPU only: no compute call is made).
+
+The host-side validation of the library rejects bad dims, shapes, alignment
+and aliasing before it touches CUDA, so those paths are exercised here too
+with fake, never-dereferenced addresses.
+"""
+
+import os
+import re
+
+import pytest
+
+from transformer_linear_layer_tcgen05_gb300 import build, lin
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                      "include", "lin.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build_library()
+    return lin.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(lin_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_family():
+    names = declared_functions()
+    for form in ("matmul", "matmul_residual", "matmul_residual_swiglu_a"):
+        assert f"lin_{form}" in names and f"lin_{form}_w16" in names
+    assert {"lin_status_string", "lin_get_device_status", "lin_last_cuda_error",
+            "lin_selftest_wait_timeout", "lin_version"} <= set(names)
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_binding_covers_every_compute_entry_point():
+    for name in declared_functions():
+        if name.startswith("lin_matmul"):
+            assert name in lin.SIGNATURES
+            assert name[len("lin_"):] in lin.FORM_FUNCS
+
+
+def test_status_strings(L):
+    for code, name in lin.STATUS.items():
+        assert lin.status_string(code) == name
+    assert lin.status_string(99) == "LIN_ERROR_UNKNOWN"
+    assert L.lin_version() >= 100
+
+
+# Fake device addresses: validation rejects these calls before any CUDA call.
+X, W, R, Y, G, U = 0x10000000, 0x20000000, 0x30000000, 0x40000000, 0x50000000, 0x60000000
+
+
+def test_negative_dims_and_null_pointers(L):
+    assert L.lin_matmul(X, W, Y, -1, 8, 8, None) == lin.LIN_ERROR_INVALID_VALUE
+    assert L.lin_matmul(X, W, Y, 8, 8, -4, None) == lin.LIN_ERROR_INVALID_VALUE
+    assert L.lin_matmul(X, W, None, 8, 8, 8, None) == lin.LIN_ERROR_INVALID_VALUE
+    assert L.lin_matmul(None, W, Y, 8, 8, 8, None) == lin.LIN_ERROR_INVALID_VALUE
+    assert L.lin_matmul_residual(X, W, None, Y, 8, 8, 8, None) == lin.LIN_ERROR_INVALID_VALUE
+    assert L.lin_matmul_residual_swiglu_a(G, None, W, R, Y, 8, 8, 8, None) == \
+        lin.LIN_ERROR_INVALID_VALUE
+    assert L.lin_matmul_residual_swiglu_a_w16(None, U, W, R, Y, 8, 8, 8, None) == \
+        lin.LIN_ERROR_INVALID_VALUE
+
+
+def test_empty_problems_are_noops(L):
+    assert L.lin_matmul(None, None, None, 0, 8, 8, None) == lin.LIN_SUCCESS
+    assert L.lin_matmul_residual_w16(None, None, None, None, 8, 0, 8, None) == lin.LIN_SUCCESS
+
+
+def test_shape_rules(L):
+    assert L.lin_matmul(X, W, Y, 8, 8, 6, None) == lin.LIN_ERROR_UNSUPPORTED_SHAPE   # K % 4
+    assert L.lin_matmul(X, W, Y, 8, 6, 8, None) == lin.LIN_ERROR_UNSUPPORTED_SHAPE   # N % 4
+    assert L.lin_matmul_w16(X, W, Y, 8, 12, 8, None) == lin.LIN_ERROR_UNSUPPORTED_SHAPE  # N % 8
+    assert L.lin_matmul(X, W, Y, 2**31, 8, 8, None) == lin.LIN_ERROR_UNSUPPORTED_SHAPE
+
+
+def test_alignment_rule(L):
+    assert L.lin_matmul(X + 4, W, Y, 8, 8, 8, None) == lin.LIN_ERROR_MISALIGNED
+    assert L.lin_matmul_residual(X, W, R + 8, Y, 8, 8, 8, None) == lin.LIN_ERROR_MISALIGNED
+    assert L.lin_matmul_w16(X, W + 2, Y, 8, 8, 8, None) == lin.LIN_ERROR_MISALIGNED
+
+
+def test_aliasing_rule(L):
+    # in-place residual
+    assert L.lin_matmul_residual(X, W, Y, Y, 8, 8, 8, None) == lin.LIN_ERROR_ALIASING
+    # Y overlapping the tail of X: X is 8x8 f32 = 256 bytes
+    assert L.lin_matmul(X, W, X + 240, 8, 8, 8, None) == lin.LIN_ERROR_ALIASING
+    assert L.lin_matmul_residual_swiglu_a(G, U, W, R, U + 16, 8, 8, 8, None) == \
+        lin.LIN_ERROR_ALIASING
+    # adjacent but disjoint is not aliasing (it fails later, at the device check)
+    assert L.lin_matmul(X, W, X + 256, 8, 8, 8, None) != lin.LIN_ERROR_ALIASING

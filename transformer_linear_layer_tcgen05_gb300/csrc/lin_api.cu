@@ -1,0 +1,372 @@
+// lin_api.cu -- the C ABI of include/lin.h: argument validation, tensor-map
+// encoding and kernel launch. No allocation, no host<->device copies on the
+// compute path; every operation runs in the kernels of lin_gemm.cuh.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "lin.h"
+#include "lin_internal.h"
+
+namespace lin_detail {
+
+// Per-device status word written by kernels whose bounded waits ran out.
+__device__ int g_status_word;
+
+constexpr uint64_t kDefaultTimeoutNs = 1000ull * 1000ull * 1000ull;   // 1 s per wait
+constexpr int kMaxDevices = 64;
+
+thread_local int t_last_cuda_error = 0;
+
+lin_status cuda_fail(cudaError_t e) {
+  t_last_cuda_error = static_cast<int>(e);
+  cudaGetLastError();   // clear the sticky-free error so later calls start clean
+  return LIN_ERROR_CUDA;
+}
+
+// Driver entry points, fetched through the runtime so the library does not
+// link libcuda directly.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+typedef CUresult (*AddressRangeFn)(CUdeviceptr*, size_t*, CUdeviceptr);
+
+struct Driver {
+  EncodeTiledFn encode = nullptr;
+  AddressRangeFn range = nullptr;
+};
+
+const Driver& driver() {
+  static Driver d;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      d.encode = reinterpret_cast<EncodeTiledFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuMemGetAddressRange", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      d.range = reinterpret_cast<AddressRangeFn>(p);
+    cudaGetLastError();
+  });
+  return d;
+}
+
+struct DeviceState {
+  std::once_flag once;
+  lin_status status = LIN_SUCCESS;
+  int cuda_error = 0;
+  int* status_word = nullptr;
+};
+DeviceState g_devices[kMaxDevices];
+
+// Checks the current device once (sm_103, driver entry points, status word).
+lin_status current_device(int* dev_out, int** status_word) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return LIN_ERROR_UNSUPPORTED_DEVICE;
+  DeviceState& s = g_devices[dev];
+  std::call_once(s.once, [&] {
+    int major = 0, minor = 0;
+    cudaError_t e1 = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaError_t e2 = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (e1 != cudaSuccess || e2 != cudaSuccess) {
+      s.status = LIN_ERROR_CUDA;
+      s.cuda_error = static_cast<int>(e1 != cudaSuccess ? e1 : e2);
+      cudaGetLastError();
+      return;
+    }
+    if (major != 10 || minor != 3) {
+      s.status = LIN_ERROR_UNSUPPORTED_DEVICE;
+      return;
+    }
+    const Driver& d = driver();
+    if (!d.encode || !d.range) {
+      s.status = LIN_ERROR_CUDA;
+      s.cuda_error = static_cast<int>(cudaErrorSymbolNotFound);
+      return;
+    }
+    void* p = nullptr;
+    cudaError_t e3 = cudaGetSymbolAddress(&p, g_status_word);
+    if (e3 != cudaSuccess) {
+      s.status = LIN_ERROR_CUDA;
+      s.cuda_error = static_cast<int>(e3);
+      cudaGetLastError();
+      return;
+    }
+    s.status_word = static_cast<int*>(p);
+  });
+  if (s.status == LIN_ERROR_CUDA) t_last_cuda_error = s.cuda_error;
+  if (s.status != LIN_SUCCESS) return s.status;
+  *dev_out = dev;
+  *status_word = s.status_word;
+  return LIN_SUCCESS;
+}
+
+// The buffer [p, p + bytes) must be device (or managed) memory of `dev`
+// lying inside one allocation.
+lin_status check_buffer(const void* p, uint64_t bytes, int dev) {
+  cudaPointerAttributes a;
+  cudaError_t e = cudaPointerGetAttributes(&a, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return LIN_ERROR_INVALID_VALUE;
+  }
+  if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged) return LIN_ERROR_INVALID_VALUE;
+  if (a.device != dev) return LIN_ERROR_INVALID_VALUE;
+  CUdeviceptr base = 0;
+  size_t size = 0;
+  if (driver().range(&base, &size, reinterpret_cast<CUdeviceptr>(p)) != CUDA_SUCCESS)
+    return LIN_ERROR_INVALID_VALUE;
+  const uint64_t off = static_cast<uint64_t>(reinterpret_cast<uintptr_t>(p)) - base;
+  if (off > size || bytes > size - off) return LIN_ERROR_INVALID_VALUE;
+  return LIN_SUCCESS;
+}
+
+bool overlaps(const void* a, uint64_t abytes, const void* b, uint64_t bbytes) {
+  if (!a || !b || abytes == 0 || bbytes == 0) return false;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + bbytes && b0 < a0 + abytes;
+}
+
+// 2-D row-major tensor map with the 128-byte swizzle; out-of-range elements
+// of a load read as zero.
+bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t cols,
+               uint64_t rows, uint64_t row_bytes, uint32_t box_cols, uint32_t box_rows) {
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return driver().encode(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+enum Form : int { F_MATMUL = 0, F_RESID = 1, F_SWIGLU = 2 };
+
+struct Problem {
+  Form form;
+  bool w16;
+  const float* X;      // matmul / residual forms
+  const float* G;      // SwiGLU forms
+  const float* U;
+  const void* W;       // float or binary16 bits
+  const float* R;
+  float* Y;
+  int64_t M, N, K;
+};
+
+lin_status run(const Problem& p, cudaStream_t stream) {
+  // 1. dims and required pointers
+  if (p.M < 0 || p.N < 0 || p.K < 0) return LIN_ERROR_INVALID_VALUE;
+  if (p.M == 0 || p.N == 0) return LIN_SUCCESS;
+  const bool resid = p.form != F_MATMUL;
+  const bool swiglu = p.form == F_SWIGLU;
+  if (!p.Y || (resid && !p.R)) return LIN_ERROR_INVALID_VALUE;
+  if (p.K > 0 && (!p.W || (swiglu ? (!p.G || !p.U) : !p.X))) return LIN_ERROR_INVALID_VALUE;
+
+  // 2. shapes
+  const int64_t kMax = 0x7fffffffLL;
+  if (p.M > kMax || p.N > kMax || p.K > kMax) return LIN_ERROR_UNSUPPORTED_SHAPE;
+  if (p.K % 4 != 0 || p.N % 4 != 0) return LIN_ERROR_UNSUPPORTED_SHAPE;
+  if (p.w16 && p.N % 8 != 0) return LIN_ERROR_UNSUPPORTED_SHAPE;
+
+  const uint64_t M = p.M, N = p.N, K = p.K;
+  const uint64_t a_bytes = M * K * 4, w_bytes = K * N * (p.w16 ? 2 : 4), mn_bytes = M * N * 4;
+
+  // 3. alignment (16 bytes: TMA base addresses and vector accesses)
+  auto misaligned = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) != 0; };
+  if (misaligned(p.Y) || (resid && misaligned(p.R))) return LIN_ERROR_MISALIGNED;
+  if (K > 0 && (misaligned(p.W) || (swiglu ? (misaligned(p.G) || misaligned(p.U))
+                                           : misaligned(p.X))))
+    return LIN_ERROR_MISALIGNED;
+
+  // 4. aliasing: Y may overlap no input
+  if (resid && overlaps(p.Y, mn_bytes, p.R, mn_bytes)) return LIN_ERROR_ALIASING;
+  if (K > 0) {
+    if (overlaps(p.Y, mn_bytes, p.W, w_bytes)) return LIN_ERROR_ALIASING;
+    if (swiglu) {
+      if (overlaps(p.Y, mn_bytes, p.G, a_bytes) || overlaps(p.Y, mn_bytes, p.U, a_bytes))
+        return LIN_ERROR_ALIASING;
+    } else if (overlaps(p.Y, mn_bytes, p.X, a_bytes)) {
+      return LIN_ERROR_ALIASING;
+    }
+  }
+
+  // 5. device
+  int dev = 0;
+  int* status_word = nullptr;
+  lin_status st = current_device(&dev, &status_word);
+  if (st != LIN_SUCCESS) return st;
+
+  // 6. every buffer is device memory of this device and large enough
+  if ((st = check_buffer(p.Y, mn_bytes, dev)) != LIN_SUCCESS) return st;
+  if (resid && (st = check_buffer(p.R, mn_bytes, dev)) != LIN_SUCCESS) return st;
+  if (K > 0) {
+    if ((st = check_buffer(p.W, w_bytes, dev)) != LIN_SUCCESS) return st;
+    if (swiglu) {
+      if ((st = check_buffer(p.G, a_bytes, dev)) != LIN_SUCCESS) return st;
+      if ((st = check_buffer(p.U, a_bytes, dev)) != LIN_SUCCESS) return st;
+    } else if ((st = check_buffer(p.X, a_bytes, dev)) != LIN_SUCCESS) {
+      return st;
+    }
+  }
+
+  // 7. K == 0: nothing is accumulated, Y = R (or 0)
+  if (K == 0) {
+    cudaError_t e = resid ? cudaMemcpyAsync(p.Y, p.R, mn_bytes, cudaMemcpyDeviceToDevice, stream)
+                          : cudaMemsetAsync(p.Y, 0, mn_bytes, stream);
+    return e == cudaSuccess ? LIN_SUCCESS : cuda_fail(e);
+  }
+
+  // 8. tensor maps and launch
+  const int bn = 128;
+  lin::TensorMaps maps;
+  std::memset(&maps, 0, sizeof(maps));
+  const CUtensorMapDataType f32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  bool ok = true;
+  const float* a_src = swiglu ? p.G : p.X;
+  ok &= encode_2d(&maps.a, f32, a_src, K, M, K * 4, 32, lin::kBM);
+  if (swiglu) ok &= encode_2d(&maps.u, f32, p.U, K, M, K * 4, 32, lin::kBM);
+  if (p.w16)
+    ok &= encode_2d(&maps.w, CU_TENSOR_MAP_DATA_TYPE_UINT16, p.W, N, K, N * 2, 64, 64);
+  else
+    ok &= encode_2d(&maps.w, f32, p.W, N, K, N * 4, 32, 32);
+  if (resid) ok &= encode_2d(&maps.r, f32, p.R, N, M, N * 4, lin::kEpiCols, lin::kEpiRows);
+  ok &= encode_2d(&maps.y, f32, p.Y, N, M, N * 4, lin::kEpiCols, lin::kEpiRows);
+  if (!ok) return cuda_fail(cudaErrorInvalidValue);
+
+  lin::KernelArgs args;
+  args.M = static_cast<int32_t>(M);
+  args.N = static_cast<int32_t>(N);
+  args.K = static_cast<int32_t>(K);
+  args.flags = 0;
+  args.timeout_ns = kDefaultTimeoutNs;
+  args.status = status_word;
+
+  cudaError_t e;
+  if (p.w16)
+    e = lin::launch_gemm_f16(swiglu ? lin::A_SWIGLU_F16 : lin::A_CVT_F16, resid, bn, maps, args,
+                             stream);
+  else
+    e = lin::launch_gemm_tf32(swiglu ? lin::A_SWIGLU_F32 : lin::A_TMA_F32, resid, bn, maps, args,
+                              stream);
+  return e == cudaSuccess ? LIN_SUCCESS : cuda_fail(e);
+}
+
+lin_status read_and_clear_status(cudaStream_t stream) {
+  int dev = 0;
+  int* word = nullptr;
+  lin_status st = current_device(&dev, &word);
+  if (st != LIN_SUCCESS) return st;
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  int v = 0;
+  e = cudaMemcpyFromSymbol(&v, g_status_word, sizeof(int));
+  if (e != cudaSuccess) return cuda_fail(e);
+  const int zero = 0;
+  e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof(int));
+  if (e != cudaSuccess) return cuda_fail(e);
+  return v == lin::KSTATUS_TIMEOUT ? LIN_ERROR_TIMEOUT : LIN_SUCCESS;
+}
+
+}  // namespace lin_detail
+
+using namespace lin_detail;
+
+extern "C" {
+
+lin_status lin_matmul(const float* X, const float* W, float* Y, int64_t M, int64_t N, int64_t K,
+                      lin_stream_t stream) {
+  return run({F_MATMUL, false, X, nullptr, nullptr, W, nullptr, Y, M, N, K},
+             reinterpret_cast<cudaStream_t>(stream));
+}
+
+lin_status lin_matmul_residual(const float* X, const float* W, const float* R, float* Y,
+                               int64_t M, int64_t N, int64_t K, lin_stream_t stream) {
+  return run({F_RESID, false, X, nullptr, nullptr, W, R, Y, M, N, K},
+             reinterpret_cast<cudaStream_t>(stream));
+}
+
+lin_status lin_matmul_residual_swiglu_a(const float* GATE, const float* UP, const float* W,
+                                        const float* R, float* Y, int64_t M, int64_t N, int64_t K,
+                                        lin_stream_t stream) {
+  return run({F_SWIGLU, false, nullptr, GATE, UP, W, R, Y, M, N, K},
+             reinterpret_cast<cudaStream_t>(stream));
+}
+
+lin_status lin_matmul_w16(const float* X, const uint16_t* W16, float* Y, int64_t M, int64_t N,
+                          int64_t K, lin_stream_t stream) {
+  return run({F_MATMUL, true, X, nullptr, nullptr, W16, nullptr, Y, M, N, K},
+             reinterpret_cast<cudaStream_t>(stream));
+}
+
+lin_status lin_matmul_residual_w16(const float* X, const uint16_t* W16, const float* R, float* Y,
+                                   int64_t M, int64_t N, int64_t K, lin_stream_t stream) {
+  return run({F_RESID, true, X, nullptr, nullptr, W16, R, Y, M, N, K},
+             reinterpret_cast<cudaStream_t>(stream));
+}
+
+lin_status lin_matmul_residual_swiglu_a_w16(const float* GATE, const float* UP,
+                                            const uint16_t* W16, const float* R, float* Y,
+                                            int64_t M, int64_t N, int64_t K,
+                                            lin_stream_t stream) {
+  return run({F_SWIGLU, true, nullptr, GATE, UP, W16, R, Y, M, N, K},
+             reinterpret_cast<cudaStream_t>(stream));
+}
+
+const char* lin_status_string(lin_status status) {
+  switch (status) {
+    case LIN_SUCCESS: return "LIN_SUCCESS";
+    case LIN_ERROR_INVALID_VALUE: return "LIN_ERROR_INVALID_VALUE";
+    case LIN_ERROR_UNSUPPORTED_SHAPE: return "LIN_ERROR_UNSUPPORTED_SHAPE";
+    case LIN_ERROR_MISALIGNED: return "LIN_ERROR_MISALIGNED";
+    case LIN_ERROR_ALIASING: return "LIN_ERROR_ALIASING";
+    case LIN_ERROR_UNSUPPORTED_DEVICE: return "LIN_ERROR_UNSUPPORTED_DEVICE";
+    case LIN_ERROR_CUDA: return "LIN_ERROR_CUDA";
+    case LIN_ERROR_TIMEOUT: return "LIN_ERROR_TIMEOUT";
+  }
+  return "LIN_ERROR_UNKNOWN";
+}
+
+int lin_last_cuda_error(void) { return t_last_cuda_error; }
+
+lin_status lin_get_device_status(lin_stream_t stream) {
+  return read_and_clear_status(reinterpret_cast<cudaStream_t>(stream));
+}
+
+lin_status lin_selftest_wait_timeout(int64_t timeout_us, lin_stream_t stream) {
+  if (timeout_us < 1 || timeout_us > 10000000) return LIN_ERROR_INVALID_VALUE;
+  int dev = 0;
+  int* word = nullptr;
+  lin_status st = current_device(&dev, &word);
+  if (st != LIN_SUCCESS) return st;
+  // The producers issue nothing, so the tensor maps are never dereferenced.
+  lin::TensorMaps maps;
+  std::memset(&maps, 0, sizeof(maps));
+  lin::KernelArgs args;
+  args.M = 128;
+  args.N = 128;
+  args.K = 128;
+  args.flags = lin::KFLAG_WITHHOLD_PRODUCER;
+  args.timeout_ns = static_cast<uint64_t>(timeout_us) * 1000ull;
+  args.status = word;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = lin::launch_gemm_tf32(lin::A_TMA_F32, false, 128, maps, args, s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return read_and_clear_status(s);
+}
+
+int lin_version(void) { return 100; }
+
+}  // extern "C"

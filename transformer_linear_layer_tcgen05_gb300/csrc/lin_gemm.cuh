@@ -1,0 +1,497 @@
+// lin_gemm.cuh -- the warp-specialised tcgen05 GEMM behind every forward
+// form of the linear-layer family (page "matmul ve matmul_residual -- Tiled
+// Matrix Multiply (Forward)", 03_linear_forward):
+//
+//   Y[M,N] = A[M,K] @ W[K,N] (+ R[M,N])
+//
+// with A = X (matmul, matmul_residual and their _w16 forms) or
+// A = silu(GATE) * UP (matmul_residual_swiglu_a and its _w16 form).
+//
+// One CTA computes one 128 x BN output tile with the accumulator in TMEM.
+// Eight warps:
+//   warp 0      TMA producer of the W tiles (and of X for the TF32 path)
+//   warp 1      single-thread UMMA issuer (tcgen05.mma + tcgen05.commit)
+//   warp 2      TMEM allocator
+//   warp 3      TMA producer of the raw f32 inputs the transform warps read
+//   warps 4-7   transform warps (build the A operand in shared memory), then
+//               the epilogue (TMEM -> registers, + R, TMA store of Y)
+//
+// The pages' design (64x64 tiles, 4x4 FMA sub-tiles per thread, TK = 16,
+// double-buffered workgroup memory, "Algoritma" and "Önemli Optimizasyonlar")
+// maps here to: a 128 x BN UMMA tile, a k-block of one 128-byte swizzle row
+// (32 f32 or 64 f16), an NS-deep mbarrier ring instead of two buffers, and TMA
+// out-of-bounds zero fill instead of `select` masking ("Code Review",
+// Bulgu 1). The SwiGLU prologue fusion ("Önemli Optimizasyonlar" 3) becomes
+// the transform warps: they compute silu(GATE) * UP from TMA-staged f32 tiles
+// and write the swizzled UMMA operand straight into shared memory.
+#pragma once
+
+#include <cuda_fp16.h>
+
+#include <atomic>
+
+#include "lin_internal.h"
+#include "lin_ptx.cuh"
+
+namespace lin {
+
+template <int AMODE, bool RESID, int BN_>
+struct GemmTraits {
+  static constexpr bool kF16 = (AMODE == A_CVT_F16 || AMODE == A_SWIGLU_F16);
+  static constexpr bool kXform = (AMODE != A_TMA_F32);
+  static constexpr bool kSwiglu = (AMODE == A_SWIGLU_F32 || AMODE == A_SWIGLU_F16);
+  static constexpr bool kResid = RESID;
+
+  static constexpr int BM = kBM;
+  static constexpr int BN = BN_;
+  static constexpr int ESZ = kF16 ? 2 : 4;      // operand element bytes
+  static constexpr int BK = 128 / ESZ;          // k-block: one 128-byte swizzle row
+  static constexpr int KSTEP = 32 / ESZ;        // UMMA K per instruction (32 bytes)
+  static constexpr int NMMA = BK / KSTEP;       // UMMAs per k-block
+  static constexpr int W_ATOM = 128 / ESZ;      // W columns per 128-byte run
+  static constexpr int W_BOXES = BN / W_ATOM;   // TMA boxes per W stage
+
+  static constexpr uint32_t A_BYTES = BM * 128;
+  static constexpr uint32_t B_ATOM_BYTES = BK * 128;            // one 128-byte run, BK rows
+  static constexpr uint32_t B_BYTES = W_BOXES * B_ATOM_BYTES;   // = BK * BN * ESZ
+  static constexpr uint32_t OP_STAGE_BYTES = A_BYTES + B_BYTES;
+
+  static constexpr int RAW_INPUTS = kSwiglu ? 2 : 1;
+  static constexpr uint32_t RAW_BOX_BYTES = BM * 128;           // [128 rows][32 f32]
+  static constexpr uint32_t RAW_STAGE_BYTES = kXform ? RAW_INPUTS * RAW_BOX_BYTES : 0;
+  static constexpr int RAW_PER_KB = kXform ? BK / 32 : 0;       // raw stages per k-block
+  static constexpr int NR = kXform ? (BN >= 256 ? 2 : 3) : 0;
+
+  static constexpr uint32_t EPI_BUF_BYTES = kEpiRows * kEpiCols * 4;   // 4 KB
+  static constexpr uint32_t EPI_BYTES = 4 * 2 * EPI_BUF_BYTES;        // 2 per epilogue warp
+
+  static constexpr uint32_t SMEM_CAP = 232448;
+  static constexpr uint32_t BAR_REGION = 1024;
+  static constexpr uint32_t ALIGN_SLACK = 1024;
+  // The epilogue buffers alias the raw ring when there is one: the raw ring
+  // is idle once the last k-block has been transformed.
+  static constexpr uint32_t FIXED_BYTES = kXform ? NR * RAW_STAGE_BYTES : EPI_BYTES;
+  static constexpr int NS_FIT =
+      (int)((SMEM_CAP - BAR_REGION - ALIGN_SLACK - FIXED_BYTES) / OP_STAGE_BYTES);
+  static constexpr int NS = NS_FIT > 8 ? 8 : NS_FIT;
+
+  static constexpr uint32_t OFF_OP = 0;
+  static constexpr uint32_t OFF_RAW = NS * OP_STAGE_BYTES;
+  static constexpr uint32_t OFF_EPI = NS * OP_STAGE_BYTES;
+  static constexpr uint32_t OFF_BAR = NS * OP_STAGE_BYTES + FIXED_BYTES;
+  static constexpr uint32_t SMEM_BYTES = ALIGN_SLACK + OFF_BAR + BAR_REGION;
+
+  // Barrier slots (8 bytes each) at OFF_BAR, then the TMEM address and the
+  // abort flag.
+  static constexpr int BAR_B_FULL = 0;
+  static constexpr int BAR_A_FULL = BAR_B_FULL + 8;
+  static constexpr int BAR_OP_EMPTY = BAR_A_FULL + 8;
+  static constexpr int BAR_RAW_FULL = BAR_OP_EMPTY + 8;
+  static constexpr int BAR_RAW_EMPTY = BAR_RAW_FULL + 4;
+  static constexpr int BAR_ACC_FULL = BAR_RAW_EMPTY + 4;
+  static constexpr int BAR_EPI = BAR_ACC_FULL + 1;   // 2 per epilogue warp
+  static constexpr int BAR_COUNT = BAR_EPI + 8;
+  static constexpr uint32_t OFF_TMEM_SLOT = BAR_COUNT * 8;
+  static constexpr uint32_t OFF_ABORT = OFF_TMEM_SLOT + 4;
+
+  static constexpr uint32_t TMEM_COLS = BN;
+  static constexpr uint32_t IDESC =
+      umma_idesc(kF16 ? 0u : 2u, /*a_mn_major=*/false, /*b_mn_major=*/true, BM, BN);
+
+  static_assert(NS >= 2, "operand ring needs two stages");
+  static_assert(NR <= 4 && NS <= 8, "barrier slots");
+  static_assert(!kXform || NR * RAW_STAGE_BYTES >= EPI_BYTES, "epilogue aliasing");
+  static_assert(OFF_ABORT + 4 <= BAR_REGION, "barrier region");
+  static_assert(SMEM_BYTES <= SMEM_CAP, "shared memory");
+  static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256 && (BN & (BN - 1)) == 0, "tile width");
+  static_assert(BN % W_ATOM == 0, "W runs per tile");
+};
+
+// ---------------------------------------------------------------- waiting
+
+struct WaitCtl {
+  uint64_t timeout_ns;
+  volatile int* abort;  // shared-memory flag: some role gave up
+  int* status;          // device status word
+};
+
+// Wait for completion of the barrier phase with parity `parity`. Returns
+// false if the wait ran out (and records the timeout) or, when
+// `honor_abort`, if another role already gave up.
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const WaitCtl& c,
+                                           bool honor_abort = true) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+#pragma unroll 1
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (honor_abort && *c.abort) return false;
+    if (global_timer_ns() - t0 > c.timeout_ns) {
+      *c.abort = 1;
+      atomicCAS(c.status, KSTATUS_OK, KSTATUS_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// Warp-uniform wait: every lane waits (each needs the acquire), and the warp
+// proceeds only if all lanes succeeded.
+__device__ __forceinline__ bool warp_wait_phase(uint32_t bar, uint32_t parity, const WaitCtl& c) {
+  const bool ok = wait_phase(bar, parity, c);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// ---------------------------------------------------------------- activation
+
+// silu(x) = x * sigma(x) with the stable, sign-branched sigmoid of page
+// 09_backward_ffn ("SiLU'"; note 2 of "WGSL-Spesifik Notlar"):
+//   x >= 0: 1 / (1 + exp(-x))      x < 0: exp(x) / (1 + exp(x)).
+// Both branches evaluate exp at -|x| <= 0, so it cannot overflow; the branch
+// is a select on the numerator. Very negative x underflows to 0.
+__device__ __forceinline__ float silu_stable(float x) {
+  const float e = __expf(-fabsf(x));
+  const float num = x >= 0.0f ? 1.0f : e;
+  return x * __fdividef(num, 1.0f + e);
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);   // round-to-nearest-even
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// ---------------------------------------------------------------- transform
+
+// Swizzled byte offset of 16-byte chunk `c` of row `r` in a [rows][128 B]
+// tile with the 128-byte swizzle (chunk index XOR row mod 8), the layout both
+// TMA (SWIZZLE_128B) and the UMMA K-major descriptor use.
+__device__ __forceinline__ uint32_t sw128(uint32_t r, uint32_t c) {
+  return r * 128u + ((c ^ (r & 7u)) << 4);
+}
+
+// Build part of one A k-block from one raw stage (32 f32 columns of X or of
+// GATE and UP). `half` selects which 32 columns of the k-block this raw stage
+// holds (always 0 for the f32 operand). tid in [0, 128).
+template <int AMODE>
+__device__ __forceinline__ void transform_raw_stage(uint32_t a_stage, uint32_t raw, int half,
+                                                    int tid) {
+  constexpr uint32_t BOX = kBM * 128;
+  if constexpr (AMODE == A_SWIGLU_F32) {
+    // f32 operand: chunk c of row r <- silu(G) * U of the same chunk.
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t idx = i * 128 + tid;
+      const uint32_t r = (idx >> 6) * 8 + (idx & 7);
+      const uint32_t c = (idx >> 3) & 7;
+      const uint32_t off = sw128(r, c);
+      const float4 g = ld_shared_v4f(raw + off);
+      const float4 u = ld_shared_v4f(raw + BOX + off);
+      st_shared_v4(a_stage + off, __float_as_uint(silu_stable(g.x) * u.x),
+                   __float_as_uint(silu_stable(g.y) * u.y), __float_as_uint(silu_stable(g.z) * u.z),
+                   __float_as_uint(silu_stable(g.w) * u.w));
+    }
+  } else {
+    // binary16 operand: chunk (4*half + cc) of row r holds 8 halves made from
+    // f32 chunks 2cc and 2cc+1 of the raw stage.
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t idx = i * 128 + tid;
+      const uint32_t r = (idx >> 5) * 8 + (idx & 7);
+      const uint32_t cc = (idx >> 3) & 3;
+      const uint32_t o0 = sw128(r, 2 * cc);
+      const uint32_t o1 = sw128(r, 2 * cc + 1);
+      float4 a0 = ld_shared_v4f(raw + o0);
+      float4 a1 = ld_shared_v4f(raw + o1);
+      if constexpr (AMODE == A_SWIGLU_F16) {
+        const float4 u0 = ld_shared_v4f(raw + BOX + o0);
+        const float4 u1 = ld_shared_v4f(raw + BOX + o1);
+        a0.x = silu_stable(a0.x) * u0.x;
+        a0.y = silu_stable(a0.y) * u0.y;
+        a0.z = silu_stable(a0.z) * u0.z;
+        a0.w = silu_stable(a0.w) * u0.w;
+        a1.x = silu_stable(a1.x) * u1.x;
+        a1.y = silu_stable(a1.y) * u1.y;
+        a1.z = silu_stable(a1.z) * u1.z;
+        a1.w = silu_stable(a1.w) * u1.w;
+      }
+      st_shared_v4(a_stage + sw128(r, 4 * half + cc), pack_half2(a0.x, a0.y),
+                   pack_half2(a0.z, a0.w), pack_half2(a1.x, a1.y), pack_half2(a1.z, a1.w));
+    }
+  }
+}
+
+// ---------------------------------------------------------------- kernel
+
+template <int AMODE, bool RESID, int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    lin_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
+                    const __grid_constant__ CUtensorMap tm_u,
+                    const __grid_constant__ CUtensorMap tm_w,
+                    const __grid_constant__ CUtensorMap tm_r,
+                    const __grid_constant__ CUtensorMap tm_y, const KernelArgs args) {
+  using T = GemmTraits<AMODE, RESID, BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + T::OFF_BAR;
+  auto bar = [&](int slot) -> uint32_t { return bar0 + 8u * (uint32_t)slot; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + T::OFF_BAR + T::OFF_TMEM_SLOT);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + T::OFF_BAR + T::OFF_ABORT);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int n0 = blockIdx.x * BN;
+  const int m0 = blockIdx.y * T::BM;
+  const int nkb = (args.K + T::BK - 1) / T::BK;
+  const bool withhold = (args.flags & KFLAG_WITHHOLD_PRODUCER) != 0;
+  const WaitCtl ctl{args.timeout_ns, abort_flag, args.status};
+
+  auto a_stage = [&](int s) -> uint32_t { return sbase + T::OFF_OP + s * T::OP_STAGE_BYTES; };
+  auto b_stage = [&](int s) -> uint32_t { return a_stage(s) + T::A_BYTES; };
+  auto raw_stage = [&](int r) -> uint32_t { return sbase + T::OFF_RAW + r * T::RAW_STAGE_BYTES; };
+
+  // ---- set-up
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < T::NS; ++s) {
+      mbar_init(bar(T::BAR_B_FULL + s), 1);
+      mbar_init(bar(T::BAR_A_FULL + s), 4);       // one arrive per transform warp
+      mbar_init(bar(T::BAR_OP_EMPTY + s), 1);     // tcgen05.commit
+    }
+    for (int r = 0; r < T::NR; ++r) {
+      mbar_init(bar(T::BAR_RAW_FULL + r), 1);
+      mbar_init(bar(T::BAR_RAW_EMPTY + r), 4);
+    }
+    mbar_init(bar(T::BAR_ACC_FULL), 1);
+    for (int e = 0; e < 8; ++e) mbar_init(bar(T::BAR_EPI + e), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 0 && lane == 0 && !withhold) {
+    tma_prefetch_desc(&tm_w);
+    tma_prefetch_desc(&tm_a);
+    if constexpr (T::kSwiglu) tma_prefetch_desc(&tm_u);
+    if constexpr (RESID) tma_prefetch_desc(&tm_r);
+    tma_prefetch_desc(&tm_y);
+  }
+  if (warp == 2) {
+    tmem_alloc(smem_u32(tmem_slot), T::TMEM_COLS);
+    tmem_relinquish_alloc_permit();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------- W (and X for the TF32 path) producer
+    if (lane == 0 && !withhold) {
+      int filled = 0;
+      for (int kb = 0; kb < nkb; ++kb) {
+        const int s = kb % T::NS;
+        const int n = kb / T::NS;
+        if (kb >= T::NS && !wait_phase(bar(T::BAR_OP_EMPTY + s), (n - 1) & 1, ctl)) break;
+        const uint32_t full = bar(T::BAR_B_FULL + s);
+        mbar_arrive_expect_tx(full, T::B_BYTES + (T::kXform ? 0u : T::A_BYTES));
+        if constexpr (!T::kXform) tma_load_2d(a_stage(s), &tm_a, kb * T::BK, m0, full);
+#pragma unroll
+        for (int j = 0; j < T::W_BOXES; ++j)
+          tma_load_2d(b_stage(s) + j * T::B_ATOM_BYTES, &tm_w, n0 + j * T::W_ATOM, kb * T::BK,
+                      full);
+        filled = kb + 1;
+      }
+      // Never leave with copies in flight: wait for the last fill of each slot.
+      for (int kb = (filled > T::NS ? filled - T::NS : 0); kb < filled; ++kb)
+        wait_phase(bar(T::BAR_B_FULL + kb % T::NS), (kb / T::NS) & 1, ctl, false);
+    }
+  } else if (warp == 1) {
+    // ---------------- UMMA issuer
+    if (lane == 0) {
+      for (int kb = 0; kb < nkb; ++kb) {
+        const int s = kb % T::NS;
+        const uint32_t ph = (kb / T::NS) & 1;
+        if (!wait_phase(bar(T::BAR_B_FULL + s), ph, ctl)) break;
+        if (T::kXform && !wait_phase(bar(T::BAR_A_FULL + s), ph, ctl)) break;
+        tc_fence_after_sync();
+#pragma unroll
+        for (int k = 0; k < T::NMMA; ++k) {
+          const uint64_t adesc = umma_desc_sw128(a_stage(s) + k * 32, 16, 1024);
+          const uint64_t bdesc =
+              umma_desc_sw128(b_stage(s) + k * T::KSTEP * 128, T::B_ATOM_BYTES, 1024);
+          if constexpr (T::kF16)
+            umma_f16(tmem, adesc, bdesc, T::IDESC, (kb | k) != 0);
+          else
+            umma_tf32(tmem, adesc, bdesc, T::IDESC, (kb | k) != 0);
+        }
+        umma_commit(bar(T::BAR_OP_EMPTY + s));   // frees the stage when these UMMAs finish
+      }
+      umma_commit(bar(T::BAR_ACC_FULL));         // accumulator complete (or drained)
+      // Keep TMEM allocated until every issued UMMA has finished.
+      wait_phase(bar(T::BAR_ACC_FULL), 0, ctl, false);
+    }
+  } else if (warp == 3) {
+    // ---------------- raw f32 input producer (transform paths)
+    if constexpr (T::kXform) {
+      if (lane == 0 && !withhold) {
+        const int nraw = nkb * T::RAW_PER_KB;
+        int filled = 0;
+        for (int t = 0; t < nraw; ++t) {
+          const int r = t % T::NR;
+          const int n = t / T::NR;
+          if (t >= T::NR && !wait_phase(bar(T::BAR_RAW_EMPTY + r), (n - 1) & 1, ctl)) break;
+          const uint32_t full = bar(T::BAR_RAW_FULL + r);
+          mbar_arrive_expect_tx(full, T::RAW_STAGE_BYTES);
+          tma_load_2d(raw_stage(r), &tm_a, t * 32, m0, full);
+          if constexpr (T::kSwiglu)
+            tma_load_2d(raw_stage(r) + T::RAW_BOX_BYTES, &tm_u, t * 32, m0, full);
+          filled = t + 1;
+        }
+        for (int t = (filled > T::NR ? filled - T::NR : 0); t < filled; ++t)
+          wait_phase(bar(T::BAR_RAW_FULL + t % T::NR), (t / T::NR) & 1, ctl, false);
+      }
+    }
+  } else {
+    // ---------------- warps 4-7: transform, then epilogue
+    const int q = warp - 4;                 // TMEM lane quadrant of this warp
+    const int tid = threadIdx.x - 128;      // 0..127
+    bool ok = true;
+    if constexpr (T::kXform) {
+      int t = 0;
+      for (int kb = 0; kb < nkb && ok; ++kb) {
+        const int s = kb % T::NS;
+        const int n = kb / T::NS;
+        if (kb >= T::NS && !warp_wait_phase(bar(T::BAR_OP_EMPTY + s), (n - 1) & 1, ctl)) {
+          ok = false;
+          break;
+        }
+#pragma unroll 1
+        for (int h = 0; h < T::RAW_PER_KB; ++h, ++t) {
+          const int r = t % T::NR;
+          if (!warp_wait_phase(bar(T::BAR_RAW_FULL + r), (t / T::NR) & 1, ctl)) {
+            ok = false;
+            break;
+          }
+          transform_raw_stage<AMODE>(a_stage(s), raw_stage(r), h, tid);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(T::BAR_RAW_EMPTY + r));
+        }
+        if (!ok) break;
+        fence_proxy_async_smem();   // operand writes -> visible to the UMMA (async proxy)
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(T::BAR_A_FULL + s));
+      }
+      // The epilogue buffers alias the raw ring: all four warps must be done
+      // reading it first.
+      named_bar_sync(1, 128);
+    }
+
+    const int row0 = m0 + q * kEpiRows;
+    const bool rows_in = row0 < args.M;      // a box starting past M would store nothing
+    const uint32_t buf0 = sbase + T::OFF_EPI + (uint32_t)(q * 2) * T::EPI_BUF_BYTES;
+    const uint32_t ebar0 = bar(T::BAR_EPI + q * 2);
+    constexpr int NC = BN / kEpiCols;
+    int nc = (args.N - n0 + kEpiCols - 1) / kEpiCols;   // chunks inside N
+    if (nc > NC) nc = NC;
+
+    // Residual tiles are prefetched one chunk ahead; r_issued / r_done count
+    // the chunks whose load was issued / waited for (lane 0's view).
+    int r_issued = 0, r_done = 0;
+    if (RESID && rows_in && lane == 0 && nc > 0) {
+      mbar_arrive_expect_tx(ebar0, T::EPI_BUF_BYTES);
+      tma_load_2d(buf0, &tm_r, n0, row0, ebar0);
+      r_issued = 1;
+    }
+    ok = warp_wait_phase(bar(T::BAR_ACC_FULL), 0, ctl);
+    tc_fence_after_sync();
+    if (ok && rows_in) {
+      for (int c = 0; c < nc; ++c) {
+        const int b = c & 1;
+        const uint32_t buf = buf0 + b * T::EPI_BUF_BYTES;
+        if (lane == 0 && c + 1 < nc) {
+          // The other buffer's previous store must have read its source.
+          bulk_wait_group_read<0>();
+          if constexpr (RESID) {
+            const uint32_t nb = ebar0 + 8u * (uint32_t)(b ^ 1);
+            mbar_arrive_expect_tx(nb, T::EPI_BUF_BYTES);
+            tma_load_2d(buf0 + (b ^ 1) * T::EPI_BUF_BYTES, &tm_r, n0 + (c + 1) * kEpiCols, row0,
+                        nb);
+            r_issued = c + 2;
+          }
+        }
+        __syncwarp();
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * kEpiCols), v);
+        tmem_wait_ld();
+        if constexpr (RESID) {
+          if (!warp_wait_phase(ebar0 + 8u * (uint32_t)b, (c >> 1) & 1, ctl)) break;
+          r_done = c + 1;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t addr = buf + sw128(lane, j);
+          float o0 = __uint_as_float(v[4 * j + 0]);
+          float o1 = __uint_as_float(v[4 * j + 1]);
+          float o2 = __uint_as_float(v[4 * j + 2]);
+          float o3 = __uint_as_float(v[4 * j + 3]);
+          if constexpr (RESID) {
+            const float4 rr = ld_shared_v4f(addr);
+            o0 += rr.x;
+            o1 += rr.y;
+            o2 += rr.z;
+            o3 += rr.w;
+          }
+          st_shared_v4(addr, __float_as_uint(o0), __float_as_uint(o1), __float_as_uint(o2),
+                       __float_as_uint(o3));
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&tm_y, n0 + c * kEpiCols, row0, buf);
+          bulk_commit_group();
+        }
+      }
+    }
+    if (lane == 0) {
+      // Never leave with a residual load in flight (only on the abort path
+      // can one be outstanding).
+      for (int c = r_done; c < r_issued; ++c)
+        wait_phase(ebar0 + 8u * (uint32_t)(c & 1), (c >> 1) & 1, ctl, false);
+    }
+    if (lane == 0) bulk_wait_group_all();
+    __syncwarp();
+  }
+
+  // ---- teardown
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, T::TMEM_COLS);
+  }
+}
+
+// Host-side launcher of one instantiation.
+template <int AMODE, bool RESID, int BN>
+cudaError_t launch_instance(const TensorMaps& m, const KernelArgs& args, cudaStream_t stream) {
+  using T = GemmTraits<AMODE, RESID, BN>;
+  auto kern = lin_gemm_kernel<AMODE, RESID, BN>;
+  // The shared-memory opt-in is per device: remember which devices have it.
+  static std::atomic<uint64_t> attr_done{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev < 64 ? (uint64_t{1} << dev) : 0;
+  if (bit == 0 || !(attr_done.load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_done.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  dim3 grid((unsigned)((args.N + BN - 1) / BN), (unsigned)((args.M + kBM - 1) / kBM), 1);
+  if (args.flags & KFLAG_WITHHOLD_PRODUCER) grid = dim3(1, 1, 1);
+  kern<<<grid, kThreads, T::SMEM_BYTES, stream>>>(m.a, m.u, m.w, m.r, m.y, args);
+  return cudaGetLastError();
+}
+
+}  // namespace lin

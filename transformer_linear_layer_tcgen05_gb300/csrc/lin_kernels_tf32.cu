@@ -1,0 +1,19 @@
+// lin_kernels_tf32.cu -- instantiations of the tcgen05 GEMM whose operands
+// are f32 consumed as TF32: matmul, matmul_residual (A copied by TMA) and
+// matmul_residual_swiglu_a (A = silu(GATE) * UP built by the transform warps).
+#include "lin_gemm.cuh"
+
+namespace lin {
+
+cudaError_t launch_gemm_tf32(int amode, bool resid, int bn, const TensorMaps& maps,
+                             const KernelArgs& args, cudaStream_t stream) {
+  if (bn != 128) return cudaErrorInvalidValue;
+  if (amode == A_TMA_F32)
+    return resid ? launch_instance<A_TMA_F32, true, 128>(maps, args, stream)
+                 : launch_instance<A_TMA_F32, false, 128>(maps, args, stream);
+  if (amode == A_SWIGLU_F32 && resid)
+    return launch_instance<A_SWIGLU_F32, true, 128>(maps, args, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace lin

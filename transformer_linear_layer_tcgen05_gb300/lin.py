@@ -1,0 +1,236 @@
+"""Thin ctypes binding of the C ABI in include/lin.h.
+
+Argument marshalling only: every function here forwards to the function of
+the same name in ``liblin.so``; all arithmetic runs in the library's CUDA
+kernels. There is no fallback: if the library is missing or fails to load,
+every call raises.
+
+Two layers:
+
+* ``lib()`` returns the ``ctypes.CDLL`` with typed signatures; its functions
+  take raw device pointers (ints), int64 dims and a stream handle, and return
+  the ``lin_status`` code.
+* ``lin_matmul(X, W, Y)`` and friends take torch CUDA tensors, derive
+  (M, N, K) from their shapes, call the C function on the current torch
+  stream (or ``stream=``) and raise ``LinError`` on a non-zero status.
+  Binary16 weights may be given as ``torch.float16``, ``torch.int16`` or
+  ``torch.uint16`` tensors (only the bit patterns are read).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "liblin.so")
+
+STATUS = {
+    0: "LIN_SUCCESS",
+    1: "LIN_ERROR_INVALID_VALUE",
+    2: "LIN_ERROR_UNSUPPORTED_SHAPE",
+    3: "LIN_ERROR_MISALIGNED",
+    4: "LIN_ERROR_ALIASING",
+    5: "LIN_ERROR_UNSUPPORTED_DEVICE",
+    6: "LIN_ERROR_CUDA",
+    7: "LIN_ERROR_TIMEOUT",
+}
+LIN_SUCCESS = 0
+LIN_ERROR_INVALID_VALUE = 1
+LIN_ERROR_UNSUPPORTED_SHAPE = 2
+LIN_ERROR_MISALIGNED = 3
+LIN_ERROR_ALIASING = 4
+LIN_ERROR_UNSUPPORTED_DEVICE = 5
+LIN_ERROR_CUDA = 6
+LIN_ERROR_TIMEOUT = 7
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int64
+_S = ctypes.c_void_p  # lin_stream_t
+
+# name -> argument types (all compute entry points return lin_status as int)
+SIGNATURES = {
+    "lin_matmul": [_P, _P, _P, _I, _I, _I, _S],
+    "lin_matmul_residual": [_P, _P, _P, _P, _I, _I, _I, _S],
+    "lin_matmul_residual_swiglu_a": [_P, _P, _P, _P, _P, _I, _I, _I, _S],
+    "lin_matmul_w16": [_P, _P, _P, _I, _I, _I, _S],
+    "lin_matmul_residual_w16": [_P, _P, _P, _P, _I, _I, _I, _S],
+    "lin_matmul_residual_swiglu_a_w16": [_P, _P, _P, _P, _P, _I, _I, _I, _S],
+    "lin_get_device_status": [_S],
+    "lin_selftest_wait_timeout": [_I, _S],
+}
+
+_lib = None
+
+
+class LinError(RuntimeError):
+    """A non-zero lin_status returned by the library."""
+
+    def __init__(self, fn: str, status: int, cuda_error: int = 0):
+        self.status = status
+        self.cuda_error = cuda_error
+        msg = f"{fn} returned {STATUS.get(status, status)}"
+        if status == LIN_ERROR_CUDA:
+            msg += f" (cudaError_t {cuda_error})"
+        super().__init__(msg)
+
+
+def lib() -> ctypes.CDLL:
+    """Load liblin.so (once) and declare its signatures. Raises if missing."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is not built; build it with "
+                "transformer_linear_layer_tcgen05_gb300.build.build_library()")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, argtypes in SIGNATURES.items():
+            f = getattr(L, name)
+            f.argtypes = argtypes
+            f.restype = ctypes.c_int
+        L.lin_status_string.argtypes = [ctypes.c_int]
+        L.lin_status_string.restype = ctypes.c_char_p
+        L.lin_last_cuda_error.argtypes = []
+        L.lin_last_cuda_error.restype = ctypes.c_int
+        L.lin_version.argtypes = []
+        L.lin_version.restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().lin_status_string(int(status)).decode()
+
+
+def check(fn: str, status: int) -> None:
+    if status != LIN_SUCCESS:
+        raise LinError(fn, status, lib().lin_last_cuda_error() if status == LIN_ERROR_CUDA else 0)
+
+
+# ----------------------------------------------------------------- tensor layer
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _f32(t, name):
+    import torch
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.float32 or not t.is_cuda:
+        raise TypeError(f"{name} must be a float32 CUDA tensor")
+    if t.dim() != 2 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous 2-D tensor")
+    return t
+
+
+def _w16(t, name):
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda or t.element_size() != 2 or \
+            t.dtype not in (torch.float16, torch.int16, getattr(torch, "uint16", torch.int16)):
+        raise TypeError(f"{name} must be a 16-bit (binary16 bits) CUDA tensor")
+    if t.dim() != 2 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous 2-D tensor")
+    return t
+
+
+def _dims(A, W, Y):
+    M, K = A.shape
+    K2, N = W.shape
+    if K2 != K or tuple(Y.shape) != (M, N):
+        raise ValueError(f"shape mismatch: A{tuple(A.shape)} W{tuple(W.shape)} Y{tuple(Y.shape)}")
+    return M, N, K
+
+
+def _call(name, *args):
+    check(name, getattr(lib(), name)(*args))
+
+
+def lin_matmul(X, W, Y, stream=None):
+    """Y = X @ W (f32; TF32 tensor cores, f32 accumulate)."""
+    M, N, K = _dims(_f32(X, "X"), _f32(W, "W"), _f32(Y, "Y"))
+    _call("lin_matmul", X.data_ptr(), W.data_ptr(), Y.data_ptr(), M, N, K,
+          _stream_handle(stream))
+    return Y
+
+
+def lin_matmul_residual(X, W, R, Y, stream=None):
+    """Y = X @ W + R."""
+    M, N, K = _dims(_f32(X, "X"), _f32(W, "W"), _f32(Y, "Y"))
+    if tuple(_f32(R, "R").shape) != (M, N):
+        raise ValueError("R must be [M, N]")
+    _call("lin_matmul_residual", X.data_ptr(), W.data_ptr(), R.data_ptr(), Y.data_ptr(),
+          M, N, K, _stream_handle(stream))
+    return Y
+
+
+def lin_matmul_residual_swiglu_a(GATE, UP, W, R, Y, stream=None):
+    """Y = (silu(GATE) * UP) @ W + R."""
+    M, N, K = _dims(_f32(GATE, "GATE"), _f32(W, "W"), _f32(Y, "Y"))
+    if tuple(_f32(UP, "UP").shape) != (M, K) or tuple(_f32(R, "R").shape) != (M, N):
+        raise ValueError("UP must be [M, K] and R [M, N]")
+    _call("lin_matmul_residual_swiglu_a", GATE.data_ptr(), UP.data_ptr(), W.data_ptr(),
+          R.data_ptr(), Y.data_ptr(), M, N, K, _stream_handle(stream))
+    return Y
+
+
+def lin_matmul_w16(X, W16, Y, stream=None):
+    """Y = X @ W16 with binary16 weights."""
+    M, N, K = _dims(_f32(X, "X"), _w16(W16, "W16"), _f32(Y, "Y"))
+    _call("lin_matmul_w16", X.data_ptr(), W16.data_ptr(), Y.data_ptr(), M, N, K,
+          _stream_handle(stream))
+    return Y
+
+
+def lin_matmul_residual_w16(X, W16, R, Y, stream=None):
+    """Y = X @ W16 + R with binary16 weights."""
+    M, N, K = _dims(_f32(X, "X"), _w16(W16, "W16"), _f32(Y, "Y"))
+    if tuple(_f32(R, "R").shape) != (M, N):
+        raise ValueError("R must be [M, N]")
+    _call("lin_matmul_residual_w16", X.data_ptr(), W16.data_ptr(), R.data_ptr(),
+          Y.data_ptr(), M, N, K, _stream_handle(stream))
+    return Y
+
+
+def lin_matmul_residual_swiglu_a_w16(GATE, UP, W16, R, Y, stream=None):
+    """Y = (silu(GATE) * UP) @ W16 + R with binary16 W_down."""
+    M, N, K = _dims(_f32(GATE, "GATE"), _w16(W16, "W16"), _f32(Y, "Y"))
+    if tuple(_f32(UP, "UP").shape) != (M, K) or tuple(_f32(R, "R").shape) != (M, N):
+        raise ValueError("UP must be [M, K] and R [M, N]")
+    _call("lin_matmul_residual_swiglu_a_w16", GATE.data_ptr(), UP.data_ptr(),
+          W16.data_ptr(), R.data_ptr(), Y.data_ptr(), M, N, K, _stream_handle(stream))
+    return Y
+
+
+def lin_get_device_status(stream=None) -> int:
+    """Synchronise the stream; return (and clear) the device status word."""
+    return lib().lin_get_device_status(_stream_handle(stream))
+
+
+def lin_selftest_wait_timeout(timeout_us: int, stream=None) -> int:
+    """Run the bounded-wait self-test; LIN_ERROR_TIMEOUT means it works."""
+    return lib().lin_selftest_wait_timeout(int(timeout_us), _stream_handle(stream))
+
+
+FORM_FUNCS = {
+    "matmul": lin_matmul,
+    "matmul_residual": lin_matmul_residual,
+    "matmul_residual_swiglu_a": lin_matmul_residual_swiglu_a,
+    "matmul_w16": lin_matmul_w16,
+    "matmul_residual_w16": lin_matmul_residual_w16,
+    "matmul_residual_swiglu_a_w16": lin_matmul_residual_swiglu_a_w16,
+}
+
+
+def run_form(form: str, d: dict, Y, stream=None):
+    """Call the entry point of ``form`` with the device tensors of dict ``d``
+    (keys as produced by ``workloads.generate``: X or GATE/UP, W or W16, R)."""
+    f = FORM_FUNCS[form]
+    w = d["W16"] if form.endswith("_w16") else d["W"]
+    if "swiglu" in form:
+        return f(d["GATE"], d["UP"], w, d["R"], Y, stream=stream)
+    if "residual" in form:
+        return f(d["X"], w, d["R"], Y, stream=stream)
+    return f(d["X"], w, Y, stream=stream)
