@@ -38,9 +38,15 @@ namespace lin {
 template <int AMODE, bool RESID, int BN_>
 struct GemmTraits {
   static constexpr bool kF16 = (AMODE == A_CVT_F16 || AMODE == A_SWIGLU_F16);
-  static constexpr bool kXform = (AMODE != A_TMA_F32);
   static constexpr bool kSwiglu = (AMODE == A_SWIGLU_F32 || AMODE == A_SWIGLU_F16);
   static constexpr bool kResid = RESID;
+  // The A operand is built by the transform warps unless X is copied as is.
+  static constexpr bool kXformA = (AMODE != A_TMA_F32);
+  // TF32 UMMA takes a K-major B only, so for the f32 forms the transform
+  // warps transpose the TMA-staged W tile (N contiguous) into a K-major
+  // operand; binary16 W is consumed MN-major straight from TMA.
+  static constexpr bool kXformB = !kF16;
+  static constexpr bool kXform = kXformA || kXformB;
 
   static constexpr int BM = kBM;
   static constexpr int BN = BN_;
@@ -49,18 +55,24 @@ struct GemmTraits {
   static constexpr int KSTEP = 32 / ESZ;        // UMMA K per instruction (32 bytes)
   static constexpr int NMMA = BK / KSTEP;       // UMMAs per k-block
   static constexpr int W_ATOM = 128 / ESZ;      // W columns per 128-byte run
-  static constexpr int W_BOXES = BN / W_ATOM;   // TMA boxes per W stage
+  static constexpr int W_BOXES = BN / W_ATOM;   // TMA boxes per W tile
 
   static constexpr uint32_t A_BYTES = BM * 128;
   static constexpr uint32_t B_ATOM_BYTES = BK * 128;            // one 128-byte run, BK rows
   static constexpr uint32_t B_BYTES = W_BOXES * B_ATOM_BYTES;   // = BK * BN * ESZ
   static constexpr uint32_t OP_STAGE_BYTES = A_BYTES + B_BYTES;
+  // bytes the TMA delivers straight into an operand stage
+  static constexpr uint32_t OP_TMA_BYTES = (kXformA ? 0u : A_BYTES) + (kXformB ? 0u : B_BYTES);
 
-  static constexpr int RAW_INPUTS = kSwiglu ? 2 : 1;
+  // Raw stage: what the transform warps read for 32 f32 columns of K:
+  // the A inputs (X, or GATE and UP) and, for TF32, the W tile of that k-block.
+  static constexpr int RAW_A_INPUTS = kXformA ? (kSwiglu ? 2 : 1) : 0;
   static constexpr uint32_t RAW_BOX_BYTES = BM * 128;           // [128 rows][32 f32]
-  static constexpr uint32_t RAW_STAGE_BYTES = kXform ? RAW_INPUTS * RAW_BOX_BYTES : 0;
-  static constexpr int RAW_PER_KB = kXform ? BK / 32 : 0;       // raw stages per k-block
-  static constexpr int NR = kXform ? (BN >= 256 ? 2 : 3) : 0;
+  static constexpr uint32_t RAW_A_BYTES = RAW_A_INPUTS * RAW_BOX_BYTES;
+  static constexpr uint32_t RAW_W_BYTES = kXformB ? B_BYTES : 0u;   // [BN/32 runs][32 rows][128 B]
+  static constexpr uint32_t RAW_STAGE_BYTES = RAW_A_BYTES + RAW_W_BYTES;
+  static constexpr int RAW_PER_KB = kF16 ? BK / 32 : 1;         // raw stages per k-block
+  static constexpr int NR = (kXformA && kXformB) ? 2 : 3;
 
   static constexpr uint32_t EPI_BUF_BYTES = kEpiRows * kEpiCols * 4;   // 4 KB
   static constexpr uint32_t EPI_BYTES = 4 * 2 * EPI_BUF_BYTES;        // 2 per epilogue warp
@@ -68,24 +80,24 @@ struct GemmTraits {
   static constexpr uint32_t SMEM_CAP = 232448;
   static constexpr uint32_t BAR_REGION = 1024;
   static constexpr uint32_t ALIGN_SLACK = 1024;
-  // The epilogue buffers alias the raw ring when there is one: the raw ring
-  // is idle once the last k-block has been transformed.
-  static constexpr uint32_t FIXED_BYTES = kXform ? NR * RAW_STAGE_BYTES : EPI_BYTES;
+  // The epilogue buffers alias the raw ring: it is idle once the last
+  // k-block has been transformed.
+  static constexpr uint32_t FIXED_BYTES = NR * RAW_STAGE_BYTES;
   static constexpr int NS_FIT =
       (int)((SMEM_CAP - BAR_REGION - ALIGN_SLACK - FIXED_BYTES) / OP_STAGE_BYTES);
   static constexpr int NS = NS_FIT > 8 ? 8 : NS_FIT;
 
   static constexpr uint32_t OFF_OP = 0;
   static constexpr uint32_t OFF_RAW = NS * OP_STAGE_BYTES;
-  static constexpr uint32_t OFF_EPI = NS * OP_STAGE_BYTES;
+  static constexpr uint32_t OFF_EPI = OFF_RAW;
   static constexpr uint32_t OFF_BAR = NS * OP_STAGE_BYTES + FIXED_BYTES;
   static constexpr uint32_t SMEM_BYTES = ALIGN_SLACK + OFF_BAR + BAR_REGION;
 
   // Barrier slots (8 bytes each) at OFF_BAR, then the TMEM address and the
   // abort flag.
-  static constexpr int BAR_B_FULL = 0;
-  static constexpr int BAR_A_FULL = BAR_B_FULL + 8;
-  static constexpr int BAR_OP_EMPTY = BAR_A_FULL + 8;
+  static constexpr int BAR_OP_TMA = 0;       // TMA bytes of an operand stage landed
+  static constexpr int BAR_OP_XF = BAR_OP_TMA + 8;    // transform warps filled the stage
+  static constexpr int BAR_OP_EMPTY = BAR_OP_XF + 8;  // UMMAs reading the stage are done
   static constexpr int BAR_RAW_FULL = BAR_OP_EMPTY + 8;
   static constexpr int BAR_RAW_EMPTY = BAR_RAW_FULL + 4;
   static constexpr int BAR_ACC_FULL = BAR_RAW_EMPTY + 4;
@@ -96,11 +108,12 @@ struct GemmTraits {
 
   static constexpr uint32_t TMEM_COLS = BN;
   static constexpr uint32_t IDESC =
-      umma_idesc(kF16 ? 0u : 2u, /*a_mn_major=*/false, /*b_mn_major=*/true, BM, BN);
+      umma_idesc(kF16 ? 0u : 2u, /*a_mn_major=*/false, /*b_mn_major=*/!kXformB, BM, BN);
 
+  static_assert(kXform, "every form has at least one transformed operand");
   static_assert(NS >= 2, "operand ring needs two stages");
   static_assert(NR <= 4 && NS <= 8, "barrier slots");
-  static_assert(!kXform || NR * RAW_STAGE_BYTES >= EPI_BYTES, "epilogue aliasing");
+  static_assert(NR * RAW_STAGE_BYTES >= EPI_BYTES, "epilogue aliasing");
   static_assert(OFF_ABORT + 4 <= BAR_REGION, "barrier region");
   static_assert(SMEM_BYTES <= SMEM_CAP, "shared memory");
   static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256 && (BN & (BN - 1)) == 0, "tile width");
@@ -141,6 +154,15 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const 
 __device__ __forceinline__ bool warp_wait_phase(uint32_t bar, uint32_t parity, const WaitCtl& c) {
   const bool ok = wait_phase(bar, parity, c);
   return __all_sync(0xffffffffu, ok);
+}
+
+// Lane 0 waits (it is the lane that issues the copies or UMMAs that follow);
+// the result is broadcast so the warp stays converged.
+__device__ __forceinline__ bool lane0_wait_phase(uint32_t bar, uint32_t parity, const WaitCtl& c,
+                                                 int lane) {
+  bool ok = true;
+  if (lane == 0) ok = wait_phase(bar, parity, c);
+  return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 }
 
 // ---------------------------------------------------------------- activation
@@ -221,6 +243,33 @@ __device__ __forceinline__ void transform_raw_stage(uint32_t a_stage, uint32_t r
   }
 }
 
+// TF32 B operand: transpose one staged W tile (BN/32 runs of [32 k-rows][32 f32
+// along N], 128-byte swizzle) into the K-major operand [BN rows n][32 f32
+// along K] with the same swizzle. Warp q handles runs q, q+4, ...; lane =
+// column inside the run. For a fixed k the 32 lanes read 32 distinct words
+// of one 128-byte row, and each group of 8 lanes writes 8 distinct 16-byte
+// bank groups, so neither side has bank conflicts.
+template <int BN>
+__device__ __forceinline__ void transpose_w_tile(uint32_t b_stage, uint32_t raw_w, int q,
+                                                 int lane) {
+#pragma unroll 1
+  for (int j = q; j < BN / 32; j += 4) {
+    const uint32_t n = (uint32_t)(j * 32 + lane);
+    const uint32_t src = raw_w + (uint32_t)j * 4096u;
+    const uint32_t col = ((uint32_t)lane >> 2), word = ((uint32_t)lane & 3u) * 4u;
+#pragma unroll
+    for (uint32_t c = 0; c < 8; ++c) {
+      uint32_t v[4];
+#pragma unroll
+      for (uint32_t e = 0; e < 4; ++e) {
+        const uint32_t k = 4 * c + e;
+        v[e] = ld_shared_u32(src + k * 128u + ((col ^ (k & 7u)) << 4) + word);
+      }
+      st_shared_v4(b_stage + sw128(n, c), v[0], v[1], v[2], v[3]);
+    }
+  }
+}
+
 // ---------------------------------------------------------------- kernel
 
 template <int AMODE, bool RESID, int BN>
@@ -254,10 +303,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- set-up
   if (threadIdx.x == 0) {
-    for (int s = 0; s < T::NS; ++s) {
-      mbar_init(bar(T::BAR_B_FULL + s), 1);
-      mbar_init(bar(T::BAR_A_FULL + s), 4);       // one arrive per transform warp
-      mbar_init(bar(T::BAR_OP_EMPTY + s), 1);     // tcgen05.commit
+    for (int st = 0; st < T::NS; ++st) {
+      mbar_init(bar(T::BAR_OP_TMA + st), 1);
+      mbar_init(bar(T::BAR_OP_XF + st), 4);       // one arrive per transform warp
+      mbar_init(bar(T::BAR_OP_EMPTY + st), 1);    // tcgen05.commit
     }
     for (int r = 0; r < T::NR; ++r) {
       mbar_init(bar(T::BAR_RAW_FULL + r), 1);
@@ -269,6 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_barrier_init();
     fence_proxy_async_smem();
   }
+  __syncwarp();
   if (warp == 0 && lane == 0 && !withhold) {
     tma_prefetch_desc(&tm_w);
     tma_prefetch_desc(&tm_a);
@@ -276,6 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if constexpr (RESID) tma_prefetch_desc(&tm_r);
     tma_prefetch_desc(&tm_y);
   }
+  __syncwarp();
   if (warp == 2) {
     tmem_alloc(smem_u32(tmem_slot), T::TMEM_COLS);
     tmem_relinquish_alloc_permit();
@@ -285,107 +336,135 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
+  // Every role below runs with its whole warp converged: lane 0 waits and
+  // issues, the other lanes follow it loop by loop, and no lane reaches the
+  // final CTA barrier while a lane of its warp still has work in flight.
   if (warp == 0) {
-    // ---------------- W (and X for the TF32 path) producer
-    if (lane == 0 && !withhold) {
+    // ---------------- operand-stage TMA producer (X for TF32, W for binary16)
+    if (T::OP_TMA_BYTES > 0 && !withhold) {
       int filled = 0;
       for (int kb = 0; kb < nkb; ++kb) {
-        const int s = kb % T::NS;
+        const int st = kb % T::NS;
         const int n = kb / T::NS;
-        if (kb >= T::NS && !wait_phase(bar(T::BAR_OP_EMPTY + s), (n - 1) & 1, ctl)) break;
-        const uint32_t full = bar(T::BAR_B_FULL + s);
-        mbar_arrive_expect_tx(full, T::B_BYTES + (T::kXform ? 0u : T::A_BYTES));
-        if constexpr (!T::kXform) tma_load_2d(a_stage(s), &tm_a, kb * T::BK, m0, full);
+        if (kb >= T::NS && !lane0_wait_phase(bar(T::BAR_OP_EMPTY + st), (n - 1) & 1, ctl, lane))
+          break;
+        if (lane == 0) {
+          const uint32_t full = bar(T::BAR_OP_TMA + st);
+          mbar_arrive_expect_tx(full, T::OP_TMA_BYTES);
+          if constexpr (!T::kXformA) tma_load_2d(a_stage(st), &tm_a, kb * T::BK, m0, full);
+          if constexpr (!T::kXformB) {
 #pragma unroll
-        for (int j = 0; j < T::W_BOXES; ++j)
-          tma_load_2d(b_stage(s) + j * T::B_ATOM_BYTES, &tm_w, n0 + j * T::W_ATOM, kb * T::BK,
-                      full);
+            for (int j = 0; j < T::W_BOXES; ++j)
+              tma_load_2d(b_stage(st) + j * T::B_ATOM_BYTES, &tm_w, n0 + j * T::W_ATOM,
+                          kb * T::BK, full);
+          }
+        }
+        __syncwarp();
         filled = kb + 1;
       }
       // Never leave with copies in flight: wait for the last fill of each slot.
-      for (int kb = (filled > T::NS ? filled - T::NS : 0); kb < filled; ++kb)
-        wait_phase(bar(T::BAR_B_FULL + kb % T::NS), (kb / T::NS) & 1, ctl, false);
+      if (lane == 0)
+        for (int kb = (filled > T::NS ? filled - T::NS : 0); kb < filled; ++kb)
+          wait_phase(bar(T::BAR_OP_TMA + kb % T::NS), (kb / T::NS) & 1, ctl, false);
+      __syncwarp();
     }
   } else if (warp == 1) {
     // ---------------- UMMA issuer
-    if (lane == 0) {
-      for (int kb = 0; kb < nkb; ++kb) {
-        const int s = kb % T::NS;
-        const uint32_t ph = (kb / T::NS) & 1;
-        if (!wait_phase(bar(T::BAR_B_FULL + s), ph, ctl)) break;
-        if (T::kXform && !wait_phase(bar(T::BAR_A_FULL + s), ph, ctl)) break;
+    for (int kb = 0; kb < nkb; ++kb) {
+      const int st = kb % T::NS;
+      const uint32_t ph = (kb / T::NS) & 1;
+      if (T::OP_TMA_BYTES > 0 && !lane0_wait_phase(bar(T::BAR_OP_TMA + st), ph, ctl, lane)) break;
+      if (!lane0_wait_phase(bar(T::BAR_OP_XF + st), ph, ctl, lane)) break;
+      if (lane == 0) {
         tc_fence_after_sync();
 #pragma unroll
         for (int k = 0; k < T::NMMA; ++k) {
-          const uint64_t adesc = umma_desc_sw128(a_stage(s) + k * 32, 16, 1024);
+          const uint64_t adesc = umma_desc_sw128(a_stage(st) + k * 32, 16, 1024);
           const uint64_t bdesc =
-              umma_desc_sw128(b_stage(s) + k * T::KSTEP * 128, T::B_ATOM_BYTES, 1024);
+              T::kXformB ? umma_desc_sw128(b_stage(st) + k * 32, 16, 1024)
+                         : umma_desc_sw128(b_stage(st) + k * T::KSTEP * 128, T::B_ATOM_BYTES, 1024);
           if constexpr (T::kF16)
             umma_f16(tmem, adesc, bdesc, T::IDESC, (kb | k) != 0);
           else
             umma_tf32(tmem, adesc, bdesc, T::IDESC, (kb | k) != 0);
         }
-        umma_commit(bar(T::BAR_OP_EMPTY + s));   // frees the stage when these UMMAs finish
+        umma_commit(bar(T::BAR_OP_EMPTY + st));   // frees the stage when these UMMAs finish
       }
-      umma_commit(bar(T::BAR_ACC_FULL));         // accumulator complete (or drained)
+      __syncwarp();
+    }
+    if (lane == 0) {
+      umma_commit(bar(T::BAR_ACC_FULL));          // accumulator complete (or drained)
       // Keep TMEM allocated until every issued UMMA has finished.
       wait_phase(bar(T::BAR_ACC_FULL), 0, ctl, false);
     }
+    __syncwarp();
   } else if (warp == 3) {
-    // ---------------- raw f32 input producer (transform paths)
-    if constexpr (T::kXform) {
-      if (lane == 0 && !withhold) {
-        const int nraw = nkb * T::RAW_PER_KB;
-        int filled = 0;
-        for (int t = 0; t < nraw; ++t) {
-          const int r = t % T::NR;
-          const int n = t / T::NR;
-          if (t >= T::NR && !wait_phase(bar(T::BAR_RAW_EMPTY + r), (n - 1) & 1, ctl)) break;
+    // ---------------- raw-stage TMA producer (inputs of the transform warps)
+    if (!withhold) {
+      const int nraw = nkb * T::RAW_PER_KB;
+      int filled = 0;
+      for (int t = 0; t < nraw; ++t) {
+        const int r = t % T::NR;
+        const int n = t / T::NR;
+        if (t >= T::NR && !lane0_wait_phase(bar(T::BAR_RAW_EMPTY + r), (n - 1) & 1, ctl, lane))
+          break;
+        if (lane == 0) {
           const uint32_t full = bar(T::BAR_RAW_FULL + r);
           mbar_arrive_expect_tx(full, T::RAW_STAGE_BYTES);
-          tma_load_2d(raw_stage(r), &tm_a, t * 32, m0, full);
-          if constexpr (T::kSwiglu)
-            tma_load_2d(raw_stage(r) + T::RAW_BOX_BYTES, &tm_u, t * 32, m0, full);
-          filled = t + 1;
+          if constexpr (T::kXformA) {
+            tma_load_2d(raw_stage(r), &tm_a, t * 32, m0, full);
+            if constexpr (T::kSwiglu)
+              tma_load_2d(raw_stage(r) + T::RAW_BOX_BYTES, &tm_u, t * 32, m0, full);
+          }
+          if constexpr (T::kXformB) {
+            // TF32: one raw stage per k-block (t == kb); W runs of 32 columns
+#pragma unroll
+            for (int j = 0; j < BN / 32; ++j)
+              tma_load_2d(raw_stage(r) + T::RAW_A_BYTES + j * 4096, &tm_w, n0 + j * 32, t * 32,
+                          full);
+          }
         }
+        __syncwarp();
+        filled = t + 1;
+      }
+      if (lane == 0)
         for (int t = (filled > T::NR ? filled - T::NR : 0); t < filled; ++t)
           wait_phase(bar(T::BAR_RAW_FULL + t % T::NR), (t / T::NR) & 1, ctl, false);
-      }
+      __syncwarp();
     }
-  } else {
+  } else if (warp >= 4) {
     // ---------------- warps 4-7: transform, then epilogue
     const int q = warp - 4;                 // TMEM lane quadrant of this warp
     const int tid = threadIdx.x - 128;      // 0..127
     bool ok = true;
-    if constexpr (T::kXform) {
-      int t = 0;
-      for (int kb = 0; kb < nkb && ok; ++kb) {
-        const int s = kb % T::NS;
-        const int n = kb / T::NS;
-        if (kb >= T::NS && !warp_wait_phase(bar(T::BAR_OP_EMPTY + s), (n - 1) & 1, ctl)) {
+    int t = 0;
+    for (int kb = 0; kb < nkb && ok; ++kb) {
+      const int st = kb % T::NS;
+      const int n = kb / T::NS;
+      if (kb >= T::NS && !warp_wait_phase(bar(T::BAR_OP_EMPTY + st), (n - 1) & 1, ctl)) {
+        ok = false;
+        break;
+      }
+#pragma unroll 1
+      for (int h = 0; h < T::RAW_PER_KB; ++h, ++t) {
+        const int r = t % T::NR;
+        if (!warp_wait_phase(bar(T::BAR_RAW_FULL + r), (t / T::NR) & 1, ctl)) {
           ok = false;
           break;
         }
-#pragma unroll 1
-        for (int h = 0; h < T::RAW_PER_KB; ++h, ++t) {
-          const int r = t % T::NR;
-          if (!warp_wait_phase(bar(T::BAR_RAW_FULL + r), (t / T::NR) & 1, ctl)) {
-            ok = false;
-            break;
-          }
-          transform_raw_stage<AMODE>(a_stage(s), raw_stage(r), h, tid);
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(T::BAR_RAW_EMPTY + r));
-        }
-        if (!ok) break;
-        fence_proxy_async_smem();   // operand writes -> visible to the UMMA (async proxy)
+        if constexpr (T::kXformA) transform_raw_stage<AMODE>(a_stage(st), raw_stage(r), h, tid);
+        if constexpr (T::kXformB) transpose_w_tile<BN>(b_stage(st), raw_stage(r) + T::RAW_A_BYTES, q, lane);
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(T::BAR_A_FULL + s));
+        if (lane == 0) mbar_arrive(bar(T::BAR_RAW_EMPTY + r));
       }
-      // The epilogue buffers alias the raw ring: all four warps must be done
-      // reading it first.
-      named_bar_sync(1, 128);
+      if (!ok) break;
+      fence_proxy_async_smem();   // operand writes -> visible to the UMMA (async proxy)
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(T::BAR_OP_XF + st));
     }
+    // The epilogue buffers alias the raw ring: all four warps must be done
+    // reading it first.
+    named_bar_sync(1, 128);
 
     const int row0 = m0 + q * kEpiRows;
     const bool rows_in = row0 < args.M;      // a box starting past M would store nothing
@@ -398,13 +477,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Residual tiles are prefetched one chunk ahead; r_issued / r_done count
     // the chunks whose load was issued / waited for (lane 0's view).
     int r_issued = 0, r_done = 0;
-    if (RESID && rows_in && lane == 0 && nc > 0) {
+    if (RESID && rows_in && !withhold && lane == 0 && nc > 0) {
       mbar_arrive_expect_tx(ebar0, T::EPI_BUF_BYTES);
       tma_load_2d(buf0, &tm_r, n0, row0, ebar0);
       r_issued = 1;
     }
     ok = warp_wait_phase(bar(T::BAR_ACC_FULL), 0, ctl);
     tc_fence_after_sync();
+    // After any role gave up (or in the self-test, whose tensor maps are
+    // empty) the accumulator is not valid: store nothing.
+    ok = ok && !withhold && (__shfl_sync(0xffffffffu, *abort_flag, 0) == 0);
     if (ok && rows_in) {
       for (int c = 0; c < nc; ++c) {
         const int b = c & 1;
