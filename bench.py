@@ -322,6 +322,9 @@ def run_ours(args, rank: int, world: int):
     lin.lib()
     peaks, peak_src = load_peaks()
     w = wl.WORKLOADS_BY_NAME[args.workload]
+    if args.m is not None:
+        import dataclasses
+        w = dataclasses.replace(w, M=args.m)
 
     def barrier():
         if dist is not None:
@@ -379,7 +382,7 @@ def run_ours(args, rank: int, world: int):
 
     # ---- end to end through the public API: pinned host buffers, H2D of the
     # step's inputs, the call, D2H of Y, all inside the timed region
-    e2e_steps = max(3, min(args.steps, args.e2e_steps))
+    e2e_steps = 0 if args.no_e2e else max(3, min(args.steps, args.e2e_steps))
     pinned = {k: torch.from_numpy(v.view(np.int16) if v.dtype == np.uint16 else v).pin_memory()
               for k, v in host.items()}
     y_host = torch.empty((w.M, w.N), dtype=torch.float32).pin_memory()
@@ -392,7 +395,8 @@ def run_ours(args, rank: int, world: int):
         lin.run_form(w.form, d, Y)
         y_host.copy_(Y, non_blocking=True)
 
-    e2e_step()
+    if e2e_steps:
+        e2e_step()
     torch.cuda.synchronize()
     barrier()
     f0 = torch.cuda.Event(enable_timing=True)
@@ -402,11 +406,11 @@ def run_ours(args, rank: int, world: int):
         e2e_step()
     f1.record(stream)
     f1.synchronize()
-    e2e_ms = f0.elapsed_time(f1) / e2e_steps
+    e2e_ms = f0.elapsed_time(f1) / max(e2e_steps, 1)
     e2e_t = torch.tensor([e2e_ms], dtype=torch.float64, device="cuda")
     if dist is not None:
         dist.all_reduce(e2e_t, op=dist.ReduceOp.MAX)
-    e2e_value = world * w.flops / (float(e2e_t.item()) * 1e-3) / 1e12
+    e2e_value = world * w.flops / (float(e2e_t.item()) * 1e-3) / 1e12 if e2e_steps else None
     del pinned, y_host
 
     # ---- roofline of the GEMM kernel (one launch per step)
@@ -469,6 +473,9 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=16)
     ap.add_argument("--no-small", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--m", type=int, default=None,
+                    help="override M (tokens) of the workload, e.g. a small case for ncu")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
