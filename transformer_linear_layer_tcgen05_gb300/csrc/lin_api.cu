@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -152,6 +153,25 @@ bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Cluster size of the binary16 kernels: enough CTAs along N to share the
+// transformed A operand, within what N can use. LIN_F16_KERNEL overrides it
+// for measurements: "tile" selects the per-tile kernel, "1", "2" or "4" a
+// cluster size.
+int f16_cluster_size(uint64_t N) {
+  static const int forced = [] {
+    const char* v = std::getenv("LIN_F16_KERNEL");
+    if (!v) return -1;
+    if (std::strcmp(v, "tile") == 0) return 0;
+    const int c = std::atoi(v);
+    return (c == 1 || c == 2 || c == 4) ? c : -1;
+  }();
+  if (forced >= 0) return forced;
+  // Pairs use all 152 SMs (clusters of 4 leave 8 idle) and measured fastest
+  // on the 16k-token SwiGLU down projection (2 > 4 > 1).
+  const uint64_t per = (uint64_t)lin::kClusterBN;
+  return N >= 2 * per ? 2 : 1;
+}
+
 enum Form : int { F_MATMUL = 0, F_RESID = 1, F_SWIGLU = 2 };
 
 struct Problem {
@@ -231,13 +251,15 @@ lin_status run(const Problem& p, cudaStream_t stream) {
 
   // 8. tensor maps and launch
   const int bn = 128;
+  const int cn = p.w16 ? f16_cluster_size(N) : 0;   // 0: the per-tile kernel
   lin::TensorMaps maps;
   std::memset(&maps, 0, sizeof(maps));
   const CUtensorMapDataType f32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   bool ok = true;
   const float* a_src = swiglu ? p.G : p.X;
-  ok &= encode_2d(&maps.a, f32, a_src, K, M, K * 4, 32, lin::kBM);
-  if (swiglu) ok &= encode_2d(&maps.u, f32, p.U, K, M, K * 4, 32, lin::kBM);
+  const uint32_t a_rows = cn > 0 ? (uint32_t)(lin::kBM / cn) : (uint32_t)lin::kBM;
+  ok &= encode_2d(&maps.a, f32, a_src, K, M, K * 4, 32, a_rows);
+  if (swiglu) ok &= encode_2d(&maps.u, f32, p.U, K, M, K * 4, 32, a_rows);
   if (p.w16)
     ok &= encode_2d(&maps.w, CU_TENSOR_MAP_DATA_TYPE_UINT16, p.W, N, K, N * 2, 64, 64);
   else
@@ -255,7 +277,10 @@ lin_status run(const Problem& p, cudaStream_t stream) {
   args.status = status_word;
 
   cudaError_t e;
-  if (p.w16)
+  if (cn > 0)
+    e = swiglu ? lin::launch_gemm_cluster_swiglu(cn, maps, args, stream)
+               : lin::launch_gemm_cluster_cvt(cn, resid, maps, args, stream);
+  else if (p.w16)
     e = lin::launch_gemm_f16(swiglu ? lin::A_SWIGLU_F16 : lin::A_CVT_F16, resid, bn, maps, args,
                              stream);
   else

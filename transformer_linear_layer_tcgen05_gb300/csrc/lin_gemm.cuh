@@ -30,8 +30,7 @@
 
 #include <atomic>
 
-#include "lin_internal.h"
-#include "lin_ptx.cuh"
+#include "lin_common.cuh"
 
 namespace lin {
 
@@ -119,78 +118,6 @@ struct GemmTraits {
   static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256 && (BN & (BN - 1)) == 0, "tile width");
   static_assert(BN % W_ATOM == 0, "W runs per tile");
 };
-
-// ---------------------------------------------------------------- waiting
-
-struct WaitCtl {
-  uint64_t timeout_ns;
-  volatile int* abort;  // shared-memory flag: some role gave up
-  int* status;          // device status word
-};
-
-// Wait for completion of the barrier phase with parity `parity`. Returns
-// false if the wait ran out (and records the timeout) or, when
-// `honor_abort`, if another role already gave up.
-__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const WaitCtl& c,
-                                           bool honor_abort = true) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-#pragma unroll 1
-  for (;;) {
-#pragma unroll 1
-    for (int i = 0; i < 16; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
-    if (honor_abort && *c.abort) return false;
-    if (global_timer_ns() - t0 > c.timeout_ns) {
-      *c.abort = 1;
-      atomicCAS(c.status, KSTATUS_OK, KSTATUS_TIMEOUT);
-      return false;
-    }
-  }
-}
-
-// Warp-uniform wait: every lane waits (each needs the acquire), and the warp
-// proceeds only if all lanes succeeded.
-__device__ __forceinline__ bool warp_wait_phase(uint32_t bar, uint32_t parity, const WaitCtl& c) {
-  const bool ok = wait_phase(bar, parity, c);
-  return __all_sync(0xffffffffu, ok);
-}
-
-// Lane 0 waits (it is the lane that issues the copies or UMMAs that follow);
-// the result is broadcast so the warp stays converged.
-__device__ __forceinline__ bool lane0_wait_phase(uint32_t bar, uint32_t parity, const WaitCtl& c,
-                                                 int lane) {
-  bool ok = true;
-  if (lane == 0) ok = wait_phase(bar, parity, c);
-  return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-}
-
-// ---------------------------------------------------------------- activation
-
-// silu(x) = x * sigma(x) with the stable, sign-branched sigmoid of page
-// 09_backward_ffn ("SiLU'"; note 2 of "WGSL-Spesifik Notlar"):
-//   x >= 0: 1 / (1 + exp(-x))      x < 0: exp(x) / (1 + exp(x)).
-// Both branches evaluate exp at -|x| <= 0, so it cannot overflow; the branch
-// is a select on the numerator. Very negative x underflows to 0.
-__device__ __forceinline__ float silu_stable(float x) {
-  const float e = __expf(-fabsf(x));
-  const float num = x >= 0.0f ? 1.0f : e;
-  return x * __fdividef(num, 1.0f + e);
-}
-
-__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
-  const __half2 h = __floats2half2_rn(lo, hi);   // round-to-nearest-even
-  return *reinterpret_cast<const uint32_t*>(&h);
-}
-
-// ---------------------------------------------------------------- transform
-
-// Swizzled byte offset of 16-byte chunk `c` of row `r` in a [rows][128 B]
-// tile with the 128-byte swizzle (chunk index XOR row mod 8), the layout both
-// TMA (SWIZZLE_128B) and the UMMA K-major descriptor use.
-__device__ __forceinline__ uint32_t sw128(uint32_t r, uint32_t c) {
-  return r * 128u + ((c ^ (r & 7u)) << 4);
-}
 
 // Build part of one A k-block from one raw stage (32 f32 columns of X or of
 // GATE and UP). `half` selects which 32 columns of the k-block this raw stage

@@ -1,0 +1,559 @@
+// lin_gemm_cluster.cuh -- persistent, clustered tcgen05 GEMM for the
+// binary16-weight forms whose A operand is built on chip:
+//
+//   matmul_residual_swiglu_a_w16   A = f16(silu(GATE) * UP)   (+ R)
+//   matmul_w16 / _residual_w16     A = f16(X)                 (+ R)
+//
+// (page "matmul ve matmul_residual -- Tiled Matrix Multiply (Forward)",
+// 03_linear_forward: "Ne Yapar?" and "Önemli Optimizasyonlar" 3).
+//
+// Why clusters: the A operand of an output row block is the same for every
+// N tile. A cluster of CN CTAs side by side along N computes CN tiles of one
+// row block at once; each CTA transforms only 128/CN rows of every A
+// k-block and writes them into the A stage of every CTA of the cluster
+// through distributed shared memory, so each GATE/UP element is read from L2
+// and transformed once per cluster instead of once per tile.
+//
+// Per CTA: a 128 x BN output tile per work item, persistent over work items
+// (cluster tiles in a static round-robin), accumulator double-buffered in
+// TMEM (2 x BN columns) so the epilogue of one tile overlaps the main loop
+// of the next. Sixteen warps:
+//   warp 0      TMA producer of the binary16 W tiles (MN-major B operand)
+//   warp 1      UMMA issuer; its per-stage commit is multicast to the whole
+//               cluster (a stage may be refilled once every CTA read it)
+//   warp 2      TMEM allocator
+//   warp 3      TMA producer of this CTA's rows of GATE/UP (or X)
+//   warps 4-11  transform: each warp turns its slice of this CTA's rows into
+//               binary16 A rows (silu(GATE)*UP, or X), writes them into the
+//               local A stage and bulk-copies them (TMA engine, shared to
+//               shared) into the same stage of every other CTA of the
+//               cluster; the copies complete on the receiver's full barrier
+//   warps 12-15 epilogue: TMEM -> registers, + R, TMA store of Y
+#pragma once
+
+#include <atomic>
+
+#include "lin_common.cuh"
+
+namespace lin {
+
+template <int AMODE, bool RESID, int BN_, int CN_>
+struct ClusterTraits {
+  static_assert(AMODE == A_CVT_F16 || AMODE == A_SWIGLU_F16, "binary16 forms only");
+  static constexpr bool kSwiglu = (AMODE == A_SWIGLU_F16);
+  static constexpr int BM = kBM;
+  static constexpr int BN = BN_;
+  static constexpr int CN = CN_;                  // CTAs per cluster, along N
+  static constexpr int BK = 64;                   // binary16 elements per k-block
+  static constexpr int KSTEP = 16;
+  static constexpr int NMMA = BK / KSTEP;
+  static constexpr int W_ATOM = 64;
+  static constexpr int W_BOXES = BN / W_ATOM;
+  static constexpr int ROWS = BM / CN;            // A rows this CTA transforms
+  static constexpr int XF_WARPS = 8;
+  static constexpr int RW = ROWS / XF_WARPS;      // A rows per transform warp
+  static constexpr uint32_t SLICE_BYTES = RW * 128;             // one warp's rows of a stage
+  static constexpr uint32_t REMOTE_BYTES_PER_WARP = SLICE_BYTES * (CN - 1);
+
+  static constexpr uint32_t A_BYTES = BM * 128;
+  static constexpr uint32_t B_ATOM_BYTES = BK * 128;
+  static constexpr uint32_t B_BYTES = W_BOXES * B_ATOM_BYTES;
+  static constexpr uint32_t OP_STAGE_BYTES = A_BYTES + B_BYTES;
+
+  static constexpr int RAW_INPUTS = kSwiglu ? 2 : 1;
+  static constexpr uint32_t RAW_BOX_BYTES = ROWS * 128;        // [ROWS][32 f32]
+  static constexpr uint32_t RAW_STAGE_BYTES = RAW_INPUTS * RAW_BOX_BYTES;
+  static constexpr int RAW_PER_KB = 2;
+  static constexpr int NR_WANT = (int)(49152u / RAW_STAGE_BYTES);
+  static constexpr int NR = NR_WANT > 8 ? 8 : (NR_WANT < 2 ? 2 : NR_WANT);
+
+  static constexpr uint32_t EPI_BUF_BYTES = kEpiRows * kEpiCols * 4;   // 4 KB
+  static constexpr uint32_t EPI_BYTES = 4 * 2 * EPI_BUF_BYTES;
+
+  static constexpr uint32_t SMEM_CAP = 232448;
+  static constexpr uint32_t BAR_REGION = 1024;
+  static constexpr uint32_t ALIGN_SLACK = 1024;
+  static constexpr uint32_t FIXED_BYTES = NR * RAW_STAGE_BYTES + EPI_BYTES;
+  static constexpr int NS_FIT =
+      (int)((SMEM_CAP - BAR_REGION - ALIGN_SLACK - FIXED_BYTES) / OP_STAGE_BYTES);
+  static constexpr int NS = NS_FIT > 8 ? 8 : NS_FIT;
+
+  static constexpr uint32_t OFF_OP = 0;
+  static constexpr uint32_t OFF_RAW = NS * OP_STAGE_BYTES;
+  static constexpr uint32_t OFF_EPI = OFF_RAW + NR * RAW_STAGE_BYTES;
+  static constexpr uint32_t OFF_BAR = OFF_EPI + EPI_BYTES;
+  static constexpr uint32_t SMEM_BYTES = ALIGN_SLACK + OFF_BAR + BAR_REGION;
+
+  static constexpr int BAR_B_FULL = 0;                   // W tile landed (local TMA)
+  static constexpr int BAR_A_FULL = BAR_B_FULL + 8;      // A rows from every CTA landed
+  static constexpr int BAR_ST_EMPTY = BAR_A_FULL + 8;    // every CTA's UMMA done with stage
+  static constexpr int BAR_RAW_FULL = BAR_ST_EMPTY + 8;
+  static constexpr int BAR_RAW_EMPTY = BAR_RAW_FULL + 8;
+  static constexpr int BAR_ACC_FULL = BAR_RAW_EMPTY + 8; // 2 accumulator buffers
+  static constexpr int BAR_ACC_EMPTY = BAR_ACC_FULL + 2;
+  static constexpr int BAR_EPI = BAR_ACC_EMPTY + 2;      // 2 per epilogue warp
+  static constexpr int BAR_COUNT = BAR_EPI + 8;
+  static constexpr uint32_t OFF_TMEM_SLOT = BAR_COUNT * 8;
+  static constexpr uint32_t OFF_ABORT = OFF_TMEM_SLOT + 4;
+
+  static constexpr uint32_t TMEM_COLS = 2 * BN;
+  static constexpr uint32_t IDESC = umma_idesc(0u, false, true, BM, BN);
+  static constexpr uint16_t CLUSTER_MASK = (uint16_t)((1u << CN) - 1u);
+  static constexpr int kThreadsC = 512;
+
+  static_assert(CN == 1 || CN == 2 || CN == 4 || CN == 8, "cluster size");
+  static_assert(ROWS % 8 == 0, "row share must hold whole swizzle atoms");
+  static_assert(RW == 4 || RW % 8 == 0, "rows per transform warp");
+  static_assert(NS >= 2 && NS <= 8 && NR <= 8, "ring depths");
+  static_assert(OFF_ABORT + 4 <= BAR_REGION, "barrier region");
+  static_assert(SMEM_BYTES <= SMEM_CAP, "shared memory");
+  static_assert(TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM columns");
+};
+
+// Transform warp `tw` (0..7): its RW rows of one raw stage (32 f32 columns:
+// half `half` of a 64-wide k-block) -> binary16 A rows in the local A stage.
+// Eight consecutive lanes take eight different rows of one 16-byte column, so
+// the 128-byte swizzle keeps loads and stores free of bank conflicts.
+template <typename T>
+__device__ __forceinline__ void transform_slice(uint32_t a_stage, uint32_t raw, int half, int tw,
+                                                int lane, uint32_t crank) {
+  constexpr uint32_t BOX = T::RAW_BOX_BYTES;
+#pragma unroll
+  for (int idx = lane; idx < T::RW * 4; idx += 32) {
+    uint32_t row, cc;
+    if constexpr (T::RW == 4) {
+      row = (uint32_t)(idx & 3);
+      cc = (uint32_t)(idx >> 2);
+    } else {
+      row = (uint32_t)((idx & 7) + 8 * (idx >> 5));
+      cc = (uint32_t)((idx >> 3) & 3);
+    }
+    const uint32_t rs = (uint32_t)(tw * T::RW) + row;          // row within this CTA's share
+    const uint32_t o0 = sw128(rs, 2 * cc);
+    const uint32_t o1 = sw128(rs, 2 * cc + 1);
+    float4 a0 = ld_shared_v4f(raw + o0);
+    float4 a1 = ld_shared_v4f(raw + o1);
+    if constexpr (T::kSwiglu) {
+      const float4 u0 = ld_shared_v4f(raw + BOX + o0);
+      const float4 u1 = ld_shared_v4f(raw + BOX + o1);
+      a0.x = silu_stable_fast(a0.x) * u0.x;
+      a0.y = silu_stable_fast(a0.y) * u0.y;
+      a0.z = silu_stable_fast(a0.z) * u0.z;
+      a0.w = silu_stable_fast(a0.w) * u0.w;
+      a1.x = silu_stable_fast(a1.x) * u1.x;
+      a1.y = silu_stable_fast(a1.y) * u1.y;
+      a1.z = silu_stable_fast(a1.z) * u1.z;
+      a1.w = silu_stable_fast(a1.w) * u1.w;
+    }
+    const uint32_t r = crank * (uint32_t)T::ROWS + rs;          // row of the A block
+    st_shared_v4(a_stage + sw128(r, 4 * (uint32_t)half + cc), pack_half2(a0.x, a0.y),
+                 pack_half2(a0.z, a0.w), pack_half2(a1.x, a1.y), pack_half2(a1.z, a1.w));
+  }
+}
+
+template <int AMODE, bool RESID, int BN, int CN>
+__global__ void __launch_bounds__(512, 1)
+    lin_gemm_cluster_kernel(const __grid_constant__ CUtensorMap tm_a,
+                            const __grid_constant__ CUtensorMap tm_u,
+                            const __grid_constant__ CUtensorMap tm_w,
+                            const __grid_constant__ CUtensorMap tm_r,
+                            const __grid_constant__ CUtensorMap tm_y, const KernelArgs args) {
+  using T = ClusterTraits<AMODE, RESID, BN, CN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + T::OFF_BAR;
+  auto bar = [&](int slot) -> uint32_t { return bar0 + 8u * (uint32_t)slot; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + T::OFF_BAR + T::OFF_TMEM_SLOT);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + T::OFF_BAR + T::OFF_ABORT);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t crank = (CN > 1) ? cluster_ctarank() : 0u;
+  const int cid = blockIdx.x / CN;                  // cluster id
+  const int ncl = gridDim.x / CN;                   // clusters in the grid
+  const int num_m = (args.M + T::BM - 1) / T::BM;
+  const int num_ng = (args.N + T::BN * CN - 1) / (T::BN * CN);
+  const int num_tiles = num_m * num_ng;
+  const int nkb = (args.K + T::BK - 1) / T::BK;
+  const WaitCtl ctl{args.timeout_ns, abort_flag, args.status};
+
+  auto a_stage = [&](int s) -> uint32_t { return sbase + T::OFF_OP + s * T::OP_STAGE_BYTES; };
+  auto b_stage = [&](int s) -> uint32_t { return a_stage(s) + T::A_BYTES; };
+  auto raw_stage = [&](int r) -> uint32_t { return sbase + T::OFF_RAW + r * T::RAW_STAGE_BYTES; };
+  auto tile_m0 = [&](int t) -> int { return (t / num_ng) * T::BM; };
+  auto tile_n0 = [&](int t) -> int { return ((t % num_ng) * CN + (int)crank) * T::BN; };
+  // number of work items this cluster processes
+  const int my_tiles = cid < num_tiles ? (num_tiles - 1 - cid) / ncl + 1 : 0;
+
+  // ---- set-up
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < T::NS; ++s) {
+      mbar_init(bar(T::BAR_B_FULL + s), 1);
+      mbar_init(bar(T::BAR_A_FULL + s), T::XF_WARPS);   // local warps (+ peers' copy bytes)
+      mbar_init(bar(T::BAR_ST_EMPTY + s), CN);     // every CTA's UMMA commit
+    }
+    for (int r = 0; r < T::NR; ++r) {
+      mbar_init(bar(T::BAR_RAW_FULL + r), 1);
+      mbar_init(bar(T::BAR_RAW_EMPTY + r), T::XF_WARPS);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(T::BAR_ACC_FULL + b), 1);
+      mbar_init(bar(T::BAR_ACC_EMPTY + b), 4);
+    }
+    for (int e = 0; e < 8; ++e) mbar_init(bar(T::BAR_EPI + e), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  __syncwarp();
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_w);
+    tma_prefetch_desc(&tm_a);
+    if constexpr (T::kSwiglu) tma_prefetch_desc(&tm_u);
+    if constexpr (RESID) tma_prefetch_desc(&tm_r);
+    tma_prefetch_desc(&tm_y);
+  }
+  __syncwarp();
+  if (warp == 2) {
+    tmem_alloc(smem_u32(tmem_slot), T::TMEM_COLS);
+    tmem_relinquish_alloc_permit();
+  }
+  tc_fence_before_sync();
+  // Peers may arrive on our barriers and write our A stages only after every
+  // CTA of the cluster initialised them.
+  if constexpr (CN > 1)
+    cluster_sync_all();
+  else
+    __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------- W producer (local TMA into the B half of each stage)
+    int g = 0;   // k-blocks issued, across tiles
+    bool ok = true;
+    for (int i = 0; i < my_tiles && ok; ++i) {
+      const int t = cid + i * ncl;
+      const int n0 = tile_n0(t);
+      for (int kb = 0; kb < nkb; ++kb, ++g) {
+        const int s = g % T::NS;
+        if (g >= T::NS) {
+          bool w = true;
+          if (lane == 0) w = wait_phase_cluster(bar(T::BAR_ST_EMPTY + s), ((g / T::NS) - 1) & 1, ctl);
+          if (!__shfl_sync(0xffffffffu, w ? 1 : 0, 0)) {
+            ok = false;
+            break;
+          }
+        }
+        if (lane == 0) {
+          const uint32_t full = bar(T::BAR_B_FULL + s);
+          mbar_arrive_expect_tx(full, T::B_BYTES);
+#pragma unroll
+          for (int j = 0; j < T::W_BOXES; ++j)
+            tma_load_2d(b_stage(s) + j * T::B_ATOM_BYTES, &tm_w, n0 + j * T::W_ATOM, kb * T::BK,
+                        full);
+        }
+        __syncwarp();
+      }
+    }
+    if (lane == 0)
+      for (int x = (g > T::NS ? g - T::NS : 0); x < g; ++x)
+        wait_phase(bar(T::BAR_B_FULL + x % T::NS), (x / T::NS) & 1, ctl, false);
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------- UMMA issuer
+    int g = 0;
+    bool ok = true;
+    int committed_tiles = 0;
+    for (int i = 0; i < my_tiles && ok; ++i) {
+      const int ab = i & 1;
+      const uint32_t d_tmem = tmem + (uint32_t)(ab * T::BN);
+      if (i >= 2 && !lane0_wait_phase(bar(T::BAR_ACC_EMPTY + ab), ((i >> 1) - 1) & 1, ctl, lane)) {
+        ok = false;
+        break;
+      }
+      for (int kb = 0; kb < nkb; ++kb, ++g) {
+        const int s = g % T::NS;
+        const uint32_t ph = (g / T::NS) & 1;
+        bool w = true;
+        if (lane == 0) {
+          w = wait_phase(bar(T::BAR_B_FULL + s), ph, ctl) &&
+              wait_phase(bar(T::BAR_A_FULL + s), ph, ctl);
+        }
+        if (!__shfl_sync(0xffffffffu, w ? 1 : 0, 0)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          tc_fence_after_sync();
+#pragma unroll
+          for (int k = 0; k < T::NMMA; ++k) {
+            const uint64_t adesc = umma_desc_sw128(a_stage(s) + k * 32, 16, 1024);
+            const uint64_t bdesc =
+                umma_desc_sw128(b_stage(s) + k * T::KSTEP * 128, T::B_ATOM_BYTES, 1024);
+            umma_f16(d_tmem, adesc, bdesc, T::IDESC, (kb | k) != 0);
+          }
+          if constexpr (CN > 1)
+            umma_commit_multicast(bar(T::BAR_ST_EMPTY + s), T::CLUSTER_MASK);
+          else
+            umma_commit(bar(T::BAR_ST_EMPTY + s));
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+      if (lane == 0) umma_commit(bar(T::BAR_ACC_FULL + ab));
+      __syncwarp();
+      committed_tiles = i + 1;
+    }
+    if (lane == 0) {
+      // Every issued UMMA must finish before TMEM is released: one more
+      // commit on a buffer whose phase we can wait for.
+      if (!ok) {
+        const int ab = committed_tiles & 1;
+        umma_commit(bar(T::BAR_ACC_FULL + ab));
+        wait_phase(bar(T::BAR_ACC_FULL + ab), (committed_tiles >> 1) & 1, ctl, false);
+      } else if (committed_tiles > 0) {
+        const int last = committed_tiles - 1;
+        wait_phase(bar(T::BAR_ACC_FULL + (last & 1)), (last >> 1) & 1, ctl, false);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 3) {
+    // ---------------- raw producer: this CTA's rows of GATE/UP (or X)
+    int tr = 0;   // raw stages issued, across tiles
+    bool ok = true;
+    for (int i = 0; i < my_tiles && ok; ++i) {
+      const int t = cid + i * ncl;
+      const int row = tile_m0(t) + (int)crank * T::ROWS;
+      for (int h = 0; h < nkb * T::RAW_PER_KB; ++h, ++tr) {
+        const int r = tr % T::NR;
+        if (tr >= T::NR &&
+            !lane0_wait_phase(bar(T::BAR_RAW_EMPTY + r), ((tr / T::NR) - 1) & 1, ctl, lane)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          const uint32_t full = bar(T::BAR_RAW_FULL + r);
+          mbar_arrive_expect_tx(full, T::RAW_STAGE_BYTES);
+          tma_load_2d(raw_stage(r), &tm_a, h * 32, row, full);
+          if constexpr (T::kSwiglu)
+            tma_load_2d(raw_stage(r) + T::RAW_BOX_BYTES, &tm_u, h * 32, row, full);
+        }
+        __syncwarp();
+      }
+    }
+    if (lane == 0)
+      for (int x = (tr > T::NR ? tr - T::NR : 0); x < tr; ++x)
+        wait_phase(bar(T::BAR_RAW_FULL + x % T::NR), (x / T::NR) & 1, ctl, false);
+    __syncwarp();
+  } else if (warp >= 4 && warp < 4 + T::XF_WARPS) {
+    // ---------------- transform warps
+    const int tw = warp - 4;
+    const uint32_t slice_off = (crank * (uint32_t)T::ROWS + (uint32_t)(tw * T::RW)) * 128u;
+    int g = 0, tr = 0;
+    bool ok = true;
+    for (int i = 0; i < my_tiles && ok; ++i) {
+      for (int kb = 0; kb < nkb; ++kb, ++g) {
+        const int s = g % T::NS;
+        if (g >= T::NS) {
+          // Every CTA's UMMA is done with this stage: ours may be rewritten
+          // and the peers' copies of it overwritten.
+          const bool w = wait_phase_cluster(bar(T::BAR_ST_EMPTY + s), ((g / T::NS) - 1) & 1, ctl);
+          if (!__all_sync(0xffffffffu, w)) {
+            ok = false;
+            break;
+          }
+        }
+#pragma unroll 1
+        for (int h = 0; h < T::RAW_PER_KB; ++h, ++tr) {
+          const int r = tr % T::NR;
+          if (!warp_wait_phase(bar(T::BAR_RAW_FULL + r), (tr / T::NR) & 1, ctl)) {
+            ok = false;
+            break;
+          }
+          transform_slice<T>(a_stage(s), raw_stage(r), h, tw, lane, crank);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(T::BAR_RAW_EMPTY + r));
+        }
+        if (!ok) break;
+        fence_proxy_async_smem();   // our rows -> visible to UMMA and to the copy engine
+        __syncwarp();
+        if (lane == 0) {
+          const uint32_t full = bar(T::BAR_A_FULL + s);
+          if constexpr (CN > 1) {
+            // The peers' slices of this stage arrive as copy bytes on our barrier.
+            mbar_arrive_expect_tx(full, T::REMOTE_BYTES_PER_WARP);
+            const uint32_t src = a_stage(s) + slice_off;
+#pragma unroll
+            for (uint32_t d = 0; d < (uint32_t)CN; ++d)
+              if (d != crank)
+                bulk_copy_s2cluster(mapa_shared(src, d), src, T::SLICE_BYTES, mapa_shared(full, d));
+          } else {
+            mbar_arrive(full);
+          }
+        }
+        __syncwarp();
+      }
+    }
+    // Every peer's commit for the stages we filled must have landed (they
+    // arrive on our barriers, and our copies read our shared memory) before
+    // this CTA may leave.
+    if (lane == 0)
+      for (int x = (g > T::NS ? g - T::NS : 0); x < g; ++x)
+        wait_phase_cluster(bar(T::BAR_ST_EMPTY + x % T::NS), (x / T::NS) & 1, ctl, false);
+    __syncwarp();
+  } else if (warp >= 4 + T::XF_WARPS) {
+    // ---------------- epilogue warps
+    const int q = warp & 3;                        // TMEM lane quadrant
+    const uint32_t buf0 = sbase + T::OFF_EPI + (uint32_t)(q * 2) * T::EPI_BUF_BYTES;
+    const uint32_t ebar0 = bar(T::BAR_EPI + q * 2);
+    constexpr int NC = T::BN / kEpiCols;
+    int gc = 0;          // epilogue chunks started, across tiles (buffer = gc & 1)
+    int r_issued = 0;    // residual loads issued (lane 0's view), indexed like gc
+    int r_done = 0;
+    bool ok = true;
+    for (int i = 0; i < my_tiles && ok; ++i) {
+      const int t = cid + i * ncl;
+      const int ab = i & 1;
+      const int row0 = tile_m0(t) + q * kEpiRows;
+      const int n0 = tile_n0(t);
+      const bool rows_in = row0 < args.M;
+      int nc = n0 < args.N ? (args.N - n0 + kEpiCols - 1) / kEpiCols : 0;
+      if (nc > NC) nc = NC;
+      if (!rows_in) nc = 0;
+      // Prefetch the residual of this tile's first chunk.
+      if (RESID && lane == 0 && nc > 0) {
+        bulk_wait_group_read<0>();
+        const uint32_t eb = ebar0 + 8u * (uint32_t)(gc & 1);
+        mbar_arrive_expect_tx(eb, T::EPI_BUF_BYTES);
+        tma_load_2d(buf0 + (gc & 1) * T::EPI_BUF_BYTES, &tm_r, n0, row0, eb);
+        r_issued = gc + 1;
+      }
+      __syncwarp();
+      ok = warp_wait_phase(bar(T::BAR_ACC_FULL + ab), (i >> 1) & 1, ctl);
+      tc_fence_after_sync();
+      ok = ok && (__shfl_sync(0xffffffffu, *abort_flag, 0) == 0);
+      if (!ok) break;
+      const uint32_t acc = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * T::BN);
+      for (int c = 0; c < nc; ++c, ++gc) {
+        const int b = gc & 1;
+        const uint32_t buf = buf0 + b * T::EPI_BUF_BYTES;
+        if (lane == 0) {
+          // Both buffers' earlier stores must have read their source: this
+          // chunk writes buffer b, the prefetch below fills buffer b ^ 1.
+          bulk_wait_group_read<0>();
+          if (RESID && c + 1 < nc) {
+            const uint32_t nb = ebar0 + 8u * (uint32_t)(b ^ 1);
+            mbar_arrive_expect_tx(nb, T::EPI_BUF_BYTES);
+            tma_load_2d(buf0 + (b ^ 1) * T::EPI_BUF_BYTES, &tm_r, n0 + (c + 1) * kEpiCols, row0,
+                        nb);
+            r_issued = gc + 2;
+          }
+        }
+        __syncwarp();
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(acc + (uint32_t)(c * kEpiCols), v);
+        tmem_wait_ld();
+        if constexpr (RESID) {
+          if (!warp_wait_phase(ebar0 + 8u * (uint32_t)b, (gc >> 1) & 1, ctl)) {
+            ok = false;
+            break;
+          }
+          r_done = gc + 1;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t addr = buf + sw128(lane, j);
+          float o0 = __uint_as_float(v[4 * j + 0]);
+          float o1 = __uint_as_float(v[4 * j + 1]);
+          float o2 = __uint_as_float(v[4 * j + 2]);
+          float o3 = __uint_as_float(v[4 * j + 3]);
+          if constexpr (RESID) {
+            const float4 rr = ld_shared_v4f(addr);
+            o0 += rr.x;
+            o1 += rr.y;
+            o2 += rr.z;
+            o3 += rr.w;
+          }
+          st_shared_v4(addr, __float_as_uint(o0), __float_as_uint(o1), __float_as_uint(o2),
+                       __float_as_uint(o3));
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&tm_y, n0 + c * kEpiCols, row0, buf);
+          bulk_commit_group();
+        }
+      }
+      if (!ok) break;
+      // TMEM reads of this buffer are complete: hand it back to the UMMA warp.
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(T::BAR_ACC_EMPTY + ab));
+    }
+    if (lane == 0) {
+      for (int x = r_done; x < r_issued; ++x)
+        wait_phase(ebar0 + 8u * (uint32_t)(x & 1), (x >> 1) & 1, ctl, false);
+      bulk_wait_group_all();
+    }
+    __syncwarp();
+  }
+
+  // ---- teardown: no CTA leaves while a peer may still write to it
+  tc_fence_before_sync();
+  if constexpr (CN > 1)
+    cluster_sync_all();
+  else
+    __syncthreads();
+  if (warp == 2) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, T::TMEM_COLS);
+  }
+}
+
+template <int AMODE, bool RESID, int BN, int CN>
+cudaError_t launch_cluster_instance(const TensorMaps& m, const KernelArgs& args,
+                                    cudaStream_t stream) {
+  using T = ClusterTraits<AMODE, RESID, BN, CN>;
+  auto kern = lin_gemm_cluster_kernel<AMODE, RESID, BN, CN>;
+  static std::atomic<uint64_t> attr_done{0};
+  static std::atomic<int> max_clusters[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 64) return cudaErrorInvalidDevice;
+  const uint64_t bit = uint64_t{1} << dev;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CN;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(T::kThreadsC, 1, 1);
+  cfg.dynamicSmemBytes = T::SMEM_BYTES;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (!(attr_done.load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3(CN, 1, 1);
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, (void*)kern, &cfg);
+    if (e != cudaSuccess) return e;
+    if (n < 1) return cudaErrorInvalidConfiguration;
+    max_clusters[dev].store(n, std::memory_order_release);
+    attr_done.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  const int num_m = (args.M + T::BM - 1) / T::BM;
+  const int num_ng = (args.N + T::BN * CN - 1) / (T::BN * CN);
+  int clusters = num_m * num_ng;
+  const int cap = max_clusters[dev].load(std::memory_order_acquire);
+  if (clusters > cap) clusters = cap;
+  cfg.gridDim = dim3((unsigned)(clusters * CN), 1, 1);
+  return cudaLaunchKernelEx(&cfg, kern, m.a, m.u, m.w, m.r, m.y, args);
+}
+
+}  // namespace lin

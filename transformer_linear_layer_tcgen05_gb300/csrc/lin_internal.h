@@ -52,4 +52,13 @@ cudaError_t launch_gemm_tf32(int amode, bool resid, int bn, const TensorMaps& ma
 cudaError_t launch_gemm_f16(int amode, bool resid, int bn, const TensorMaps& maps,
                             const KernelArgs& args, cudaStream_t stream);
 
+// Clustered persistent kernels for the binary16-weight forms: a cluster of
+// `cn` CTAs along N shares the on-chip A operand (128/cn rows each). The
+// A-side tensor maps (X, or GATE and UP) must use boxes of 32 x (128/cn).
+constexpr int kClusterBN = 256;
+cudaError_t launch_gemm_cluster_swiglu(int cn, const TensorMaps& maps, const KernelArgs& args,
+                                       cudaStream_t stream);
+cudaError_t launch_gemm_cluster_cvt(int cn, bool resid, const TensorMaps& maps,
+                                    const KernelArgs& args, cudaStream_t stream);
+
 }  // namespace lin
