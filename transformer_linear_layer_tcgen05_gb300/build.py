@@ -61,7 +61,8 @@ def build_library(force: bool = False, verbose: bool = False, extra_flags=()) ->
     for src in SOURCES:
         obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
         objs.append(obj)
-        cmd = [nvcc, *ARCH, *CFLAGS, *extra_flags, "-c", os.path.join(CSRC, src), "-o", obj]
+        cmd = [nvcc, *ARCH, *CFLAGS, *extra_flags, *os.environ.get("LIN_NVCC_FLAGS", "").split(),
+               "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             print(" ".join(cmd), file=sys.stderr)
         procs.append((src, subprocess.Popen(cmd, stdout=subprocess.PIPE,

@@ -275,6 +275,8 @@ lin_status run(const Problem& p, cudaStream_t stream) {
   args.flags = 0;
   args.timeout_ns = kDefaultTimeoutNs;
   args.status = status_word;
+  args.R = resid ? p.R : nullptr;
+  args.Y = p.Y;
 
   cudaError_t e;
   if (cn > 0)
@@ -386,6 +388,8 @@ lin_status lin_selftest_wait_timeout(int64_t timeout_us, lin_stream_t stream) {
   args.flags = lin::KFLAG_WITHHOLD_PRODUCER;
   args.timeout_ns = static_cast<uint64_t>(timeout_us) * 1000ull;
   args.status = word;
+  args.R = nullptr;
+  args.Y = nullptr;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = lin::launch_gemm_tf32(lin::A_TMA_F32, false, 128, maps, args, s);
   if (e != cudaSuccess) return cuda_fail(e);

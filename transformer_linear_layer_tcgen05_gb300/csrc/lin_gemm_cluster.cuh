@@ -28,7 +28,9 @@
 //               local A stage and bulk-copies them (TMA engine, shared to
 //               shared) into the same stage of every other CTA of the
 //               cluster; the copies complete on the receiver's full barrier
-//   warps 12-15 epilogue: TMEM -> registers, + R, TMA store of Y
+//   warps 12-15 epilogue: TMEM -> registers, + R, Y; each thread owns one
+//               output row and moves it with 16-byte global loads/stores,
+//               which keeps shared memory free for a deeper input ring
 #pragma once
 
 #include <atomic>
@@ -64,24 +66,19 @@ struct ClusterTraits {
   static constexpr uint32_t RAW_BOX_BYTES = ROWS * 128;        // [ROWS][32 f32]
   static constexpr uint32_t RAW_STAGE_BYTES = RAW_INPUTS * RAW_BOX_BYTES;
   static constexpr int RAW_PER_KB = 2;
-  static constexpr int NR_WANT = (int)(49152u / RAW_STAGE_BYTES);
-  static constexpr int NR = NR_WANT > 8 ? 8 : (NR_WANT < 2 ? 2 : NR_WANT);
-
-  static constexpr uint32_t EPI_BUF_BYTES = kEpiRows * kEpiCols * 4;   // 4 KB
-  static constexpr uint32_t EPI_BYTES = 4 * 2 * EPI_BUF_BYTES;
-
   static constexpr uint32_t SMEM_CAP = 232448;
   static constexpr uint32_t BAR_REGION = 1024;
   static constexpr uint32_t ALIGN_SLACK = 1024;
-  static constexpr uint32_t FIXED_BYTES = NR * RAW_STAGE_BYTES + EPI_BYTES;
-  static constexpr int NS_FIT =
-      (int)((SMEM_CAP - BAR_REGION - ALIGN_SLACK - FIXED_BYTES) / OP_STAGE_BYTES);
-  static constexpr int NS = NS_FIT > 8 ? 8 : NS_FIT;
+  static constexpr uint32_t DATA_CAP = SMEM_CAP - BAR_REGION - ALIGN_SLACK;
+  // Three operand stages; the rest of shared memory goes to the input ring,
+  // whose depth is what hides the latency of the f32 GATE/UP (or X) loads.
+  static constexpr int NS = 3;
+  static constexpr int NR_FIT = (int)((DATA_CAP - NS * OP_STAGE_BYTES) / RAW_STAGE_BYTES);
+  static constexpr int NR = NR_FIT > 8 ? 8 : NR_FIT;
 
   static constexpr uint32_t OFF_OP = 0;
   static constexpr uint32_t OFF_RAW = NS * OP_STAGE_BYTES;
-  static constexpr uint32_t OFF_EPI = OFF_RAW + NR * RAW_STAGE_BYTES;
-  static constexpr uint32_t OFF_BAR = OFF_EPI + EPI_BYTES;
+  static constexpr uint32_t OFF_BAR = OFF_RAW + NR * RAW_STAGE_BYTES;
   static constexpr uint32_t SMEM_BYTES = ALIGN_SLACK + OFF_BAR + BAR_REGION;
 
   static constexpr int BAR_B_FULL = 0;                   // W tile landed (local TMA)
@@ -91,8 +88,7 @@ struct ClusterTraits {
   static constexpr int BAR_RAW_EMPTY = BAR_RAW_FULL + 8;
   static constexpr int BAR_ACC_FULL = BAR_RAW_EMPTY + 8; // 2 accumulator buffers
   static constexpr int BAR_ACC_EMPTY = BAR_ACC_FULL + 2;
-  static constexpr int BAR_EPI = BAR_ACC_EMPTY + 2;      // 2 per epilogue warp
-  static constexpr int BAR_COUNT = BAR_EPI + 8;
+  static constexpr int BAR_COUNT = BAR_ACC_EMPTY + 2;
   static constexpr uint32_t OFF_TMEM_SLOT = BAR_COUNT * 8;
   static constexpr uint32_t OFF_ABORT = OFF_TMEM_SLOT + 4;
 
@@ -104,23 +100,27 @@ struct ClusterTraits {
   static_assert(CN == 1 || CN == 2 || CN == 4 || CN == 8, "cluster size");
   static_assert(ROWS % 8 == 0, "row share must hold whole swizzle atoms");
   static_assert(RW == 4 || RW % 8 == 0, "rows per transform warp");
-  static_assert(NS >= 2 && NS <= 8 && NR <= 8, "ring depths");
+  static_assert(NS >= 2 && NS <= 8 && NR >= 2 && NR <= 8, "ring depths");
   static_assert(OFF_ABORT + 4 <= BAR_REGION, "barrier region");
   static_assert(SMEM_BYTES <= SMEM_CAP, "shared memory");
   static_assert(TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM columns");
+  // A CTA holding all 512 TMEM columns must be alone on its SM (a second one
+  // would wait in tcgen05.alloc while its cluster peers wait for it).
+  static_assert(TMEM_COLS < 512 || 2 * SMEM_BYTES > SMEM_CAP + BAR_REGION, "one CTA per SM");
 };
 
 // Transform warp `tw` (0..7): its RW rows of one raw stage (32 f32 columns:
-// half `half` of a 64-wide k-block) -> binary16 A rows in the local A stage.
-// Eight consecutive lanes take eight different rows of one 16-byte column, so
-// the 128-byte swizzle keeps loads and stores free of bank conflicts.
+// half `half` of a 64-wide k-block) -> binary16 A rows. Eight consecutive
+// lanes take eight different rows of one 16-byte column, so the 128-byte
+// swizzle keeps loads and stores free of bank conflicts. The work is split
+// into a compute step (results kept in registers, four words per 16-byte
+// chunk) and a store step, so a warp does the arithmetic of a k-block before
+// the stage it writes has been released.
 template <typename T>
-__device__ __forceinline__ void transform_slice(uint32_t a_stage, uint32_t raw, int half, int tw,
-                                                int lane, uint32_t crank) {
-  constexpr uint32_t BOX = T::RAW_BOX_BYTES;
-#pragma unroll
-  for (int idx = lane; idx < T::RW * 4; idx += 32) {
-    uint32_t row, cc;
+struct SliceMap {
+  static constexpr int ITEMS = T::RW * 4;                 // 16-byte chunks per half
+  static constexpr int PER_LANE = (ITEMS + 31) / 32;
+  __device__ static __forceinline__ void item(int idx, uint32_t& row, uint32_t& cc) {
     if constexpr (T::RW == 4) {
       row = (uint32_t)(idx & 3);
       cc = (uint32_t)(idx >> 2);
@@ -128,7 +128,20 @@ __device__ __forceinline__ void transform_slice(uint32_t a_stage, uint32_t raw, 
       row = (uint32_t)((idx & 7) + 8 * (idx >> 5));
       cc = (uint32_t)((idx >> 3) & 3);
     }
-    const uint32_t rs = (uint32_t)(tw * T::RW) + row;          // row within this CTA's share
+  }
+};
+
+template <typename T>
+__device__ __forceinline__ void transform_compute(uint32_t raw, int tw, int lane,
+                                                  uint32_t (&out)[SliceMap<T>::PER_LANE][4]) {
+  constexpr uint32_t BOX = T::RAW_BOX_BYTES;
+#pragma unroll
+  for (int j = 0; j < SliceMap<T>::PER_LANE; ++j) {
+    const int idx = lane + 32 * j;
+    if (idx >= SliceMap<T>::ITEMS) break;
+    uint32_t row, cc;
+    SliceMap<T>::item(idx, row, cc);
+    const uint32_t rs = (uint32_t)(tw * T::RW) + row;
     const uint32_t o0 = sw128(rs, 2 * cc);
     const uint32_t o1 = sw128(rs, 2 * cc + 1);
     float4 a0 = ld_shared_v4f(raw + o0);
@@ -145,9 +158,25 @@ __device__ __forceinline__ void transform_slice(uint32_t a_stage, uint32_t raw, 
       a1.z = silu_stable_fast(a1.z) * u1.z;
       a1.w = silu_stable_fast(a1.w) * u1.w;
     }
-    const uint32_t r = crank * (uint32_t)T::ROWS + rs;          // row of the A block
-    st_shared_v4(a_stage + sw128(r, 4 * (uint32_t)half + cc), pack_half2(a0.x, a0.y),
-                 pack_half2(a0.z, a0.w), pack_half2(a1.x, a1.y), pack_half2(a1.z, a1.w));
+    out[j][0] = pack_half2(a0.x, a0.y);
+    out[j][1] = pack_half2(a0.z, a0.w);
+    out[j][2] = pack_half2(a1.x, a1.y);
+    out[j][3] = pack_half2(a1.z, a1.w);
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ void transform_store(uint32_t a_stage, int half, int tw, int lane,
+                                                uint32_t crank,
+                                                const uint32_t (&v)[SliceMap<T>::PER_LANE][4]) {
+#pragma unroll
+  for (int j = 0; j < SliceMap<T>::PER_LANE; ++j) {
+    const int idx = lane + 32 * j;
+    if (idx >= SliceMap<T>::ITEMS) break;
+    uint32_t row, cc;
+    SliceMap<T>::item(idx, row, cc);
+    const uint32_t r = crank * (uint32_t)T::ROWS + (uint32_t)(tw * T::RW) + row;
+    st_shared_v4(a_stage + sw128(r, 4 * (uint32_t)half + cc), v[j][0], v[j][1], v[j][2], v[j][3]);
   }
 }
 
@@ -202,7 +231,6 @@ __global__ void __launch_bounds__(512, 1)
       mbar_init(bar(T::BAR_ACC_FULL + b), 1);
       mbar_init(bar(T::BAR_ACC_EMPTY + b), 4);
     }
-    for (int e = 0; e < 8; ++e) mbar_init(bar(T::BAR_EPI + e), 1);
     *abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
@@ -212,8 +240,6 @@ __global__ void __launch_bounds__(512, 1)
     tma_prefetch_desc(&tm_w);
     tma_prefetch_desc(&tm_a);
     if constexpr (T::kSwiglu) tma_prefetch_desc(&tm_u);
-    if constexpr (RESID) tma_prefetch_desc(&tm_r);
-    tma_prefetch_desc(&tm_y);
   }
   __syncwarp();
   if (warp == 2) {
@@ -357,6 +383,21 @@ __global__ void __launch_bounds__(512, 1)
     for (int i = 0; i < my_tiles && ok; ++i) {
       for (int kb = 0; kb < nkb; ++kb, ++g) {
         const int s = g % T::NS;
+        // Arithmetic first (registers); then wait for the stage to be free.
+        uint32_t vals[T::RAW_PER_KB][SliceMap<T>::PER_LANE][4];
+#pragma unroll
+        for (int h = 0; h < T::RAW_PER_KB; ++h) {
+          const int r = (tr + h) % T::NR;
+          if (!warp_wait_phase(bar(T::BAR_RAW_FULL + r), ((tr + h) / T::NR) & 1, ctl)) {
+            ok = false;
+            break;
+          }
+          transform_compute<T>(raw_stage(r), tw, lane, vals[h]);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(T::BAR_RAW_EMPTY + r));
+        }
+        tr += T::RAW_PER_KB;
+        if (!ok) break;
         if (g >= T::NS) {
           // Every CTA's UMMA is done with this stage: ours may be rewritten
           // and the peers' copies of it overwritten.
@@ -366,18 +407,9 @@ __global__ void __launch_bounds__(512, 1)
             break;
           }
         }
-#pragma unroll 1
-        for (int h = 0; h < T::RAW_PER_KB; ++h, ++tr) {
-          const int r = tr % T::NR;
-          if (!warp_wait_phase(bar(T::BAR_RAW_FULL + r), (tr / T::NR) & 1, ctl)) {
-            ok = false;
-            break;
-          }
-          transform_slice<T>(a_stage(s), raw_stage(r), h, tw, lane, crank);
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(T::BAR_RAW_EMPTY + r));
-        }
-        if (!ok) break;
+#pragma unroll
+        for (int h = 0; h < T::RAW_PER_KB; ++h)
+          transform_store<T>(a_stage(s), h, tw, lane, crank, vals[h]);
         fence_proxy_async_smem();   // our rows -> visible to UMMA and to the copy engine
         __syncwarp();
         if (lane == 0) {
@@ -405,98 +437,58 @@ __global__ void __launch_bounds__(512, 1)
         wait_phase_cluster(bar(T::BAR_ST_EMPTY + x % T::NS), (x / T::NS) & 1, ctl, false);
     __syncwarp();
   } else if (warp >= 4 + T::XF_WARPS) {
-    // ---------------- epilogue warps
+    // ---------------- epilogue warps: lane = one output row of the tile
     const int q = warp & 3;                        // TMEM lane quadrant
-    const uint32_t buf0 = sbase + T::OFF_EPI + (uint32_t)(q * 2) * T::EPI_BUF_BYTES;
-    const uint32_t ebar0 = bar(T::BAR_EPI + q * 2);
     constexpr int NC = T::BN / kEpiCols;
-    int gc = 0;          // epilogue chunks started, across tiles (buffer = gc & 1)
-    int r_issued = 0;    // residual loads issued (lane 0's view), indexed like gc
-    int r_done = 0;
     bool ok = true;
     for (int i = 0; i < my_tiles && ok; ++i) {
       const int t = cid + i * ncl;
       const int ab = i & 1;
-      const int row0 = tile_m0(t) + q * kEpiRows;
+      const int row = tile_m0(t) + q * kEpiRows + lane;
       const int n0 = tile_n0(t);
-      const bool rows_in = row0 < args.M;
       int nc = n0 < args.N ? (args.N - n0 + kEpiCols - 1) / kEpiCols : 0;
       if (nc > NC) nc = NC;
-      if (!rows_in) nc = 0;
-      // Prefetch the residual of this tile's first chunk.
-      if (RESID && lane == 0 && nc > 0) {
-        bulk_wait_group_read<0>();
-        const uint32_t eb = ebar0 + 8u * (uint32_t)(gc & 1);
-        mbar_arrive_expect_tx(eb, T::EPI_BUF_BYTES);
-        tma_load_2d(buf0 + (gc & 1) * T::EPI_BUF_BYTES, &tm_r, n0, row0, eb);
-        r_issued = gc + 1;
-      }
-      __syncwarp();
       ok = warp_wait_phase(bar(T::BAR_ACC_FULL + ab), (i >> 1) & 1, ctl);
       tc_fence_after_sync();
       ok = ok && (__shfl_sync(0xffffffffu, *abort_flag, 0) == 0);
       if (!ok) break;
       const uint32_t acc = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * T::BN);
-      for (int c = 0; c < nc; ++c, ++gc) {
-        const int b = gc & 1;
-        const uint32_t buf = buf0 + b * T::EPI_BUF_BYTES;
-        if (lane == 0) {
-          // Both buffers' earlier stores must have read their source: this
-          // chunk writes buffer b, the prefetch below fills buffer b ^ 1.
-          bulk_wait_group_read<0>();
-          if (RESID && c + 1 < nc) {
-            const uint32_t nb = ebar0 + 8u * (uint32_t)(b ^ 1);
-            mbar_arrive_expect_tx(nb, T::EPI_BUF_BYTES);
-            tma_load_2d(buf0 + (b ^ 1) * T::EPI_BUF_BYTES, &tm_r, n0 + (c + 1) * kEpiCols, row0,
-                        nb);
-            r_issued = gc + 2;
-          }
+      const bool row_in = row < args.M;
+      float* yrow = args.Y + (size_t)(row_in ? row : 0) * (size_t)args.N;
+      const float* rrow = RESID ? args.R + (size_t)(row_in ? row : 0) * (size_t)args.N : nullptr;
+      for (int c = 0; c < nc; ++c) {
+        const int col0 = n0 + c * kEpiCols;
+        float4 rr[8];
+        if constexpr (RESID) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            rr[j] = (row_in && col0 + 4 * j < args.N)
+                        ? __ldg(reinterpret_cast<const float4*>(rrow + col0 + 4 * j))
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        __syncwarp();
         uint32_t v[32];
         tmem_ld_32x32b_x32(acc + (uint32_t)(c * kEpiCols), v);
         tmem_wait_ld();
-        if constexpr (RESID) {
-          if (!warp_wait_phase(ebar0 + 8u * (uint32_t)b, (gc >> 1) & 1, ctl)) {
-            ok = false;
-            break;
-          }
-          r_done = gc + 1;
-        }
+        if (row_in) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint32_t addr = buf + sw128(lane, j);
-          float o0 = __uint_as_float(v[4 * j + 0]);
-          float o1 = __uint_as_float(v[4 * j + 1]);
-          float o2 = __uint_as_float(v[4 * j + 2]);
-          float o3 = __uint_as_float(v[4 * j + 3]);
-          if constexpr (RESID) {
-            const float4 rr = ld_shared_v4f(addr);
-            o0 += rr.x;
-            o1 += rr.y;
-            o2 += rr.z;
-            o3 += rr.w;
+          for (int j = 0; j < 8; ++j) {
+            if (col0 + 4 * j >= args.N) break;
+            float4 o = make_float4(__uint_as_float(v[4 * j + 0]), __uint_as_float(v[4 * j + 1]),
+                                   __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+            if constexpr (RESID) {
+              o.x += rr[j].x;
+              o.y += rr[j].y;
+              o.z += rr[j].z;
+              o.w += rr[j].w;
+            }
+            *reinterpret_cast<float4*>(yrow + col0 + 4 * j) = o;
           }
-          st_shared_v4(addr, __float_as_uint(o0), __float_as_uint(o1), __float_as_uint(o2),
-                       __float_as_uint(o3));
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tma_store_2d(&tm_y, n0 + c * kEpiCols, row0, buf);
-          bulk_commit_group();
         }
       }
-      if (!ok) break;
       // TMEM reads of this buffer are complete: hand it back to the UMMA warp.
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(T::BAR_ACC_EMPTY + ab));
-    }
-    if (lane == 0) {
-      for (int x = r_done; x < r_issued; ++x)
-        wait_phase(ebar0 + 8u * (uint32_t)(x & 1), (x >> 1) & 1, ctl, false);
-      bulk_wait_group_all();
     }
     __syncwarp();
   }

@@ -30,6 +30,8 @@ struct KernelArgs {
   uint32_t flags;
   uint64_t timeout_ns;  // limit for any single wait inside the kernel
   int* status;          // device status word (first failure wins)
+  const float* R;       // residual [M, N] (kernels that read it directly)
+  float* Y;             // output [M, N] (kernels that write it directly)
 };
 
 // Tensor maps of one call. `a` is X (A_TMA_F32 / A_CVT_F16) or GATE, `u` is
