@@ -86,6 +86,17 @@ def recorded_traffic(workload: str):
     return None
 
 
+def kernel_label(w: wl.Workload) -> str:
+    """Name of the kernel the library dispatches for workload w (the
+    binary16 forms run the clustered kernel, cluster size 2 from N >= 512)."""
+    if w.form.endswith("_w16"):
+        cn = os.environ.get("LIN_F16_KERNEL") or ("2" if w.N >= 512 else "1")
+        if cn == "tile":
+            return "lin_gemm_kernel (per-tile, BN=128)"
+        return f"lin_gemm_cluster_kernel (BN=256, cluster {cn} along N)"
+    return "lin_gemm_kernel (per-tile, BN=128, TF32)"
+
+
 def mma_dtype(form: str) -> str:
     return "f16" if form.endswith("_w16") else "tf32"
 
@@ -420,7 +431,7 @@ def run_ours(args, rank: int, world: int):
                 "frac": kernel_tflops / roof, "traffic": traffic,
                 "peak_source": f"{peak_src} bf16 {'x nominal f16/bf16 ratio 1.0' if mma_dtype(w.form) == 'f16' else 'x nominal tf32/bf16 ratio 0.489'} (burst)",
                 "peak_sustained": roofline(w, peaks, sustained=True)[1],
-                "kernel": "lin_gemm_kernel<A_SWIGLU_F16,resid,128>",
+                "kernel": kernel_label(w),
                 "algorithmic_bytes": wl.input_bytes(w.form, w.M, w.N, w.K),
                 "algorithmic_flops": w.flops}
 
