@@ -37,6 +37,10 @@
 
 #include "lin_common.cuh"
 
+#ifndef LIN_XF_WARPS
+#define LIN_XF_WARPS 8
+#endif
+
 namespace lin {
 
 template <int AMODE, bool RESID, int BN_, int CN_>
@@ -52,7 +56,7 @@ struct ClusterTraits {
   static constexpr int W_ATOM = 64;
   static constexpr int W_BOXES = BN / W_ATOM;
   static constexpr int ROWS = BM / CN;            // A rows this CTA transforms
-  static constexpr int XF_WARPS = 8;
+  static constexpr int XF_WARPS = LIN_XF_WARPS;
   static constexpr int RW = ROWS / XF_WARPS;      // A rows per transform warp
   static constexpr uint32_t SLICE_BYTES = RW * 128;             // one warp's rows of a stage
   static constexpr uint32_t REMOTE_BYTES_PER_WARP = SLICE_BYTES * (CN - 1);
@@ -62,17 +66,22 @@ struct ClusterTraits {
   static constexpr uint32_t B_BYTES = W_BOXES * B_ATOM_BYTES;
   static constexpr uint32_t OP_STAGE_BYTES = A_BYTES + B_BYTES;
 
+  // One input stage per k-block: [input][half][ROWS rows][32 f32], loaded as
+  // 2 (X) or 4 (GATE, UP) TMA boxes behind a single barrier. Few large
+  // stages matter: each stage costs the issuing thread a barrier wait and
+  // the first box's issue latency, whatever its size.
   static constexpr int RAW_INPUTS = kSwiglu ? 2 : 1;
   static constexpr uint32_t RAW_BOX_BYTES = ROWS * 128;        // [ROWS][32 f32]
-  static constexpr uint32_t RAW_STAGE_BYTES = RAW_INPUTS * RAW_BOX_BYTES;
-  static constexpr int RAW_PER_KB = 2;
+  static constexpr int RAW_BOXES = RAW_INPUTS * 2;              // two 32-column halves
+  static constexpr uint32_t RAW_STAGE_BYTES = RAW_BOXES * RAW_BOX_BYTES;
+
   static constexpr uint32_t SMEM_CAP = 232448;
   static constexpr uint32_t BAR_REGION = 1024;
   static constexpr uint32_t ALIGN_SLACK = 1024;
   static constexpr uint32_t DATA_CAP = SMEM_CAP - BAR_REGION - ALIGN_SLACK;
-  // Three operand stages; the rest of shared memory goes to the input ring,
-  // whose depth is what hides the latency of the f32 GATE/UP (or X) loads.
-  static constexpr int NS = 3;
+  // Three operand stages when two input stages still fit, else two; the rest
+  // of shared memory goes to the input ring.
+  static constexpr int NS = (DATA_CAP - 3 * OP_STAGE_BYTES) / RAW_STAGE_BYTES >= 2 ? 3 : 2;
   static constexpr int NR_FIT = (int)((DATA_CAP - NS * OP_STAGE_BYTES) / RAW_STAGE_BYTES);
   static constexpr int NR = NR_FIT > 8 ? 8 : NR_FIT;
 
@@ -95,11 +104,12 @@ struct ClusterTraits {
   static constexpr uint32_t TMEM_COLS = 2 * BN;
   static constexpr uint32_t IDESC = umma_idesc(0u, false, true, BM, BN);
   static constexpr uint16_t CLUSTER_MASK = (uint16_t)((1u << CN) - 1u);
-  static constexpr int kThreadsC = 512;
+  static constexpr int kThreadsC = (8 + XF_WARPS) * 32;
 
   static_assert(CN == 1 || CN == 2 || CN == 4 || CN == 8, "cluster size");
   static_assert(ROWS % 8 == 0, "row share must hold whole swizzle atoms");
   static_assert(RW == 4 || RW % 8 == 0, "rows per transform warp");
+  static_assert(XF_WARPS == 4 || XF_WARPS == 8, "transform warps");
   static_assert(NS >= 2 && NS <= 8 && NR >= 2 && NR <= 8, "ring depths");
   static_assert(OFF_ABORT + 4 <= BAR_REGION, "barrier region");
   static_assert(SMEM_BYTES <= SMEM_CAP, "shared memory");
@@ -132,9 +142,8 @@ struct SliceMap {
 };
 
 template <typename T>
-__device__ __forceinline__ void transform_compute(uint32_t raw, int tw, int lane,
+__device__ __forceinline__ void transform_compute(uint32_t g_box, uint32_t u_box, int tw, int lane,
                                                   uint32_t (&out)[SliceMap<T>::PER_LANE][4]) {
-  constexpr uint32_t BOX = T::RAW_BOX_BYTES;
 #pragma unroll
   for (int j = 0; j < SliceMap<T>::PER_LANE; ++j) {
     const int idx = lane + 32 * j;
@@ -144,11 +153,11 @@ __device__ __forceinline__ void transform_compute(uint32_t raw, int tw, int lane
     const uint32_t rs = (uint32_t)(tw * T::RW) + row;
     const uint32_t o0 = sw128(rs, 2 * cc);
     const uint32_t o1 = sw128(rs, 2 * cc + 1);
-    float4 a0 = ld_shared_v4f(raw + o0);
-    float4 a1 = ld_shared_v4f(raw + o1);
+    float4 a0 = ld_shared_v4f(g_box + o0);
+    float4 a1 = ld_shared_v4f(g_box + o1);
     if constexpr (T::kSwiglu) {
-      const float4 u0 = ld_shared_v4f(raw + BOX + o0);
-      const float4 u1 = ld_shared_v4f(raw + BOX + o1);
+      const float4 u0 = ld_shared_v4f(u_box + o0);
+      const float4 u1 = ld_shared_v4f(u_box + o1);
       a0.x = silu_stable_fast(a0.x) * u0.x;
       a0.y = silu_stable_fast(a0.y) * u0.y;
       a0.z = silu_stable_fast(a0.z) * u0.z;
@@ -181,7 +190,7 @@ __device__ __forceinline__ void transform_store(uint32_t a_stage, int half, int 
 }
 
 template <int AMODE, bool RESID, int BN, int CN>
-__global__ void __launch_bounds__(512, 1)
+__global__ void __launch_bounds__((8 + LIN_XF_WARPS) * 32, 1)
     lin_gemm_cluster_kernel(const __grid_constant__ CUtensorMap tm_a,
                             const __grid_constant__ CUtensorMap tm_u,
                             const __grid_constant__ CUtensorMap tm_w,
@@ -348,12 +357,12 @@ __global__ void __launch_bounds__(512, 1)
     __syncwarp();
   } else if (warp == 3) {
     // ---------------- raw producer: this CTA's rows of GATE/UP (or X)
-    int tr = 0;   // raw stages issued, across tiles
+    int tr = 0;   // input stages (k-blocks) issued, across tiles
     bool ok = true;
     for (int i = 0; i < my_tiles && ok; ++i) {
       const int t = cid + i * ncl;
       const int row = tile_m0(t) + (int)crank * T::ROWS;
-      for (int h = 0; h < nkb * T::RAW_PER_KB; ++h, ++tr) {
+      for (int kb = 0; kb < nkb; ++kb, ++tr) {
         const int r = tr % T::NR;
         if (tr >= T::NR &&
             !lane0_wait_phase(bar(T::BAR_RAW_EMPTY + r), ((tr / T::NR) - 1) & 1, ctl, lane)) {
@@ -363,9 +372,13 @@ __global__ void __launch_bounds__(512, 1)
         if (lane == 0) {
           const uint32_t full = bar(T::BAR_RAW_FULL + r);
           mbar_arrive_expect_tx(full, T::RAW_STAGE_BYTES);
-          tma_load_2d(raw_stage(r), &tm_a, h * 32, row, full);
-          if constexpr (T::kSwiglu)
-            tma_load_2d(raw_stage(r) + T::RAW_BOX_BYTES, &tm_u, h * 32, row, full);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            tma_load_2d(raw_stage(r) + h * T::RAW_BOX_BYTES, &tm_a, kb * T::BK + h * 32, row, full);
+            if constexpr (T::kSwiglu)
+              tma_load_2d(raw_stage(r) + (2 + h) * T::RAW_BOX_BYTES, &tm_u, kb * T::BK + h * 32, row,
+                          full);
+          }
         }
         __syncwarp();
       }
@@ -384,20 +397,22 @@ __global__ void __launch_bounds__(512, 1)
       for (int kb = 0; kb < nkb; ++kb, ++g) {
         const int s = g % T::NS;
         // Arithmetic first (registers); then wait for the stage to be free.
-        uint32_t vals[T::RAW_PER_KB][SliceMap<T>::PER_LANE][4];
-#pragma unroll
-        for (int h = 0; h < T::RAW_PER_KB; ++h) {
-          const int r = (tr + h) % T::NR;
-          if (!warp_wait_phase(bar(T::BAR_RAW_FULL + r), ((tr + h) / T::NR) & 1, ctl)) {
+        uint32_t vals[2][SliceMap<T>::PER_LANE][4];
+        {
+          const int r = tr % T::NR;
+          if (!warp_wait_phase(bar(T::BAR_RAW_FULL + r), (tr / T::NR) & 1, ctl)) {
             ok = false;
             break;
           }
-          transform_compute<T>(raw_stage(r), tw, lane, vals[h]);
+          const uint32_t rs = raw_stage(r);
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            transform_compute<T>(rs + h * T::RAW_BOX_BYTES, rs + (2 + h) * T::RAW_BOX_BYTES, tw, lane,
+                                 vals[h]);
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(T::BAR_RAW_EMPTY + r));
+          ++tr;
         }
-        tr += T::RAW_PER_KB;
-        if (!ok) break;
         if (g >= T::NS) {
           // Every CTA's UMMA is done with this stage: ours may be rewritten
           // and the peers' copies of it overwritten.
@@ -408,7 +423,7 @@ __global__ void __launch_bounds__(512, 1)
           }
         }
 #pragma unroll
-        for (int h = 0; h < T::RAW_PER_KB; ++h)
+        for (int h = 0; h < 2; ++h)
           transform_store<T>(a_stage(s), h, tw, lane, crank, vals[h]);
         fence_proxy_async_smem();   // our rows -> visible to UMMA and to the copy engine
         __syncwarp();
