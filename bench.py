@@ -88,9 +88,10 @@ def recorded_traffic(workload: str):
 
 def kernel_label(w: wl.Workload) -> str:
     """Name of the kernel the library dispatches for workload w (the
-    binary16 forms run the clustered kernel, cluster size 2 from N >= 512)."""
+    binary16 forms run the clustered kernel: clusters of 4 from N >= 1024,
+    pairs from N >= 512, else single CTAs)."""
     if w.form.endswith("_w16"):
-        cn = os.environ.get("LIN_F16_KERNEL") or ("2" if w.N >= 512 else "1")
+        cn = os.environ.get("LIN_F16_KERNEL") or ("4" if w.N >= 1024 else "2" if w.N >= 512 else "1")
         if cn == "tile":
             return "lin_gemm_kernel (per-tile, BN=128)"
         return f"lin_gemm_cluster_kernel (BN=256, cluster {cn} along N)"

@@ -166,10 +166,12 @@ int f16_cluster_size(uint64_t N) {
     return (c == 1 || c == 2 || c == 4) ? c : -1;
   }();
   if (forced >= 0) return forced;
-  // Pairs use all 152 SMs (clusters of 4 leave 8 idle) and measured fastest
-  // on the 16k-token SwiGLU down projection (2 > 4 > 1).
+  // Clusters of 4 leave 8 of 152 SMs idle but transform each A row half as
+  // often as pairs; with the transform warps taking turns by k-block they
+  // measured fastest on the 16k-token SwiGLU down projection (4 > 2 > 1) and
+  // level with the others on the 512-token vocabulary projection.
   const uint64_t per = (uint64_t)lin::kClusterBN;
-  return N >= 2 * per ? 2 : 1;
+  return N >= 4 * per ? 4 : (N >= 2 * per ? 2 : 1);
 }
 
 enum Form : int { F_MATMUL = 0, F_RESID = 1, F_SWIGLU = 2 };
@@ -268,7 +270,7 @@ lin_status run(const Problem& p, cudaStream_t stream) {
   ok &= encode_2d(&maps.y, f32, p.Y, N, M, N * 4, lin::kEpiCols, lin::kEpiRows);
   if (!ok) return cuda_fail(cudaErrorInvalidValue);
 
-  lin::KernelArgs args;
+  lin::KernelArgs args{};
   args.M = static_cast<int32_t>(M);
   args.N = static_cast<int32_t>(N);
   args.K = static_cast<int32_t>(K);
@@ -381,7 +383,7 @@ lin_status lin_selftest_wait_timeout(int64_t timeout_us, lin_stream_t stream) {
   // The producers issue nothing, so the tensor maps are never dereferenced.
   lin::TensorMaps maps;
   std::memset(&maps, 0, sizeof(maps));
-  lin::KernelArgs args;
+  lin::KernelArgs args{};
   args.M = 128;
   args.N = 128;
   args.K = 128;

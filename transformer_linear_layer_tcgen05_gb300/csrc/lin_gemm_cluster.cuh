@@ -40,6 +40,9 @@
 #ifndef LIN_XF_WARPS
 #define LIN_XF_WARPS 8
 #endif
+#ifndef LIN_XF_GROUPS
+#define LIN_XF_GROUPS 2
+#endif
 
 namespace lin {
 
@@ -57,7 +60,12 @@ struct ClusterTraits {
   static constexpr int W_BOXES = BN / W_ATOM;
   static constexpr int ROWS = BM / CN;            // A rows this CTA transforms
   static constexpr int XF_WARPS = LIN_XF_WARPS;
-  static constexpr int RW = ROWS / XF_WARPS;      // A rows per transform warp
+  // The transform warps form XF_GROUPS groups that take turns by k-block, so
+  // each warp's fixed cost per k-block (two barrier waits, a proxy fence, the
+  // copy issue) is spread over XF_GROUPS k-blocks of UMMA time.
+  static constexpr int XF_GROUPS = LIN_XF_GROUPS;
+  static constexpr int XF_PER_GROUP = XF_WARPS / XF_GROUPS;
+  static constexpr int RW = ROWS / XF_PER_GROUP;  // A rows per transform warp
   static constexpr uint32_t SLICE_BYTES = RW * 128;             // one warp's rows of a stage
   static constexpr uint32_t REMOTE_BYTES_PER_WARP = SLICE_BYTES * (CN - 1);
 
@@ -83,16 +91,25 @@ struct ClusterTraits {
   // of shared memory goes to the input ring.
   static constexpr int NS = (DATA_CAP - 3 * OP_STAGE_BYTES) / RAW_STAGE_BYTES >= 2 ? 3 : 2;
   static constexpr int NR_FIT = (int)((DATA_CAP - NS * OP_STAGE_BYTES) / RAW_STAGE_BYTES);
-  static constexpr int NR = NR_FIT > 8 ? 8 : NR_FIT;
+  // A parity wait is only sound for a waiter at most one phase ahead. A group
+  // reaching use u of a ring slot must therefore already have seen use u-1
+  // complete: true for the input ring when NR is a multiple of XF_GROUPS (the
+  // slot's previous use was the same group's), and for the operand ring's
+  // empty barriers when XF_GROUPS <= NS (the group's previous k-block waited
+  // for a later UMMA than the slot's use before last).
+  static constexpr int NR_CAP = NR_FIT > 8 ? 8 : NR_FIT;
+  static constexpr int NR = NR_CAP - NR_CAP % XF_GROUPS;
 
   static constexpr uint32_t OFF_OP = 0;
   static constexpr uint32_t OFF_RAW = NS * OP_STAGE_BYTES;
   static constexpr uint32_t OFF_BAR = OFF_RAW + NR * RAW_STAGE_BYTES;
   static constexpr uint32_t SMEM_BYTES = ALIGN_SLACK + OFF_BAR + BAR_REGION;
 
-  static constexpr int BAR_B_FULL = 0;                   // W tile landed (local TMA)
-  static constexpr int BAR_A_FULL = BAR_B_FULL + 8;      // A rows from every CTA landed
-  static constexpr int BAR_ST_EMPTY = BAR_A_FULL + 8;    // every CTA's UMMA done with stage
+  // One full barrier per operand stage: the W tile's TMA bytes, the local
+  // transform warps' arrivals and the peers' copied A rows all land on it, so
+  // the UMMA warp waits once per k-block.
+  static constexpr int BAR_FULL = 0;
+  static constexpr int BAR_ST_EMPTY = BAR_FULL + 8;      // every CTA's UMMA done with stage
   static constexpr int BAR_RAW_FULL = BAR_ST_EMPTY + 8;
   static constexpr int BAR_RAW_EMPTY = BAR_RAW_FULL + 8;
   static constexpr int BAR_ACC_FULL = BAR_RAW_EMPTY + 8; // 2 accumulator buffers
@@ -110,6 +127,9 @@ struct ClusterTraits {
   static_assert(ROWS % 8 == 0, "row share must hold whole swizzle atoms");
   static_assert(RW == 4 || RW % 8 == 0, "rows per transform warp");
   static_assert(XF_WARPS == 4 || XF_WARPS == 8, "transform warps");
+  static_assert(XF_GROUPS >= 1 && XF_WARPS % XF_GROUPS == 0 && ROWS % XF_PER_GROUP == 0,
+                "transform groups");
+  static_assert(NR % XF_GROUPS == 0 && XF_GROUPS <= NS, "ring depths vs transform groups");
   static_assert(NS >= 2 && NS <= 8 && NR >= 2 && NR <= 8, "ring depths");
   static_assert(OFF_ABORT + 4 <= BAR_REGION, "barrier region");
   static_assert(SMEM_BYTES <= SMEM_CAP, "shared memory");
@@ -119,7 +139,7 @@ struct ClusterTraits {
   static_assert(TMEM_COLS < 512 || 2 * SMEM_BYTES > SMEM_CAP + BAR_REGION, "one CTA per SM");
 };
 
-// Transform warp `tw` (0..7): its RW rows of one raw stage (32 f32 columns:
+// Transform warp `tw` (its index within its group): its RW rows of one raw stage (32 f32 columns:
 // half `half` of a 64-wide k-block) -> binary16 A rows. Eight consecutive
 // lanes take eight different rows of one 16-byte column, so the 128-byte
 // swizzle keeps loads and stores free of bank conflicts. The work is split
@@ -228,13 +248,12 @@ __global__ void __launch_bounds__((8 + LIN_XF_WARPS) * 32, 1)
   // ---- set-up
   if (threadIdx.x == 0) {
     for (int s = 0; s < T::NS; ++s) {
-      mbar_init(bar(T::BAR_B_FULL + s), 1);
-      mbar_init(bar(T::BAR_A_FULL + s), T::XF_WARPS);   // local warps (+ peers' copy bytes)
+      mbar_init(bar(T::BAR_FULL + s), T::XF_PER_GROUP + 1);   // W producer + one transform group
       mbar_init(bar(T::BAR_ST_EMPTY + s), CN);     // every CTA's UMMA commit
     }
     for (int r = 0; r < T::NR; ++r) {
       mbar_init(bar(T::BAR_RAW_FULL + r), 1);
-      mbar_init(bar(T::BAR_RAW_EMPTY + r), T::XF_WARPS);
+      mbar_init(bar(T::BAR_RAW_EMPTY + r), T::XF_PER_GROUP);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(T::BAR_ACC_FULL + b), 1);
@@ -283,7 +302,7 @@ __global__ void __launch_bounds__((8 + LIN_XF_WARPS) * 32, 1)
           }
         }
         if (lane == 0) {
-          const uint32_t full = bar(T::BAR_B_FULL + s);
+          const uint32_t full = bar(T::BAR_FULL + s);
           mbar_arrive_expect_tx(full, T::B_BYTES);
 #pragma unroll
           for (int j = 0; j < T::W_BOXES; ++j)
@@ -295,7 +314,7 @@ __global__ void __launch_bounds__((8 + LIN_XF_WARPS) * 32, 1)
     }
     if (lane == 0)
       for (int x = (g > T::NS ? g - T::NS : 0); x < g; ++x)
-        wait_phase(bar(T::BAR_B_FULL + x % T::NS), (x / T::NS) & 1, ctl, false);
+        wait_phase(bar(T::BAR_FULL + x % T::NS), (x / T::NS) & 1, ctl, false);
     __syncwarp();
   } else if (warp == 1) {
     // ---------------- UMMA issuer
@@ -314,8 +333,7 @@ __global__ void __launch_bounds__((8 + LIN_XF_WARPS) * 32, 1)
         const uint32_t ph = (g / T::NS) & 1;
         bool w = true;
         if (lane == 0) {
-          w = wait_phase(bar(T::BAR_B_FULL + s), ph, ctl) &&
-              wait_phase(bar(T::BAR_A_FULL + s), ph, ctl);
+          w = wait_phase(bar(T::BAR_FULL + s), ph, ctl);
         }
         if (!__shfl_sync(0xffffffffu, w ? 1 : 0, 0)) {
           ok = false;
@@ -389,18 +407,20 @@ __global__ void __launch_bounds__((8 + LIN_XF_WARPS) * 32, 1)
     __syncwarp();
   } else if (warp >= 4 && warp < 4 + T::XF_WARPS) {
     // ---------------- transform warps
-    const int tw = warp - 4;
+    const int grp = (warp - 4) / T::XF_PER_GROUP;
+    const int tw = (warp - 4) % T::XF_PER_GROUP;
     const uint32_t slice_off = (crank * (uint32_t)T::ROWS + (uint32_t)(tw * T::RW)) * 128u;
-    int g = 0, tr = 0;
+    int g = 0;   // k-blocks across tiles (operand and input stages alike)
     bool ok = true;
     for (int i = 0; i < my_tiles && ok; ++i) {
       for (int kb = 0; kb < nkb; ++kb, ++g) {
+        if (g % T::XF_GROUPS != grp) continue;
         const int s = g % T::NS;
         // Arithmetic first (registers); then wait for the stage to be free.
         uint32_t vals[2][SliceMap<T>::PER_LANE][4];
         {
-          const int r = tr % T::NR;
-          if (!warp_wait_phase(bar(T::BAR_RAW_FULL + r), (tr / T::NR) & 1, ctl)) {
+          const int r = g % T::NR;
+          if (!warp_wait_phase(bar(T::BAR_RAW_FULL + r), (g / T::NR) & 1, ctl)) {
             ok = false;
             break;
           }
@@ -411,7 +431,6 @@ __global__ void __launch_bounds__((8 + LIN_XF_WARPS) * 32, 1)
                                  vals[h]);
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(T::BAR_RAW_EMPTY + r));
-          ++tr;
         }
         if (g >= T::NS) {
           // Every CTA's UMMA is done with this stage: ours may be rewritten
@@ -428,7 +447,7 @@ __global__ void __launch_bounds__((8 + LIN_XF_WARPS) * 32, 1)
         fence_proxy_async_smem();   // our rows -> visible to UMMA and to the copy engine
         __syncwarp();
         if (lane == 0) {
-          const uint32_t full = bar(T::BAR_A_FULL + s);
+          const uint32_t full = bar(T::BAR_FULL + s);
           if constexpr (CN > 1) {
             // The peers' slices of this stage arrive as copy bytes on our barrier.
             mbar_arrive_expect_tx(full, T::REMOTE_BYTES_PER_WARP);
