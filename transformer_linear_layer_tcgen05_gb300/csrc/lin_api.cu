@@ -259,9 +259,10 @@ lin_status run(const Problem& p, cudaStream_t stream) {
   const CUtensorMapDataType f32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   bool ok = true;
   const float* a_src = swiglu ? p.G : p.X;
-  const uint32_t a_rows = cn > 0 ? (uint32_t)(lin::kBM / cn) : (uint32_t)lin::kBM;
-  ok &= encode_2d(&maps.a, f32, a_src, K, M, K * 4, 32, a_rows);
-  if (swiglu) ok &= encode_2d(&maps.u, f32, p.U, K, M, K * 4, 32, a_rows);
+  if (cn == 0) {   // the clustered kernels load X / GATE / UP without tensor maps
+    ok &= encode_2d(&maps.a, f32, a_src, K, M, K * 4, 32, lin::kBM);
+    if (swiglu) ok &= encode_2d(&maps.u, f32, p.U, K, M, K * 4, 32, lin::kBM);
+  }
   if (p.w16)
     ok &= encode_2d(&maps.w, CU_TENSOR_MAP_DATA_TYPE_UINT16, p.W, N, K, N * 2, 64, 64);
   else
@@ -277,6 +278,8 @@ lin_status run(const Problem& p, cudaStream_t stream) {
   args.flags = 0;
   args.timeout_ns = kDefaultTimeoutNs;
   args.status = status_word;
+  args.A = a_src;
+  args.U = swiglu ? p.U : nullptr;
   args.R = resid ? p.R : nullptr;
   args.Y = p.Y;
 

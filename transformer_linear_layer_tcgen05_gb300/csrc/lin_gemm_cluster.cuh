@@ -21,16 +21,21 @@
 //   warp 0      TMA producer of the binary16 W tiles (MN-major B operand)
 //   warp 1      UMMA issuer; its per-stage commit is multicast to the whole
 //               cluster (a stage may be refilled once every CTA read it)
-//   warp 2      TMEM allocator
-//   warp 3      TMA producer of this CTA's rows of GATE/UP (or X)
-//   warps 4-11  transform: each warp turns its slice of this CTA's rows into
-//               binary16 A rows (silu(GATE)*UP, or X), writes them into the
-//               local A stage and bulk-copies them (TMA engine, shared to
-//               shared) into the same stage of every other CTA of the
-//               cluster; the copies complete on the receiver's full barrier
+//   warp 2      TMEM allocator (warps 2 and 3 are otherwise idle)
+//   warps 4-11  transform, two groups of four taking turns by k-block: each
+//               warp loads its rows of GATE/UP (or X) with coalesced 16-byte
+//               global loads into registers, several of its k-blocks ahead,
+//               turns them into binary16 A rows (silu(GATE)*UP, or X),
+//               writes them into the local A stage and bulk-copies them (TMA
+//               engine, shared to shared) into the same stage of every other
+//               CTA of the cluster; the copies complete on the receiver's
+//               full barrier
 //   warps 12-15 epilogue: TMEM -> registers, + R, Y; each thread owns one
-//               output row and moves it with 16-byte global loads/stores,
-//               which keeps shared memory free for a deeper input ring
+//               output row and moves it with 16-byte global loads/stores
+// The f32 inputs are staged in registers rather than shared memory: the
+// register file is as large as shared memory, and shared memory is then left
+// whole to the operand ring, whose depth has to cover the round trip of a
+// stage (W load or peer copies, UMMA, commit to every CTA).
 #pragma once
 
 #include <atomic>
@@ -39,9 +44,6 @@
 
 #ifndef LIN_XF_WARPS
 #define LIN_XF_WARPS 8
-#endif
-#ifndef LIN_XF_GROUPS
-#define LIN_XF_GROUPS 2
 #endif
 
 namespace lin {
@@ -59,50 +61,40 @@ struct ClusterTraits {
   static constexpr int W_ATOM = 64;
   static constexpr int W_BOXES = BN / W_ATOM;
   static constexpr int ROWS = BM / CN;            // A rows this CTA transforms
+  static constexpr int INPUTS = kSwiglu ? 2 : 1;  // GATE and UP, or X
   static constexpr int XF_WARPS = LIN_XF_WARPS;
   // The transform warps form XF_GROUPS groups that take turns by k-block, so
-  // each warp's fixed cost per k-block (two barrier waits, a proxy fence, the
-  // copy issue) is spread over XF_GROUPS k-blocks of UMMA time.
-  static constexpr int XF_GROUPS = LIN_XF_GROUPS;
+  // each warp's fixed cost per k-block (a barrier wait, a proxy fence, the
+  // copy issue) is spread over XF_GROUPS k-blocks of UMMA time. A single CTA
+  // transforming all 128 rows of the SwiGLU form keeps one group, so that a
+  // warp's share of a k-block still fits its registers.
+  static constexpr int XF_GROUPS = (kSwiglu && CN == 1) ? 1 : 2;
   static constexpr int XF_PER_GROUP = XF_WARPS / XF_GROUPS;
-  static constexpr int RW = ROWS / XF_PER_GROUP;  // A rows per transform warp
+  static constexpr int RW = ROWS / XF_PER_GROUP;  // A rows per transform warp (contiguous)
   static constexpr uint32_t SLICE_BYTES = RW * 128;             // one warp's rows of a stage
   static constexpr uint32_t REMOTE_BYTES_PER_WARP = SLICE_BYTES * (CN - 1);
+  // A warp's 16-byte loads cover two rows of a 64-wide k-block at a time
+  // (lanes 0-15 one row, 16-31 the next): LPI loads per input and lane.
+  static constexpr int LPI = RW / 2;
+  static constexpr int LOADS = INPUTS * LPI;      // float4 registers per lane per k-block
+  // Register prefetch depth, in the group's own k-blocks: as many as fit in
+  // 64 registers of staged input per lane.
+  static constexpr int PF = LOADS >= 16 ? 1 : (LOADS >= 8 ? 2 : 4);
 
   static constexpr uint32_t A_BYTES = BM * 128;
   static constexpr uint32_t B_ATOM_BYTES = BK * 128;
   static constexpr uint32_t B_BYTES = W_BOXES * B_ATOM_BYTES;
   static constexpr uint32_t OP_STAGE_BYTES = A_BYTES + B_BYTES;
 
-  // One input stage per k-block: [input][half][ROWS rows][32 f32], loaded as
-  // 2 (X) or 4 (GATE, UP) TMA boxes behind a single barrier. Few large
-  // stages matter: each stage costs the issuing thread a barrier wait and
-  // the first box's issue latency, whatever its size.
-  static constexpr int RAW_INPUTS = kSwiglu ? 2 : 1;
-  static constexpr uint32_t RAW_BOX_BYTES = ROWS * 128;        // [ROWS][32 f32]
-  static constexpr int RAW_BOXES = RAW_INPUTS * 2;              // two 32-column halves
-  static constexpr uint32_t RAW_STAGE_BYTES = RAW_BOXES * RAW_BOX_BYTES;
-
   static constexpr uint32_t SMEM_CAP = 232448;
   static constexpr uint32_t BAR_REGION = 1024;
   static constexpr uint32_t ALIGN_SLACK = 1024;
   static constexpr uint32_t DATA_CAP = SMEM_CAP - BAR_REGION - ALIGN_SLACK;
-  // Three operand stages when two input stages still fit, else two; the rest
-  // of shared memory goes to the input ring.
-  static constexpr int NS = (DATA_CAP - 3 * OP_STAGE_BYTES) / RAW_STAGE_BYTES >= 2 ? 3 : 2;
-  static constexpr int NR_FIT = (int)((DATA_CAP - NS * OP_STAGE_BYTES) / RAW_STAGE_BYTES);
-  // A parity wait is only sound for a waiter at most one phase ahead. A group
-  // reaching use u of a ring slot must therefore already have seen use u-1
-  // complete: true for the input ring when NR is a multiple of XF_GROUPS (the
-  // slot's previous use was the same group's), and for the operand ring's
-  // empty barriers when XF_GROUPS <= NS (the group's previous k-block waited
-  // for a later UMMA than the slot's use before last).
-  static constexpr int NR_CAP = NR_FIT > 8 ? 8 : NR_FIT;
-  static constexpr int NR = NR_CAP - NR_CAP % XF_GROUPS;
+  static constexpr int NS_FIT = (int)(DATA_CAP / OP_STAGE_BYTES);
+  static constexpr int NS = NS_FIT > 8 ? 8 : NS_FIT;
 
   static constexpr uint32_t OFF_OP = 0;
-  static constexpr uint32_t OFF_RAW = NS * OP_STAGE_BYTES;
-  static constexpr uint32_t OFF_BAR = OFF_RAW + NR * RAW_STAGE_BYTES;
+  static constexpr uint32_t OFF_BAR = NS * OP_STAGE_BYTES;
   static constexpr uint32_t SMEM_BYTES = ALIGN_SLACK + OFF_BAR + BAR_REGION;
 
   // One full barrier per operand stage: the W tile's TMA bytes, the local
@@ -110,9 +102,7 @@ struct ClusterTraits {
   // the UMMA warp waits once per k-block.
   static constexpr int BAR_FULL = 0;
   static constexpr int BAR_ST_EMPTY = BAR_FULL + 8;      // every CTA's UMMA done with stage
-  static constexpr int BAR_RAW_FULL = BAR_ST_EMPTY + 8;
-  static constexpr int BAR_RAW_EMPTY = BAR_RAW_FULL + 8;
-  static constexpr int BAR_ACC_FULL = BAR_RAW_EMPTY + 8; // 2 accumulator buffers
+  static constexpr int BAR_ACC_FULL = BAR_ST_EMPTY + 8;  // 2 accumulator buffers
   static constexpr int BAR_ACC_EMPTY = BAR_ACC_FULL + 2;
   static constexpr int BAR_COUNT = BAR_ACC_EMPTY + 2;
   static constexpr uint32_t OFF_TMEM_SLOT = BAR_COUNT * 8;
@@ -124,13 +114,16 @@ struct ClusterTraits {
   static constexpr int kThreadsC = (8 + XF_WARPS) * 32;
 
   static_assert(CN == 1 || CN == 2 || CN == 4 || CN == 8, "cluster size");
-  static_assert(ROWS % 8 == 0, "row share must hold whole swizzle atoms");
-  static_assert(RW == 4 || RW % 8 == 0, "rows per transform warp");
   static_assert(XF_WARPS == 4 || XF_WARPS == 8, "transform warps");
-  static_assert(XF_GROUPS >= 1 && XF_WARPS % XF_GROUPS == 0 && ROWS % XF_PER_GROUP == 0,
+  static_assert(XF_WARPS % XF_GROUPS == 0 && ROWS % XF_PER_GROUP == 0 && RW % 2 == 0,
                 "transform groups");
-  static_assert(NR % XF_GROUPS == 0 && XF_GROUPS <= NS, "ring depths vs transform groups");
-  static_assert(NS >= 2 && NS <= 8 && NR >= 2 && NR <= 8, "ring depths");
+  static_assert(LOADS <= 16, "staged input per lane");
+  // A parity wait is only sound for a waiter at most one phase ahead: a group
+  // reaching use u of an operand stage must already have seen use u-1's
+  // UMMA complete, true when its previous k-block (XF_GROUPS earlier) waited
+  // for a UMMA no older than the stage's use before last.
+  static_assert(XF_GROUPS <= NS, "ring depth vs transform groups");
+  static_assert(NS >= 2 && NS <= 8, "ring depth");
   static_assert(OFF_ABORT + 4 <= BAR_REGION, "barrier region");
   static_assert(SMEM_BYTES <= SMEM_CAP, "shared memory");
   static_assert(TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM columns");
@@ -139,83 +132,68 @@ struct ClusterTraits {
   static_assert(TMEM_COLS < 512 || 2 * SMEM_BYTES > SMEM_CAP + BAR_REGION, "one CTA per SM");
 };
 
-// Transform warp `tw` (its index within its group): its RW rows of one raw stage (32 f32 columns:
-// half `half` of a 64-wide k-block) -> binary16 A rows. Eight consecutive
-// lanes take eight different rows of one 16-byte column, so the 128-byte
-// swizzle keeps loads and stores free of bank conflicts. The work is split
-// into a compute step (results kept in registers, four words per 16-byte
-// chunk) and a store step, so a warp does the arithmetic of a k-block before
-// the stage it writes has been released.
+// Register-staged inputs of one k-block for one transform lane: load q of
+// input i is row (tw*RW + 2q + lane/16) of this CTA's slice, columns
+// k0 + 4*(lane%16) .. +3. Rows at or past M and columns at or past K read as
+// zero (K is a multiple of 4, so a 16-byte load is wholly in or out).
 template <typename T>
-struct SliceMap {
-  static constexpr int ITEMS = T::RW * 4;                 // 16-byte chunks per half
-  static constexpr int PER_LANE = (ITEMS + 31) / 32;
-  __device__ static __forceinline__ void item(int idx, uint32_t& row, uint32_t& cc) {
-    if constexpr (T::RW == 4) {
-      row = (uint32_t)(idx & 3);
-      cc = (uint32_t)(idx >> 2);
-    } else {
-      row = (uint32_t)((idx & 7) + 8 * (idx >> 5));
-      cc = (uint32_t)((idx >> 3) & 3);
-    }
-  }
+struct Staged {
+  float4 v[T::INPUTS][T::LPI];
 };
 
 template <typename T>
-__device__ __forceinline__ void transform_compute(uint32_t g_box, uint32_t u_box, int tw, int lane,
-                                                  uint32_t (&out)[SliceMap<T>::PER_LANE][4]) {
+__device__ __forceinline__ void stage_load(Staged<T>& st, const float* __restrict__ a,
+                                           const float* __restrict__ u, int row0, int k0,
+                                           int M, int K, int tw, int lane) {
+  const int col = k0 + 4 * (lane & 15);
+  const bool col_in = col < K;
 #pragma unroll
-  for (int j = 0; j < SliceMap<T>::PER_LANE; ++j) {
-    const int idx = lane + 32 * j;
-    if (idx >= SliceMap<T>::ITEMS) break;
-    uint32_t row, cc;
-    SliceMap<T>::item(idx, row, cc);
-    const uint32_t rs = (uint32_t)(tw * T::RW) + row;
-    const uint32_t o0 = sw128(rs, 2 * cc);
-    const uint32_t o1 = sw128(rs, 2 * cc + 1);
-    float4 a0 = ld_shared_v4f(g_box + o0);
-    float4 a1 = ld_shared_v4f(g_box + o1);
-    if constexpr (T::kSwiglu) {
-      const float4 u0 = ld_shared_v4f(u_box + o0);
-      const float4 u1 = ld_shared_v4f(u_box + o1);
-      a0.x = silu_stable_fast(a0.x) * u0.x;
-      a0.y = silu_stable_fast(a0.y) * u0.y;
-      a0.z = silu_stable_fast(a0.z) * u0.z;
-      a0.w = silu_stable_fast(a0.w) * u0.w;
-      a1.x = silu_stable_fast(a1.x) * u1.x;
-      a1.y = silu_stable_fast(a1.y) * u1.y;
-      a1.z = silu_stable_fast(a1.z) * u1.z;
-      a1.w = silu_stable_fast(a1.w) * u1.w;
-    }
-    out[j][0] = pack_half2(a0.x, a0.y);
-    out[j][1] = pack_half2(a0.z, a0.w);
-    out[j][2] = pack_half2(a1.x, a1.y);
-    out[j][3] = pack_half2(a1.z, a1.w);
+  for (int q = 0; q < T::LPI; ++q) {
+    const int row = row0 + tw * T::RW + 2 * q + (lane >> 4);
+    const bool in = col_in && row < M;
+    const size_t off = (size_t)(in ? row : 0) * (size_t)K + (size_t)(in ? col : 0);
+    st.v[0][q] = in ? ldg_stream_v4f(a + off) : make_float4(0.f, 0.f, 0.f, 0.f);
+    if constexpr (T::kSwiglu)
+      st.v[1][q] = in ? ldg_stream_v4f(u + off) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
 }
 
+// A values of the staged k-block, binary16 pairs: out[q] = 4 consecutive k.
 template <typename T>
-__device__ __forceinline__ void transform_store(uint32_t a_stage, int half, int tw, int lane,
-                                                uint32_t crank,
-                                                const uint32_t (&v)[SliceMap<T>::PER_LANE][4]) {
+__device__ __forceinline__ void stage_compute(const Staged<T>& st, uint32_t (&out)[T::LPI][2]) {
 #pragma unroll
-  for (int j = 0; j < SliceMap<T>::PER_LANE; ++j) {
-    const int idx = lane + 32 * j;
-    if (idx >= SliceMap<T>::ITEMS) break;
-    uint32_t row, cc;
-    SliceMap<T>::item(idx, row, cc);
-    const uint32_t r = crank * (uint32_t)T::ROWS + (uint32_t)(tw * T::RW) + row;
-    st_shared_v4(a_stage + sw128(r, 4 * (uint32_t)half + cc), v[j][0], v[j][1], v[j][2], v[j][3]);
+  for (int q = 0; q < T::LPI; ++q) {
+    float4 a = st.v[0][q];
+    if constexpr (T::kSwiglu) {
+      const float4 u = st.v[1][q];
+      a.x = silu_stable_fast(a.x) * u.x;
+      a.y = silu_stable_fast(a.y) * u.y;
+      a.z = silu_stable_fast(a.z) * u.z;
+      a.w = silu_stable_fast(a.w) * u.w;
+    }
+    out[q][0] = pack_half2(a.x, a.y);
+    out[q][1] = pack_half2(a.z, a.w);
+  }
+}
+
+// Into the A stage (128 rows x 128 bytes, 128-byte swizzle): this CTA's
+// slice starts at row crank*ROWS; lane%16 is the 8-byte quarter-pair of the
+// row, so 16 lanes fill one row and a warp's store covers two whole rows
+// (every bank twice, the minimum for 256 bytes).
+template <typename T>
+__device__ __forceinline__ void stage_store(uint32_t a_stage, uint32_t crank, int tw, int lane,
+                                            const uint32_t (&out)[T::LPI][2]) {
+  const uint32_t c4 = (uint32_t)(lane & 15);
+#pragma unroll
+  for (int q = 0; q < T::LPI; ++q) {
+    const uint32_t r = crank * (uint32_t)T::ROWS + (uint32_t)(tw * T::RW + 2 * q + (lane >> 4));
+    st_shared_v2(a_stage + sw128(r, c4 >> 1) + (c4 & 1u) * 8u, out[q][0], out[q][1]);
   }
 }
 
 template <int AMODE, bool RESID, int BN, int CN>
 __global__ void __launch_bounds__((8 + LIN_XF_WARPS) * 32, 1)
-    lin_gemm_cluster_kernel(const __grid_constant__ CUtensorMap tm_a,
-                            const __grid_constant__ CUtensorMap tm_u,
-                            const __grid_constant__ CUtensorMap tm_w,
-                            const __grid_constant__ CUtensorMap tm_r,
-                            const __grid_constant__ CUtensorMap tm_y, const KernelArgs args) {
+    lin_gemm_cluster_kernel(const __grid_constant__ CUtensorMap tm_w, const KernelArgs args) {
   using T = ClusterTraits<AMODE, RESID, BN, CN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -239,7 +217,6 @@ __global__ void __launch_bounds__((8 + LIN_XF_WARPS) * 32, 1)
 
   auto a_stage = [&](int s) -> uint32_t { return sbase + T::OFF_OP + s * T::OP_STAGE_BYTES; };
   auto b_stage = [&](int s) -> uint32_t { return a_stage(s) + T::A_BYTES; };
-  auto raw_stage = [&](int r) -> uint32_t { return sbase + T::OFF_RAW + r * T::RAW_STAGE_BYTES; };
   auto tile_m0 = [&](int t) -> int { return (t / num_ng) * T::BM; };
   auto tile_n0 = [&](int t) -> int { return ((t % num_ng) * CN + (int)crank) * T::BN; };
   // number of work items this cluster processes
@@ -251,10 +228,6 @@ __global__ void __launch_bounds__((8 + LIN_XF_WARPS) * 32, 1)
       mbar_init(bar(T::BAR_FULL + s), T::XF_PER_GROUP + 1);   // W producer + one transform group
       mbar_init(bar(T::BAR_ST_EMPTY + s), CN);     // every CTA's UMMA commit
     }
-    for (int r = 0; r < T::NR; ++r) {
-      mbar_init(bar(T::BAR_RAW_FULL + r), 1);
-      mbar_init(bar(T::BAR_RAW_EMPTY + r), T::XF_PER_GROUP);
-    }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(T::BAR_ACC_FULL + b), 1);
       mbar_init(bar(T::BAR_ACC_EMPTY + b), 4);
@@ -264,11 +237,7 @@ __global__ void __launch_bounds__((8 + LIN_XF_WARPS) * 32, 1)
     fence_proxy_async_smem();
   }
   __syncwarp();
-  if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tm_w);
-    tma_prefetch_desc(&tm_a);
-    if constexpr (T::kSwiglu) tma_prefetch_desc(&tm_u);
-  }
+  if (warp == 0 && lane == 0) tma_prefetch_desc(&tm_w);
   __syncwarp();
   if (warp == 2) {
     tmem_alloc(smem_u32(tmem_slot), T::TMEM_COLS);
@@ -373,65 +342,47 @@ __global__ void __launch_bounds__((8 + LIN_XF_WARPS) * 32, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 3) {
-    // ---------------- raw producer: this CTA's rows of GATE/UP (or X)
-    int tr = 0;   // input stages (k-blocks) issued, across tiles
-    bool ok = true;
-    for (int i = 0; i < my_tiles && ok; ++i) {
-      const int t = cid + i * ncl;
-      const int row = tile_m0(t) + (int)crank * T::ROWS;
-      for (int kb = 0; kb < nkb; ++kb, ++tr) {
-        const int r = tr % T::NR;
-        if (tr >= T::NR &&
-            !lane0_wait_phase(bar(T::BAR_RAW_EMPTY + r), ((tr / T::NR) - 1) & 1, ctl, lane)) {
-          ok = false;
-          break;
-        }
-        if (lane == 0) {
-          const uint32_t full = bar(T::BAR_RAW_FULL + r);
-          mbar_arrive_expect_tx(full, T::RAW_STAGE_BYTES);
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            tma_load_2d(raw_stage(r) + h * T::RAW_BOX_BYTES, &tm_a, kb * T::BK + h * 32, row, full);
-            if constexpr (T::kSwiglu)
-              tma_load_2d(raw_stage(r) + (2 + h) * T::RAW_BOX_BYTES, &tm_u, kb * T::BK + h * 32, row,
-                          full);
-          }
-        }
-        __syncwarp();
-      }
-    }
-    if (lane == 0)
-      for (int x = (tr > T::NR ? tr - T::NR : 0); x < tr; ++x)
-        wait_phase(bar(T::BAR_RAW_FULL + x % T::NR), (x / T::NR) & 1, ctl, false);
-    __syncwarp();
   } else if (warp >= 4 && warp < 4 + T::XF_WARPS) {
     // ---------------- transform warps
     const int grp = (warp - 4) / T::XF_PER_GROUP;
     const int tw = (warp - 4) % T::XF_PER_GROUP;
     const uint32_t slice_off = (crank * (uint32_t)T::ROWS + (uint32_t)(tw * T::RW)) * 128u;
-    int g = 0;   // k-blocks across tiles (operand and input stages alike)
-    bool ok = true;
-    for (int i = 0; i < my_tiles && ok; ++i) {
-      for (int kb = 0; kb < nkb; ++kb, ++g) {
-        if (g % T::XF_GROUPS != grp) continue;
-        const int s = g % T::NS;
-        // Arithmetic first (registers); then wait for the stage to be free.
-        uint32_t vals[2][SliceMap<T>::PER_LANE][4];
-        {
-          const int r = g % T::NR;
-          if (!warp_wait_phase(bar(T::BAR_RAW_FULL + r), (g / T::NR) & 1, ctl)) {
-            ok = false;
-            break;
-          }
-          const uint32_t rs = raw_stage(r);
+    const int total = my_tiles * nkb;   // k-blocks of this CTA, across tiles
+    // k-block g (counted across tiles) -> first row of this CTA's slice, k0
+    auto coords = [&](int g, int& row0, int& k0) {
+      const int i = g / nkb;
+      const int kb = g - i * nkb;
+      row0 = tile_m0(cid + i * ncl) + (int)crank * T::ROWS;
+      k0 = kb * T::BK;
+    };
+    // This group's k-blocks are g = grp + XF_GROUPS * j; buffer j % PF holds
+    // the inputs of k-block j, loaded PF of the group's k-blocks ahead.
+    Staged<T> buf[T::PF];
 #pragma unroll
-          for (int h = 0; h < 2; ++h)
-            transform_compute<T>(rs + h * T::RAW_BOX_BYTES, rs + (2 + h) * T::RAW_BOX_BYTES, tw, lane,
-                                 vals[h]);
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(T::BAR_RAW_EMPTY + r));
+    for (int d = 0; d < T::PF; ++d) {
+      const int g = grp + T::XF_GROUPS * d;
+      if (g < total) {
+        int row0, k0;
+        coords(g, row0, k0);
+        stage_load<T>(buf[d], args.A, args.U, row0, k0, args.M, args.K, tw, lane);
+      }
+    }
+    bool ok = true;
+    int g_end = 0;   // k-blocks (of every group) before the first one not filled
+    for (int j0 = 0; ok && grp + T::XF_GROUPS * j0 < total; j0 += T::PF) {
+#pragma unroll
+      for (int d = 0; d < T::PF; ++d) {
+        const int g = grp + T::XF_GROUPS * (j0 + d);
+        if (g >= total) break;
+        uint32_t vals[T::LPI][2];
+        stage_compute<T>(buf[d], vals);
+        const int gn = g + T::XF_GROUPS * T::PF;
+        if (gn < total) {
+          int row0, k0;
+          coords(gn, row0, k0);
+          stage_load<T>(buf[d], args.A, args.U, row0, k0, args.M, args.K, tw, lane);
         }
+        const int s = g % T::NS;
         if (g >= T::NS) {
           // Every CTA's UMMA is done with this stage: ours may be rewritten
           // and the peers' copies of it overwritten.
@@ -441,9 +392,7 @@ __global__ void __launch_bounds__((8 + LIN_XF_WARPS) * 32, 1)
             break;
           }
         }
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-          transform_store<T>(a_stage(s), h, tw, lane, crank, vals[h]);
+        stage_store<T>(a_stage(s), crank, tw, lane, vals);
         fence_proxy_async_smem();   // our rows -> visible to UMMA and to the copy engine
         __syncwarp();
         if (lane == 0) {
@@ -453,21 +402,23 @@ __global__ void __launch_bounds__((8 + LIN_XF_WARPS) * 32, 1)
             mbar_arrive_expect_tx(full, T::REMOTE_BYTES_PER_WARP);
             const uint32_t src = a_stage(s) + slice_off;
 #pragma unroll
-            for (uint32_t d = 0; d < (uint32_t)CN; ++d)
-              if (d != crank)
-                bulk_copy_s2cluster(mapa_shared(src, d), src, T::SLICE_BYTES, mapa_shared(full, d));
+            for (uint32_t dst = 0; dst < (uint32_t)CN; ++dst)
+              if (dst != crank)
+                bulk_copy_s2cluster(mapa_shared(src, dst), src, T::SLICE_BYTES,
+                                    mapa_shared(full, dst));
           } else {
             mbar_arrive(full);
           }
         }
         __syncwarp();
+        g_end = g + 1;
       }
     }
-    // Every peer's commit for the stages we filled must have landed (they
+    // Every peer's commit for the stages filled must have landed (they
     // arrive on our barriers, and our copies read our shared memory) before
     // this CTA may leave.
     if (lane == 0)
-      for (int x = (g > T::NS ? g - T::NS : 0); x < g; ++x)
+      for (int x = (g_end > T::NS ? g_end - T::NS : 0); x < g_end; ++x)
         wait_phase_cluster(bar(T::BAR_ST_EMPTY + x % T::NS), (x / T::NS) & 1, ctl, false);
     __syncwarp();
   } else if (warp >= 4 + T::XF_WARPS) {
@@ -579,7 +530,7 @@ cudaError_t launch_cluster_instance(const TensorMaps& m, const KernelArgs& args,
   const int cap = max_clusters[dev].load(std::memory_order_acquire);
   if (clusters > cap) clusters = cap;
   cfg.gridDim = dim3((unsigned)(clusters * CN), 1, 1);
-  return cudaLaunchKernelEx(&cfg, kern, m.a, m.u, m.w, m.r, m.y, args);
+  return cudaLaunchKernelEx(&cfg, kern, m.w, args);
 }
 
 }  // namespace lin

@@ -30,6 +30,8 @@ struct KernelArgs {
   uint32_t flags;
   uint64_t timeout_ns;  // limit for any single wait inside the kernel
   int* status;          // device status word (first failure wins)
+  const float* A;       // X or GATE [M, K] (kernels that load it directly)
+  const float* U;       // UP [M, K] (SwiGLU forms, kernels that load it directly)
   const float* R;       // residual [M, N] (kernels that read it directly)
   float* Y;             // output [M, N] (kernels that write it directly)
 };
@@ -55,8 +57,9 @@ cudaError_t launch_gemm_f16(int amode, bool resid, int bn, const TensorMaps& map
                             const KernelArgs& args, cudaStream_t stream);
 
 // Clustered persistent kernels for the binary16-weight forms: a cluster of
-// `cn` CTAs along N shares the on-chip A operand (128/cn rows each). The
-// A-side tensor maps (X, or GATE and UP) must use boxes of 32 x (128/cn).
+// `cn` CTAs along N shares the on-chip A operand (128/cn rows each). They
+// read X (or GATE and UP) through KernelArgs::A/U and W through its tensor
+// map; R and Y through KernelArgs.
 constexpr int kClusterBN = 256;
 cudaError_t launch_gemm_cluster_swiglu(int cn, const TensorMaps& maps, const KernelArgs& args,
                                        cudaStream_t stream);
