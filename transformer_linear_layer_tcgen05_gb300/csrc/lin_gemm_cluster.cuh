@@ -71,8 +71,11 @@ struct ClusterTraits {
   static constexpr int XF_GROUPS = (kSwiglu && CN == 1) ? 1 : 2;
   static constexpr int XF_PER_GROUP = XF_WARPS / XF_GROUPS;
   static constexpr int RW = ROWS / XF_PER_GROUP;  // A rows per transform warp (contiguous)
-  static constexpr uint32_t SLICE_BYTES = RW * 128;             // one warp's rows of a stage
+  // Each transform warp bulk-copies its RW rows of a stage to every peer as
+  // soon as it has written them (measured faster than one copy per group).
+  static constexpr uint32_t SLICE_BYTES = RW * 128;
   static constexpr uint32_t REMOTE_BYTES_PER_WARP = SLICE_BYTES * (CN - 1);
+
   // A warp's 16-byte loads cover two rows of a 64-wide k-block at a time
   // (lanes 0-15 one row, 16-31 the next): LPI loads per input and lane.
   static constexpr int LPI = RW / 2;
@@ -84,8 +87,16 @@ struct ClusterTraits {
   static constexpr uint32_t A_BYTES = BM * 128;
   static constexpr uint32_t B_ATOM_BYTES = BK * 128;
   static constexpr uint32_t B_BYTES = W_BOXES * B_ATOM_BYTES;
+
   static constexpr uint32_t OP_STAGE_BYTES = A_BYTES + B_BYTES;
 
+  // One operand ring; shared memory holds as many stages as fit (the round
+  // trip of a stage -- W load and peer copies, UMMA, commit to every CTA --
+  // is several UMMA k-blocks long). A stage has one full barrier: the W
+  // tile's TMA bytes, the arrivals of the transform group's warps and the
+  // peers' copied A rows all land on it, so the UMMA thread waits once per
+  // k-block. (Separate A and W rings of their own depths measured
+  // slower: two waits and two commits per k-block.)
   static constexpr uint32_t SMEM_CAP = 232448;
   static constexpr uint32_t BAR_REGION = 1024;
   static constexpr uint32_t ALIGN_SLACK = 1024;
@@ -97,12 +108,9 @@ struct ClusterTraits {
   static constexpr uint32_t OFF_BAR = NS * OP_STAGE_BYTES;
   static constexpr uint32_t SMEM_BYTES = ALIGN_SLACK + OFF_BAR + BAR_REGION;
 
-  // One full barrier per operand stage: the W tile's TMA bytes, the local
-  // transform warps' arrivals and the peers' copied A rows all land on it, so
-  // the UMMA warp waits once per k-block.
   static constexpr int BAR_FULL = 0;
-  static constexpr int BAR_ST_EMPTY = BAR_FULL + 8;      // every CTA's UMMA done with stage
-  static constexpr int BAR_ACC_FULL = BAR_ST_EMPTY + 8;  // 2 accumulator buffers
+  static constexpr int BAR_EMPTY = BAR_FULL + 8;         // every CTA's UMMA done with stage
+  static constexpr int BAR_ACC_FULL = BAR_EMPTY + 8;     // 2 accumulator buffers
   static constexpr int BAR_ACC_EMPTY = BAR_ACC_FULL + 2;
   static constexpr int BAR_COUNT = BAR_ACC_EMPTY + 2;
   static constexpr uint32_t OFF_TMEM_SLOT = BAR_COUNT * 8;
@@ -119,12 +127,13 @@ struct ClusterTraits {
                 "transform groups");
   static_assert(LOADS <= 16, "staged input per lane");
   // A parity wait is only sound for a waiter at most one phase ahead: a group
-  // reaching use u of an operand stage must already have seen use u-1's
-  // UMMA complete, true when its previous k-block (XF_GROUPS earlier) waited
-  // for a UMMA no older than the stage's use before last.
+  // reaching use u of a stage must already have seen use u-1's UMMA
+  // complete, true when its previous k-block (XF_GROUPS earlier) waited for
+  // a UMMA no older than the stage's use before last.
   static_assert(XF_GROUPS <= NS, "ring depth vs transform groups");
   static_assert(NS >= 2 && NS <= 8, "ring depth");
   static_assert(OFF_ABORT + 4 <= BAR_REGION, "barrier region");
+  static_assert(OP_STAGE_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "swizzle atoms");
   static_assert(SMEM_BYTES <= SMEM_CAP, "shared memory");
   static_assert(TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM columns");
   // A CTA holding all 512 TMEM columns must be alone on its SM (a second one
@@ -225,8 +234,8 @@ __global__ void __launch_bounds__((8 + LIN_XF_WARPS) * 32, 1)
   // ---- set-up
   if (threadIdx.x == 0) {
     for (int s = 0; s < T::NS; ++s) {
-      mbar_init(bar(T::BAR_FULL + s), T::XF_PER_GROUP + 1);   // W producer + one transform group
-      mbar_init(bar(T::BAR_ST_EMPTY + s), CN);     // every CTA's UMMA commit
+      mbar_init(bar(T::BAR_FULL + s), 1 + T::XF_PER_GROUP);   // W producer, the group's warps
+      mbar_init(bar(T::BAR_EMPTY + s), CN);        // every CTA's UMMA commit
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(T::BAR_ACC_FULL + b), 1);
@@ -264,7 +273,7 @@ __global__ void __launch_bounds__((8 + LIN_XF_WARPS) * 32, 1)
         const int s = g % T::NS;
         if (g >= T::NS) {
           bool w = true;
-          if (lane == 0) w = wait_phase_cluster(bar(T::BAR_ST_EMPTY + s), ((g / T::NS) - 1) & 1, ctl);
+          if (lane == 0) w = wait_phase_cluster(bar(T::BAR_EMPTY + s), ((g / T::NS) - 1) & 1, ctl);
           if (!__shfl_sync(0xffffffffu, w ? 1 : 0, 0)) {
             ok = false;
             break;
@@ -318,9 +327,9 @@ __global__ void __launch_bounds__((8 + LIN_XF_WARPS) * 32, 1)
             umma_f16(d_tmem, adesc, bdesc, T::IDESC, (kb | k) != 0);
           }
           if constexpr (CN > 1)
-            umma_commit_multicast(bar(T::BAR_ST_EMPTY + s), T::CLUSTER_MASK);
+            umma_commit_multicast(bar(T::BAR_EMPTY + s), T::CLUSTER_MASK);
           else
-            umma_commit(bar(T::BAR_ST_EMPTY + s));
+            umma_commit(bar(T::BAR_EMPTY + s));
         }
         __syncwarp();
       }
@@ -347,6 +356,7 @@ __global__ void __launch_bounds__((8 + LIN_XF_WARPS) * 32, 1)
     const int grp = (warp - 4) / T::XF_PER_GROUP;
     const int tw = (warp - 4) % T::XF_PER_GROUP;
     const uint32_t slice_off = (crank * (uint32_t)T::ROWS + (uint32_t)(tw * T::RW)) * 128u;
+
     const int total = my_tiles * nkb;   // k-blocks of this CTA, across tiles
     // k-block g (counted across tiles) -> first row of this CTA's slice, k0
     auto coords = [&](int g, int& row0, int& k0) {
@@ -386,7 +396,7 @@ __global__ void __launch_bounds__((8 + LIN_XF_WARPS) * 32, 1)
         if (g >= T::NS) {
           // Every CTA's UMMA is done with this stage: ours may be rewritten
           // and the peers' copies of it overwritten.
-          const bool w = wait_phase_cluster(bar(T::BAR_ST_EMPTY + s), ((g / T::NS) - 1) & 1, ctl);
+          const bool w = wait_phase_cluster(bar(T::BAR_EMPTY + s), ((g / T::NS) - 1) & 1, ctl);
           if (!__all_sync(0xffffffffu, w)) {
             ok = false;
             break;
@@ -419,7 +429,7 @@ __global__ void __launch_bounds__((8 + LIN_XF_WARPS) * 32, 1)
     // this CTA may leave.
     if (lane == 0)
       for (int x = (g_end > T::NS ? g_end - T::NS : 0); x < g_end; ++x)
-        wait_phase_cluster(bar(T::BAR_ST_EMPTY + x % T::NS), (x / T::NS) & 1, ctl, false);
+        wait_phase_cluster(bar(T::BAR_EMPTY + x % T::NS), (x / T::NS) & 1, ctl, false);
     __syncwarp();
   } else if (warp >= 4 + T::XF_WARPS) {
     // ---------------- epilogue warps: lane = one output row of the tile
