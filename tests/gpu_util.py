@@ -50,8 +50,10 @@ def oracle_error(form: str, d: dict, Y: np.ndarray, rows=None) -> float:
 
 def integer_inputs(form: str, M: int, N: int, K: int, seed: int) -> dict:
     """Small-integer inputs for which every product, partial sum and operand
-    rounding of the GPU path is exact (|x|, |w| <= 4, K <= 256; GATE >= 40 so
-    sigma(GATE) is 1.0 in float32 and float64 alike)."""
+    rounding of the GPU path is exact: |X|, |UP|, |W| <= 4 and GATE in
+    [40, 60], so sigma(GATE) is 1.0 in float32 and float64 alike, every A
+    value is an integer of magnitude <= 240 (exact in binary16) and every
+    partial sum is an integer below K * 960 < 2**24 for K <= 16384."""
     rng = np.random.default_rng(seed)
     d = {}
     if wl.form_is_swiglu(form):

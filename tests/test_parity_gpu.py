@@ -42,6 +42,38 @@ def test_exact_small_integers(form, shape):
     assert np.array_equal(Y, Yref), f"max |diff| = {np.max(np.abs(Y - Yref))}"
 
 
+# Persistent launches that split the last partial round along K (clustered
+# kernels, binary16 forms): each tail tile's K ranges leave f32 partial
+# tiles that the warp completing a quadrant adds up in K order. On a GB300
+# with 36 resident clusters of four, the first shape splits its 6 tiles 4
+# ways with no whole round before; the second runs two whole rounds, then
+# splits its last 2 tiles 2 ways.
+SPLIT_SHAPES = [(300, 2048, 2048), (4736, 2048, 1024)]
+
+
+@pytest.mark.parametrize("form", W16_FORMS)
+@pytest.mark.parametrize("shape", SPLIT_SHAPES)
+def test_split_tail_exact(form, shape):
+    M, N, K = shape
+    d = integer_inputs(form, M, N, K, seed=M + N + K)
+    Y = run_device(form, to_device(d), M, N).cpu().numpy().astype(np.float64)
+    Yref, _ = oracle.reference(form, d)
+    assert np.array_equal(Y, Yref), f"max |diff| = {np.max(np.abs(Y - Yref))}"
+
+
+@pytest.mark.parametrize("form", W16_FORMS)
+def test_split_tail_random_reproducible(form):
+    import torch
+    M, N, K = SPLIT_SHAPES[0]
+    d = wl.generate(form, M, N, K, seed=23, outlier_frac=0.01)
+    dd = to_device(d)
+    Y1 = run_device(form, dd, M, N)
+    Y2 = run_device(form, dd, M, N)
+    assert torch.equal(Y1, Y2)
+    err = oracle_error(form, d, Y1.cpu().numpy())
+    assert err <= TOL, err
+
+
 RANDOM_SHAPES = [(300, 392, 200), (257, 136, 1028), (64, 1024, 96), (513, 264, 516)]
 
 

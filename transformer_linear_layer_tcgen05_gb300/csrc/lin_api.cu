@@ -66,8 +66,33 @@ struct DeviceState {
   lin_status status = LIN_SUCCESS;
   int cuda_error = 0;
   int* status_word = nullptr;
+  std::once_flag pool_once;
+  cudaMemPool_t pool = nullptr;   // workspace of split launches (stream-ordered)
 };
 DeviceState g_devices[kMaxDevices];
+
+// The library's own memory pool on device `dev`, created on first use, that
+// keeps freed workspace for reuse (it never trims itself); null if the pool
+// cannot be created.
+cudaMemPool_t workspace_pool(int dev) {
+  DeviceState& s = g_devices[dev];
+  std::call_once(s.pool_once, [&] {
+    cudaMemPoolProps props = {};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    cudaMemPool_t pool = nullptr;
+    if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) {
+      cudaGetLastError();
+      return;
+    }
+    uint64_t keep = UINT64_MAX;
+    if (cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep) != cudaSuccess)
+      cudaGetLastError();
+    s.pool = pool;
+  });
+  return s.pool;
+}
 
 // Checks the current device once (sm_103, driver entry points, status word).
 lin_status current_device(int* dev_out, int** status_word) {
@@ -282,17 +307,63 @@ lin_status run(const Problem& p, cudaStream_t stream) {
   args.U = swiglu ? p.U : nullptr;
   args.R = resid ? p.R : nullptr;
   args.Y = p.Y;
+  args.split_r = 0;
+  args.split_rem = 0;
+  args.split_s = 1;
 
   cudaError_t e;
-  if (cn > 0)
+  if (cn > 0) {
+    // Persistent launch: split the K range of the last partial round when
+    // that keeps idle clusters busy, with a workspace from the library's
+    // stream-ordered pool (freed on the same stream after the launch). If
+    // no workspace can be had, or the stream is being captured into a graph,
+    // the launch runs unsplit.
+    cudaError_t ce = cudaSuccess;
+    const int cap = swiglu ? lin::cluster_capacity_swiglu(cn, &ce)
+                           : lin::cluster_capacity_cvt(cn, resid, &ce);
+    if (cap < 1) return cuda_fail(ce);
+    const int num_m = (int)((M + lin::kBM - 1) / lin::kBM);
+    const int num_ng = (int)((N + (uint64_t)lin::kClusterBN * cn - 1) / ((uint64_t)lin::kClusterBN * cn));
+    const int nkb = (int)((K + 63) / 64);
+    lin::SplitPlan plan = lin::split_plan(num_m * num_ng, cap, nkb);
+    void* ws = nullptr;
+    cudaStreamCaptureStatus cap_status = cudaStreamCaptureStatusNone;
+    if (plan.s >= 2 && (cudaStreamIsCapturing(stream, &cap_status) != cudaSuccess ||
+                        cap_status != cudaStreamCaptureStatusNone)) {
+      cudaGetLastError();
+      plan.s = 1;
+    }
+    if (plan.s >= 2) {
+      const size_t pb = lin::split_part_bytes(plan, cn, lin::kClusterBN);
+      cudaMemPool_t pool = workspace_pool(dev);
+      if (pool && cudaMallocFromPoolAsync(&ws, pb, pool, stream) == cudaSuccess) {
+        args.part = static_cast<float*>(ws);
+        args.split_r = plan.r;
+        args.split_rem = plan.rem;
+        args.split_s = plan.s;
+      } else {
+        cudaGetLastError();
+        if (ws) cudaFreeAsync(ws, stream);
+        ws = nullptr;
+      }
+    }
     e = swiglu ? lin::launch_gemm_cluster_swiglu(cn, maps, args, stream)
                : lin::launch_gemm_cluster_cvt(cn, resid, maps, args, stream);
-  else if (p.w16)
+    if (e == cudaSuccess && args.split_s >= 2) {
+      const int clusters = args.split_r > 0 ? cap : args.split_rem * args.split_s;
+      e = lin::launch_split_reduce(args, resid, cn, clusters, num_ng, stream);
+    }
+    if (ws) {
+      const cudaError_t ef = cudaFreeAsync(ws, stream);
+      if (e == cudaSuccess) e = ef;
+    }
+  } else if (p.w16) {
     e = lin::launch_gemm_f16(swiglu ? lin::A_SWIGLU_F16 : lin::A_CVT_F16, resid, bn, maps, args,
                              stream);
-  else
+  } else {
     e = lin::launch_gemm_tf32(swiglu ? lin::A_SWIGLU_F32 : lin::A_TMA_F32, resid, bn, maps, args,
                               stream);
+  }
   return e == cudaSuccess ? LIN_SUCCESS : cuda_fail(e);
 }
 

@@ -228,8 +228,24 @@ __global__ void __launch_bounds__((8 + LIN_XF_WARPS) * 32, 1)
   auto b_stage = [&](int s) -> uint32_t { return a_stage(s) + T::A_BYTES; };
   auto tile_m0 = [&](int t) -> int { return (t / num_ng) * T::BM; };
   auto tile_n0 = [&](int t) -> int { return ((t % num_ng) * CN + (int)crank) * T::BN; };
-  // number of work items this cluster processes
-  const int my_tiles = cid < num_tiles ? (num_tiles - 1 - cid) / ncl + 1 : 0;
+  // Work items of this cluster: whole tiles cid + i*ncl, round robin; with a
+  // split tail (split_s >= 2), split_r whole tiles and then, for clusters
+  // below split_rem*split_s, K range `unit_p` of tail tile split_r*ncl +
+  // cid/split_s (unit index = cid).
+  const bool split = args.split_s >= 2;
+  const int S = split ? args.split_s : 1;
+  const int n_full =
+      split ? args.split_r : (cid < num_tiles ? (num_tiles - 1 - cid) / ncl + 1 : 0);
+  const bool has_unit = split && cid < args.split_rem * S;
+  const int n_items = n_full + (has_unit ? 1 : 0);
+  const int unit_p = cid % S;
+  const int unit_kb0 = unit_p * nkb / S;
+  const int unit_kb1 = (unit_p + 1) * nkb / S;
+  auto item_tile = [&](int i) -> int {
+    return i < n_full ? cid + i * ncl : args.split_r * ncl + cid / S;
+  };
+  auto item_kb0 = [&](int i) -> int { return i < n_full ? 0 : unit_kb0; };
+  auto item_kb1 = [&](int i) -> int { return i < n_full ? nkb : unit_kb1; };
 
   // ---- set-up
   if (threadIdx.x == 0) {
@@ -266,10 +282,10 @@ __global__ void __launch_bounds__((8 + LIN_XF_WARPS) * 32, 1)
     // ---------------- W producer (local TMA into the B half of each stage)
     int g = 0;   // k-blocks issued, across tiles
     bool ok = true;
-    for (int i = 0; i < my_tiles && ok; ++i) {
-      const int t = cid + i * ncl;
-      const int n0 = tile_n0(t);
-      for (int kb = 0; kb < nkb; ++kb, ++g) {
+    for (int i = 0; i < n_items && ok; ++i) {
+      const int n0 = tile_n0(item_tile(i));
+      const int kb1 = item_kb1(i);
+      for (int kb = item_kb0(i); kb < kb1; ++kb, ++g) {
         const int s = g % T::NS;
         if (g >= T::NS) {
           bool w = true;
@@ -299,14 +315,15 @@ __global__ void __launch_bounds__((8 + LIN_XF_WARPS) * 32, 1)
     int g = 0;
     bool ok = true;
     int committed_tiles = 0;
-    for (int i = 0; i < my_tiles && ok; ++i) {
+    for (int i = 0; i < n_items && ok; ++i) {
       const int ab = i & 1;
       const uint32_t d_tmem = tmem + (uint32_t)(ab * T::BN);
       if (i >= 2 && !lane0_wait_phase(bar(T::BAR_ACC_EMPTY + ab), ((i >> 1) - 1) & 1, ctl, lane)) {
         ok = false;
         break;
       }
-      for (int kb = 0; kb < nkb; ++kb, ++g) {
+      const int kb0 = item_kb0(i), kb1 = item_kb1(i);
+      for (int kb = kb0; kb < kb1; ++kb, ++g) {
         const int s = g % T::NS;
         const uint32_t ph = (g / T::NS) & 1;
         bool w = true;
@@ -324,7 +341,7 @@ __global__ void __launch_bounds__((8 + LIN_XF_WARPS) * 32, 1)
             const uint64_t adesc = umma_desc_sw128(a_stage(s) + k * 32, 16, 1024);
             const uint64_t bdesc =
                 umma_desc_sw128(b_stage(s) + k * T::KSTEP * 128, T::B_ATOM_BYTES, 1024);
-            umma_f16(d_tmem, adesc, bdesc, T::IDESC, (kb | k) != 0);
+            umma_f16(d_tmem, adesc, bdesc, T::IDESC, kb != kb0 || k != 0);
           }
           if constexpr (CN > 1)
             umma_commit_multicast(bar(T::BAR_EMPTY + s), T::CLUSTER_MASK);
@@ -357,12 +374,19 @@ __global__ void __launch_bounds__((8 + LIN_XF_WARPS) * 32, 1)
     const int tw = (warp - 4) % T::XF_PER_GROUP;
     const uint32_t slice_off = (crank * (uint32_t)T::ROWS + (uint32_t)(tw * T::RW)) * 128u;
 
-    const int total = my_tiles * nkb;   // k-blocks of this CTA, across tiles
-    // k-block g (counted across tiles) -> first row of this CTA's slice, k0
+    // k-blocks of this CTA, across work items
+    const int total = n_full * nkb + (has_unit ? unit_kb1 - unit_kb0 : 0);
+    // k-block g (counted across items) -> first row of this CTA's slice, k0
     auto coords = [&](int g, int& row0, int& k0) {
-      const int i = g / nkb;
-      const int kb = g - i * nkb;
-      row0 = tile_m0(cid + i * ncl) + (int)crank * T::ROWS;
+      int i, kb;
+      if (g < n_full * nkb) {
+        i = g / nkb;
+        kb = g - i * nkb;
+      } else {
+        i = n_full;
+        kb = unit_kb0 + (g - n_full * nkb);
+      }
+      row0 = tile_m0(item_tile(i)) + (int)crank * T::ROWS;
       k0 = kb * T::BK;
     };
     // This group's k-blocks are g = grp + XF_GROUPS * j; buffer j % PF holds
@@ -435,9 +459,11 @@ __global__ void __launch_bounds__((8 + LIN_XF_WARPS) * 32, 1)
     // ---------------- epilogue warps: lane = one output row of the tile
     const int q = warp & 3;                        // TMEM lane quadrant
     constexpr int NC = T::BN / kEpiCols;
+    constexpr int C4 = T::BN / 4;                  // float4 columns of a tile
     bool ok = true;
-    for (int i = 0; i < my_tiles && ok; ++i) {
-      const int t = cid + i * ncl;
+    for (int i = 0; i < n_items && ok; ++i) {
+      const int t = item_tile(i);
+      const bool is_unit = i >= n_full;            // a K range of a split tail tile
       const int ab = i & 1;
       const int row = tile_m0(t) + q * kEpiRows + lane;
       const int n0 = tile_n0(t);
@@ -451,20 +477,32 @@ __global__ void __launch_bounds__((8 + LIN_XF_WARPS) * 32, 1)
       const bool row_in = row < args.M;
       float* yrow = args.Y + (size_t)(row_in ? row : 0) * (size_t)args.N;
       const float* rrow = RESID ? args.R + (size_t)(row_in ? row : 0) * (size_t)args.N : nullptr;
+      // partial tile of this unit: [C4 float4 columns][128 rows]
+      float4* part = is_unit ? reinterpret_cast<float4*>(args.part) +
+                                   (size_t)(cid * CN + (int)crank) * C4 * T::BM + q * kEpiRows + lane
+                             : nullptr;
       for (int c = 0; c < nc; ++c) {
         const int col0 = n0 + c * kEpiCols;
         float4 rr[8];
         if constexpr (RESID) {
+          if (!is_unit) {
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            rr[j] = (row_in && col0 + 4 * j < args.N)
-                        ? __ldg(reinterpret_cast<const float4*>(rrow + col0 + 4 * j))
-                        : make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int j = 0; j < 8; ++j)
+              rr[j] = (row_in && col0 + 4 * j < args.N)
+                          ? __ldg(reinterpret_cast<const float4*>(rrow + col0 + 4 * j))
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
         }
         uint32_t v[32];
         tmem_ld_32x32b_x32(acc + (uint32_t)(c * kEpiCols), v);
         tmem_wait_ld();
-        if (row_in) {
+        if (is_unit) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            part[(size_t)(c * 8 + j) * T::BM] =
+                make_float4(__uint_as_float(v[4 * j + 0]), __uint_as_float(v[4 * j + 1]),
+                            __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+        } else if (row_in) {
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             if (col0 + 4 * j >= args.N) break;
@@ -500,47 +538,114 @@ __global__ void __launch_bounds__((8 + LIN_XF_WARPS) * 32, 1)
   }
 }
 
+// Launch configuration of one instantiation; the first call per device sets
+// the shared-memory attribute and records how many clusters fit at once.
 template <int AMODE, bool RESID, int BN, int CN>
-cudaError_t launch_cluster_instance(const TensorMaps& m, const KernelArgs& args,
-                                    cudaStream_t stream) {
+struct ClusterLaunch {
   using T = ClusterTraits<AMODE, RESID, BN, CN>;
-  auto kern = lin_gemm_cluster_kernel<AMODE, RESID, BN, CN>;
-  static std::atomic<uint64_t> attr_done{0};
-  static std::atomic<int> max_clusters[64];
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev >= 64) return cudaErrorInvalidDevice;
-  const uint64_t bit = uint64_t{1} << dev;
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = CN;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(T::kThreadsC, 1, 1);
-  cfg.dynamicSmemBytes = T::SMEM_BYTES;
-  cfg.stream = stream;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (!(attr_done.load(std::memory_order_acquire) & bit)) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    cfg.gridDim = dim3(CN, 1, 1);
-    int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, (void*)kern, &cfg);
-    if (e != cudaSuccess) return e;
-    if (n < 1) return cudaErrorInvalidConfiguration;
-    max_clusters[dev].store(n, std::memory_order_release);
-    attr_done.fetch_or(bit, std::memory_order_acq_rel);
+  static cudaLaunchConfig_t config(cudaLaunchAttribute* attr, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CN;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(T::kThreadsC, 1, 1);
+    cfg.dynamicSmemBytes = T::SMEM_BYTES;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cfg;
   }
-  const int num_m = (args.M + T::BM - 1) / T::BM;
-  const int num_ng = (args.N + T::BN * CN - 1) / (T::BN * CN);
-  int clusters = num_m * num_ng;
-  const int cap = max_clusters[dev].load(std::memory_order_acquire);
-  if (clusters > cap) clusters = cap;
-  cfg.gridDim = dim3((unsigned)(clusters * CN), 1, 1);
-  return cudaLaunchKernelEx(&cfg, kern, m.w, args);
+  // Clusters resident at once on the current device (> 0), or 0 with *err.
+  static int capacity(cudaError_t* err) {
+    static std::atomic<uint64_t> attr_done{0};
+    static std::atomic<int> max_clusters[64];
+    auto kern = lin_gemm_cluster_kernel<AMODE, RESID, BN, CN>;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess && dev >= 64) e = cudaErrorInvalidDevice;
+    if (e != cudaSuccess) {
+      *err = e;
+      return 0;
+    }
+    const uint64_t bit = uint64_t{1} << dev;
+    if (!(attr_done.load(std::memory_order_acquire) & bit)) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
+      cudaLaunchAttribute attr[1];
+      cudaLaunchConfig_t cfg = config(attr, nullptr);
+      cfg.gridDim = dim3(CN, 1, 1);
+      int n = 0;
+      if (e == cudaSuccess) e = cudaOccupancyMaxActiveClusters(&n, (void*)kern, &cfg);
+      if (e == cudaSuccess && n < 1) e = cudaErrorInvalidConfiguration;
+      if (e != cudaSuccess) {
+        *err = e;
+        return 0;
+      }
+      max_clusters[dev].store(n, std::memory_order_release);
+      attr_done.fetch_or(bit, std::memory_order_acq_rel);
+    }
+    return max_clusters[dev].load(std::memory_order_acquire);
+  }
+  // Grid: every resident cluster when whole rounds remain; with a split tail
+  // alone, one cluster per K range; else one per tile.
+  static cudaError_t launch(const TensorMaps& m, const KernelArgs& args, cudaStream_t stream) {
+    cudaError_t e = cudaSuccess;
+    const int cap = capacity(&e);
+    if (cap < 1) return e;
+    const int num_m = (args.M + T::BM - 1) / T::BM;
+    const int num_ng = (args.N + T::BN * CN - 1) / (T::BN * CN);
+    int clusters;
+    if (args.split_s >= 2)
+      clusters = args.split_r > 0 ? cap : args.split_rem * args.split_s;
+    else
+      clusters = num_m * num_ng < cap ? num_m * num_ng : cap;
+    if (clusters > cap) return cudaErrorInvalidConfiguration;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = config(attr, stream);
+    cfg.gridDim = dim3((unsigned)(clusters * CN), 1, 1);
+    return cudaLaunchKernelEx(&cfg, lin_gemm_cluster_kernel<AMODE, RESID, BN, CN>, m.w, args);
+  }
+};
+
+// Sum of a split tail: one thread per float4 of Y. Thread x is float4
+// column c4 = (x / 128) % C4 and row x % 128 of CTA `crank` of tail tile j,
+// x / (128 * C4) = j * CN + crank, the same order as the partial tiles, so
+// consecutive threads read consecutive partial rows. Y = sum over the S K
+// ranges in K order (+ R): independent of timing, so bitwise reproducible.
+template <bool RESID>
+__global__ void __launch_bounds__(256)
+    lin_split_reduce_kernel(const float4* __restrict__ part, const float* __restrict__ R,
+                            float* __restrict__ Y, int M, int N, int cn, int bn, int tile0,
+                            int num_ng, int rem, int s) {
+  const int c4n = bn / 4;
+  const long long per_cta = 128LL * c4n;
+  const long long x = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (x >= (long long)rem * cn * per_cta) return;
+  const int jc = (int)(x / per_cta);          // j * cn + crank
+  const int j = jc / cn, crank = jc % cn;
+  const int c4 = (int)((x / 128) % c4n);
+  const int r = (int)(x % 128);
+  const int t = tile0 + j;
+  const int row = (t / num_ng) * 128 + r;
+  const int col = ((t % num_ng) * cn + crank) * bn + 4 * c4;
+  if (row >= M || col >= N) return;
+  float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int p = 0; p < s; ++p) {
+    const float4 v = part[((long long)((j * s + p) * cn + crank) * c4n + c4) * 128 + r];
+    sum.x += v.x;
+    sum.y += v.y;
+    sum.z += v.z;
+    sum.w += v.w;
+  }
+  const size_t off = (size_t)row * (size_t)N + (size_t)col;
+  if constexpr (RESID) {
+    const float4 rv = *reinterpret_cast<const float4*>(R + off);
+    sum.x += rv.x;
+    sum.y += rv.y;
+    sum.z += rv.z;
+    sum.w += rv.w;
+  }
+  *reinterpret_cast<float4*>(Y + off) = sum;
 }
 
 }  // namespace lin

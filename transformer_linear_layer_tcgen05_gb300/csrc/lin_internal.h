@@ -34,7 +34,38 @@ struct KernelArgs {
   const float* U;       // UP [M, K] (SwiGLU forms, kernels that load it directly)
   const float* R;       // residual [M, N] (kernels that read it directly)
   float* Y;             // output [M, N] (kernels that write it directly)
+  // Split tail of the clustered kernels (see SplitPlan); unused when split_s < 2.
+  int32_t split_r, split_rem, split_s;
+  float* part;          // partial tiles [unit][cta][BN/4 float4 columns][128 rows] (float4)
 };
+
+// Work plan of a persistent launch over `tiles` cluster tiles on `clusters`
+// clusters: `r` whole rounds (every cluster runs tiles cid + i*clusters), then
+// the `rem` tiles left over are each cut into `s` K ranges (s >= 2), one per
+// cluster, so that the last round keeps every cluster busy. The ranges' f32
+// partial tiles go to a workspace, and a second kernel adds them up in K
+// order (bitwise reproducible). s < 2: no split, whole tiles round robin.
+struct SplitPlan {
+  int r, rem, s;
+};
+constexpr int kSplitMinKb = 8;   // k-blocks per K range at least (else no split)
+
+__host__ __device__ inline SplitPlan split_plan(int tiles, int clusters, int nkb) {
+  SplitPlan p{0, 0, 1};
+  if (clusters < 1 || tiles < 1) return p;
+  const int r = tiles / clusters, rem = tiles % clusters;
+  if (rem == 0) return p;
+  int s = clusters / rem;
+  if (s > nkb / kSplitMinKb) s = nkb / kSplitMinKb;
+  if (s < 2) return p;
+  return SplitPlan{r, rem, s};
+}
+
+// Workspace bytes of a split plan (partial tiles) for clusters of `cn` CTAs
+// with tiles of 128 x `bn`.
+inline size_t split_part_bytes(const SplitPlan& p, int cn, int bn) {
+  return p.s >= 2 ? (size_t)p.rem * p.s * cn * 128 * bn * sizeof(float) : 0;
+}
 
 // Tensor maps of one call. `a` is X (A_TMA_F32 / A_CVT_F16) or GATE, `u` is
 // UP (SwiGLU forms only), `w` the weights, `r` the residual, `y` the output.
@@ -65,5 +96,13 @@ cudaError_t launch_gemm_cluster_swiglu(int cn, const TensorMaps& maps, const Ker
                                        cudaStream_t stream);
 cudaError_t launch_gemm_cluster_cvt(int cn, bool resid, const TensorMaps& maps,
                                     const KernelArgs& args, cudaStream_t stream);
+// Clusters of `cn` CTAs that can be resident at once (sets the kernel's
+// shared-memory attribute on first use); > 0, or 0 with *err set.
+int cluster_capacity_swiglu(int cn, cudaError_t* err);
+int cluster_capacity_cvt(int cn, bool resid, cudaError_t* err);
+// Y (+ R) from the partial tiles of a split tail: `clusters` is the
+// clustered launch's cluster count, `num_ng` its cluster tiles per row block.
+cudaError_t launch_split_reduce(const KernelArgs& args, bool resid, int cn, int clusters,
+                                int num_ng, cudaStream_t stream);
 
 }  // namespace lin

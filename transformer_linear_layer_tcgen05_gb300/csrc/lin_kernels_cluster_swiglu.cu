@@ -4,13 +4,25 @@
 
 namespace lin {
 
+template <int CN>
+using SwigluLaunch = ClusterLaunch<A_SWIGLU_F16, true, 256, CN>;
+
 cudaError_t launch_gemm_cluster_swiglu(int cn, const TensorMaps& maps, const KernelArgs& args,
                                        cudaStream_t stream) {
   switch (cn) {
-    case 1: return launch_cluster_instance<A_SWIGLU_F16, true, 256, 1>(maps, args, stream);
-    case 2: return launch_cluster_instance<A_SWIGLU_F16, true, 256, 2>(maps, args, stream);
-    case 4: return launch_cluster_instance<A_SWIGLU_F16, true, 256, 4>(maps, args, stream);
+    case 1: return SwigluLaunch<1>::launch(maps, args, stream);
+    case 2: return SwigluLaunch<2>::launch(maps, args, stream);
+    case 4: return SwigluLaunch<4>::launch(maps, args, stream);
     default: return cudaErrorInvalidValue;
+  }
+}
+
+int cluster_capacity_swiglu(int cn, cudaError_t* err) {
+  switch (cn) {
+    case 1: return SwigluLaunch<1>::capacity(err);
+    case 2: return SwigluLaunch<2>::capacity(err);
+    case 4: return SwigluLaunch<4>::capacity(err);
+    default: *err = cudaErrorInvalidValue; return 0;
   }
 }
 
