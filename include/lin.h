@@ -33,7 +33,18 @@
  *             CUDA half type.
  * Memory      Every pointer is device memory of the current CUDA device,
  *             owned by the caller. The library keeps no reference after the
- *             call returns and allocates no device memory per call.
+ *             call returns. The w16 forms run a persistent launch; when its
+ *             last round would leave SMs idle it splits that round along K
+ *             and takes a workspace for the f32 partial tiles (at most
+ *             128 KiB per SM, 19 MiB on a 152-SM GB300) from a memory pool
+ *             the library creates on first use of each device. The workspace
+ *             is allocated and freed in stream order on `stream`, so calls
+ *             on different streams never share it; the pool keeps freed
+ *             memory for reuse. On a stream that is being captured into a
+ *             graph, or if the pool cannot supply the workspace, the launch
+ *             runs unsplit (same results, bitwise, up to the summation order
+ *             of the tail: see Arithmetic). lin_last_launch_info() reports
+ *             what a call used.
  * Stream      Work is enqueued on `stream` (a cudaStream_t; NULL means the
  *             legacy default stream) and the call returns without waiting.
  *             Inputs must stay valid, and Y must not be read, until the
@@ -43,7 +54,10 @@
  *             accumulation. The w16 forms round the A operand (X, or
  *             silu(GATE) * UP) to binary16, round-to-nearest-even, and
  *             multiply binary16 x binary16 with float32 accumulation. The
- *             residual is added once in float32. Results satisfy
+ *             residual is added once in float32. A split tail sums its K
+ *             ranges' float32 partial tiles in K order, so every call with
+ *             the same inputs, device and stream state gives the same bits.
+ *             Results satisfy
  *             max |Y - Y_exact| / sum_k |A[i,k] W[k,j]| <= 4e-3.
  *             Values of A beyond the binary16 range (|A| > 65504) become
  *             +-inf in the w16 forms.
@@ -144,6 +158,12 @@ const char *lin_status_string(lin_status status);
 
 /* The cudaError_t value behind the calling thread's last LIN_ERROR_CUDA (0 if none). */
 int lin_last_cuda_error(void);
+
+/* What the last compute call made on the calling thread enqueued: the number
+ * of kernels it launched (1, or 2 with a split tail; 0 if it enqueued none or
+ * failed) and the workspace bytes it took from the library's pool. Either
+ * pointer may be NULL. */
+void lin_last_launch_info(int* kernels, uint64_t* workspace_bytes);
 
 /* Waits for `stream`, then returns and clears the current device's status
  * word: LIN_SUCCESS, or LIN_ERROR_TIMEOUT if a kernel gave up on a wait since

@@ -34,7 +34,7 @@ def test_header_declares_the_family():
     for form in ("matmul", "matmul_residual", "matmul_residual_swiglu_a"):
         assert f"lin_{form}" in names and f"lin_{form}_w16" in names
     assert {"lin_status_string", "lin_get_device_status", "lin_last_cuda_error",
-            "lin_selftest_wait_timeout", "lin_version"} <= set(names)
+            "lin_selftest_wait_timeout", "lin_version", "lin_last_launch_info"} <= set(names)
 
 
 def test_every_declared_symbol_is_exported(L):
@@ -47,6 +47,16 @@ def test_binding_covers_every_compute_entry_point():
         if name.startswith("lin_matmul"):
             assert name in lin.SIGNATURES
             assert name[len("lin_"):] in lin.FORM_FUNCS
+
+
+def test_launch_info_after_rejected_and_empty_calls(L):
+    # a call rejected by validation, or one with nothing to do, launches
+    # nothing and takes no workspace
+    fake = 1 << 40
+    assert L.lin_matmul_w16(fake, fake, fake, -1, 8, 8, None) == lin.LIN_ERROR_INVALID_VALUE
+    assert lin.lin_last_launch_info() == (0, 0)
+    assert L.lin_matmul_w16(fake, fake, fake, 0, 8, 8, None) == lin.LIN_SUCCESS
+    assert lin.lin_last_launch_info() == (0, 0)
 
 
 def test_status_strings(L):

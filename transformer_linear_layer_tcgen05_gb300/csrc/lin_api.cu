@@ -21,6 +21,8 @@ constexpr uint64_t kDefaultTimeoutNs = 1000ull * 1000ull * 1000ull;   // 1 s per
 constexpr int kMaxDevices = 64;
 
 thread_local int t_last_cuda_error = 0;
+thread_local int t_last_kernels = 0;            // lin_last_launch_info
+thread_local uint64_t t_last_workspace = 0;
 
 lin_status cuda_fail(cudaError_t e) {
   t_last_cuda_error = static_cast<int>(e);
@@ -214,6 +216,8 @@ struct Problem {
 };
 
 lin_status run(const Problem& p, cudaStream_t stream) {
+  t_last_kernels = 0;
+  t_last_workspace = 0;
   // 1. dims and required pointers
   if (p.M < 0 || p.N < 0 || p.K < 0) return LIN_ERROR_INVALID_VALUE;
   if (p.M == 0 || p.N == 0) return LIN_SUCCESS;
@@ -312,6 +316,8 @@ lin_status run(const Problem& p, cudaStream_t stream) {
   args.split_s = 1;
 
   cudaError_t e;
+  int kernels = 1;
+  uint64_t workspace = 0;
   if (cn > 0) {
     // Persistent launch: split the K range of the last partial round when
     // that keeps idle clusters busy, with a workspace from the library's
@@ -338,6 +344,7 @@ lin_status run(const Problem& p, cudaStream_t stream) {
       cudaMemPool_t pool = workspace_pool(dev);
       if (pool && cudaMallocFromPoolAsync(&ws, pb, pool, stream) == cudaSuccess) {
         args.part = static_cast<float*>(ws);
+        workspace = pb;
         args.split_r = plan.r;
         args.split_rem = plan.rem;
         args.split_s = plan.s;
@@ -352,6 +359,7 @@ lin_status run(const Problem& p, cudaStream_t stream) {
     if (e == cudaSuccess && args.split_s >= 2) {
       const int clusters = args.split_r > 0 ? cap : args.split_rem * args.split_s;
       e = lin::launch_split_reduce(args, resid, cn, clusters, num_ng, stream);
+      kernels = 2;
     }
     if (ws) {
       const cudaError_t ef = cudaFreeAsync(ws, stream);
@@ -364,7 +372,10 @@ lin_status run(const Problem& p, cudaStream_t stream) {
     e = lin::launch_gemm_tf32(swiglu ? lin::A_SWIGLU_F32 : lin::A_TMA_F32, resid, bn, maps, args,
                               stream);
   }
-  return e == cudaSuccess ? LIN_SUCCESS : cuda_fail(e);
+  if (e != cudaSuccess) return cuda_fail(e);
+  t_last_kernels = kernels;
+  t_last_workspace = workspace;
+  return LIN_SUCCESS;
 }
 
 lin_status read_and_clear_status(cudaStream_t stream) {
@@ -443,6 +454,11 @@ const char* lin_status_string(lin_status status) {
 }
 
 int lin_last_cuda_error(void) { return t_last_cuda_error; }
+
+void lin_last_launch_info(int* kernels, uint64_t* workspace_bytes) {
+  if (kernels) *kernels = t_last_kernels;
+  if (workspace_bytes) *workspace_bytes = t_last_workspace;
+}
 
 lin_status lin_get_device_status(lin_stream_t stream) {
   return read_and_clear_status(reinterpret_cast<cudaStream_t>(stream));

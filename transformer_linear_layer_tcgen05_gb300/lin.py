@@ -93,6 +93,9 @@ def lib() -> ctypes.CDLL:
         L.lin_last_cuda_error.restype = ctypes.c_int
         L.lin_version.argtypes = []
         L.lin_version.restype = ctypes.c_int
+        L.lin_last_launch_info.argtypes = [ctypes.POINTER(ctypes.c_int),
+                                           ctypes.POINTER(ctypes.c_uint64)]
+        L.lin_last_launch_info.restype = None
         _lib = L
     return _lib
 
@@ -202,6 +205,15 @@ def lin_matmul_residual_swiglu_a_w16(GATE, UP, W16, R, Y, stream=None):
     _call("lin_matmul_residual_swiglu_a_w16", GATE.data_ptr(), UP.data_ptr(),
           W16.data_ptr(), R.data_ptr(), Y.data_ptr(), M, N, K, _stream_handle(stream))
     return Y
+
+
+def lin_last_launch_info() -> tuple:
+    """(kernels launched, workspace bytes taken) by the last compute call made
+    on this thread."""
+    k = ctypes.c_int(0)
+    b = ctypes.c_uint64(0)
+    lib().lin_last_launch_info(ctypes.byref(k), ctypes.byref(b))
+    return k.value, b.value
 
 
 def lin_get_device_status(stream=None) -> int:
