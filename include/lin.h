@@ -153,6 +153,38 @@ lin_status lin_matmul_residual_swiglu_a_w16(const float *GATE, const float *UP,
                                             int64_t M, int64_t N, int64_t K,
                                             lin_stream_t stream);
 
+/* lin_matmul_residual_swiglu_a_w16 that allocates no device memory. The pages
+ * have no counterpart: their engine has no such constraint. It exists for
+ * callers that must not allocate while a call runs, for example a serving
+ * loop that reserves all of its device memory up front, or code for which
+ * growing a memory pool (which maps new memory, can fail, and can take
+ * milliseconds the first time) is not acceptable.
+ *
+ * Same arguments, layouts, validation, errors and results as
+ * lin_matmul_residual_swiglu_a_w16 (bitwise, for the same device). The one
+ * difference is where the workspace of a split tail lives: in a static
+ * 19 MiB array on each device (152 SMs x 128 KiB), which the library loads
+ * with the module that holds it, instead of the library's memory pool. The
+ * call makes no cudaMalloc/cudaFree or pool allocation and never reports
+ * workspace bytes in lin_last_launch_info.
+ *   Limit     a problem whose split would need more than 19 MiB (possible
+ *             only on a device with more than 152 SMs) is rejected with
+ *             LIN_ERROR_UNSUPPORTED_SHAPE before anything is enqueued.
+ *   Set-up    the first call on a device that passes validation looks up
+ *             the array's address (cudaGetSymbolAddress, which loads its
+ *             module); make that first call before capturing a stream.
+ *             A failed look-up returns LIN_ERROR_CUDA every time.
+ *   Zeroing   nothing in the array needs to start at zero: a call writes
+ *             every byte of it that it reads first.
+ *   Races     every call on a device shares the one array. Calls whose
+ *             execution can overlap (on different streams, or from threads
+ *             that do not order their streams) corrupt each other's
+ *             results; calls on a single stream are ordered and safe. */
+lin_status lin_matmul_residual_swiglu_a_w16_noalloc(const float *GATE, const float *UP,
+                                                    const uint16_t *W16, const float *R,
+                                                    float *Y, int64_t M, int64_t N, int64_t K,
+                                                    lin_stream_t stream);
+
 /* Static, NUL-terminated name of a status code ("LIN_SUCCESS", ...). Never NULL. */
 const char *lin_status_string(lin_status status);
 

@@ -46,7 +46,19 @@ def test_binding_covers_every_compute_entry_point():
     for name in declared_functions():
         if name.startswith("lin_matmul"):
             assert name in lin.SIGNATURES
-            assert name[len("lin_"):] in lin.FORM_FUNCS
+            assert hasattr(lin, name)
+            # a _noalloc variant is its base form with a fixed workspace
+            assert name[len("lin_"):].removesuffix("_noalloc") in lin.FORM_FUNCS
+
+
+def test_noalloc_validates_before_touching_cuda(L):
+    # rejected like the base entry point, without any CUDA call
+    fake = 1 << 40
+    f = L.lin_matmul_residual_swiglu_a_w16_noalloc
+    assert f(fake, fake, fake, fake, fake, -1, 8, 8, None) == lin.LIN_ERROR_INVALID_VALUE
+    assert f(fake, fake, fake, fake, fake, 8, 12, 8, None) == lin.LIN_ERROR_UNSUPPORTED_SHAPE
+    assert f(fake, fake, fake, fake, fake, 0, 8, 8, None) == lin.LIN_SUCCESS
+    assert lin.lin_last_launch_info() == (0, 0)
 
 
 def test_launch_info_after_rejected_and_empty_calls(L):

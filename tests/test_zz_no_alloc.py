@@ -1,0 +1,77 @@
+"""lin_matmul_residual_swiglu_a_w16_noalloc against the entry point it varies.
+
+The variant keeps its split-tail workspace in a static device array instead
+of the library's memory pool. Two calls in a row must give exactly the result
+of lin_matmul_residual_swiglu_a_w16, take no workspace from the pool, and
+launch the same kernels. The file is collected last, after every other GPU
+test, and also passes on its own.
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+from tests.gpu_util import TOL, integer_inputs, oracle_error, require_gpu, to_device
+from transformer_linear_layer_tcgen05_gb300 import lin
+from transformer_linear_layer_tcgen05_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+FORM = "matmul_residual_swiglu_a_w16"
+# On a GB300 (36 resident clusters of four) the first shape splits its last
+# round along K (6 tiles cut into 4 K ranges each), so the static workspace
+# is used; the second runs whole tiles only.
+SPLIT = (300, 2048, 2048)
+SHAPES = [SPLIT, (256, 1024, 256)]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    require_gpu()
+
+
+def _nan_like(M, N):
+    import torch
+    return torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+
+
+def _noalloc(dd, Y):
+    return lin.lin_matmul_residual_swiglu_a_w16_noalloc(dd["GATE"], dd["UP"], dd["W16"],
+                                                        dd["R"], Y)
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+def test_two_calls_match_the_pool_entry_point(shape):
+    import torch
+    M, N, K = shape
+    d = wl.generate(FORM, M, N, K, seed=31 + M, outlier_frac=0.01)
+    dd = to_device(d)
+    ref = _nan_like(M, N)
+    lin.lin_matmul_residual_swiglu_a_w16(dd["GATE"], dd["UP"], dd["W16"], dd["R"], ref)
+    kernels_ref, pool_bytes_ref = lin.lin_last_launch_info()
+    if shape == SPLIT:
+        assert kernels_ref == 2 and pool_bytes_ref > 0   # the split path is exercised
+    outs = []
+    for _ in range(2):
+        Y = _nan_like(M, N)
+        _noalloc(dd, Y)
+        kernels, pool_bytes = lin.lin_last_launch_info()
+        assert kernels == kernels_ref
+        assert pool_bytes == 0
+        outs.append(Y)
+    torch.cuda.synchronize()
+    assert lin.lin_get_device_status() == lin.LIN_SUCCESS
+    assert torch.equal(outs[0], ref)
+    assert torch.equal(outs[1], ref)
+    assert oracle_error(FORM, d, outs[1].cpu().numpy()) <= TOL
+
+
+def test_split_tail_is_exact_on_integer_inputs():
+    M, N, K = SPLIT
+    d = integer_inputs(FORM, M, N, K, seed=5)
+    dd = to_device(d)
+    Y = _nan_like(M, N)
+    _noalloc(dd, Y)
+    assert lin.lin_get_device_status() == lin.LIN_SUCCESS
+    Yref, _ = oracle.reference(FORM, d)
+    assert np.array_equal(Y.cpu().numpy().astype(np.float64), Yref)

@@ -215,7 +215,10 @@ struct Problem {
   int64_t M, N, K;
 };
 
-lin_status run(const Problem& p, cudaStream_t stream) {
+// `fixed`: where a split tail's workspace comes from instead of the library's
+// pool (null for the ordinary entry points); it is resolved once validation
+// has passed and reports its base address and size.
+lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed = nullptr) {
   t_last_kernels = 0;
   t_last_workspace = 0;
   // 1. dims and required pointers
@@ -272,6 +275,11 @@ lin_status run(const Problem& p, cudaStream_t stream) {
       return st;
     }
   }
+
+  // 6b. a caller-provided workspace (its set-up runs on the first valid call)
+  void* fixed_ptr = nullptr;
+  size_t fixed_bytes = 0;
+  if (fixed && (st = fixed(dev, &fixed_ptr, &fixed_bytes)) != LIN_SUCCESS) return st;
 
   // 7. K == 0: nothing is accumulated, Y = R (or 0)
   if (K == 0) {
@@ -339,7 +347,15 @@ lin_status run(const Problem& p, cudaStream_t stream) {
       cudaGetLastError();
       plan.s = 1;
     }
-    if (plan.s >= 2) {
+    if (plan.s >= 2 && fixed) {
+      // fixed workspace: a plan that needs more than it holds is rejected
+      const size_t pb = lin::split_part_bytes(plan, cn, lin::kClusterBN);
+      if (pb > fixed_bytes) return LIN_ERROR_UNSUPPORTED_SHAPE;
+      args.part = static_cast<float*>(fixed_ptr);
+      args.split_r = plan.r;
+      args.split_rem = plan.rem;
+      args.split_s = plan.s;
+    } else if (plan.s >= 2) {
       const size_t pb = lin::split_part_bytes(plan, cn, lin::kClusterBN);
       cudaMemPool_t pool = workspace_pool(dev);
       if (pool && cudaMallocFromPoolAsync(&ws, pb, pool, stream) == cudaSuccess) {
@@ -376,6 +392,14 @@ lin_status run(const Problem& p, cudaStream_t stream) {
   t_last_kernels = kernels;
   t_last_workspace = workspace;
   return LIN_SUCCESS;
+}
+
+lin_status record_cuda_error(cudaError_t e) { return cuda_fail(e); }
+
+lin_status run_swiglu_w16_fixed(const float* GATE, const float* UP, const uint16_t* W16,
+                                const float* R, float* Y, int64_t M, int64_t N, int64_t K,
+                                cudaStream_t stream, lin::WorkspaceGetter get) {
+  return run({F_SWIGLU, true, nullptr, GATE, UP, W16, R, Y, M, N, K}, stream, get);
 }
 
 lin_status read_and_clear_status(cudaStream_t stream) {

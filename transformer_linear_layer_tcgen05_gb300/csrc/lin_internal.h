@@ -2,9 +2,12 @@
 // translation units (not part of the public C ABI).
 #pragma once
 
+#include <cstddef>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
+
+#include "lin.h"
 
 namespace lin {
 
@@ -105,4 +108,18 @@ int cluster_capacity_cvt(int cn, bool resid, cudaError_t* err);
 cudaError_t launch_split_reduce(const KernelArgs& args, bool resid, int cn, int clusters,
                                 int num_ng, cudaStream_t stream);
 
+// A caller-provided split-tail workspace: returns its base and size on
+// device `dev`, or an error status.
+typedef lin_status (*WorkspaceGetter)(int dev, void** ptr, size_t* bytes);
+
 }  // namespace lin
+
+namespace lin_detail {
+// lin_matmul_residual_swiglu_a_w16 with the split-tail workspace from `get`
+// instead of the library's pool (lin_api.cu).
+lin_status run_swiglu_w16_fixed(const float* GATE, const float* UP, const uint16_t* W16,
+                                const float* R, float* Y, int64_t M, int64_t N, int64_t K,
+                                cudaStream_t stream, lin::WorkspaceGetter get);
+// Records `e` as the calling thread's last CUDA error; returns LIN_ERROR_CUDA.
+lin_status record_cuda_error(cudaError_t e);
+}  // namespace lin_detail

@@ -57,6 +57,7 @@ SIGNATURES = {
     "lin_matmul_residual_swiglu_a_w16": [_P, _P, _P, _P, _P, _I, _I, _I, _S],
     "lin_get_device_status": [_S],
     "lin_selftest_wait_timeout": [_I, _S],
+    "lin_matmul_residual_swiglu_a_w16_noalloc": [_P, _P, _P, _P, _P, _I, _I, _I, _S],
 }
 
 _lib = None
@@ -203,6 +204,21 @@ def lin_matmul_residual_swiglu_a_w16(GATE, UP, W16, R, Y, stream=None):
     if tuple(_f32(UP, "UP").shape) != (M, K) or tuple(_f32(R, "R").shape) != (M, N):
         raise ValueError("UP must be [M, K] and R [M, N]")
     _call("lin_matmul_residual_swiglu_a_w16", GATE.data_ptr(), UP.data_ptr(),
+          W16.data_ptr(), R.data_ptr(), Y.data_ptr(), M, N, K, _stream_handle(stream))
+    return Y
+
+
+def lin_matmul_residual_swiglu_a_w16_noalloc(GATE, UP, W16, R, Y, stream=None):
+    """lin_matmul_residual_swiglu_a_w16 with its split-tail workspace in the
+    library's static device array: allocates no device memory. Calls whose
+    execution can overlap (different streams) must not be issued."""
+    M, K = _f32(GATE, "GATE").shape
+    N = W16.shape[1]
+    if tuple(W16.shape) != (K, N) or tuple(_f32(Y, "Y").shape) != (M, N):
+        raise ValueError("W16 must be [K, N] and Y [M, N]")
+    if tuple(_f32(UP, "UP").shape) != (M, K) or tuple(_f32(R, "R").shape) != (M, N):
+        raise ValueError("UP must be [M, K] and R [M, N]")
+    _call("lin_matmul_residual_swiglu_a_w16_noalloc", GATE.data_ptr(), UP.data_ptr(),
           W16.data_ptr(), R.data_ptr(), Y.data_ptr(), M, N, K, _stream_handle(stream))
     return Y
 
