@@ -41,10 +41,13 @@
  *             is allocated and freed in stream order on `stream`, so calls
  *             on different streams never share it; the pool keeps freed
  *             memory for reuse. On a stream that is being captured into a
- *             graph, or if the pool cannot supply the workspace, the launch
- *             runs unsplit (same results, bitwise, up to the summation order
- *             of the tail: see Arithmetic). lin_last_launch_info() reports
- *             what a call used.
+ *             graph the workspace is a graph memory node (cudaMallocAsync /
+ *             cudaFreeAsync), owned by that graph. If no workspace can be
+ *             had the launch runs unsplit (the same results up to the order
+ *             in which the tail's K ranges are summed). The f32 forms split
+ *             K in the same way when a problem has too few 128 x 128 tiles
+ *             to fill the SMs (at most 64 KiB of workspace per SM).
+ *             lin_last_launch_info() reports what a call used.
  * Stream      Work is enqueued on `stream` (a cudaStream_t; NULL means the
  *             legacy default stream) and the call returns without waiting.
  *             Inputs must stay valid, and Y must not be read, until the

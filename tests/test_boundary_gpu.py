@@ -154,3 +154,33 @@ def test_bounded_wait_times_out_cleanly():
     Y = run_device("matmul", to_device(d), 128, 128).cpu().numpy().astype(np.float64)
     assert np.array_equal(Y, oracle.reference("matmul", d)[0])
     assert torch.cuda.is_available()
+
+
+@pytest.mark.parametrize("form,shape", [("matmul", (512, 768, 768)),
+                                        ("matmul_residual_swiglu_a_w16", (300, 2048, 2048))])
+def test_split_inside_a_cuda_graph(form, shape):
+    # A split launch captured into a graph takes its workspace as a graph
+    # memory node; replays must equal a direct call bit for bit.
+    torch = _torch()
+    M, N, K = shape
+    dd = to_device(wl.generate(form, M, N, K, seed=9))
+    direct = run_device(form, dd, M, N)
+    kernels, _ = lin.lin_last_launch_info()
+    assert kernels == 2                     # the problem splits on a GB300
+    Y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            lin.run_form(form, dd, Y)
+            captured = lin.lin_last_launch_info()
+    torch.cuda.current_stream().wait_stream(s)
+    assert captured[0] == 2 and captured[1] > 0
+    for _ in range(2):
+        Y.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert lin.lin_get_device_status() == lin.LIN_SUCCESS
+        assert torch.equal(Y, direct)
+    del g

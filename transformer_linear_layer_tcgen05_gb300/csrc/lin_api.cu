@@ -1,9 +1,10 @@
 // lin_api.cu -- the C ABI of include/lin.h: argument validation, tensor-map
-// encoding and kernel launch. No allocation, no host<->device copies on the
-// compute path; every operation runs in the kernels of lin_gemm.cuh.
+// encoding, the workspace of split launches and kernel launch. No host<->device
+// copies on the compute path; every operation runs in the library's kernels.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -97,6 +98,20 @@ cudaMemPool_t workspace_pool(int dev) {
 }
 
 // Checks the current device once (sm_103, driver entry points, status word).
+// SMs of device `dev` (queried once per device).
+int sm_count(int dev) {
+  static std::atomic<int> counts[kMaxDevices];
+  int n = counts[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) {
+      cudaGetLastError();
+      n = 1;
+    }
+    counts[dev].store(n, std::memory_order_relaxed);
+  }
+  return n;
+}
+
 lin_status current_device(int* dev_out, int** status_word) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -323,15 +338,51 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
   args.split_rem = 0;
   args.split_s = 1;
 
+  // Workspace for f32 partial tiles of a split (either kernel): the caller's
+  // fixed workspace, or a stream-ordered allocation freed on the same stream
+  // after the launch -- from the library's pool, or, while the stream is
+  // being captured into a graph, a graph memory node (cudaMallocAsync), so
+  // that each graph owns its workspace. 1: got it; 0: run unsplit (no memory
+  // to be had); -1: the fixed workspace is too small (the call is rejected).
+  void* ws = nullptr;           // pool allocation to free
+  uint64_t workspace = 0;       // pool bytes taken
+  auto take_workspace = [&](size_t bytes) -> int {
+    if (fixed) {
+      if (bytes > fixed_bytes) return -1;
+      args.part = static_cast<float*>(fixed_ptr);
+      return 1;
+    }
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    if (cs != cudaStreamCaptureStatusNone) {
+      if (cs != cudaStreamCaptureStatusActive || cudaMallocAsync(&ws, bytes, stream) != cudaSuccess) {
+        cudaGetLastError();
+        ws = nullptr;
+        return 0;
+      }
+      args.part = static_cast<float*>(ws);
+      workspace = bytes;
+      return 1;
+    }
+    cudaMemPool_t pool = workspace_pool(dev);
+    if (!pool || cudaMallocFromPoolAsync(&ws, bytes, pool, stream) != cudaSuccess) {
+      cudaGetLastError();
+      ws = nullptr;
+      return 0;
+    }
+    args.part = static_cast<float*>(ws);
+    workspace = bytes;
+    return 1;
+  };
+
   cudaError_t e;
   int kernels = 1;
-  uint64_t workspace = 0;
   if (cn > 0) {
     // Persistent launch: split the K range of the last partial round when
-    // that keeps idle clusters busy, with a workspace from the library's
-    // stream-ordered pool (freed on the same stream after the launch). If
-    // no workspace can be had, or the stream is being captured into a graph,
-    // the launch runs unsplit.
+    // that keeps idle clusters busy.
     cudaError_t ce = cudaSuccess;
     const int cap = swiglu ? lin::cluster_capacity_swiglu(cn, &ce)
                            : lin::cluster_capacity_cvt(cn, resid, &ce);
@@ -339,54 +390,56 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
     const int num_m = (int)((M + lin::kBM - 1) / lin::kBM);
     const int num_ng = (int)((N + (uint64_t)lin::kClusterBN * cn - 1) / ((uint64_t)lin::kClusterBN * cn));
     const int nkb = (int)((K + 63) / 64);
-    lin::SplitPlan plan = lin::split_plan(num_m * num_ng, cap, nkb);
-    void* ws = nullptr;
-    cudaStreamCaptureStatus cap_status = cudaStreamCaptureStatusNone;
-    if (plan.s >= 2 && (cudaStreamIsCapturing(stream, &cap_status) != cudaSuccess ||
-                        cap_status != cudaStreamCaptureStatusNone)) {
-      cudaGetLastError();
-      plan.s = 1;
-    }
-    if (plan.s >= 2 && fixed) {
-      // fixed workspace: a plan that needs more than it holds is rejected
-      const size_t pb = lin::split_part_bytes(plan, cn, lin::kClusterBN);
-      if (pb > fixed_bytes) return LIN_ERROR_UNSUPPORTED_SHAPE;
-      args.part = static_cast<float*>(fixed_ptr);
-      args.split_r = plan.r;
-      args.split_rem = plan.rem;
-      args.split_s = plan.s;
-    } else if (plan.s >= 2) {
-      const size_t pb = lin::split_part_bytes(plan, cn, lin::kClusterBN);
-      cudaMemPool_t pool = workspace_pool(dev);
-      if (pool && cudaMallocFromPoolAsync(&ws, pb, pool, stream) == cudaSuccess) {
-        args.part = static_cast<float*>(ws);
-        workspace = pb;
+    const lin::SplitPlan plan = lin::split_plan(num_m * num_ng, cap, nkb);
+    if (plan.s >= 2) {
+      const int got = take_workspace(lin::split_part_bytes(plan, cn, lin::kClusterBN));
+      if (got < 0) return LIN_ERROR_UNSUPPORTED_SHAPE;
+      if (got > 0) {
         args.split_r = plan.r;
         args.split_rem = plan.rem;
         args.split_s = plan.s;
-      } else {
-        cudaGetLastError();
-        if (ws) cudaFreeAsync(ws, stream);
-        ws = nullptr;
       }
     }
     e = swiglu ? lin::launch_gemm_cluster_swiglu(cn, maps, args, stream)
                : lin::launch_gemm_cluster_cvt(cn, resid, maps, args, stream);
     if (e == cudaSuccess && args.split_s >= 2) {
       const int clusters = args.split_r > 0 ? cap : args.split_rem * args.split_s;
-      e = lin::launch_split_reduce(args, resid, cn, clusters, num_ng, stream);
+      e = lin::launch_split_reduce(args, resid, cn, lin::kClusterBN, args.split_r * clusters,
+                                   num_ng, stream);
       kernels = 2;
     }
-    if (ws) {
-      const cudaError_t ef = cudaFreeAsync(ws, stream);
-      if (e == cudaSuccess) e = ef;
-    }
-  } else if (p.w16) {
-    e = lin::launch_gemm_f16(swiglu ? lin::A_SWIGLU_F16 : lin::A_CVT_F16, resid, bn, maps, args,
-                             stream);
   } else {
-    e = lin::launch_gemm_tf32(swiglu ? lin::A_SWIGLU_F32 : lin::A_TMA_F32, resid, bn, maps, args,
-                              stream);
+    // One CTA per 128 x bn tile; when the tiles leave most SMs idle, split K
+    // into S ranges (grid.z) of at least 4 k-blocks each.
+    const int tiles_n = (int)((N + bn - 1) / bn);
+    const int tiles = tiles_n * (int)((M + lin::kBM - 1) / lin::kBM);
+    const int nkb = (int)((K + (p.w16 ? 63 : 31)) / (p.w16 ? 64 : 32));
+    int split = sm_count(dev) / tiles;
+    if (split > nkb / 4) split = nkb / 4;
+    if (split >= 2) {
+      const size_t bytes = (size_t)tiles * split * lin::kBM * bn * sizeof(float);
+      const int got = take_workspace(bytes);
+      if (got < 0) return LIN_ERROR_UNSUPPORTED_SHAPE;
+      if (got > 0) {
+        args.split_r = 0;
+        args.split_rem = tiles;
+        args.split_s = split;
+      }
+    }
+    if (p.w16)
+      e = lin::launch_gemm_f16(swiglu ? lin::A_SWIGLU_F16 : lin::A_CVT_F16, resid, bn, maps, args,
+                               stream);
+    else
+      e = lin::launch_gemm_tf32(swiglu ? lin::A_SWIGLU_F32 : lin::A_TMA_F32, resid, bn, maps,
+                                args, stream);
+    if (e == cudaSuccess && args.split_s >= 2) {
+      e = lin::launch_split_reduce(args, resid, 1, bn, 0, tiles_n, stream);
+      kernels = 2;
+    }
+  }
+  if (ws) {
+    const cudaError_t ef = cudaFreeAsync(ws, stream);
+    if (e == cudaSuccess) e = ef;
   }
   if (e != cudaSuccess) return cuda_fail(e);
   t_last_kernels = kernels;

@@ -71,7 +71,10 @@ struct GemmTraits {
   static constexpr uint32_t RAW_W_BYTES = kXformB ? B_BYTES : 0u;   // [BN/32 runs][32 rows][128 B]
   static constexpr uint32_t RAW_STAGE_BYTES = RAW_A_BYTES + RAW_W_BYTES;
   static constexpr int RAW_PER_KB = kF16 ? BK / 32 : 1;         // raw stages per k-block
-  static constexpr int NR = (kXformA && kXformB) ? 2 : 3;
+  // Both operands transformed (f32 SwiGLU): raw stages (GATE, UP and W of a
+  // k-block, 48 KB) carry the memory latency, operand stages only the local
+  // hand-off, so three raw stages and what is left for operand stages.
+  static constexpr int NR = 3;
 
   static constexpr uint32_t EPI_BUF_BYTES = kEpiRows * kEpiCols * 4;   // 4 KB
   static constexpr uint32_t EPI_BYTES = 4 * 2 * EPI_BUF_BYTES;        // 2 per epilogue warp
@@ -220,7 +223,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int n0 = blockIdx.x * BN;
   const int m0 = blockIdx.y * T::BM;
-  const int nkb = (args.K + T::BK - 1) / T::BK;
+  const int nkb_all = (args.K + T::BK - 1) / T::BK;
+  // Split K (gridDim.z = split_s > 1): this CTA accumulates k-blocks
+  // [kb0, kb0 + nkb) and writes an f32 partial tile to args.part; a second
+  // kernel adds the partials in K order (+ R) into Y.
+  const bool split = gridDim.z > 1;
+  const int kb0 = (int)blockIdx.z * nkb_all / (int)gridDim.z;
+  const int nkb = ((int)blockIdx.z + 1) * nkb_all / (int)gridDim.z - kb0;
   const bool withhold = (args.flags & KFLAG_WITHHOLD_PRODUCER) != 0;
   const WaitCtl ctl{args.timeout_ns, abort_flag, args.status};
 
@@ -278,12 +287,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
           const uint32_t full = bar(T::BAR_OP_TMA + st);
           mbar_arrive_expect_tx(full, T::OP_TMA_BYTES);
-          if constexpr (!T::kXformA) tma_load_2d(a_stage(st), &tm_a, kb * T::BK, m0, full);
+          const int kk = (kb0 + kb) * T::BK;
+          if constexpr (!T::kXformA) tma_load_2d(a_stage(st), &tm_a, kk, m0, full);
           if constexpr (!T::kXformB) {
 #pragma unroll
             for (int j = 0; j < T::W_BOXES; ++j)
-              tma_load_2d(b_stage(st) + j * T::B_ATOM_BYTES, &tm_w, n0 + j * T::W_ATOM,
-                          kb * T::BK, full);
+              tma_load_2d(b_stage(st) + j * T::B_ATOM_BYTES, &tm_w, n0 + j * T::W_ATOM, kk, full);
           }
         }
         __syncwarp();
@@ -338,17 +347,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
           const uint32_t full = bar(T::BAR_RAW_FULL + r);
           mbar_arrive_expect_tx(full, T::RAW_STAGE_BYTES);
+          const int kk = (kb0 * T::RAW_PER_KB + t) * 32;   // f32 column of this raw stage
           if constexpr (T::kXformA) {
-            tma_load_2d(raw_stage(r), &tm_a, t * 32, m0, full);
+            tma_load_2d(raw_stage(r), &tm_a, kk, m0, full);
             if constexpr (T::kSwiglu)
-              tma_load_2d(raw_stage(r) + T::RAW_BOX_BYTES, &tm_u, t * 32, m0, full);
+              tma_load_2d(raw_stage(r) + T::RAW_BOX_BYTES, &tm_u, kk, m0, full);
           }
           if constexpr (T::kXformB) {
             // TF32: one raw stage per k-block (t == kb); W runs of 32 columns
 #pragma unroll
             for (int j = 0; j < BN / 32; ++j)
-              tma_load_2d(raw_stage(r) + T::RAW_A_BYTES + j * 4096, &tm_w, n0 + j * 32, t * 32,
-                          full);
+              tma_load_2d(raw_stage(r) + T::RAW_A_BYTES + j * 4096, &tm_w, n0 + j * 32, kk, full);
           }
         }
         __syncwarp();
@@ -404,16 +413,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Residual tiles are prefetched one chunk ahead; r_issued / r_done count
     // the chunks whose load was issued / waited for (lane 0's view).
     int r_issued = 0, r_done = 0;
-    if (RESID && rows_in && !withhold && lane == 0 && nc > 0) {
+    if (split) {
+      // partial tile of (tile, K range): [BN/4 float4 columns][128 rows]
+      ok = warp_wait_phase(bar(T::BAR_ACC_FULL), 0, ctl);
+      tc_fence_after_sync();
+      if (q == 0 && lane == 0) pdl_launch_dependents();   // the split sum may be scheduled
+      ok = ok && !withhold && (__shfl_sync(0xffffffffu, *abort_flag, 0) == 0);
+      if (ok) {
+        const size_t tile = (size_t)blockIdx.y * gridDim.x + blockIdx.x;
+        float4* part = reinterpret_cast<float4*>(args.part) +
+                       (tile * gridDim.z + blockIdx.z) * (BN / 4) * T::BM + q * kEpiRows + lane;
+        for (int c = 0; c < nc; ++c) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * kEpiCols), v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            part[(size_t)(c * 8 + j) * T::BM] =
+                make_float4(__uint_as_float(v[4 * j + 0]), __uint_as_float(v[4 * j + 1]),
+                            __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+        }
+      }
+      ok = false;   // nothing below: no residual, no store of Y
+    }
+    if (!split && RESID && rows_in && !withhold && lane == 0 && nc > 0) {
       mbar_arrive_expect_tx(ebar0, T::EPI_BUF_BYTES);
       tma_load_2d(buf0, &tm_r, n0, row0, ebar0);
       r_issued = 1;
     }
-    ok = warp_wait_phase(bar(T::BAR_ACC_FULL), 0, ctl);
-    tc_fence_after_sync();
-    // After any role gave up (or in the self-test, whose tensor maps are
-    // empty) the accumulator is not valid: store nothing.
-    ok = ok && !withhold && (__shfl_sync(0xffffffffu, *abort_flag, 0) == 0);
+    if (!split) {
+      ok = warp_wait_phase(bar(T::BAR_ACC_FULL), 0, ctl);
+      tc_fence_after_sync();
+      // After any role gave up (or in the self-test, whose tensor maps are
+      // empty) the accumulator is not valid: store nothing.
+      ok = ok && !withhold && (__shfl_sync(0xffffffffu, *abort_flag, 0) == 0);
+    }
     if (ok && rows_in) {
       for (int c = 0; c < nc; ++c) {
         const int b = c & 1;
@@ -497,7 +531,8 @@ cudaError_t launch_instance(const TensorMaps& m, const KernelArgs& args, cudaStr
     if (e != cudaSuccess) return e;
     attr_done.fetch_or(bit, std::memory_order_acq_rel);
   }
-  dim3 grid((unsigned)((args.N + BN - 1) / BN), (unsigned)((args.M + kBM - 1) / kBM), 1);
+  dim3 grid((unsigned)((args.N + BN - 1) / BN), (unsigned)((args.M + kBM - 1) / kBM),
+            (unsigned)(args.split_s > 1 ? args.split_s : 1));
   if (args.flags & KFLAG_WITHHOLD_PRODUCER) grid = dim3(1, 1, 1);
   kern<<<grid, kThreads, T::SMEM_BYTES, stream>>>(m.a, m.u, m.w, m.r, m.y, args);
   return cudaGetLastError();

@@ -471,13 +471,16 @@ __global__ void __launch_bounds__((8 + LIN_XF_WARPS) * 32, 1)
       if (nc > NC) nc = NC;
       ok = warp_wait_phase(bar(T::BAR_ACC_FULL + ab), (i >> 1) & 1, ctl);
       tc_fence_after_sync();
+      // last item's accumulator complete: a split sum may be scheduled
+      if (i == n_items - 1 && q == 0 && lane == 0) pdl_launch_dependents();
       ok = ok && (__shfl_sync(0xffffffffu, *abort_flag, 0) == 0);
       if (!ok) break;
       const uint32_t acc = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * T::BN);
       const bool row_in = row < args.M;
       float* yrow = args.Y + (size_t)(row_in ? row : 0) * (size_t)args.N;
       const float* rrow = RESID ? args.R + (size_t)(row_in ? row : 0) * (size_t)args.N : nullptr;
-      // partial tile of this unit: [C4 float4 columns][128 rows]
+      // partial tile of this unit: [C4 float4 columns][128 rows], so that the
+      // 32 lanes (rows) of a store write 512 consecutive bytes
       float4* part = is_unit ? reinterpret_cast<float4*>(args.part) +
                                    (size_t)(cid * CN + (int)crank) * C4 * T::BM + q * kEpiRows + lane
                              : nullptr;
@@ -607,11 +610,12 @@ struct ClusterLaunch {
   }
 };
 
-// Sum of a split tail: one thread per float4 of Y. Thread x is float4
-// column c4 = (x / 128) % C4 and row x % 128 of CTA `crank` of tail tile j,
-// x / (128 * C4) = j * CN + crank, the same order as the partial tiles, so
-// consecutive threads read consecutive partial rows. Y = sum over the S K
-// ranges in K order (+ R): independent of timing, so bitwise reproducible.
+// Sum of a split: one thread per float4 of Y. Thread x is row x % 128 of
+// float4 column c4 = (x / 128) % C4 of CTA `crank` of tile j, with
+// x / (128 * C4) = j * cn + crank: the order of the partial tiles
+// [unit][cta][C4][128 rows], so that consecutive threads load consecutive
+// partial float4s. Y = sum over the s K ranges in K order (+ R):
+// independent of timing, so bitwise reproducible.
 template <bool RESID>
 __global__ void __launch_bounds__(256)
     lin_split_reduce_kernel(const float4* __restrict__ part, const float* __restrict__ R,
@@ -629,13 +633,27 @@ __global__ void __launch_bounds__(256)
   const int row = (t / num_ng) * 128 + r;
   const int col = ((t % num_ng) * cn + crank) * bn + 4 * c4;
   if (row >= M || col >= N) return;
+  // Launched as a programmatic dependent of the GEMM: wait here until the
+  // GEMM's partial tiles are complete and visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // Up to 8 partials in flight per thread, added in K order.
+  const float4* src = part + ((long long)(j * s * cn + crank) * c4n + c4) * 128 + r;
+  const long long stride = (long long)cn * c4n * 128;   // next K range
   float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int p = 0; p < s; ++p) {
-    const float4 v = part[((long long)((j * s + p) * cn + crank) * c4n + c4) * 128 + r];
-    sum.x += v.x;
-    sum.y += v.y;
-    sum.z += v.z;
-    sum.w += v.w;
+  for (int p0 = 0; p0 < s; p0 += 8) {
+    float4 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (p0 + i < s) v[i] = __ldcg(src + (p0 + i) * stride);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (p0 + i < s) {
+        sum.x += v[i].x;
+        sum.y += v[i].y;
+        sum.z += v[i].z;
+        sum.w += v[i].w;
+      }
+    }
   }
   const size_t off = (size_t)row * (size_t)N + (size_t)col;
   if constexpr (RESID) {

@@ -103,9 +103,10 @@ cudaError_t launch_gemm_cluster_cvt(int cn, bool resid, const TensorMaps& maps,
 // shared-memory attribute on first use); > 0, or 0 with *err set.
 int cluster_capacity_swiglu(int cn, cudaError_t* err);
 int cluster_capacity_cvt(int cn, bool resid, cudaError_t* err);
-// Y (+ R) from the partial tiles of a split tail: `clusters` is the
-// clustered launch's cluster count, `num_ng` its cluster tiles per row block.
-cudaError_t launch_split_reduce(const KernelArgs& args, bool resid, int cn, int clusters,
+// Y (+ R) from the partial tiles of a split: tiles tile0 .. tile0 +
+// split_rem - 1 of width `bn` (cluster tiles of `cn` CTAs, `num_ng` of them
+// per row block), each summed over its split_s K ranges.
+cudaError_t launch_split_reduce(const KernelArgs& args, bool resid, int cn, int bn, int tile0,
                                 int num_ng, cudaStream_t stream);
 
 // A caller-provided split-tail workspace: returns its base and size on

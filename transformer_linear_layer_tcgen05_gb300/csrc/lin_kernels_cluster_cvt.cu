@@ -43,22 +43,26 @@ int cluster_capacity_cvt(int cn, bool resid, cudaError_t* err) {
   }
 }
 
-cudaError_t launch_split_reduce(const KernelArgs& args, bool resid, int cn, int clusters,
+cudaError_t launch_split_reduce(const KernelArgs& args, bool resid, int cn, int bn, int tile0,
                                 int num_ng, cudaStream_t stream) {
-  const long long threads = (long long)args.split_rem * cn * 128 * (kClusterBN / 4);
-  const unsigned blocks = (unsigned)((threads + 255) / 256);
-  const int tile0 = args.split_r * clusters;
+  const long long threads = (long long)args.split_rem * cn * 128 * (bn / 4);
+  // Programmatic dependent launch: the sum is scheduled while the GEMM still
+  // runs and waits for it in griddepcontrol.wait, hiding the launch gap.
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((threads + 255) / 256), 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   const float4* part = reinterpret_cast<const float4*>(args.part);
   if (resid)
-    lin_split_reduce_kernel<true><<<blocks, 256, 0, stream>>>(part, args.R, args.Y, args.M, args.N,
-                                                             cn, kClusterBN, tile0, num_ng,
-                                                             args.split_rem, args.split_s);
-  else
-    lin_split_reduce_kernel<false><<<blocks, 256, 0, stream>>>(part, args.R, args.Y, args.M,
-                                                              args.N, cn, kClusterBN, tile0,
-                                                              num_ng, args.split_rem,
-                                                              args.split_s);
-  return cudaGetLastError();
+    return cudaLaunchKernelEx(&cfg, lin_split_reduce_kernel<true>, part, args.R, args.Y, args.M,
+                              args.N, cn, bn, tile0, num_ng, args.split_rem, args.split_s);
+  return cudaLaunchKernelEx(&cfg, lin_split_reduce_kernel<false>, part, args.R, args.Y, args.M,
+                            args.N, cn, bn, tile0, num_ng, args.split_rem, args.split_s);
 }
 
 }  // namespace lin

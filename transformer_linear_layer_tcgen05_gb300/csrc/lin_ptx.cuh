@@ -56,6 +56,13 @@ __device__ __forceinline__ float4 ldg_stream_v4f(const float* p) {
   return v;
 }
 
+// Programmatic dependent launch: this CTA lets a dependent grid be
+// scheduled (the dependent still waits for this grid's completion and
+// memory flush in griddepcontrol.wait before it reads anything).
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
   uint32_t v;
   asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
