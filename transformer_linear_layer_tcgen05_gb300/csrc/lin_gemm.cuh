@@ -267,6 +267,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(tmem_slot), T::TMEM_COLS);
     tmem_relinquish_alloc_permit();
   }
+  // Launched as a programmatic dependent: the set-up above overlapped the
+  // previous kernel on the stream; nothing below touches global memory
+  // before that kernel has completed.
+  pdl_wait();
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
@@ -444,6 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!split) {
       ok = warp_wait_phase(bar(T::BAR_ACC_FULL), 0, ctl);
       tc_fence_after_sync();
+      if (q == 0 && lane == 0) pdl_launch_dependents();   // accumulator complete
       // After any role gave up (or in the self-test, whose tensor maps are
       // empty) the accumulator is not valid: store nothing.
       ok = ok && !withhold && (__shfl_sync(0xffffffffu, *abort_flag, 0) == 0);
@@ -534,8 +539,19 @@ cudaError_t launch_instance(const TensorMaps& m, const KernelArgs& args, cudaStr
   dim3 grid((unsigned)((args.N + BN - 1) / BN), (unsigned)((args.M + kBM - 1) / kBM),
             (unsigned)(args.split_s > 1 ? args.split_s : 1));
   if (args.flags & KFLAG_WITHHOLD_PRODUCER) grid = dim3(1, 1, 1);
-  kern<<<grid, kThreads, T::SMEM_BYTES, stream>>>(m.a, m.u, m.w, m.r, m.y, args);
-  return cudaGetLastError();
+  // A programmatic dependent of the previous kernel on the stream (the
+  // kernel waits for it in griddepcontrol.wait after its set-up).
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = T::SMEM_BYTES;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, m.a, m.u, m.w, m.r, m.y, args);
 }
 
 }  // namespace lin

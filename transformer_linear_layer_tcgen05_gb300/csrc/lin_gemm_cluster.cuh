@@ -268,6 +268,10 @@ __global__ void __launch_bounds__((8 + LIN_XF_WARPS) * 32, 1)
     tmem_alloc(smem_u32(tmem_slot), T::TMEM_COLS);
     tmem_relinquish_alloc_permit();
   }
+  // Launched as a programmatic dependent: the set-up above overlapped the
+  // previous kernel on the stream; nothing below touches global memory
+  // before that kernel has completed.
+  pdl_wait();
   tc_fence_before_sync();
   // Peers may arrive on our barriers and write our A stages only after every
   // CTA of the cluster initialised them.
@@ -546,17 +550,22 @@ __global__ void __launch_bounds__((8 + LIN_XF_WARPS) * 32, 1)
 template <int AMODE, bool RESID, int BN, int CN>
 struct ClusterLaunch {
   using T = ClusterTraits<AMODE, RESID, BN, CN>;
-  static cudaLaunchConfig_t config(cudaLaunchAttribute* attr, cudaStream_t stream) {
+  // attr must hold 2 entries: the cluster shape and, for launches, the
+  // programmatic dependence on the previous kernel of the stream.
+  static cudaLaunchConfig_t config(cudaLaunchAttribute* attr, cudaStream_t stream,
+                                   bool dependent) {
     cudaLaunchConfig_t cfg = {};
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = CN;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.blockDim = dim3(T::kThreadsC, 1, 1);
     cfg.dynamicSmemBytes = T::SMEM_BYTES;
     cfg.stream = stream;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = dependent ? 2 : 1;
     return cfg;
   }
   // Clusters resident at once on the current device (> 0), or 0 with *err.
@@ -574,8 +583,8 @@ struct ClusterLaunch {
     const uint64_t bit = uint64_t{1} << dev;
     if (!(attr_done.load(std::memory_order_acquire) & bit)) {
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
-      cudaLaunchAttribute attr[1];
-      cudaLaunchConfig_t cfg = config(attr, nullptr);
+      cudaLaunchAttribute attr[2];
+      cudaLaunchConfig_t cfg = config(attr, nullptr, false);
       cfg.gridDim = dim3(CN, 1, 1);
       int n = 0;
       if (e == cudaSuccess) e = cudaOccupancyMaxActiveClusters(&n, (void*)kern, &cfg);
@@ -603,8 +612,8 @@ struct ClusterLaunch {
     else
       clusters = num_m * num_ng < cap ? num_m * num_ng : cap;
     if (clusters > cap) return cudaErrorInvalidConfiguration;
-    cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = config(attr, stream);
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = config(attr, stream, true);
     cfg.gridDim = dim3((unsigned)(clusters * CN), 1, 1);
     return cudaLaunchKernelEx(&cfg, lin_gemm_cluster_kernel<AMODE, RESID, BN, CN>, m.w, args);
   }
@@ -632,10 +641,13 @@ __global__ void __launch_bounds__(256)
   const int t = tile0 + j;
   const int row = (t / num_ng) * 128 + r;
   const int col = ((t % num_ng) * cn + crank) * bn + 4 * c4;
+  // The next kernel on the stream may be scheduled now: it waits for this
+  // grid's completion itself before it touches memory.
+  pdl_launch_dependents();
   if (row >= M || col >= N) return;
   // Launched as a programmatic dependent of the GEMM: wait here until the
   // GEMM's partial tiles are complete and visible.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  pdl_wait();
   // Up to 8 partials in flight per thread, added in K order.
   const float4* src = part + ((long long)(j * s * cn + crank) * c4n + c4) * 128 + r;
   const long long stride = (long long)cn * c4n * 128;   // next K range
