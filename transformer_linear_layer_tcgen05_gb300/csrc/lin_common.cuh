@@ -88,18 +88,14 @@ __device__ __forceinline__ float silu_stable(float x) {
   return x * __fdividef(num, 1.0f + e);
 }
 
-// Same function with one MUFU operation per element: exp(-|x|) by ex2, and
-// the reciprocal of d = 1 + exp(-|x|), which lies in [1, 2], by Newton-Raphson
-// on the FMA pipe from the linear minimax start 24/17 - (8/17) d (relative
-// error <= 1/17; each step squares it: two steps give <= 1.2e-5).
+// Same function in six instructions: exp(-|x|) by the hardware ex2, and the
+// reciprocal of d = 1 + exp(-|x|), which lies in [1, 2], by the hardware
+// reciprocal approximation (about 1 ulp there). Measured faster than a
+// Newton-Raphson reciprocal on the FMA pipe, which needs five instructions
+// more per element.
 __device__ __forceinline__ float silu_stable_fast(float x) {
   const float e = ex2_approx(fabsf(x) * -1.4426950408889634f);   // exp(-|x|)
-  const float d = 1.0f + e;
-  float r = fmaf(d, -8.0f / 17.0f, 24.0f / 17.0f);
-  float t = fmaf(-d, r, 1.0f);
-  r = fmaf(r, t, r);
-  t = fmaf(-d, r, 1.0f);
-  r = fmaf(r, t, r);
+  const float r = rcp_approx(1.0f + e);
   const float num = x >= 0.0f ? 1.0f : e;
   return x * (num * r);
 }

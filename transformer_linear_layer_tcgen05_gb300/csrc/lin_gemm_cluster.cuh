@@ -81,7 +81,10 @@ struct ClusterTraits {
   static constexpr int LPI = RW / 2;
   static constexpr int LOADS = INPUTS * LPI;      // float4 registers per lane per k-block
   // Register prefetch depth, in the group's own k-blocks: as many as fit in
-  // 64 registers of staged input per lane.
+  // 64 registers of staged input per lane. (Moving registers from the other
+  // warpgroups to the transform with setmaxnreg, for twice the depth,
+  // measured slower: the loads are bound by the L1 request path, not by
+  // their latency.)
   static constexpr int PF = LOADS >= 16 ? 1 : (LOADS >= 8 ? 2 : 4);
 
   static constexpr uint32_t A_BYTES = BM * 128;

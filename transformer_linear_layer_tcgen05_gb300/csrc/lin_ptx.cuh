@@ -29,6 +29,14 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// Hardware reciprocal approximation (relative error about 1 ulp); used on
+// arguments in [1, 2].
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
