@@ -337,6 +337,10 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
   args.split_r = 0;
   args.split_rem = 0;
   args.split_s = 1;
+  // 32-byte loads of the A-side inputs when every row start allows them
+  auto align32 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 31u) == 0; };
+  if (cn > 0 && K % 8 == 0 && align32(a_src) && (!swiglu || align32(p.U)))
+    args.flags |= lin::KFLAG_A_V8;
 
   // Workspace for f32 partial tiles of a split (either kernel): the caller's
   // fixed workspace, or a stream-ordered allocation freed on the same stream

@@ -48,7 +48,7 @@
 
 namespace lin {
 
-template <int AMODE, bool RESID, int BN_, int CN_>
+template <int AMODE, bool RESID, int BN_, int CN_, bool V8_ = false>
 struct ClusterTraits {
   static_assert(AMODE == A_CVT_F16 || AMODE == A_SWIGLU_F16, "binary16 forms only");
   static constexpr bool kSwiglu = (AMODE == A_SWIGLU_F16);
@@ -76,10 +76,16 @@ struct ClusterTraits {
   static constexpr uint32_t SLICE_BYTES = RW * 128;
   static constexpr uint32_t REMOTE_BYTES_PER_WARP = SLICE_BYTES * (CN - 1);
 
-  // A warp's 16-byte loads cover two rows of a 64-wide k-block at a time
-  // (lanes 0-15 one row, 16-31 the next): LPI loads per input and lane.
-  static constexpr int LPI = RW / 2;
-  static constexpr int LOADS = INPUTS * LPI;      // float4 registers per lane per k-block
+  // A lane loads CHUNK consecutive f32 of one row per instruction: 4 (16-byte
+  // loads) or, when the inputs allow 32-byte loads, 8, which make one
+  // 16-byte binary16 chunk of the A row. A warp instruction covers
+  // ROWS_PER_LOAD rows of a 64-wide k-block: LPI loads per input and lane.
+  static constexpr bool V8 = V8_;
+  static constexpr int CHUNK = V8 ? 8 : 4;
+  static constexpr int LANES_PER_ROW = 64 / CHUNK;
+  static constexpr int ROWS_PER_LOAD = 32 / LANES_PER_ROW;
+  static constexpr int LPI = RW / ROWS_PER_LOAD;
+  static constexpr int LOADS = INPUTS * LPI * (CHUNK / 4);   // float4 registers per lane per k-block
   // Register prefetch depth, in the group's own k-blocks: as many as fit in
   // 64 registers of staged input per lane. (Moving registers from the other
   // warpgroups to the transform with setmaxnreg, for twice the depth,
@@ -126,7 +132,8 @@ struct ClusterTraits {
 
   static_assert(CN == 1 || CN == 2 || CN == 4 || CN == 8, "cluster size");
   static_assert(XF_WARPS == 4 || XF_WARPS == 8, "transform warps");
-  static_assert(XF_WARPS % XF_GROUPS == 0 && ROWS % XF_PER_GROUP == 0 && RW % 2 == 0,
+  static_assert(XF_WARPS % XF_GROUPS == 0 && ROWS % XF_PER_GROUP == 0 &&
+                    RW % ROWS_PER_LOAD == 0,
                 "transform groups");
   static_assert(LOADS <= 16, "staged input per lane");
   // A parity wait is only sound for a waiter at most one phase ahead: a group
@@ -145,68 +152,89 @@ struct ClusterTraits {
 };
 
 // Register-staged inputs of one k-block for one transform lane: load q of
-// input i is row (tw*RW + 2q + lane/16) of this CTA's slice, columns
-// k0 + 4*(lane%16) .. +3. Rows at or past M and columns at or past K read as
-// zero (K is a multiple of 4, so a 16-byte load is wholly in or out).
+// input i is row (tw*RW + q*ROWS_PER_LOAD + lane/LANES_PER_ROW) of this
+// CTA's slice, columns k0 + CHUNK*(lane%LANES_PER_ROW) onwards. Rows at or
+// past M and columns at or past K read as zero (K is a multiple of CHUNK on
+// each path, so a load is wholly in or out).
 template <typename T>
 struct Staged {
-  float4 v[T::INPUTS][T::LPI];
+  float4 v[T::INPUTS][T::LPI][T::CHUNK / 4];
 };
 
 template <typename T>
 __device__ __forceinline__ void stage_load(Staged<T>& st, const float* __restrict__ a,
                                            const float* __restrict__ u, int row0, int k0,
                                            int M, int K, int tw, int lane) {
-  const int col = k0 + 4 * (lane & 15);
+  const int col = k0 + T::CHUNK * (lane % T::LANES_PER_ROW);
   const bool col_in = col < K;
+  const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
   for (int q = 0; q < T::LPI; ++q) {
-    const int row = row0 + tw * T::RW + 2 * q + (lane >> 4);
+    const int row = row0 + tw * T::RW + q * T::ROWS_PER_LOAD + lane / T::LANES_PER_ROW;
     const bool in = col_in && row < M;
     const size_t off = (size_t)(in ? row : 0) * (size_t)K + (size_t)(in ? col : 0);
-    st.v[0][q] = in ? ldg_stream_v4f(a + off) : make_float4(0.f, 0.f, 0.f, 0.f);
-    if constexpr (T::kSwiglu)
-      st.v[1][q] = in ? ldg_stream_v4f(u + off) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < T::INPUTS; ++i) {
+      const float* src = (i == 0 ? a : u) + off;
+      if constexpr (T::V8) {
+        if (in)
+          ldg_stream_v8f(src, st.v[i][q][0], st.v[i][q][1]);
+        else
+          st.v[i][q][0] = st.v[i][q][1] = zero;
+      } else {
+        st.v[i][q][0] = in ? ldg_stream_v4f(src) : zero;
+      }
+    }
   }
 }
 
-// A values of the staged k-block, binary16 pairs: out[q] = 4 consecutive k.
+// A values of the staged k-block as binary16 pairs: out[q] holds CHUNK
+// consecutive k (CHUNK/2 words).
 template <typename T>
-__device__ __forceinline__ void stage_compute(const Staged<T>& st, uint32_t (&out)[T::LPI][2]) {
+__device__ __forceinline__ void stage_compute(const Staged<T>& st,
+                                              uint32_t (&out)[T::LPI][T::CHUNK / 2]) {
 #pragma unroll
   for (int q = 0; q < T::LPI; ++q) {
-    float4 a = st.v[0][q];
-    if constexpr (T::kSwiglu) {
-      const float4 u = st.v[1][q];
-      a.x = silu_stable_fast(a.x) * u.x;
-      a.y = silu_stable_fast(a.y) * u.y;
-      a.z = silu_stable_fast(a.z) * u.z;
-      a.w = silu_stable_fast(a.w) * u.w;
+#pragma unroll
+    for (int h = 0; h < T::CHUNK / 4; ++h) {
+      float4 a = st.v[0][q][h];
+      if constexpr (T::kSwiglu) {
+        const float4 u = st.v[1][q][h];
+        a.x = silu_stable_fast(a.x) * u.x;
+        a.y = silu_stable_fast(a.y) * u.y;
+        a.z = silu_stable_fast(a.z) * u.z;
+        a.w = silu_stable_fast(a.w) * u.w;
+      }
+      out[q][2 * h] = pack_half2(a.x, a.y);
+      out[q][2 * h + 1] = pack_half2(a.z, a.w);
     }
-    out[q][0] = pack_half2(a.x, a.y);
-    out[q][1] = pack_half2(a.z, a.w);
   }
 }
 
-// Into the A stage (128 rows x 128 bytes, 128-byte swizzle): this CTA's
-// slice starts at row crank*ROWS; lane%16 is the 8-byte quarter-pair of the
-// row, so 16 lanes fill one row and a warp's store covers two whole rows
-// (every bank twice, the minimum for 256 bytes).
+// Into the A stage (128 rows x 128 bytes, 128-byte swizzle); this CTA's
+// slice starts at row crank*ROWS. With 32-byte loads a lane stores one whole
+// 16-byte chunk and a warp covers four rows; with 16-byte loads it stores
+// half a chunk (lane%16 is the 8-byte quarter-pair) and a warp covers two
+// rows. Either way each row's bytes spread over all 32 banks once.
 template <typename T>
 __device__ __forceinline__ void stage_store(uint32_t a_stage, uint32_t crank, int tw, int lane,
-                                            const uint32_t (&out)[T::LPI][2]) {
-  const uint32_t c4 = (uint32_t)(lane & 15);
+                                            const uint32_t (&out)[T::LPI][T::CHUNK / 2]) {
+  const uint32_t c = (uint32_t)(lane % T::LANES_PER_ROW);
 #pragma unroll
   for (int q = 0; q < T::LPI; ++q) {
-    const uint32_t r = crank * (uint32_t)T::ROWS + (uint32_t)(tw * T::RW + 2 * q + (lane >> 4));
-    st_shared_v2(a_stage + sw128(r, c4 >> 1) + (c4 & 1u) * 8u, out[q][0], out[q][1]);
+    const uint32_t r = crank * (uint32_t)T::ROWS +
+                       (uint32_t)(tw * T::RW + q * T::ROWS_PER_LOAD + lane / T::LANES_PER_ROW);
+    if constexpr (T::V8)
+      st_shared_v4(a_stage + sw128(r, c), out[q][0], out[q][1], out[q][2], out[q][3]);
+    else
+      st_shared_v2(a_stage + sw128(r, c >> 1) + (c & 1u) * 8u, out[q][0], out[q][1]);
   }
 }
 
-template <int AMODE, bool RESID, int BN, int CN>
+template <int AMODE, bool RESID, int BN, int CN, bool V8>
 __global__ void __launch_bounds__((8 + LIN_XF_WARPS) * 32, 1)
     lin_gemm_cluster_kernel(const __grid_constant__ CUtensorMap tm_w, const KernelArgs args) {
-  using T = ClusterTraits<AMODE, RESID, BN, CN>;
+  using T = ClusterTraits<AMODE, RESID, BN, CN, V8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -415,7 +443,7 @@ __global__ void __launch_bounds__((8 + LIN_XF_WARPS) * 32, 1)
       for (int d = 0; d < T::PF; ++d) {
         const int g = grp + T::XF_GROUPS * (j0 + d);
         if (g >= total) break;
-        uint32_t vals[T::LPI][2];
+        uint32_t vals[T::LPI][T::CHUNK / 2];
         stage_compute<T>(buf[d], vals);
         const int gn = g + T::XF_GROUPS * T::PF;
         if (gn < total) {
@@ -575,7 +603,8 @@ struct ClusterLaunch {
   static int capacity(cudaError_t* err) {
     static std::atomic<uint64_t> attr_done{0};
     static std::atomic<int> max_clusters[64];
-    auto kern = lin_gemm_cluster_kernel<AMODE, RESID, BN, CN>;
+    auto kern = lin_gemm_cluster_kernel<AMODE, RESID, BN, CN, false>;
+    auto kern8 = lin_gemm_cluster_kernel<AMODE, RESID, BN, CN, true>;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess && dev >= 64) e = cudaErrorInvalidDevice;
@@ -586,6 +615,9 @@ struct ClusterLaunch {
     const uint64_t bit = uint64_t{1} << dev;
     if (!(attr_done.load(std::memory_order_acquire) & bit)) {
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(kern8, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 ClusterTraits<AMODE, RESID, BN, CN, true>::SMEM_BYTES);
       cudaLaunchAttribute attr[2];
       cudaLaunchConfig_t cfg = config(attr, nullptr, false);
       cfg.gridDim = dim3(CN, 1, 1);
@@ -618,7 +650,10 @@ struct ClusterLaunch {
     cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = config(attr, stream, true);
     cfg.gridDim = dim3((unsigned)(clusters * CN), 1, 1);
-    return cudaLaunchKernelEx(&cfg, lin_gemm_cluster_kernel<AMODE, RESID, BN, CN>, m.w, args);
+    if (args.flags & KFLAG_A_V8)
+      return cudaLaunchKernelEx(&cfg, lin_gemm_cluster_kernel<AMODE, RESID, BN, CN, true>, m.w,
+                                args);
+    return cudaLaunchKernelEx(&cfg, lin_gemm_cluster_kernel<AMODE, RESID, BN, CN, false>, m.w, args);
   }
 };
 

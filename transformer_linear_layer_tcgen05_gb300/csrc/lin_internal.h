@@ -23,6 +23,9 @@ enum : uint32_t {
   // Self-test only: the TMA producers issue nothing, so every consumer wait
   // must run out and the kernel must leave through its timeout path.
   KFLAG_WITHHOLD_PRODUCER = 1u << 0,
+  // The A-side inputs (X, or GATE and UP) allow 32-byte loads: K % 8 == 0
+  // and every base 32-byte aligned (clustered kernels).
+  KFLAG_A_V8 = 1u << 1,
 };
 
 // Device status word values (mirror lin_status).

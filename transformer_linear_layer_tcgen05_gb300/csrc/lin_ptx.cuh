@@ -76,6 +76,15 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 // the grid was launched without the attribute).
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// 32-byte load of read-only global data used once by this SM (the address
+// must be 32-byte aligned); same placement rules as ldg_stream_v4f.
+__device__ __forceinline__ void ldg_stream_v8f(const float* p, float4& lo, float4& hi) {
+  asm volatile("ld.global.nc.L1::no_allocate.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=f"(lo.x), "=f"(lo.y), "=f"(lo.z), "=f"(lo.w), "=f"(hi.x), "=f"(hi.y),
+                 "=f"(hi.z), "=f"(hi.w)
+               : "l"(p));
+}
+
 __device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
   uint32_t v;
   asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
