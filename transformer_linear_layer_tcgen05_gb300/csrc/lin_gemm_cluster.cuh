@@ -68,7 +68,7 @@ struct ClusterTraits {
   // copy issue) is spread over XF_GROUPS k-blocks of UMMA time. A single CTA
   // transforming all 128 rows of the SwiGLU form keeps one group, so that a
   // warp's share of a k-block still fits its registers.
-  static constexpr int XF_GROUPS = (kSwiglu && CN == 1) ? 1 : 2;
+  static constexpr int XF_GROUPS = (kSwiglu && CN == 1) ? 1 : XF_WARPS / 4;
   static constexpr int XF_PER_GROUP = XF_WARPS / XF_GROUPS;
   static constexpr int RW = ROWS / XF_PER_GROUP;  // A rows per transform warp (contiguous)
   // Each transform warp bulk-copies its RW rows of a stage to every peer as
@@ -87,11 +87,13 @@ struct ClusterTraits {
   static constexpr int LPI = RW / ROWS_PER_LOAD;
   static constexpr int LOADS = INPUTS * LPI * (CHUNK / 4);   // float4 registers per lane per k-block
   // Register prefetch depth, in the group's own k-blocks: as many as fit in
-  // 64 registers of staged input per lane. (Moving registers from the other
-  // warpgroups to the transform with setmaxnreg, for twice the depth,
-  // measured slower: the loads are bound by the L1 request path, not by
-  // their latency.)
-  static constexpr int PF = LOADS >= 16 ? 1 : (LOADS >= 8 ? 2 : 4);
+  // the registers a lane can give to staged input (64 with 16 warps).
+  // Measured and left out: twice the depth (registers moved from the other
+  // warpgroups with setmaxnreg), twelve transform warps in three groups, and
+  // GATE/UP resident in L2 all left the time of the loads unchanged.
+  static constexpr int STAGE_REGS = XF_WARPS > 8 ? 32 : 64;   // per lane, for staged input
+  static constexpr int PF_FIT = STAGE_REGS / (4 * LOADS);
+  static constexpr int PF = PF_FIT < 1 ? 1 : (PF_FIT > 4 ? 4 : PF_FIT);
 
   static constexpr uint32_t A_BYTES = BM * 128;
   static constexpr uint32_t B_ATOM_BYTES = BK * 128;
@@ -131,7 +133,7 @@ struct ClusterTraits {
   static constexpr int kThreadsC = (8 + XF_WARPS) * 32;
 
   static_assert(CN == 1 || CN == 2 || CN == 4 || CN == 8, "cluster size");
-  static_assert(XF_WARPS == 4 || XF_WARPS == 8, "transform warps");
+  static_assert(XF_WARPS == 4 || XF_WARPS == 8 || XF_WARPS == 12, "transform warps");
   static_assert(XF_WARPS % XF_GROUPS == 0 && ROWS % XF_PER_GROUP == 0 &&
                     RW % ROWS_PER_LOAD == 0,
                 "transform groups");
@@ -232,7 +234,7 @@ __device__ __forceinline__ void stage_store(uint32_t a_stage, uint32_t crank, in
 }
 
 template <int AMODE, bool RESID, int BN, int CN, bool V8>
-__global__ void __launch_bounds__((8 + LIN_XF_WARPS) * 32, 1)
+__global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8>::kThreadsC, 1)
     lin_gemm_cluster_kernel(const __grid_constant__ CUtensorMap tm_w, const KernelArgs args) {
   using T = ClusterTraits<AMODE, RESID, BN, CN, V8>;
   extern __shared__ uint8_t smem_raw[];
