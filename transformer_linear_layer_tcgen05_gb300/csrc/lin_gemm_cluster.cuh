@@ -112,18 +112,27 @@ struct ClusterTraits {
   static constexpr uint32_t BAR_REGION = 1024;
   static constexpr uint32_t ALIGN_SLACK = 1024;
   static constexpr uint32_t DATA_CAP = SMEM_CAP - BAR_REGION - ALIGN_SLACK;
-  static constexpr int NS_FIT = (int)(DATA_CAP / OP_STAGE_BYTES);
+  static constexpr int NS_FIT = (int)((DATA_CAP - 4 * 2 * kEpiRows * kEpiCols * 4) / OP_STAGE_BYTES);
   static constexpr int NS = NS_FIT > 8 ? 8 : NS_FIT;
 
+  // Epilogue staging: two [32 rows][32 f32] swizzled buffers per epilogue
+  // warp. R arrives in them by TMA, the accumulator is added in place and Y
+  // leaves by TMA store, so that the epilogue moves whole 128-byte lines
+  // instead of one 16-byte piece per row and lane.
+  static constexpr uint32_t EPI_BUF_BYTES = kEpiRows * kEpiCols * 4;   // 4 KB
+  static constexpr uint32_t EPI_BYTES = 4 * 2 * EPI_BUF_BYTES;
+
   static constexpr uint32_t OFF_OP = 0;
-  static constexpr uint32_t OFF_BAR = NS * OP_STAGE_BYTES;
+  static constexpr uint32_t OFF_EPI = NS * OP_STAGE_BYTES;
+  static constexpr uint32_t OFF_BAR = OFF_EPI + EPI_BYTES;
   static constexpr uint32_t SMEM_BYTES = ALIGN_SLACK + OFF_BAR + BAR_REGION;
 
   static constexpr int BAR_FULL = 0;
   static constexpr int BAR_EMPTY = BAR_FULL + 8;         // every CTA's UMMA done with stage
   static constexpr int BAR_ACC_FULL = BAR_EMPTY + 8;     // 2 accumulator buffers
   static constexpr int BAR_ACC_EMPTY = BAR_ACC_FULL + 2;
-  static constexpr int BAR_COUNT = BAR_ACC_EMPTY + 2;
+  static constexpr int BAR_EPI = BAR_ACC_EMPTY + 2;      // R landed, 2 per epilogue warp
+  static constexpr int BAR_COUNT = BAR_EPI + 8;
   static constexpr uint32_t OFF_TMEM_SLOT = BAR_COUNT * 8;
   static constexpr uint32_t OFF_ABORT = OFF_TMEM_SLOT + 4;
 
@@ -235,7 +244,9 @@ __device__ __forceinline__ void stage_store(uint32_t a_stage, uint32_t crank, in
 
 template <int AMODE, bool RESID, int BN, int CN, bool V8>
 __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8>::kThreadsC, 1)
-    lin_gemm_cluster_kernel(const __grid_constant__ CUtensorMap tm_w, const KernelArgs args) {
+    lin_gemm_cluster_kernel(const __grid_constant__ CUtensorMap tm_w,
+                            const __grid_constant__ CUtensorMap tm_r,
+                            const __grid_constant__ CUtensorMap tm_y, const KernelArgs args) {
   using T = ClusterTraits<AMODE, RESID, BN, CN, V8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -290,12 +301,17 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8>::kThre
       mbar_init(bar(T::BAR_ACC_FULL + b), 1);
       mbar_init(bar(T::BAR_ACC_EMPTY + b), 4);
     }
+    for (int e = 0; e < 8; ++e) mbar_init(bar(T::BAR_EPI + e), 1);
     *abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
   }
   __syncwarp();
-  if (warp == 0 && lane == 0) tma_prefetch_desc(&tm_w);
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_w);
+    if constexpr (RESID) tma_prefetch_desc(&tm_r);
+    tma_prefetch_desc(&tm_y);
+  }
   __syncwarp();
   if (warp == 2) {
     tmem_alloc(smem_u32(tmem_slot), T::TMEM_COLS);
@@ -493,19 +509,37 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8>::kThre
         wait_phase_cluster(bar(T::BAR_EMPTY + x % T::NS), (x / T::NS) & 1, ctl, false);
     __syncwarp();
   } else if (warp >= 4 + T::XF_WARPS) {
-    // ---------------- epilogue warps: lane = one output row of the tile
+    // ---------------- epilogue warps: rows q*32 .. q*32+31 of the tile
     const int q = warp & 3;                        // TMEM lane quadrant
     constexpr int NC = T::BN / kEpiCols;
     constexpr int C4 = T::BN / 4;                  // float4 columns of a tile
+    const uint32_t buf0 = sbase + T::OFF_EPI + (uint32_t)(q * 2) * T::EPI_BUF_BYTES;
+    auto buf = [&](uint32_t b) -> uint32_t { return buf0 + b * T::EPI_BUF_BYTES; };
+    auto ebar = [&](uint32_t b) -> uint32_t { return bar(T::BAR_EPI + q * 2 + (int)b); };
+    // Chunks of 32 columns this warp has staged so far (across tiles): chunk
+    // e uses buffer e & 1 and, for R, phase (e >> 1) & 1 of that buffer's
+    // barrier. R loads are issued and waited for in chunk order: r_issued /
+    // r_done count them, e_wait is the chunk of the next one to wait for.
+    uint32_t ec = 0, r_issued = 0, r_done = 0, e_wait = 0;
     bool ok = true;
     for (int i = 0; i < n_items && ok; ++i) {
       const int t = item_tile(i);
       const bool is_unit = i >= n_full;            // a K range of a split tail tile
       const int ab = i & 1;
-      const int row = tile_m0(t) + q * kEpiRows + lane;
+      const int row0 = tile_m0(t) + q * kEpiRows;
       const int n0 = tile_n0(t);
       int nc = n0 < args.N ? (args.N - n0 + kEpiCols - 1) / kEpiCols : 0;
       if (nc > NC) nc = NC;
+      // rows wholly past M: nothing to store (a store box may not start there)
+      const bool rows_in = row0 < args.M;
+      const bool staged = !is_unit && rows_in && nc > 0;
+      if (RESID && staged && lane == 0) {
+        // R of the first chunk, into a buffer whose last store has read it
+        bulk_wait_group_read<0>();
+        mbar_arrive_expect_tx(ebar(ec & 1), T::EPI_BUF_BYTES);
+        tma_load_2d(buf(ec & 1), &tm_r, n0, row0, ebar(ec & 1));
+        ++r_issued;
+      }
       ok = warp_wait_phase(bar(T::BAR_ACC_FULL + ab), (i >> 1) & 1, ctl);
       tc_fence_after_sync();
       // last item's accumulator complete: a split sum may be scheduled
@@ -513,55 +547,90 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8>::kThre
       ok = ok && (__shfl_sync(0xffffffffu, *abort_flag, 0) == 0);
       if (!ok) break;
       const uint32_t acc = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * T::BN);
-      const bool row_in = row < args.M;
-      float* yrow = args.Y + (size_t)(row_in ? row : 0) * (size_t)args.N;
-      const float* rrow = RESID ? args.R + (size_t)(row_in ? row : 0) * (size_t)args.N : nullptr;
-      // partial tile of this unit: [C4 float4 columns][128 rows], so that the
-      // 32 lanes (rows) of a store write 512 consecutive bytes
-      float4* part = is_unit ? reinterpret_cast<float4*>(args.part) +
-                                   (size_t)(cid * CN + (int)crank) * C4 * T::BM + q * kEpiRows + lane
-                             : nullptr;
-      for (int c = 0; c < nc; ++c) {
-        const int col0 = n0 + c * kEpiCols;
-        float4 rr[8];
-        if constexpr (RESID) {
-          if (!is_unit) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              rr[j] = (row_in && col0 + 4 * j < args.N)
-                          ? __ldg(reinterpret_cast<const float4*>(rrow + col0 + 4 * j))
-                          : make_float4(0.f, 0.f, 0.f, 0.f);
-          }
-        }
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(acc + (uint32_t)(c * kEpiCols), v);
-        tmem_wait_ld();
-        if (is_unit) {
+      if (is_unit) {
+        // partial tile of this unit: [C4 float4 columns][128 rows], so that
+        // the 32 lanes (rows) of a store write 512 consecutive bytes
+        float4* part = reinterpret_cast<float4*>(args.part) +
+                       (size_t)(cid * CN + (int)crank) * C4 * T::BM + q * kEpiRows + lane;
+        for (int c = 0; c < nc; ++c) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(acc + (uint32_t)(c * kEpiCols), v);
+          tmem_wait_ld();
 #pragma unroll
           for (int j = 0; j < 8; ++j)
             part[(size_t)(c * 8 + j) * T::BM] =
                 make_float4(__uint_as_float(v[4 * j + 0]), __uint_as_float(v[4 * j + 1]),
                             __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
-        } else if (row_in) {
+        }
+      } else if (staged) {
+        for (int c = 0; c < nc && ok; ++c) {
+          const uint32_t e = ec + (uint32_t)c;
+          const uint32_t b = e & 1u;
+          if (lane == 0 && c + 1 < nc) {
+            // the other buffer's last store must have read it before it is
+            // refilled (or, without R, rewritten below)
+            bulk_wait_group_read<0>();
+            if constexpr (RESID) {
+              mbar_arrive_expect_tx(ebar(b ^ 1u), T::EPI_BUF_BYTES);
+              tma_load_2d(buf(b ^ 1u), &tm_r, n0 + (c + 1) * kEpiCols, row0, ebar(b ^ 1u));
+              ++r_issued;
+            }
+          }
+          __syncwarp();
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(acc + (uint32_t)(c * kEpiCols), v);
+          tmem_wait_ld();
+          if constexpr (RESID) {
+            if (!warp_wait_phase(ebar(b), (e >> 1) & 1u, ctl)) {
+              ok = false;
+              break;
+            }
+            ++r_done;
+            e_wait = e + 1;
+          } else if (c == 0 && lane == 0) {
+            bulk_wait_group_read<0>();   // this buffer's last store has read it
+          }
+          __syncwarp();
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            if (col0 + 4 * j >= args.N) break;
-            float4 o = make_float4(__uint_as_float(v[4 * j + 0]), __uint_as_float(v[4 * j + 1]),
-                                   __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+            const uint32_t addr = buf(b) + sw128((uint32_t)lane, (uint32_t)j);
+            float o0 = __uint_as_float(v[4 * j + 0]);
+            float o1 = __uint_as_float(v[4 * j + 1]);
+            float o2 = __uint_as_float(v[4 * j + 2]);
+            float o3 = __uint_as_float(v[4 * j + 3]);
             if constexpr (RESID) {
-              o.x += rr[j].x;
-              o.y += rr[j].y;
-              o.z += rr[j].z;
-              o.w += rr[j].w;
+              const float4 rr = ld_shared_v4f(addr);
+              o0 += rr.x;
+              o1 += rr.y;
+              o2 += rr.z;
+              o3 += rr.w;
             }
-            *reinterpret_cast<float4*>(yrow + col0 + 4 * j) = o;
+            st_shared_v4(addr, __float_as_uint(o0), __float_as_uint(o1), __float_as_uint(o2),
+                         __float_as_uint(o3));
           }
+          fence_proxy_async_smem();   // staged Y -> visible to the TMA store
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tm_y, n0 + c * kEpiCols, row0, buf(b));
+            bulk_commit_group();
+          }
+          __syncwarp();
         }
+        ec += (uint32_t)nc;
       }
       // TMEM reads of this buffer are complete: hand it back to the UMMA warp.
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(T::BAR_ACC_EMPTY + ab));
+    }
+    if (lane == 0) {
+      // Never leave with an R load in flight (only possible when a wait gave
+      // up) or with a store still reading the buffers or writing Y.
+      for (uint32_t x = 0; x < r_issued - r_done; ++x) {
+        const uint32_t e = e_wait + x;   // the outstanding loads, oldest first
+        wait_phase(ebar(e & 1u), (e >> 1) & 1u, ctl, false);
+      }
+      bulk_wait_group_all();
     }
     __syncwarp();
   }
@@ -654,8 +723,9 @@ struct ClusterLaunch {
     cfg.gridDim = dim3((unsigned)(clusters * CN), 1, 1);
     if (args.flags & KFLAG_A_V8)
       return cudaLaunchKernelEx(&cfg, lin_gemm_cluster_kernel<AMODE, RESID, BN, CN, true>, m.w,
-                                args);
-    return cudaLaunchKernelEx(&cfg, lin_gemm_cluster_kernel<AMODE, RESID, BN, CN, false>, m.w, args);
+                                m.r, m.y, args);
+    return cudaLaunchKernelEx(&cfg, lin_gemm_cluster_kernel<AMODE, RESID, BN, CN, false>, m.w, m.r,
+                              m.y, args);
   }
 };
 
