@@ -501,11 +501,16 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8>::kThre
         g_end = g + 1;
       }
     }
-    // Every peer's commit for the stages filled must have landed (they
-    // arrive on our barriers, and our copies read our shared memory) before
-    // this CTA may leave.
+    // Every peer's commit for the final use of each stage must have landed
+    // (they arrive on our barriers, and our copies read our shared memory)
+    // before this CTA may leave. The final uses are the CTA's last NS
+    // k-blocks, whichever group filled them: waiting instead for this
+    // group's own last ones could ask for a phase of a stage that the other
+    // group has since used again, whose parity then reads as not yet
+    // complete. After a failure, the k-blocks this group reached.
+    const int g_last = ok ? total : g_end;
     if (lane == 0)
-      for (int x = (g_end > T::NS ? g_end - T::NS : 0); x < g_end; ++x)
+      for (int x = (g_last > T::NS ? g_last - T::NS : 0); x < g_last; ++x)
         wait_phase_cluster(bar(T::BAR_EMPTY + x % T::NS), (x / T::NS) & 1, ctl, false);
     __syncwarp();
   } else if (warp >= 4 + T::XF_WARPS) {
