@@ -216,6 +216,21 @@ int f16_cluster_size(uint64_t N) {
   return N >= 4 * per ? 4 : (N >= 2 * per ? 2 : 1);
 }
 
+// Whether matmul_w16 / matmul_residual_w16 round X to binary16 in a
+// pre-pass and feed the clustered kernel by TMA: by default when a row block
+// spans several cluster tiles along N (each would otherwise transform the
+// same rows again). LIN_F16_PRECONVERT=0 / 1 forces it off / on
+// (measurements).
+bool f16_preconvert(int num_ng) {
+  static const int forced = [] {
+    const char* v = std::getenv("LIN_F16_PRECONVERT");
+    if (!v) return -1;
+    return std::strcmp(v, "0") == 0 ? 0 : (std::strcmp(v, "1") == 0 ? 1 : -1);
+  }();
+  if (forced >= 0) return forced == 1;
+  return num_ng >= 2;
+}
+
 enum Form : int { F_MATMUL = 0, F_RESID = 1, F_SWIGLU = 2 };
 
 struct Problem {
@@ -388,29 +403,53 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
     // Persistent launch: split the K range of the last partial round when
     // that keeps idle clusters busy.
     cudaError_t ce = cudaSuccess;
-    const int cap = swiglu ? lin::cluster_capacity_swiglu(cn, &ce)
-                           : lin::cluster_capacity_cvt(cn, resid, &ce);
-    if (cap < 1) return cuda_fail(ce);
     const int num_m = (int)((M + lin::kBM - 1) / lin::kBM);
     const int num_ng = (int)((N + (uint64_t)lin::kClusterBN * cn - 1) / ((uint64_t)lin::kClusterBN * cn));
     const int nkb = (int)((K + 63) / 64);
-    const lin::SplitPlan plan = lin::split_plan(num_m * num_ng, cap, nkb);
-    if (plan.s >= 2) {
-      const int got = take_workspace(lin::split_part_bytes(plan, cn, lin::kClusterBN));
-      if (got < 0) return LIN_ERROR_UNSUPPORTED_SHAPE;
-      if (got > 0) {
-        args.split_r = plan.r;
-        args.split_rem = plan.rem;
-        args.split_s = plan.s;
-      }
+    // binary16 X from a pre-pass, in the workspace after the partial tiles
+    bool tma_a = !swiglu && !fixed && K % 8 == 0 && f16_preconvert(num_ng);
+    auto capacity = [&]() {
+      return swiglu ? lin::cluster_capacity_swiglu(cn, &ce)
+                    : (tma_a ? lin::cluster_capacity_tma(cn, resid, &ce)
+                             : lin::cluster_capacity_cvt(cn, resid, &ce));
+    };
+    int cap = capacity();
+    if (cap < 1) return cuda_fail(ce);
+    lin::SplitPlan plan = lin::split_plan(num_m * num_ng, cap, nkb);
+    const size_t part_bytes = lin::split_part_bytes(plan, cn, lin::kClusterBN);
+    const size_t xh_off = (part_bytes + 255) & ~size_t(255);
+    const size_t xh_bytes = tma_a ? (size_t)M * (size_t)K * 2 : 0;
+    const size_t need = xh_bytes ? xh_off + xh_bytes : part_bytes;
+    const int got = need ? take_workspace(need) : 0;
+    if (got < 0) return LIN_ERROR_UNSUPPORTED_SHAPE;
+    if (got == 0 && tma_a) {   // no memory for the pre-pass: transform X in the GEMM
+      tma_a = false;
+      cap = capacity();
+      if (cap < 1) return cuda_fail(ce);
     }
-    e = swiglu ? lin::launch_gemm_cluster_swiglu(cn, maps, args, stream)
-               : lin::launch_gemm_cluster_cvt(cn, resid, maps, args, stream);
+    if (got > 0 && plan.s >= 2) {
+      args.split_r = plan.r;
+      args.split_rem = plan.rem;
+      args.split_s = plan.s;
+    }
+    if (tma_a) {
+      uint16_t* xh = reinterpret_cast<uint16_t*>(reinterpret_cast<char*>(args.part) + xh_off);
+      if (!encode_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT16, xh, K, M, K * 2, 64,
+                     (uint32_t)(lin::kBM / cn)))
+        e = cudaErrorInvalidValue;
+      else
+        e = lin::launch_cvt_f16(p.X, xh, M * K, sm_count(dev), stream);
+      if (e == cudaSuccess) e = lin::launch_gemm_cluster_tma(cn, resid, maps, args, stream);
+      kernels = 2;
+    } else {
+      e = swiglu ? lin::launch_gemm_cluster_swiglu(cn, maps, args, stream)
+                 : lin::launch_gemm_cluster_cvt(cn, resid, maps, args, stream);
+    }
     if (e == cudaSuccess && args.split_s >= 2) {
       const int clusters = args.split_r > 0 ? cap : args.split_rem * args.split_s;
       e = lin::launch_split_reduce(args, resid, cn, lin::kClusterBN, args.split_r * clusters,
                                    num_ng, stream);
-      kernels = 2;
+      kernels += 1;
     }
   } else {
     // One CTA per 128 x bn tile; when the tiles leave most SMs idle, split K

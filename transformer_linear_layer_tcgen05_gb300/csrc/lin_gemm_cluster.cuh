@@ -50,8 +50,12 @@ namespace lin {
 
 template <int AMODE, bool RESID, int BN_, int CN_, bool V8_ = false>
 struct ClusterTraits {
-  static_assert(AMODE == A_CVT_F16 || AMODE == A_SWIGLU_F16, "binary16 forms only");
+  static_assert(AMODE == A_CVT_F16 || AMODE == A_SWIGLU_F16 || AMODE == A_TMA_F16,
+                "binary16 forms only");
   static constexpr bool kSwiglu = (AMODE == A_SWIGLU_F16);
+  // A already binary16 in global memory: each CTA copies its ROWS rows of
+  // every A k-block by TMA, multicast to the whole cluster; no transform warps.
+  static constexpr bool kTmaA = (AMODE == A_TMA_F16);
   static constexpr int BM = kBM;
   static constexpr int BN = BN_;
   static constexpr int CN = CN_;                  // CTAs per cluster, along N
@@ -62,14 +66,14 @@ struct ClusterTraits {
   static constexpr int W_BOXES = BN / W_ATOM;
   static constexpr int ROWS = BM / CN;            // A rows this CTA transforms
   static constexpr int INPUTS = kSwiglu ? 2 : 1;  // GATE and UP, or X
-  static constexpr int XF_WARPS = LIN_XF_WARPS;
+  static constexpr int XF_WARPS = kTmaA ? 0 : LIN_XF_WARPS;
   // The transform warps form XF_GROUPS groups that take turns by k-block, so
   // each warp's fixed cost per k-block (a barrier wait, a proxy fence, the
   // copy issue) is spread over XF_GROUPS k-blocks of UMMA time. A single CTA
   // transforming all 128 rows of the SwiGLU form keeps one group, so that a
   // warp's share of a k-block still fits its registers.
-  static constexpr int XF_GROUPS = (kSwiglu && CN == 1) ? 1 : XF_WARPS / 4;
-  static constexpr int XF_PER_GROUP = XF_WARPS / XF_GROUPS;
+  static constexpr int XF_GROUPS = kTmaA ? 1 : ((kSwiglu && CN == 1) ? 1 : XF_WARPS / 4);
+  static constexpr int XF_PER_GROUP = kTmaA ? 1 : XF_WARPS / XF_GROUPS;
   static constexpr int RW = ROWS / XF_PER_GROUP;  // A rows per transform warp (contiguous)
   // Each transform warp bulk-copies its RW rows of a stage to every peer as
   // soon as it has written them (measured faster than one copy per group).
@@ -142,11 +146,11 @@ struct ClusterTraits {
   static constexpr int kThreadsC = (8 + XF_WARPS) * 32;
 
   static_assert(CN == 1 || CN == 2 || CN == 4 || CN == 8, "cluster size");
-  static_assert(XF_WARPS == 4 || XF_WARPS == 8 || XF_WARPS == 12, "transform warps");
+  static_assert(kTmaA || XF_WARPS == 4 || XF_WARPS == 8 || XF_WARPS == 12, "transform warps");
   static_assert(XF_WARPS % XF_GROUPS == 0 && ROWS % XF_PER_GROUP == 0 &&
                     RW % ROWS_PER_LOAD == 0,
                 "transform groups");
-  static_assert(LOADS <= 16, "staged input per lane");
+  static_assert(kTmaA || LOADS <= 16, "staged input per lane");
   // A parity wait is only sound for a waiter at most one phase ahead: a group
   // reaching use u of a stage must already have seen use u-1's UMMA
   // complete, true when its previous k-block (XF_GROUPS earlier) waited for
@@ -245,6 +249,7 @@ __device__ __forceinline__ void stage_store(uint32_t a_stage, uint32_t crank, in
 template <int AMODE, bool RESID, int BN, int CN, bool V8>
 __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8>::kThreadsC, 1)
     lin_gemm_cluster_kernel(const __grid_constant__ CUtensorMap tm_w,
+                            const __grid_constant__ CUtensorMap tm_a,
                             const __grid_constant__ CUtensorMap tm_r,
                             const __grid_constant__ CUtensorMap tm_y, const KernelArgs args) {
   using T = ClusterTraits<AMODE, RESID, BN, CN, V8>;
@@ -294,7 +299,8 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8>::kThre
   // ---- set-up
   if (threadIdx.x == 0) {
     for (int s = 0; s < T::NS; ++s) {
-      mbar_init(bar(T::BAR_FULL + s), 1 + T::XF_PER_GROUP);   // W producer, the group's warps
+      // the producer, and the transform group's warps
+      mbar_init(bar(T::BAR_FULL + s), T::kTmaA ? 1 : 1 + T::XF_PER_GROUP);
       mbar_init(bar(T::BAR_EMPTY + s), CN);        // every CTA's UMMA commit
     }
     for (int b = 0; b < 2; ++b) {
@@ -309,6 +315,7 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8>::kThre
   __syncwarp();
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tm_w);
+    if constexpr (T::kTmaA) tma_prefetch_desc(&tm_a);
     if constexpr (RESID) tma_prefetch_desc(&tm_r);
     tma_prefetch_desc(&tm_y);
   }
@@ -332,11 +339,14 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8>::kThre
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    // ---------------- W producer (local TMA into the B half of each stage)
+    // ---------------- W producer (local TMA into the B half of each stage);
+    // with a binary16 A in global memory also this CTA's rows of A, to
+    // every CTA of the cluster
     int g = 0;   // k-blocks issued, across tiles
     bool ok = true;
     for (int i = 0; i < n_items && ok; ++i) {
-      const int n0 = tile_n0(item_tile(i));
+      const int t = item_tile(i);
+      const int n0 = tile_n0(t);
       const int kb1 = item_kb1(i);
       for (int kb = item_kb0(i); kb < kb1; ++kb, ++g) {
         const int s = g % T::NS;
@@ -350,18 +360,33 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8>::kThre
         }
         if (lane == 0) {
           const uint32_t full = bar(T::BAR_FULL + s);
-          mbar_arrive_expect_tx(full, T::B_BYTES);
+          // the whole A stage lands here too: one slice from each CTA
+          mbar_arrive_expect_tx(full, T::B_BYTES + (T::kTmaA ? T::A_BYTES : 0u));
 #pragma unroll
           for (int j = 0; j < T::W_BOXES; ++j)
             tma_load_2d(b_stage(s) + j * T::B_ATOM_BYTES, &tm_w, n0 + j * T::W_ATOM, kb * T::BK,
                         full);
+          if constexpr (T::kTmaA) {
+            const uint32_t dst = a_stage(s) + crank * (uint32_t)(T::ROWS * 128);
+            const int row = tile_m0(t) + (int)crank * T::ROWS;
+            if constexpr (CN > 1)
+              tma_load_2d_multicast(dst, &tm_a, kb * T::BK, row, full, T::CLUSTER_MASK);
+            else
+              tma_load_2d(dst, &tm_a, kb * T::BK, row, full);
+          }
         }
         __syncwarp();
       }
     }
-    if (lane == 0)
+    if (lane == 0) {
       for (int x = (g > T::NS ? g - T::NS : 0); x < g; ++x)
         wait_phase(bar(T::BAR_FULL + x % T::NS), (x / T::NS) & 1, ctl, false);
+      // The peers' commits for the final use of each stage land on our
+      // barriers (without transform warps, nobody else waits for them).
+      if constexpr (T::kTmaA && CN > 1)
+        for (int x = (g > T::NS ? g - T::NS : 0); x < g; ++x)
+          wait_phase_cluster(bar(T::BAR_EMPTY + x % T::NS), (x / T::NS) & 1, ctl, false);
+    }
     __syncwarp();
   } else if (warp == 1) {
     // ---------------- UMMA issuer
@@ -422,6 +447,7 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8>::kThre
     }
     __syncwarp();
   } else if (warp >= 4 && warp < 4 + T::XF_WARPS) {
+    if constexpr (!T::kTmaA) {
     // ---------------- transform warps
     const int grp = (warp - 4) / T::XF_PER_GROUP;
     const int tw = (warp - 4) % T::XF_PER_GROUP;
@@ -513,6 +539,7 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8>::kThre
       for (int x = (g_last > T::NS ? g_last - T::NS : 0); x < g_last; ++x)
         wait_phase_cluster(bar(T::BAR_EMPTY + x % T::NS), (x / T::NS) & 1, ctl, false);
     __syncwarp();
+    }
   } else if (warp >= 4 + T::XF_WARPS) {
     // ---------------- epilogue warps: rows q*32 .. q*32+31 of the tile
     const int q = warp & 3;                        // TMEM lane quadrant
@@ -680,7 +707,6 @@ struct ClusterLaunch {
     static std::atomic<uint64_t> attr_done{0};
     static std::atomic<int> max_clusters[64];
     auto kern = lin_gemm_cluster_kernel<AMODE, RESID, BN, CN, false>;
-    auto kern8 = lin_gemm_cluster_kernel<AMODE, RESID, BN, CN, true>;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess && dev >= 64) e = cudaErrorInvalidDevice;
@@ -691,9 +717,12 @@ struct ClusterLaunch {
     const uint64_t bit = uint64_t{1} << dev;
     if (!(attr_done.load(std::memory_order_acquire) & bit)) {
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
-      if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(kern8, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 ClusterTraits<AMODE, RESID, BN, CN, true>::SMEM_BYTES);
+      if constexpr (!T::kTmaA) {   // the 32-byte-load variant of the transform
+        if (e == cudaSuccess)
+          e = cudaFuncSetAttribute(lin_gemm_cluster_kernel<AMODE, RESID, BN, CN, true>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   ClusterTraits<AMODE, RESID, BN, CN, true>::SMEM_BYTES);
+      }
       cudaLaunchAttribute attr[2];
       cudaLaunchConfig_t cfg = config(attr, nullptr, false);
       cfg.gridDim = dim3(CN, 1, 1);
@@ -726,11 +755,13 @@ struct ClusterLaunch {
     cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = config(attr, stream, true);
     cfg.gridDim = dim3((unsigned)(clusters * CN), 1, 1);
-    if (args.flags & KFLAG_A_V8)
-      return cudaLaunchKernelEx(&cfg, lin_gemm_cluster_kernel<AMODE, RESID, BN, CN, true>, m.w,
-                                m.r, m.y, args);
-    return cudaLaunchKernelEx(&cfg, lin_gemm_cluster_kernel<AMODE, RESID, BN, CN, false>, m.w, m.r,
-                              m.y, args);
+    if constexpr (!T::kTmaA) {
+      if (args.flags & KFLAG_A_V8)
+        return cudaLaunchKernelEx(&cfg, lin_gemm_cluster_kernel<AMODE, RESID, BN, CN, true>, m.w,
+                                  m.a, m.r, m.y, args);
+    }
+    return cudaLaunchKernelEx(&cfg, lin_gemm_cluster_kernel<AMODE, RESID, BN, CN, false>, m.w, m.a,
+                              m.r, m.y, args);
   }
 };
 

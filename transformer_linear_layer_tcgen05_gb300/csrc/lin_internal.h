@@ -17,6 +17,7 @@ enum AMode : int {
   A_CVT_F16 = 1,     // X f32 staged by TMA, rounded to binary16 by transform warps
   A_SWIGLU_F32 = 2,  // GATE, UP staged by TMA; silu(GATE) * UP written as f32 (TF32 MMA)
   A_SWIGLU_F16 = 3,  // GATE, UP staged by TMA; silu(GATE) * UP rounded to binary16
+  A_TMA_F16 = 4,     // X rounded to binary16 by a pre-pass, copied by TMA (clustered kernels)
 };
 
 enum : uint32_t {
@@ -106,6 +107,15 @@ cudaError_t launch_gemm_cluster_cvt(int cn, bool resid, const TensorMaps& maps,
 // shared-memory attribute on first use); > 0, or 0 with *err set.
 int cluster_capacity_swiglu(int cn, cudaError_t* err);
 int cluster_capacity_cvt(int cn, bool resid, cudaError_t* err);
+// matmul_w16 / matmul_residual_w16 with A = binary16 X already in global
+// memory (tensor map `a`, boxes of 64 x 128/cn): each CTA copies its rows of
+// every A k-block by TMA multicast to its cluster.
+cudaError_t launch_gemm_cluster_tma(int cn, bool resid, const TensorMaps& maps,
+                                    const KernelArgs& args, cudaStream_t stream);
+int cluster_capacity_tma(int cn, bool resid, cudaError_t* err);
+// Xh[i] = binary16(X[i]) (round to nearest even) for i < n, n % 4 == 0,
+// both bases 16-byte aligned.
+cudaError_t launch_cvt_f16(const float* X, uint16_t* Xh, int64_t n, int sms, cudaStream_t stream);
 // Y (+ R) from the partial tiles of a split: tiles tile0 .. tile0 +
 // split_rem - 1 of width `bn` (cluster tiles of `cn` CTAs, `num_ng` of them
 // per row block), each summed over its split_s K ranges.

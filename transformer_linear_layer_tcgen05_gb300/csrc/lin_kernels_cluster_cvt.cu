@@ -1,12 +1,79 @@
 // lin_kernels_cluster_cvt.cu -- instantiations of the clustered persistent
-// GEMM for matmul_w16 and matmul_residual_w16 (cluster sizes 1, 2, 4), and
-// the split-tail sum shared by every clustered form.
+// GEMM for matmul_w16 and matmul_residual_w16 (cluster sizes 1, 2, 4; A
+// rounded to binary16 by the transform warps, or by a pre-pass and then
+// copied by TMA), the pre-pass, and the split-tail sum shared by every
+// clustered form.
 #include "lin_gemm_cluster.cuh"
 
 namespace lin {
 
 template <bool RESID, int CN>
 using CvtLaunch = ClusterLaunch<A_CVT_F16, RESID, 256, CN>;
+
+template <bool RESID, int CN>
+using TmaLaunch = ClusterLaunch<A_TMA_F16, RESID, 256, CN>;
+
+cudaError_t launch_gemm_cluster_tma(int cn, bool resid, const TensorMaps& maps,
+                                    const KernelArgs& args, cudaStream_t stream) {
+  if (resid) {
+    switch (cn) {
+      case 1: return TmaLaunch<true, 1>::launch(maps, args, stream);
+      case 2: return TmaLaunch<true, 2>::launch(maps, args, stream);
+      case 4: return TmaLaunch<true, 4>::launch(maps, args, stream);
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  switch (cn) {
+    case 1: return TmaLaunch<false, 1>::launch(maps, args, stream);
+    case 2: return TmaLaunch<false, 2>::launch(maps, args, stream);
+    case 4: return TmaLaunch<false, 4>::launch(maps, args, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+int cluster_capacity_tma(int cn, bool resid, cudaError_t* err) {
+  if (resid) {
+    switch (cn) {
+      case 1: return TmaLaunch<true, 1>::capacity(err);
+      case 2: return TmaLaunch<true, 2>::capacity(err);
+      case 4: return TmaLaunch<true, 4>::capacity(err);
+      default: *err = cudaErrorInvalidValue; return 0;
+    }
+  }
+  switch (cn) {
+    case 1: return TmaLaunch<false, 1>::capacity(err);
+    case 2: return TmaLaunch<false, 2>::capacity(err);
+    case 4: return TmaLaunch<false, 4>::capacity(err);
+    default: *err = cudaErrorInvalidValue; return 0;
+  }
+}
+
+// X -> binary16, four elements per thread and step (one 16-byte load, one
+// 8-byte store), the same rounding as the transform warps (pack_half2).
+__global__ void __launch_bounds__(256)
+    lin_cvt_f16_kernel(const float4* __restrict__ x, uint2* __restrict__ y, long long n4) {
+  // The GEMM that reads the result may be scheduled now; it waits for this
+  // grid's completion itself before it touches memory.
+  pdl_launch_dependents();
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
+       i += (long long)gridDim.x * blockDim.x) {
+    const float4 v = ldg_stream_v4f(reinterpret_cast<const float*>(x + i));
+    y[i] = make_uint2(pack_half2(v.x, v.y), pack_half2(v.z, v.w));
+  }
+}
+
+cudaError_t launch_cvt_f16(const float* X, uint16_t* Xh, int64_t n, int sms, cudaStream_t stream) {
+  const long long n4 = n / 4;
+  long long blocks = (n4 + 255) / 256;
+  if (blocks > (long long)sms * 8) blocks = (long long)sms * 8;
+  if (blocks < 1) blocks = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks, 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = stream;
+  return cudaLaunchKernelEx(&cfg, lin_cvt_f16_kernel, reinterpret_cast<const float4*>(X),
+                            reinterpret_cast<uint2*>(Xh), n4);
+}
 
 cudaError_t launch_gemm_cluster_cvt(int cn, bool resid, const TensorMaps& maps,
                                     const KernelArgs& args, cudaStream_t stream) {
