@@ -47,6 +47,12 @@
  *             in which the tail's K ranges are summed). The f32 forms split
  *             K in the same way when a problem has too few 128 x 128 tiles
  *             to fill the SMs (at most 64 KiB of workspace per SM).
+ *             lin_matmul_w16 and lin_matmul_residual_w16 also place a
+ *             binary16 copy of X (M*K*2 bytes) in the workspace, written by
+ *             a first kernel, when each row block of X feeds several
+ *             clusters of output tiles along N (N > 1024 on a GB300) and
+ *             K % 8 == 0; without the memory they round X inside the GEMM
+ *             instead (the same results).
  *             lin_last_launch_info() reports what a call used.
  * Stream      Work is enqueued on `stream` (a cudaStream_t; NULL means the
  *             legacy default stream) and the call returns without waiting.
