@@ -194,6 +194,31 @@ lin_status lin_matmul_residual_swiglu_a_w16_noalloc(const float *GATE, const flo
                                                     float *Y, int64_t M, int64_t N, int64_t K,
                                                     lin_stream_t stream);
 
+/* Backward of the linear layer, input gradient: dX[M,K] = dY[M,N] @ W[K,N]^T
+ * (dY, W, dX binary32; TF32 tensor cores, f32 accumulate). The pages' backward
+ * linear page is not part of the material; the operation is the adjoint of
+ * lin_matmul (03_linear_forward, "Ne Yapar?"): for every X,
+ * sum(lin_matmul(X, W) * dY) == sum(X * dX). Same layout conventions (row
+ * major, W as the forward stores it), validation and errors as lin_matmul:
+ * K % 4 == 0 and N % 4 == 0; dX may overlap no input. */
+lin_status lin_matmul_t(const float *DY, const float *W, float *DX,
+                        int64_t M, int64_t N, int64_t K, lin_stream_t stream);
+
+/* dX += dY @ W^T: dX is read and written in place (the accumulating form
+ * of a gradient reaching X through several branches). */
+lin_status lin_matmul_t_acc(const float *DY, const float *W, float *DX,
+                            int64_t M, int64_t N, int64_t K, lin_stream_t stream);
+
+/* lin_matmul_t with binary16 weights W16[K,N] (bit patterns); dY is rounded
+ * to binary16 for the f16 tensor cores, as X is in lin_matmul_w16.
+ * N % 8 == 0. */
+lin_status lin_matmul_t_w16(const float *DY, const uint16_t *W16, float *DX,
+                            int64_t M, int64_t N, int64_t K, lin_stream_t stream);
+
+/* dX += dY @ W16^T (in place), binary16 weights. N % 8 == 0. */
+lin_status lin_matmul_t_acc_w16(const float *DY, const uint16_t *W16, float *DX,
+                                int64_t M, int64_t N, int64_t K, lin_stream_t stream);
+
 /* Static, NUL-terminated name of a status code ("LIN_SUCCESS", ...). Never NULL. */
 const char *lin_status_string(lin_status status);
 

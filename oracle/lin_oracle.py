@@ -28,6 +28,14 @@ e / (1 + e) with e = exp(x), so exp() never sees a positive argument and no
 clamp is applied. The same page (note 3) says the forward kernels share this
 helper.
 
+Backward input gradient (``matmul_t``; the material does not include the
+pages' backward-linear page, "11_backward_linear"). Reading: the input
+gradient of Y = X @ W is the adjoint of the forward map X -> X @ W under the
+Frobenius inner product, dX = dY @ W^T, i.e. the unique dX with
+sum(dX * X) == sum(dY * (X @ W)) for every X; ``matmul_t_acc`` adds it to
+an existing dX (dX += dY @ W^T), ``_w16`` takes W as binary16 bits. dY is
+[M,N], W is [K,N] as the forward stores it, dX is [M,K].
+
 Everything is evaluated in float64. Inputs are widened exactly: float32 to
 float64 by numpy, binary16 bit patterns by ``f16_bits_to_f64`` below (an
 IEEE 754 decoder written from the format's definition). The contraction uses
@@ -59,6 +67,10 @@ __all__ = [
     "matmul_w16",
     "matmul_residual_w16",
     "matmul_residual_swiglu_a_w16",
+    "matmul_t",
+    "matmul_t_acc",
+    "matmul_t_w16",
+    "matmul_t_acc_w16",
     "normaliser",
     "normalised_error",
     "reference",
@@ -72,6 +84,10 @@ FORMS = (
     "matmul_w16",
     "matmul_residual_w16",
     "matmul_residual_swiglu_a_w16",
+    "matmul_t",
+    "matmul_t_acc",
+    "matmul_t_w16",
+    "matmul_t_acc_w16",
 )
 
 
@@ -181,6 +197,35 @@ def matmul_residual_swiglu_a_w16(GATE, UP, W16, R) -> np.ndarray:
     return matmul_residual_swiglu_a(GATE, UP, f16_bits_to_f64(W16), R)
 
 
+def matmul_t(DY, W) -> np.ndarray:
+    """dX[M,K] = dY[M,N] @ W[K,N]^T: the adjoint of X -> X @ W (input
+    gradient of the forward "matmul"), in float64."""
+    DY = _f64(DY)
+    W = _f64(W)
+    if DY.ndim != 2 or W.ndim != 2 or DY.shape[1] != W.shape[1]:
+        raise ValueError(f"shape mismatch: dY{DY.shape} @ W{W.shape}^T")
+    return DY @ W.T
+
+
+def matmul_t_acc(DY, W, DX0) -> np.ndarray:
+    """dX0 + dY @ W^T (the accumulating form)."""
+    Y = matmul_t(DY, W)
+    DX0 = _f64(DX0)
+    if DX0.shape != Y.shape:
+        raise ValueError(f"initial dX shape {DX0.shape} != output shape {Y.shape}")
+    return DX0 + Y
+
+
+def matmul_t_w16(DY, W16) -> np.ndarray:
+    """matmul_t with W given as binary16 bit patterns (uint16 [K,N])."""
+    return matmul_t(DY, f16_bits_to_f64(W16))
+
+
+def matmul_t_acc_w16(DY, W16, DX0) -> np.ndarray:
+    """matmul_t_acc with binary16 weights."""
+    return matmul_t_acc(DY, f16_bits_to_f64(W16), DX0)
+
+
 # --------------------------------------------------------------------------
 # Acceptance metric
 # --------------------------------------------------------------------------
@@ -225,8 +270,9 @@ def normalised_error(Y, Y_ref, S, R=None) -> float:
 def reference(form: str, inputs: dict, rows=None):
     """Evaluate ``form`` on an input dict; return (Y_ref, S).
 
-    ``inputs`` holds the arrays named by the C ABI: X or GATE/UP, W (float32)
-    or W16 (uint16 bit patterns), and R for the residual forms. ``rows`` picks
+    ``inputs`` holds the arrays named by the C ABI: X or GATE/UP (DY for the
+    transposed forms), W (float32) or W16 (uint16 bit patterns), and R for
+    the residual forms (the initial dX of the accumulating ones). ``rows`` picks
     a subset of output rows: every output row depends only on the same row of
     X / GATE / UP / R, so a row subset is the definition applied to those rows.
     """
@@ -235,6 +281,14 @@ def reference(form: str, inputs: dict, rows=None):
     sel = (lambda a: a) if rows is None else (lambda a: np.asarray(a)[rows])
     w16 = form.endswith("_w16")
     W = f16_bits_to_f64(inputs["W16"]) if w16 else _f64(inputs["W"])
+    if form.startswith("matmul_t"):
+        # dX row i depends only on dY row i (and R row i)
+        A = _f64(sel(inputs["DY"]))
+        if "_acc" in form:
+            Y = matmul_t_acc(A, W, sel(inputs["R"]))
+        else:
+            Y = matmul_t(A, W)
+        return Y, normaliser(A, W.T)
     if "swiglu" in form:
         A = swiglu_a(sel(inputs["GATE"]), sel(inputs["UP"]))
     else:

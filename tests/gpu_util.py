@@ -56,6 +56,16 @@ def integer_inputs(form: str, M: int, N: int, K: int, seed: int) -> dict:
     partial sum is an integer below K * 960 < 2**24 for K <= 16384."""
     rng = np.random.default_rng(seed)
     d = {}
+    if wl.form_is_t(form):   # dX[M,K] = dY[M,N] @ W[K,N]^T (+ R [M,K])
+        d["DY"] = rng.integers(-4, 5, size=(M, N)).astype(np.float32)
+        w = rng.integers(-4, 5, size=(K, N)).astype(np.float32)
+        if wl.form_is_w16(form):
+            d["W16"] = w.astype(np.float16).view(np.uint16)
+        else:
+            d["W"] = w
+        if wl.form_has_residual(form):
+            d["R"] = rng.integers(-64, 65, size=(M, K)).astype(np.float32)
+        return d
     if wl.form_is_swiglu(form):
         d["GATE"] = rng.integers(40, 61, size=(M, K)).astype(np.float32)
         d["UP"] = rng.integers(-4, 5, size=(M, K)).astype(np.float32)

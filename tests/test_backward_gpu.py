@@ -1,0 +1,149 @@
+"""The backward input gradient dX = dY @ W^T (lin_matmul_t, _acc, _w16) on
+the GPU against the oracle.
+
+The backward-linear page is not part of the material; the operation is the
+adjoint of the forward product (see the oracle). Shapes use the C ABI's
+convention: dY [M,N], W [K,N], dX [M,K]; the contraction runs over N.
+"""
+
+import os
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+
+import oracle
+from tests.gpu_util import TOL, integer_inputs, oracle_error, require_gpu, to_device
+from transformer_linear_layer_tcgen05_gb300 import lin
+from transformer_linear_layer_tcgen05_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+T_FORMS = wl.T_FORMS
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+# (M, N, K): ragged tiles, a single row, a contraction shorter than a
+# k-block, and an output wide enough for clusters of four with several N
+# groups (binary16 W: N % 8 == 0). The last two split K (the contraction)
+# across CTAs or clusters.
+SHAPES = [(128, 256, 128), (129, 136, 260), (1, 8, 4), (300, 64, 1032), (257, 1024, 2048),
+          (300, 2048, 2048), (520, 512, 768)]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    require_gpu()
+
+
+def _run(form, dd, M, K):
+    import torch
+    Y = torch.full((M, K), float("nan"), dtype=torch.float32, device="cuda")
+    lin.run_form(form, dd, Y)
+    torch.cuda.synchronize()
+    assert lin.lin_get_device_status() == lin.LIN_SUCCESS
+    return Y
+
+
+@pytest.mark.parametrize("form", T_FORMS)
+@pytest.mark.parametrize("shape", SHAPES)
+def test_exact_small_integers(form, shape):
+    M, N, K = shape
+    d = integer_inputs(form, M, N, K, seed=M + 3 * N + 5 * K)
+    Y = _run(form, to_device(d), M, K).cpu().numpy().astype(np.float64)
+    Yref, _ = oracle.reference(form, d)
+    assert np.array_equal(Y, Yref), f"max |diff| = {np.max(np.abs(Y - Yref))}"
+
+
+@pytest.mark.parametrize("form", T_FORMS)
+@pytest.mark.parametrize("shape", [(300, 392, 200), (513, 264, 1024), (512, 768, 768)])
+def test_random_within_bound(form, shape):
+    M, N, K = shape
+    d = wl.generate(form, M, N, K, seed=29 + M + N)
+    Y = _run(form, to_device(d), M, K).cpu().numpy()
+    assert oracle_error(form, d, Y) <= TOL
+
+
+@pytest.mark.parametrize("form", T_FORMS)
+def test_empty_contraction_gives_initial_or_zero(form):
+    import torch
+    M, N, K = 70, 0, 48
+    d = to_device(wl.generate(form, M, 8, K, seed=1))
+    d["DY"] = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    w = "W16" if form.endswith("_w16") else "W"
+    d[w] = torch.empty((K, N), dtype=d[w].dtype, device="cuda")
+    Y = _run(form, d, M, K)
+    want = d["R"] if "R" in d else torch.zeros_like(Y)
+    assert torch.equal(Y, want)
+
+
+def test_adjoint_of_the_forward_kernel():
+    # sum(dY * (X @ W)) == sum(dX * X) with both sides computed on the GPU,
+    # exactly on small integers
+    import torch
+    M, N, K = 200, 136, 264
+    rng = np.random.default_rng(3)
+    X = rng.integers(-3, 4, size=(M, K)).astype(np.float32)
+    W = rng.integers(-3, 4, size=(K, N)).astype(np.float32)
+    DY = rng.integers(-3, 4, size=(M, N)).astype(np.float32)
+    Xd, Wd, DYd = (torch.from_numpy(a).cuda() for a in (X, W, DY))
+    Y = torch.empty((M, N), device="cuda")
+    DX = torch.empty((M, K), device="cuda")
+    lin.lin_matmul(Xd, Wd, Y)
+    lin.lin_matmul_t(DYd, Wd, DX)
+    torch.cuda.synchronize()
+    lhs = float(np.sum(Y.cpu().numpy().astype(np.float64) * DY))
+    rhs = float(np.sum(DX.cpu().numpy().astype(np.float64) * X))
+    assert lhs == rhs
+
+
+def test_acc_reads_and_writes_in_place():
+    import torch
+    M, N, K = 256, 512, 1024
+    d = integer_inputs("matmul_t_acc_w16", M, N, K, seed=8)
+    dd = to_device(d)
+    DX = dd["R"].clone()
+    lin.lin_matmul_t_acc_w16(dd["DY"], dd["W16"], DX)
+    lin.lin_matmul_t_acc_w16(dd["DY"], dd["W16"], DX)   # twice: dX0 + 2 dY W^T
+    torch.cuda.synchronize()
+    once = oracle.matmul_t_w16(d["DY"], d["W16"])
+    assert np.array_equal(DX.cpu().numpy().astype(np.float64), d["R"] + 2.0 * once)
+
+
+CHILD = r"""
+import sys
+import numpy as np
+import torch
+sys.path.insert(0, sys.argv[1])
+import oracle
+from tests.gpu_util import integer_inputs, require_gpu, to_device
+from transformer_linear_layer_tcgen05_gb300 import lin
+require_gpu()
+bad = 0
+for form in ("matmul_t_w16", "matmul_t_acc_w16"):
+    for (M, N, K) in [(128, 64, 256), (300, 200, 2048), (129, 520, 1032), (1, 1032, 4),
+                      (700, 1536, 1024), (4736, 1024, 2048)]:
+        d = integer_inputs(form, M, N, K, seed=M + N + K)
+        Yd = torch.full((M, K), float("nan"), dtype=torch.float32, device="cuda")
+        lin.run_form(form, to_device(d), Yd)
+        torch.cuda.synchronize()
+        st = lin.lin_get_device_status()
+        Y = Yd.cpu().numpy().astype(np.float64)
+        nd = int(np.sum(Y != oracle.reference(form, d)[0]))
+        if nd or st != lin.LIN_SUCCESS:
+            print(f"{form} {M}x{N}x{K}: status {st}, {nd} mismatches", flush=True)
+        bad += nd + (st != lin.LIN_SUCCESS)
+sys.exit(1 if bad else 0)
+"""
+
+VARIANTS = [{"LIN_F16_KERNEL": "1"}, {"LIN_F16_KERNEL": "2"}, {"LIN_F16_KERNEL": "4"},
+            {"LIN_F16_KERNEL": "tile"}, {"LIN_F16_KERNEL": "4", "LIN_F16_PRECONVERT": "0"},
+            {"LIN_F16_KERNEL": "1", "LIN_F16_PRECONVERT": "1"}]
+
+
+@pytest.mark.parametrize("variant", VARIANTS, ids=lambda v: "-".join(v.values()))
+def test_w16_every_kernel_exact(variant):
+    env = dict(os.environ, **variant)
+    r = subprocess.run([sys.executable, "-c", CHILD, ROOT], env=env, cwd=ROOT,
+                       stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout[-4000:]

@@ -121,3 +121,22 @@ def test_aliasing_rule(L):
         lin.LIN_ERROR_ALIASING
     # adjacent but disjoint is not aliasing (it fails later, at the device check)
     assert L.lin_matmul(X, W, X + 256, 8, 8, 8, None) != lin.LIN_ERROR_ALIASING
+
+
+def test_transposed_forms_validate_before_touching_cuda(L):
+    # dX[M,K] = dY[M,N] @ W[K,N]^T: N is the contraction, K the output width
+    fake = 1 << 40
+    assert L.lin_matmul_t(fake, fake, fake, -1, 8, 8, None) == lin.LIN_ERROR_INVALID_VALUE
+    assert L.lin_matmul_t(fake, fake, fake, 8, 8, 6, None) == lin.LIN_ERROR_UNSUPPORTED_SHAPE
+    assert L.lin_matmul_t(fake, fake, fake, 8, 6, 8, None) == lin.LIN_ERROR_UNSUPPORTED_SHAPE
+    # binary16 W [K,N]: its rows (N elements) must be whole 16-byte units
+    assert L.lin_matmul_t_w16(fake, fake, fake, 8, 12, 8, None) == lin.LIN_ERROR_UNSUPPORTED_SHAPE
+    assert L.lin_matmul_t_w16(fake, fake, fake, 0, 16, 8, None) == lin.LIN_SUCCESS
+    assert lin.lin_last_launch_info() == (0, 0)
+    # dX may not overlap dY or W ...
+    assert L.lin_matmul_t(X, W, X, 8, 8, 8, None) == lin.LIN_ERROR_ALIASING
+    assert L.lin_matmul_t_acc(X, W, W, 8, 8, 8, None) == lin.LIN_ERROR_ALIASING
+    # ... but the accumulating forms read and write dX itself (rejected here
+    # only later, because the fake addresses are not device memory)
+    assert L.lin_matmul_t_acc(X, W, Y, 8, 8, 8, None) != lin.LIN_ERROR_ALIASING
+    assert L.lin_matmul_t_acc(None, W, Y, 8, 8, 8, None) == lin.LIN_ERROR_INVALID_VALUE

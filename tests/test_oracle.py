@@ -235,3 +235,74 @@ def test_reference_row_subset_equals_full():
         Yr, Sr = oracle.reference(form, inp, rows=rows)
         assert np.array_equal(Yr, Y[rows]) and np.array_equal(Sr, S[rows])
         assert np.all(S >= np.abs(Y - (inp["R"] if "R" in inp else 0.0)) - 1e-12)
+
+
+# ---------------------------------------------------------------- backward: dX = dY @ W^T
+# The backward-linear page is not in the material; matmul_t is read as the
+# adjoint of the forward product (oracle module docstring). These pins tie it
+# to that definition, not to its own formula.
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (2, 3, 5), (4, 1, 3), (3, 6, 2)])
+def test_matmul_t_integer_brute_force(M, N, K):
+    rng = np.random.default_rng(100 + M * 7 + N * 3 + K)
+    DY = rng.integers(-4, 5, size=(M, N)).astype(np.float32)
+    W = rng.integers(-4, 5, size=(K, N)).astype(np.float32)
+    want = np.zeros((M, K))
+    for i, k, n in itertools.product(range(M), range(K), range(N)):
+        want[i, k] += float(DY[i, n]) * float(W[k, n])
+    assert np.array_equal(oracle.matmul_t(DY, W), want)
+
+
+@pytest.mark.parametrize("M,N,K", [(3, 5, 7), (8, 2, 4), (1, 9, 6)])
+def test_matmul_t_is_the_adjoint_of_matmul(M, N, K):
+    # sum(dY * (X @ W)) == sum(dX * X) for every X: exact on integers, and
+    # non-square shapes catch a transposed operand
+    rng = np.random.default_rng(7 * M + N + K)
+    X = rng.integers(-5, 6, size=(M, K)).astype(np.float32)
+    W = rng.integers(-5, 6, size=(K, N)).astype(np.float32)
+    DY = rng.integers(-5, 6, size=(M, N)).astype(np.float32)
+    lhs = float(np.sum(oracle.matmul(X, W) * DY))
+    rhs = float(np.sum(oracle.matmul_t(DY, W) * X))
+    assert lhs == rhs
+    # and it is the only such map: unit X picks out single entries
+    dX = oracle.matmul_t(DY, W)
+    for i, k in [(0, 0), (M - 1, K - 1), (M // 2, K // 2)]:
+        E = np.zeros((M, K), dtype=np.float32)
+        E[i, k] = 1.0
+        assert float(np.sum(oracle.matmul(E, W) * DY)) == dX[i, k]
+
+
+def test_matmul_t_acc_and_w16():
+    rng = np.random.default_rng(11)
+    DY = rng.integers(-4, 5, size=(4, 8)).astype(np.float32)
+    Wf = rng.integers(-4, 5, size=(6, 8)).astype(np.float32)
+    D0 = rng.integers(-64, 65, size=(4, 6)).astype(np.float32)
+    assert np.array_equal(oracle.matmul_t_acc(DY, Wf, D0) - oracle.matmul_t(DY, Wf),
+                          D0.astype(np.float64))
+    # binary16 weights decoded by numpy's own float16 type
+    W16 = (rng.standard_normal((6, 8)) * 0.3).astype(np.float16)
+    bits = W16.view(np.uint16)
+    want = np.zeros((4, 6))
+    for i, k, n in itertools.product(range(4), range(6), range(8)):
+        want[i, k] += float(DY[i, n]) * float(W16[k, n])
+    np.testing.assert_allclose(oracle.matmul_t_w16(DY, bits), want, rtol=1e-15, atol=1e-15)
+    np.testing.assert_allclose(oracle.matmul_t_acc_w16(DY, bits, D0), want + D0,
+                               rtol=1e-15, atol=1e-15)
+    with pytest.raises(ValueError):
+        oracle.matmul_t(DY, Wf.T)
+    with pytest.raises(ValueError):
+        oracle.matmul_t_acc(DY, Wf, D0.T)
+
+
+def test_reference_t_forms():
+    rng = np.random.default_rng(5)
+    d = {"DY": rng.standard_normal((5, 8)).astype(np.float32),
+         "W": rng.standard_normal((3, 8)).astype(np.float32),
+         "R": rng.standard_normal((5, 3)).astype(np.float32)}
+    d["DY"][2] = 0.0                      # a zero row accumulates nothing
+    Y, S = oracle.reference("matmul_t_acc", d)
+    assert Y.shape == S.shape == (5, 3)
+    assert np.all(S + 1e-12 >= np.abs(Y - d["R"]))      # |sum| <= sum of |terms|
+    assert np.all(S[2] == 0.0) and np.array_equal(Y[2], d["R"][2].astype(np.float64))
+    Ysub, Ssub = oracle.reference("matmul_t_acc", d, rows=[4, 1])
+    assert np.array_equal(Ysub, Y[[4, 1]]) and np.array_equal(Ssub, S[[4, 1]])

@@ -36,7 +36,7 @@ EXACT_SHAPES = [(256, 256, 128), (129, 136, 20), (1, 8, 4), (300, 264, 68), (128
                 (257, 136, 1028)]
 
 
-@pytest.mark.parametrize("form", wl.FORMS)
+@pytest.mark.parametrize("form", wl.FORWARD_FORMS)
 @pytest.mark.parametrize("shape", EXACT_SHAPES)
 def test_exact_small_integers(form, shape):
     M, N, K = shape
@@ -81,7 +81,7 @@ def test_split_tail_random_reproducible(form):
 RANDOM_SHAPES = [(300, 392, 200), (257, 136, 1028), (64, 1024, 96), (513, 264, 516)]
 
 
-@pytest.mark.parametrize("form", wl.FORMS)
+@pytest.mark.parametrize("form", wl.FORWARD_FORMS)
 @pytest.mark.parametrize("shape", RANDOM_SHAPES)
 def test_random_within_bound(form, shape):
     M, N, K = shape

@@ -10,7 +10,12 @@ from transformer_linear_layer_tcgen05_gb300 import workloads as wl
 def test_shapes_and_dtypes(form):
     M, N, K = 33, 24, 20
     d = wl.generate(form, M, N, K, seed=1)
-    if wl.form_is_swiglu(form):
+    if wl.form_is_t(form):
+        assert d["DY"].shape == (M, N) and d["DY"].dtype == np.float32
+        assert ("R" in d) == wl.form_has_residual(form)
+        if "R" in d:
+            assert d["R"].shape == (M, K) and d["R"].dtype == np.float32
+    elif wl.form_is_swiglu(form):
         assert d["GATE"].shape == (M, K) and d["UP"].shape == (M, K)
         assert d["GATE"].dtype == np.float32 and d["UP"].dtype == np.float32
     else:

@@ -233,6 +233,9 @@ bool f16_preconvert(int num_ng) {
 
 enum Form : int { F_MATMUL = 0, F_RESID = 1, F_SWIGLU = 2 };
 
+// In the kernels' terms: Y[M,N] = A[M,K] · B[K,N] (+ R), A = X or
+// silu(G)·U. B = W [K,N], or, for the transposed product (bt), W given as
+// [N][K] (the backward dX = dY · W^T: X = dY, N = the output columns).
 struct Problem {
   Form form;
   bool w16;
@@ -243,6 +246,8 @@ struct Problem {
   const float* R;
   float* Y;
   int64_t M, N, K;
+  bool bt = false;     // W is [N][K]
+  bool acc = false;    // R is Y itself (Y += A · B)
 };
 
 // `fixed`: where a split tail's workspace comes from instead of the library's
@@ -263,7 +268,8 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
   const int64_t kMax = 0x7fffffffLL;
   if (p.M > kMax || p.N > kMax || p.K > kMax) return LIN_ERROR_UNSUPPORTED_SHAPE;
   if (p.K % 4 != 0 || p.N % 4 != 0) return LIN_ERROR_UNSUPPORTED_SHAPE;
-  if (p.w16 && p.N % 8 != 0) return LIN_ERROR_UNSUPPORTED_SHAPE;
+  // binary16 W rows must be whole 16-byte units for TMA
+  if (p.w16 && (p.bt ? p.K : p.N) % 8 != 0) return LIN_ERROR_UNSUPPORTED_SHAPE;
 
   const uint64_t M = p.M, N = p.N, K = p.K;
   const uint64_t a_bytes = M * K * 4, w_bytes = K * N * (p.w16 ? 2 : 4), mn_bytes = M * N * 4;
@@ -275,8 +281,9 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
                                            : misaligned(p.X))))
     return LIN_ERROR_MISALIGNED;
 
-  // 4. aliasing: Y may overlap no input
-  if (resid && overlaps(p.Y, mn_bytes, p.R, mn_bytes)) return LIN_ERROR_ALIASING;
+  // 4. aliasing: Y may overlap no input (an accumulating call reads and
+  // writes the same Y, element by element)
+  if (resid && !p.acc && overlaps(p.Y, mn_bytes, p.R, mn_bytes)) return LIN_ERROR_ALIASING;
   if (K > 0) {
     if (overlaps(p.Y, mn_bytes, p.W, w_bytes)) return LIN_ERROR_ALIASING;
     if (swiglu) {
@@ -312,9 +319,12 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
   if (fixed && (st = fixed(dev, &fixed_ptr, &fixed_bytes)) != LIN_SUCCESS) return st;
 
   // 7. K == 0: nothing is accumulated, Y = R (or 0)
-  if (K == 0) {
-    cudaError_t e = resid ? cudaMemcpyAsync(p.Y, p.R, mn_bytes, cudaMemcpyDeviceToDevice, stream)
-                          : cudaMemsetAsync(p.Y, 0, mn_bytes, stream);
+  if (K == 0) {   // nothing to accumulate: Y = R (already so when accumulating in place), or 0
+    cudaError_t e = cudaSuccess;
+    if (!resid)
+      e = cudaMemsetAsync(p.Y, 0, mn_bytes, stream);
+    else if (p.R != p.Y)
+      e = cudaMemcpyAsync(p.Y, p.R, mn_bytes, cudaMemcpyDeviceToDevice, stream);
     return e == cudaSuccess ? LIN_SUCCESS : cuda_fail(e);
   }
 
@@ -330,10 +340,17 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
     ok &= encode_2d(&maps.a, f32, a_src, K, M, K * 4, 32, lin::kBM);
     if (swiglu) ok &= encode_2d(&maps.u, f32, p.U, K, M, K * 4, 32, lin::kBM);
   }
-  if (p.w16)
+  if (p.bt) {   // W as [N][K]: boxes of one k-block by the tile's rows
+    if (p.w16)
+      ok &= encode_2d(&maps.w, CU_TENSOR_MAP_DATA_TYPE_UINT16, p.W, K, N, K * 2, 64,
+                      cn > 0 ? (uint32_t)lin::kClusterBN : (uint32_t)bn);
+    else
+      ok &= encode_2d(&maps.w, f32, p.W, K, N, K * 4, 32, (uint32_t)bn);
+  } else if (p.w16) {
     ok &= encode_2d(&maps.w, CU_TENSOR_MAP_DATA_TYPE_UINT16, p.W, N, K, N * 2, 64, 64);
-  else
+  } else {
     ok &= encode_2d(&maps.w, f32, p.W, N, K, N * 4, 32, 32);
+  }
   if (resid) ok &= encode_2d(&maps.r, f32, p.R, N, M, N * 4, lin::kEpiCols, lin::kEpiRows);
   ok &= encode_2d(&maps.y, f32, p.Y, N, M, N * 4, lin::kEpiCols, lin::kEpiRows);
   if (!ok) return cuda_fail(cudaErrorInvalidValue);
@@ -409,6 +426,7 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
     // binary16 X from a pre-pass, in the workspace after the partial tiles
     bool tma_a = !swiglu && !fixed && K % 8 == 0 && f16_preconvert(num_ng);
     auto capacity = [&]() {
+      if (p.bt) return lin::cluster_capacity_bt(tma_a, cn, resid, &ce);
       return swiglu ? lin::cluster_capacity_swiglu(cn, &ce)
                     : (tma_a ? lin::cluster_capacity_tma(cn, resid, &ce)
                              : lin::cluster_capacity_cvt(cn, resid, &ce));
@@ -439,8 +457,12 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
         e = cudaErrorInvalidValue;
       else
         e = lin::launch_cvt_f16(p.X, xh, M * K, sm_count(dev), stream);
-      if (e == cudaSuccess) e = lin::launch_gemm_cluster_tma(cn, resid, maps, args, stream);
+      if (e == cudaSuccess)
+        e = p.bt ? lin::launch_gemm_cluster_bt(true, cn, resid, maps, args, stream)
+                 : lin::launch_gemm_cluster_tma(cn, resid, maps, args, stream);
       kernels = 2;
+    } else if (p.bt) {
+      e = lin::launch_gemm_cluster_bt(false, cn, resid, maps, args, stream);
     } else {
       e = swiglu ? lin::launch_gemm_cluster_swiglu(cn, maps, args, stream)
                  : lin::launch_gemm_cluster_cvt(cn, resid, maps, args, stream);
@@ -470,11 +492,11 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
       }
     }
     if (p.w16)
-      e = lin::launch_gemm_f16(swiglu ? lin::A_SWIGLU_F16 : lin::A_CVT_F16, resid, bn, maps, args,
-                               stream);
+      e = lin::launch_gemm_f16(swiglu ? lin::A_SWIGLU_F16 : lin::A_CVT_F16, resid, bn, p.bt, maps,
+                               args, stream);
     else
-      e = lin::launch_gemm_tf32(swiglu ? lin::A_SWIGLU_F32 : lin::A_TMA_F32, resid, bn, maps,
-                                args, stream);
+      e = lin::launch_gemm_tf32(swiglu ? lin::A_SWIGLU_F32 : lin::A_TMA_F32, resid, bn, p.bt,
+                                maps, args, stream);
     if (e == cudaSuccess && args.split_s >= 2) {
       e = lin::launch_split_reduce(args, resid, 1, bn, 0, tiles_n, stream);
       kernels = 2;
@@ -559,6 +581,39 @@ lin_status lin_matmul_residual_swiglu_a_w16(const float* GATE, const float* UP,
              reinterpret_cast<cudaStream_t>(stream));
 }
 
+// Backward of the linear layer: dX[M,K] = dY[M,N] · W[K,N]^T (+ dX).
+// In the kernels' terms the output has K columns and the contraction runs
+// over N, with W read as [K rows][N] = B^T.
+lin_status lin_matmul_t(const float* DY, const float* W, float* DX, int64_t M, int64_t N,
+                        int64_t K, lin_stream_t stream) {
+  Problem p{F_MATMUL, false, DY, nullptr, nullptr, W, nullptr, DX, M, K, N};
+  p.bt = true;
+  return run(p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+lin_status lin_matmul_t_acc(const float* DY, const float* W, float* DX, int64_t M, int64_t N,
+                            int64_t K, lin_stream_t stream) {
+  Problem p{F_RESID, false, DY, nullptr, nullptr, W, DX, DX, M, K, N};
+  p.bt = true;
+  p.acc = true;
+  return run(p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+lin_status lin_matmul_t_w16(const float* DY, const uint16_t* W16, float* DX, int64_t M, int64_t N,
+                            int64_t K, lin_stream_t stream) {
+  Problem p{F_MATMUL, true, DY, nullptr, nullptr, W16, nullptr, DX, M, K, N};
+  p.bt = true;
+  return run(p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+lin_status lin_matmul_t_acc_w16(const float* DY, const uint16_t* W16, float* DX, int64_t M,
+                                int64_t N, int64_t K, lin_stream_t stream) {
+  Problem p{F_RESID, true, DY, nullptr, nullptr, W16, DX, DX, M, K, N};
+  p.bt = true;
+  p.acc = true;
+  return run(p, reinterpret_cast<cudaStream_t>(stream));
+}
+
 const char* lin_status_string(lin_status status) {
   switch (status) {
     case LIN_SUCCESS: return "LIN_SUCCESS";
@@ -603,7 +658,7 @@ lin_status lin_selftest_wait_timeout(int64_t timeout_us, lin_stream_t stream) {
   args.R = nullptr;
   args.Y = nullptr;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = lin::launch_gemm_tf32(lin::A_TMA_F32, false, 128, maps, args, s);
+  cudaError_t e = lin::launch_gemm_tf32(lin::A_TMA_F32, false, 128, false, maps, args, s);
   if (e != cudaSuccess) return cuda_fail(e);
   return read_and_clear_status(s);
 }

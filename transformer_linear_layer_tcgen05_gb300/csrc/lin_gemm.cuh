@@ -34,7 +34,10 @@
 
 namespace lin {
 
-template <int AMODE, bool RESID, int BN_>
+// BT: W is given as [N][K] (K contiguous; the transposed product dY · W^T
+// of the backward pass, with N the output columns), so its tiles are a
+// K-major B operand that TMA copies as they are.
+template <int AMODE, bool RESID, int BN_, bool BT = false>
 struct GemmTraits {
   static constexpr bool kF16 = (AMODE == A_CVT_F16 || AMODE == A_SWIGLU_F16);
   static constexpr bool kSwiglu = (AMODE == A_SWIGLU_F32 || AMODE == A_SWIGLU_F16);
@@ -44,7 +47,8 @@ struct GemmTraits {
   // TF32 UMMA takes a K-major B only, so for the f32 forms the transform
   // warps transpose the TMA-staged W tile (N contiguous) into a K-major
   // operand; binary16 W is consumed MN-major straight from TMA.
-  static constexpr bool kXformB = !kF16;
+  static constexpr bool kXformB = !kF16 && !BT;
+  static constexpr bool kBT = BT;
   static constexpr bool kXform = kXformA || kXformB;
 
   static constexpr int BM = kBM;
@@ -54,10 +58,12 @@ struct GemmTraits {
   static constexpr int KSTEP = 32 / ESZ;        // UMMA K per instruction (32 bytes)
   static constexpr int NMMA = BK / KSTEP;       // UMMAs per k-block
   static constexpr int W_ATOM = 128 / ESZ;      // W columns per 128-byte run
-  static constexpr int W_BOXES = BN / W_ATOM;   // TMA boxes per W tile
+  static constexpr int W_BOXES = BT ? 1 : BN / W_ATOM;   // TMA boxes per W tile
 
   static constexpr uint32_t A_BYTES = BM * 128;
-  static constexpr uint32_t B_ATOM_BYTES = BK * 128;            // one 128-byte run, BK rows
+  // one 128-byte run of BK rows (MN-major), or the whole [BN rows][128 B]
+  // K-major tile (BT)
+  static constexpr uint32_t B_ATOM_BYTES = BT ? BN * 128 : BK * 128;
   static constexpr uint32_t B_BYTES = W_BOXES * B_ATOM_BYTES;   // = BK * BN * ESZ
   static constexpr uint32_t OP_STAGE_BYTES = A_BYTES + B_BYTES;
   // bytes the TMA delivers straight into an operand stage
@@ -83,8 +89,9 @@ struct GemmTraits {
   static constexpr uint32_t BAR_REGION = 1024;
   static constexpr uint32_t ALIGN_SLACK = 1024;
   // The epilogue buffers alias the raw ring: it is idle once the last
-  // k-block has been transformed.
-  static constexpr uint32_t FIXED_BYTES = NR * RAW_STAGE_BYTES;
+  // k-block has been transformed (with nothing to transform, they stand
+  // alone).
+  static constexpr uint32_t FIXED_BYTES = kXform ? NR * RAW_STAGE_BYTES : EPI_BYTES;
   static constexpr int NS_FIT =
       (int)((SMEM_CAP - BAR_REGION - ALIGN_SLACK - FIXED_BYTES) / OP_STAGE_BYTES);
   static constexpr int NS = NS_FIT > 8 ? 8 : NS_FIT;
@@ -110,12 +117,11 @@ struct GemmTraits {
 
   static constexpr uint32_t TMEM_COLS = BN;
   static constexpr uint32_t IDESC =
-      umma_idesc(kF16 ? 0u : 2u, /*a_mn_major=*/false, /*b_mn_major=*/!kXformB, BM, BN);
+      umma_idesc(kF16 ? 0u : 2u, /*a_mn_major=*/false, /*b_mn_major=*/!kXformB && !BT, BM, BN);
 
-  static_assert(kXform, "every form has at least one transformed operand");
   static_assert(NS >= 2, "operand ring needs two stages");
   static_assert(NR <= 4 && NS <= 8, "barrier slots");
-  static_assert(NR * RAW_STAGE_BYTES >= EPI_BYTES, "epilogue aliasing");
+  static_assert(!kXform || NR * RAW_STAGE_BYTES >= EPI_BYTES, "epilogue aliasing");
   static_assert(OFF_ABORT + 4 <= BAR_REGION, "barrier region");
   static_assert(SMEM_BYTES <= SMEM_CAP, "shared memory");
   static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256 && (BN & (BN - 1)) == 0, "tile width");
@@ -202,14 +208,14 @@ __device__ __forceinline__ void transpose_w_tile(uint32_t b_stage, uint32_t raw_
 
 // ---------------------------------------------------------------- kernel
 
-template <int AMODE, bool RESID, int BN>
+template <int AMODE, bool RESID, int BN, bool BT>
 __global__ void __launch_bounds__(kThreads, 1)
     lin_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                     const __grid_constant__ CUtensorMap tm_u,
                     const __grid_constant__ CUtensorMap tm_w,
                     const __grid_constant__ CUtensorMap tm_r,
                     const __grid_constant__ CUtensorMap tm_y, const KernelArgs args) {
-  using T = GemmTraits<AMODE, RESID, BN>;
+  using T = GemmTraits<AMODE, RESID, BN, BT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -293,7 +299,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(full, T::OP_TMA_BYTES);
           const int kk = (kb0 + kb) * T::BK;
           if constexpr (!T::kXformA) tma_load_2d(a_stage(st), &tm_a, kk, m0, full);
-          if constexpr (!T::kXformB) {
+          if constexpr (T::kBT) {
+            // W as [N][K]: the tile's BN rows, this k-block's 128 bytes
+            tma_load_2d(b_stage(st), &tm_w, kk, n0, full);
+          } else if constexpr (!T::kXformB) {
 #pragma unroll
             for (int j = 0; j < T::W_BOXES; ++j)
               tma_load_2d(b_stage(st) + j * T::B_ATOM_BYTES, &tm_w, n0 + j * T::W_ATOM, kk, full);
@@ -314,15 +323,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int st = kb % T::NS;
       const uint32_t ph = (kb / T::NS) & 1;
       if (T::OP_TMA_BYTES > 0 && !lane0_wait_phase(bar(T::BAR_OP_TMA + st), ph, ctl, lane)) break;
-      if (!lane0_wait_phase(bar(T::BAR_OP_XF + st), ph, ctl, lane)) break;
+      if (T::kXform && !lane0_wait_phase(bar(T::BAR_OP_XF + st), ph, ctl, lane)) break;
       if (lane == 0) {
         tc_fence_after_sync();
 #pragma unroll
         for (int k = 0; k < T::NMMA; ++k) {
           const uint64_t adesc = umma_desc_sw128(a_stage(st) + k * 32, 16, 1024);
-          const uint64_t bdesc =
-              T::kXformB ? umma_desc_sw128(b_stage(st) + k * 32, 16, 1024)
-                         : umma_desc_sw128(b_stage(st) + k * T::KSTEP * 128, T::B_ATOM_BYTES, 1024);
+          const uint64_t bdesc =   // K-major (transposed on chip, or W given as [N][K])
+              (T::kXformB || T::kBT)
+                  ? umma_desc_sw128(b_stage(st) + k * 32, 16, 1024)
+                  : umma_desc_sw128(b_stage(st) + k * T::KSTEP * 128, T::B_ATOM_BYTES, 1024);
           if constexpr (T::kF16)
             umma_f16(tmem, adesc, bdesc, T::IDESC, (kb | k) != 0);
           else
@@ -340,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 3) {
     // ---------------- raw-stage TMA producer (inputs of the transform warps)
-    if (!withhold) {
+    if (T::kXform && !withhold) {
       const int nraw = nkb * T::RAW_PER_KB;
       int filled = 0;
       for (int t = 0; t < nraw; ++t) {
@@ -378,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tid = threadIdx.x - 128;      // 0..127
     bool ok = true;
     int t = 0;
-    for (int kb = 0; kb < nkb && ok; ++kb) {
+    for (int kb = 0; kb < (T::kXform ? nkb : 0) && ok; ++kb) {
       const int st = kb % T::NS;
       const int n = kb / T::NS;
       if (kb >= T::NS && !warp_wait_phase(bar(T::BAR_OP_EMPTY + st), (n - 1) & 1, ctl)) {
@@ -521,10 +531,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // Host-side launcher of one instantiation.
-template <int AMODE, bool RESID, int BN>
+template <int AMODE, bool RESID, int BN, bool BT = false>
 cudaError_t launch_instance(const TensorMaps& m, const KernelArgs& args, cudaStream_t stream) {
-  using T = GemmTraits<AMODE, RESID, BN>;
-  auto kern = lin_gemm_kernel<AMODE, RESID, BN>;
+  using T = GemmTraits<AMODE, RESID, BN, BT>;
+  auto kern = lin_gemm_kernel<AMODE, RESID, BN, BT>;
   // The shared-memory opt-in is per device: remember which devices have it.
   static std::atomic<uint64_t> attr_done{0};
   int dev = 0;

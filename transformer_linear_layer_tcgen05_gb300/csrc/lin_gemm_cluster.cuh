@@ -48,7 +48,9 @@
 
 namespace lin {
 
-template <int AMODE, bool RESID, int BN_, int CN_, bool V8_ = false>
+// BT: W given as [N][K] (K contiguous, the backward product dY · W^T): its
+// tiles are a K-major B operand, one TMA box of BN rows per k-block.
+template <int AMODE, bool RESID, int BN_, int CN_, bool V8_ = false, bool BT_ = false>
 struct ClusterTraits {
   static_assert(AMODE == A_CVT_F16 || AMODE == A_SWIGLU_F16 || AMODE == A_TMA_F16,
                 "binary16 forms only");
@@ -63,7 +65,8 @@ struct ClusterTraits {
   static constexpr int KSTEP = 16;
   static constexpr int NMMA = BK / KSTEP;
   static constexpr int W_ATOM = 64;
-  static constexpr int W_BOXES = BN / W_ATOM;
+  static constexpr bool kBT = BT_;
+  static constexpr int W_BOXES = kBT ? 1 : BN / W_ATOM;
   static constexpr int ROWS = BM / CN;            // A rows this CTA transforms
   static constexpr int INPUTS = kSwiglu ? 2 : 1;  // GATE and UP, or X
   static constexpr int XF_WARPS = kTmaA ? 0 : LIN_XF_WARPS;
@@ -100,7 +103,7 @@ struct ClusterTraits {
   static constexpr int PF = PF_FIT < 1 ? 1 : (PF_FIT > 4 ? 4 : PF_FIT);
 
   static constexpr uint32_t A_BYTES = BM * 128;
-  static constexpr uint32_t B_ATOM_BYTES = BK * 128;
+  static constexpr uint32_t B_ATOM_BYTES = kBT ? BN * 128 : BK * 128;
   static constexpr uint32_t B_BYTES = W_BOXES * B_ATOM_BYTES;
 
   static constexpr uint32_t OP_STAGE_BYTES = A_BYTES + B_BYTES;
@@ -141,7 +144,7 @@ struct ClusterTraits {
   static constexpr uint32_t OFF_ABORT = OFF_TMEM_SLOT + 4;
 
   static constexpr uint32_t TMEM_COLS = 2 * BN;
-  static constexpr uint32_t IDESC = umma_idesc(0u, false, true, BM, BN);
+  static constexpr uint32_t IDESC = umma_idesc(0u, false, /*b_mn_major=*/!kBT, BM, BN);
   static constexpr uint16_t CLUSTER_MASK = (uint16_t)((1u << CN) - 1u);
   static constexpr int kThreadsC = (8 + XF_WARPS) * 32;
 
@@ -246,13 +249,13 @@ __device__ __forceinline__ void stage_store(uint32_t a_stage, uint32_t crank, in
   }
 }
 
-template <int AMODE, bool RESID, int BN, int CN, bool V8>
-__global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8>::kThreadsC, 1)
+template <int AMODE, bool RESID, int BN, int CN, bool V8, bool BT>
+__global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT>::kThreadsC, 1)
     lin_gemm_cluster_kernel(const __grid_constant__ CUtensorMap tm_w,
                             const __grid_constant__ CUtensorMap tm_a,
                             const __grid_constant__ CUtensorMap tm_r,
                             const __grid_constant__ CUtensorMap tm_y, const KernelArgs args) {
-  using T = ClusterTraits<AMODE, RESID, BN, CN, V8>;
+  using T = ClusterTraits<AMODE, RESID, BN, CN, V8, BT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -362,10 +365,14 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8>::kThre
           const uint32_t full = bar(T::BAR_FULL + s);
           // the whole A stage lands here too: one slice from each CTA
           mbar_arrive_expect_tx(full, T::B_BYTES + (T::kTmaA ? T::A_BYTES : 0u));
+          if constexpr (T::kBT) {
+            tma_load_2d(b_stage(s), &tm_w, kb * T::BK, n0, full);   // W as [N][K]
+          } else {
 #pragma unroll
-          for (int j = 0; j < T::W_BOXES; ++j)
-            tma_load_2d(b_stage(s) + j * T::B_ATOM_BYTES, &tm_w, n0 + j * T::W_ATOM, kb * T::BK,
-                        full);
+            for (int j = 0; j < T::W_BOXES; ++j)
+              tma_load_2d(b_stage(s) + j * T::B_ATOM_BYTES, &tm_w, n0 + j * T::W_ATOM, kb * T::BK,
+                          full);
+          }
           if constexpr (T::kTmaA) {
             const uint32_t dst = a_stage(s) + crank * (uint32_t)(T::ROWS * 128);
             const int row = tile_m0(t) + (int)crank * T::ROWS;
@@ -418,7 +425,8 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8>::kThre
           for (int k = 0; k < T::NMMA; ++k) {
             const uint64_t adesc = umma_desc_sw128(a_stage(s) + k * 32, 16, 1024);
             const uint64_t bdesc =
-                umma_desc_sw128(b_stage(s) + k * T::KSTEP * 128, T::B_ATOM_BYTES, 1024);
+                T::kBT ? umma_desc_sw128(b_stage(s) + k * 32, 16, 1024)
+                       : umma_desc_sw128(b_stage(s) + k * T::KSTEP * 128, T::B_ATOM_BYTES, 1024);
             umma_f16(d_tmem, adesc, bdesc, T::IDESC, kb != kb0 || k != 0);
           }
           if constexpr (CN > 1)
@@ -681,9 +689,9 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8>::kThre
 
 // Launch configuration of one instantiation; the first call per device sets
 // the shared-memory attribute and records how many clusters fit at once.
-template <int AMODE, bool RESID, int BN, int CN>
+template <int AMODE, bool RESID, int BN, int CN, bool BT = false>
 struct ClusterLaunch {
-  using T = ClusterTraits<AMODE, RESID, BN, CN>;
+  using T = ClusterTraits<AMODE, RESID, BN, CN, false, BT>;
   // attr must hold 2 entries: the cluster shape and, for launches, the
   // programmatic dependence on the previous kernel of the stream.
   static cudaLaunchConfig_t config(cudaLaunchAttribute* attr, cudaStream_t stream,
@@ -706,7 +714,7 @@ struct ClusterLaunch {
   static int capacity(cudaError_t* err) {
     static std::atomic<uint64_t> attr_done{0};
     static std::atomic<int> max_clusters[64];
-    auto kern = lin_gemm_cluster_kernel<AMODE, RESID, BN, CN, false>;
+    auto kern = lin_gemm_cluster_kernel<AMODE, RESID, BN, CN, false, BT>;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess && dev >= 64) e = cudaErrorInvalidDevice;
@@ -719,9 +727,9 @@ struct ClusterLaunch {
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
       if constexpr (!T::kTmaA) {   // the 32-byte-load variant of the transform
         if (e == cudaSuccess)
-          e = cudaFuncSetAttribute(lin_gemm_cluster_kernel<AMODE, RESID, BN, CN, true>,
+          e = cudaFuncSetAttribute(lin_gemm_cluster_kernel<AMODE, RESID, BN, CN, true, BT>,
                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   ClusterTraits<AMODE, RESID, BN, CN, true>::SMEM_BYTES);
+                                   ClusterTraits<AMODE, RESID, BN, CN, true, BT>::SMEM_BYTES);
       }
       cudaLaunchAttribute attr[2];
       cudaLaunchConfig_t cfg = config(attr, nullptr, false);
@@ -757,11 +765,11 @@ struct ClusterLaunch {
     cfg.gridDim = dim3((unsigned)(clusters * CN), 1, 1);
     if constexpr (!T::kTmaA) {
       if (args.flags & KFLAG_A_V8)
-        return cudaLaunchKernelEx(&cfg, lin_gemm_cluster_kernel<AMODE, RESID, BN, CN, true>, m.w,
-                                  m.a, m.r, m.y, args);
+        return cudaLaunchKernelEx(&cfg, lin_gemm_cluster_kernel<AMODE, RESID, BN, CN, true, BT>,
+                                  m.w, m.a, m.r, m.y, args);
     }
-    return cudaLaunchKernelEx(&cfg, lin_gemm_cluster_kernel<AMODE, RESID, BN, CN, false>, m.w, m.a,
-                              m.r, m.y, args);
+    return cudaLaunchKernelEx(&cfg, lin_gemm_cluster_kernel<AMODE, RESID, BN, CN, false, BT>, m.w,
+                              m.a, m.r, m.y, args);
   }
 };
 

@@ -89,9 +89,9 @@ constexpr int kEpiCols = 32;       // columns per epilogue chunk (128 bytes of f
 // Launchers, one per translation unit family. `bn` is the tile width (128 or
 // 256). They set the shared-memory attribute on first use and launch a grid
 // of (ceil(N/bn), ceil(M/128)) CTAs.
-cudaError_t launch_gemm_tf32(int amode, bool resid, int bn, const TensorMaps& maps,
+cudaError_t launch_gemm_tf32(int amode, bool resid, int bn, bool bt, const TensorMaps& maps,
                              const KernelArgs& args, cudaStream_t stream);
-cudaError_t launch_gemm_f16(int amode, bool resid, int bn, const TensorMaps& maps,
+cudaError_t launch_gemm_f16(int amode, bool resid, int bn, bool bt, const TensorMaps& maps,
                             const KernelArgs& args, cudaStream_t stream);
 
 // Clustered persistent kernels for the binary16-weight forms: a cluster of
@@ -113,6 +113,11 @@ int cluster_capacity_cvt(int cn, bool resid, cudaError_t* err);
 cudaError_t launch_gemm_cluster_tma(int cn, bool resid, const TensorMaps& maps,
                                     const KernelArgs& args, cudaStream_t stream);
 int cluster_capacity_tma(int cn, bool resid, cudaError_t* err);
+// The transposed product dY · W^T (binary16 W given as [N][K]): A rounded by
+// the transform warps, or (tma_a) copied by TMA from the pre-pass's output.
+cudaError_t launch_gemm_cluster_bt(bool tma_a, int cn, bool resid, const TensorMaps& maps,
+                                   const KernelArgs& args, cudaStream_t stream);
+int cluster_capacity_bt(bool tma_a, int cn, bool resid, cudaError_t* err);
 // Xh[i] = binary16(X[i]) (round to nearest even) for i < n, n % 4 == 0,
 // both bases 16-byte aligned.
 cudaError_t launch_cvt_f16(const float* X, uint16_t* Xh, int64_t n, int sms, cudaStream_t stream);

@@ -6,8 +6,13 @@
 
 namespace lin {
 
-cudaError_t launch_gemm_f16(int amode, bool resid, int bn, const TensorMaps& maps,
+cudaError_t launch_gemm_f16(int amode, bool resid, int bn, bool bt, const TensorMaps& maps,
                             const KernelArgs& args, cudaStream_t stream) {
+  if (bt) {   // dY · W^T with binary16 W as [N][K]
+    if (amode != A_CVT_F16 || bn != 128) return cudaErrorInvalidValue;
+    return resid ? launch_instance<A_CVT_F16, true, 128, true>(maps, args, stream)
+                 : launch_instance<A_CVT_F16, false, 128, true>(maps, args, stream);
+  }
   if (bn != 128) return cudaErrorInvalidValue;
   if (amode == A_CVT_F16)
     return resid ? launch_instance<A_CVT_F16, true, 128>(maps, args, stream)

@@ -58,6 +58,10 @@ SIGNATURES = {
     "lin_get_device_status": [_S],
     "lin_selftest_wait_timeout": [_I, _S],
     "lin_matmul_residual_swiglu_a_w16_noalloc": [_P, _P, _P, _P, _P, _I, _I, _I, _S],
+    "lin_matmul_t": [_P, _P, _P, _I, _I, _I, _S],
+    "lin_matmul_t_acc": [_P, _P, _P, _I, _I, _I, _S],
+    "lin_matmul_t_w16": [_P, _P, _P, _I, _I, _I, _S],
+    "lin_matmul_t_acc_w16": [_P, _P, _P, _I, _I, _I, _S],
 }
 
 _lib = None
@@ -223,6 +227,46 @@ def lin_matmul_residual_swiglu_a_w16_noalloc(GATE, UP, W16, R, Y, stream=None):
     return Y
 
 
+def _dims_t(DY, W, DX):
+    M, N = DY.shape
+    K, N2 = W.shape
+    if N2 != N or tuple(DX.shape) != (M, K):
+        raise ValueError(f"shape mismatch: dY{tuple(DY.shape)} W{tuple(W.shape)} dX{tuple(DX.shape)}")
+    return M, N, K
+
+
+def lin_matmul_t(DY, W, DX, stream=None):
+    """dX = dY @ W^T (dY [M,N], W [K,N], dX [M,K]; TF32, f32 accumulate)."""
+    M, N, K = _dims_t(_f32(DY, "dY"), _f32(W, "W"), _f32(DX, "dX"))
+    _call("lin_matmul_t", DY.data_ptr(), W.data_ptr(), DX.data_ptr(), M, N, K,
+          _stream_handle(stream))
+    return DX
+
+
+def lin_matmul_t_acc(DY, W, DX, stream=None):
+    """dX += dY @ W^T."""
+    M, N, K = _dims_t(_f32(DY, "dY"), _f32(W, "W"), _f32(DX, "dX"))
+    _call("lin_matmul_t_acc", DY.data_ptr(), W.data_ptr(), DX.data_ptr(), M, N, K,
+          _stream_handle(stream))
+    return DX
+
+
+def lin_matmul_t_w16(DY, W16, DX, stream=None):
+    """dX = dY @ W16^T with binary16 weights (dY rounded to binary16)."""
+    M, N, K = _dims_t(_f32(DY, "dY"), _w16(W16, "W16"), _f32(DX, "dX"))
+    _call("lin_matmul_t_w16", DY.data_ptr(), W16.data_ptr(), DX.data_ptr(), M, N, K,
+          _stream_handle(stream))
+    return DX
+
+
+def lin_matmul_t_acc_w16(DY, W16, DX, stream=None):
+    """dX += dY @ W16^T with binary16 weights."""
+    M, N, K = _dims_t(_f32(DY, "dY"), _w16(W16, "W16"), _f32(DX, "dX"))
+    _call("lin_matmul_t_acc_w16", DY.data_ptr(), W16.data_ptr(), DX.data_ptr(), M, N, K,
+          _stream_handle(stream))
+    return DX
+
+
 def lin_last_launch_info() -> tuple:
     """(kernels launched, workspace bytes taken) by the last compute call made
     on this thread."""
@@ -249,6 +293,10 @@ FORM_FUNCS = {
     "matmul_w16": lin_matmul_w16,
     "matmul_residual_w16": lin_matmul_residual_w16,
     "matmul_residual_swiglu_a_w16": lin_matmul_residual_swiglu_a_w16,
+    "matmul_t": lin_matmul_t,
+    "matmul_t_acc": lin_matmul_t_acc,
+    "matmul_t_w16": lin_matmul_t_w16,
+    "matmul_t_acc_w16": lin_matmul_t_acc_w16,
 }
 
 
@@ -257,6 +305,12 @@ def run_form(form: str, d: dict, Y, stream=None):
     (keys as produced by ``workloads.generate``: X or GATE/UP, W or W16, R)."""
     f = FORM_FUNCS[form]
     w = d["W16"] if form.endswith("_w16") else d["W"]
+    if form.startswith("matmul_t"):
+        # dX = dY @ W^T; the accumulating forms add into Y, which must hold
+        # the initial dX (d["R"]) when called
+        if "_acc" in form:
+            Y.copy_(d["R"])
+        return f(d["DY"], w, Y, stream=stream)
     if "swiglu" in form:
         return f(d["GATE"], d["UP"], w, d["R"], Y, stream=stream)
     if "residual" in form:

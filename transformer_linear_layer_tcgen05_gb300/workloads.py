@@ -27,7 +27,7 @@ from dataclasses import dataclass
 
 import numpy as np
 
-FORMS = (
+FORWARD_FORMS = (
     "matmul",
     "matmul_residual",
     "matmul_residual_swiglu_a",
@@ -35,10 +35,25 @@ FORMS = (
     "matmul_residual_w16",
     "matmul_residual_swiglu_a_w16",
 )
+# backward input gradient dX[M,K] = dY[M,N] @ W[K,N]^T (+ dX)
+T_FORMS = (
+    "matmul_t",
+    "matmul_t_acc",
+    "matmul_t_w16",
+    "matmul_t_acc_w16",
+)
+FORMS = FORWARD_FORMS + T_FORMS
+
+
+def form_is_t(form: str) -> bool:
+    """dX = dY @ W^T: output [M,K], contraction over N."""
+    return form.startswith("matmul_t")
 
 
 def form_has_residual(form: str) -> bool:
-    return "residual" in form
+    """An R input added to the product: the forward residual [M,N], or the
+    initial dX [M,K] of an accumulating transposed form."""
+    return "residual" in form or "_acc" in form
 
 
 def form_is_swiglu(form: str) -> bool:
@@ -116,7 +131,9 @@ def generate(form: str, M: int, N: int, K: int, seed: int, *, a_var: float = 1.0
     Returns a dict of C-contiguous numpy arrays named as in the C ABI:
     ``X`` [M,K] float32 or ``GATE``/``UP`` [M,K] float32; ``W`` [K,N] float32
     or ``W16`` [K,N] uint16 (binary16 bits); ``R`` [M,N] float32 for the
-    residual forms. ``w_var`` defaults to 1/K.
+    residual forms. ``w_var`` defaults to 1/K. The transposed forms draw
+    ``DY`` [M,N] (variance ``a_var``) in place of X, then W, then ``R`` =
+    the initial dX [M,K] of the accumulating ones.
     """
     if form not in FORMS:
         raise ValueError(f"unknown form {form!r}")
@@ -124,6 +141,16 @@ def generate(form: str, M: int, N: int, K: int, seed: int, *, a_var: float = 1.0
     if w_var is None:
         w_var = 1.0 / max(K, 1)
     out = {}
+    if form_is_t(form):
+        out["DY"] = _normal(rng, (M, N), a_var)
+        w = _normal(rng, (K, N), w_var)
+        if form_is_w16(form):
+            out["W16"] = w.astype(np.float16).view(np.uint16)
+        else:
+            out["W"] = w
+        if form_has_residual(form):
+            out["R"] = _normal(rng, (M, K), r_var)
+        return out
     if form_is_swiglu(form):
         gate = _normal(rng, (M, K), gate_var)
         _outliers(rng, gate, outlier_frac)
@@ -151,8 +178,10 @@ def input_bytes(form: str, M: int, N: int, K: int) -> int:
     """Bytes of every input read once plus Y written once (the algorithmic
     traffic of one call; the SwiGLU hidden matrix is not counted because the
     fused form never stores it)."""
-    a = 2 * M * K * 4 if form_is_swiglu(form) else M * K * 4
     w = K * N * (2 if form_is_w16(form) else 4)
+    if form_is_t(form):   # dY [M,N] in, dX [M,K] out (read too when accumulating)
+        return M * N * 4 + w + (M * K * 4 if form_has_residual(form) else 0) + M * K * 4
+    a = 2 * M * K * 4 if form_is_swiglu(form) else M * K * 4
     r = M * N * 4 if form_has_residual(form) else 0
     y = M * N * 4
     return a + w + r + y
