@@ -97,7 +97,8 @@ def kernel_label(w: wl.Workload) -> str:
     binary16 forms run the clustered kernel: clusters of 4 from N >= 1024,
     pairs from N >= 512, else single CTAs)."""
     if w.form.endswith("_w16"):
-        cn = os.environ.get("LIN_F16_KERNEL") or ("4" if w.N >= 1024 else "2" if w.N >= 512 else "1")
+        cols = w.K if wl.form_is_t(w.form) else w.N   # output columns
+        cn = os.environ.get("LIN_F16_KERNEL") or ("4" if cols >= 1024 else "2" if cols >= 512 else "1")
         if cn == "tile":
             return "lin_gemm_kernel (per-tile, BN=128)"
         return f"lin_gemm_cluster_kernel (BN=256, cluster {cn} along N)"
@@ -284,7 +285,7 @@ def time_small(w: wl.Workload, iters: int, flush_buf):
     import torch
     from transformer_linear_layer_tcgen05_gb300 import lin
     d = device_inputs(wl.generate_workload(w))
-    Y = torch.empty((w.M, w.N), dtype=torch.float32, device="cuda")
+    Y = torch.empty(wl.output_shape(w.form, w.M, w.N, w.K), dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
     for _ in range(5):
         lin.run_form(w.form, d, Y)
@@ -351,7 +352,7 @@ def run_ours(args, rank: int, world: int):
     # ---- inputs resident in HBM before the timed region
     host = wl.generate_workload(w)
     d = device_inputs(host)
-    Y = torch.empty((w.M, w.N), dtype=torch.float32, device="cuda")
+    Y = torch.empty(wl.output_shape(w.form, w.M, w.N, w.K), dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
 
     def step():
@@ -408,7 +409,7 @@ def run_ours(args, rank: int, world: int):
     e2e_steps = 0 if args.no_e2e else max(3, min(args.steps, args.e2e_steps))
     pinned = {k: torch.from_numpy(v.view(np.int16) if v.dtype == np.uint16 else v).pin_memory()
               for k, v in host.items()}
-    y_host = torch.empty((w.M, w.N), dtype=torch.float32).pin_memory()
+    y_host = torch.empty(wl.output_shape(w.form, w.M, w.N, w.K), dtype=torch.float32).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in pinned.values())
     d2h = y_host.numel() * 4
 
@@ -489,6 +490,18 @@ def run_ours(args, rank: int, world: int):
                           "warm_us": warm_us, "warm_tflops": sw.flops / warm_us / 1e6,
                           "warm_frac": sw.flops / warm_us / 1e6 / r})
         line["workloads"] = table
+        # the backward input gradients of the same layers, timed the same way
+        table = []
+        for sw in wl.BACKWARD_WORKLOADS:
+            cold_us, warm_us = time_small(sw, args.small_iters, flush)
+            b, r, tp, _ = roofline(sw, peaks)
+            table.append({"workload": sw.name, "form": sw.form, "M": sw.M, "N": sw.N, "K": sw.K,
+                          "bound": b, "roofline_tflops": r,
+                          "cold_us": cold_us, "cold_tflops": sw.flops / cold_us / 1e6,
+                          "cold_frac": sw.flops / cold_us / 1e6 / r,
+                          "warm_us": warm_us, "warm_tflops": sw.flops / warm_us / 1e6,
+                          "warm_frac": sw.flops / warm_us / 1e6 / r})
+        line["backward"] = table
         del flush
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, host, budget_s=args.cpu_seconds)
@@ -504,7 +517,8 @@ def main():
                          "nvidia-smi clock samples fall inside the timed region)")
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", default=HEADLINE, choices=[w.name for w in wl.WORKLOADS])
+    ap.add_argument("--workload", default=HEADLINE,
+                    choices=[w.name for w in wl.WORKLOADS + wl.BACKWARD_WORKLOADS])
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--small-iters", type=int, default=50)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)

@@ -103,7 +103,22 @@ WORKLOADS = (
              16384, 2048, 8192, w_var=1.0 / 8192),
 )
 
-WORKLOADS_BY_NAME = {w.name: w for w in WORKLOADS}
+# Backward input gradients of the same layers (dX = dY @ W^T; the contraction
+# runs over the forward's output width N): measured beside the forward table,
+# not part of the five configurations.
+BACKWARD_WORKLOADS = (
+    Workload(11, "attn_proj_dx_f32", "matmul_t", 512, 768, 768, w_var=1.0 / 768),
+    Workload(12, "ffn_up_dx_f32", "matmul_t", 512, 3072, 768, w_var=1.0 / 768),
+    Workload(14, "lm_head_dx_w16", "matmul_t_w16", 512, 16384, 768, w_var=0.02),
+    Workload(15, "ffn_down_dx_w16_16k", "matmul_t_w16", 16384, 2048, 8192, w_var=1.0 / 8192),
+)
+
+WORKLOADS_BY_NAME = {w.name: w for w in WORKLOADS + BACKWARD_WORKLOADS}
+
+
+def output_shape(form: str, M: int, N: int, K: int) -> tuple:
+    """Shape of the output: Y [M,N], or dX [M,K] for the transposed forms."""
+    return (M, K) if form_is_t(form) else (M, N)
 
 
 def _normal(rng: np.random.Generator, shape, var: float) -> np.ndarray:
