@@ -219,6 +219,20 @@ lin_status lin_matmul_t_w16(const float *DY, const uint16_t *W16, float *DX,
 lin_status lin_matmul_t_acc_w16(const float *DY, const uint16_t *W16, float *DX,
                                 int64_t M, int64_t N, int64_t K, lin_stream_t stream);
 
+/* Backward of the linear layer, weight gradient: dW[K,N] = X[M,K]^T @ dY[M,N]
+ * (X, dY, dW binary32; TF32 tensor cores, f32 accumulate; the contraction
+ * runs over the M tokens). Like lin_matmul_t it is defined as the adjoint of
+ * the forward product, here with respect to W: for every W,
+ * sum(lin_matmul(X, W) * dY) == sum(W * dW). K % 4 == 0 and N % 4 == 0
+ * (the row strides of X, dY and dW); M is free. dW may overlap no input. */
+lin_status lin_matmul_at(const float *X, const float *DY, float *DW,
+                         int64_t M, int64_t N, int64_t K, lin_stream_t stream);
+
+/* dW += X^T @ dY, dW read and written in place (gradient accumulation over
+ * micro-batches). */
+lin_status lin_matmul_at_acc(const float *X, const float *DY, float *DW,
+                             int64_t M, int64_t N, int64_t K, lin_stream_t stream);
+
 /* Static, NUL-terminated name of a status code ("LIN_SUCCESS", ...). Never NULL. */
 const char *lin_status_string(lin_status status);
 

@@ -34,7 +34,10 @@ gradient of Y = X @ W is the adjoint of the forward map X -> X @ W under the
 Frobenius inner product, dX = dY @ W^T, i.e. the unique dX with
 sum(dX * X) == sum(dY * (X @ W)) for every X; ``matmul_t_acc`` adds it to
 an existing dX (dX += dY @ W^T), ``_w16`` takes W as binary16 bits. dY is
-[M,N], W is [K,N] as the forward stores it, dX is [M,K].
+[M,N], W is [K,N] as the forward stores it, dX is [M,K]. The weight
+gradient (``matmul_at``) is the adjoint with respect to W: dW = X^T @ dY
+[K,N], the unique dW with sum(dW * W) == sum(dY * (X @ W)) for every W;
+``matmul_at_acc`` adds it to an existing dW.
 
 Everything is evaluated in float64. Inputs are widened exactly: float32 to
 float64 by numpy, binary16 bit patterns by ``f16_bits_to_f64`` below (an
@@ -71,6 +74,8 @@ __all__ = [
     "matmul_t_acc",
     "matmul_t_w16",
     "matmul_t_acc_w16",
+    "matmul_at",
+    "matmul_at_acc",
     "normaliser",
     "normalised_error",
     "reference",
@@ -88,6 +93,8 @@ FORMS = (
     "matmul_t_acc",
     "matmul_t_w16",
     "matmul_t_acc_w16",
+    "matmul_at",
+    "matmul_at_acc",
 )
 
 
@@ -226,6 +233,25 @@ def matmul_t_acc_w16(DY, W16, DX0) -> np.ndarray:
     return matmul_t_acc(DY, f16_bits_to_f64(W16), DX0)
 
 
+def matmul_at(X, DY) -> np.ndarray:
+    """dW[K,N] = X[M,K]^T @ dY[M,N]: the adjoint of W -> X @ W (weight
+    gradient of the forward "matmul"), in float64."""
+    X = _f64(X)
+    DY = _f64(DY)
+    if X.ndim != 2 or DY.ndim != 2 or X.shape[0] != DY.shape[0]:
+        raise ValueError(f"shape mismatch: X{X.shape}^T @ dY{DY.shape}")
+    return X.T @ DY
+
+
+def matmul_at_acc(X, DY, DW0) -> np.ndarray:
+    """dW0 + X^T @ dY (the accumulating form)."""
+    Y = matmul_at(X, DY)
+    DW0 = _f64(DW0)
+    if DW0.shape != Y.shape:
+        raise ValueError(f"initial dW shape {DW0.shape} != output shape {Y.shape}")
+    return DW0 + Y
+
+
 # --------------------------------------------------------------------------
 # Acceptance metric
 # --------------------------------------------------------------------------
@@ -279,6 +305,17 @@ def reference(form: str, inputs: dict, rows=None):
     if form not in FORMS:
         raise ValueError(f"unknown form {form!r}")
     sel = (lambda a: a) if rows is None else (lambda a: np.asarray(a)[rows])
+    if form.startswith("matmul_at"):
+        # dW row k depends on column k of X (all rows of X and dY): ``rows``
+        # picks output rows of dW here
+        X = _f64(inputs["X"])
+        DY = _f64(inputs["DY"])
+        Xk = X if rows is None else X[:, rows]
+        if "_acc" in form:
+            Y = matmul_at_acc(Xk, DY, sel(inputs["R"]))
+        else:
+            Y = matmul_at(Xk, DY)
+        return Y, normaliser(Xk.T, DY)
     w16 = form.endswith("_w16")
     W = f16_bits_to_f64(inputs["W16"]) if w16 else _f64(inputs["W"])
     if form.startswith("matmul_t"):

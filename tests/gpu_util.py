@@ -56,6 +56,12 @@ def integer_inputs(form: str, M: int, N: int, K: int, seed: int) -> dict:
     partial sum is an integer below K * 960 < 2**24 for K <= 16384."""
     rng = np.random.default_rng(seed)
     d = {}
+    if wl.form_is_at(form):   # dW[K,N] = X[M,K]^T @ dY[M,N] (+ R [K,N])
+        d["X"] = rng.integers(-4, 5, size=(M, K)).astype(np.float32)
+        d["DY"] = rng.integers(-4, 5, size=(M, N)).astype(np.float32)
+        if wl.form_has_residual(form):
+            d["R"] = rng.integers(-64, 65, size=(K, N)).astype(np.float32)
+        return d
     if wl.form_is_t(form):   # dX[M,K] = dY[M,N] @ W[K,N]^T (+ R [M,K])
         d["DY"] = rng.integers(-4, 5, size=(M, N)).astype(np.float32)
         w = rng.integers(-4, 5, size=(K, N)).astype(np.float32)

@@ -147,3 +147,65 @@ def test_w16_every_kernel_exact(variant):
     r = subprocess.run([sys.executable, "-c", CHILD, ROOT], env=env, cwd=ROOT,
                        stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True, timeout=600)
     assert r.returncode == 0, r.stdout[-4000:]
+
+
+# ---------------------------------------------------------------- weight gradient dW = X^T @ dY
+
+AT_FORMS = wl.AT_FORMS
+# (M, N, K): dW is [K,N]; the contraction runs over the M tokens, which need
+# no alignment (ragged M: 1, 129, 777); the last shapes split M across CTAs
+AT_SHAPES = [(128, 128, 128), (129, 136, 260), (1, 8, 4), (777, 264, 132), (512, 768, 768),
+             (2048, 256, 128)]
+
+
+@pytest.mark.parametrize("form", AT_FORMS)
+@pytest.mark.parametrize("shape", AT_SHAPES)
+def test_weight_gradient_exact_small_integers(form, shape):
+    M, N, K = shape
+    d = integer_inputs(form, M, N, K, seed=M + 7 * N + 3 * K)
+    Y = _run(form, to_device(d), K, N).cpu().numpy().astype(np.float64)
+    Yref, _ = oracle.reference(form, d)
+    assert np.array_equal(Y, Yref), f"max |diff| = {np.max(np.abs(Y - Yref))}"
+
+
+@pytest.mark.parametrize("form", AT_FORMS)
+@pytest.mark.parametrize("shape", [(300, 392, 200), (512, 3072, 768)])
+def test_weight_gradient_random_within_bound(form, shape):
+    M, N, K = shape
+    d = wl.generate(form, M, N, K, seed=41 + M + N)
+    Y = _run(form, to_device(d), K, N).cpu().numpy()
+    assert oracle_error(form, d, Y) <= TOL
+
+
+def test_weight_gradient_is_the_adjoint_in_w():
+    # sum(dY * (X @ W)) == sum(dW * W), both products computed on the GPU
+    import torch
+    M, N, K = 300, 136, 264
+    rng = np.random.default_rng(4)
+    X = rng.integers(-3, 4, size=(M, K)).astype(np.float32)
+    W = rng.integers(-3, 4, size=(K, N)).astype(np.float32)
+    DY = rng.integers(-3, 4, size=(M, N)).astype(np.float32)
+    Xd, Wd, DYd = (torch.from_numpy(a).cuda() for a in (X, W, DY))
+    Y = torch.empty((M, N), device="cuda")
+    DW = torch.empty((K, N), device="cuda")
+    lin.lin_matmul(Xd, Wd, Y)
+    lin.lin_matmul_at(Xd, DYd, DW)
+    torch.cuda.synchronize()
+    lhs = float(np.sum(Y.cpu().numpy().astype(np.float64) * DY))
+    rhs = float(np.sum(DW.cpu().numpy().astype(np.float64) * W))
+    assert lhs == rhs
+
+
+def test_weight_gradient_accumulates_over_micro_batches():
+    # dW over two halves of the tokens, accumulated in place, equals dW over
+    # all tokens (exact on small integers)
+    import torch
+    M, N, K = 512, 256, 384
+    d = integer_inputs("matmul_at", M, N, K, seed=12)
+    X, DY = (torch.from_numpy(d[k]).cuda() for k in ("X", "DY"))
+    DW = torch.zeros((K, N), device="cuda")
+    for h in range(2):
+        rows = slice(h * M // 2, (h + 1) * M // 2)
+        lin.lin_matmul_at_acc(X[rows].contiguous(), DY[rows].contiguous(), DW)
+    torch.cuda.synchronize()
+    assert np.array_equal(DW.cpu().numpy().astype(np.float64), oracle.matmul_at(d["X"], d["DY"]))

@@ -227,11 +227,12 @@ def test_normalised_error_zero_rows():
 
 
 def test_reference_row_subset_equals_full():
-    from transformer_linear_layer_tcgen05_gb300.workloads import generate
+    from transformer_linear_layer_tcgen05_gb300.workloads import generate, output_shape
     for form in oracle.FORMS:
         inp = generate(form, 20, 16, 12, seed=42)
         Y, S = oracle.reference(form, inp)
-        rows = np.array([0, 3, 19, 7])
+        last = output_shape(form, 20, 16, 12)[0] - 1
+        rows = np.array([0, 3, last, 7])
         Yr, Sr = oracle.reference(form, inp, rows=rows)
         assert np.array_equal(Yr, Y[rows]) and np.array_equal(Sr, S[rows])
         assert np.all(S >= np.abs(Y - (inp["R"] if "R" in inp else 0.0)) - 1e-12)
@@ -306,3 +307,46 @@ def test_reference_t_forms():
     assert np.all(S[2] == 0.0) and np.array_equal(Y[2], d["R"][2].astype(np.float64))
     Ysub, Ssub = oracle.reference("matmul_t_acc", d, rows=[4, 1])
     assert np.array_equal(Ysub, Y[[4, 1]]) and np.array_equal(Ssub, S[[4, 1]])
+
+
+# ---------------------------------------------------------------- backward: dW = X^T @ dY
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (3, 2, 5), (5, 4, 1), (2, 6, 3)])
+def test_matmul_at_integer_brute_force(M, N, K):
+    rng = np.random.default_rng(200 + M * 7 + N * 3 + K)
+    X = rng.integers(-4, 5, size=(M, K)).astype(np.float32)
+    DY = rng.integers(-4, 5, size=(M, N)).astype(np.float32)
+    want = np.zeros((K, N))
+    for k, n, m in itertools.product(range(K), range(N), range(M)):
+        want[k, n] += float(X[m, k]) * float(DY[m, n])
+    assert np.array_equal(oracle.matmul_at(X, DY), want)
+
+
+@pytest.mark.parametrize("M,N,K", [(3, 5, 7), (9, 2, 4), (6, 8, 1)])
+def test_matmul_at_is_the_adjoint_in_w(M, N, K):
+    # sum(dY * (X @ W)) == sum(dW * W) for every W, exactly on integers; unit
+    # W pick out single entries of dW
+    rng = np.random.default_rng(13 * M + N + K)
+    X = rng.integers(-5, 6, size=(M, K)).astype(np.float32)
+    W = rng.integers(-5, 6, size=(K, N)).astype(np.float32)
+    DY = rng.integers(-5, 6, size=(M, N)).astype(np.float32)
+    dW = oracle.matmul_at(X, DY)
+    assert float(np.sum(oracle.matmul(X, W) * DY)) == float(np.sum(dW * W))
+    for k, n in [(0, 0), (K - 1, N - 1), (K // 2, N // 2)]:
+        E = np.zeros((K, N), dtype=np.float32)
+        E[k, n] = 1.0
+        assert float(np.sum(oracle.matmul(X, E) * DY)) == dW[k, n]
+
+
+def test_matmul_at_acc_and_reference_rows():
+    rng = np.random.default_rng(17)
+    d = {"X": rng.integers(-4, 5, size=(6, 5)).astype(np.float32),
+         "DY": rng.integers(-4, 5, size=(6, 3)).astype(np.float32),
+         "R": rng.integers(-64, 65, size=(5, 3)).astype(np.float32)}
+    Y, S = oracle.reference("matmul_at_acc", d)
+    assert np.array_equal(Y - oracle.matmul_at(d["X"], d["DY"]), d["R"].astype(np.float64))
+    assert np.all(S >= np.abs(Y - d["R"]))
+    Ysub, Ssub = oracle.reference("matmul_at_acc", d, rows=[4, 0])
+    assert np.array_equal(Ysub, Y[[4, 0]]) and np.array_equal(Ssub, S[[4, 0]])
+    with pytest.raises(ValueError):
+        oracle.matmul_at(d["X"], d["DY"][:5])

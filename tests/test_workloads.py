@@ -10,7 +10,12 @@ from transformer_linear_layer_tcgen05_gb300 import workloads as wl
 def test_shapes_and_dtypes(form):
     M, N, K = 33, 24, 20
     d = wl.generate(form, M, N, K, seed=1)
-    if wl.form_is_t(form):
+    if wl.form_is_at(form):
+        assert d["X"].shape == (M, K) and d["DY"].shape == (M, N)
+        assert ("R" in d) == wl.form_has_residual(form)
+        if "R" in d:
+            assert d["R"].shape == (K, N) and d["R"].dtype == np.float32
+    elif wl.form_is_t(form):
         assert d["DY"].shape == (M, N) and d["DY"].dtype == np.float32
         assert ("R" in d) == wl.form_has_residual(form)
         if "R" in d:
@@ -20,7 +25,9 @@ def test_shapes_and_dtypes(form):
         assert d["GATE"].dtype == np.float32 and d["UP"].dtype == np.float32
     else:
         assert d["X"].shape == (M, K) and d["X"].dtype == np.float32
-    if wl.form_is_w16(form):
+    if wl.form_is_at(form):
+        assert "W" not in d and "W16" not in d
+    elif wl.form_is_w16(form):
         assert d["W16"].shape == (K, N) and d["W16"].dtype == np.uint16
     else:
         assert d["W"].shape == (K, N) and d["W"].dtype == np.float32

@@ -247,6 +247,7 @@ struct Problem {
   float* Y;
   int64_t M, N, K;
   bool bt = false;     // W is [N][K]
+  bool at = false;     // A = X^T: X is [K][M] (the weight gradient X^T · dY, W = dY)
   bool acc = false;    // R is Y itself (Y += A · B)
 };
 
@@ -267,7 +268,9 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
   // 2. shapes
   const int64_t kMax = 0x7fffffffLL;
   if (p.M > kMax || p.N > kMax || p.K > kMax) return LIN_ERROR_UNSUPPORTED_SHAPE;
-  if (p.K % 4 != 0 || p.N % 4 != 0) return LIN_ERROR_UNSUPPORTED_SHAPE;
+  // row strides of the row-major operands: whole 16-byte units (A^T's rows
+  // are M long; its contraction K then needs no rule)
+  if ((p.at ? p.M : p.K) % 4 != 0 || p.N % 4 != 0) return LIN_ERROR_UNSUPPORTED_SHAPE;
   // binary16 W rows must be whole 16-byte units for TMA
   if (p.w16 && (p.bt ? p.K : p.N) % 8 != 0) return LIN_ERROR_UNSUPPORTED_SHAPE;
 
@@ -330,13 +333,15 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
 
   // 8. tensor maps and launch
   const int bn = 128;
-  const int cn = p.w16 ? f16_cluster_size(N) : 0;   // 0: the per-tile kernel
+  const int cn = (p.w16 && !p.at) ? f16_cluster_size(N) : 0;   // 0: the per-tile kernel
   lin::TensorMaps maps;
   std::memset(&maps, 0, sizeof(maps));
   const CUtensorMapDataType f32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   bool ok = true;
   const float* a_src = swiglu ? p.G : p.X;
-  if (cn == 0) {   // the clustered kernels load X / GATE / UP without tensor maps
+  if (p.at) {   // X^T: X is [K rows][M], transposed on chip from [32 x 32] boxes
+    ok &= encode_2d(&maps.a, f32, a_src, M, K, M * 4, 32, 32);
+  } else if (cn == 0) {   // the clustered kernels load X / GATE / UP without tensor maps
     ok &= encode_2d(&maps.a, f32, a_src, K, M, K * 4, 32, lin::kBM);
     if (swiglu) ok &= encode_2d(&maps.u, f32, p.U, K, M, K * 4, 32, lin::kBM);
   }
@@ -495,8 +500,9 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
       e = lin::launch_gemm_f16(swiglu ? lin::A_SWIGLU_F16 : lin::A_CVT_F16, resid, bn, p.bt, maps,
                                args, stream);
     else
-      e = lin::launch_gemm_tf32(swiglu ? lin::A_SWIGLU_F32 : lin::A_TMA_F32, resid, bn, p.bt,
-                                maps, args, stream);
+      e = lin::launch_gemm_tf32(swiglu ? lin::A_SWIGLU_F32
+                                       : (p.at ? lin::A_TRANS_F32 : lin::A_TMA_F32),
+                                resid, bn, p.bt, maps, args, stream);
     if (e == cudaSuccess && args.split_s >= 2) {
       e = lin::launch_split_reduce(args, resid, 1, bn, 0, tiles_n, stream);
       kernels = 2;
@@ -610,6 +616,24 @@ lin_status lin_matmul_t_acc_w16(const float* DY, const uint16_t* W16, float* DX,
                                 int64_t N, int64_t K, lin_stream_t stream) {
   Problem p{F_RESID, true, DY, nullptr, nullptr, W16, DX, DX, M, K, N};
   p.bt = true;
+  p.acc = true;
+  return run(p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+// Weight gradient of the linear layer: dW[K,N] = X[M,K]^T · dY[M,N] (+ dW).
+// In the kernels' terms the output has K rows and the contraction runs over
+// the M tokens, with A = X^T.
+lin_status lin_matmul_at(const float* X, const float* DY, float* DW, int64_t M, int64_t N,
+                         int64_t K, lin_stream_t stream) {
+  Problem p{F_MATMUL, false, X, nullptr, nullptr, DY, nullptr, DW, K, N, M};
+  p.at = true;
+  return run(p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+lin_status lin_matmul_at_acc(const float* X, const float* DY, float* DW, int64_t M, int64_t N,
+                             int64_t K, lin_stream_t stream) {
+  Problem p{F_RESID, false, X, nullptr, nullptr, DY, DW, DW, K, N, M};
+  p.at = true;
   p.acc = true;
   return run(p, reinterpret_cast<cudaStream_t>(stream));
 }

@@ -40,10 +40,12 @@ namespace lin {
 template <int AMODE, bool RESID, int BN_, bool BT = false>
 struct GemmTraits {
   static constexpr bool kF16 = (AMODE == A_CVT_F16 || AMODE == A_SWIGLU_F16);
+  static_assert(AMODE != A_TMA_F16, "the per-tile kernel rounds A itself");
   static constexpr bool kSwiglu = (AMODE == A_SWIGLU_F32 || AMODE == A_SWIGLU_F16);
   static constexpr bool kResid = RESID;
   // The A operand is built by the transform warps unless X is copied as is.
   static constexpr bool kXformA = (AMODE != A_TMA_F32);
+  static constexpr bool kTransA = (AMODE == A_TRANS_F32);   // A = X^T
   // TF32 UMMA takes a K-major B only, so for the f32 forms the transform
   // warps transpose the TMA-staged W tile (N contiguous) into a K-major
   // operand; binary16 W is consumed MN-major straight from TMA.
@@ -362,7 +364,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t full = bar(T::BAR_RAW_FULL + r);
           mbar_arrive_expect_tx(full, T::RAW_STAGE_BYTES);
           const int kk = (kb0 * T::RAW_PER_KB + t) * 32;   // f32 column of this raw stage
-          if constexpr (T::kXformA) {
+          if constexpr (T::kTransA) {
+            // X^T: BM/32 boxes of [32 rows of the contraction][32 of the tile's rows]
+#pragma unroll
+            for (int j = 0; j < T::BM / 32; ++j)
+              tma_load_2d(raw_stage(r) + j * 4096, &tm_a, m0 + j * 32, kk, full);
+          } else if constexpr (T::kXformA) {
             tma_load_2d(raw_stage(r), &tm_a, kk, m0, full);
             if constexpr (T::kSwiglu)
               tma_load_2d(raw_stage(r) + T::RAW_BOX_BYTES, &tm_u, kk, m0, full);
@@ -402,7 +409,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        if constexpr (T::kXformA) transform_raw_stage<AMODE>(a_stage(st), raw_stage(r), h, tid);
+        if constexpr (T::kTransA) transpose_w_tile<T::BM>(a_stage(st), raw_stage(r), q, lane);
+        else if constexpr (T::kXformA) transform_raw_stage<AMODE>(a_stage(st), raw_stage(r), h, tid);
         if constexpr (T::kXformB) transpose_w_tile<BN>(b_stage(st), raw_stage(r) + T::RAW_A_BYTES, q, lane);
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(T::BAR_RAW_EMPTY + r));

@@ -62,6 +62,8 @@ SIGNATURES = {
     "lin_matmul_t_acc": [_P, _P, _P, _I, _I, _I, _S],
     "lin_matmul_t_w16": [_P, _P, _P, _I, _I, _I, _S],
     "lin_matmul_t_acc_w16": [_P, _P, _P, _I, _I, _I, _S],
+    "lin_matmul_at": [_P, _P, _P, _I, _I, _I, _S],
+    "lin_matmul_at_acc": [_P, _P, _P, _I, _I, _I, _S],
 }
 
 _lib = None
@@ -267,6 +269,30 @@ def lin_matmul_t_acc_w16(DY, W16, DX, stream=None):
     return DX
 
 
+def _dims_at(X, DY, DW):
+    M, K = X.shape
+    M2, N = DY.shape
+    if M2 != M or tuple(DW.shape) != (K, N):
+        raise ValueError(f"shape mismatch: X{tuple(X.shape)} dY{tuple(DY.shape)} dW{tuple(DW.shape)}")
+    return M, N, K
+
+
+def lin_matmul_at(X, DY, DW, stream=None):
+    """dW = X^T @ dY (X [M,K], dY [M,N], dW [K,N]; TF32, f32 accumulate)."""
+    M, N, K = _dims_at(_f32(X, "X"), _f32(DY, "dY"), _f32(DW, "dW"))
+    _call("lin_matmul_at", X.data_ptr(), DY.data_ptr(), DW.data_ptr(), M, N, K,
+          _stream_handle(stream))
+    return DW
+
+
+def lin_matmul_at_acc(X, DY, DW, stream=None):
+    """dW += X^T @ dY."""
+    M, N, K = _dims_at(_f32(X, "X"), _f32(DY, "dY"), _f32(DW, "dW"))
+    _call("lin_matmul_at_acc", X.data_ptr(), DY.data_ptr(), DW.data_ptr(), M, N, K,
+          _stream_handle(stream))
+    return DW
+
+
 def lin_last_launch_info() -> tuple:
     """(kernels launched, workspace bytes taken) by the last compute call made
     on this thread."""
@@ -297,6 +323,8 @@ FORM_FUNCS = {
     "matmul_t_acc": lin_matmul_t_acc,
     "matmul_t_w16": lin_matmul_t_w16,
     "matmul_t_acc_w16": lin_matmul_t_acc_w16,
+    "matmul_at": lin_matmul_at,
+    "matmul_at_acc": lin_matmul_at_acc,
 }
 
 
@@ -304,6 +332,11 @@ def run_form(form: str, d: dict, Y, stream=None):
     """Call the entry point of ``form`` with the device tensors of dict ``d``
     (keys as produced by ``workloads.generate``: X or GATE/UP, W or W16, R)."""
     f = FORM_FUNCS[form]
+    if form.startswith("matmul_at"):
+        # dW = X^T @ dY; the accumulating form adds into Y (initial dW = d["R"])
+        if "_acc" in form:
+            Y.copy_(d["R"])
+        return f(d["X"], d["DY"], Y, stream=stream)
     w = d["W16"] if form.endswith("_w16") else d["W"]
     if form.startswith("matmul_t"):
         # dX = dY @ W^T; the accumulating forms add into Y, which must hold

@@ -42,12 +42,22 @@ T_FORMS = (
     "matmul_t_w16",
     "matmul_t_acc_w16",
 )
-FORMS = FORWARD_FORMS + T_FORMS
+# backward weight gradient dW[K,N] = X[M,K]^T @ dY[M,N] (+ dW)
+AT_FORMS = (
+    "matmul_at",
+    "matmul_at_acc",
+)
+FORMS = FORWARD_FORMS + T_FORMS + AT_FORMS
 
 
 def form_is_t(form: str) -> bool:
     """dX = dY @ W^T: output [M,K], contraction over N."""
     return form.startswith("matmul_t")
+
+
+def form_is_at(form: str) -> bool:
+    """dW = X^T @ dY: output [K,N], contraction over the M rows."""
+    return form.startswith("matmul_at")
 
 
 def form_has_residual(form: str) -> bool:
@@ -109,6 +119,8 @@ WORKLOADS = (
 BACKWARD_WORKLOADS = (
     Workload(11, "attn_proj_dx_f32", "matmul_t", 512, 768, 768, w_var=1.0 / 768),
     Workload(12, "ffn_up_dx_f32", "matmul_t", 512, 3072, 768, w_var=1.0 / 768),
+    Workload(13, "attn_proj_dw_f32", "matmul_at", 512, 768, 768, w_var=1.0),
+    Workload(16, "ffn_up_dw_f32", "matmul_at", 512, 3072, 768, w_var=1.0),
     Workload(14, "lm_head_dx_w16", "matmul_t_w16", 512, 16384, 768, w_var=0.02),
     Workload(15, "ffn_down_dx_w16_16k", "matmul_t_w16", 16384, 2048, 8192, w_var=1.0 / 8192),
 )
@@ -117,7 +129,9 @@ WORKLOADS_BY_NAME = {w.name: w for w in WORKLOADS + BACKWARD_WORKLOADS}
 
 
 def output_shape(form: str, M: int, N: int, K: int) -> tuple:
-    """Shape of the output: Y [M,N], or dX [M,K] for the transposed forms."""
+    """Shape of the output: Y [M,N], dX [M,K] (transposed forms) or dW [K,N]."""
+    if form_is_at(form):
+        return (K, N)
     return (M, K) if form_is_t(form) else (M, N)
 
 
@@ -148,7 +162,9 @@ def generate(form: str, M: int, N: int, K: int, seed: int, *, a_var: float = 1.0
     or ``W16`` [K,N] uint16 (binary16 bits); ``R`` [M,N] float32 for the
     residual forms. ``w_var`` defaults to 1/K. The transposed forms draw
     ``DY`` [M,N] (variance ``a_var``) in place of X, then W, then ``R`` =
-    the initial dX [M,K] of the accumulating ones.
+    the initial dX [M,K] of the accumulating ones. The weight-gradient forms
+    draw ``X`` [M,K], ``DY`` [M,N] (variance ``w_var``) and ``R`` = the
+    initial dW [K,N].
     """
     if form not in FORMS:
         raise ValueError(f"unknown form {form!r}")
@@ -156,6 +172,12 @@ def generate(form: str, M: int, N: int, K: int, seed: int, *, a_var: float = 1.0
     if w_var is None:
         w_var = 1.0 / max(K, 1)
     out = {}
+    if form_is_at(form):   # X [M,K], dY [M,N], R = the initial dW [K,N]
+        out["X"] = _normal(rng, (M, K), a_var)
+        out["DY"] = _normal(rng, (M, N), w_var)
+        if form_has_residual(form):
+            out["R"] = _normal(rng, (K, N), r_var)
+        return out
     if form_is_t(form):
         out["DY"] = _normal(rng, (M, N), a_var)
         w = _normal(rng, (K, N), w_var)
@@ -194,6 +216,8 @@ def input_bytes(form: str, M: int, N: int, K: int) -> int:
     traffic of one call; the SwiGLU hidden matrix is not counted because the
     fused form never stores it)."""
     w = K * N * (2 if form_is_w16(form) else 4)
+    if form_is_at(form):  # X, dY in; dW [K,N] out (read too when accumulating)
+        return M * K * 4 + M * N * 4 + (K * N * 4 if form_has_residual(form) else 0) + K * N * 4
     if form_is_t(form):   # dY [M,N] in, dX [M,K] out (read too when accumulating)
         return M * N * 4 + w + (M * K * 4 if form_has_residual(form) else 0) + M * K * 4
     a = 2 * M * K * 4 if form_is_swiglu(form) else M * K * 4
