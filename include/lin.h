@@ -233,6 +233,20 @@ lin_status lin_matmul_at(const float *X, const float *DY, float *DW,
 lin_status lin_matmul_at_acc(const float *X, const float *DY, float *DW,
                              int64_t M, int64_t N, int64_t K, lin_stream_t stream);
 
+/* Weight gradient of the SwiGLU down projection: dW[K,N] =
+ * (silu(GATE) * UP)^T @ dY, GATE and UP [M,K] (K = d_ff), dY [M,N], dW [K,N]
+ * (W_down's shape). The product silu(GATE) * UP is recomputed on chip, as in
+ * the forward lin_matmul_residual_swiglu_a, and never stored; TF32 tensor
+ * cores. K % 4 == 0, N % 4 == 0; M is free. */
+lin_status lin_matmul_at_swiglu_a(const float *GATE, const float *UP, const float *DY,
+                                  float *DW, int64_t M, int64_t N, int64_t K,
+                                  lin_stream_t stream);
+
+/* dW += (silu(GATE) * UP)^T @ dY, dW in place. */
+lin_status lin_matmul_at_swiglu_a_acc(const float *GATE, const float *UP, const float *DY,
+                                      float *DW, int64_t M, int64_t N, int64_t K,
+                                      lin_stream_t stream);
+
 /* Static, NUL-terminated name of a status code ("LIN_SUCCESS", ...). Never NULL. */
 const char *lin_status_string(lin_status status);
 

@@ -37,7 +37,9 @@ an existing dX (dX += dY @ W^T), ``_w16`` takes W as binary16 bits. dY is
 [M,N], W is [K,N] as the forward stores it, dX is [M,K]. The weight
 gradient (``matmul_at``) is the adjoint with respect to W: dW = X^T @ dY
 [K,N], the unique dW with sum(dW * W) == sum(dY * (X @ W)) for every W;
-``matmul_at_acc`` adds it to an existing dW.
+``matmul_at_acc`` adds it to an existing dW. ``matmul_at_swiglu_a`` is the
+weight gradient of the SwiGLU down projection, (silu(GATE) * UP)^T @ dY,
+the left factor recomputed from GATE and UP as in the forward form.
 
 Everything is evaluated in float64. Inputs are widened exactly: float32 to
 float64 by numpy, binary16 bit patterns by ``f16_bits_to_f64`` below (an
@@ -76,6 +78,8 @@ __all__ = [
     "matmul_t_acc_w16",
     "matmul_at",
     "matmul_at_acc",
+    "matmul_at_swiglu_a",
+    "matmul_at_swiglu_a_acc",
     "normaliser",
     "normalised_error",
     "reference",
@@ -95,6 +99,8 @@ FORMS = (
     "matmul_t_acc_w16",
     "matmul_at",
     "matmul_at_acc",
+    "matmul_at_swiglu_a",
+    "matmul_at_swiglu_a_acc",
 )
 
 
@@ -252,6 +258,21 @@ def matmul_at_acc(X, DY, DW0) -> np.ndarray:
     return DW0 + Y
 
 
+def matmul_at_swiglu_a(GATE, UP, DY) -> np.ndarray:
+    """dW[K,N] = (silu(GATE) * UP)[M,K]^T @ dY[M,N]: the weight gradient of
+    W_down in matmul_residual_swiglu_a, in float64."""
+    GATE = _f64(GATE)
+    UP = _f64(UP)
+    if GATE.shape != UP.shape:
+        raise ValueError(f"GATE{GATE.shape} and UP{UP.shape} differ")
+    return matmul_at(swiglu_a(GATE, UP), DY)
+
+
+def matmul_at_swiglu_a_acc(GATE, UP, DY, DW0) -> np.ndarray:
+    """dW0 + (silu(GATE) * UP)^T @ dY."""
+    return matmul_at_acc(swiglu_a(_f64(GATE), _f64(UP)), DY, DW0)
+
+
 # --------------------------------------------------------------------------
 # Acceptance metric
 # --------------------------------------------------------------------------
@@ -308,7 +329,7 @@ def reference(form: str, inputs: dict, rows=None):
     if form.startswith("matmul_at"):
         # dW row k depends on column k of X (all rows of X and dY): ``rows``
         # picks output rows of dW here
-        X = _f64(inputs["X"])
+        X = swiglu_a(inputs["GATE"], inputs["UP"]) if "swiglu" in form else _f64(inputs["X"])
         DY = _f64(inputs["DY"])
         Xk = X if rows is None else X[:, rows]
         if "_acc" in form:

@@ -57,7 +57,11 @@ def integer_inputs(form: str, M: int, N: int, K: int, seed: int) -> dict:
     rng = np.random.default_rng(seed)
     d = {}
     if wl.form_is_at(form):   # dW[K,N] = X[M,K]^T @ dY[M,N] (+ R [K,N])
-        d["X"] = rng.integers(-4, 5, size=(M, K)).astype(np.float32)
+        if wl.form_is_swiglu(form):
+            d["GATE"] = rng.integers(40, 61, size=(M, K)).astype(np.float32)
+            d["UP"] = rng.integers(-4, 5, size=(M, K)).astype(np.float32)
+        else:
+            d["X"] = rng.integers(-4, 5, size=(M, K)).astype(np.float32)
         d["DY"] = rng.integers(-4, 5, size=(M, N)).astype(np.float32)
         if wl.form_has_residual(form):
             d["R"] = rng.integers(-64, 65, size=(K, N)).astype(np.float32)

@@ -209,3 +209,24 @@ def test_weight_gradient_accumulates_over_micro_batches():
         lin.lin_matmul_at_acc(X[rows].contiguous(), DY[rows].contiguous(), DW)
     torch.cuda.synchronize()
     assert np.array_equal(DW.cpu().numpy().astype(np.float64), oracle.matmul_at(d["X"], d["DY"]))
+
+
+def test_swiglu_weight_gradient_is_the_adjoint_of_the_forward_kernel():
+    # sum(dY * (silu(G)*U) @ W) == sum(dW_down * W), both sides on the GPU;
+    # GATE >= 40 keeps every value an exact small integer in TF32
+    import torch
+    M, N, K = 333, 136, 264
+    rng = np.random.default_rng(6)
+    G = rng.integers(40, 61, size=(M, K)).astype(np.float32)
+    U = rng.integers(-3, 4, size=(M, K)).astype(np.float32)
+    W = rng.integers(-3, 4, size=(K, N)).astype(np.float32)
+    DY = rng.integers(-3, 4, size=(M, N)).astype(np.float32)
+    Gd, Ud, Wd, DYd = (torch.from_numpy(a).cuda() for a in (G, U, W, DY))
+    Y = torch.empty((M, N), device="cuda")
+    DW = torch.empty((K, N), device="cuda")
+    lin.lin_matmul_residual_swiglu_a(Gd, Ud, Wd, torch.zeros((M, N), device="cuda"), Y)
+    lin.lin_matmul_at_swiglu_a(Gd, Ud, DYd, DW)
+    torch.cuda.synchronize()
+    lhs = float(np.sum(Y.cpu().numpy().astype(np.float64) * DY))
+    rhs = float(np.sum(DW.cpu().numpy().astype(np.float64) * W))
+    assert lhs == rhs

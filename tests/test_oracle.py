@@ -350,3 +350,23 @@ def test_matmul_at_acc_and_reference_rows():
     assert np.array_equal(Ysub, Y[[4, 0]]) and np.array_equal(Ssub, S[[4, 0]])
     with pytest.raises(ValueError):
         oracle.matmul_at(d["X"], d["DY"][:5])
+
+
+def test_matmul_at_swiglu_a_is_the_adjoint_of_the_swiglu_form():
+    # GATE >= 40: sigma(GATE) == 1.0 in float64, so A = GATE * UP exactly and
+    # the identity sum(dY * Y(W)) == sum(dW * W) holds exactly (R = 0)
+    rng = np.random.default_rng(23)
+    M, N, K = 7, 5, 6
+    G = rng.integers(40, 61, size=(M, K)).astype(np.float32)
+    U = rng.integers(-4, 5, size=(M, K)).astype(np.float32)
+    W = rng.integers(-4, 5, size=(K, N)).astype(np.float32)
+    DY = rng.integers(-4, 5, size=(M, N)).astype(np.float32)
+    Y = oracle.matmul_residual_swiglu_a(G, U, W, np.zeros((M, N), dtype=np.float32))
+    dW = oracle.matmul_at_swiglu_a(G, U, DY)
+    assert float(np.sum(Y * DY)) == float(np.sum(dW * W))
+    want = np.zeros((K, N))
+    for k, n, m in itertools.product(range(K), range(N), range(M)):
+        want[k, n] += float(G[m, k]) * float(U[m, k]) * float(DY[m, n])
+    assert np.array_equal(dW, want)
+    D0 = rng.integers(-64, 65, size=(K, N)).astype(np.float32)
+    assert np.array_equal(oracle.matmul_at_swiglu_a_acc(G, U, DY, D0) - dW, D0.astype(np.float64))

@@ -11,7 +11,8 @@ def test_shapes_and_dtypes(form):
     M, N, K = 33, 24, 20
     d = wl.generate(form, M, N, K, seed=1)
     if wl.form_is_at(form):
-        assert d["X"].shape == (M, K) and d["DY"].shape == (M, N)
+        assert d["GATE" if wl.form_is_swiglu(form) else "X"].shape == (M, K)
+        assert d["DY"].shape == (M, N)
         assert ("R" in d) == wl.form_has_residual(form)
         if "R" in d:
             assert d["R"].shape == (K, N) and d["R"].dtype == np.float32

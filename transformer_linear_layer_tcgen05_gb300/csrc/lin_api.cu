@@ -260,7 +260,8 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
   // 1. dims and required pointers
   if (p.M < 0 || p.N < 0 || p.K < 0) return LIN_ERROR_INVALID_VALUE;
   if (p.M == 0 || p.N == 0) return LIN_SUCCESS;
-  const bool resid = p.form != F_MATMUL;
+  // an R operand: the forward residual forms, and every accumulating form
+  const bool resid = p.acc || p.form == F_RESID || (p.form == F_SWIGLU && !p.at);
   const bool swiglu = p.form == F_SWIGLU;
   if (!p.Y || (resid && !p.R)) return LIN_ERROR_INVALID_VALUE;
   if (p.K > 0 && (!p.W || (swiglu ? (!p.G || !p.U) : !p.X))) return LIN_ERROR_INVALID_VALUE;
@@ -341,6 +342,7 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
   const float* a_src = swiglu ? p.G : p.X;
   if (p.at) {   // X^T: X is [K rows][M], transposed on chip from [32 x 32] boxes
     ok &= encode_2d(&maps.a, f32, a_src, M, K, M * 4, 32, 32);
+    if (swiglu) ok &= encode_2d(&maps.u, f32, p.U, M, K, M * 4, 32, 32);
   } else if (cn == 0) {   // the clustered kernels load X / GATE / UP without tensor maps
     ok &= encode_2d(&maps.a, f32, a_src, K, M, K * 4, 32, lin::kBM);
     if (swiglu) ok &= encode_2d(&maps.u, f32, p.U, K, M, K * 4, 32, lin::kBM);
@@ -500,7 +502,7 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
       e = lin::launch_gemm_f16(swiglu ? lin::A_SWIGLU_F16 : lin::A_CVT_F16, resid, bn, p.bt, maps,
                                args, stream);
     else
-      e = lin::launch_gemm_tf32(swiglu ? lin::A_SWIGLU_F32
+      e = lin::launch_gemm_tf32(swiglu ? (p.at ? lin::A_TRANS_SWIGLU_F32 : lin::A_SWIGLU_F32)
                                        : (p.at ? lin::A_TRANS_F32 : lin::A_TMA_F32),
                                 resid, bn, p.bt, maps, args, stream);
     if (e == cudaSuccess && args.split_s >= 2) {
@@ -633,6 +635,24 @@ lin_status lin_matmul_at(const float* X, const float* DY, float* DW, int64_t M, 
 lin_status lin_matmul_at_acc(const float* X, const float* DY, float* DW, int64_t M, int64_t N,
                              int64_t K, lin_stream_t stream) {
   Problem p{F_RESID, false, X, nullptr, nullptr, DY, DW, DW, K, N, M};
+  p.at = true;
+  p.acc = true;
+  return run(p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+// Weight gradient of the SwiGLU down projection: dW[K,N] =
+// (silu(GATE) * UP)[M,K]^T · dY[M,N] (+ dW), the product recomputed on chip.
+lin_status lin_matmul_at_swiglu_a(const float* GATE, const float* UP, const float* DY, float* DW,
+                                  int64_t M, int64_t N, int64_t K, lin_stream_t stream) {
+  Problem p{F_SWIGLU, false, nullptr, GATE, UP, DY, nullptr, DW, K, N, M};
+  p.at = true;
+  return run(p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+lin_status lin_matmul_at_swiglu_a_acc(const float* GATE, const float* UP, const float* DY,
+                                      float* DW, int64_t M, int64_t N, int64_t K,
+                                      lin_stream_t stream) {
+  Problem p{F_SWIGLU, false, nullptr, GATE, UP, DY, DW, DW, K, N, M};
   p.at = true;
   p.acc = true;
   return run(p, reinterpret_cast<cudaStream_t>(stream));

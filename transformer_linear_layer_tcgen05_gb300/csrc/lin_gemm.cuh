@@ -41,11 +41,12 @@ template <int AMODE, bool RESID, int BN_, bool BT = false>
 struct GemmTraits {
   static constexpr bool kF16 = (AMODE == A_CVT_F16 || AMODE == A_SWIGLU_F16);
   static_assert(AMODE != A_TMA_F16, "the per-tile kernel rounds A itself");
-  static constexpr bool kSwiglu = (AMODE == A_SWIGLU_F32 || AMODE == A_SWIGLU_F16);
+  static constexpr bool kSwiglu =
+      (AMODE == A_SWIGLU_F32 || AMODE == A_SWIGLU_F16 || AMODE == A_TRANS_SWIGLU_F32);
   static constexpr bool kResid = RESID;
   // The A operand is built by the transform warps unless X is copied as is.
   static constexpr bool kXformA = (AMODE != A_TMA_F32);
-  static constexpr bool kTransA = (AMODE == A_TRANS_F32);   // A = X^T
+  static constexpr bool kTransA = (AMODE == A_TRANS_F32 || AMODE == A_TRANS_SWIGLU_F32);  // A = X^T
   // TF32 UMMA takes a K-major B only, so for the f32 forms the transform
   // warps transpose the TMA-staged W tile (N contiguous) into a K-major
   // operand; binary16 W is consumed MN-major straight from TMA.
@@ -204,6 +205,35 @@ __device__ __forceinline__ void transpose_w_tile(uint32_t b_stage, uint32_t raw_
         v[e] = ld_shared_u32(src + k * 128u + ((col ^ (k & 7u)) << 4) + word);
       }
       st_shared_v4(b_stage + sw128(n, c), v[0], v[1], v[2], v[3]);
+    }
+  }
+}
+
+// TF32 A operand of a weight gradient: (silu(GATE) * UP)^T. The raw stage
+// holds [32 rows of the contraction][32 columns] boxes of GATE and of UP
+// (BM/32 of each, UP at `raw_u`); warp q forms silu(g) * u of runs q, q+4,
+// ... and writes them transposed, exactly as transpose_w_tile moves W.
+template <int BM>
+__device__ __forceinline__ void transpose_swiglu_tile(uint32_t a_stage, uint32_t raw_g,
+                                                      uint32_t raw_u, int q, int lane) {
+#pragma unroll 1
+  for (int j = q; j < BM / 32; j += 4) {
+    const uint32_t n = (uint32_t)(j * 32 + lane);
+    const uint32_t sg = raw_g + (uint32_t)j * 4096u;
+    const uint32_t su = raw_u + (uint32_t)j * 4096u;
+    const uint32_t col = ((uint32_t)lane >> 2), word = ((uint32_t)lane & 3u) * 4u;
+#pragma unroll
+    for (uint32_t c = 0; c < 8; ++c) {
+      uint32_t v[4];
+#pragma unroll
+      for (uint32_t e = 0; e < 4; ++e) {
+        const uint32_t k = 4 * c + e;
+        const uint32_t off = k * 128u + ((col ^ (k & 7u)) << 4) + word;
+        const float g = __uint_as_float(ld_shared_u32(sg + off));
+        const float u = __uint_as_float(ld_shared_u32(su + off));
+        v[e] = __float_as_uint(silu_stable(g) * u);
+      }
+      st_shared_v4(a_stage + sw128(n, c), v[0], v[1], v[2], v[3]);
     }
   }
 }
@@ -367,8 +397,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if constexpr (T::kTransA) {
             // X^T: BM/32 boxes of [32 rows of the contraction][32 of the tile's rows]
 #pragma unroll
-            for (int j = 0; j < T::BM / 32; ++j)
+            for (int j = 0; j < T::BM / 32; ++j) {
               tma_load_2d(raw_stage(r) + j * 4096, &tm_a, m0 + j * 32, kk, full);
+              if constexpr (T::kSwiglu)
+                tma_load_2d(raw_stage(r) + T::RAW_BOX_BYTES + j * 4096, &tm_u, m0 + j * 32, kk,
+                            full);
+            }
           } else if constexpr (T::kXformA) {
             tma_load_2d(raw_stage(r), &tm_a, kk, m0, full);
             if constexpr (T::kSwiglu)
@@ -409,7 +443,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        if constexpr (T::kTransA) transpose_w_tile<T::BM>(a_stage(st), raw_stage(r), q, lane);
+        if constexpr (T::kTransA && T::kSwiglu)
+          transpose_swiglu_tile<T::BM>(a_stage(st), raw_stage(r),
+                                       raw_stage(r) + T::RAW_BOX_BYTES, q, lane);
+        else if constexpr (T::kTransA)
+          transpose_w_tile<T::BM>(a_stage(st), raw_stage(r), q, lane);
         else if constexpr (T::kXformA) transform_raw_stage<AMODE>(a_stage(st), raw_stage(r), h, tid);
         if constexpr (T::kXformB) transpose_w_tile<BN>(b_stage(st), raw_stage(r) + T::RAW_A_BYTES, q, lane);
         __syncwarp();

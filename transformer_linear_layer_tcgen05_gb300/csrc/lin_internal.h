@@ -20,6 +20,8 @@ enum AMode : int {
   A_TMA_F16 = 4,     // X rounded to binary16 by a pre-pass, copied by TMA (clustered kernels)
   A_TRANS_F32 = 5,   // A = X^T (the weight gradient X^T dY): TMA-staged [32 m][32 k] tiles
                      // of X transposed on chip into the K-major TF32 operand
+  A_TRANS_SWIGLU_F32 = 6,  // A = (silu(GATE) * UP)^T, recomputed from staged GATE/UP tiles
+                           // and transposed on chip (the weight gradient of W_down)
 };
 
 enum : uint32_t {

@@ -19,6 +19,9 @@ cudaError_t launch_gemm_tf32(int amode, bool resid, int bn, bool bt, const Tenso
   if (amode == A_TRANS_F32)   // the weight gradient X^T dY (+ dW)
     return resid ? launch_instance<A_TRANS_F32, true, 128>(maps, args, stream)
                  : launch_instance<A_TRANS_F32, false, 128>(maps, args, stream);
+  if (amode == A_TRANS_SWIGLU_F32)   // the weight gradient of W_down (+ dW)
+    return resid ? launch_instance<A_TRANS_SWIGLU_F32, true, 128>(maps, args, stream)
+                 : launch_instance<A_TRANS_SWIGLU_F32, false, 128>(maps, args, stream);
   if (amode == A_SWIGLU_F32 && resid)
     return launch_instance<A_SWIGLU_F32, true, 128>(maps, args, stream);
   return cudaErrorInvalidValue;

@@ -64,6 +64,8 @@ SIGNATURES = {
     "lin_matmul_t_acc_w16": [_P, _P, _P, _I, _I, _I, _S],
     "lin_matmul_at": [_P, _P, _P, _I, _I, _I, _S],
     "lin_matmul_at_acc": [_P, _P, _P, _I, _I, _I, _S],
+    "lin_matmul_at_swiglu_a": [_P, _P, _P, _P, _I, _I, _I, _S],
+    "lin_matmul_at_swiglu_a_acc": [_P, _P, _P, _P, _I, _I, _I, _S],
 }
 
 _lib = None
@@ -293,6 +295,26 @@ def lin_matmul_at_acc(X, DY, DW, stream=None):
     return DW
 
 
+def lin_matmul_at_swiglu_a(GATE, UP, DY, DW, stream=None):
+    """dW = (silu(GATE) * UP)^T @ dY (GATE, UP [M,K], dY [M,N], dW [K,N])."""
+    M, N, K = _dims_at(_f32(GATE, "GATE"), _f32(DY, "dY"), _f32(DW, "dW"))
+    if tuple(_f32(UP, "UP").shape) != (M, K):
+        raise ValueError("UP must be [M, K]")
+    _call("lin_matmul_at_swiglu_a", GATE.data_ptr(), UP.data_ptr(), DY.data_ptr(),
+          DW.data_ptr(), M, N, K, _stream_handle(stream))
+    return DW
+
+
+def lin_matmul_at_swiglu_a_acc(GATE, UP, DY, DW, stream=None):
+    """dW += (silu(GATE) * UP)^T @ dY."""
+    M, N, K = _dims_at(_f32(GATE, "GATE"), _f32(DY, "dY"), _f32(DW, "dW"))
+    if tuple(_f32(UP, "UP").shape) != (M, K):
+        raise ValueError("UP must be [M, K]")
+    _call("lin_matmul_at_swiglu_a_acc", GATE.data_ptr(), UP.data_ptr(), DY.data_ptr(),
+          DW.data_ptr(), M, N, K, _stream_handle(stream))
+    return DW
+
+
 def lin_last_launch_info() -> tuple:
     """(kernels launched, workspace bytes taken) by the last compute call made
     on this thread."""
@@ -325,6 +347,8 @@ FORM_FUNCS = {
     "matmul_t_acc_w16": lin_matmul_t_acc_w16,
     "matmul_at": lin_matmul_at,
     "matmul_at_acc": lin_matmul_at_acc,
+    "matmul_at_swiglu_a": lin_matmul_at_swiglu_a,
+    "matmul_at_swiglu_a_acc": lin_matmul_at_swiglu_a_acc,
 }
 
 
@@ -336,6 +360,8 @@ def run_form(form: str, d: dict, Y, stream=None):
         # dW = X^T @ dY; the accumulating form adds into Y (initial dW = d["R"])
         if "_acc" in form:
             Y.copy_(d["R"])
+        if "swiglu" in form:
+            return f(d["GATE"], d["UP"], d["DY"], Y, stream=stream)
         return f(d["X"], d["DY"], Y, stream=stream)
     w = d["W16"] if form.endswith("_w16") else d["W"]
     if form.startswith("matmul_t"):

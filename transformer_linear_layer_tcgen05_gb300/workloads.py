@@ -46,6 +46,8 @@ T_FORMS = (
 AT_FORMS = (
     "matmul_at",
     "matmul_at_acc",
+    "matmul_at_swiglu_a",       # dW_down = (silu(GATE) * UP)^T @ dY
+    "matmul_at_swiglu_a_acc",
 )
 FORMS = FORWARD_FORMS + T_FORMS + AT_FORMS
 
@@ -121,6 +123,8 @@ BACKWARD_WORKLOADS = (
     Workload(12, "ffn_up_dx_f32", "matmul_t", 512, 3072, 768, w_var=1.0 / 768),
     Workload(13, "attn_proj_dw_f32", "matmul_at", 512, 768, 768, w_var=1.0),
     Workload(16, "ffn_up_dw_f32", "matmul_at", 512, 3072, 768, w_var=1.0),
+    Workload(17, "ffn_down_dw_swiglu_f32", "matmul_at_swiglu_a", 512, 768, 3072, w_var=1.0,
+             outlier_frac=0.01),
     Workload(14, "lm_head_dx_w16", "matmul_t_w16", 512, 16384, 768, w_var=0.02),
     Workload(15, "ffn_down_dx_w16_16k", "matmul_t_w16", 16384, 2048, 8192, w_var=1.0 / 8192),
 )
@@ -172,8 +176,14 @@ def generate(form: str, M: int, N: int, K: int, seed: int, *, a_var: float = 1.0
     if w_var is None:
         w_var = 1.0 / max(K, 1)
     out = {}
-    if form_is_at(form):   # X [M,K], dY [M,N], R = the initial dW [K,N]
-        out["X"] = _normal(rng, (M, K), a_var)
+    if form_is_at(form):   # X [M,K] (or GATE, UP), dY [M,N], R = the initial dW [K,N]
+        if form_is_swiglu(form):
+            gate = _normal(rng, (M, K), gate_var)
+            _outliers(rng, gate, outlier_frac)
+            out["GATE"] = gate
+            out["UP"] = _normal(rng, (M, K), a_var)
+        else:
+            out["X"] = _normal(rng, (M, K), a_var)
         out["DY"] = _normal(rng, (M, N), w_var)
         if form_has_residual(form):
             out["R"] = _normal(rng, (K, N), r_var)
@@ -216,8 +226,9 @@ def input_bytes(form: str, M: int, N: int, K: int) -> int:
     traffic of one call; the SwiGLU hidden matrix is not counted because the
     fused form never stores it)."""
     w = K * N * (2 if form_is_w16(form) else 4)
-    if form_is_at(form):  # X, dY in; dW [K,N] out (read too when accumulating)
-        return M * K * 4 + M * N * 4 + (K * N * 4 if form_has_residual(form) else 0) + K * N * 4
+    if form_is_at(form):  # X (or GATE, UP), dY in; dW [K,N] out (read too when accumulating)
+        a = 2 * M * K * 4 if form_is_swiglu(form) else M * K * 4
+        return a + M * N * 4 + (K * N * 4 if form_has_residual(form) else 0) + K * N * 4
     if form_is_t(form):   # dY [M,N] in, dX [M,K] out (read too when accumulating)
         return M * N * 4 + w + (M * K * 4 if form_has_residual(form) else 0) + M * K * 4
     a = 2 * M * K * 4 if form_is_swiglu(form) else M * K * 4
