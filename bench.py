@@ -286,6 +286,8 @@ def time_small(w: wl.Workload, iters: int, flush_buf):
     from transformer_linear_layer_tcgen05_gb300 import lin
     d = device_inputs(wl.generate_workload(w))
     Y = torch.empty(wl.output_shape(w.form, w.M, w.N, w.K), dtype=torch.float32, device="cuda")
+    if wl.form_is_swiglu_bwd(w.form):   # two outputs: dGATE, dUP
+        Y = (Y, torch.empty_like(Y))
     stream = torch.cuda.current_stream()
     for _ in range(5):
         lin.run_form(w.form, d, Y)
@@ -353,6 +355,8 @@ def run_ours(args, rank: int, world: int):
     host = wl.generate_workload(w)
     d = device_inputs(host)
     Y = torch.empty(wl.output_shape(w.form, w.M, w.N, w.K), dtype=torch.float32, device="cuda")
+    if wl.form_is_swiglu_bwd(w.form):   # two outputs: dGATE, dUP
+        Y = (Y, torch.empty_like(Y))
     stream = torch.cuda.current_stream()
 
     def step():
@@ -409,15 +413,17 @@ def run_ours(args, rank: int, world: int):
     e2e_steps = 0 if args.no_e2e else max(3, min(args.steps, args.e2e_steps))
     pinned = {k: torch.from_numpy(v.view(np.int16) if v.dtype == np.uint16 else v).pin_memory()
               for k, v in host.items()}
-    y_host = torch.empty(wl.output_shape(w.form, w.M, w.N, w.K), dtype=torch.float32).pin_memory()
+    outs = Y if isinstance(Y, tuple) else (Y,)
+    y_host = [torch.empty(o.shape, dtype=torch.float32).pin_memory() for o in outs]
     h2d = sum(t.numel() * t.element_size() for t in pinned.values())
-    d2h = y_host.numel() * 4
+    d2h = sum(y.numel() * 4 for y in y_host)
 
     def e2e_step():
         for k, t in pinned.items():
             d[k].copy_(t, non_blocking=True)
         lin.run_form(w.form, d, Y)
-        y_host.copy_(Y, non_blocking=True)
+        for yh, o in zip(y_host, outs):
+            yh.copy_(o, non_blocking=True)
 
     if e2e_steps:
         e2e_step()

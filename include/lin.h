@@ -247,6 +247,27 @@ lin_status lin_matmul_at_swiglu_a_acc(const float *GATE, const float *UP, const 
                                       float *DW, int64_t M, int64_t N, int64_t K,
                                       lin_stream_t stream);
 
+/* Backward of the SwiGLU FFN's down projection and of the SwiGLU itself in
+ * one call: dA = dY[M,N] @ W[K,N]^T (the input gradient of
+ * lin_matmul_residual_swiglu_a, K = d_ff) is formed on chip and never
+ * stored; the epilogue applies ffn_swiglu_backward of page 09_backward_ffn
+ * ("SwiGLU backward", "ffn_swiglu_backward") element by element:
+ *   dGATE = nan_guard(dA * UP * silu'(GATE)),  dUP = nan_guard(dA * silu(GATE)),
+ *   silu'(x) = s * (1 + x * (1 - s)), s = the stable sigmoid of x,
+ * nan_guard(x) = x if x is finite (|x| < FLT_MAX), else 0 (the pages'
+ * shared preamble). GATE, UP, DGATE, DUP are [M,K] binary32, 16-byte
+ * aligned; DGATE and DUP overlap nothing. Same shape rules and errors as
+ * lin_matmul_t. */
+lin_status lin_matmul_t_swiglu_backward(const float *DY, const float *W, const float *GATE,
+                                        const float *UP, float *DGATE, float *DUP,
+                                        int64_t M, int64_t N, int64_t K, lin_stream_t stream);
+
+/* The same with binary16 W_down (dY rounded to binary16). N % 8 == 0. */
+lin_status lin_matmul_t_swiglu_backward_w16(const float *DY, const uint16_t *W16,
+                                            const float *GATE, const float *UP, float *DGATE,
+                                            float *DUP, int64_t M, int64_t N, int64_t K,
+                                            lin_stream_t stream);
+
 /* Static, NUL-terminated name of a status code ("LIN_SUCCESS", ...). Never NULL. */
 const char *lin_status_string(lin_status status);
 

@@ -41,6 +41,15 @@ gradient (``matmul_at``) is the adjoint with respect to W: dW = X^T @ dY
 weight gradient of the SwiGLU down projection, (silu(GATE) * UP)^T @ dY,
 the left factor recomputed from GATE and UP as in the forward form.
 
+SwiGLU backward (page "ffn_gelu_backward ve ffn_swiglu_backward",
+09_backward_ffn, sections "SwiGLU backward", "SiLU'" and the
+"ffn_swiglu_backward" walk-through): for the hidden gradient g,
+grad_gate = g * up * silu'(gate) and grad_up = g * silu(gate), with
+silu'(x) = s * (1 + x * (1 - s)), s the stable sigmoid, each passed through
+nan_guard (page "00_shared", "C. NaN/Inf Guard": x if x == x and
+|x| < F32_MAX, else 0). ``matmul_t_swiglu_backward`` applies it to
+g = dY @ W^T, the input gradient of the SwiGLU form's down projection.
+
 Everything is evaluated in float64. Inputs are widened exactly: float32 to
 float64 by numpy, binary16 bit patterns by ``f16_bits_to_f64`` below (an
 IEEE 754 decoder written from the format's definition). The contraction uses
@@ -80,6 +89,11 @@ __all__ = [
     "matmul_at_acc",
     "matmul_at_swiglu_a",
     "matmul_at_swiglu_a_acc",
+    "silu_derivative",
+    "nan_guard",
+    "ffn_swiglu_backward",
+    "matmul_t_swiglu_backward",
+    "matmul_t_swiglu_backward_w16",
     "normaliser",
     "normalised_error",
     "reference",
@@ -101,6 +115,8 @@ FORMS = (
     "matmul_at_acc",
     "matmul_at_swiglu_a",
     "matmul_at_swiglu_a_acc",
+    "matmul_t_swiglu_backward",
+    "matmul_t_swiglu_backward_w16",
 )
 
 
@@ -273,6 +289,50 @@ def matmul_at_swiglu_a_acc(GATE, UP, DY, DW0) -> np.ndarray:
     return matmul_at_acc(swiglu_a(_f64(GATE), _f64(UP)), DY, DW0)
 
 
+F32_MAX = float(np.finfo(np.float32).max)
+
+
+def silu_derivative(x) -> np.ndarray:
+    """silu'(x) = s * (1 + x * (1 - s)), s = sigmoid(x) (09_backward_ffn, "SiLU'")."""
+    x = _f64(x)
+    s = sigmoid(x)
+    return s * (1.0 + x * (1.0 - s))
+
+
+def nan_guard(x) -> np.ndarray:
+    """x where x == x and |x| < F32_MAX, else 0 (00_shared, "C. NaN/Inf Guard").
+    The limit is binary32's: a float64 value beyond it is what binary32
+    arithmetic would have turned into an infinity."""
+    x = _f64(x)
+    with np.errstate(invalid="ignore"):
+        ok = (x == x) & (np.abs(x) < F32_MAX)
+    return np.where(ok, x, 0.0)
+
+
+def ffn_swiglu_backward(G, GATE, UP):
+    """(grad_gate, grad_up) for the hidden gradient G of A = silu(GATE) * UP:
+    nan_guard(G * UP * silu'(GATE)) and nan_guard(G * silu(GATE))."""
+    G = _f64(G)
+    GATE = _f64(GATE)
+    UP = _f64(UP)
+    if not (G.shape == GATE.shape == UP.shape):
+        raise ValueError(f"G{G.shape}, GATE{GATE.shape} and UP{UP.shape} differ")
+    with np.errstate(invalid="ignore", over="ignore"):
+        dgate = nan_guard(G * UP * silu_derivative(GATE))
+        dup = nan_guard(G * silu(GATE))
+    return dgate, dup
+
+
+def matmul_t_swiglu_backward(DY, W, GATE, UP):
+    """ffn_swiglu_backward of dA = dY @ W^T (dY [M,N], W [K,N], GATE/UP [M,K])."""
+    return ffn_swiglu_backward(matmul_t(DY, W), GATE, UP)
+
+
+def matmul_t_swiglu_backward_w16(DY, W16, GATE, UP):
+    """matmul_t_swiglu_backward with binary16 W_down bits."""
+    return matmul_t_swiglu_backward(DY, f16_bits_to_f64(W16), GATE, UP)
+
+
 # --------------------------------------------------------------------------
 # Acceptance metric
 # --------------------------------------------------------------------------
@@ -339,6 +399,22 @@ def reference(form: str, inputs: dict, rows=None):
         return Y, normaliser(Xk.T, DY)
     w16 = form.endswith("_w16")
     W = f16_bits_to_f64(inputs["W16"]) if w16 else _f64(inputs["W"])
+    if "swiglu_backward" in form:
+        # two outputs: ((dGATE, dUP), (S_dGATE, S_dUP)). As for the product,
+        # S sums the magnitudes of the terms: the product's S times those of
+        # the element-wise factor, silu'(x) = s + x*s*(1-s) -> s + |x|*s*(1-s)
+        # (its two terms cancel near x = -1.28, where silu' is 0) and
+        # silu(x) = x*s -> |x|*s.
+        DY = _f64(sel(inputs["DY"]))
+        GATE = _f64(sel(inputs["GATE"]))
+        UP = _f64(sel(inputs["UP"]))
+        dgate, dup = matmul_t_swiglu_backward(DY, W, GATE, UP)
+        S = normaliser(DY, W.T)
+        s = sigmoid(GATE)
+        with np.errstate(invalid="ignore", over="ignore"):
+            Sg = nan_guard(S * np.abs(UP) * (s + np.abs(GATE) * s * (1.0 - s)))
+            Su = nan_guard(S * np.abs(GATE) * s)
+        return (dgate, dup), (Sg, Su)
     if form.startswith("matmul_t"):
         # dX row i depends only on dY row i (and R row i)
         A = _f64(sel(inputs["DY"]))

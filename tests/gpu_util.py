@@ -75,6 +75,9 @@ def integer_inputs(form: str, M: int, N: int, K: int, seed: int) -> dict:
             d["W"] = w
         if wl.form_has_residual(form):
             d["R"] = rng.integers(-64, 65, size=(M, K)).astype(np.float32)
+        if wl.form_is_swiglu_bwd(form):   # sigma(GATE) == 1.0: every gradient an integer
+            d["GATE"] = rng.integers(40, 61, size=(M, K)).astype(np.float32)
+            d["UP"] = rng.integers(-4, 5, size=(M, K)).astype(np.float32)
         return d
     if wl.form_is_swiglu(form):
         d["GATE"] = rng.integers(40, 61, size=(M, K)).astype(np.float32)

@@ -230,3 +230,73 @@ def test_swiglu_weight_gradient_is_the_adjoint_of_the_forward_kernel():
     lhs = float(np.sum(Y.cpu().numpy().astype(np.float64) * DY))
     rhs = float(np.sum(DW.cpu().numpy().astype(np.float64) * W))
     assert lhs == rhs
+
+
+# ---------------------------------------------------------------- fused SwiGLU backward
+
+SWB_FORMS = wl.SWIGLU_BWD_FORMS
+
+
+def _run_swb(form, dd, M, K):
+    import torch
+    DG = torch.full((M, K), float("nan"), dtype=torch.float32, device="cuda")
+    DU = torch.full((M, K), float("nan"), dtype=torch.float32, device="cuda")
+    lin.run_form(form, dd, (DG, DU))
+    torch.cuda.synchronize()
+    assert lin.lin_get_device_status() == lin.LIN_SUCCESS
+    return DG.cpu().numpy().astype(np.float64), DU.cpu().numpy().astype(np.float64)
+
+
+# (M, N, K): dA = dY[M,N] @ W[K,N]^T is [M,K]; the last two split the
+# contraction (per-tile split K for the f32 form, the split tail of the
+# clustered kernel for binary16 W)
+SWB_SHAPES = [(128, 256, 128), (129, 136, 260), (1, 8, 4), (300, 64, 1032), (300, 2048, 2048),
+              (777, 512, 768)]
+
+
+@pytest.mark.parametrize("form", SWB_FORMS)
+@pytest.mark.parametrize("shape", SWB_SHAPES)
+def test_swiglu_backward_exact_small_integers(form, shape):
+    M, N, K = shape
+    d = integer_inputs(form, M, N, K, seed=5 * M + N + 3 * K)
+    DG, DU = _run_swb(form, to_device(d), M, K)
+    (rg, ru), _ = oracle.reference(form, d)
+    assert np.array_equal(DG, rg), f"dGATE max |diff| = {np.max(np.abs(DG - rg))}"
+    assert np.array_equal(DU, ru), f"dUP max |diff| = {np.max(np.abs(DU - ru))}"
+
+
+@pytest.mark.parametrize("form", SWB_FORMS)
+@pytest.mark.parametrize("shape", [(300, 392, 200), (512, 768, 3072), (1100, 2048, 1024)])
+def test_swiglu_backward_random_within_bound(form, shape):
+    M, N, K = shape
+    d = wl.generate(form, M, N, K, seed=53 + M + N, outlier_frac=0.01)
+    DG, DU = _run_swb(form, to_device(d), M, K)
+    (rg, ru), (sg, su) = oracle.reference(form, d)
+    # Underflow: the pages let exp() of a very negative gate resolve to 0
+    # (09_backward_ffn, note 2), so a gradient below binary32's smallest
+    # subnormal (2**-149) may come out as 0 or as that subnormal: the
+    # comparison allows one subnormal step on top of the relative bound.
+    tiny = 2.0 ** -149
+    for Y, ref, S in ((DG, rg, sg), (DU, ru, su)):
+        assert np.all(np.isfinite(Y))
+        nz = S > 0
+        dev = np.maximum(np.abs(Y - ref) - tiny, 0.0)
+        err = float(np.max(dev[nz] / S[nz])) if np.any(nz) else 0.0
+        assert err <= TOL, err
+        assert np.all(dev[~nz] == 0.0)
+
+
+@pytest.mark.parametrize("form", SWB_FORMS)
+def test_swiglu_backward_guards_non_finite_values(form):
+    # NaN and infinite gates give NaN products, which nan_guard turns into 0;
+    # the other elements are untouched
+    M, N, K = 130, 64, 136
+    d = integer_inputs(form, M, N, K, seed=2)
+    d["GATE"][3, 5] = np.nan
+    d["GATE"][7, 9] = np.inf
+    d["GATE"][11, 13] = -np.inf
+    DG, DU = _run_swb(form, to_device(d), M, K)
+    (rg, ru), _ = oracle.reference(form, d)
+    assert np.array_equal(DG, rg) and np.array_equal(DU, ru)
+    for i, k in ((3, 5), (7, 9)):
+        assert DG[i, k] == 0.0 and DU[i, k] == 0.0

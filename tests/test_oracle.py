@@ -233,6 +233,13 @@ def test_reference_row_subset_equals_full():
         Y, S = oracle.reference(form, inp)
         last = output_shape(form, 20, 16, 12)[0] - 1
         rows = np.array([0, 3, last, 7])
+        if "swiglu_backward" in form:   # two outputs and two normalisers
+            (Yg, Yu), (Sg, Su) = Y, S
+            (Ygr, Yur), (Sgr, Sur) = oracle.reference(form, inp, rows=rows)
+            for a, b in ((Ygr, Yg), (Yur, Yu), (Sgr, Sg), (Sur, Su)):
+                assert np.array_equal(a, b[rows])
+            assert np.all(Sg >= np.abs(Yg) - 1e-12) and np.all(Su >= np.abs(Yu) - 1e-12)
+            continue
         Yr, Sr = oracle.reference(form, inp, rows=rows)
         assert np.array_equal(Yr, Y[rows]) and np.array_equal(Sr, S[rows])
         assert np.all(S >= np.abs(Y - (inp["R"] if "R" in inp else 0.0)) - 1e-12)
@@ -370,3 +377,58 @@ def test_matmul_at_swiglu_a_is_the_adjoint_of_the_swiglu_form():
     assert np.array_equal(dW, want)
     D0 = rng.integers(-64, 65, size=(K, N)).astype(np.float32)
     assert np.array_equal(oracle.matmul_at_swiglu_a_acc(G, U, DY, D0) - dW, D0.astype(np.float64))
+
+
+# ---------------------------------------------------------------- SwiGLU backward (09_backward_ffn)
+
+def test_silu_derivative_closed_forms_and_identities():
+    # silu'(0) = 1/2; sigma(ln 3) = 3/4 gives silu'(ln 3) = 3/4 (1 + ln(3)/4)
+    assert oracle.silu_derivative(np.array([0.0]))[0] == 0.5
+    assert math.isclose(oracle.silu_derivative(np.array([math.log(3.0)]))[0],
+                        0.75 * (1.0 + math.log(3.0) / 4.0), rel_tol=1e-15)
+    # silu'(x) + silu'(-x) = 1, and a central difference of silu agrees
+    x = np.linspace(-30.0, 30.0, 601)
+    np.testing.assert_allclose(oracle.silu_derivative(x) + oracle.silu_derivative(-x), 1.0,
+                               rtol=0, atol=1e-13)   # fp64 rounding of x*s*(1-s), |x| <= 30
+    h = 1e-6
+    fd = (oracle.silu(x + h) - oracle.silu(x - h)) / (2 * h)
+    np.testing.assert_allclose(oracle.silu_derivative(x), fd, rtol=0, atol=1e-8)
+    # far out: silu' -> 1 for large x, -> 0 (from below) for very negative x
+    assert oracle.silu_derivative(np.array([100.0]))[0] == 1.0
+    assert abs(oracle.silu_derivative(np.array([-100.0]))[0]) < 1e-40
+
+
+def test_nan_guard_is_the_pages_finite_check():
+    f32max = float(np.finfo(np.float32).max)
+    x = np.array([np.nan, np.inf, -np.inf, f32max, -f32max, 3.4e38, -1e-45, 0.0, 2.5])
+    assert np.array_equal(oracle.nan_guard(x), [0, 0, 0, 0, 0, 3.4e38, -1e-45, 0.0, 2.5])
+
+
+def test_ffn_swiglu_backward_values():
+    # large gates: sigma == 1 in float64, so silu = gate, silu' = 1 exactly
+    G = np.array([[3.0, -2.0, 0.5]])
+    gate = np.array([[40.0, 50.0, 60.0]])
+    up = np.array([[2.0, -3.0, 4.0]])
+    dg, du = oracle.ffn_swiglu_backward(G, gate, up)
+    assert np.array_equal(dg, G * up) and np.array_equal(du, G * gate)
+    # gate 0: silu(0) = 0, silu'(0) = 1/2
+    dg, du = oracle.ffn_swiglu_backward(np.array([4.0]), np.array([0.0]), np.array([3.0]))
+    assert dg[0] == 6.0 and du[0] == 0.0
+    # non-finite inputs and overflowing products are guarded to 0
+    dg, du = oracle.ffn_swiglu_backward(np.array([1.0, 1.0, 1e30]), np.array([np.nan, np.inf, 1e10]),
+                                        np.array([1.0, 1.0, 1e10]))
+    assert np.array_equal(dg, [0.0, 0.0, 0.0]) and np.array_equal(du, [0.0, 0.0, 0.0])
+
+
+def test_matmul_t_swiglu_backward_composes_the_pages_steps():
+    # the fused form is the pages' element-wise backward applied to dY @ W^T
+    # (two steps the tests above pin separately); brute force on integers
+    rng = np.random.default_rng(31)
+    DY = rng.integers(-4, 5, size=(3, 5)).astype(np.float32)
+    W = rng.integers(-4, 5, size=(4, 5)).astype(np.float32)
+    gate = rng.integers(40, 61, size=(3, 4)).astype(np.float32)
+    up = rng.integers(-4, 5, size=(3, 4)).astype(np.float32)
+    dg, du = oracle.matmul_t_swiglu_backward(DY, W, gate, up)
+    for i, k in itertools.product(range(3), range(4)):
+        dA = sum(float(DY[i, n]) * float(W[k, n]) for n in range(5))
+        assert dg[i, k] == dA * float(up[i, k]) and du[i, k] == dA * float(gate[i, k])

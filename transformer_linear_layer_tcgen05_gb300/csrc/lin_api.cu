@@ -249,6 +249,11 @@ struct Problem {
   bool bt = false;     // W is [N][K]
   bool at = false;     // A = X^T: X is [K][M] (the weight gradient X^T · dY, W = dY)
   bool acc = false;    // R is Y itself (Y += A · B)
+  // SwiGLU backward epilogue: Y = dGATE, Y2 = dUP of the product dA, from
+  // G2 = GATE and U2 = UP, all [M,N]
+  const float* G2 = nullptr;
+  const float* U2 = nullptr;
+  float* Y2 = nullptr;
 };
 
 // `fixed`: where a split tail's workspace comes from instead of the library's
@@ -285,6 +290,20 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
                                            : misaligned(p.X))))
     return LIN_ERROR_MISALIGNED;
 
+  const bool swb = p.Y2 != nullptr;
+  if (swb) {
+    if (!p.G2 || !p.U2 || resid) return LIN_ERROR_INVALID_VALUE;
+    if (misaligned(p.G2) || misaligned(p.U2) || misaligned(p.Y2)) return LIN_ERROR_MISALIGNED;
+    // both outputs overlap nothing: each other, GATE, UP, or the inputs below
+    const void* ins[] = {p.Y2, p.G2, p.U2};
+    for (const void* q : ins)
+      if (overlaps(p.Y, mn_bytes, q, mn_bytes)) return LIN_ERROR_ALIASING;
+    if (overlaps(p.Y2, mn_bytes, p.G2, mn_bytes) || overlaps(p.Y2, mn_bytes, p.U2, mn_bytes))
+      return LIN_ERROR_ALIASING;
+    if (K > 0 && (overlaps(p.Y2, mn_bytes, p.W, w_bytes) || overlaps(p.Y2, mn_bytes, p.X, a_bytes)))
+      return LIN_ERROR_ALIASING;
+  }
+
   // 4. aliasing: Y may overlap no input (an accumulating call reads and
   // writes the same Y, element by element)
   if (resid && !p.acc && overlaps(p.Y, mn_bytes, p.R, mn_bytes)) return LIN_ERROR_ALIASING;
@@ -307,6 +326,11 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
   // 6. every buffer is device memory of this device and large enough
   if ((st = check_buffer(p.Y, mn_bytes, dev)) != LIN_SUCCESS) return st;
   if (resid && (st = check_buffer(p.R, mn_bytes, dev)) != LIN_SUCCESS) return st;
+  if (swb) {
+    if ((st = check_buffer(p.Y2, mn_bytes, dev)) != LIN_SUCCESS) return st;
+    if ((st = check_buffer(p.G2, mn_bytes, dev)) != LIN_SUCCESS) return st;
+    if ((st = check_buffer(p.U2, mn_bytes, dev)) != LIN_SUCCESS) return st;
+  }
   if (K > 0) {
     if ((st = check_buffer(p.W, w_bytes, dev)) != LIN_SUCCESS) return st;
     if (swiglu) {
@@ -325,7 +349,10 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
   // 7. K == 0: nothing is accumulated, Y = R (or 0)
   if (K == 0) {   // nothing to accumulate: Y = R (already so when accumulating in place), or 0
     cudaError_t e = cudaSuccess;
-    if (!resid)
+    if (swb) {   // dA = 0: both gradients are 0 (nan_guard maps a NaN product to 0 too)
+      e = cudaMemsetAsync(p.Y, 0, mn_bytes, stream);
+      if (e == cudaSuccess) e = cudaMemsetAsync(p.Y2, 0, mn_bytes, stream);
+    } else if (!resid)
       e = cudaMemsetAsync(p.Y, 0, mn_bytes, stream);
     else if (p.R != p.Y)
       e = cudaMemcpyAsync(p.Y, p.R, mn_bytes, cudaMemcpyDeviceToDevice, stream);
@@ -360,6 +387,11 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
   }
   if (resid) ok &= encode_2d(&maps.r, f32, p.R, N, M, N * 4, lin::kEpiCols, lin::kEpiRows);
   ok &= encode_2d(&maps.y, f32, p.Y, N, M, N * 4, lin::kEpiCols, lin::kEpiRows);
+  if (swb) {   // the SwiGLU-backward epilogue's GATE, UP in and dUP out
+    ok &= encode_2d(&maps.g2, f32, p.G2, N, M, N * 4, lin::kEpiCols, lin::kEpiRows);
+    ok &= encode_2d(&maps.u2, f32, p.U2, N, M, N * 4, lin::kEpiCols, lin::kEpiRows);
+    ok &= encode_2d(&maps.y2, f32, p.Y2, N, M, N * 4, lin::kEpiCols, lin::kEpiRows);
+  }
   if (!ok) return cuda_fail(cudaErrorInvalidValue);
 
   lin::KernelArgs args{};
@@ -380,6 +412,12 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
   auto align32 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 31u) == 0; };
   if (cn > 0 && K % 8 == 0 && align32(a_src) && (!swiglu || align32(p.U)))
     args.flags |= lin::KFLAG_A_V8;
+  if (swb) {
+    args.flags |= lin::KFLAG_SWIGLU_BWD;
+    args.G2 = p.G2;
+    args.U2 = p.U2;
+    args.Y2 = p.Y2;
+  }
 
   // Workspace for f32 partial tiles of a split (either kernel): the caller's
   // fixed workspace, or a stream-ordered allocation freed on the same stream
@@ -655,6 +693,34 @@ lin_status lin_matmul_at_swiglu_a_acc(const float* GATE, const float* UP, const 
   Problem p{F_SWIGLU, false, nullptr, GATE, UP, DY, DW, DW, K, N, M};
   p.at = true;
   p.acc = true;
+  return run(p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+// Backward of the FFN down projection and its SwiGLU in one call: dA =
+// dY · W^T stays on chip, and the epilogue writes dGATE and dUP of
+// A = silu(GATE) * UP (page 09_backward_ffn, ffn_swiglu_backward).
+lin_status lin_matmul_t_swiglu_backward(const float* DY, const float* W, const float* GATE,
+                                        const float* UP, float* DGATE, float* DUP, int64_t M,
+                                        int64_t N, int64_t K, lin_stream_t stream) {
+  Problem p{F_MATMUL, false, DY, nullptr, nullptr, W, nullptr, DGATE, M, K, N};
+  p.bt = true;
+  p.G2 = GATE;
+  p.U2 = UP;
+  p.Y2 = DUP;
+  if (!DUP) return LIN_ERROR_INVALID_VALUE;
+  return run(p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+lin_status lin_matmul_t_swiglu_backward_w16(const float* DY, const uint16_t* W16,
+                                            const float* GATE, const float* UP, float* DGATE,
+                                            float* DUP, int64_t M, int64_t N, int64_t K,
+                                            lin_stream_t stream) {
+  Problem p{F_MATMUL, true, DY, nullptr, nullptr, W16, nullptr, DGATE, M, K, N};
+  p.bt = true;
+  p.G2 = GATE;
+  p.U2 = UP;
+  p.Y2 = DUP;
+  if (!DUP) return LIN_ERROR_INVALID_VALUE;
   return run(p, reinterpret_cast<cudaStream_t>(stream));
 }
 

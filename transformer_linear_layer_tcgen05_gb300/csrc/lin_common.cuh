@@ -88,6 +88,24 @@ __device__ __forceinline__ float silu_stable(float x) {
   return x * __fdividef(num, 1.0f + e);
 }
 
+// nan_guard of the pages' shared preamble: x if it is finite (x == x and
+// |x| < FLT_MAX, the pages' is_finite), else 0.
+__device__ __forceinline__ float nan_guard(float x) {
+  return (x == x && fabsf(x) < 3.40282347e+38f) ? x : 0.0f;
+}
+
+// The SwiGLU backward of page 09_backward_ffn ("SwiGLU backward" and
+// "ffn_swiglu_backward"): with s = sigma(gate) (the stable sigmoid above),
+// dgate = g * u * silu'(gate), silu'(x) = s * (1 + x * (1 - s)), and
+// dup = g * silu(gate), each through nan_guard.
+__device__ __forceinline__ void swiglu_backward(float g, float gate, float u, float& dgate,
+                                                float& dup) {
+  const float e = __expf(-fabsf(gate));
+  const float s = __fdividef(gate >= 0.0f ? 1.0f : e, 1.0f + e);
+  dgate = nan_guard(g * u * (s * (1.0f + gate * (1.0f - s))));
+  dup = nan_guard(g * (gate * s));
+}
+
 // Same function in six instructions: exp(-|x|) by the hardware ex2, and the
 // reciprocal of d = 1 + exp(-|x|), which lies in [1, 2], by the hardware
 // reciprocal approximation (about 1 ulp there). Measured faster than a

@@ -246,7 +246,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap tm_u,
                     const __grid_constant__ CUtensorMap tm_w,
                     const __grid_constant__ CUtensorMap tm_r,
-                    const __grid_constant__ CUtensorMap tm_y, const KernelArgs args) {
+                    const __grid_constant__ CUtensorMap tm_y,
+                    const __grid_constant__ CUtensorMap tm_g2,
+                    const __grid_constant__ CUtensorMap tm_u2,
+                    const __grid_constant__ CUtensorMap tm_y2, const KernelArgs args) {
   using T = GemmTraits<AMODE, RESID, BN, BT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -299,6 +302,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if constexpr (T::kSwiglu) tma_prefetch_desc(&tm_u);
     if constexpr (RESID) tma_prefetch_desc(&tm_r);
     tma_prefetch_desc(&tm_y);
+    if (args.flags & KFLAG_SWIGLU_BWD) {
+      tma_prefetch_desc(&tm_g2);
+      tma_prefetch_desc(&tm_u2);
+      tma_prefetch_desc(&tm_y2);
+    }
   }
   __syncwarp();
   if (warp == 2) {
@@ -509,7 +517,49 @@ __global__ void __launch_bounds__(kThreads, 1)
       // empty) the accumulator is not valid: store nothing.
       ok = ok && !withhold && (__shfl_sync(0xffffffffu, *abort_flag, 0) == 0);
     }
-    if (ok && rows_in) {
+    int sw_issued = 0, sw_done = 0;   // GATE/UP chunk loads (lane 0's view)
+    if (ok && rows_in && (args.flags & KFLAG_SWIGLU_BWD)) {
+      // dA -> dGATE, dUP: GATE and UP arrive by TMA in the warp's two
+      // buffers, the gradients replace them there and leave by TMA store
+      const uint32_t bg = buf0, bu = buf0 + T::EPI_BUF_BYTES;
+      for (int c = 0; c < nc; ++c) {
+        if (lane == 0) {
+          bulk_wait_group_read<0>();   // the last stores have read both buffers
+          mbar_arrive_expect_tx(ebar0, 2 * T::EPI_BUF_BYTES);
+          tma_load_2d(bg, &tm_g2, n0 + c * kEpiCols, row0, ebar0);
+          tma_load_2d(bu, &tm_u2, n0 + c * kEpiCols, row0, ebar0);
+          sw_issued = c + 1;
+        }
+        __syncwarp();
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * kEpiCols), v);
+        tmem_wait_ld();
+        if (!warp_wait_phase(ebar0, c & 1, ctl)) break;
+        sw_done = c + 1;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t off = sw128(lane, j);
+          const float4 gt = ld_shared_v4f(bg + off);
+          const float4 up = ld_shared_v4f(bu + off);
+          float4 dg, du;
+          swiglu_backward(__uint_as_float(v[4 * j + 0]), gt.x, up.x, dg.x, du.x);
+          swiglu_backward(__uint_as_float(v[4 * j + 1]), gt.y, up.y, dg.y, du.y);
+          swiglu_backward(__uint_as_float(v[4 * j + 2]), gt.z, up.z, dg.z, du.z);
+          swiglu_backward(__uint_as_float(v[4 * j + 3]), gt.w, up.w, dg.w, du.w);
+          st_shared_v4(bg + off, __float_as_uint(dg.x), __float_as_uint(dg.y),
+                       __float_as_uint(dg.z), __float_as_uint(dg.w));
+          st_shared_v4(bu + off, __float_as_uint(du.x), __float_as_uint(du.y),
+                       __float_as_uint(du.z), __float_as_uint(du.w));
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&tm_y, n0 + c * kEpiCols, row0, bg);
+          tma_store_2d(&tm_y2, n0 + c * kEpiCols, row0, bu);
+          bulk_commit_group();
+        }
+      }
+    } else if (ok && rows_in) {
       for (int c = 0; c < nc; ++c) {
         const int b = c & 1;
         const uint32_t buf = buf0 + b * T::EPI_BUF_BYTES;
@@ -562,6 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // can one be outstanding).
       for (int c = r_done; c < r_issued; ++c)
         wait_phase(ebar0 + 8u * (uint32_t)(c & 1), (c >> 1) & 1, ctl, false);
+      if (sw_issued > sw_done) wait_phase(ebar0, sw_done & 1, ctl, false);
     }
     if (lane == 0) bulk_wait_group_all();
     __syncwarp();
@@ -607,7 +658,7 @@ cudaError_t launch_instance(const TensorMaps& m, const KernelArgs& args, cudaStr
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, m.a, m.u, m.w, m.r, m.y, args);
+  return cudaLaunchKernelEx(&cfg, kern, m.a, m.u, m.w, m.r, m.y, m.g2, m.u2, m.y2, args);
 }
 
 }  // namespace lin

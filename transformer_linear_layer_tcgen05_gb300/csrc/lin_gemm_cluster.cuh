@@ -254,7 +254,10 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT>::k
     lin_gemm_cluster_kernel(const __grid_constant__ CUtensorMap tm_w,
                             const __grid_constant__ CUtensorMap tm_a,
                             const __grid_constant__ CUtensorMap tm_r,
-                            const __grid_constant__ CUtensorMap tm_y, const KernelArgs args) {
+                            const __grid_constant__ CUtensorMap tm_y,
+                            const __grid_constant__ CUtensorMap tm_g2,
+                            const __grid_constant__ CUtensorMap tm_u2,
+                            const __grid_constant__ CUtensorMap tm_y2, const KernelArgs args) {
   using T = ClusterTraits<AMODE, RESID, BN, CN, V8, BT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -321,6 +324,11 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT>::k
     if constexpr (T::kTmaA) tma_prefetch_desc(&tm_a);
     if constexpr (RESID) tma_prefetch_desc(&tm_r);
     tma_prefetch_desc(&tm_y);
+    if (args.flags & KFLAG_SWIGLU_BWD) {
+      tma_prefetch_desc(&tm_g2);
+      tma_prefetch_desc(&tm_u2);
+      tma_prefetch_desc(&tm_y2);
+    }
   }
   __syncwarp();
   if (warp == 2) {
@@ -561,6 +569,9 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT>::k
     // barrier. R loads are issued and waited for in chunk order: r_issued /
     // r_done count them, e_wait is the chunk of the next one to wait for.
     uint32_t ec = 0, r_issued = 0, r_done = 0, e_wait = 0;
+    // SwiGLU-backward epilogue: GATE and UP of a chunk land in this warp's
+    // two buffers together (barrier BAR_EPI + 2q, one phase per chunk)
+    uint32_t sw_issued = 0, sw_done = 0;
     bool ok = true;
     for (int i = 0; i < n_items && ok; ++i) {
       const int t = item_tile(i);
@@ -601,6 +612,51 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT>::k
             part[(size_t)(c * 8 + j) * T::BM] =
                 make_float4(__uint_as_float(v[4 * j + 0]), __uint_as_float(v[4 * j + 1]),
                             __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+        }
+      } else if (staged && (args.flags & KFLAG_SWIGLU_BWD)) {
+        // dA -> dGATE, dUP: GATE and UP arrive by TMA in the two buffers,
+        // the gradients replace them there and leave by TMA store
+        const uint32_t bg = buf(0), bu = buf(1);
+        for (int c = 0; c < nc && ok; ++c) {
+          if (lane == 0) {
+            bulk_wait_group_read<0>();   // the last stores have read both buffers
+            mbar_arrive_expect_tx(ebar(0), 2 * T::EPI_BUF_BYTES);
+            tma_load_2d(bg, &tm_g2, n0 + c * kEpiCols, row0, ebar(0));
+            tma_load_2d(bu, &tm_u2, n0 + c * kEpiCols, row0, ebar(0));
+            ++sw_issued;
+          }
+          __syncwarp();
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(acc + (uint32_t)(c * kEpiCols), v);
+          tmem_wait_ld();
+          if (!warp_wait_phase(ebar(0), sw_done & 1u, ctl)) {
+            ok = false;
+            break;
+          }
+          ++sw_done;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t off = sw128((uint32_t)lane, (uint32_t)j);
+            const float4 gt = ld_shared_v4f(bg + off);
+            const float4 up = ld_shared_v4f(bu + off);
+            float4 dg, du;
+            swiglu_backward(__uint_as_float(v[4 * j + 0]), gt.x, up.x, dg.x, du.x);
+            swiglu_backward(__uint_as_float(v[4 * j + 1]), gt.y, up.y, dg.y, du.y);
+            swiglu_backward(__uint_as_float(v[4 * j + 2]), gt.z, up.z, dg.z, du.z);
+            swiglu_backward(__uint_as_float(v[4 * j + 3]), gt.w, up.w, dg.w, du.w);
+            st_shared_v4(bg + off, __float_as_uint(dg.x), __float_as_uint(dg.y),
+                         __float_as_uint(dg.z), __float_as_uint(dg.w));
+            st_shared_v4(bu + off, __float_as_uint(du.x), __float_as_uint(du.y),
+                         __float_as_uint(du.z), __float_as_uint(du.w));
+          }
+          fence_proxy_async_smem();   // staged gradients -> visible to the TMA stores
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tm_y, n0 + c * kEpiCols, row0, bg);
+            tma_store_2d(&tm_y2, n0 + c * kEpiCols, row0, bu);
+            bulk_commit_group();
+          }
+          __syncwarp();
         }
       } else if (staged) {
         for (int c = 0; c < nc && ok; ++c) {
@@ -670,6 +726,7 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT>::k
         const uint32_t e = e_wait + x;   // the outstanding loads, oldest first
         wait_phase(ebar(e & 1u), (e >> 1) & 1u, ctl, false);
       }
+      if (sw_issued > sw_done) wait_phase(ebar(0), sw_done & 1u, ctl, false);
       bulk_wait_group_all();
     }
     __syncwarp();
@@ -766,10 +823,10 @@ struct ClusterLaunch {
     if constexpr (!T::kTmaA) {
       if (args.flags & KFLAG_A_V8)
         return cudaLaunchKernelEx(&cfg, lin_gemm_cluster_kernel<AMODE, RESID, BN, CN, true, BT>,
-                                  m.w, m.a, m.r, m.y, args);
+                                  m.w, m.a, m.r, m.y, m.g2, m.u2, m.y2, args);
     }
     return cudaLaunchKernelEx(&cfg, lin_gemm_cluster_kernel<AMODE, RESID, BN, CN, false, BT>, m.w,
-                              m.a, m.r, m.y, args);
+                              m.a, m.r, m.y, m.g2, m.u2, m.y2, args);
   }
 };
 
@@ -779,11 +836,12 @@ struct ClusterLaunch {
 // [unit][cta][C4][128 rows], so that consecutive threads load consecutive
 // partial float4s. Y = sum over the s K ranges in K order (+ R):
 // independent of timing, so bitwise reproducible.
-template <bool RESID>
+template <bool RESID, bool SWB>
 __global__ void __launch_bounds__(256)
     lin_split_reduce_kernel(const float4* __restrict__ part, const float* __restrict__ R,
                             float* __restrict__ Y, int M, int N, int cn, int bn, int tile0,
-                            int num_ng, int rem, int s) {
+                            int num_ng, int rem, int s, const float* __restrict__ G2,
+                            const float* __restrict__ U2, float* __restrict__ Y2) {
   const int c4n = bn / 4;
   const long long per_cta = 128LL * c4n;
   const long long x = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -822,6 +880,18 @@ __global__ void __launch_bounds__(256)
     }
   }
   const size_t off = (size_t)row * (size_t)N + (size_t)col;
+  if constexpr (SWB) {   // the SwiGLU backward of the summed dA
+    const float4 gt = *reinterpret_cast<const float4*>(G2 + off);
+    const float4 up = *reinterpret_cast<const float4*>(U2 + off);
+    float4 dg, du;
+    swiglu_backward(sum.x, gt.x, up.x, dg.x, du.x);
+    swiglu_backward(sum.y, gt.y, up.y, dg.y, du.y);
+    swiglu_backward(sum.z, gt.z, up.z, dg.z, du.z);
+    swiglu_backward(sum.w, gt.w, up.w, dg.w, du.w);
+    *reinterpret_cast<float4*>(Y + off) = dg;
+    *reinterpret_cast<float4*>(Y2 + off) = du;
+    return;
+  }
   if constexpr (RESID) {
     const float4 rv = *reinterpret_cast<const float4*>(R + off);
     sum.x += rv.x;

@@ -31,6 +31,10 @@ enum : uint32_t {
   // The A-side inputs (X, or GATE and UP) allow 32-byte loads: K % 8 == 0
   // and every base 32-byte aligned (clustered kernels).
   KFLAG_A_V8 = 1u << 1,
+  // Epilogue: the SwiGLU backward of the product dA (page 09_backward_ffn,
+  // ffn_swiglu_backward) instead of a store of it: dGATE -> Y, dUP -> Y2,
+  // from GATE (G2) and UP (U2) at the same [M,N] coordinates.
+  KFLAG_SWIGLU_BWD = 1u << 2,
 };
 
 // Device status word values (mirror lin_status).
@@ -48,6 +52,9 @@ struct KernelArgs {
   // Split tail of the clustered kernels (see SplitPlan); unused when split_s < 2.
   int32_t split_r, split_rem, split_s;
   float* part;          // partial tiles [unit][cta][BN/4 float4 columns][128 rows] (float4)
+  const float* G2;      // GATE [M,N] of the SwiGLU-backward epilogue
+  const float* U2;      // UP [M,N] of the SwiGLU-backward epilogue
+  float* Y2;            // dUP [M,N] of the SwiGLU-backward epilogue (dGATE goes to Y)
 };
 
 // Work plan of a persistent launch over `tiles` cluster tiles on `clusters`
@@ -82,6 +89,7 @@ inline size_t split_part_bytes(const SplitPlan& p, int cn, int bn) {
 // UP (SwiGLU forms only), `w` the weights, `r` the residual, `y` the output.
 struct TensorMaps {
   CUtensorMap a, u, w, r, y;
+  CUtensorMap g2, u2, y2;   // GATE, UP, dUP of the SwiGLU-backward epilogue ([32 x 32] boxes)
 };
 
 // Block-tile geometry shared by host and device.

@@ -66,6 +66,8 @@ SIGNATURES = {
     "lin_matmul_at_acc": [_P, _P, _P, _I, _I, _I, _S],
     "lin_matmul_at_swiglu_a": [_P, _P, _P, _P, _I, _I, _I, _S],
     "lin_matmul_at_swiglu_a_acc": [_P, _P, _P, _P, _I, _I, _I, _S],
+    "lin_matmul_t_swiglu_backward": [_P, _P, _P, _P, _P, _P, _I, _I, _I, _S],
+    "lin_matmul_t_swiglu_backward_w16": [_P, _P, _P, _P, _P, _P, _I, _I, _I, _S],
 }
 
 _lib = None
@@ -315,6 +317,29 @@ def lin_matmul_at_swiglu_a_acc(GATE, UP, DY, DW, stream=None):
     return DW
 
 
+def _swiglu_bwd(name, DY, W, GATE, UP, DGATE, DUP, stream):
+    M, N, K = _dims_t(_f32(DY, "dY"), W, _f32(DGATE, "dGATE"))
+    for t, nm in ((GATE, "GATE"), (UP, "UP"), (DUP, "dUP")):
+        if tuple(_f32(t, nm).shape) != (M, K):
+            raise ValueError(f"{nm} must be [M, K]")
+    _call(name, DY.data_ptr(), W.data_ptr(), GATE.data_ptr(), UP.data_ptr(), DGATE.data_ptr(),
+          DUP.data_ptr(), M, N, K, _stream_handle(stream))
+    return DGATE, DUP
+
+
+def lin_matmul_t_swiglu_backward(DY, W, GATE, UP, DGATE, DUP, stream=None):
+    """dA = dY @ W^T on chip; dGATE = nan_guard(dA * UP * silu'(GATE)),
+    dUP = nan_guard(dA * silu(GATE)) (TF32)."""
+    return _swiglu_bwd("lin_matmul_t_swiglu_backward", DY, _f32(W, "W"), GATE, UP, DGATE, DUP,
+                       stream)
+
+
+def lin_matmul_t_swiglu_backward_w16(DY, W16, GATE, UP, DGATE, DUP, stream=None):
+    """lin_matmul_t_swiglu_backward with binary16 W_down."""
+    return _swiglu_bwd("lin_matmul_t_swiglu_backward_w16", DY, _w16(W16, "W16"), GATE, UP,
+                       DGATE, DUP, stream)
+
+
 def lin_last_launch_info() -> tuple:
     """(kernels launched, workspace bytes taken) by the last compute call made
     on this thread."""
@@ -349,12 +374,16 @@ FORM_FUNCS = {
     "matmul_at_acc": lin_matmul_at_acc,
     "matmul_at_swiglu_a": lin_matmul_at_swiglu_a,
     "matmul_at_swiglu_a_acc": lin_matmul_at_swiglu_a_acc,
+    "matmul_t_swiglu_backward": lin_matmul_t_swiglu_backward,
+    "matmul_t_swiglu_backward_w16": lin_matmul_t_swiglu_backward_w16,
 }
 
 
 def run_form(form: str, d: dict, Y, stream=None):
     """Call the entry point of ``form`` with the device tensors of dict ``d``
-    (keys as produced by ``workloads.generate``: X or GATE/UP, W or W16, R)."""
+    (keys as produced by ``workloads.generate``: X or GATE/UP, W or W16, R;
+    DY for the backward forms). For the SwiGLU-backward forms Y is the pair
+    (dGATE, dUP)."""
     f = FORM_FUNCS[form]
     if form.startswith("matmul_at"):
         # dW = X^T @ dY; the accumulating form adds into Y (initial dW = d["R"])
@@ -364,6 +393,8 @@ def run_form(form: str, d: dict, Y, stream=None):
             return f(d["GATE"], d["UP"], d["DY"], Y, stream=stream)
         return f(d["X"], d["DY"], Y, stream=stream)
     w = d["W16"] if form.endswith("_w16") else d["W"]
+    if "swiglu_backward" in form:   # two outputs: Y is the pair (dGATE, dUP)
+        return f(d["DY"], w, d["GATE"], d["UP"], Y[0], Y[1], stream=stream)
     if form.startswith("matmul_t"):
         # dX = dY @ W^T; the accumulating forms add into Y, which must hold
         # the initial dX (d["R"]) when called

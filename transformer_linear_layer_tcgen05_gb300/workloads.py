@@ -49,12 +49,22 @@ AT_FORMS = (
     "matmul_at_swiglu_a",       # dW_down = (silu(GATE) * UP)^T @ dY
     "matmul_at_swiglu_a_acc",
 )
-FORMS = FORWARD_FORMS + T_FORMS + AT_FORMS
+# the FFN down projection's input gradient and the SwiGLU backward in one
+# call: dA = dY @ W^T on chip, outputs dGATE and dUP [M,K]
+SWIGLU_BWD_FORMS = (
+    "matmul_t_swiglu_backward",
+    "matmul_t_swiglu_backward_w16",
+)
+FORMS = FORWARD_FORMS + T_FORMS + AT_FORMS + SWIGLU_BWD_FORMS
 
 
 def form_is_t(form: str) -> bool:
     """dX = dY @ W^T: output [M,K], contraction over N."""
     return form.startswith("matmul_t")
+
+
+def form_is_swiglu_bwd(form: str) -> bool:
+    return "swiglu_backward" in form
 
 
 def form_is_at(form: str) -> bool:
@@ -125,8 +135,12 @@ BACKWARD_WORKLOADS = (
     Workload(16, "ffn_up_dw_f32", "matmul_at", 512, 3072, 768, w_var=1.0),
     Workload(17, "ffn_down_dw_swiglu_f32", "matmul_at_swiglu_a", 512, 768, 3072, w_var=1.0,
              outlier_frac=0.01),
+    Workload(18, "ffn_down_dgu_swiglu_f32", "matmul_t_swiglu_backward", 512, 768, 3072,
+             w_var=1.0 / 3072, outlier_frac=0.01),
     Workload(14, "lm_head_dx_w16", "matmul_t_w16", 512, 16384, 768, w_var=0.02),
     Workload(15, "ffn_down_dx_w16_16k", "matmul_t_w16", 16384, 2048, 8192, w_var=1.0 / 8192),
+    Workload(19, "ffn_down_dgu_w16_16k", "matmul_t_swiglu_backward_w16", 16384, 2048, 8192,
+             w_var=1.0 / 8192),
 )
 
 WORKLOADS_BY_NAME = {w.name: w for w in WORKLOADS + BACKWARD_WORKLOADS}
@@ -197,6 +211,11 @@ def generate(form: str, M: int, N: int, K: int, seed: int, *, a_var: float = 1.0
             out["W"] = w
         if form_has_residual(form):
             out["R"] = _normal(rng, (M, K), r_var)
+        if form_is_swiglu_bwd(form):   # the forward's GATE and UP [M,K]
+            gate = _normal(rng, (M, K), gate_var)
+            _outliers(rng, gate, outlier_frac)
+            out["GATE"] = gate
+            out["UP"] = _normal(rng, (M, K), 1.0)
         return out
     if form_is_swiglu(form):
         gate = _normal(rng, (M, K), gate_var)
@@ -229,6 +248,8 @@ def input_bytes(form: str, M: int, N: int, K: int) -> int:
     if form_is_at(form):  # X (or GATE, UP), dY in; dW [K,N] out (read too when accumulating)
         a = 2 * M * K * 4 if form_is_swiglu(form) else M * K * 4
         return a + M * N * 4 + (K * N * 4 if form_has_residual(form) else 0) + K * N * 4
+    if form_is_swiglu_bwd(form):   # dY, W, GATE, UP in; dGATE, dUP out
+        return M * N * 4 + w + 2 * M * K * 4 + 2 * M * K * 4
     if form_is_t(form):   # dY [M,N] in, dX [M,K] out (read too when accumulating)
         return M * N * 4 + w + (M * K * 4 if form_has_residual(form) else 0) + M * K * 4
     a = 2 * M * K * 4 if form_is_swiglu(form) else M * K * 4
