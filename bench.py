@@ -328,6 +328,72 @@ def time_small(w: wl.Workload, iters: int, flush_buf):
     return statistics.median(cold), statistics.median(warm)
 
 
+def time_lm_head_loss(iters: int, flush_buf, peaks: dict) -> dict:
+    """lm_head_w16's shape (512 x 16384 x 768) through
+    lin_lm_head_cross_entropy_w16 (label smoothing 0.1, z-loss 1e-4), cold
+    and warm like the small table. Algorithmic bytes: X, W16, targets in,
+    dLogits and the losses out."""
+    import numpy as np
+    import torch
+    from transformer_linear_layer_tcgen05_gb300 import lin
+    w = wl.WORKLOADS_BY_NAME["lm_head_w16"]
+    d = device_inputs(wl.generate_workload(w))
+    rng = np.random.default_rng(77)
+    t = torch.from_numpy(rng.integers(0, w.N, size=w.M).astype(np.int32)).cuda()
+    DL = torch.empty((w.M, w.N), device="cuda")
+    losses = torch.empty((w.M,), device="cuda")
+    total = torch.empty((1,), device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def call():
+        lin.lin_lm_head_cross_entropy_w16(d["X"], d["W16"], t, DL, losses, total, 0.1, 1e-4,
+                                          1.0 / w.M)
+    for _ in range(5):
+        call()
+    torch.cuda.synchronize()
+    cold = []
+    for _ in range(iters):
+        flush_buf.fill_(1.0)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        call()
+        e1.record(stream)
+        e1.synchronize()
+        cold.append(e0.elapsed_time(e1) * 1e3)
+    reps = 20
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(stream)
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s, capture_error_mode="relaxed"):
+            for _ in range(reps):
+                call()
+    stream.wait_stream(s)
+    g.replay()
+    torch.cuda.synchronize()
+    warm = []
+    for _ in range(max(3, iters // 10)):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        e1.synchronize()
+        warm.append(e0.elapsed_time(e1) * 1e3 / reps)
+    assert lin.lin_get_device_status() == lin.LIN_SUCCESS
+    del g
+    nbytes = w.M * w.K * 4 + w.K * w.N * 2 + w.M * 4 + w.M * w.N * 4 + w.M * 4
+    bf16 = peaks["bf16_tflops"]
+    r = min(bf16, w.flops / nbytes * peaks["hbm_gbs"] / 1e3)
+    c, wm = statistics.median(cold), statistics.median(warm)
+    return {"workload": "lm_head_cross_entropy_w16", "M": w.M, "N": w.N, "K": w.K,
+            "alpha": 0.1, "beta": 1e-4, "bound": "hbm" if r < bf16 else "tensor",
+            "roofline_tflops": r, "cold_us": c, "cold_tflops": w.flops / c / 1e6,
+            "cold_frac": w.flops / c / 1e6 / r, "warm_us": wm, "warm_tflops": w.flops / wm / 1e6,
+            "warm_frac": w.flops / wm / 1e6 / r}
+
+
 def run_ours(args, rank: int, world: int):
     import numpy as np
     import torch
@@ -508,6 +574,7 @@ def run_ours(args, rank: int, world: int):
                           "warm_us": warm_us, "warm_tflops": sw.flops / warm_us / 1e6,
                           "warm_frac": sw.flops / warm_us / 1e6 / r})
         line["backward"] = table
+        line["loss"] = [time_lm_head_loss(args.small_iters, flush, peaks)]
         del flush
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, host, budget_s=args.cpu_seconds)

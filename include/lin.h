@@ -268,6 +268,27 @@ lin_status lin_matmul_t_swiglu_backward_w16(const float *DY, const uint16_t *W16
                                             float *DUP, int64_t M, int64_t N, int64_t K,
                                             lin_stream_t stream);
 
+/* lm_head and the fused cross-entropy of page 07_loss ("cross_entropy ve
+ * sum_losses -- Fused Loss + dLogits") in one call. The logits X[M,K] @
+ * W16[K,V] (binary16 W, X rounded to binary16) are written to DLOGITS [M,V]
+ * and then replaced in place by
+ *   dLogits[s,v] = ((p[v] - target_dist[v]) + 2 beta LSE p[v]) * inv_norm,
+ *   p = softmax of the row, target_dist = (1 - alpha) one_hot(targets[s]) + alpha / V,
+ * losses[s] = LSE - (1 - alpha) l[t] - alpha mean(l) + beta LSE^2 with
+ * LSE = max + log(max(sum exp(l - max), 1e-30)), and *loss_sum = the sum of
+ * the M losses (a fixed-order, reproducible sum). A target outside [0, V)
+ * (padding) gives loss 0 and a zero dLogits row. The GEMM's epilogue keeps
+ * per-row online-softmax partials (max, sum of exponentials over each 256
+ * columns), so the loss kernel reads each logits row once instead of three
+ * times. targets: int32 [M]; losses: f32 [M]; loss_sum: one f32. V % 8 == 0,
+ * K % 4 == 0; DLOGITS, losses and loss_sum overlap no input or each other.
+ * Kernels: the GEMM (and its binary16 pre-pass), the loss, the sum. */
+lin_status lin_lm_head_cross_entropy_w16(const float *X, const uint16_t *W16,
+                                         const int32_t *targets, float *DLOGITS, float *losses,
+                                         float *loss_sum, int64_t M, int64_t V, int64_t K,
+                                         float alpha, float beta, float inv_norm,
+                                         lin_stream_t stream);
+
 /* Static, NUL-terminated name of a status code ("LIN_SUCCESS", ...). Never NULL. */
 const char *lin_status_string(lin_status status);
 

@@ -50,6 +50,16 @@ nan_guard (page "00_shared", "C. NaN/Inf Guard": x if x == x and
 |x| < F32_MAX, else 0). ``matmul_t_swiglu_backward`` applies it to
 g = dY @ W^T, the input gradient of the SwiGLU form's down projection.
 
+Cross-entropy (page "cross_entropy ve sum_losses -- Fused Loss + dLogits",
+07_loss, sections "Ne Yapar?" and "Satir Satir -- cross_entropy"): for a logits row l over
+the vocabulary V with target t, LSE = row_max + log sum_v exp(l_v -
+row_max) (the sum guarded below by 1e-30), loss = LSE - (1 - alpha) l_t -
+alpha mean(l) + beta LSE^2, and dLogits_v = ((p_v - target_dist_v) +
+2 beta LSE p_v) * inv_norm with p = softmax(l) and target_dist =
+(1 - alpha) one_hot(t) + alpha / V; a target outside [0, V) gives loss 0
+and dLogits 0. ``sum_losses`` adds the per-row losses. ``lm_head_cross_entropy``
+applies both to the logits X @ W16 of the lm_head projection.
+
 Everything is evaluated in float64. Inputs are widened exactly: float32 to
 float64 by numpy, binary16 bit patterns by ``f16_bits_to_f64`` below (an
 IEEE 754 decoder written from the format's definition). The contraction uses
@@ -67,6 +77,8 @@ invariants and numpy's own binary16 type.
 """
 
 from __future__ import annotations
+
+import math
 
 import numpy as np
 
@@ -94,6 +106,8 @@ __all__ = [
     "ffn_swiglu_backward",
     "matmul_t_swiglu_backward",
     "matmul_t_swiglu_backward_w16",
+    "cross_entropy",
+    "lm_head_cross_entropy_w16",
     "normaliser",
     "normalised_error",
     "reference",
@@ -331,6 +345,40 @@ def matmul_t_swiglu_backward(DY, W, GATE, UP):
 def matmul_t_swiglu_backward_w16(DY, W16, GATE, UP):
     """matmul_t_swiglu_backward with binary16 W_down bits."""
     return matmul_t_swiglu_backward(DY, f16_bits_to_f64(W16), GATE, UP)
+
+
+def cross_entropy(logits, targets, alpha=0.0, beta=0.0, inv_norm=1.0):
+    """(losses [M], dlogits [M,V]) of the pages' fused cross-entropy with
+    label smoothing alpha and z-loss beta, in float64."""
+    L = _f64(logits)
+    if L.ndim != 2:
+        raise ValueError("logits must be [M, V]")
+    M, V = L.shape
+    t = np.asarray(targets).astype(np.int64).reshape(-1)
+    if t.shape != (M,):
+        raise ValueError("one target per row")
+    losses = np.zeros(M)
+    dl = np.zeros((M, V))
+    for s in range(M):
+        if not (0 <= t[s] < V):
+            continue                      # ignored row: loss 0, gradient 0
+        row = L[s]
+        mx = np.max(row)
+        denom = max(float(np.sum(np.exp(row - mx))), 1e-30)
+        lse = mx + math.log(denom)
+        p = np.exp(row - mx) / denom
+        losses[s] = lse - (1.0 - alpha) * row[t[s]] - alpha * float(np.mean(row)) \
+            + beta * lse * lse
+        tgt = np.full(V, alpha / V)
+        tgt[t[s]] += 1.0 - alpha
+        dl[s] = ((p - tgt) + 2.0 * beta * lse * p) * inv_norm
+    return losses, dl
+
+
+def lm_head_cross_entropy_w16(X, W16, targets, alpha=0.0, beta=0.0, inv_norm=1.0):
+    """(losses, dlogits, loss_sum) for logits = X @ W16 (binary16 bits)."""
+    losses, dl = cross_entropy(matmul_w16(X, W16), targets, alpha, beta, inv_norm)
+    return losses, dl, float(np.sum(losses))
 
 
 # --------------------------------------------------------------------------

@@ -49,6 +49,8 @@ def test_binding_covers_every_compute_entry_point():
             assert hasattr(lin, name)
             # a _noalloc variant is its base form with a fixed workspace
             assert name[len("lin_"):].removesuffix("_noalloc") in lin.FORM_FUNCS
+        if name.startswith("lin_lm_head"):
+            assert name in lin.SIGNATURES and name[len("lin_"):] in lin.OTHER_FUNCS
 
 
 def test_noalloc_validates_before_touching_cuda(L):
@@ -140,3 +142,18 @@ def test_transposed_forms_validate_before_touching_cuda(L):
     # only later, because the fake addresses are not device memory)
     assert L.lin_matmul_t_acc(X, W, Y, 8, 8, 8, None) != lin.LIN_ERROR_ALIASING
     assert L.lin_matmul_t_acc(None, W, Y, 8, 8, 8, None) == lin.LIN_ERROR_INVALID_VALUE
+
+
+def test_lm_head_cross_entropy_validates_before_touching_cuda(L):
+    import ctypes
+    fake = 1 << 40
+    f = L.lin_lm_head_cross_entropy_w16
+    a, b, c = ctypes.c_float(0.0), ctypes.c_float(0.0), ctypes.c_float(1.0)
+    assert f(fake, fake, fake, fake, fake, None, 8, 8, 8, a, b, c, None) == lin.LIN_ERROR_INVALID_VALUE
+    assert f(fake, fake, fake, fake, fake, fake, -1, 8, 8, a, b, c, None) == lin.LIN_ERROR_INVALID_VALUE
+    assert f(fake, fake, fake, fake, fake, fake, 8, 12, 8, a, b, c, None) == lin.LIN_ERROR_UNSUPPORTED_SHAPE
+    assert f(fake, fake, fake, fake, fake, fake, 8, 16, 6, a, b, c, None) == lin.LIN_ERROR_UNSUPPORTED_SHAPE
+    assert f(fake + 2, fake, fake, fake, fake, fake, 8, 16, 8, a, b, c, None) == lin.LIN_ERROR_MISALIGNED
+    # dLogits over X
+    assert f(fake, fake + (1 << 30), fake + (2 << 30), fake, fake + (3 << 30), fake + (4 << 30),
+             8, 16, 8, a, b, c, None) == lin.LIN_ERROR_ALIASING

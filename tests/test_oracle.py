@@ -432,3 +432,47 @@ def test_matmul_t_swiglu_backward_composes_the_pages_steps():
     for i, k in itertools.product(range(3), range(4)):
         dA = sum(float(DY[i, n]) * float(W[k, n]) for n in range(5))
         assert dg[i, k] == dA * float(up[i, k]) and du[i, k] == dA * float(gate[i, k])
+
+
+# ---------------------------------------------------------------- cross-entropy (07_loss)
+
+def test_cross_entropy_closed_forms():
+    V = 8
+    # uniform logits: p = 1/V, loss = log V; ignored target: loss 0, gradient 0
+    losses, dl = oracle.cross_entropy(np.zeros((2, V)), [3, V + 1])
+    assert math.isclose(losses[0], math.log(V), rel_tol=1e-15) and losses[1] == 0.0
+    np.testing.assert_allclose(dl[0], np.full(V, 1.0 / V) - np.eye(V)[3], rtol=0, atol=1e-16)
+    assert np.all(dl[1] == 0.0)
+    # a dominant target logit: loss -> 0; shifting every logit changes nothing
+    L = np.zeros((1, V))
+    L[0, 5] = 60.0
+    assert oracle.cross_entropy(L, [5])[0][0] < 1e-25
+    a, b = oracle.cross_entropy(L + 1000.0, [5])
+    c, d = oracle.cross_entropy(L, [5])
+    assert math.isclose(a[0], c[0], abs_tol=1e-12) and np.allclose(b, d, atol=1e-15)
+    # label smoothing and z-loss terms, by hand: uniform logits l = 2
+    l, _ = oracle.cross_entropy(np.full((1, V), 2.0), [0], alpha=0.1, beta=0.01)
+    lse = 2.0 + math.log(V)
+    assert math.isclose(l[0], lse - 0.9 * 2.0 - 0.1 * 2.0 + 0.01 * lse * lse, rel_tol=1e-14)
+
+
+@pytest.mark.parametrize("alpha,beta", [(0.0, 0.0), (0.1, 0.0), (0.0, 1e-3), (0.2, 1e-2)])
+def test_cross_entropy_gradient_is_the_loss_derivative(alpha, beta):
+    # dLogits / inv_norm is d loss / d logits: central differences agree, and
+    # each row's gradient sums to 2 beta LSE inv_norm
+    rng = np.random.default_rng(9)
+    L = rng.standard_normal((3, 7)) * 3.0
+    t = [0, 4, 6]
+    losses, dl = oracle.cross_entropy(L, t, alpha, beta, inv_norm=0.5)
+    h = 1e-6
+    for s, v in [(0, 0), (1, 3), (2, 6), (2, 2)]:
+        Lp, Lm = L.copy(), L.copy()
+        Lp[s, v] += h
+        Lm[s, v] -= h
+        fd = (oracle.cross_entropy(Lp, t, alpha, beta)[0][s] -
+              oracle.cross_entropy(Lm, t, alpha, beta)[0][s]) / (2 * h)
+        assert math.isclose(dl[s, v] / 0.5, fd, rel_tol=1e-6, abs_tol=1e-8)
+    for s in range(3):
+        mx = np.max(L[s])
+        lse = mx + math.log(np.sum(np.exp(L[s] - mx)))
+        assert math.isclose(float(np.sum(dl[s])), 2 * beta * lse * 0.5, abs_tol=1e-12)

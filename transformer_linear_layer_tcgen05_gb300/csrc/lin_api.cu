@@ -254,6 +254,9 @@ struct Problem {
   const float* G2 = nullptr;
   const float* U2 = nullptr;
   float* Y2 = nullptr;
+  // online-softmax partials of every output row (clustered kernel, no split)
+  float2* row_stats = nullptr;
+  int stats_cols = 0;
 };
 
 // `fixed`: where a split tail's workspace comes from instead of the library's
@@ -361,7 +364,8 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
 
   // 8. tensor maps and launch
   const int bn = 128;
-  const int cn = (p.w16 && !p.at) ? f16_cluster_size(N) : 0;   // 0: the per-tile kernel
+  int cn = (p.w16 && !p.at) ? f16_cluster_size(N) : 0;   // 0: the per-tile kernel
+  if (p.row_stats && cn == 0) cn = 1;   // the partials come from the clustered epilogue
   lin::TensorMaps maps;
   std::memset(&maps, 0, sizeof(maps));
   const CUtensorMapDataType f32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
@@ -412,6 +416,11 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
   auto align32 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 31u) == 0; };
   if (cn > 0 && K % 8 == 0 && align32(a_src) && (!swiglu || align32(p.U)))
     args.flags |= lin::KFLAG_A_V8;
+  if (p.row_stats) {
+    args.flags |= lin::KFLAG_ROW_STATS;
+    args.row_stats = p.row_stats;
+    args.stats_cols = p.stats_cols;
+  }
   if (swb) {
     args.flags |= lin::KFLAG_SWIGLU_BWD;
     args.G2 = p.G2;
@@ -478,7 +487,9 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
     };
     int cap = capacity();
     if (cap < 1) return cuda_fail(ce);
-    lin::SplitPlan plan = lin::split_plan(num_m * num_ng, cap, nkb);
+    // (a split tail's rows are finished by the split sum, which has no partials)
+    lin::SplitPlan plan = p.row_stats ? lin::SplitPlan{0, 0, 1}
+                                      : lin::split_plan(num_m * num_ng, cap, nkb);
     const size_t part_bytes = lin::split_part_bytes(plan, cn, lin::kClusterBN);
     const size_t xh_off = (part_bytes + 255) & ~size_t(255);
     const size_t xh_bytes = tma_a ? (size_t)M * (size_t)K * 2 : 0;
@@ -555,6 +566,99 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
   if (e != cudaSuccess) return cuda_fail(e);
   t_last_kernels = kernels;
   t_last_workspace = workspace;
+  return LIN_SUCCESS;
+}
+
+// lm_head (logits = X @ W16 into DLOGITS) and the fused cross-entropy of
+// page 07_loss on them: the GEMM's epilogue leaves online-softmax partials
+// per row, the loss kernel turns the logits into dLogits in place and
+// writes the per-row losses, and a last kernel their sum.
+lin_status lm_head_cross_entropy(const float* X, const uint16_t* W16, const int32_t* targets,
+                                 float* dlogits, float* losses, float* loss_sum, int64_t M,
+                                 int64_t V, int64_t K, float alpha, float beta, float inv_norm,
+                                 cudaStream_t stream) {
+  t_last_kernels = 0;
+  t_last_workspace = 0;
+  if (M < 0 || V < 0 || K < 0 || !loss_sum) return LIN_ERROR_INVALID_VALUE;
+  if (M > 0 && (!targets || !dlogits || !losses)) return LIN_ERROR_INVALID_VALUE;
+  if (M > 0 && V > 0 && K > 0 && (!X || !W16)) return LIN_ERROR_INVALID_VALUE;
+  const int64_t kMax = 0x7fffffffLL;
+  if (M > kMax || V > kMax || K > kMax) return LIN_ERROR_UNSUPPORTED_SHAPE;
+  if (V % 8 != 0 || K % 4 != 0) return LIN_ERROR_UNSUPPORTED_SHAPE;
+  auto misaligned16 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) != 0; };
+  auto misaligned4 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 3u) != 0; };
+  if (misaligned4(loss_sum)) return LIN_ERROR_MISALIGNED;
+  if (M > 0 && (misaligned16(dlogits) || misaligned4(targets) || misaligned4(losses) ||
+                (K > 0 && (misaligned16(X) || misaligned16(W16)))))
+    return LIN_ERROR_MISALIGNED;
+  const uint64_t mv = (uint64_t)M * (uint64_t)V * 4, mk = (uint64_t)M * (uint64_t)K * 4,
+                 kv = (uint64_t)K * (uint64_t)V * 2, m4 = (uint64_t)M * 4;
+  if (M > 0) {
+    const struct { const void* p; uint64_t n; } ins[] = {{X, K > 0 ? mk : 0},
+                                                         {W16, K > 0 ? kv : 0}, {targets, m4}};
+    for (const auto& in : ins)
+      if (overlaps(dlogits, mv, in.p, in.n) || overlaps(losses, m4, in.p, in.n) ||
+          overlaps(loss_sum, 4, in.p, in.n))
+        return LIN_ERROR_ALIASING;
+    if (overlaps(dlogits, mv, losses, m4) || overlaps(dlogits, mv, loss_sum, 4) ||
+        overlaps(losses, m4, loss_sum, 4))
+      return LIN_ERROR_ALIASING;
+  }
+  int dev = 0;
+  int* word = nullptr;
+  lin_status st = current_device(&dev, &word);
+  if (st != LIN_SUCCESS) return st;
+  if ((st = check_buffer(loss_sum, 4, dev)) != LIN_SUCCESS) return st;
+  if (M == 0) {   // no rows: the sum of no losses
+    const cudaError_t e = cudaMemsetAsync(loss_sum, 0, 4, stream);
+    return e == cudaSuccess ? LIN_SUCCESS : cuda_fail(e);
+  }
+  if ((st = check_buffer(targets, m4, dev)) != LIN_SUCCESS) return st;
+  if ((st = check_buffer(losses, m4, dev)) != LIN_SUCCESS) return st;
+  if (V == 0) {   // every target is outside the (empty) vocabulary
+    cudaError_t e = cudaMemsetAsync(losses, 0, m4, stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(loss_sum, 0, 4, stream);
+    return e == cudaSuccess ? LIN_SUCCESS : cuda_fail(e);
+  }
+  // the row partials: stream-ordered workspace (a graph memory node under
+  // capture), freed after the loss kernel; without it the loss kernel reads
+  // each row three times instead of once
+  const int cols = (int)((V + lin::kClusterBN - 1) / lin::kClusterBN);
+  const size_t stats_bytes = (size_t)M * cols * sizeof(float2);
+  void* ws = nullptr;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) cudaGetLastError();
+  if (cs == cudaStreamCaptureStatusActive) {
+    if (cudaMallocAsync(&ws, stats_bytes, stream) != cudaSuccess) {
+      cudaGetLastError();
+      ws = nullptr;
+    }
+  } else if (cs == cudaStreamCaptureStatusNone) {
+    cudaMemPool_t pool = workspace_pool(dev);
+    if (!pool || cudaMallocFromPoolAsync(&ws, stats_bytes, pool, stream) != cudaSuccess) {
+      cudaGetLastError();
+      ws = nullptr;
+    }
+  }
+  Problem p{F_MATMUL, true, X, nullptr, nullptr, W16, nullptr, dlogits, M, V, K};
+  // (with K == 0 the GEMM only zeroes the logits and leaves no partials)
+  p.row_stats = K > 0 ? static_cast<float2*>(ws) : nullptr;
+  p.stats_cols = cols;
+  st = run(p, stream);
+  const int gemm_kernels = t_last_kernels;
+  const uint64_t gemm_ws = t_last_workspace;
+  cudaError_t e = cudaSuccess;
+  if (st == LIN_SUCCESS)
+    e = lin::launch_cross_entropy(dlogits, p.row_stats, cols, targets, losses, loss_sum,
+                                  (int)M, (int)V, alpha, beta, inv_norm, stream);
+  if (ws) {
+    const cudaError_t ef = cudaFreeAsync(ws, stream);
+    if (e == cudaSuccess) e = ef;
+  }
+  if (st != LIN_SUCCESS) return st;
+  if (e != cudaSuccess) return cuda_fail(e);
+  t_last_kernels = gemm_kernels + 2;
+  t_last_workspace = gemm_ws + (ws ? stats_bytes : 0);
   return LIN_SUCCESS;
 }
 
@@ -722,6 +826,15 @@ lin_status lin_matmul_t_swiglu_backward_w16(const float* DY, const uint16_t* W16
   p.Y2 = DUP;
   if (!DUP) return LIN_ERROR_INVALID_VALUE;
   return run(p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+lin_status lin_lm_head_cross_entropy_w16(const float* X, const uint16_t* W16,
+                                         const int32_t* targets, float* DLOGITS, float* losses,
+                                         float* loss_sum, int64_t M, int64_t V, int64_t K,
+                                         float alpha, float beta, float inv_norm,
+                                         lin_stream_t stream) {
+  return lm_head_cross_entropy(X, W16, targets, DLOGITS, losses, loss_sum, M, V, K, alpha, beta,
+                               inv_norm, reinterpret_cast<cudaStream_t>(stream));
 }
 
 const char* lin_status_string(lin_status status) {

@@ -659,6 +659,9 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT>::k
           __syncwarp();
         }
       } else if (staged) {
+        // online-softmax partials of this lane's row over the tile's columns
+        const bool stats = (args.flags & KFLAG_ROW_STATS) != 0;
+        float rm = -INFINITY, rs = 0.0f;
         for (int c = 0; c < nc && ok; ++c) {
           const uint32_t e = ec + (uint32_t)c;
           const uint32_t b = e & 1u;
@@ -687,6 +690,22 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT>::k
             bulk_wait_group_read<0>();   // this buffer's last store has read it
           }
           __syncwarp();
+          if (stats) {   // (max, sum exp(y - max)) over the columns below N
+            const int col = n0 + c * kEpiCols;
+            float cm = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (col + i < args.N) cm = fmaxf(cm, __uint_as_float(v[i]));
+            const float mn = fmaxf(rm, cm);
+            float sum = (rm == -INFINITY) ? 0.0f : rs * __expf(rm - mn);
+            if (mn != -INFINITY) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (col + i < args.N) sum += __expf(__uint_as_float(v[i]) - mn);
+            }
+            rm = mn;
+            rs = sum;
+          }
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const uint32_t addr = buf(b) + sw128((uint32_t)lane, (uint32_t)j);
@@ -713,6 +732,9 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT>::k
           __syncwarp();
         }
         ec += (uint32_t)nc;
+        if (stats && ok && row0 + lane < args.M)
+          args.row_stats[(size_t)(row0 + lane) * args.stats_cols + n0 / T::BN] =
+              make_float2(rm, rs);
       }
       // TMEM reads of this buffer are complete: hand it back to the UMMA warp.
       tc_fence_before_sync();

@@ -35,6 +35,10 @@ enum : uint32_t {
   // ffn_swiglu_backward) instead of a store of it: dGATE -> Y, dUP -> Y2,
   // from GATE (G2) and UP (U2) at the same [M,N] coordinates.
   KFLAG_SWIGLU_BWD = 1u << 2,
+  // Epilogue (clustered kernels): also the online-softmax partials of each
+  // output row over this CTA's columns of a tile -- (max, sum of exp(y -
+  // max)) -- into row_stats[row][n0 / BN] (cross-entropy of the lm_head).
+  KFLAG_ROW_STATS = 1u << 3,
 };
 
 // Device status word values (mirror lin_status).
@@ -55,6 +59,8 @@ struct KernelArgs {
   const float* G2;      // GATE [M,N] of the SwiGLU-backward epilogue
   const float* U2;      // UP [M,N] of the SwiGLU-backward epilogue
   float* Y2;            // dUP [M,N] of the SwiGLU-backward epilogue (dGATE goes to Y)
+  float2* row_stats;    // [M][stats_cols] (max, sum exp) partials (KFLAG_ROW_STATS)
+  int32_t stats_cols;
 };
 
 // Work plan of a persistent launch over `tiles` cluster tiles on `clusters`
@@ -133,6 +139,14 @@ int cluster_capacity_bt(bool tma_a, int cn, bool resid, cudaError_t* err);
 // Xh[i] = binary16(X[i]) (round to nearest even) for i < n, n % 4 == 0,
 // both bases 16-byte aligned.
 cudaError_t launch_cvt_f16(const float* X, uint16_t* Xh, int64_t n, int sms, cudaStream_t stream);
+// Cross-entropy of page 07_loss on logits [M,V] in place (dLogits), one CTA
+// per row; with row_stats (stats_cols partials per row from the GEMM) the
+// row max and the sum of exponentials come from them, else from two passes
+// over the row. Then the deterministic sum of the M losses into *loss_sum.
+cudaError_t launch_cross_entropy(float* logits, const float2* row_stats, int stats_cols,
+                                 const int32_t* targets, float* losses, float* loss_sum, int M,
+                                 int V, float alpha, float beta, float inv_norm,
+                                 cudaStream_t stream);
 // Y (+ R) from the partial tiles of a split: tiles tile0 .. tile0 +
 // split_rem - 1 of width `bn` (cluster tiles of `cn` CTAs, `num_ng` of them
 // per row block), each summed over its split_s K ranges.

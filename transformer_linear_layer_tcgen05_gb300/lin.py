@@ -46,6 +46,7 @@ LIN_ERROR_TIMEOUT = 7
 _P = ctypes.c_void_p
 _I = ctypes.c_int64
 _S = ctypes.c_void_p  # lin_stream_t
+_F = ctypes.c_float
 
 # name -> argument types (all compute entry points return lin_status as int)
 SIGNATURES = {
@@ -68,6 +69,7 @@ SIGNATURES = {
     "lin_matmul_at_swiglu_a_acc": [_P, _P, _P, _P, _I, _I, _I, _S],
     "lin_matmul_t_swiglu_backward": [_P, _P, _P, _P, _P, _P, _I, _I, _I, _S],
     "lin_matmul_t_swiglu_backward_w16": [_P, _P, _P, _P, _P, _P, _I, _I, _I, _S],
+    "lin_lm_head_cross_entropy_w16": [_P, _P, _P, _P, _P, _P, _I, _I, _I, _F, _F, _F, _S],
 }
 
 _lib = None
@@ -340,6 +342,26 @@ def lin_matmul_t_swiglu_backward_w16(DY, W16, GATE, UP, DGATE, DUP, stream=None)
                        DGATE, DUP, stream)
 
 
+def lin_lm_head_cross_entropy_w16(X, W16, targets, DLOGITS, losses, loss_sum, alpha=0.0,
+                                  beta=0.0, inv_norm=1.0, stream=None):
+    """Logits X @ W16 into DLOGITS, then the fused cross-entropy in place:
+    DLOGITS becomes dLogits, losses [M] the per-row losses, loss_sum [1]
+    their sum. targets: int32 [M] (outside [0, V): ignored row)."""
+    import torch
+    M, V, K = _dims(_f32(X, "X"), _w16(W16, "W16"), _f32(DLOGITS, "dLogits"))
+    if not isinstance(targets, torch.Tensor) or targets.dtype != torch.int32 or \
+            not targets.is_cuda or targets.numel() != M or not targets.is_contiguous():
+        raise TypeError("targets must be a contiguous int32 CUDA tensor of M entries")
+    for t, nm, n in ((losses, "losses", M), (loss_sum, "loss_sum", 1)):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.float32 or not t.is_cuda or \
+                t.numel() != n or not t.is_contiguous():
+            raise TypeError(f"{nm} must be a contiguous float32 CUDA tensor of {n} entries")
+    _call("lin_lm_head_cross_entropy_w16", X.data_ptr(), W16.data_ptr(), targets.data_ptr(),
+          DLOGITS.data_ptr(), losses.data_ptr(), loss_sum.data_ptr(), M, V, K, float(alpha),
+          float(beta), float(inv_norm), _stream_handle(stream))
+    return DLOGITS, losses, loss_sum
+
+
 def lin_last_launch_info() -> tuple:
     """(kernels launched, workspace bytes taken) by the last compute call made
     on this thread."""
@@ -376,6 +398,11 @@ FORM_FUNCS = {
     "matmul_at_swiglu_a_acc": lin_matmul_at_swiglu_a_acc,
     "matmul_t_swiglu_backward": lin_matmul_t_swiglu_backward,
     "matmul_t_swiglu_backward_w16": lin_matmul_t_swiglu_backward_w16,
+}
+
+# entry points whose outputs are not a single [M, N] product (no run_form)
+OTHER_FUNCS = {
+    "lm_head_cross_entropy_w16": lin_lm_head_cross_entropy_w16,
 }
 
 
