@@ -394,6 +394,58 @@ def time_lm_head_loss(iters: int, flush_buf, peaks: dict) -> dict:
             "warm_frac": w.flops / wm / 1e6 / r}
 
 
+def time_gate_up(iters: int, flush_buf, peaks: dict) -> dict:
+    """The producer of the 16k SwiGLU workload's GATE and UP through
+    lin_gate_up_w16: X [16384, 2048] f32, W_gate and W_up [2048, 8192]
+    binary16 (2 x 550 GFLOP), timed cold (inputs above L2 anyway) and warm."""
+    import numpy as np
+    import torch
+    from transformer_linear_layer_tcgen05_gb300 import lin
+    M, N, K = 16384, 8192, 2048
+    g = wl.generate("matmul_w16", M, N, K, seed=1020)
+    wu = wl.generate("matmul_w16", 1, N, K, seed=1021)["W16"]
+    X = torch.from_numpy(g["X"]).cuda()
+    WG = torch.from_numpy(g["W16"].view(np.int16)).cuda()
+    WU = torch.from_numpy(wu.view(np.int16)).cuda()
+    G = torch.empty((M, N), device="cuda")
+    U = torch.empty((M, N), device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def call():
+        lin.lin_gate_up_w16(X, WG, WU, G, U)
+
+    def separate():   # the two products it replaces, one lin_matmul_w16 each
+        lin.lin_matmul_w16(X, WG, G)
+        lin.lin_matmul_w16(X, WU, U)
+
+    def median_us(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        times = []
+        for _ in range(max(5, iters // 5)):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            e1.synchronize()
+            times.append(e0.elapsed_time(e1) * 1e3)
+        assert lin.lin_get_device_status() == lin.LIN_SUCCESS
+        return statistics.median(times)
+    sep_us = median_us(separate)
+    us = median_us(call)
+    flops = 2 * 2 * M * N * K
+    nbytes = M * K * 4 + 2 * K * N * 2 + 2 * M * N * 4
+    bf16 = peaks["bf16_tflops"]
+    r = min(bf16, flops / nbytes * peaks["hbm_gbs"] / 1e3)
+    return {"workload": "ffn_gate_up_w16_16k", "form": "gate_up_w16", "M": M, "N": N, "K": K,
+            "two_matmul_w16_us": sep_us,
+            "bound": "hbm" if r < bf16 else "tensor", "roofline_tflops": r, "cold_us": us,
+            "cold_tflops": flops / us / 1e6, "cold_frac": flops / us / 1e6 / r, "warm_us": us,
+            "warm_tflops": flops / us / 1e6, "warm_frac": flops / us / 1e6 / r}
+
+
 def run_ours(args, rank: int, world: int):
     import numpy as np
     import torch
@@ -575,6 +627,7 @@ def run_ours(args, rank: int, world: int):
                           "warm_frac": sw.flops / warm_us / 1e6 / r})
         line["backward"] = table
         line["loss"] = [time_lm_head_loss(args.small_iters, flush, peaks)]
+        line["gate_up"] = [time_gate_up(args.small_iters, flush, peaks)]
         del flush
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, host, budget_s=args.cpu_seconds)

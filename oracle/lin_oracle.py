@@ -108,6 +108,7 @@ __all__ = [
     "matmul_t_swiglu_backward_w16",
     "cross_entropy",
     "lm_head_cross_entropy_w16",
+    "gate_up_w16",
     "normaliser",
     "normalised_error",
     "reference",
@@ -379,6 +380,13 @@ def lm_head_cross_entropy_w16(X, W16, targets, alpha=0.0, beta=0.0, inv_norm=1.0
     """(losses, dlogits, loss_sum) for logits = X @ W16 (binary16 bits)."""
     losses, dl = cross_entropy(matmul_w16(X, W16), targets, alpha, beta, inv_norm)
     return losses, dl, float(np.sum(losses))
+
+
+def gate_up_w16(X, WG16, WU16):
+    """(GATE, UP) = (X @ W_gate, X @ W_up), binary16 weight bits [K,N]: the
+    producer of the SwiGLU form's inputs (not on the pages; two matmul_w16
+    products of one X)."""
+    return matmul_w16(X, WG16), matmul_w16(X, WU16)
 
 
 # --------------------------------------------------------------------------

@@ -476,3 +476,14 @@ def test_cross_entropy_gradient_is_the_loss_derivative(alpha, beta):
         mx = np.max(L[s])
         lse = mx + math.log(np.sum(np.exp(L[s] - mx)))
         assert math.isclose(float(np.sum(dl[s])), 2 * beta * lse * 0.5, abs_tol=1e-12)
+
+
+def test_gate_up_brute_force():
+    rng = np.random.default_rng(41)
+    X = rng.integers(-4, 5, size=(3, 5)).astype(np.float32)
+    wg = (rng.standard_normal((5, 4)) * 0.5).astype(np.float16)
+    wu = (rng.standard_normal((5, 4)) * 0.5).astype(np.float16)
+    G, U = oracle.gate_up_w16(X, wg.view(np.uint16), wu.view(np.uint16))
+    for i, n in itertools.product(range(3), range(4)):
+        assert G[i, n] == sum(float(X[i, k]) * float(wg[k, n]) for k in range(5))
+        assert U[i, n] == sum(float(X[i, k]) * float(wu[k, n]) for k in range(5))

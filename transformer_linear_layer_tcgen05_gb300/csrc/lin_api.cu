@@ -257,6 +257,8 @@ struct Problem {
   // online-softmax partials of every output row (clustered kernel, no split)
   float2* row_stats = nullptr;
   int stats_cols = 0;
+  // dual GEMM: Y2 = A · W2 beside Y = A · W (binary16 W2 [K,N]; Y2 [M,N])
+  const void* W2 = nullptr;
 };
 
 // `fixed`: where a split tail's workspace comes from instead of the library's
@@ -293,7 +295,16 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
                                            : misaligned(p.X))))
     return LIN_ERROR_MISALIGNED;
 
-  const bool swb = p.Y2 != nullptr;
+  const bool dual = p.W2 != nullptr;
+  if (dual) {   // a second binary16 weight matrix and a second output
+    if (!p.w16 || !p.Y2 || resid || p.bt || p.at || swiglu) return LIN_ERROR_INVALID_VALUE;
+    if (misaligned(p.Y2) || (K > 0 && misaligned(p.W2))) return LIN_ERROR_MISALIGNED;
+    if (overlaps(p.Y2, mn_bytes, p.Y, mn_bytes) || overlaps(p.Y2, mn_bytes, p.X, a_bytes) ||
+        overlaps(p.Y2, mn_bytes, p.W, w_bytes) || overlaps(p.Y2, mn_bytes, p.W2, w_bytes) ||
+        overlaps(p.Y, mn_bytes, p.W2, w_bytes))
+      return LIN_ERROR_ALIASING;
+  }
+  const bool swb = p.Y2 != nullptr && !dual;
   if (swb) {
     if (!p.G2 || !p.U2 || resid) return LIN_ERROR_INVALID_VALUE;
     if (misaligned(p.G2) || misaligned(p.U2) || misaligned(p.Y2)) return LIN_ERROR_MISALIGNED;
@@ -329,6 +340,10 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
   // 6. every buffer is device memory of this device and large enough
   if ((st = check_buffer(p.Y, mn_bytes, dev)) != LIN_SUCCESS) return st;
   if (resid && (st = check_buffer(p.R, mn_bytes, dev)) != LIN_SUCCESS) return st;
+  if (dual) {
+    if ((st = check_buffer(p.Y2, mn_bytes, dev)) != LIN_SUCCESS) return st;
+    if (K > 0 && (st = check_buffer(p.W2, w_bytes, dev)) != LIN_SUCCESS) return st;
+  }
   if (swb) {
     if ((st = check_buffer(p.Y2, mn_bytes, dev)) != LIN_SUCCESS) return st;
     if ((st = check_buffer(p.G2, mn_bytes, dev)) != LIN_SUCCESS) return st;
@@ -352,7 +367,7 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
   // 7. K == 0: nothing is accumulated, Y = R (or 0)
   if (K == 0) {   // nothing to accumulate: Y = R (already so when accumulating in place), or 0
     cudaError_t e = cudaSuccess;
-    if (swb) {   // dA = 0: both gradients are 0 (nan_guard maps a NaN product to 0 too)
+    if (swb || dual) {   // both outputs 0 (for swb: nan_guard maps a NaN product to 0 too)
       e = cudaMemsetAsync(p.Y, 0, mn_bytes, stream);
       if (e == cudaSuccess) e = cudaMemsetAsync(p.Y2, 0, mn_bytes, stream);
     } else if (!resid)
@@ -365,7 +380,8 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
   // 8. tensor maps and launch
   const int bn = 128;
   int cn = (p.w16 && !p.at) ? f16_cluster_size(N) : 0;   // 0: the per-tile kernel
-  if (p.row_stats && cn == 0) cn = 1;   // the partials come from the clustered epilogue
+  // the row partials and the dual product exist in the clustered kernel only
+  if ((p.row_stats || p.W2) && cn == 0) cn = 1;
   lin::TensorMaps maps;
   std::memset(&maps, 0, sizeof(maps));
   const CUtensorMapDataType f32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
@@ -386,6 +402,10 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
       ok &= encode_2d(&maps.w, f32, p.W, K, N, K * 4, 32, (uint32_t)bn);
   } else if (p.w16) {
     ok &= encode_2d(&maps.w, CU_TENSOR_MAP_DATA_TYPE_UINT16, p.W, N, K, N * 2, 64, 64);
+    if (dual) {
+      ok &= encode_2d(&maps.w2, CU_TENSOR_MAP_DATA_TYPE_UINT16, p.W2, N, K, N * 2, 64, 64);
+      ok &= encode_2d(&maps.y2, f32, p.Y2, N, M, N * 4, lin::kEpiCols, lin::kEpiRows);
+    }
   } else {
     ok &= encode_2d(&maps.w, f32, p.W, N, K, N * 4, 32, 32);
   }
@@ -480,6 +500,7 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
     // binary16 X from a pre-pass, in the workspace after the partial tiles
     bool tma_a = !swiglu && !fixed && K % 8 == 0 && f16_preconvert(num_ng);
     auto capacity = [&]() {
+      if (dual) return lin::cluster_capacity_dual(tma_a, cn, &ce);
       if (p.bt) return lin::cluster_capacity_bt(tma_a, cn, resid, &ce);
       return swiglu ? lin::cluster_capacity_swiglu(cn, &ce)
                     : (tma_a ? lin::cluster_capacity_tma(cn, resid, &ce)
@@ -488,8 +509,12 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
     int cap = capacity();
     if (cap < 1) return cuda_fail(ce);
     // (a split tail's rows are finished by the split sum, which has no partials)
-    lin::SplitPlan plan = p.row_stats ? lin::SplitPlan{0, 0, 1}
-                                      : lin::split_plan(num_m * num_ng, cap, nkb);
+    // (the dual product's tiles are split nowhere either: the split sum
+    // writes one output)
+    const int bno = dual ? lin::kClusterBN / 2 : lin::kClusterBN;
+    const int num_ng_o = (int)((N + (uint64_t)bno * cn - 1) / ((uint64_t)bno * cn));
+    lin::SplitPlan plan = (p.row_stats || dual) ? lin::SplitPlan{0, 0, 1}
+                                                : lin::split_plan(num_m * num_ng_o, cap, nkb);
     const size_t part_bytes = lin::split_part_bytes(plan, cn, lin::kClusterBN);
     const size_t xh_off = (part_bytes + 255) & ~size_t(255);
     const size_t xh_bytes = tma_a ? (size_t)M * (size_t)K * 2 : 0;
@@ -514,9 +539,12 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
       else
         e = lin::launch_cvt_f16(p.X, xh, M * K, sm_count(dev), stream);
       if (e == cudaSuccess)
-        e = p.bt ? lin::launch_gemm_cluster_bt(true, cn, resid, maps, args, stream)
-                 : lin::launch_gemm_cluster_tma(cn, resid, maps, args, stream);
+        e = dual   ? lin::launch_gemm_cluster_dual(true, cn, maps, args, stream)
+            : p.bt ? lin::launch_gemm_cluster_bt(true, cn, resid, maps, args, stream)
+                   : lin::launch_gemm_cluster_tma(cn, resid, maps, args, stream);
       kernels = 2;
+    } else if (dual) {
+      e = lin::launch_gemm_cluster_dual(false, cn, maps, args, stream);
     } else if (p.bt) {
       e = lin::launch_gemm_cluster_bt(false, cn, resid, maps, args, stream);
     } else {
@@ -835,6 +863,18 @@ lin_status lin_lm_head_cross_entropy_w16(const float* X, const uint16_t* W16,
                                          lin_stream_t stream) {
   return lm_head_cross_entropy(X, W16, targets, DLOGITS, losses, loss_sum, M, V, K, alpha, beta,
                                inv_norm, reinterpret_cast<cudaStream_t>(stream));
+}
+
+// The FFN's gate and up projections in one launch: GATE = X @ W_gate and
+// UP = X @ W_up (binary16 weights) from one read of X.
+lin_status lin_gate_up_w16(const float* X, const uint16_t* WG16, const uint16_t* WU16,
+                           float* GATE, float* UP, int64_t M, int64_t N, int64_t K,
+                           lin_stream_t stream) {
+  Problem p{F_MATMUL, true, X, nullptr, nullptr, WG16, nullptr, GATE, M, N, K};
+  p.W2 = WU16;
+  p.Y2 = UP;
+  if (!UP || (K > 0 && !WU16)) return LIN_ERROR_INVALID_VALUE;
+  return run(p, reinterpret_cast<cudaStream_t>(stream));
 }
 
 const char* lin_status_string(lin_status status) {

@@ -50,7 +50,12 @@ namespace lin {
 
 // BT: W given as [N][K] (K contiguous, the backward product dY · W^T): its
 // tiles are a K-major B operand, one TMA box of BN rows per k-block.
-template <int AMODE, bool RESID, int BN_, int CN_, bool V8_ = false, bool BT_ = false>
+// DUAL: two products of the same A, Y = A @ W and Y2 = A @ W2 (the FFN's
+// gate and up projections from one read of X): the B stage holds BN/2
+// columns of W and the same BN/2 columns of W2 side by side, so one UMMA of
+// N = BN computes both tiles; each CTA then covers BN/2 output columns.
+template <int AMODE, bool RESID, int BN_, int CN_, bool V8_ = false, bool BT_ = false,
+          bool DUAL_ = false>
 struct ClusterTraits {
   static_assert(AMODE == A_CVT_F16 || AMODE == A_SWIGLU_F16 || AMODE == A_TMA_F16,
                 "binary16 forms only");
@@ -66,6 +71,8 @@ struct ClusterTraits {
   static constexpr int NMMA = BK / KSTEP;
   static constexpr int W_ATOM = 64;
   static constexpr bool kBT = BT_;
+  static constexpr bool kDual = DUAL_;
+  static constexpr int BNO = kDual ? BN_ / 2 : BN_;   // output columns per CTA and product
   static constexpr int W_BOXES = kBT ? 1 : BN / W_ATOM;
   static constexpr int ROWS = BM / CN;            // A rows this CTA transforms
   static constexpr int INPUTS = kSwiglu ? 2 : 1;  // GATE and UP, or X
@@ -249,16 +256,17 @@ __device__ __forceinline__ void stage_store(uint32_t a_stage, uint32_t crank, in
   }
 }
 
-template <int AMODE, bool RESID, int BN, int CN, bool V8, bool BT>
-__global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT>::kThreadsC, 1)
+template <int AMODE, bool RESID, int BN, int CN, bool V8, bool BT, bool DUAL>
+__global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DUAL>::kThreadsC, 1)
     lin_gemm_cluster_kernel(const __grid_constant__ CUtensorMap tm_w,
+                            const __grid_constant__ CUtensorMap tm_w2,
                             const __grid_constant__ CUtensorMap tm_a,
                             const __grid_constant__ CUtensorMap tm_r,
                             const __grid_constant__ CUtensorMap tm_y,
                             const __grid_constant__ CUtensorMap tm_g2,
                             const __grid_constant__ CUtensorMap tm_u2,
                             const __grid_constant__ CUtensorMap tm_y2, const KernelArgs args) {
-  using T = ClusterTraits<AMODE, RESID, BN, CN, V8, BT>;
+  using T = ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DUAL>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -274,7 +282,7 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT>::k
   const int cid = blockIdx.x / CN;                  // cluster id
   const int ncl = gridDim.x / CN;                   // clusters in the grid
   const int num_m = (args.M + T::BM - 1) / T::BM;
-  const int num_ng = (args.N + T::BN * CN - 1) / (T::BN * CN);
+  const int num_ng = (args.N + T::BNO * CN - 1) / (T::BNO * CN);
   const int num_tiles = num_m * num_ng;
   const int nkb = (args.K + T::BK - 1) / T::BK;
   const WaitCtl ctl{args.timeout_ns, abort_flag, args.status};
@@ -282,7 +290,7 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT>::k
   auto a_stage = [&](int s) -> uint32_t { return sbase + T::OFF_OP + s * T::OP_STAGE_BYTES; };
   auto b_stage = [&](int s) -> uint32_t { return a_stage(s) + T::A_BYTES; };
   auto tile_m0 = [&](int t) -> int { return (t / num_ng) * T::BM; };
-  auto tile_n0 = [&](int t) -> int { return ((t % num_ng) * CN + (int)crank) * T::BN; };
+  auto tile_n0 = [&](int t) -> int { return ((t % num_ng) * CN + (int)crank) * T::BNO; };
   // Work items of this cluster: whole tiles cid + i*ncl, round robin; with a
   // split tail (split_s >= 2), split_r whole tiles and then, for clusters
   // below split_rem*split_s, K range `unit_p` of tail tile split_r*ncl +
@@ -375,6 +383,13 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT>::k
           mbar_arrive_expect_tx(full, T::B_BYTES + (T::kTmaA ? T::A_BYTES : 0u));
           if constexpr (T::kBT) {
             tma_load_2d(b_stage(s), &tm_w, kb * T::BK, n0, full);   // W as [N][K]
+          } else if constexpr (T::kDual) {   // [W tile | W2 tile], BN/2 columns each
+#pragma unroll
+            for (int j = 0; j < T::W_BOXES; ++j) {
+              const int jj = j % (T::W_BOXES / 2);
+              tma_load_2d(b_stage(s) + j * T::B_ATOM_BYTES, j < T::W_BOXES / 2 ? &tm_w : &tm_w2,
+                          n0 + jj * T::W_ATOM, kb * T::BK, full);
+            }
           } else {
 #pragma unroll
             for (int j = 0; j < T::W_BOXES; ++j)
@@ -580,7 +595,9 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT>::k
       const int row0 = tile_m0(t) + q * kEpiRows;
       const int n0 = tile_n0(t);
       int nc = n0 < args.N ? (args.N - n0 + kEpiCols - 1) / kEpiCols : 0;
-      if (nc > NC) nc = NC;
+      if (nc > T::BNO / kEpiCols) nc = T::BNO / kEpiCols;
+      // chunks staged: nc, or nc of each product (Y's, then Y2's)
+      const int nct = T::kDual ? 2 * nc : nc;
       // rows wholly past M: nothing to store (a store box may not start there)
       const bool rows_in = row0 < args.M;
       const bool staged = !is_unit && rows_in && nc > 0;
@@ -660,12 +677,17 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT>::k
         }
       } else if (staged) {
         // online-softmax partials of this lane's row over the tile's columns
-        const bool stats = (args.flags & KFLAG_ROW_STATS) != 0;
+        const bool stats = !T::kDual && (args.flags & KFLAG_ROW_STATS) != 0;
         float rm = -INFINITY, rs = 0.0f;
-        for (int c = 0; c < nc && ok; ++c) {
+        for (int c = 0; c < nct && ok; ++c) {
           const uint32_t e = ec + (uint32_t)c;
           const uint32_t b = e & 1u;
-          if (lane == 0 && c + 1 < nc) {
+          // DUAL: chunk c < nc is Y's, else Y2's; its TMEM columns follow
+          // the B stage ([W tile | W2 tile])
+          const bool second = T::kDual && c >= nc;
+          const int oc = second ? c - nc : c;                       // chunk of its output
+          const int tc = second ? NC / 2 + oc : c;                  // chunk of the accumulator
+          if (lane == 0 && c + 1 < nct) {
             // the other buffer's last store must have read it before it is
             // refilled (or, without R, rewritten below)
             bulk_wait_group_read<0>();
@@ -677,7 +699,7 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT>::k
           }
           __syncwarp();
           uint32_t v[32];
-          tmem_ld_32x32b_x32(acc + (uint32_t)(c * kEpiCols), v);
+          tmem_ld_32x32b_x32(acc + (uint32_t)(tc * kEpiCols), v);
           tmem_wait_ld();
           if constexpr (RESID) {
             if (!warp_wait_phase(ebar(b), (e >> 1) & 1u, ctl)) {
@@ -726,12 +748,12 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT>::k
           fence_proxy_async_smem();   // staged Y -> visible to the TMA store
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(&tm_y, n0 + c * kEpiCols, row0, buf(b));
+            tma_store_2d(second ? &tm_y2 : &tm_y, n0 + oc * kEpiCols, row0, buf(b));
             bulk_commit_group();
           }
           __syncwarp();
         }
-        ec += (uint32_t)nc;
+        ec += (uint32_t)nct;
         if (stats && ok && row0 + lane < args.M)
           args.row_stats[(size_t)(row0 + lane) * args.stats_cols + n0 / T::BN] =
               make_float2(rm, rs);
@@ -768,9 +790,9 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT>::k
 
 // Launch configuration of one instantiation; the first call per device sets
 // the shared-memory attribute and records how many clusters fit at once.
-template <int AMODE, bool RESID, int BN, int CN, bool BT = false>
+template <int AMODE, bool RESID, int BN, int CN, bool BT = false, bool DUAL = false>
 struct ClusterLaunch {
-  using T = ClusterTraits<AMODE, RESID, BN, CN, false, BT>;
+  using T = ClusterTraits<AMODE, RESID, BN, CN, false, BT, DUAL>;
   // attr must hold 2 entries: the cluster shape and, for launches, the
   // programmatic dependence on the previous kernel of the stream.
   static cudaLaunchConfig_t config(cudaLaunchAttribute* attr, cudaStream_t stream,
@@ -793,7 +815,7 @@ struct ClusterLaunch {
   static int capacity(cudaError_t* err) {
     static std::atomic<uint64_t> attr_done{0};
     static std::atomic<int> max_clusters[64];
-    auto kern = lin_gemm_cluster_kernel<AMODE, RESID, BN, CN, false, BT>;
+    auto kern = lin_gemm_cluster_kernel<AMODE, RESID, BN, CN, false, BT, DUAL>;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess && dev >= 64) e = cudaErrorInvalidDevice;
@@ -806,9 +828,9 @@ struct ClusterLaunch {
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
       if constexpr (!T::kTmaA) {   // the 32-byte-load variant of the transform
         if (e == cudaSuccess)
-          e = cudaFuncSetAttribute(lin_gemm_cluster_kernel<AMODE, RESID, BN, CN, true, BT>,
+          e = cudaFuncSetAttribute(lin_gemm_cluster_kernel<AMODE, RESID, BN, CN, true, BT, DUAL>,
                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   ClusterTraits<AMODE, RESID, BN, CN, true, BT>::SMEM_BYTES);
+                                   ClusterTraits<AMODE, RESID, BN, CN, true, BT, DUAL>::SMEM_BYTES);
       }
       cudaLaunchAttribute attr[2];
       cudaLaunchConfig_t cfg = config(attr, nullptr, false);
@@ -832,7 +854,7 @@ struct ClusterLaunch {
     const int cap = capacity(&e);
     if (cap < 1) return e;
     const int num_m = (args.M + T::BM - 1) / T::BM;
-    const int num_ng = (args.N + T::BN * CN - 1) / (T::BN * CN);
+    const int num_ng = (args.N + T::BNO * CN - 1) / (T::BNO * CN);
     int clusters;
     if (args.split_s >= 2)
       clusters = args.split_r > 0 ? cap : args.split_rem * args.split_s;
@@ -844,11 +866,12 @@ struct ClusterLaunch {
     cfg.gridDim = dim3((unsigned)(clusters * CN), 1, 1);
     if constexpr (!T::kTmaA) {
       if (args.flags & KFLAG_A_V8)
-        return cudaLaunchKernelEx(&cfg, lin_gemm_cluster_kernel<AMODE, RESID, BN, CN, true, BT>,
-                                  m.w, m.a, m.r, m.y, m.g2, m.u2, m.y2, args);
+        return cudaLaunchKernelEx(&cfg,
+                                  lin_gemm_cluster_kernel<AMODE, RESID, BN, CN, true, BT, DUAL>,
+                                  m.w, m.w2, m.a, m.r, m.y, m.g2, m.u2, m.y2, args);
     }
-    return cudaLaunchKernelEx(&cfg, lin_gemm_cluster_kernel<AMODE, RESID, BN, CN, false, BT>, m.w,
-                              m.a, m.r, m.y, m.g2, m.u2, m.y2, args);
+    return cudaLaunchKernelEx(&cfg, lin_gemm_cluster_kernel<AMODE, RESID, BN, CN, false, BT, DUAL>,
+                              m.w, m.w2, m.a, m.r, m.y, m.g2, m.u2, m.y2, args);
   }
 };
 

@@ -95,7 +95,9 @@ inline size_t split_part_bytes(const SplitPlan& p, int cn, int bn) {
 // UP (SwiGLU forms only), `w` the weights, `r` the residual, `y` the output.
 struct TensorMaps {
   CUtensorMap a, u, w, r, y;
-  CUtensorMap g2, u2, y2;   // GATE, UP, dUP of the SwiGLU-backward epilogue ([32 x 32] boxes)
+  CUtensorMap g2, u2, y2;   // GATE, UP, dUP of the SwiGLU-backward epilogue ([32 x 32] boxes);
+                            // y2 is also the second output of the dual GEMM
+  CUtensorMap w2;           // the second weight matrix of the dual GEMM
 };
 
 // Block-tile geometry shared by host and device.
@@ -136,6 +138,11 @@ int cluster_capacity_tma(int cn, bool resid, cudaError_t* err);
 cudaError_t launch_gemm_cluster_bt(bool tma_a, int cn, bool resid, const TensorMaps& maps,
                                    const KernelArgs& args, cudaStream_t stream);
 int cluster_capacity_bt(bool tma_a, int cn, bool resid, cudaError_t* err);
+// Two products of one A (Y = A @ W, Y2 = A @ W2; tensor maps w, w2, y, y2):
+// each CTA covers 128 output columns of both.
+cudaError_t launch_gemm_cluster_dual(bool tma_a, int cn, const TensorMaps& maps,
+                                     const KernelArgs& args, cudaStream_t stream);
+int cluster_capacity_dual(bool tma_a, int cn, cudaError_t* err);
 // Xh[i] = binary16(X[i]) (round to nearest even) for i < n, n % 4 == 0,
 // both bases 16-byte aligned.
 cudaError_t launch_cvt_f16(const float* X, uint16_t* Xh, int64_t n, int sms, cudaStream_t stream);

@@ -70,6 +70,7 @@ SIGNATURES = {
     "lin_matmul_t_swiglu_backward": [_P, _P, _P, _P, _P, _P, _I, _I, _I, _S],
     "lin_matmul_t_swiglu_backward_w16": [_P, _P, _P, _P, _P, _P, _I, _I, _I, _S],
     "lin_lm_head_cross_entropy_w16": [_P, _P, _P, _P, _P, _P, _I, _I, _I, _F, _F, _F, _S],
+    "lin_gate_up_w16": [_P, _P, _P, _P, _P, _I, _I, _I, _S],
 }
 
 _lib = None
@@ -362,6 +363,16 @@ def lin_lm_head_cross_entropy_w16(X, W16, targets, DLOGITS, losses, loss_sum, al
     return DLOGITS, losses, loss_sum
 
 
+def lin_gate_up_w16(X, WG16, WU16, GATE, UP, stream=None):
+    """GATE = X @ WG16 and UP = X @ WU16 (binary16 weights) in one launch."""
+    M, N, K = _dims(_f32(X, "X"), _w16(WG16, "WG16"), _f32(GATE, "GATE"))
+    if tuple(_w16(WU16, "WU16").shape) != (K, N) or tuple(_f32(UP, "UP").shape) != (M, N):
+        raise ValueError("WU16 must be [K, N] and UP [M, N]")
+    _call("lin_gate_up_w16", X.data_ptr(), WG16.data_ptr(), WU16.data_ptr(), GATE.data_ptr(),
+          UP.data_ptr(), M, N, K, _stream_handle(stream))
+    return GATE, UP
+
+
 def lin_last_launch_info() -> tuple:
     """(kernels launched, workspace bytes taken) by the last compute call made
     on this thread."""
@@ -403,6 +414,7 @@ FORM_FUNCS = {
 # entry points whose outputs are not a single [M, N] product (no run_form)
 OTHER_FUNCS = {
     "lm_head_cross_entropy_w16": lin_lm_head_cross_entropy_w16,
+    "gate_up_w16": lin_gate_up_w16,
 }
 
 
