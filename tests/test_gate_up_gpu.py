@@ -54,7 +54,7 @@ from tests.test_gate_up_gpu import _int_inputs, _run
 require_gpu()
 bad = 0
 for (M, N, K) in [(128, 128, 64), (129, 136, 68), (1, 1032, 4), (300, 2048, 200),
-                  (700, 1536, 256), (4736, 1024, 1024), (513, 8192, 512)]:
+                  (700, 1536, 256), (4736, 1024, 1024), (513, 8192, 512), (257, 8192, 4096)]:
     X, WG, WU = _int_inputs(M, N, K, seed=M + N + K)
     G, U = _run(X, WG, WU)
     rg, ru = oracle.gate_up_w16(X, WG, WU)

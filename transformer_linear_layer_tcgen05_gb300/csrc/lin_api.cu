@@ -515,6 +515,14 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
     const int num_ng_o = (int)((N + (uint64_t)bno * cn - 1) / ((uint64_t)bno * cn));
     lin::SplitPlan plan = (p.row_stats || dual) ? lin::SplitPlan{0, 0, 1}
                                                 : lin::split_plan(num_m * num_ng_o, cap, nkb);
+    // Bands of column groups whose weights stay in L2 (every cluster tile
+    // reads K x cn x 256 binary16 weights, both halves of the dual form
+    // included), when the whole W would not fit.
+    {
+      const long long per_ng = (long long)K * cn * lin::kClusterBN * 2;
+      const long long band = per_ng > 0 ? lin::kBandWeightBytes / per_ng : 0;
+      args.band_ng = band >= 1 && band < num_ng_o ? (int)band : 0;
+    }
     const size_t part_bytes = lin::split_part_bytes(plan, cn, lin::kClusterBN);
     const size_t xh_off = (part_bytes + 255) & ~size_t(255);
     const size_t xh_bytes = tma_a ? (size_t)M * (size_t)K * 2 : 0;

@@ -289,8 +289,12 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
 
   auto a_stage = [&](int s) -> uint32_t { return sbase + T::OFF_OP + s * T::OP_STAGE_BYTES; };
   auto b_stage = [&](int s) -> uint32_t { return a_stage(s) + T::A_BYTES; };
-  auto tile_m0 = [&](int t) -> int { return (t / num_ng) * T::BM; };
-  auto tile_n0 = [&](int t) -> int { return ((t % num_ng) * CN + (int)crank) * T::BNO; };
+  auto tile_m0 = [&](int t) -> int {
+    return tile_coords(t, num_m, num_ng, args.band_ng).m * T::BM;
+  };
+  auto tile_n0 = [&](int t) -> int {
+    return (tile_coords(t, num_m, num_ng, args.band_ng).ng * CN + (int)crank) * T::BNO;
+  };
   // Work items of this cluster: whole tiles cid + i*ncl, round robin; with a
   // split tail (split_s >= 2), split_r whole tiles and then, for clusters
   // below split_rem*split_s, K range `unit_p` of tail tile split_r*ncl +
@@ -885,7 +889,7 @@ template <bool RESID, bool SWB>
 __global__ void __launch_bounds__(256)
     lin_split_reduce_kernel(const float4* __restrict__ part, const float* __restrict__ R,
                             float* __restrict__ Y, int M, int N, int cn, int bn, int tile0,
-                            int num_ng, int rem, int s, const float* __restrict__ G2,
+                            int num_ng, int band, int rem, int s, const float* __restrict__ G2,
                             const float* __restrict__ U2, float* __restrict__ Y2) {
   const int c4n = bn / 4;
   const long long per_cta = 128LL * c4n;
@@ -896,8 +900,9 @@ __global__ void __launch_bounds__(256)
   const int c4 = (int)((x / 128) % c4n);
   const int r = (int)(x % 128);
   const int t = tile0 + j;
-  const int row = (t / num_ng) * 128 + r;
-  const int col = ((t % num_ng) * cn + crank) * bn + 4 * c4;
+  const TileRC rc = tile_coords(t, (M + 127) / 128, num_ng, band);
+  const int row = rc.m * 128 + r;
+  const int col = (rc.ng * cn + crank) * bn + 4 * c4;
   // The next kernel on the stream may be scheduled now: it waits for this
   // grid's completion itself before it touches memory.
   pdl_launch_dependents();

@@ -61,7 +61,29 @@ struct KernelArgs {
   float* Y2;            // dUP [M,N] of the SwiGLU-backward epilogue (dGATE goes to Y)
   float2* row_stats;    // [M][stats_cols] (max, sum exp) partials (KFLAG_ROW_STATS)
   int32_t stats_cols;
+  int32_t band_ng;      // column groups per band of the clustered tile order (0: one band)
 };
+
+// Order of the clustered kernels' tiles: tile t of a grid of num_m row
+// blocks x num_ng column groups. The column groups are taken in bands of
+// `band` (the last one narrower); the bands run one after another, and within
+// a band the column group varies fastest. While a band runs, the clusters
+// share its slice of the weights, which stays resident in L2 when the whole
+// W would not. band <= 0 or >= num_ng: one band, plain row-major order.
+struct TileRC {
+  int m, ng;
+};
+__host__ __device__ inline TileRC tile_coords(int t, int num_m, int num_ng, int band) {
+  if (band <= 0 || band >= num_ng) return TileRC{t / num_ng, t % num_ng};
+  const int per_band = num_m * band;
+  const int b = t / per_band;
+  const int w = num_ng - b * band < band ? num_ng - b * band : band;
+  const int i = t - b * per_band;
+  return TileRC{i / w, b * band + i % w};
+}
+// Weight bytes a band may span (the L2 holds 126 MB; the streamed operands
+// and outputs need the rest).
+constexpr long long kBandWeightBytes = 32ll << 20;
 
 // Work plan of a persistent launch over `tiles` cluster tiles on `clusters`
 // clusters: `r` whole rounds (every cluster runs tiles cid + i*clusters), then

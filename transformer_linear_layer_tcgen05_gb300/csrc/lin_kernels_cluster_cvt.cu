@@ -127,14 +127,14 @@ cudaError_t launch_split_reduce(const KernelArgs& args, bool resid, int cn, int 
   const float4* part = reinterpret_cast<const float4*>(args.part);
   if (args.flags & KFLAG_SWIGLU_BWD)
     return cudaLaunchKernelEx(&cfg, lin_split_reduce_kernel<false, true>, part, args.R, args.Y,
-                              args.M, args.N, cn, bn, tile0, num_ng, args.split_rem, args.split_s,
+                              args.M, args.N, cn, bn, tile0, num_ng, args.band_ng, args.split_rem, args.split_s,
                               args.G2, args.U2, args.Y2);
   if (resid)
     return cudaLaunchKernelEx(&cfg, lin_split_reduce_kernel<true, false>, part, args.R, args.Y,
-                              args.M, args.N, cn, bn, tile0, num_ng, args.split_rem, args.split_s,
+                              args.M, args.N, cn, bn, tile0, num_ng, args.band_ng, args.split_rem, args.split_s,
                               args.G2, args.U2, args.Y2);
   return cudaLaunchKernelEx(&cfg, lin_split_reduce_kernel<false, false>, part, args.R, args.Y,
-                            args.M, args.N, cn, bn, tile0, num_ng, args.split_rem, args.split_s,
+                            args.M, args.N, cn, bn, tile0, num_ng, args.band_ng, args.split_rem, args.split_s,
                             args.G2, args.U2, args.Y2);
 }
 
