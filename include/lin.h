@@ -299,6 +299,63 @@ lin_status lin_gate_up_w16(const float *X, const uint16_t *WG16, const uint16_t 
                            float *GATE, float *UP, int64_t M, int64_t N, int64_t K,
                            lin_stream_t stream);
 
+/*
+ * Host-operand forms
+ * ------------------
+ * lin_<form>_host: the six forward forms above with every operand (X or GATE
+ * and UP, W or W16, R, Y) in HOST memory, same layouts, arithmetic, bound
+ * and shape rules. The pages' engine binds device buffers only; these entry
+ * points are the library's own, for callers whose activations live on the
+ * host. The call copies the operands to the device and Y back itself, in
+ * blocks of whole 128-row tiles (about 64 MiB of operands and result per
+ * block; lin_set_host_block_bytes changes it): the copy of block c+1 to the
+ * device and of block c-1 back run on two copy streams of the library's
+ * while the caller's stream runs the device form on block c. Each block is
+ * one call of the device form on its rows (its own split tail, if any), so
+ * results satisfy the same bound but need not equal the device form's bits
+ * where that splits differently.
+ * Memory      Operands are host memory, pinned (cudaHostAlloc /
+ *             cudaHostRegister: the copies then overlap the GEMMs) or
+ *             pageable (correct, but the runtime stages each copy and the
+ *             call is then largely synchronous). Device or managed memory
+ *             -> LIN_ERROR_INVALID_VALUE. Staging memory on the device (W
+ *             once, then three blocks' worth of each other operand) is one
+ *             stream-ordered allocation from the library's pool, taken and
+ *             given back on `stream`.
+ * Stream      Enqueued work ends on `stream`, which waits for the last copy
+ *             back: host inputs must stay unchanged, and Y must not be read,
+ *             until `stream` gets there (cudaStreamSynchronize).
+ * Errors      Validation as for the device forms, before anything is
+ *             enqueued (Y overlapping an input -> LIN_ERROR_ALIASING; the
+ *             16-byte alignment rule does not apply to host operands). A
+ *             CUDA failure part-way returns LIN_ERROR_CUDA after the blocks
+ *             already enqueued; Y is then partly written.
+ * lin_last_launch_info reports the kernels of all blocks and the staging
+ * plus the largest per-block workspace.
+ */
+lin_status lin_matmul_host(const float *X, const float *W, float *Y,
+                           int64_t M, int64_t N, int64_t K, lin_stream_t stream);
+lin_status lin_matmul_residual_host(const float *X, const float *W, const float *R, float *Y,
+                                    int64_t M, int64_t N, int64_t K, lin_stream_t stream);
+lin_status lin_matmul_residual_swiglu_a_host(const float *GATE, const float *UP, const float *W,
+                                             const float *R, float *Y,
+                                             int64_t M, int64_t N, int64_t K,
+                                             lin_stream_t stream);
+lin_status lin_matmul_w16_host(const float *X, const uint16_t *W16, float *Y,
+                               int64_t M, int64_t N, int64_t K, lin_stream_t stream);
+lin_status lin_matmul_residual_w16_host(const float *X, const uint16_t *W16, const float *R,
+                                        float *Y, int64_t M, int64_t N, int64_t K,
+                                        lin_stream_t stream);
+lin_status lin_matmul_residual_swiglu_a_w16_host(const float *GATE, const float *UP,
+                                                 const uint16_t *W16, const float *R, float *Y,
+                                                 int64_t M, int64_t N, int64_t K,
+                                                 lin_stream_t stream);
+
+/* Operand-plus-result bytes per block of the host-operand forms (rounded
+ * down to whole 128-row tiles, at least one tile); 0 restores the default
+ * (64 MiB). Process-wide; values from 1 to 65535 -> LIN_ERROR_INVALID_VALUE. */
+lin_status lin_set_host_block_bytes(uint64_t bytes);
+
 /* Static, NUL-terminated name of a status code ("LIN_SUCCESS", ...). Never NULL. */
 const char *lin_status_string(lin_status status);
 

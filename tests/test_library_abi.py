@@ -47,6 +47,9 @@ def test_binding_covers_every_compute_entry_point():
         if name.startswith("lin_matmul"):
             assert name in lin.SIGNATURES
             assert hasattr(lin, name)
+            if name.endswith("_host"):   # a forward form on host operands
+                assert name[len("lin_"):-len("_host")] in lin.HOST_FORM_FUNCS
+                continue
             # a _noalloc variant is its base form with a fixed workspace
             assert name[len("lin_"):].removesuffix("_noalloc") in lin.FORM_FUNCS
         if name.startswith(("lin_lm_head", "lin_gate_up")):
@@ -123,6 +126,26 @@ def test_aliasing_rule(L):
         lin.LIN_ERROR_ALIASING
     # adjacent but disjoint is not aliasing (it fails later, at the device check)
     assert L.lin_matmul(X, W, X + 256, 8, 8, 8, None) != lin.LIN_ERROR_ALIASING
+
+
+def test_host_forms_validate_before_touching_cuda(L):
+    # the device forms' dims, pointer, shape and aliasing rules, checked
+    # before the operands' memory type is looked up (no CUDA call)
+    assert L.lin_matmul_host(X, W, Y, -1, 8, 8, None) == lin.LIN_ERROR_INVALID_VALUE
+    assert L.lin_matmul_host(X, W, None, 8, 8, 8, None) == lin.LIN_ERROR_INVALID_VALUE
+    assert L.lin_matmul_residual_host(X, W, None, Y, 8, 8, 8, None) == lin.LIN_ERROR_INVALID_VALUE
+    assert L.lin_matmul_residual_swiglu_a_w16_host(G, None, W, R, Y, 8, 8, 8, None) == \
+        lin.LIN_ERROR_INVALID_VALUE
+    assert L.lin_matmul_host(X, W, Y, 8, 8, 6, None) == lin.LIN_ERROR_UNSUPPORTED_SHAPE
+    assert L.lin_matmul_w16_host(X, W, Y, 8, 12, 8, None) == lin.LIN_ERROR_UNSUPPORTED_SHAPE
+    assert L.lin_matmul_residual_host(X, W, Y, Y, 8, 8, 8, None) == lin.LIN_ERROR_ALIASING
+    assert L.lin_matmul_host(X, W, X + 240, 8, 8, 8, None) == lin.LIN_ERROR_ALIASING
+    assert L.lin_matmul_residual_swiglu_a_host(G, U, W, R, U + 16, 8, 8, 8, None) == \
+        lin.LIN_ERROR_ALIASING
+    assert L.lin_matmul_host(None, None, None, 0, 8, 8, None) == lin.LIN_SUCCESS
+    assert lin.lin_last_launch_info() == (0, 0)
+    assert L.lin_set_host_block_bytes(100) == lin.LIN_ERROR_INVALID_VALUE
+    assert L.lin_set_host_block_bytes(0) == lin.LIN_SUCCESS
 
 
 def test_transposed_forms_validate_before_touching_cuda(L):

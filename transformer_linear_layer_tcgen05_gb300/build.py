@@ -24,7 +24,7 @@ LIB_PATH = os.path.join(PKG_DIR, "liblin.so")
 SOURCES = ["lin_api.cu", "lin_kernels_tf32.cu", "lin_kernels_f16.cu",
            "lin_kernels_cluster_swiglu.cu", "lin_kernels_cluster_cvt.cu",
            "lin_kernels_cluster_bt.cu", "lin_kernels_cluster_dual.cu", "lin_loss.cu",
-           "lin_noalloc.cu"]
+           "lin_noalloc.cu", "lin_host.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
           "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

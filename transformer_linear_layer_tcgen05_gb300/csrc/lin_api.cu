@@ -259,6 +259,9 @@ struct Problem {
   int stats_cols = 0;
   // dual GEMM: Y2 = A · W2 beside Y = A · W (binary16 W2 [K,N]; Y2 [M,N])
   const void* W2 = nullptr;
+  // every buffer is a piece of one of the library's own device allocations
+  // (the host-operand entry points' staging): step 6 is skipped
+  bool staged = false;
 };
 
 // `fixed`: where a split tail's workspace comes from instead of the library's
@@ -338,8 +341,8 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
   if (st != LIN_SUCCESS) return st;
 
   // 6. every buffer is device memory of this device and large enough
-  if ((st = check_buffer(p.Y, mn_bytes, dev)) != LIN_SUCCESS) return st;
-  if (resid && (st = check_buffer(p.R, mn_bytes, dev)) != LIN_SUCCESS) return st;
+  if (!p.staged && (st = check_buffer(p.Y, mn_bytes, dev)) != LIN_SUCCESS) return st;
+  if (!p.staged && resid && (st = check_buffer(p.R, mn_bytes, dev)) != LIN_SUCCESS) return st;
   if (dual) {
     if ((st = check_buffer(p.Y2, mn_bytes, dev)) != LIN_SUCCESS) return st;
     if (K > 0 && (st = check_buffer(p.W2, w_bytes, dev)) != LIN_SUCCESS) return st;
@@ -349,7 +352,7 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
     if ((st = check_buffer(p.G2, mn_bytes, dev)) != LIN_SUCCESS) return st;
     if ((st = check_buffer(p.U2, mn_bytes, dev)) != LIN_SUCCESS) return st;
   }
-  if (K > 0) {
+  if (K > 0 && !p.staged) {
     if ((st = check_buffer(p.W, w_bytes, dev)) != LIN_SUCCESS) return st;
     if (swiglu) {
       if ((st = check_buffer(p.G, a_bytes, dev)) != LIN_SUCCESS) return st;
@@ -699,6 +702,34 @@ lin_status lm_head_cross_entropy(const float* X, const uint16_t* W16, const int3
 }
 
 lin_status record_cuda_error(cudaError_t e) { return cuda_fail(e); }
+
+lin_status forward_shape_status(bool w16, int64_t M, int64_t N, int64_t K) {
+  const int64_t kMax = 0x7fffffffLL;
+  if (M > kMax || N > kMax || K > kMax) return LIN_ERROR_UNSUPPORTED_SHAPE;
+  if (K % 4 != 0 || N % 4 != 0) return LIN_ERROR_UNSUPPORTED_SHAPE;
+  if (w16 && N % 8 != 0) return LIN_ERROR_UNSUPPORTED_SHAPE;
+  return LIN_SUCCESS;
+}
+
+lin_status checked_device(int* dev) {
+  int* word = nullptr;
+  return current_device(dev, &word);
+}
+
+cudaMemPool_t device_pool(int dev) { return workspace_pool(dev); }
+
+void set_last_launch_info(int kernels, uint64_t workspace_bytes) {
+  t_last_kernels = kernels;
+  t_last_workspace = workspace_bytes;
+}
+
+lin_status run_forward_staged(int form, bool w16, const float* X, const float* G, const float* U,
+                              const void* W, const float* R, float* Y, int64_t M, int64_t N,
+                              int64_t K, cudaStream_t stream) {
+  Problem p{static_cast<Form>(form), w16, X, G, U, W, R, Y, M, N, K};
+  p.staged = true;
+  return run(p, stream);
+}
 
 lin_status run_swiglu_w16_fixed(const float* GATE, const float* UP, const uint16_t* W16,
                                 const float* R, float* Y, int64_t M, int64_t N, int64_t K,

@@ -196,4 +196,18 @@ lin_status run_swiglu_w16_fixed(const float* GATE, const float* UP, const uint16
                                 cudaStream_t stream, lin::WorkspaceGetter get);
 // Records `e` as the calling thread's last CUDA error; returns LIN_ERROR_CUDA.
 lin_status record_cuda_error(cudaError_t e);
+// The shape rules of the forward forms (dims below 2^31, K and N multiples
+// of 4, N a multiple of 8 with binary16 W).
+lin_status forward_shape_status(bool w16, int64_t M, int64_t N, int64_t K);
+// The current device after the library's checks (sm_103, driver entry points).
+lin_status checked_device(int* dev);
+// The library's stream-ordered memory pool on `dev` (null if none).
+cudaMemPool_t device_pool(int dev);
+// What lin_last_launch_info() reports for the calling thread.
+void set_last_launch_info(int kernels, uint64_t workspace_bytes);
+// A forward form (0 matmul, 1 residual, 2 SwiGLU) on buffers that are pieces
+// of the library's own device allocations (no allocation-range checks).
+lin_status run_forward_staged(int form, bool w16, const float* X, const float* G, const float* U,
+                              const void* W, const float* R, float* Y, int64_t M, int64_t N,
+                              int64_t K, cudaStream_t stream);
 }  // namespace lin_detail

@@ -71,6 +71,13 @@ SIGNATURES = {
     "lin_matmul_t_swiglu_backward_w16": [_P, _P, _P, _P, _P, _P, _I, _I, _I, _S],
     "lin_lm_head_cross_entropy_w16": [_P, _P, _P, _P, _P, _P, _I, _I, _I, _F, _F, _F, _S],
     "lin_gate_up_w16": [_P, _P, _P, _P, _P, _I, _I, _I, _S],
+    "lin_matmul_host": [_P, _P, _P, _I, _I, _I, _S],
+    "lin_matmul_residual_host": [_P, _P, _P, _P, _I, _I, _I, _S],
+    "lin_matmul_residual_swiglu_a_host": [_P, _P, _P, _P, _P, _I, _I, _I, _S],
+    "lin_matmul_w16_host": [_P, _P, _P, _I, _I, _I, _S],
+    "lin_matmul_residual_w16_host": [_P, _P, _P, _P, _I, _I, _I, _S],
+    "lin_matmul_residual_swiglu_a_w16_host": [_P, _P, _P, _P, _P, _I, _I, _I, _S],
+    "lin_set_host_block_bytes": [ctypes.c_uint64],
 }
 
 _lib = None
@@ -390,6 +397,84 @@ def lin_get_device_status(stream=None) -> int:
 def lin_selftest_wait_timeout(timeout_us: int, stream=None) -> int:
     """Run the bounded-wait self-test; LIN_ERROR_TIMEOUT means it works."""
     return lib().lin_selftest_wait_timeout(int(timeout_us), _stream_handle(stream))
+
+
+# ------------------------------------------------- host-operand forms (CPU tensors)
+
+def _host(t, name, w16=False):
+    import torch
+    ok = isinstance(t, torch.Tensor) and not t.is_cuda and (
+        t.element_size() == 2 and t.dtype in (torch.float16, torch.int16,
+                                              getattr(torch, "uint16", torch.int16))
+        if w16 else t.dtype == torch.float32)
+    if not ok:
+        raise TypeError(f"{name} must be a {'16-bit' if w16 else 'float32'} CPU tensor")
+    if t.dim() != 2 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous 2-D tensor")
+    return t
+
+
+def _host_call(name, A, U, W, R, Y, w16, stream):
+    M, N, K = _dims(_host(A, "A"), _host(W, "W", w16), _host(Y, "Y"))
+    if U is not None and tuple(_host(U, "UP").shape) != (M, K):
+        raise ValueError("UP must be [M, K]")
+    if R is not None and tuple(_host(R, "R").shape) != (M, N):
+        raise ValueError("R must be [M, N]")
+    ptrs = [A.data_ptr()] + ([U.data_ptr()] if U is not None else []) + [W.data_ptr()] + \
+        ([R.data_ptr()] if R is not None else []) + [Y.data_ptr()]
+    _call(name, *ptrs, M, N, K, _stream_handle(stream))
+    return Y
+
+
+def lin_matmul_host(X, W, Y, stream=None):
+    """lin_matmul on host (CPU) tensors; pinned memory lets the copies overlap."""
+    return _host_call("lin_matmul_host", X, None, W, None, Y, False, stream)
+
+
+def lin_matmul_residual_host(X, W, R, Y, stream=None):
+    return _host_call("lin_matmul_residual_host", X, None, W, R, Y, False, stream)
+
+
+def lin_matmul_residual_swiglu_a_host(GATE, UP, W, R, Y, stream=None):
+    return _host_call("lin_matmul_residual_swiglu_a_host", GATE, UP, W, R, Y, False, stream)
+
+
+def lin_matmul_w16_host(X, W16, Y, stream=None):
+    return _host_call("lin_matmul_w16_host", X, None, W16, None, Y, True, stream)
+
+
+def lin_matmul_residual_w16_host(X, W16, R, Y, stream=None):
+    return _host_call("lin_matmul_residual_w16_host", X, None, W16, R, Y, True, stream)
+
+
+def lin_matmul_residual_swiglu_a_w16_host(GATE, UP, W16, R, Y, stream=None):
+    return _host_call("lin_matmul_residual_swiglu_a_w16_host", GATE, UP, W16, R, Y, True, stream)
+
+
+def lin_set_host_block_bytes(nbytes: int) -> None:
+    """Operand-plus-result bytes per block of the host-operand forms (0: default)."""
+    check("lin_set_host_block_bytes", lib().lin_set_host_block_bytes(int(nbytes)))
+
+
+HOST_FORM_FUNCS = {
+    "matmul": lin_matmul_host,
+    "matmul_residual": lin_matmul_residual_host,
+    "matmul_residual_swiglu_a": lin_matmul_residual_swiglu_a_host,
+    "matmul_w16": lin_matmul_w16_host,
+    "matmul_residual_w16": lin_matmul_residual_w16_host,
+    "matmul_residual_swiglu_a_w16": lin_matmul_residual_swiglu_a_w16_host,
+}
+
+
+def run_form_host(form: str, d: dict, Y, stream=None):
+    """run_form for the forward forms with host (CPU) tensors throughout."""
+    f = HOST_FORM_FUNCS[form]
+    w = d["W16"] if form.endswith("_w16") else d["W"]
+    if "swiglu" in form:
+        return f(d["GATE"], d["UP"], w, d["R"], Y, stream=stream)
+    if "residual" in form:
+        return f(d["X"], w, d["R"], Y, stream=stream)
+    return f(d["X"], w, Y, stream=stream)
 
 
 FORM_FUNCS = {
