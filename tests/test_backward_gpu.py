@@ -120,16 +120,19 @@ from tests.gpu_util import integer_inputs, require_gpu, to_device
 from transformer_linear_layer_tcgen05_gb300 import lin
 require_gpu()
 bad = 0
-for form in ("matmul_t_w16", "matmul_t_acc_w16"):
+for form in ("matmul_t_w16", "matmul_t_acc_w16", "matmul_t_swiglu_backward_w16"):
     for (M, N, K) in [(128, 64, 256), (300, 200, 2048), (129, 520, 1032), (1, 1032, 4),
                       (700, 1536, 1024), (4736, 1024, 2048)]:
         d = integer_inputs(form, M, N, K, seed=M + N + K)
-        Yd = torch.full((M, K), float("nan"), dtype=torch.float32, device="cuda")
-        lin.run_form(form, to_device(d), Yd)
+        two = "swiglu" in form        # (dGATE, dUP)
+        Yd = tuple(torch.full((M, K), float("nan"), dtype=torch.float32, device="cuda")
+                   for _ in range(2 if two else 1))
+        lin.run_form(form, to_device(d), Yd if two else Yd[0])
         torch.cuda.synchronize()
         st = lin.lin_get_device_status()
-        Y = Yd.cpu().numpy().astype(np.float64)
-        nd = int(np.sum(Y != oracle.reference(form, d)[0]))
+        ref = oracle.reference(form, d)[0]
+        refs = ref if two else (ref,)
+        nd = sum(int(np.sum(y.cpu().numpy().astype(np.float64) != r)) for y, r in zip(Yd, refs))
         if nd or st != lin.LIN_SUCCESS:
             print(f"{form} {M}x{N}x{K}: status {st}, {nd} mismatches", flush=True)
         bad += nd + (st != lin.LIN_SUCCESS)
