@@ -45,8 +45,10 @@
  *             cudaFreeAsync), owned by that graph. If no workspace can be
  *             had the launch runs unsplit (the same results up to the order
  *             in which the tail's K ranges are summed). The f32 forms split
- *             K in the same way when a problem has too few 128 x 128 tiles
- *             to fill the SMs (at most 64 KiB of workspace per SM).
+ *             K when a problem has too few 128 x 128 tiles to fill the SMs:
+ *             the (at most 8) CTAs of a tile form a cluster and add their
+ *             partial tiles through distributed shared memory, in K order;
+ *             no workspace, one kernel.
  *             lin_matmul_w16 and lin_matmul_residual_w16 also place a
  *             binary16 copy of X (M*K*2 bytes) in the workspace, written by
  *             a first kernel, when each row block of X feeds several

@@ -156,17 +156,20 @@ def test_bounded_wait_times_out_cleanly():
     assert torch.cuda.is_available()
 
 
-@pytest.mark.parametrize("form,shape", [("matmul", (512, 768, 768)),
-                                        ("matmul_residual_swiglu_a_w16", (300, 2048, 2048))])
-def test_split_inside_a_cuda_graph(form, shape):
-    # A split launch captured into a graph takes its workspace as a graph
-    # memory node; replays must equal a direct call bit for bit.
+# (form, shape, kernels, workspace): the per-tile f32 kernel splits K inside
+# a cluster (one kernel, no workspace); the clustered binary16 kernel splits
+# its last round (GEMM + split sum, a workspace)
+@pytest.mark.parametrize("form,shape,kernels,workspace",
+                         [("matmul", (512, 768, 768), 1, False),
+                          ("matmul_residual_swiglu_a_w16", (300, 2048, 2048), 2, True)])
+def test_split_inside_a_cuda_graph(form, shape, kernels, workspace):
+    # A split launch captured into a graph takes its workspace (if any) as a
+    # graph memory node; replays must equal a direct call bit for bit.
     torch = _torch()
     M, N, K = shape
     dd = to_device(wl.generate(form, M, N, K, seed=9))
     direct = run_device(form, dd, M, N)
-    kernels, _ = lin.lin_last_launch_info()
-    assert kernels == 2                     # the problem splits on a GB300
+    assert lin.lin_last_launch_info()[0] == kernels   # the problem splits on a GB300
     Y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
     g = torch.cuda.CUDAGraph()
     s = torch.cuda.Stream()
@@ -176,7 +179,7 @@ def test_split_inside_a_cuda_graph(form, shape):
             lin.run_form(form, dd, Y)
             captured = lin.lin_last_launch_info()
     torch.cuda.current_stream().wait_stream(s)
-    assert captured[0] == 2 and captured[1] > 0
+    assert captured[0] == kernels and (captured[1] > 0) == workspace
     for _ in range(2):
         Y.fill_(float("nan"))
         g.replay()

@@ -570,13 +570,26 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
     }
   } else {
     // One CTA per 128 x bn tile; when the tiles leave most SMs idle, split K
-    // into S ranges (grid.z) of at least 4 k-blocks each.
+    // into S ranges (grid.z) of at least 4 k-blocks each. Where A is X (or
+    // X^T, or dY) the S CTAs of a tile form a cluster and sum their partial
+    // tiles through distributed shared memory (S at most 8, and lowered at
+    // launch until every tile's cluster is resident at once); the SwiGLU
+    // forms, whose A is built by the transform warps, gain more from every
+    // SM than from one kernel, and keep the workspace and the split sum
+    // (measured on the 512-token shapes).
     const int tiles_n = (int)((N + bn - 1) / bn);
     const int tiles = tiles_n * (int)((M + lin::kBM - 1) / lin::kBM);
     const int nkb = (int)((K + (p.w16 ? 63 : 31)) / (p.w16 ? 64 : 32));
     int split = sm_count(dev) / tiles;
     if (split > nkb / 4) split = nkb / 4;
-    if (split >= 2) {
+    const bool cl = !(swiglu && !p.at);
+    if (cl && split > lin::kMaxClusterSplit) split = lin::kMaxClusterSplit;
+    if (split >= 2 && cl) {
+      args.split_r = 0;
+      args.split_rem = tiles;
+      args.split_s = split;
+      args.flags |= lin::KFLAG_CLUSTER_SPLIT;
+    } else if (split >= 2) {
       const size_t bytes = (size_t)tiles * split * lin::kBM * bn * sizeof(float);
       const int got = take_workspace(bytes);
       if (got < 0) return LIN_ERROR_UNSUPPORTED_SHAPE;
@@ -593,7 +606,7 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
       e = lin::launch_gemm_tf32(swiglu ? (p.at ? lin::A_TRANS_SWIGLU_F32 : lin::A_SWIGLU_F32)
                                        : (p.at ? lin::A_TRANS_F32 : lin::A_TMA_F32),
                                 resid, bn, p.bt, maps, args, stream);
-    if (e == cudaSuccess && args.split_s >= 2) {
+    if (e == cudaSuccess && args.split_s >= 2 && !(args.flags & lin::KFLAG_CLUSTER_SPLIT)) {
       e = lin::launch_split_reduce(args, resid, 1, bn, 0, tiles_n, stream);
       kernels = 2;
     }

@@ -123,6 +123,7 @@ struct GemmTraits {
       umma_idesc(kF16 ? 0u : 2u, /*a_mn_major=*/false, /*b_mn_major=*/!kXformB && !BT, BM, BN);
 
   static_assert(NS >= 2, "operand ring needs two stages");
+  static_assert(NS * OP_STAGE_BYTES >= BM * BN * 4, "a cluster split's partial tile in the ring");
   static_assert(NR <= 4 && NS <= 8, "barrier slots");
   static_assert(!kXform || NR * RAW_STAGE_BYTES >= EPI_BYTES, "epilogue aliasing");
   static_assert(OFF_ABORT + 4 <= BAR_REGION, "barrier region");
@@ -238,6 +239,73 @@ __device__ __forceinline__ void transpose_swiglu_tile(uint32_t a_stage, uint32_t
   }
 }
 
+// ---------------------------------------------------------------- cluster split K
+
+// Partial tile of a cluster split in shared memory (at the start of the
+// operand ring, idle once the accumulator is complete): [128 rows][BN f32],
+// the 16-byte column c of row r at ((c ^ (r & 7)) * 16) within the row, so
+// that the 32 lanes of a warp (32 rows) store one column without bank
+// conflicts and consecutive threads of the sum read consecutive columns.
+template <typename T>
+__device__ __forceinline__ uint32_t csplit_off(int r, int c4) {
+  return (uint32_t)(r * T::BN * 4 + ((c4 ^ (r & 7)) * 16));
+}
+
+// The sum of a cluster split: CTA `rank` of the S takes its share of the
+// tile's 128 x BN/4 float4s (row-major, so that the 128 threads touch
+// consecutive columns of a row) and adds the S partials in K order (rank 0
+// first, as the split sum kernel does), then the residual or the SwiGLU
+// backward, and writes Y (and Y2) with 16-byte global stores.
+template <typename T>
+__device__ __forceinline__ void cluster_split_sum(uint32_t part, int S, int rank, int tid,
+                                                  int m0, int n0, const KernelArgs& args) {
+  constexpr int C4 = T::BN / 4;
+  constexpr int TOTAL = T::BM * C4;
+  const int beg = rank * TOTAL / S, end = (rank + 1) * TOTAL / S;
+  const bool swb = (args.flags & KFLAG_SWIGLU_BWD) != 0;
+  for (int idx = beg + tid; idx < end; idx += 128) {
+    const int r = idx / C4, c4 = idx % C4;
+    const int row = m0 + r, col = n0 + 4 * c4;
+    if (row >= args.M || col >= args.N) continue;
+    const uint32_t off = part + csplit_off<T>(r, c4);
+    float4 v[kMaxClusterSplit];
+#pragma unroll
+    for (int p = 0; p < kMaxClusterSplit; ++p)
+      if (p < S) v[p] = ld_cluster_v4f(mapa_shared(off, (uint32_t)p));
+    float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int p = 0; p < kMaxClusterSplit; ++p) {
+      if (p < S) {
+        sum.x += v[p].x;
+        sum.y += v[p].y;
+        sum.z += v[p].z;
+        sum.w += v[p].w;
+      }
+    }
+    const size_t o = (size_t)row * (size_t)args.N + (size_t)col;
+    if (swb) {   // the SwiGLU backward of the summed dA
+      const float4 gt = *reinterpret_cast<const float4*>(args.G2 + o);
+      const float4 up = *reinterpret_cast<const float4*>(args.U2 + o);
+      float4 dg, du;
+      swiglu_backward(sum.x, gt.x, up.x, dg.x, du.x);
+      swiglu_backward(sum.y, gt.y, up.y, dg.y, du.y);
+      swiglu_backward(sum.z, gt.z, up.z, dg.z, du.z);
+      swiglu_backward(sum.w, gt.w, up.w, dg.w, du.w);
+      *reinterpret_cast<float4*>(args.Y + o) = dg;
+      *reinterpret_cast<float4*>(args.Y2 + o) = du;
+      continue;
+    }
+    if constexpr (T::kResid) {
+      const float4 rv = *reinterpret_cast<const float4*>(args.R + o);
+      sum.x += rv.x;
+      sum.y += rv.y;
+      sum.z += rv.z;
+      sum.w += rv.w;
+    }
+    *reinterpret_cast<float4*>(args.Y + o) = sum;
+  }
+}
+
 // ---------------------------------------------------------------- kernel
 
 template <int AMODE, bool RESID, int BN, bool BT>
@@ -269,6 +337,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // [kb0, kb0 + nkb) and writes an f32 partial tile to args.part; a second
   // kernel adds the partials in K order (+ R) into Y.
   const bool split = gridDim.z > 1;
+  // ... or, with KFLAG_CLUSTER_SPLIT, keeps it in shared memory for the
+  // cluster's sum (cluster dims (1, 1, gridDim.z): CTA rank = blockIdx.z).
+  const bool csplit = split && (args.flags & KFLAG_CLUSTER_SPLIT) != 0;
   const int kb0 = (int)blockIdx.z * nkb_all / (int)gridDim.z;
   const int nkb = ((int)blockIdx.z + 1) * nkb_all / (int)gridDim.z - kb0;
   const bool withhold = (args.flags & KFLAG_WITHHOLD_PRODUCER) != 0;
@@ -487,7 +558,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after_sync();
       if (q == 0 && lane == 0) pdl_launch_dependents();   // the split sum may be scheduled
       ok = ok && !withhold && (__shfl_sync(0xffffffffu, *abort_flag, 0) == 0);
-      if (ok) {
+      if (ok && csplit) {
+        const int r = q * kEpiRows + lane;
+        for (int c = 0; c < nc; ++c) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * kEpiCols), v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            st_shared_v4(sbase + T::OFF_OP + csplit_off<T>(r, c * 8 + j), v[4 * j + 0],
+                         v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        }
+      } else if (ok) {
         const size_t tile = (size_t)blockIdx.y * gridDim.x + blockIdx.x;
         float4* part = reinterpret_cast<float4*>(args.part) +
                        (tile * gridDim.z + blockIdx.z) * (BN / 4) * T::BM + q * kEpiRows + lane;
@@ -618,9 +700,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   }
 
-  // ---- teardown
+  // ---- teardown (a cluster split first sums the partials: every CTA's is
+  // complete after the first cluster barrier, and none may leave before the
+  // second, while peers still read its shared memory)
   tc_fence_before_sync();
-  __syncthreads();
+  if (csplit) {
+    cluster_sync_all();
+    if (warp >= 4 && !withhold)
+      cluster_split_sum<T>(sbase + T::OFF_OP, (int)gridDim.z, (int)blockIdx.z,
+                           (int)threadIdx.x - 128, m0, n0, args);
+    cluster_sync_all();
+  } else {
+    __syncthreads();
+  }
   if (warp == 2) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, T::TMEM_COLS);
@@ -646,18 +738,54 @@ cudaError_t launch_instance(const TensorMaps& m, const KernelArgs& args, cudaStr
   dim3 grid((unsigned)((args.N + BN - 1) / BN), (unsigned)((args.M + kBM - 1) / kBM),
             (unsigned)(args.split_s > 1 ? args.split_s : 1));
   if (args.flags & KFLAG_WITHHOLD_PRODUCER) grid = dim3(1, 1, 1);
+  const bool csplit = grid.z > 1 && (args.flags & KFLAG_CLUSTER_SPLIT) != 0;
+  if (csplit && grid.z > (unsigned)kMaxClusterSplit) return cudaErrorInvalidValue;
+  if (csplit && dev < 64) {
+    // The largest split up to the one asked for whose clusters are all
+    // resident at once (clusters of S CTAs of this size per GPC set the
+    // limit; the K ranges follow gridDim.z).
+    static std::atomic<int> caps[64][kMaxClusterSplit + 1];
+    const unsigned tiles = grid.x * grid.y;
+    while (grid.z > 2) {
+      int n = caps[dev][grid.z].load(std::memory_order_relaxed);
+      if (n == 0) {
+        cudaLaunchAttribute ca[1];
+        ca[0].id = cudaLaunchAttributeClusterDimension;
+        ca[0].val.clusterDim.x = 1;
+        ca[0].val.clusterDim.y = 1;
+        ca[0].val.clusterDim.z = grid.z;
+        cudaLaunchConfig_t q = {};
+        q.gridDim = dim3(1, 1, grid.z);
+        q.blockDim = dim3(kThreads, 1, 1);
+        q.dynamicSmemBytes = T::SMEM_BYTES;
+        q.attrs = ca;
+        q.numAttrs = 1;
+        e = cudaOccupancyMaxActiveClusters(&n, (void*)kern, &q);
+        if (e != cudaSuccess) return e;
+        n = n > 0 ? n : -1;
+        caps[dev][grid.z].store(n, std::memory_order_relaxed);
+      }
+      if (n >= (int)tiles) break;
+      --grid.z;
+    }
+  }
   // A programmatic dependent of the previous kernel on the stream (the
   // kernel waits for it in griddepcontrol.wait after its set-up).
-  cudaLaunchAttribute attr[1];
+  // With a cluster split, the CTAs of one tile form a cluster along z.
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 1;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = grid.z;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = T::SMEM_BYTES;
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = csplit ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, kern, m.a, m.u, m.w, m.r, m.y, m.g2, m.u2, m.y2, args);
 }
 

@@ -39,7 +39,15 @@ enum : uint32_t {
   // output row over this CTA's columns of a tile -- (max, sum of exp(y -
   // max)) -- into row_stats[row][n0 / BN] (cross-entropy of the lm_head).
   KFLAG_ROW_STATS = 1u << 3,
+  // Split K of the per-tile kernel within a cluster (gridDim.z CTAs of one
+  // tile, cluster dims (1, 1, split_s)): each CTA leaves its partial tile in
+  // its shared memory, and after a cluster barrier each sums a share of the
+  // tile over the cluster's partials in K order (+ R) and writes Y; no
+  // workspace and no second kernel.
+  KFLAG_CLUSTER_SPLIT = 1u << 4,
 };
+// Largest split of the per-tile kernel: the portable cluster size.
+constexpr int kMaxClusterSplit = 8;
 
 // Device status word values (mirror lin_status).
 enum : int { KSTATUS_OK = 0, KSTATUS_TIMEOUT = 7 };

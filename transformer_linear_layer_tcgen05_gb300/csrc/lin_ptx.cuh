@@ -308,6 +308,17 @@ __device__ __forceinline__ void cluster_sync_all() {
                    "memory");
 }
 
+// 16-byte load from the shared memory of a CTA of the cluster (address
+// from mapa).
+__device__ __forceinline__ float4 ld_cluster_v4f(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
 // Address of the same shared-memory offset in CTA `rank` of this cluster.
 __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   uint32_t r;
