@@ -95,10 +95,14 @@ def recorded_traffic(workload: str):
 def kernel_label(w: wl.Workload) -> str:
     """Name of the kernel the library dispatches for workload w (the
     binary16 forms run the clustered kernel: clusters of 4 from N >= 1024,
-    pairs from N >= 512, else single CTAs)."""
+    pairs from N >= 512, else single CTAs; single CTAs too where X is
+    rounded to binary16 by a pre-pass, from N >= 2048 for the forms that
+    read X)."""
     if w.form.endswith("_w16"):
         cols = w.K if wl.form_is_t(w.form) else w.N   # output columns
         cn = os.environ.get("LIN_F16_KERNEL") or ("4" if cols >= 1024 else "2" if cols >= 512 else "1")
+        if not os.environ.get("LIN_F16_KERNEL") and "swiglu_a" not in w.form and cols >= 2048:
+            return "lin_cvt_f16_kernel + lin_gemm_cluster_kernel (BN=256, single CTAs, A by TMA)"
         if cn == "tile":
             return "lin_gemm_kernel (per-tile, BN=128)"
         return f"lin_gemm_cluster_kernel (BN=256, cluster {cn} along N)"

@@ -199,7 +199,7 @@ bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_
 // transformed A operand, within what N can use. LIN_F16_KERNEL overrides it
 // for measurements: "tile" selects the per-tile kernel, "1", "2" or "4" a
 // cluster size.
-int f16_cluster_size(uint64_t N) {
+int f16_forced_kernel() {
   static const int forced = [] {
     const char* v = std::getenv("LIN_F16_KERNEL");
     if (!v) return -1;
@@ -207,6 +207,11 @@ int f16_cluster_size(uint64_t N) {
     const int c = std::atoi(v);
     return (c == 1 || c == 2 || c == 4) ? c : -1;
   }();
+  return forced;
+}
+
+int f16_cluster_size(uint64_t N) {
+  const int forced = f16_forced_kernel();
   if (forced >= 0) return forced;
   // Clusters of 4 leave 8 of 152 SMs idle but transform each A row half as
   // often as pairs; with the transform warps taking turns by k-block they
@@ -502,6 +507,12 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
     const int nkb = (int)((K + 63) / 64);
     // binary16 X from a pre-pass, in the workspace after the partial tiles
     bool tma_a = !swiglu && !fixed && K % 8 == 0 && f16_preconvert(num_ng);
+    // With A already binary16 in global memory a cluster only multicasts
+    // it, and single CTAs on every SM measured faster at every shape (the
+    // 16k-token dX 447 -> 417 us, the gate/up pair 868 -> 821 us, the
+    // 512-token dX 39.1 -> 35.6 us): clusters stay for the forms whose A is
+    // built on chip.
+    if (tma_a && f16_forced_kernel() < 0) cn = 1;
     auto capacity = [&]() {
       if (dual) return lin::cluster_capacity_dual(tma_a, cn, &ce);
       if (p.bt) return lin::cluster_capacity_bt(tma_a, cn, resid, &ce);
@@ -565,7 +576,7 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
     if (e == cudaSuccess && args.split_s >= 2) {
       const int clusters = args.split_r > 0 ? cap : args.split_rem * args.split_s;
       e = lin::launch_split_reduce(args, resid, cn, lin::kClusterBN, args.split_r * clusters,
-                                   num_ng, stream);
+                                   num_ng_o, stream);
       kernels += 1;
     }
   } else {
