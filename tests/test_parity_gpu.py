@@ -30,8 +30,10 @@ def _gpu():
 
 # (M, N, K): several tiles plus ragged tails; N % 8 == 0 so the w16 forms run too.
 # The last two split K across CTAs when tiles are few (per-tile kernel: 2 and
-# 8 K ranges on a 152-SM GB300), so their partial tiles are summed by the
-# split-sum kernel.
+# 8 K ranges on a 152-SM GB300): for the f32 forms that read X the CTAs of
+# a tile form a cluster and sum their partial tiles through distributed
+# shared memory (ragged rows and columns included); the SwiGLU forms' partial
+# tiles go to the workspace and the split-sum kernel.
 EXACT_SHAPES = [(256, 256, 128), (129, 136, 20), (1, 8, 4), (300, 264, 68), (128, 392, 256),
                 (257, 136, 1028)]
 
