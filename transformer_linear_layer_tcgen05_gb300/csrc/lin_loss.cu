@@ -99,19 +99,32 @@ __global__ void __launch_bounds__(kLossThreads)
   const float inv_V = 1.0f / (float)V;
   const float zl = 2.0f * beta * lse;
   const float smooth = alpha * inv_V;
-  // phase 4: dLogits in place (and the sum of the logits for smoothing)
+  // phase 4: dLogits in place (and the sum of the logits for smoothing);
+  // kUnroll of the thread's float4s are loaded before any is rewritten, so
+  // that as many loads are in flight
+  constexpr int kUnroll = 4;
   float sum_l = 0.0f;
-  for (int v = tid; v < V4; v += kLossThreads) {
-    float4 l = row4[v];
-    sum_l += (l.x + l.y) + (l.z + l.w);
-    float* e = &l.x;
+  for (int v0 = tid; v0 < V4; v0 += kUnroll * kLossThreads) {
+    float4 l[kUnroll];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float p = __expf(e[i] - row_max) * inv_denom;
-      const float tgt_dist = (4 * v + i == tgt ? 1.0f - alpha : 0.0f) + smooth;
-      e[i] = ((p - tgt_dist) + zl * p) * inv_norm;
+    for (int u = 0; u < kUnroll; ++u) {
+      const int v = v0 + u * kLossThreads;
+      if (v < V4) l[u] = row4[v];
     }
-    row4[v] = l;
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int v = v0 + u * kLossThreads;
+      if (v >= V4) break;
+      sum_l += (l[u].x + l[u].y) + (l[u].z + l[u].w);
+      float* e = &l[u].x;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float p = __expf(e[i] - row_max) * inv_denom;
+        const float tgt_dist = (4 * v + i == tgt ? 1.0f - alpha : 0.0f) + smooth;
+        e[i] = ((p - tgt_dist) + zl * p) * inv_norm;
+      }
+      row4[v] = l[u];
+    }
   }
   if (alpha > 0.0f) sum_l = block_reduce<false>(sum_l, sh);
   if (tid == 0) {
