@@ -62,17 +62,20 @@ def load_peaks():
 
 # host-side files of the library (validation, dispatch, workspace): not part
 # of the kernels whose counters profiles/dram_traffic.txt records
-HOST_SOURCES = ("lin_api.cu", "lin_noalloc.cu", "lin_host.cu")
+# The sources the dominant kernel (the clustered SwiGLU GEMM) is compiled
+# from: its translation unit and every header it includes.
+DOMINANT_KERNEL_SOURCES = ("lin_kernels_cluster_swiglu.cu", "lin_gemm_cluster.cuh",
+                           "lin_common.cuh", "lin_ptx.cuh", "lin_internal.h")
 
 
 def kernel_source_hash() -> str:
-    """Hash of the device-code sources (every csrc file but the host-side ones)."""
+    """Hash of the dominant kernel's sources (a recorded DRAM figure is
+    valid only for the code it was captured on)."""
     csrc = os.path.join(ROOT, "transformer_linear_layer_tcgen05_gb300", "csrc")
     h = hashlib.sha256()
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")) and name not in HOST_SOURCES:
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+    for name in sorted(DOMINANT_KERNEL_SOURCES):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
