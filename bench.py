@@ -239,6 +239,25 @@ def cpu_baseline(w: wl.Workload, inputs: dict, budget_s: float = 12.0, chunk: in
 
 # ----------------------------------------------------------------- reference arm
 
+def max_over_ranks(value: float, dist, device) -> float:
+    """The largest of every rank's value (with times: the slowest rank's),
+    by an all-reduce on `device` (cuda under NCCL, cpu under gloo); the value
+    itself without a process group."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replicas_value(world: int, flops_per_rank: float, ms_max: float) -> float:
+    """Whole-job TFLOP/s of `world` replicas of one workload: every rank's
+    FLOPs over the slowest rank's time (the path shards over tokens with no
+    exchange, so each rank runs the whole workload: weak scaling)."""
+    return world * flops_per_rank / (ms_max * 1e-3) / 1e12
+
+
 def run_reference(args, rank: int):
     if rank != 0:
         return
@@ -526,11 +545,8 @@ def run_ours(args, rank: int, world: int):
     if status != lin.LIN_SUCCESS:
         raise RuntimeError(f"device status {lin.STATUS.get(status, status)} after timed region")
 
-    ms_t = torch.tensor([ms], dtype=torch.float64, device="cuda")
-    if dist is not None:
-        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
-    ms_max = float(ms_t.item())
-    value = world * w.flops / (ms_max * 1e-3) / 1e12
+    ms_max = max_over_ranks(ms, dist, "cuda")
+    value = replicas_value(world, w.flops, ms_max)
     kernel_tflops = w.flops / (ms * 1e-3) / 1e12
 
     # ---- end to end through the public API: pinned host buffers, H2D of the
@@ -570,10 +586,8 @@ def run_ours(args, rank: int, world: int):
     f1.record(stream)
     f1.synchronize()
     e2e_ms = f0.elapsed_time(f1) / max(e2e_steps, 1)
-    e2e_t = torch.tensor([e2e_ms], dtype=torch.float64, device="cuda")
-    if dist is not None:
-        dist.all_reduce(e2e_t, op=dist.ReduceOp.MAX)
-    e2e_value = world * w.flops / (float(e2e_t.item()) * 1e-3) / 1e12 if e2e_steps else None
+    e2e_max = max_over_ranks(e2e_ms, dist, "cuda")
+    e2e_value = replicas_value(world, w.flops, e2e_max) if e2e_steps else None
     del pinned, y_host
 
     # ---- roofline of the step's GEMM; achieved = the step's FLOPs over the
