@@ -329,7 +329,8 @@ lin_status lin_gate_up_w16(const float *X, const uint16_t *WG16, const uint16_t 
  *             until `stream` gets there (cudaStreamSynchronize).
  * Errors      Validation as for the device forms, before anything is
  *             enqueued (Y overlapping an input -> LIN_ERROR_ALIASING; the
- *             16-byte alignment rule does not apply to host operands). A
+ *             16-byte alignment rule does not apply to host operands);
+ *             `stream` under graph capture -> LIN_ERROR_INVALID_VALUE. A
  *             CUDA failure part-way returns LIN_ERROR_CUDA after the blocks
  *             already enqueued; Y is then partly written.
  * lin_last_launch_info reports the kernels of all blocks and the staging

@@ -90,3 +90,22 @@ def test_device_memory_is_rejected():
     st = lin.lib().lin_matmul_host(X.data_ptr(), W.data_ptr(), Y.data_ptr(), M, N, K,
                                    torch.cuda.current_stream().cuda_stream)
     assert st == lin.LIN_ERROR_INVALID_VALUE
+
+
+def test_rejected_under_stream_capture():
+    import torch
+    M, N, K = 128, 64, 64
+    X = torch.zeros((M, K)).pin_memory()
+    W = torch.zeros((K, N)).pin_memory()
+    Y = torch.zeros((M, N)).pin_memory()
+    Z = torch.zeros(16, device="cuda")
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            Z.add_(1.0)     # the graph is not empty
+            st = lin.lib().lin_matmul_host(X.data_ptr(), W.data_ptr(), Y.data_ptr(), M, N, K,
+                                           s.cuda_stream)
+    torch.cuda.current_stream().wait_stream(s)
+    assert st == lin.LIN_ERROR_INVALID_VALUE

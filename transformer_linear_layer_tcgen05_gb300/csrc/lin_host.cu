@@ -133,9 +133,14 @@ lin_status run_host(const HostProblem& h, cudaStream_t stream) {
   for (const void* p : host_ops)
     if (p && !is_host(p)) return LIN_ERROR_INVALID_VALUE;
 
-  // 3. device and copy streams
+  // 3. device and copy streams (not under stream capture: the call's own
+  // copy streams and events would become part of the caller's graph)
   int dev = 0;
   if ((st = lin_detail::checked_device(&dev)) != LIN_SUCCESS) return st;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t ce = cudaStreamIsCapturing(stream, &cs);
+  if (ce != cudaSuccess) return lin_detail::record_cuda_error(ce);
+  if (cs != cudaStreamCaptureStatusNone) return LIN_ERROR_INVALID_VALUE;
   cudaStream_t s_in = nullptr, s_out = nullptr;
   cudaError_t e = copy_streams(dev, &s_in, &s_out);
   if (e != cudaSuccess) return lin_detail::record_cuda_error(e);
