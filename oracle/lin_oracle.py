@@ -60,6 +60,12 @@ alpha mean(l) + beta LSE^2, and dLogits_v = ((p_v - target_dist_v) +
 and dLogits 0. ``sum_losses`` adds the per-row losses. ``lm_head_cross_entropy``
 applies both to the logits X @ W16 of the lm_head projection.
 
+Gate and up projections (``gate_up_w16``): the pages name GATE and UP as the
+outputs of the FFN's gate and up projections (03_linear_forward, the
+SwiGLU form's bind group) without describing their producer. Reading: the
+two plain products GATE = X @ W_gate and UP = X @ W_up of one X, binary16
+weights, evaluated here as two ``matmul_w16`` calls.
+
 Everything is evaluated in float64. Inputs are widened exactly: float32 to
 float64 by numpy, binary16 bit patterns by ``f16_bits_to_f64`` below (an
 IEEE 754 decoder written from the format's definition). The contraction uses
