@@ -366,7 +366,9 @@ const char *lin_status_string(lin_status status);
 int lin_last_cuda_error(void);
 
 /* What the last compute call made on the calling thread enqueued: the number
- * of kernels it launched (1, or 2 with a split tail; 0 if it enqueued none or
+ * of kernels it launched (the GEMM, plus the binary16 pre-pass of X and the
+ * split-tail sum where those run, plus the loss kernels of the lm_head form;
+ * all blocks' kernels for a host-operand form; 0 if it enqueued none or
  * failed) and the workspace bytes it took from the library's pool. Either
  * pointer may be NULL. */
 void lin_last_launch_info(int* kernels, uint64_t* workspace_bytes);
