@@ -645,6 +645,14 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
             tma_load_2d(bg, &tm_g2, n0 + c * kEpiCols, row0, ebar(0));
             tma_load_2d(bu, &tm_u2, n0 + c * kEpiCols, row0, ebar(0));
             ++sw_issued;
+            // the next chunk's GATE and UP on their way into L2, so that
+            // its loads, issued after this chunk's stores, hit there
+            // (16k-token shape: 640 -> 617 us; two chunks ahead 622, three
+            // 655)
+            if (c + 1 < nc) {
+              tma_prefetch_l2_2d(&tm_g2, n0 + (c + 1) * kEpiCols, row0);
+              tma_prefetch_l2_2d(&tm_u2, n0 + (c + 1) * kEpiCols, row0);
+            }
           }
           __syncwarp();
           uint32_t v[32];
