@@ -611,6 +611,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(bg, &tm_g2, n0 + c * kEpiCols, row0, ebar0);
           tma_load_2d(bu, &tm_u2, n0 + c * kEpiCols, row0, ebar0);
           sw_issued = c + 1;
+          if (c + 1 < nc) {   // the next chunk's GATE and UP into L2
+            tma_prefetch_l2_2d(&tm_g2, n0 + (c + 1) * kEpiCols, row0);
+            tma_prefetch_l2_2d(&tm_u2, n0 + (c + 1) * kEpiCols, row0);
+          }
         }
         __syncwarp();
         uint32_t v[32];
