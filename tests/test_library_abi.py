@@ -180,3 +180,22 @@ def test_lm_head_cross_entropy_validates_before_touching_cuda(L):
     # dLogits over X
     assert f(fake, fake + (1 << 30), fake + (2 << 30), fake, fake + (3 << 30), fake + (4 << 30),
              8, 16, 8, a, b, c, None) == lin.LIN_ERROR_ALIASING
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path, monkeypatch):
+    # no fallback: with liblin.so missing every call raises before any work,
+    # and the package never imports the oracle
+    import subprocess
+    import sys
+    monkeypatch.setattr(lin, "LIB_PATH", str(tmp_path / "liblin.so"))
+    monkeypatch.setattr(lin, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        lin.lib()
+    with pytest.raises(RuntimeError, match="not built"):
+        lin.lin_last_launch_info()
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = ("import sys; import transformer_linear_layer_tcgen05_gb300.lin, "
+            "transformer_linear_layer_tcgen05_gb300.build, "
+            "transformer_linear_layer_tcgen05_gb300.workloads; "
+            "sys.exit(1 if any(m == 'oracle' or m.startswith('oracle.') for m in sys.modules) else 0)")
+    assert subprocess.run([sys.executable, "-c", code], cwd=root).returncode == 0
