@@ -420,14 +420,15 @@ def time_lm_head_loss(iters: int, flush_buf, peaks: dict) -> dict:
             "warm_frac": w.flops / wm / 1e6 / r}
 
 
-def time_gate_up(iters: int, flush_buf, peaks: dict) -> dict:
+def time_gate_up(iters: int, flush_buf, peaks: dict, M: int = 16384) -> dict:
     """The producer of the 16k SwiGLU workload's GATE and UP through
-    lin_gate_up_w16: X [16384, 2048] f32, W_gate and W_up [2048, 8192]
-    binary16 (2 x 550 GFLOP), timed cold (inputs above L2 anyway) and warm."""
+    lin_gate_up_w16: X [M, 2048] f32, W_gate and W_up [2048, 8192] binary16
+    (2 x 550 GFLOP at M = 16384), timed cold (inputs above L2 anyway) and
+    warm. A smaller M serves profiling captures."""
     import numpy as np
     import torch
     from transformer_linear_layer_tcgen05_gb300 import lin
-    M, N, K = 16384, 8192, 2048
+    N, K = 8192, 2048
     g = wl.generate("matmul_w16", M, N, K, seed=1020)
     wu = wl.generate("matmul_w16", 1, N, K, seed=1021)["W16"]
     X = torch.from_numpy(g["X"]).cuda()
@@ -631,8 +632,10 @@ def run_ours(args, rank: int, world: int):
         "clocks": sampler.summary(h0, h1),
     }
 
+    tables = set(args.tables.split(","))
     if rank == 0 and not args.no_small:
         flush = torch.empty(int(2 * L2_BYTES // 4), dtype=torch.float32, device="cuda")
+    if rank == 0 and not args.no_small and "workloads" in tables:
         table = []
         for name in SMALL:
             sw = wl.WORKLOADS_BY_NAME[name]
@@ -645,7 +648,8 @@ def run_ours(args, rank: int, world: int):
                           "warm_us": warm_us, "warm_tflops": sw.flops / warm_us / 1e6,
                           "warm_frac": sw.flops / warm_us / 1e6 / r})
         line["workloads"] = table
-        # the backward input gradients of the same layers, timed the same way
+    if rank == 0 and not args.no_small and "backward" in tables:
+        # the backward products of the same layers, timed the same way
         table = []
         for sw in wl.BACKWARD_WORKLOADS:
             cold_us, warm_us = time_small(sw, args.small_iters, flush)
@@ -657,8 +661,11 @@ def run_ours(args, rank: int, world: int):
                           "warm_us": warm_us, "warm_tflops": sw.flops / warm_us / 1e6,
                           "warm_frac": sw.flops / warm_us / 1e6 / r})
         line["backward"] = table
+    if rank == 0 and not args.no_small and "loss" in tables:
         line["loss"] = [time_lm_head_loss(args.small_iters, flush, peaks)]
-        line["gate_up"] = [time_gate_up(args.small_iters, flush, peaks)]
+    if rank == 0 and not args.no_small and "gate_up" in tables:
+        line["gate_up"] = [time_gate_up(args.small_iters, flush, peaks, M=args.gate_up_m)]
+    if rank == 0 and not args.no_small:
         del flush
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, host, budget_s=args.cpu_seconds)
@@ -681,6 +688,10 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-rows", type=int, default=16)
     ap.add_argument("--no-small", action="store_true")
+    ap.add_argument("--tables", default="workloads,backward,loss,gate_up",
+                    help="comma-separated tables to run besides the headline")
+    ap.add_argument("--gate-up-m", type=int, default=16384,
+                    help="M of the gate/up table (a smaller M for profiling captures)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--m", type=int, default=None,
