@@ -575,7 +575,7 @@ def run_ours(args, rank: int, world: int):
         for yh, o in zip(y_host, outs):
             yh.copy_(o, non_blocking=True)
 
-    for _ in range(3 if e2e_steps else 0):   # warm-up calls (the pinned buffers' first copies)
+    for _ in range(args.e2e_warmup if e2e_steps else 0):   # untimed calls first
         e2e_step()
     torch.cuda.synchronize()
     barrier()
@@ -684,6 +684,8 @@ def main():
     ap.add_argument("--workload", default=HEADLINE,
                     choices=[w.name for w in wl.WORKLOADS + wl.BACKWARD_WORKLOADS])
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--e2e-warmup", type=int, default=30,
+                    help="untimed end-to-end calls before the timed ones")
     ap.add_argument("--small-iters", type=int, default=50)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-rows", type=int, default=16)
