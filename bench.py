@@ -60,8 +60,6 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-# host-side files of the library (validation, dispatch, workspace): not part
-# of the kernels whose counters profiles/dram_traffic.txt records
 # The sources the dominant kernel (the clustered SwiGLU GEMM) is compiled
 # from: its translation unit and every header it includes.
 DOMINANT_KERNEL_SOURCES = ("lin_kernels_cluster_swiglu.cu", "lin_gemm_cluster.cuh",
