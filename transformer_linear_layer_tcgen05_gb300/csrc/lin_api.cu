@@ -989,6 +989,6 @@ lin_status lin_selftest_wait_timeout(int64_t timeout_us, lin_stream_t stream) {
   return read_and_clear_status(s);
 }
 
-int lin_version(void) { return 100; }
+int lin_version(void) { return 200; }   // 0.2.0: backward, loss, gate/up and host-operand entry points
 
 }  // extern "C"
