@@ -199,3 +199,21 @@ def test_binding_fails_loudly_without_the_library(tmp_path, monkeypatch):
             "transformer_linear_layer_tcgen05_gb300.workloads; "
             "sys.exit(1 if any(m == 'oracle' or m.startswith('oracle.') for m in sys.modules) else 0)")
     assert subprocess.run([sys.executable, "-c", code], cwd=root).returncode == 0
+
+
+def test_binding_checks_tensors_before_calling(L):
+    # the tensor layer rejects wrong devices, dtypes and shapes itself (no
+    # library call is made)
+    import torch
+    X = torch.zeros((8, 8))
+    W = torch.zeros((8, 8))
+    with pytest.raises(TypeError):
+        lin.lin_matmul(X, W, X.clone())                  # CPU tensors for a device form
+    with pytest.raises(ValueError):
+        lin.lin_matmul_host(X, torch.zeros((4, 8)), torch.zeros((8, 8)))   # K mismatch
+    with pytest.raises(TypeError):
+        lin.lin_matmul_w16_host(X, W, torch.zeros((8, 8)))                 # f32 as W16
+    with pytest.raises(ValueError):
+        lin.lin_matmul_residual_host(X, W, torch.zeros((8, 4)), torch.zeros((8, 8)))  # R shape
+    with pytest.raises(ValueError):
+        lin.lin_matmul_host(X.t(), W, torch.zeros((8, 8)))                 # not contiguous
