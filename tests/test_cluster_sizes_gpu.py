@@ -2,7 +2,10 @@
 
 The library picks the cluster size from N; LIN_F16_KERNEL overrides it for a
 process ("1", "2", "4", or "tile" for the per-tile kernel), so each size runs
-in a child process of its own. The shapes cover ragged M, N and K, a single
+in a child process of its own. The override applies where the transform
+warps build A on chip; the pre-converted binary16 A (a TMA-loaded operand)
+always runs as single CTAs, so under every variant those shapes check the
+single-CTA path beside the forced cluster size. The shapes cover ragged M, N and K, a single
 row, and launches whose last round is split along K after whole rounds or
 alone. A child also fails on a device status other than success (a bounded
 wait that ran out), even when the output is right.

@@ -507,12 +507,13 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
     const int nkb = (int)((K + 63) / 64);
     // binary16 X from a pre-pass, in the workspace after the partial tiles
     bool tma_a = !swiglu && !fixed && K % 8 == 0 && f16_preconvert(num_ng);
-    // With A already binary16 in global memory a cluster only multicasts
-    // it, and single CTAs on every SM measured faster at every shape (the
+    // With A already binary16 in global memory a CTA copies its own A tiles
+    // by TMA and has nothing to share: single CTAs on every SM (152 rather
+    // than 144 in clusters of four) measured faster at every shape (the
     // 16k-token dX 447 -> 417 us, the gate/up pair 868 -> 821 us, the
-    // 512-token dX 39.1 -> 35.6 us): clusters stay for the forms whose A is
-    // built on chip.
-    if (tma_a && f16_forced_kernel() < 0) cn = 1;
+    // 512-token dX 39.1 -> 35.6 us). Clusters stay for the forms whose A is
+    // built on chip; a forced cluster size applies to those only.
+    if (tma_a) cn = 1;
     auto capacity = [&]() {
       if (dual) return lin::cluster_capacity_dual(tma_a, cn, &ce);
       if (p.bt) return lin::cluster_capacity_bt(tma_a, cn, resid, &ce);
@@ -556,7 +557,7 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
     if (tma_a) {
       uint16_t* xh = reinterpret_cast<uint16_t*>(reinterpret_cast<char*>(args.part) + xh_off);
       if (!encode_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT16, xh, K, M, K * 2, 64,
-                     (uint32_t)(lin::kBM / cn)))
+                     (uint32_t)lin::kBM))
         e = cudaErrorInvalidValue;
       else
         e = lin::launch_cvt_f16(p.X, xh, M * K, sm_count(dev), stream);

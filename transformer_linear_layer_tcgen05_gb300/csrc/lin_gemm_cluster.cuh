@@ -60,8 +60,9 @@ struct ClusterTraits {
   static_assert(AMODE == A_CVT_F16 || AMODE == A_SWIGLU_F16 || AMODE == A_TMA_F16,
                 "binary16 forms only");
   static constexpr bool kSwiglu = (AMODE == A_SWIGLU_F16);
-  // A already binary16 in global memory: each CTA copies its ROWS rows of
-  // every A k-block by TMA, multicast to the whole cluster; no transform warps.
+  // A already binary16 in global memory: the CTA copies every A k-block of
+  // its tile by TMA; no transform warps. Such a CTA has nothing to share with
+  // peers, so it runs alone (cluster size 1).
   static constexpr bool kTmaA = (AMODE == A_TMA_F16);
   static constexpr int BM = kBM;
   static constexpr int BN = BN_;
@@ -156,6 +157,7 @@ struct ClusterTraits {
   static constexpr int kThreadsC = (8 + XF_WARPS) * 32;
 
   static_assert(CN == 1 || CN == 2 || CN == 4 || CN == 8, "cluster size");
+  static_assert(!kTmaA || CN == 1, "a binary16 A from global memory is loaded by each CTA alone");
   static_assert(kTmaA || XF_WARPS == 4 || XF_WARPS == 8 || XF_WARPS == 12, "transform warps");
   static_assert(XF_WARPS % XF_GROUPS == 0 && ROWS % XF_PER_GROUP == 0 &&
                     RW % ROWS_PER_LOAD == 0,
@@ -363,8 +365,7 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
 
   if (warp == 0) {
     // ---------------- W producer (local TMA into the B half of each stage);
-    // with a binary16 A in global memory also this CTA's rows of A, to
-    // every CTA of the cluster
+    // with a binary16 A in global memory also the tile's rows of A
     int g = 0;   // k-blocks issued, across tiles
     bool ok = true;
     for (int i = 0; i < n_items && ok; ++i) {
@@ -383,7 +384,7 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
         }
         if (lane == 0) {
           const uint32_t full = bar(T::BAR_FULL + s);
-          // the whole A stage lands here too: one slice from each CTA
+          // with a binary16 A in global memory the A stage lands here too
           mbar_arrive_expect_tx(full, T::B_BYTES + (T::kTmaA ? T::A_BYTES : 0u));
           if constexpr (T::kBT) {
             tma_load_2d(b_stage(s), &tm_w, kb * T::BK, n0, full);   // W as [N][K]
@@ -400,27 +401,14 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
               tma_load_2d(b_stage(s) + j * T::B_ATOM_BYTES, &tm_w, n0 + j * T::W_ATOM, kb * T::BK,
                           full);
           }
-          if constexpr (T::kTmaA) {
-            const uint32_t dst = a_stage(s) + crank * (uint32_t)(T::ROWS * 128);
-            const int row = tile_m0(t) + (int)crank * T::ROWS;
-            if constexpr (CN > 1)
-              tma_load_2d_multicast(dst, &tm_a, kb * T::BK, row, full, T::CLUSTER_MASK);
-            else
-              tma_load_2d(dst, &tm_a, kb * T::BK, row, full);
-          }
+          if constexpr (T::kTmaA) tma_load_2d(a_stage(s), &tm_a, kb * T::BK, tile_m0(t), full);
         }
         __syncwarp();
       }
     }
-    if (lane == 0) {
+    if (lane == 0)
       for (int x = (g > T::NS ? g - T::NS : 0); x < g; ++x)
         wait_phase(bar(T::BAR_FULL + x % T::NS), (x / T::NS) & 1, ctl, false);
-      // The peers' commits for the final use of each stage land on our
-      // barriers (without transform warps, nobody else waits for them).
-      if constexpr (T::kTmaA && CN > 1)
-        for (int x = (g > T::NS ? g - T::NS : 0); x < g; ++x)
-          wait_phase_cluster(bar(T::BAR_EMPTY + x % T::NS), (x / T::NS) & 1, ctl, false);
-    }
     __syncwarp();
   } else if (warp == 1) {
     // ---------------- UMMA issuer

@@ -158,8 +158,8 @@ cudaError_t launch_gemm_cluster_cvt(int cn, bool resid, const TensorMaps& maps,
 int cluster_capacity_swiglu(int cn, cudaError_t* err);
 int cluster_capacity_cvt(int cn, bool resid, cudaError_t* err);
 // matmul_w16 / matmul_residual_w16 with A = binary16 X already in global
-// memory (tensor map `a`, boxes of 64 x 128/cn): each CTA copies its rows of
-// every A k-block by TMA multicast to its cluster.
+// memory (tensor map `a`, boxes of 64 x 128): each CTA copies every A
+// k-block of its tile by TMA. Single CTAs only (cn must be 1).
 cudaError_t launch_gemm_cluster_tma(int cn, bool resid, const TensorMaps& maps,
                                     const KernelArgs& args, cudaStream_t stream);
 int cluster_capacity_tma(int cn, bool resid, cudaError_t* err);

@@ -2,7 +2,7 @@
 // GEMM for the transposed product dY · W^T with binary16 W
 // (lin_matmul_t_w16 and its accumulating form): W is read as [N][K], a
 // K-major B operand; A = dY is rounded to binary16 by the transform warps or
-// by the pre-pass and then copied by TMA.
+// by the pre-pass and then copied by TMA (single CTAs).
 #include "lin_gemm_cluster.cuh"
 
 namespace lin {
@@ -10,30 +10,41 @@ namespace lin {
 template <int AMODE, bool RESID, int CN>
 using BtLaunch = ClusterLaunch<AMODE, RESID, 256, CN, /*BT=*/true>;
 
+// The rounded-by-the-transform form in clusters of 1, 2 or 4 CTAs; the
+// pre-converted form (TMA-loaded A) in single CTAs only.
 template <int AMODE>
 cudaError_t bt_launch(int cn, bool resid, const TensorMaps& m, const KernelArgs& a,
                       cudaStream_t s) {
-  switch (cn * 2 + (resid ? 1 : 0)) {
-    case 2: return BtLaunch<AMODE, false, 1>::launch(m, a, s);
-    case 3: return BtLaunch<AMODE, true, 1>::launch(m, a, s);
-    case 4: return BtLaunch<AMODE, false, 2>::launch(m, a, s);
-    case 5: return BtLaunch<AMODE, true, 2>::launch(m, a, s);
-    case 8: return BtLaunch<AMODE, false, 4>::launch(m, a, s);
-    case 9: return BtLaunch<AMODE, true, 4>::launch(m, a, s);
-    default: return cudaErrorInvalidValue;
+  if (cn == 1) return resid ? BtLaunch<AMODE, true, 1>::launch(m, a, s)
+                            : BtLaunch<AMODE, false, 1>::launch(m, a, s);
+  if constexpr (AMODE == A_TMA_F16) {
+    return cudaErrorInvalidValue;
+  } else {
+    switch (cn * 2 + (resid ? 1 : 0)) {
+      case 4: return BtLaunch<AMODE, false, 2>::launch(m, a, s);
+      case 5: return BtLaunch<AMODE, true, 2>::launch(m, a, s);
+      case 8: return BtLaunch<AMODE, false, 4>::launch(m, a, s);
+      case 9: return BtLaunch<AMODE, true, 4>::launch(m, a, s);
+      default: return cudaErrorInvalidValue;
+    }
   }
 }
 
 template <int AMODE>
 int bt_capacity(int cn, bool resid, cudaError_t* err) {
-  switch (cn * 2 + (resid ? 1 : 0)) {
-    case 2: return BtLaunch<AMODE, false, 1>::capacity(err);
-    case 3: return BtLaunch<AMODE, true, 1>::capacity(err);
-    case 4: return BtLaunch<AMODE, false, 2>::capacity(err);
-    case 5: return BtLaunch<AMODE, true, 2>::capacity(err);
-    case 8: return BtLaunch<AMODE, false, 4>::capacity(err);
-    case 9: return BtLaunch<AMODE, true, 4>::capacity(err);
-    default: *err = cudaErrorInvalidValue; return 0;
+  if (cn == 1) return resid ? BtLaunch<AMODE, true, 1>::capacity(err)
+                            : BtLaunch<AMODE, false, 1>::capacity(err);
+  if constexpr (AMODE == A_TMA_F16) {
+    *err = cudaErrorInvalidValue;
+    return 0;
+  } else {
+    switch (cn * 2 + (resid ? 1 : 0)) {
+      case 4: return BtLaunch<AMODE, false, 2>::capacity(err);
+      case 5: return BtLaunch<AMODE, true, 2>::capacity(err);
+      case 8: return BtLaunch<AMODE, false, 4>::capacity(err);
+      case 9: return BtLaunch<AMODE, true, 4>::capacity(err);
+      default: *err = cudaErrorInvalidValue; return 0;
+    }
   }
 }
 

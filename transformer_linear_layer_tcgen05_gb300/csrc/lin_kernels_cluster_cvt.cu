@@ -1,8 +1,8 @@
 // lin_kernels_cluster_cvt.cu -- instantiations of the clustered persistent
-// GEMM for matmul_w16 and matmul_residual_w16 (cluster sizes 1, 2, 4; A
-// rounded to binary16 by the transform warps, or by a pre-pass and then
-// copied by TMA), the pre-pass, and the split-tail sum shared by every
-// clustered form.
+// GEMM for matmul_w16 and matmul_residual_w16 (A rounded to binary16 by
+// the transform warps in clusters of 1, 2 or 4 CTAs, or by a pre-pass and
+// then copied by TMA into single CTAs), the pre-pass, and the split-tail sum
+// shared by every clustered form.
 #include "lin_gemm_cluster.cuh"
 
 namespace lin {
@@ -15,37 +15,17 @@ using TmaLaunch = ClusterLaunch<A_TMA_F16, RESID, 256, CN>;
 
 cudaError_t launch_gemm_cluster_tma(int cn, bool resid, const TensorMaps& maps,
                                     const KernelArgs& args, cudaStream_t stream) {
-  if (resid) {
-    switch (cn) {
-      case 1: return TmaLaunch<true, 1>::launch(maps, args, stream);
-      case 2: return TmaLaunch<true, 2>::launch(maps, args, stream);
-      case 4: return TmaLaunch<true, 4>::launch(maps, args, stream);
-      default: return cudaErrorInvalidValue;
-    }
-  }
-  switch (cn) {
-    case 1: return TmaLaunch<false, 1>::launch(maps, args, stream);
-    case 2: return TmaLaunch<false, 2>::launch(maps, args, stream);
-    case 4: return TmaLaunch<false, 4>::launch(maps, args, stream);
-    default: return cudaErrorInvalidValue;
-  }
+  if (cn != 1) return cudaErrorInvalidValue;
+  return resid ? TmaLaunch<true, 1>::launch(maps, args, stream)
+               : TmaLaunch<false, 1>::launch(maps, args, stream);
 }
 
 int cluster_capacity_tma(int cn, bool resid, cudaError_t* err) {
-  if (resid) {
-    switch (cn) {
-      case 1: return TmaLaunch<true, 1>::capacity(err);
-      case 2: return TmaLaunch<true, 2>::capacity(err);
-      case 4: return TmaLaunch<true, 4>::capacity(err);
-      default: *err = cudaErrorInvalidValue; return 0;
-    }
+  if (cn != 1) {
+    *err = cudaErrorInvalidValue;
+    return 0;
   }
-  switch (cn) {
-    case 1: return TmaLaunch<false, 1>::capacity(err);
-    case 2: return TmaLaunch<false, 2>::capacity(err);
-    case 4: return TmaLaunch<false, 4>::capacity(err);
-    default: *err = cudaErrorInvalidValue; return 0;
-  }
+  return resid ? TmaLaunch<true, 1>::capacity(err) : TmaLaunch<false, 1>::capacity(err);
 }
 
 // X -> binary16, four elements per thread and step (one 16-byte load, one

@@ -9,23 +9,34 @@ namespace lin {
 template <int AMODE, int CN>
 using DualLaunch = ClusterLaunch<AMODE, false, 256, CN, /*BT=*/false, /*DUAL=*/true>;
 
+// The rounded-by-the-transform form in clusters of 1, 2 or 4 CTAs; the
+// pre-converted form (TMA-loaded A) in single CTAs only.
 template <int AMODE>
 cudaError_t dual_launch(int cn, const TensorMaps& m, const KernelArgs& a, cudaStream_t s) {
-  switch (cn) {
-    case 1: return DualLaunch<AMODE, 1>::launch(m, a, s);
-    case 2: return DualLaunch<AMODE, 2>::launch(m, a, s);
-    case 4: return DualLaunch<AMODE, 4>::launch(m, a, s);
-    default: return cudaErrorInvalidValue;
+  if (cn == 1) return DualLaunch<AMODE, 1>::launch(m, a, s);
+  if constexpr (AMODE == A_TMA_F16) {
+    return cudaErrorInvalidValue;
+  } else {
+    switch (cn) {
+      case 2: return DualLaunch<AMODE, 2>::launch(m, a, s);
+      case 4: return DualLaunch<AMODE, 4>::launch(m, a, s);
+      default: return cudaErrorInvalidValue;
+    }
   }
 }
 
 template <int AMODE>
 int dual_capacity(int cn, cudaError_t* err) {
-  switch (cn) {
-    case 1: return DualLaunch<AMODE, 1>::capacity(err);
-    case 2: return DualLaunch<AMODE, 2>::capacity(err);
-    case 4: return DualLaunch<AMODE, 4>::capacity(err);
-    default: *err = cudaErrorInvalidValue; return 0;
+  if (cn == 1) return DualLaunch<AMODE, 1>::capacity(err);
+  if constexpr (AMODE == A_TMA_F16) {
+    *err = cudaErrorInvalidValue;
+    return 0;
+  } else {
+    switch (cn) {
+      case 2: return DualLaunch<AMODE, 2>::capacity(err);
+      case 4: return DualLaunch<AMODE, 4>::capacity(err);
+      default: *err = cudaErrorInvalidValue; return 0;
+    }
   }
 }
 
