@@ -68,9 +68,15 @@ weights, evaluated here as two ``matmul_w16`` calls.
 
 Everything is evaluated in float64. Inputs are widened exactly: float32 to
 float64 by numpy, binary16 bit patterns by ``f16_bits_to_f64`` below (an
-IEEE 754 decoder written from the format's definition). The contraction uses
-numpy's float64 matmul as a library primitive; nothing is blocked, fused or
-reordered beyond the definitions above.
+IEEE 754 decoder written from the format's definition). Every contraction
+(the forward products, both backward products and the normaliser) is the
+plain triple loop of ``gemm_f64.c`` in this directory: for each output row i,
+for k in ascending order, for every column j, Y[i,j] += A[i,k] * B[k,j] and
+S[i,j] += |A[i,k] * B[k,j]|, in fp64 with no fused multiply-add; it is
+compiled by gcc on first use (``build_native.py``). The transposed operands
+of the backward products are copied to row-major form first (a copy, no
+arithmetic). Nothing is blocked, fused or reordered beyond the definitions
+above.
 
 Acceptance metric (the normalised error) is ``normalised_error``: for every
 output element, |Y - Y_ref| / S with S[i,j] = sum_k |A[i,k] * W[k,j]|, A being
@@ -84,6 +90,7 @@ invariants and numpy's own binary16 type.
 
 from __future__ import annotations
 
+import ctypes
 import math
 
 import numpy as np
@@ -118,6 +125,7 @@ __all__ = [
     "normaliser",
     "normalised_error",
     "reference",
+    "contraction_threads",
     "FORMS",
 ]
 
@@ -143,6 +151,49 @@ FORMS = (
 
 def _f64(a) -> np.ndarray:
     return np.asarray(a, dtype=np.float64)
+
+
+# --------------------------------------------------------------------------
+# The contraction: the triple loop of gemm_f64.c
+# --------------------------------------------------------------------------
+
+_LIB = None
+
+
+def _gemm_lib():
+    global _LIB
+    if _LIB is None:
+        from . import build_native
+
+        lib = ctypes.CDLL(build_native.build())
+        lib.oracle_gemm_f64.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int64] * 3
+        lib.oracle_gemm_f64.restype = None
+        lib.oracle_gemm_threads.argtypes = []
+        lib.oracle_gemm_threads.restype = ctypes.c_int
+        _LIB = lib
+    return _LIB
+
+
+def contraction_threads() -> int:
+    """Host threads the contraction's row loop runs on."""
+    return int(_gemm_lib().oracle_gemm_threads())
+
+
+def _contract(A, B, with_s: bool):
+    """(Y, S) with Y[i,j] = sum_k A[i,k] B[k,j] and, if asked, S[i,j] =
+    sum_k |A[i,k] B[k,j]| (else None): the triple loop, k ascending."""
+    A = np.ascontiguousarray(_f64(A))
+    B = np.ascontiguousarray(_f64(B))
+    if A.ndim != 2 or B.ndim != 2 or A.shape[1] != B.shape[0]:
+        raise ValueError(f"shape mismatch: {A.shape} @ {B.shape}")
+    M, K = A.shape
+    N = B.shape[1]
+    Y = np.zeros((M, N))
+    S = np.zeros((M, N)) if with_s else None
+    if M and N:
+        _gemm_lib().oracle_gemm_f64(A.ctypes.data, B.ctypes.data, Y.ctypes.data,
+                                    S.ctypes.data if with_s else None, M, N, K)
+    return Y, S
 
 
 # --------------------------------------------------------------------------
@@ -211,7 +262,7 @@ def matmul(X, W) -> np.ndarray:
     W = _f64(W)
     if X.ndim != 2 or W.ndim != 2 or X.shape[1] != W.shape[0]:
         raise ValueError(f"shape mismatch: X{X.shape} @ W{W.shape}")
-    return X @ W
+    return _contract(X, W, False)[0]
 
 
 def matmul_residual(X, W, R) -> np.ndarray:
@@ -254,7 +305,7 @@ def matmul_t(DY, W) -> np.ndarray:
     W = _f64(W)
     if DY.ndim != 2 or W.ndim != 2 or DY.shape[1] != W.shape[1]:
         raise ValueError(f"shape mismatch: dY{DY.shape} @ W{W.shape}^T")
-    return DY @ W.T
+    return _contract(DY, W.T, False)[0]
 
 
 def matmul_t_acc(DY, W, DX0) -> np.ndarray:
@@ -283,7 +334,7 @@ def matmul_at(X, DY) -> np.ndarray:
     DY = _f64(DY)
     if X.ndim != 2 or DY.ndim != 2 or X.shape[0] != DY.shape[0]:
         raise ValueError(f"shape mismatch: X{X.shape}^T @ dY{DY.shape}")
-    return X.T @ DY
+    return _contract(X.T, DY, False)[0]
 
 
 def matmul_at_acc(X, DY, DW0) -> np.ndarray:
@@ -400,13 +451,13 @@ def gate_up_w16(X, WG16, WU16):
 # --------------------------------------------------------------------------
 
 def normaliser(A, W) -> np.ndarray:
-    """S[i,j] = sum_k |A[i,k] * W[k,j]| = (|A| @ |W|)[i,j], in float64.
+    """S[i,j] = sum_k |A[i,k] * W[k,j]|, in float64 (the triple loop).
 
     A is the left operand as the definition states it (X, or
     silu(GATE) * UP), before any rounding a fast path may apply; W is the
     weight matrix as stored (binary16 values decoded exactly).
     """
-    return np.abs(_f64(A)) @ np.abs(_f64(W))
+    return _contract(A, W, True)[1]
 
 
 def normalised_error(Y, Y_ref, S, R=None) -> float:
@@ -448,17 +499,21 @@ def reference(form: str, inputs: dict, rows=None):
     if form not in FORMS:
         raise ValueError(f"unknown form {form!r}")
     sel = (lambda a: a) if rows is None else (lambda a: np.asarray(a)[rows])
+    # Y and its normaliser S come from one pass of the triple loop; the
+    # residual (or the initial value of an accumulating form) is added after
+    # the sum, as in matmul_residual / matmul_t_acc / matmul_at_acc.
     if form.startswith("matmul_at"):
         # dW row k depends on column k of X (all rows of X and dY): ``rows``
         # picks output rows of dW here
         X = swiglu_a(inputs["GATE"], inputs["UP"]) if "swiglu" in form else _f64(inputs["X"])
         DY = _f64(inputs["DY"])
         Xk = X if rows is None else X[:, rows]
+        if Xk.shape[0] != DY.shape[0]:
+            raise ValueError(f"shape mismatch: X{Xk.shape}^T @ dY{DY.shape}")
+        Y, S = _contract(Xk.T, DY, True)
         if "_acc" in form:
-            Y = matmul_at_acc(Xk, DY, sel(inputs["R"]))
-        else:
-            Y = matmul_at(Xk, DY)
-        return Y, normaliser(Xk.T, DY)
+            Y = _plus(Y, sel(inputs["R"]))
+        return Y, S
     w16 = form.endswith("_w16")
     W = f16_bits_to_f64(inputs["W16"]) if w16 else _f64(inputs["W"])
     if "swiglu_backward" in form:
@@ -470,8 +525,10 @@ def reference(form: str, inputs: dict, rows=None):
         DY = _f64(sel(inputs["DY"]))
         GATE = _f64(sel(inputs["GATE"]))
         UP = _f64(sel(inputs["UP"]))
-        dgate, dup = matmul_t_swiglu_backward(DY, W, GATE, UP)
-        S = normaliser(DY, W.T)
+        if DY.shape[1] != W.shape[1]:
+            raise ValueError(f"shape mismatch: dY{DY.shape} @ W{W.shape}^T")
+        dA, S = _contract(DY, W.T, True)
+        dgate, dup = ffn_swiglu_backward(dA, GATE, UP)
         s = sigmoid(GATE)
         with np.errstate(invalid="ignore", over="ignore"):
             Sg = nan_guard(S * np.abs(UP) * (s + np.abs(GATE) * s * (1.0 - s)))
@@ -480,17 +537,25 @@ def reference(form: str, inputs: dict, rows=None):
     if form.startswith("matmul_t"):
         # dX row i depends only on dY row i (and R row i)
         A = _f64(sel(inputs["DY"]))
+        if A.shape[1] != W.shape[1]:
+            raise ValueError(f"shape mismatch: dY{A.shape} @ W{W.shape}^T")
+        Y, S = _contract(A, W.T, True)
         if "_acc" in form:
-            Y = matmul_t_acc(A, W, sel(inputs["R"]))
-        else:
-            Y = matmul_t(A, W)
-        return Y, normaliser(A, W.T)
+            Y = _plus(Y, sel(inputs["R"]))
+        return Y, S
     if "swiglu" in form:
         A = swiglu_a(sel(inputs["GATE"]), sel(inputs["UP"]))
     else:
         A = _f64(sel(inputs["X"]))
+    Y, S = _contract(A, W, True)
     if "residual" in form:
-        Y = matmul_residual(A, W, sel(inputs["R"]))
-    else:
-        Y = matmul(A, W)
-    return Y, normaliser(A, W)
+        Y = _plus(Y, sel(inputs["R"]))
+    return Y, S
+
+
+def _plus(Y, R) -> np.ndarray:
+    """Y + R for an [M,N] residual (or initial value) R."""
+    R = _f64(R)
+    if R.shape != Y.shape:
+        raise ValueError(f"residual shape {R.shape} != output shape {Y.shape}")
+    return Y + R

@@ -487,3 +487,38 @@ def test_gate_up_brute_force():
     for i, n in itertools.product(range(3), range(4)):
         assert G[i, n] == sum(float(X[i, k]) * float(wg[k, n]) for k in range(5))
         assert U[i, n] == sum(float(X[i, k]) * float(wu[k, n]) for k in range(5))
+
+
+# ---------------------------------------------------------------- hand-worked fixtures of the
+# widened rows: the SwiGLU-backward normalisers and the loss total
+
+def test_golden_swiglu_backward_and_normalisers():
+    # tests/golden/swiglu_backward_1x2x4.txt: sigma(+-ln 3), gate 0 and
+    # gate 40 worked by hand, including the normalisers S_dGATE, S_dUP that
+    # widen the acceptance bound of the fused SwiGLU backward
+    g = read_blocks("swiglu_backward_1x2x4.txt")
+    W16 = g["W"].astype(np.float16).view(np.uint16)
+    for form, w in (("matmul_t_swiglu_backward", {"W": g["W"].astype(np.float32)}),
+                    ("matmul_t_swiglu_backward_w16", {"W16": W16})):
+        d = {"DY": g["DY"].astype(np.float32), "GATE": g["GATE"], "UP": g["UP"], **w}
+        (dgate, dup), (Sg, Su) = oracle.reference(form, d)
+        for got, want in ((dgate, g["DGATE"]), (dup, g["DUP"]), (Sg, g["SG"]), (Su, g["SU"])):
+            np.testing.assert_allclose(got, want, rtol=4e-15, atol=0, err_msg=form)
+    # the direct function gives the same gradients
+    dgate, dup = oracle.matmul_t_swiglu_backward(g["DY"], g["W"], g["GATE"], g["UP"])
+    np.testing.assert_allclose(dgate, g["DGATE"], rtol=4e-15, atol=0)
+    np.testing.assert_allclose(dup, g["DUP"], rtol=4e-15, atol=0)
+
+
+def test_golden_lm_head_cross_entropy_total():
+    # tests/golden/cross_entropy_total.txt: per-row losses and their SUM
+    # (page 07_loss, "sum_losses"), with and without smoothing and z-loss
+    X = np.array([[1.0, 0.0], [0.0, 1.0], [1.0, 1.0]], dtype=np.float32)
+    W16 = np.array([[0x0000] * 4, [0x3C00, 0, 0, 0]], dtype=np.uint16)
+    targets = [1, 0, 7]
+    for alpha, beta, l0, l1, l2, total in (map(float, r) for r in
+                                           read_rows("cross_entropy_total.txt")):
+        losses, dl, got_total = oracle.lm_head_cross_entropy_w16(X, W16, targets, alpha, beta)
+        np.testing.assert_allclose(losses, [l0, l1, l2], rtol=1e-15, atol=0)
+        assert math.isclose(got_total, total, rel_tol=1e-15), (alpha, beta, got_total, total)
+        assert np.all(dl[2] == 0.0)            # the ignored row has no gradient
