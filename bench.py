@@ -17,9 +17,14 @@ shapes (each timed cold, after an L2 flush, and warm, back to back).
 ``--impl reference`` times the fp64 CPU oracle instead (rank 0 only), each
 step a bounded sample of rows of the same workload.
 
-Multi-GPU: one process per GPU (torchrun); the path shards over tokens with
-no exchange, so every rank runs its own replica of the workload ("replicas
+Multi-GPU: one process per GPU, under torchrun, or started by ``--gpus N``
+itself when no launcher set WORLD_SIZE; the path shards over tokens with no
+exchange, so every rank runs its own replica of the workload ("replicas
 only", weak scaling) and value = all ranks' FLOPs / the slowest rank's time.
+
+``--measure-peaks`` prints this GPU's cuBLAS TF32 / binary16 / bfloat16
+peaks (the TF32 one, recorded in profiles/tensor_peaks.txt, is the roofline
+peak of the f32 forms).
 """
 
 from __future__ import annotations
@@ -51,13 +56,32 @@ NOMINAL_RATIO = {"f16": 1.0, "tf32": 1.1 / 2.25}
 
 # ----------------------------------------------------------------- helpers
 
+def recorded_tensor_peaks() -> dict:
+    """The TF32 peaks (burst, sustained; TFLOP/s) measured on this machine's
+    GB300s by ``--measure-peaks`` and recorded in profiles/tensor_peaks.txt
+    (empty if absent)."""
+    p = os.path.join(ROOT, "profiles", "tensor_peaks.txt")
+    out = {}
+    if os.path.exists(p):
+        with open(p) as f:
+            for line in f:
+                parts = line.split()
+                if len(parts) == 2 and not line.startswith("#") and \
+                        parts[0] in ("tf32_tflops", "tf32_tflops_sustained"):
+                    out[parts[0]] = float(parts[1])
+    return out
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         with open(p) as f:
             d = json.load(f)
-        return d, "measured"
-    return dict(FALLBACK_PEAKS), "fallback"
+        src = "measured"
+    else:
+        d, src = dict(FALLBACK_PEAKS), "fallback"
+    d.update(recorded_tensor_peaks())
+    return d, src
 
 
 # The sources the dominant kernel (the clustered SwiGLU GEMM) is compiled
@@ -114,11 +138,21 @@ def mma_dtype(form: str) -> str:
     return "f16" if form.endswith("_w16") else "tf32"
 
 
+def tensor_peak(dtype: str, peaks: dict, sustained: bool = False):
+    """(peak TFLOP/s, where it comes from) of the contraction's own dtype:
+    the measured TF32 peak for the f32 forms where one is recorded, else the
+    measured bfloat16 peak times the nominal ratio (binary16: 1.0)."""
+    key = f"{dtype}_tflops" + ("_sustained" if sustained else "")
+    if dtype == "tf32" and key in peaks:
+        return peaks[key], "measured tf32 (cuBLAS, profiles/tensor_peaks.txt)"
+    bf16 = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
+    return bf16 * NOMINAL_RATIO[dtype], f"bf16 x nominal {dtype}/bf16 ratio {NOMINAL_RATIO[dtype]:.3g}"
+
+
 def roofline(w: wl.Workload, peaks: dict, sustained: bool = False):
     """(bound, roofline TFLOP/s, tensor peak TFLOP/s, HBM GB/s) of workload w:
     min(peak FLOP/s, algorithmic bytes / HBM bandwidth * FLOP/byte)."""
-    bf16 = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
-    tpeak = bf16 * NOMINAL_RATIO[mma_dtype(w.form)]
+    tpeak = tensor_peak(mma_dtype(w.form), peaks, sustained)[0]
     hbm = peaks["hbm_gbs"]
     nbytes = wl.input_bytes(w.form, w.M, w.N, w.K)
     mem_tflops = w.flops / nbytes * hbm / 1e3
@@ -128,19 +162,99 @@ def roofline(w: wl.Workload, peaks: dict, sustained: bool = False):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons every 200 ms in a thread."""
+    """SM clock, power and clock-event reasons sampled during a timed region.
+
+    Read-only NVML queries (libnvidia-ml through ctypes: the SM clock, its
+    maximum, the power draw and the active clock-event reasons) every
+    `period_s` in a thread, so that even a timed region of a few milliseconds
+    holds several samples; where NVML cannot be loaded, nvidia-smi's own
+    200 ms loop. Nothing here sets any GPU state. A sample is (host time,
+    SM MHz, max SM MHz, power W, set of reason names)."""
 
     FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # nvmlClocksEventReason* bits (nvml.h) of the reasons the bench reports
+    REASON_BITS = ((0x8, "hw_slowdown"), (0x40, "hw_thermal_slowdown"),
+                   (0x20, "sw_thermal_slowdown"), (0x4, "sw_power_cap"))
+    NVML_CLOCK_SM = 1
 
-    def __init__(self, gpu_id: str | None):
-        self.gpu_id = gpu_id
-        self.samples = []   # (host time, fields...)
+    def __init__(self, gpu_id: str | None, period_s: float = 0.002):
+        self.gpu_id = gpu_id          # "GPU-<uuid>", or None for the first GPU
+        self.period_s = period_s
+        self.samples = []
+        self.source = None
         self.proc = None
         self.thread = None
+        self._stop = threading.Event()
+
+    # -- NVML (read-only queries)
+    def _nvml_open(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit_v2 failed")
+        dev = ctypes.c_void_p()
+        if self.gpu_id:
+            rc = lib.nvmlDeviceGetHandleByUUID(self.gpu_id.encode(), ctypes.byref(dev))
+        else:
+            rc = lib.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(dev))
+        if rc != 0:
+            lib.nvmlShutdown()
+            raise OSError("no NVML handle for the device")
+        reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        return lib, dev, reasons_fn
+
+    def _nvml_loop(self, lib, dev, reasons_fn):
+        import ctypes
+        sm, smax, mw = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        lib.nvmlDeviceGetMaxClockInfo(dev, self.NVML_CLOCK_SM, ctypes.byref(smax))
+        try:
+            while not self._stop.is_set():
+                t = time.time()
+                ok = lib.nvmlDeviceGetClockInfo(dev, self.NVML_CLOCK_SM, ctypes.byref(sm)) == 0
+                pw = lib.nvmlDeviceGetPowerUsage(dev, ctypes.byref(mw)) == 0
+                rok = reasons_fn(dev, ctypes.byref(rs)) == 0
+                if ok:
+                    names = frozenset(n for b, n in self.REASON_BITS if rok and rs.value & b)
+                    self.samples.append((t, float(sm.value), float(smax.value) or None,
+                                         mw.value / 1000.0 if pw else None, names))
+                time.sleep(self.period_s)
+        finally:
+            lib.nvmlShutdown()
+
+    # -- nvidia-smi fallback
+    def _smi_read(self):
+        for line in self.proc.stdout:
+            self.samples.append(self.parse_smi_row(time.time(), line))
+
+    @classmethod
+    def parse_smi_row(cls, t: float, line: str):
+        f = [x.strip() for x in line.split(",")]
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        if len(f) < 9:
+            return (t, None, None, None, frozenset())
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        active = frozenset(n for n, v in zip(names, f[5:9]) if v.lower() == "active")
+        return (t, num(f[1]), num(f[2]), num(f[3]), active)
 
     def start(self):
+        try:
+            lib, dev, reasons_fn = self._nvml_open()
+            self.source = f"NVML every {self.period_s * 1e3:.0f} ms"
+            self.thread = threading.Thread(target=self._nvml_loop, args=(lib, dev, reasons_fn),
+                                           daemon=True)
+            self.thread.start()
+            return
+        except (OSError, AttributeError):
+            pass
         cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
                "-lms", "200"]
         if self.gpu_id:
@@ -151,14 +265,12 @@ class ClockSampler:
         except OSError:
             self.proc = None
             return
-        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.source = "nvidia-smi every 200 ms"
+        self.thread = threading.Thread(target=self._smi_read, daemon=True)
         self.thread.start()
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
-
     def stop(self):
+        self._stop.set()
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -169,47 +281,31 @@ class ClockSampler:
             self.thread.join(timeout=5)
 
     def summary(self, t0: float, t1: float):
-        inside = [s for t, s in self.samples if t0 <= t <= t1 + 0.2]
-        used = inside if inside else [s for _, s in self.samples]
+        """Median SM clock, its maximum, the reasons seen and the peak power
+        over the samples taken between host times t0 and t1 (all samples when
+        none fell inside)."""
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        used = inside if inside else list(self.samples)
         if not used:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
-                    "note": "nvidia-smi unavailable"}
-
-        def num(x):
-            try:
-                return float(x)
-            except ValueError:
-                return None
-        sm = [num(s[1]) for s in used if len(s) > 8 and num(s[1]) is not None]
-        smax = [num(s[2]) for s in used if len(s) > 8 and num(s[2]) is not None]
-        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        reasons = set()
-        for s in used:
-            if len(s) > 8:
-                for name, v in zip(names, s[5:9]):
-                    if v.lower() == "active":
-                        reasons.add(name)
-        power = [num(s[3]) for s in used if len(s) > 8 and num(s[3]) is not None]
+                    "samples_in_timed_region": 0, "source": self.source,
+                    "note": "no clock source available"}
+        sm = [s[1] for s in used if s[1] is not None]
+        smax = [s[2] for s in used if s[2] is not None]
+        power = [s[3] for s in used if s[3] is not None]
+        reasons = sorted(set().union(*(s[4] for s in used)))
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons),
+                "reasons": reasons,
                 "power_w_max": max(power) if power else None,
-                "samples": len(used), "samples_in_timed_region": len(inside)}
+                "samples": len(used), "samples_in_timed_region": len(inside),
+                "source": self.source}
 
 
 def oracle_threads() -> int:
-    try:
-        from threadpoolctl import threadpool_info
-        import numpy  # noqa: F401
-        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
-        if n and max(n) > 0:
-            return max(n)
-    except Exception:
-        pass
-    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
-        if os.environ.get(var, "").isdigit():
-            return int(os.environ[var])
-    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    """Host threads the oracle's contraction runs on (its OpenMP row loop)."""
+    import oracle
+    return oracle.contraction_threads()
 
 
 def cpu_baseline(w: wl.Workload, inputs: dict, budget_s: float = 12.0, chunk: int = 64):
@@ -232,7 +328,7 @@ def cpu_baseline(w: wl.Workload, inputs: dict, budget_s: float = 12.0, chunk: in
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle_threads(),
             "kind": "oracle",
             "sample": f"{rows_done} of {w.M} rows of {w.name} ({w.describe()}), "
-                      f"fp64 numpy oracle incl. normaliser, {dt:.1f} s"}
+                      f"fp64 C triple-loop oracle incl. normaliser, {dt:.1f} s"}
 
 
 # ----------------------------------------------------------------- reference arm
@@ -258,6 +354,9 @@ def replicas_value(world: int, flops_per_rank: float, ms_max: float) -> float:
 
 def run_reference(args, rank: int):
     if rank != 0:
+        world = os.environ.get("WORLD_SIZE", "?")
+        print(f"bench: rank {rank} of {world}: the reference arm runs on rank 0 only",
+              file=sys.stderr, flush=True)
         return
     import numpy as np
     import oracle
@@ -598,11 +697,10 @@ def run_ours(args, rank: int, world: int):
     sustained = timed_s > 1.0
     bound, roof, tpeak, hbm = roofline(w, peaks, sustained=sustained)
     traffic = recorded_traffic(w.name)
-    ratio_txt = ("x nominal f16/bf16 ratio 1.0" if mma_dtype(w.form) == "f16"
-                 else "x nominal tf32/bf16 ratio 0.489")
+    peak_txt = tensor_peak(mma_dtype(w.form), peaks, sustained)[1]
     roof_obj = {"bound": bound, "achieved": kernel_tflops, "peak": roof, "unit": "TFLOP/s",
                 "frac": kernel_tflops / roof, "traffic": traffic,
-                "peak_source": f"{peak_src} bf16 {ratio_txt} "
+                "peak_source": f"{peak_src} peaks: {peak_txt} "
                                f"({'sustained: timed region %.1f s' % timed_s if sustained else 'burst: timed region %.2f s' % timed_s})",
                 "peak_burst": roofline(w, peaks, sustained=False)[1],
                 "peak_sustained": roofline(w, peaks, sustained=True)[1],
@@ -641,6 +739,7 @@ def run_ours(args, rank: int, world: int):
             b, r, tp, _ = roofline(sw, peaks)
             table.append({"workload": name, "form": sw.form, "M": sw.M, "N": sw.N, "K": sw.K,
                           "bound": b, "roofline_tflops": r,
+                          "tensor_peak_source": tensor_peak(mma_dtype(sw.form), peaks)[1],
                           "cold_us": cold_us, "cold_tflops": sw.flops / cold_us / 1e6,
                           "cold_frac": sw.flops / cold_us / 1e6 / r,
                           "warm_us": warm_us, "warm_tflops": sw.flops / warm_us / 1e6,
@@ -654,6 +753,7 @@ def run_ours(args, rank: int, world: int):
             b, r, tp, _ = roofline(sw, peaks)
             table.append({"workload": sw.name, "form": sw.form, "M": sw.M, "N": sw.N, "K": sw.K,
                           "bound": b, "roofline_tflops": r,
+                          "tensor_peak_source": tensor_peak(mma_dtype(sw.form), peaks)[1],
                           "cold_us": cold_us, "cold_tflops": sw.flops / cold_us / 1e6,
                           "cold_frac": sw.flops / cold_us / 1e6 / r,
                           "warm_us": warm_us, "warm_tflops": sw.flops / warm_us / 1e6,
@@ -669,6 +769,77 @@ def run_ours(args, rank: int, world: int):
         line["cpu_baseline"] = cpu_baseline(w, host, budget_s=args.cpu_seconds)
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def launch_command(nproc: int, argv: list[str], port: int) -> list[str]:
+    """The command that re-runs this script as `nproc` ranks of one node
+    (torch.distributed.run on 127.0.0.1), with the same arguments."""
+    return [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+            f"--nproc-per-node={nproc}", "--master-addr", "127.0.0.1",
+            "--master-port", str(port), os.path.abspath(__file__), *argv]
+
+
+def _free_port() -> int:
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def measure_peaks(seconds: float = 3.0) -> dict:
+    """Dense tensor-core peaks of this GPU as cuBLAS reaches them through
+    torch.matmul at 8192^3 (2 N^3 FLOPs): TF32 (float32 with TF32 allowed),
+    binary16 and bfloat16; each the best of 10 single calls (burst) and the
+    rate of back-to-back calls over `seconds` (sustained), CUDA events on the
+    current stream, with SM clocks sampled meanwhile."""
+    import torch
+    n = 8192
+    flops = 2.0 * n ** 3
+    out = {"how": f"torch.matmul {n}^3 (2*N^3): best of 10 (burst) and back to back for "
+                  f"{seconds:.0f} s (sustained); CUDA events", "torch": torch.__version__,
+           "gpu_name": torch.cuda.get_device_name()}
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = True
+    try:
+        for name, dt in (("tf32", torch.float32), ("f16", torch.float16),
+                         ("bf16", torch.bfloat16)):
+            a = torch.randn(n, n, device="cuda").to(dt)
+            b = torch.randn(n, n, device="cuda").to(dt)
+            for _ in range(3):
+                torch.matmul(a, b)
+            torch.cuda.synchronize()
+            best = float("inf")
+            for _ in range(10):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record()
+                torch.matmul(a, b)
+                e1.record()
+                e1.synchronize()
+                best = min(best, e0.elapsed_time(e1) * 1e-3)
+            iters = max(1, int(seconds / best))
+            sampler = ClockSampler(None, period_s=0.01)
+            sampler.start()
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            h0 = time.time()
+            e0.record()
+            for _ in range(iters):
+                torch.matmul(a, b)
+            e1.record()
+            e1.synchronize()
+            h1 = time.time()
+            sampler.stop()
+            sus = e0.elapsed_time(e1) * 1e-3 / iters
+            out[f"{name}_tflops"] = flops / best / 1e12
+            out[f"{name}_tflops_sustained"] = flops / sus / 1e12
+            out[f"{name}_clocks_sustained"] = sampler.summary(h0, h1)
+            del a, b
+            torch.cuda.empty_cache()
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+    return out
 
 
 def main():
@@ -696,9 +867,23 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--m", type=int, default=None,
                     help="override M (tokens) of the workload, e.g. a small case for ncu")
+    ap.add_argument("--measure-peaks", action="store_true",
+                    help="print the TF32, binary16 and bfloat16 cuBLAS peaks of this GPU "
+                         "as one JSON line and exit")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.gpus < 1:
+        ap.error("--gpus must be >= 1")
+    if args.measure_peaks:
+        print(json.dumps(measure_peaks()), flush=True)
+        return
+
+    # --gpus N outside a launcher: start N ranks on this node, one per GPU
+    # (each runs its own replica; rank 0 prints the line) and exit with
+    # their status.
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        sys.exit(subprocess.call(launch_command(args.gpus, sys.argv[1:], _free_port())))
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -8,8 +8,10 @@ The reference arm runs on rank 0 alone. No GPU is used.
 """
 
 import io
+import json
 import os
 import socket
+import subprocess
 import sys
 from contextlib import redirect_stdout
 
@@ -79,3 +81,23 @@ def test_reference_arm_runs_on_rank_0_only():
     with redirect_stdout(buf):
         assert bench.run_reference(args, rank=1) is None
     assert buf.getvalue() == ""
+
+
+def test_gpus_flag_starts_the_ranks():
+    # `bench.py --gpus 2` with no launcher around it starts two ranks itself
+    # (torch.distributed.run on 127.0.0.1); the reference arm then runs on
+    # rank 0, which prints the one JSON line, and rank 1 says it has no work.
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT")}
+    env["OMP_NUM_THREADS"] = "2"
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2",
+                        "--impl", "reference", "--workload", "attn_proj_f32", "--steps", "1",
+                        "--warmup", "3", "--ref-rows", "2"],
+                       cwd=ROOT, env=env, stdout=subprocess.PIPE, stderr=subprocess.PIPE,
+                       text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-3000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["config"]["workload"] == "attn_proj_f32"
+    assert "rank 1 of 2: the reference arm runs on rank 0 only" in r.stderr
