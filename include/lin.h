@@ -184,7 +184,10 @@ lin_status lin_matmul_residual_swiglu_a_w16(const float *GATE, const float *UP,
  *   Set-up    the first call on a device that passes validation looks up
  *             the array's address (cudaGetSymbolAddress, which loads its
  *             module); make that first call before capturing a stream.
- *             A failed look-up returns LIN_ERROR_CUDA every time.
+ *             The address is kept for that device's context and looked up
+ *             again once the context has changed (after cudaDeviceReset,
+ *             for example). A failed look-up returns LIN_ERROR_CUDA and is
+ *             not remembered: the next call tries again.
  *   Zeroing   nothing in the array needs to start at zero: a call writes
  *             every byte of it that it reads first.
  *   Races     every call on a device shares the one array. Calls whose

@@ -16,12 +16,44 @@ namespace {
 constexpr size_t kNoallocWorkspaceBytes = size_t{152} * 128 * 1024;
 constexpr int kMaxDevices = 64;
 
+// The array's address on one device, and the context it belongs to: the
+// address is valid only while that context lives (a cudaDeviceReset ends it;
+// the next context loads the module again, possibly elsewhere).
 struct NoallocDevice {
-  std::once_flag once;
-  cudaError_t error = cudaSuccess;
+  std::mutex mu;
+  unsigned long long ctx_id = 0;   // unique id of that context; 0: none yet
   void* base = nullptr;
 };
 NoallocDevice g_noalloc_devices[kMaxDevices];
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// Unique id (cuCtxGetId: never reused within a process) of the calling
+// thread's current context, or 0 when it cannot be told.
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+    cudaGetLastError();
+  });
+  CUcontext c = nullptr;
+  if (!get_current || !get_id || get_current(&c) != CUDA_SUCCESS || !c) return 0;
+  unsigned long long id = 0;
+  return get_id(c, &id) == CUDA_SUCCESS ? id : 0;
+}
 
 }  // namespace
 
@@ -31,22 +63,27 @@ static __device__ __align__(256) unsigned char g_noalloc_workspace[kNoallocWorks
 
 namespace {
 
-// Base and size of the array on device `dev`; its address is looked up
-// once per device (the first call that passes validation).
+// Base and size of the array on device `dev` (current). The address is
+// looked up on the first call that passes validation and again whenever the
+// device's context has changed since (or cannot be identified); a failed
+// look-up is not remembered, so the next call tries again.
 lin_status noalloc_workspace(int dev, void** ptr, size_t* bytes) {
   if (dev < 0 || dev >= kMaxDevices) return LIN_ERROR_UNSUPPORTED_DEVICE;
   NoallocDevice& d = g_noalloc_devices[dev];
-  std::call_once(d.once, [&] {
+  const unsigned long long ctx = current_context_id();
+  std::lock_guard<std::mutex> lock(d.mu);
+  if (!d.base || ctx == 0 || ctx != d.ctx_id) {
     void* p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_workspace);
     if (e != cudaSuccess) {
-      d.error = e;
       cudaGetLastError();
-      return;
+      d.base = nullptr;
+      d.ctx_id = 0;
+      return lin_detail::record_cuda_error(e);
     }
     d.base = p;
-  });
-  if (d.error != cudaSuccess) return lin_detail::record_cuda_error(d.error);
+    d.ctx_id = ctx;
+  }
   *ptr = d.base;
   *bytes = kNoallocWorkspaceBytes;
   return LIN_SUCCESS;
