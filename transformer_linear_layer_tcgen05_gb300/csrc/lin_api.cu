@@ -181,17 +181,18 @@ bool overlaps(const void* a, uint64_t abytes, const void* b, uint64_t bbytes) {
   return a0 < b0 + bbytes && b0 < a0 + abytes;
 }
 
-// 2-D row-major tensor map with the 128-byte swizzle; out-of-range elements
-// of a load read as zero.
+// 2-D row-major tensor map with the 128-byte swizzle (16-byte atoms, or
+// 32-byte atoms for an MN-major TF32 operand); out-of-range elements of a
+// load read as zero.
 bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t cols,
-               uint64_t rows, uint64_t row_bytes, uint32_t box_cols, uint32_t box_rows) {
+               uint64_t rows, uint64_t row_bytes, uint32_t box_cols, uint32_t box_rows,
+               CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   const cuuint64_t dims[2] = {cols, rows};
   const cuuint64_t strides[1] = {row_bytes};
   const cuuint32_t box[2] = {box_cols, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   return driver().encode(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -414,8 +415,8 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
       ok &= encode_2d(&maps.w2, CU_TENSOR_MAP_DATA_TYPE_UINT16, p.W2, N, K, N * 2, 64, 64);
       ok &= encode_2d(&maps.y2, f32, p.Y2, N, M, N * 4, lin::kEpiCols, lin::kEpiRows);
     }
-  } else {
-    ok &= encode_2d(&maps.w, f32, p.W, N, K, N * 4, 32, 32);
+  } else {   // W [K,N] f32: an MN-major TF32 operand, 128-byte swizzle with 32-byte atoms
+    ok &= encode_2d(&maps.w, f32, p.W, N, K, N * 4, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B);
   }
   if (resid) ok &= encode_2d(&maps.r, f32, p.R, N, M, N * 4, lin::kEpiCols, lin::kEpiRows);
   ok &= encode_2d(&maps.y, f32, p.Y, N, M, N * 4, lin::kEpiCols, lin::kEpiRows);

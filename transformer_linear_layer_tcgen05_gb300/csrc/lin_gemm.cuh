@@ -47,12 +47,11 @@ struct GemmTraits {
   // The A operand is built by the transform warps unless X is copied as is.
   static constexpr bool kXformA = (AMODE != A_TMA_F32);
   static constexpr bool kTransA = (AMODE == A_TRANS_F32 || AMODE == A_TRANS_SWIGLU_F32);  // A = X^T
-  // TF32 UMMA takes a K-major B only, so for the f32 forms the transform
-  // warps transpose the TMA-staged W tile (N contiguous) into a K-major
-  // operand; binary16 W is consumed MN-major straight from TMA.
-  static constexpr bool kXformB = !kF16 && !BT;
+  // W [K,N] (N contiguous) is consumed MN-major straight from TMA: binary16
+  // in the 128-byte swizzle, f32 (TF32) in the 128-byte swizzle with 32-byte
+  // atoms (the layout an MN-major TF32 operand needs).
   static constexpr bool kBT = BT;
-  static constexpr bool kXform = kXformA || kXformB;
+  static constexpr bool kXform = kXformA;
 
   static constexpr int BM = kBM;
   static constexpr int BN = BN_;
@@ -70,19 +69,18 @@ struct GemmTraits {
   static constexpr uint32_t B_BYTES = W_BOXES * B_ATOM_BYTES;   // = BK * BN * ESZ
   static constexpr uint32_t OP_STAGE_BYTES = A_BYTES + B_BYTES;
   // bytes the TMA delivers straight into an operand stage
-  static constexpr uint32_t OP_TMA_BYTES = (kXformA ? 0u : A_BYTES) + (kXformB ? 0u : B_BYTES);
+  static constexpr uint32_t OP_TMA_BYTES = (kXformA ? 0u : A_BYTES) + B_BYTES;
 
-  // Raw stage: what the transform warps read for 32 f32 columns of K:
-  // the A inputs (X, or GATE and UP) and, for TF32, the W tile of that k-block.
+  // Raw stage: what the transform warps read for 32 f32 columns of K: the A
+  // inputs (X, or GATE and UP).
   static constexpr int RAW_A_INPUTS = kXformA ? (kSwiglu ? 2 : 1) : 0;
   static constexpr uint32_t RAW_BOX_BYTES = BM * 128;           // [128 rows][32 f32]
   static constexpr uint32_t RAW_A_BYTES = RAW_A_INPUTS * RAW_BOX_BYTES;
-  static constexpr uint32_t RAW_W_BYTES = kXformB ? B_BYTES : 0u;   // [BN/32 runs][32 rows][128 B]
-  static constexpr uint32_t RAW_STAGE_BYTES = RAW_A_BYTES + RAW_W_BYTES;
+  static constexpr uint32_t RAW_STAGE_BYTES = RAW_A_BYTES;
   static constexpr int RAW_PER_KB = kF16 ? BK / 32 : 1;         // raw stages per k-block
-  // Both operands transformed (f32 SwiGLU): raw stages (GATE, UP and W of a
-  // k-block, 48 KB) carry the memory latency, operand stages only the local
-  // hand-off, so three raw stages and what is left for operand stages.
+  // Raw stages carry the memory latency of the transformed inputs, operand
+  // stages that of W and the local hand-off: three raw stages and what is
+  // left for operand stages.
   static constexpr int NR = 3;
 
   static constexpr uint32_t EPI_BUF_BYTES = kEpiRows * kEpiCols * 4;   // 4 KB
@@ -120,7 +118,7 @@ struct GemmTraits {
 
   static constexpr uint32_t TMEM_COLS = BN;
   static constexpr uint32_t IDESC =
-      umma_idesc(kF16 ? 0u : 2u, /*a_mn_major=*/false, /*b_mn_major=*/!kXformB && !BT, BM, BN);
+      umma_idesc(kF16 ? 0u : 2u, /*a_mn_major=*/false, /*b_mn_major=*/!BT, BM, BN);
 
   static_assert(NS >= 2, "operand ring needs two stages");
   static_assert(NS * OP_STAGE_BYTES >= BM * BN * 4, "a cluster split's partial tile in the ring");
@@ -183,15 +181,16 @@ __device__ __forceinline__ void transform_raw_stage(uint32_t a_stage, uint32_t r
   }
 }
 
-// TF32 B operand: transpose one staged W tile (BN/32 runs of [32 k-rows][32 f32
-// along N], 128-byte swizzle) into the K-major operand [BN rows n][32 f32
-// along K] with the same swizzle. Warp q handles runs q, q+4, ...; lane =
-// column inside the run. For a fixed k the 32 lanes read 32 distinct words
-// of one 128-byte row, and each group of 8 lanes writes 8 distinct 16-byte
-// bank groups, so neither side has bank conflicts.
+// TF32 A operand of a weight gradient, X^T: transpose one staged tile (BN/32
+// runs of [32 rows of the contraction][32 f32 of the tile's rows], 128-byte
+// swizzle) into the K-major operand [BN rows][32 f32 along K] with the same
+// swizzle. Warp q handles runs q, q+4, ...; lane = column inside the run.
+// For a fixed k the 32 lanes read 32 distinct words of one 128-byte row, and
+// each group of 8 lanes writes 8 distinct 16-byte bank groups, so neither
+// side has bank conflicts.
 template <int BN>
-__device__ __forceinline__ void transpose_w_tile(uint32_t b_stage, uint32_t raw_w, int q,
-                                                 int lane) {
+__device__ __forceinline__ void transpose_tile(uint32_t b_stage, uint32_t raw_w, int q,
+                                               int lane) {
 #pragma unroll 1
   for (int j = q; j < BN / 32; j += 4) {
     const uint32_t n = (uint32_t)(j * 32 + lane);
@@ -213,7 +212,7 @@ __device__ __forceinline__ void transpose_w_tile(uint32_t b_stage, uint32_t raw_
 // TF32 A operand of a weight gradient: (silu(GATE) * UP)^T. The raw stage
 // holds [32 rows of the contraction][32 columns] boxes of GATE and of UP
 // (BM/32 of each, UP at `raw_u`); warp q forms silu(g) * u of runs q, q+4,
-// ... and writes them transposed, exactly as transpose_w_tile moves W.
+// ... and writes them transposed, exactly as transpose_tile moves X^T.
 template <int BM>
 __device__ __forceinline__ void transpose_swiglu_tile(uint32_t a_stage, uint32_t raw_g,
                                                       uint32_t raw_u, int q, int lane) {
@@ -413,7 +412,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if constexpr (T::kBT) {
             // W as [N][K]: the tile's BN rows, this k-block's 128 bytes
             tma_load_2d(b_stage(st), &tm_w, kk, n0, full);
-          } else if constexpr (!T::kXformB) {
+          } else {
+            // W as [K][N]: 128-byte runs of W_ATOM columns, BK rows each
 #pragma unroll
             for (int j = 0; j < T::W_BOXES; ++j)
               tma_load_2d(b_stage(st) + j * T::B_ATOM_BYTES, &tm_w, n0 + j * T::W_ATOM, kk, full);
@@ -440,10 +440,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int k = 0; k < T::NMMA; ++k) {
           const uint64_t adesc = umma_desc_sw128(a_stage(st) + k * 32, 16, 1024);
-          const uint64_t bdesc =   // K-major (transposed on chip, or W given as [N][K])
-              (T::kXformB || T::kBT)
-                  ? umma_desc_sw128(b_stage(st) + k * 32, 16, 1024)
-                  : umma_desc_sw128(b_stage(st) + k * T::KSTEP * 128, T::B_ATOM_BYTES, 1024);
+          // W given as [N][K]: K-major. Else MN-major: a K step is KSTEP rows
+          // of 128 bytes further; runs of W_ATOM columns B_ATOM_BYTES apart;
+          // 8-row (binary16) or 4-row (TF32, 32-byte atoms) groups along K.
+          const uint64_t bdesc =
+              T::kBT ? umma_desc_sw128(b_stage(st) + k * 32, 16, 1024)
+              : T::kF16
+                  ? umma_desc_sw128(b_stage(st) + k * T::KSTEP * 128, T::B_ATOM_BYTES, 1024)
+                  : umma_desc_sw128_atom32(b_stage(st) + k * T::KSTEP * 128, T::B_ATOM_BYTES,
+                                           512);
           if constexpr (T::kF16)
             umma_f16(tmem, adesc, bdesc, T::IDESC, (kb | k) != 0);
           else
@@ -487,12 +492,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             if constexpr (T::kSwiglu)
               tma_load_2d(raw_stage(r) + T::RAW_BOX_BYTES, &tm_u, kk, m0, full);
           }
-          if constexpr (T::kXformB) {
-            // TF32: one raw stage per k-block (t == kb); W runs of 32 columns
-#pragma unroll
-            for (int j = 0; j < BN / 32; ++j)
-              tma_load_2d(raw_stage(r) + T::RAW_A_BYTES + j * 4096, &tm_w, n0 + j * 32, kk, full);
-          }
         }
         __syncwarp();
         filled = t + 1;
@@ -526,9 +525,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           transpose_swiglu_tile<T::BM>(a_stage(st), raw_stage(r),
                                        raw_stage(r) + T::RAW_BOX_BYTES, q, lane);
         else if constexpr (T::kTransA)
-          transpose_w_tile<T::BM>(a_stage(st), raw_stage(r), q, lane);
+          transpose_tile<T::BM>(a_stage(st), raw_stage(r), q, lane);
         else if constexpr (T::kXformA) transform_raw_stage<AMODE>(a_stage(st), raw_stage(r), h, tid);
-        if constexpr (T::kXformB) transpose_w_tile<BN>(b_stage(st), raw_stage(r) + T::RAW_A_BYTES, q, lane);
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(T::BAR_RAW_EMPTY + r));
       }

@@ -45,6 +45,9 @@
 #ifndef LIN_XF_WARPS
 #define LIN_XF_WARPS 8
 #endif
+#ifndef LIN_W_STAGES
+#define LIN_W_STAGES 4
+#endif
 
 namespace lin {
 
@@ -114,39 +117,54 @@ struct ClusterTraits {
   static constexpr uint32_t B_ATOM_BYTES = kBT ? BN * 128 : BK * 128;
   static constexpr uint32_t B_BYTES = W_BOXES * B_ATOM_BYTES;
 
-  static constexpr uint32_t OP_STAGE_BYTES = A_BYTES + B_BYTES;
+  // Split rings: the SwiGLU form in clusters, whose A stage makes the
+  // longest round trip. A stage of its W ring is refilled as soon as this
+  // CTA's UMMA has read it (a TMA load from L2: a round trip of about three
+  // k-blocks of UMMA time); a stage of its A ring only once every CTA of the
+  // cluster has read its copy, and then takes the transform's store and the
+  // copies to the peers (about five k-blocks). So its W ring keeps
+  // LIN_W_STAGES stages, one full and one empty barrier each, and its A ring
+  // takes what shared memory is left. Every other form keeps one ring: a
+  // stage of A and of W share one full barrier (the W tile's TMA bytes, the
+  // transform group's arrivals, the peers' copied rows) and one empty
+  // barrier, so the UMMA thread waits and commits once per k-block (two
+  // rings measured slower there: 834 against 934 us on the gate/up pair).
+  static constexpr bool kSplit = kSwiglu && CN > 1;
 
-  // One operand ring; shared memory holds as many stages as fit (the round
-  // trip of a stage -- W load and peer copies, UMMA, commit to every CTA --
-  // is several UMMA k-blocks long). A stage has one full barrier: the W
-  // tile's TMA bytes, the arrivals of the transform group's warps and the
-  // peers' copied A rows all land on it, so the UMMA thread waits once per
-  // k-block. (Separate A and W rings of their own depths measured
-  // slower: two waits and two commits per k-block.)
+  // Epilogue staging: [32 rows][32 f32] swizzled buffers, EPI_BUFS per
+  // epilogue warp. R arrives in them by TMA, the accumulator is added in
+  // place and Y leaves by TMA store, so that the epilogue moves whole
+  // 128-byte lines instead of one 16-byte piece per row and lane. Two per
+  // warp, so that a chunk's R load (or the transposed product's SwiGLU
+  // backward's GATE and UP) overlaps the previous chunk's store; the split
+  // rings' form keeps one: with K = d_ff its epilogue has a long main loop
+  // to overlap, and the shared memory goes to its A ring.
+  static constexpr int EPI_BUFS = kSplit ? 1 : 2;
+  static constexpr uint32_t EPI_BUF_BYTES = kEpiRows * kEpiCols * 4;   // 4 KB
+  static constexpr uint32_t EPI_BYTES = 4 * EPI_BUFS * EPI_BUF_BYTES;
+
   static constexpr uint32_t SMEM_CAP = 232448;
   static constexpr uint32_t BAR_REGION = 1024;
   static constexpr uint32_t ALIGN_SLACK = 1024;
-  static constexpr uint32_t DATA_CAP = SMEM_CAP - BAR_REGION - ALIGN_SLACK;
-  static constexpr int NS_FIT = (int)((DATA_CAP - 4 * 2 * kEpiRows * kEpiCols * 4) / OP_STAGE_BYTES);
-  static constexpr int NS = NS_FIT > 8 ? 8 : NS_FIT;
+  static constexpr uint32_t DATA_CAP = SMEM_CAP - BAR_REGION - ALIGN_SLACK - EPI_BYTES;
+  static constexpr int NS_FIT = (int)(DATA_CAP / (A_BYTES + B_BYTES));
+  static constexpr int NW = kSplit ? LIN_W_STAGES : (NS_FIT > 8 ? 8 : NS_FIT);
+  static constexpr int NA_FIT = (int)((DATA_CAP - NW * B_BYTES) / A_BYTES);
+  static constexpr int NA = kSplit ? (NA_FIT > 8 ? 8 : NA_FIT) : NW;
 
-  // Epilogue staging: two [32 rows][32 f32] swizzled buffers per epilogue
-  // warp. R arrives in them by TMA, the accumulator is added in place and Y
-  // leaves by TMA store, so that the epilogue moves whole 128-byte lines
-  // instead of one 16-byte piece per row and lane.
-  static constexpr uint32_t EPI_BUF_BYTES = kEpiRows * kEpiCols * 4;   // 4 KB
-  static constexpr uint32_t EPI_BYTES = 4 * 2 * EPI_BUF_BYTES;
-
-  static constexpr uint32_t OFF_OP = 0;
-  static constexpr uint32_t OFF_EPI = NS * OP_STAGE_BYTES;
+  static constexpr uint32_t OFF_A = 0;
+  static constexpr uint32_t OFF_W = OFF_A + NA * A_BYTES;
+  static constexpr uint32_t OFF_EPI = OFF_W + NW * B_BYTES;
   static constexpr uint32_t OFF_BAR = OFF_EPI + EPI_BYTES;
   static constexpr uint32_t SMEM_BYTES = ALIGN_SLACK + OFF_BAR + BAR_REGION;
 
-  static constexpr int BAR_FULL = 0;
-  static constexpr int BAR_EMPTY = BAR_FULL + 8;         // every CTA's UMMA done with stage
-  static constexpr int BAR_ACC_FULL = BAR_EMPTY + 8;     // 2 accumulator buffers
+  static constexpr int BAR_AFULL = 0;
+  static constexpr int BAR_AEMPTY = BAR_AFULL + 8;       // every CTA's UMMA done with the A stage
+  static constexpr int BAR_WFULL = BAR_AEMPTY + 8;
+  static constexpr int BAR_WEMPTY = BAR_WFULL + 8;       // this CTA's UMMA done with the W stage
+  static constexpr int BAR_ACC_FULL = BAR_WEMPTY + 8;    // 2 accumulator buffers
   static constexpr int BAR_ACC_EMPTY = BAR_ACC_FULL + 2;
-  static constexpr int BAR_EPI = BAR_ACC_EMPTY + 2;      // R landed, 2 per epilogue warp
+  static constexpr int BAR_EPI = BAR_ACC_EMPTY + 2;      // R landed, EPI_BUFS per epilogue warp
   static constexpr int BAR_COUNT = BAR_EPI + 8;
   static constexpr uint32_t OFF_TMEM_SLOT = BAR_COUNT * 8;
   static constexpr uint32_t OFF_ABORT = OFF_TMEM_SLOT + 4;
@@ -167,10 +185,11 @@ struct ClusterTraits {
   // reaching use u of a stage must already have seen use u-1's UMMA
   // complete, true when its previous k-block (XF_GROUPS earlier) waited for
   // a UMMA no older than the stage's use before last.
-  static_assert(XF_GROUPS <= NS, "ring depth vs transform groups");
-  static_assert(NS >= 2 && NS <= 8, "ring depth");
+  static_assert(XF_GROUPS <= NA, "ring depth vs transform groups");
+  static_assert(NA >= 2 && NA <= 8 && NW >= 2 && NW <= 8, "ring depths");
+  static_assert(kSplit || NA == NW, "one ring: A and W stages in step");
   static_assert(OFF_ABORT + 4 <= BAR_REGION, "barrier region");
-  static_assert(OP_STAGE_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "swizzle atoms");
+  static_assert(B_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "swizzle atoms");
   static_assert(SMEM_BYTES <= SMEM_CAP, "shared memory");
   static_assert(TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM columns");
   // A CTA holding all 512 TMEM columns must be alone on its SM (a second one
@@ -289,8 +308,8 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
   const int nkb = (args.K + T::BK - 1) / T::BK;
   const WaitCtl ctl{args.timeout_ns, abort_flag, args.status};
 
-  auto a_stage = [&](int s) -> uint32_t { return sbase + T::OFF_OP + s * T::OP_STAGE_BYTES; };
-  auto b_stage = [&](int s) -> uint32_t { return a_stage(s) + T::A_BYTES; };
+  auto a_stage = [&](int s) -> uint32_t { return sbase + T::OFF_A + s * T::A_BYTES; };
+  auto b_stage = [&](int s) -> uint32_t { return sbase + T::OFF_W + s * T::B_BYTES; };
   auto tile_m0 = [&](int t) -> int {
     return tile_coords(t, num_m, num_ng, args.band_ng).m * T::BM;
   };
@@ -318,11 +337,17 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
 
   // ---- set-up
   if (threadIdx.x == 0) {
-    for (int s = 0; s < T::NS; ++s) {
-      // the producer, and the transform group's warps
-      mbar_init(bar(T::BAR_FULL + s), T::kTmaA ? 1 : 1 + T::XF_PER_GROUP);
-      mbar_init(bar(T::BAR_EMPTY + s), CN);        // every CTA's UMMA commit
+    for (int s = 0; s < T::NA; ++s) {
+      // the transform group's warps, and with one ring the producer (its
+      // W bytes, or a binary16 A and W from global memory)
+      mbar_init(bar(T::BAR_AFULL + s), T::kTmaA ? 1 : (T::kSplit ? 0 : 1) + T::XF_PER_GROUP);
+      mbar_init(bar(T::BAR_AEMPTY + s), CN);       // every CTA's UMMA commit
     }
+    if constexpr (T::kSplit)
+      for (int s = 0; s < T::NW; ++s) {
+        mbar_init(bar(T::BAR_WFULL + s), 1);       // the producer's TMA bytes
+        mbar_init(bar(T::BAR_WEMPTY + s), 1);      // this CTA's UMMA commit
+      }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(T::BAR_ACC_FULL + b), 1);
       mbar_init(bar(T::BAR_ACC_EMPTY + b), 4);
@@ -373,18 +398,22 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
       const int n0 = tile_n0(t);
       const int kb1 = item_kb1(i);
       for (int kb = item_kb0(i); kb < kb1; ++kb, ++g) {
-        const int s = g % T::NS;
-        if (g >= T::NS) {
+        // one ring: the stage's single barriers (every CTA's UMMA done with
+        // it; its TMA bytes, A's too when A comes from global memory)
+        const int s = g % T::NW;
+        const uint32_t wempty = bar((T::kSplit ? T::BAR_WEMPTY : T::BAR_AEMPTY) + s);
+        const uint32_t full = bar((T::kSplit ? T::BAR_WFULL : T::BAR_AFULL) + s);
+        if (g >= T::NW) {
           bool w = true;
-          if (lane == 0) w = wait_phase_cluster(bar(T::BAR_EMPTY + s), ((g / T::NS) - 1) & 1, ctl);
+          if (lane == 0)
+            w = T::kSplit ? wait_phase(wempty, ((g / T::NW) - 1) & 1, ctl)
+                          : wait_phase_cluster(wempty, ((g / T::NW) - 1) & 1, ctl);
           if (!__shfl_sync(0xffffffffu, w ? 1 : 0, 0)) {
             ok = false;
             break;
           }
         }
         if (lane == 0) {
-          const uint32_t full = bar(T::BAR_FULL + s);
-          // with a binary16 A in global memory the A stage lands here too
           mbar_arrive_expect_tx(full, T::B_BYTES + (T::kTmaA ? T::A_BYTES : 0u));
           if constexpr (T::kBT) {
             tma_load_2d(b_stage(s), &tm_w, kb * T::BK, n0, full);   // W as [N][K]
@@ -406,9 +435,11 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
         __syncwarp();
       }
     }
+    // no TMA load of ours may still be in flight when the CTA leaves
     if (lane == 0)
-      for (int x = (g > T::NS ? g - T::NS : 0); x < g; ++x)
-        wait_phase(bar(T::BAR_FULL + x % T::NS), (x / T::NS) & 1, ctl, false);
+      for (int x = (g > T::NW ? g - T::NW : 0); x < g; ++x)
+        wait_phase(bar((T::kSplit ? T::BAR_WFULL : T::BAR_AFULL) + x % T::NW), (x / T::NW) & 1,
+                   ctl, false);
     __syncwarp();
   } else if (warp == 1) {
     // ---------------- UMMA issuer
@@ -424,11 +455,12 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
       }
       const int kb0 = item_kb0(i), kb1 = item_kb1(i);
       for (int kb = kb0; kb < kb1; ++kb, ++g) {
-        const int s = g % T::NS;
-        const uint32_t ph = (g / T::NS) & 1;
+        const int sa = g % T::NA;
+        const int s = g % T::NW;
         bool w = true;
         if (lane == 0) {
-          w = wait_phase(bar(T::BAR_FULL + s), ph, ctl);
+          w = wait_phase(bar(T::BAR_AFULL + sa), (g / T::NA) & 1, ctl) &&
+              (!T::kSplit || wait_phase(bar(T::BAR_WFULL + s), (g / T::NW) & 1, ctl));
         }
         if (!__shfl_sync(0xffffffffu, w ? 1 : 0, 0)) {
           ok = false;
@@ -438,16 +470,17 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
           tc_fence_after_sync();
 #pragma unroll
           for (int k = 0; k < T::NMMA; ++k) {
-            const uint64_t adesc = umma_desc_sw128(a_stage(s) + k * 32, 16, 1024);
+            const uint64_t adesc = umma_desc_sw128(a_stage(sa) + k * 32, 16, 1024);
             const uint64_t bdesc =
                 T::kBT ? umma_desc_sw128(b_stage(s) + k * 32, 16, 1024)
                        : umma_desc_sw128(b_stage(s) + k * T::KSTEP * 128, T::B_ATOM_BYTES, 1024);
             umma_f16(d_tmem, adesc, bdesc, T::IDESC, kb != kb0 || k != 0);
           }
           if constexpr (CN > 1)
-            umma_commit_multicast(bar(T::BAR_EMPTY + s), T::CLUSTER_MASK);
+            umma_commit_multicast(bar(T::BAR_AEMPTY + sa), T::CLUSTER_MASK);
           else
-            umma_commit(bar(T::BAR_EMPTY + s));
+            umma_commit(bar(T::BAR_AEMPTY + sa));
+          if constexpr (T::kSplit) umma_commit(bar(T::BAR_WEMPTY + s));
         }
         __syncwarp();
       }
@@ -518,11 +551,11 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
           coords(gn, row0, k0);
           stage_load<T>(buf[d], args.A, args.U, row0, k0, args.M, args.K, tw, lane);
         }
-        const int s = g % T::NS;
-        if (g >= T::NS) {
+        const int s = g % T::NA;
+        if (g >= T::NA) {
           // Every CTA's UMMA is done with this stage: ours may be rewritten
           // and the peers' copies of it overwritten.
-          const bool w = wait_phase_cluster(bar(T::BAR_EMPTY + s), ((g / T::NS) - 1) & 1, ctl);
+          const bool w = wait_phase_cluster(bar(T::BAR_AEMPTY + s), ((g / T::NA) - 1) & 1, ctl);
           if (!__all_sync(0xffffffffu, w)) {
             ok = false;
             break;
@@ -531,19 +564,22 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
         stage_store<T>(a_stage(s), crank, tw, lane, vals);
         fence_proxy_async_smem();   // our rows -> visible to UMMA and to the copy engine
         __syncwarp();
-        if (lane == 0) {
-          const uint32_t full = bar(T::BAR_FULL + s);
+        {
+          const uint32_t full = bar(T::BAR_AFULL + s);
           if constexpr (CN > 1) {
-            // The peers' slices of this stage arrive as copy bytes on our barrier.
-            mbar_arrive_expect_tx(full, T::REMOTE_BYTES_PER_WARP);
-            const uint32_t src = a_stage(s) + slice_off;
-#pragma unroll
-            for (uint32_t dst = 0; dst < (uint32_t)CN; ++dst)
-              if (dst != crank)
-                bulk_copy_s2cluster(mapa_shared(src, dst), src, T::SLICE_BYTES,
-                                    mapa_shared(full, dst));
+            // The peers' slices of this stage arrive as copy bytes on our
+            // barrier; our slice goes to peer (crank + l) % CN from lane l,
+            // so that the copies are issued side by side (measured faster
+            // than lane 0 issuing them in turn).
+            if (lane == 0) mbar_arrive_expect_tx(full, T::REMOTE_BYTES_PER_WARP);
+            if (lane >= 1 && lane < CN) {
+              const uint32_t dst = (crank + (uint32_t)lane) % (uint32_t)CN;
+              const uint32_t src = a_stage(s) + slice_off;
+              bulk_copy_s2cluster(mapa_shared(src, dst), src, T::SLICE_BYTES,
+                                  mapa_shared(full, dst));
+            }
           } else {
-            mbar_arrive(full);
+            if (lane == 0) mbar_arrive(full);
           }
         }
         __syncwarp();
@@ -552,15 +588,15 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
     }
     // Every peer's commit for the final use of each stage must have landed
     // (they arrive on our barriers, and our copies read our shared memory)
-    // before this CTA may leave. The final uses are the CTA's last NS
+    // before this CTA may leave. The final uses are the CTA's last NA
     // k-blocks, whichever group filled them: waiting instead for this
     // group's own last ones could ask for a phase of a stage that the other
     // group has since used again, whose parity then reads as not yet
     // complete. After a failure, the k-blocks this group reached.
     const int g_last = ok ? total : g_end;
     if (lane == 0)
-      for (int x = (g_last > T::NS ? g_last - T::NS : 0); x < g_last; ++x)
-        wait_phase_cluster(bar(T::BAR_EMPTY + x % T::NS), (x / T::NS) & 1, ctl, false);
+      for (int x = (g_last > T::NA ? g_last - T::NA : 0); x < g_last; ++x)
+        wait_phase_cluster(bar(T::BAR_AEMPTY + x % T::NA), (x / T::NA) & 1, ctl, false);
     __syncwarp();
     }
   } else if (warp >= 4 + T::XF_WARPS) {
@@ -568,16 +604,22 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
     const int q = warp & 3;                        // TMEM lane quadrant
     constexpr int NC = T::BN / kEpiCols;
     constexpr int C4 = T::BN / 4;                  // float4 columns of a tile
-    const uint32_t buf0 = sbase + T::OFF_EPI + (uint32_t)(q * 2) * T::EPI_BUF_BYTES;
+    constexpr uint32_t NB = (uint32_t)T::EPI_BUFS;
+    const uint32_t buf0 = sbase + T::OFF_EPI + (uint32_t)q * NB * T::EPI_BUF_BYTES;
     auto buf = [&](uint32_t b) -> uint32_t { return buf0 + b * T::EPI_BUF_BYTES; };
-    auto ebar = [&](uint32_t b) -> uint32_t { return bar(T::BAR_EPI + q * 2 + (int)b); };
+    auto ebar = [&](uint32_t b) -> uint32_t { return bar(T::BAR_EPI + q * (int)NB + (int)b); };
     // Chunks of 32 columns this warp has staged so far (across tiles): chunk
-    // e uses buffer e & 1 and, for R, phase (e >> 1) & 1 of that buffer's
+    // e uses buffer e % NB and, for R, phase (e / NB) & 1 of that buffer's
     // barrier. R loads are issued and waited for in chunk order: r_issued /
     // r_done count them, e_wait is the chunk of the next one to wait for.
+    // With two buffers the R of chunk e+1 is loaded while chunk e is worked
+    // on; with one, after chunk e's store has read the buffer.
+    auto ebuf = [&](uint32_t e) -> uint32_t { return e % NB; };
+    auto ephase = [&](uint32_t e) -> uint32_t { return (e / NB) & 1u; };
     uint32_t ec = 0, r_issued = 0, r_done = 0, e_wait = 0;
-    // SwiGLU-backward epilogue: GATE and UP of a chunk land in this warp's
-    // two buffers together (barrier BAR_EPI + 2q, one phase per chunk)
+    // SwiGLU-backward epilogue (two buffers): GATE and UP of a chunk land in
+    // this warp's two buffers together (barrier BAR_EPI + 2q, one phase per
+    // chunk)
     uint32_t sw_issued = 0, sw_done = 0;
     bool ok = true;
     for (int i = 0; i < n_items && ok; ++i) {
@@ -596,8 +638,8 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
       if (RESID && staged && lane == 0) {
         // R of the first chunk, into a buffer whose last store has read it
         bulk_wait_group_read<0>();
-        mbar_arrive_expect_tx(ebar(ec & 1), T::EPI_BUF_BYTES);
-        tma_load_2d(buf(ec & 1), &tm_r, n0, row0, ebar(ec & 1));
+        mbar_arrive_expect_tx(ebar(ebuf(ec)), T::EPI_BUF_BYTES);
+        tma_load_2d(buf(ebuf(ec)), &tm_r, n0, row0, ebar(ebuf(ec)));
         ++r_issued;
       }
       ok = warp_wait_phase(bar(T::BAR_ACC_FULL + ab), (i >> 1) & 1, ctl);
@@ -622,7 +664,7 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
                 make_float4(__uint_as_float(v[4 * j + 0]), __uint_as_float(v[4 * j + 1]),
                             __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
         }
-      } else if (staged && (args.flags & KFLAG_SWIGLU_BWD)) {
+      } else if (staged && NB == 2 && (args.flags & KFLAG_SWIGLU_BWD)) {
         // dA -> dGATE, dUP: GATE and UP arrive by TMA in the two buffers,
         // the gradients replace them there and leave by TMA store
         const uint32_t bg = buf(0), bu = buf(1);
@@ -681,13 +723,13 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
         float rm = -INFINITY, rs = 0.0f;
         for (int c = 0; c < nct && ok; ++c) {
           const uint32_t e = ec + (uint32_t)c;
-          const uint32_t b = e & 1u;
+          const uint32_t b = ebuf(e);
           // DUAL: chunk c < nc is Y's, else Y2's; its TMEM columns follow
           // the B stage ([W tile | W2 tile])
           const bool second = T::kDual && c >= nc;
           const int oc = second ? c - nc : c;                       // chunk of its output
           const int tc = second ? NC / 2 + oc : c;                  // chunk of the accumulator
-          if (lane == 0 && c + 1 < nct) {
+          if (NB == 2 && lane == 0 && c + 1 < nct) {
             // the other buffer's last store must have read it before it is
             // refilled (or, without R, rewritten below)
             bulk_wait_group_read<0>();
@@ -702,13 +744,13 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
           tmem_ld_32x32b_x32(acc + (uint32_t)(tc * kEpiCols), v);
           tmem_wait_ld();
           if constexpr (RESID) {
-            if (!warp_wait_phase(ebar(b), (e >> 1) & 1u, ctl)) {
+            if (!warp_wait_phase(ebar(b), ephase(e), ctl)) {
               ok = false;
               break;
             }
             ++r_done;
             e_wait = e + 1;
-          } else if (c == 0 && lane == 0) {
+          } else if ((NB == 1 || c == 0) && lane == 0) {
             bulk_wait_group_read<0>();   // this buffer's last store has read it
           }
           __syncwarp();
@@ -750,6 +792,13 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
           if (lane == 0) {
             tma_store_2d(second ? &tm_y2 : &tm_y, n0 + oc * kEpiCols, row0, buf(b));
             bulk_commit_group();
+            if (RESID && NB == 1 && c + 1 < nct) {
+              // the single buffer: the next chunk's R once this store has read it
+              bulk_wait_group_read<0>();
+              mbar_arrive_expect_tx(ebar(0), T::EPI_BUF_BYTES);
+              tma_load_2d(buf(0), &tm_r, n0 + (c + 1) * kEpiCols, row0, ebar(0));
+              ++r_issued;
+            }
           }
           __syncwarp();
         }
@@ -768,7 +817,7 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
       // up) or with a store still reading the buffers or writing Y.
       for (uint32_t x = 0; x < r_issued - r_done; ++x) {
         const uint32_t e = e_wait + x;   // the outstanding loads, oldest first
-        wait_phase(ebar(e & 1u), (e >> 1) & 1u, ctl, false);
+        wait_phase(ebar(ebuf(e)), ephase(e), ctl, false);
       }
       if (sw_issued > sw_done) wait_phase(ebar(0), sw_done & 1u, ctl, false);
       bulk_wait_group_all();

@@ -394,6 +394,21 @@ __host__ __device__ constexpr uint64_t umma_desc_sw128(uint32_t saddr, uint32_t 
          ((uint64_t)2 << 61);
 }
 
+// UMMA shared-memory descriptor for an MN-major operand of 4-byte elements
+// (kind::tf32) in the 128-byte swizzle with 32-byte atoms (layout type 1):
+// rows of 128 bytes along M/N, the 32-byte piece j of row r stored at
+// position j XOR (r mod 4), which is what a TMA load with
+// CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B writes. LBO is the offset between
+// 128-byte runs along M/N, SBO between 4-row groups along K (512 bytes when
+// the rows are packed). (With the 16-byte-atom layout of umma_desc_sw128 an
+// MN-major TF32 operand reads as zeros.)
+__host__ __device__ constexpr uint64_t umma_desc_sw128_atom32(uint32_t saddr, uint32_t lbo_bytes,
+                                                              uint32_t sbo_bytes) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46) |
+         ((uint64_t)1 << 61);
+}
+
 // UMMA instruction descriptor for kind::f16 / kind::tf32 with f32 accumulator.
 //   bits 4-5 D format (1: f32); bits 7-9 A format, 10-12 B format
 //   (f16: 0, tf32: 2); bit 15 A major, bit 16 B major (0: K-major, 1: MN-major);
