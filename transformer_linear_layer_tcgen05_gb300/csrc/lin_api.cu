@@ -396,9 +396,13 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
   const CUtensorMapDataType f32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   bool ok = true;
   const float* a_src = swiglu ? p.G : p.X;
-  if (p.at) {   // X^T: X is [K rows][M], transposed on chip from [32 x 32] boxes
-    ok &= encode_2d(&maps.a, f32, a_src, M, K, M * 4, 32, 32);
-    if (swiglu) ok &= encode_2d(&maps.u, f32, p.U, M, K, M * 4, 32, 32);
+  if (p.at) {   // X^T: X is [K rows][M] in [32 x 32] boxes
+    if (swiglu) {   // GATE, UP: transformed and transposed on chip
+      ok &= encode_2d(&maps.a, f32, a_src, M, K, M * 4, 32, 32);
+      ok &= encode_2d(&maps.u, f32, p.U, M, K, M * 4, 32, 32);
+    } else {        // X: an MN-major TF32 operand as it is (32-byte atoms)
+      ok &= encode_2d(&maps.a, f32, a_src, M, K, M * 4, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B);
+    }
   } else if (cn == 0) {   // the clustered kernels load X / GATE / UP without tensor maps
     ok &= encode_2d(&maps.a, f32, a_src, K, M, K * 4, 32, lin::kBM);
     if (swiglu) ok &= encode_2d(&maps.u, f32, p.U, K, M, K * 4, 32, lin::kBM);

@@ -44,9 +44,13 @@ struct GemmTraits {
   static constexpr bool kSwiglu =
       (AMODE == A_SWIGLU_F32 || AMODE == A_SWIGLU_F16 || AMODE == A_TRANS_SWIGLU_F32);
   static constexpr bool kResid = RESID;
-  // The A operand is built by the transform warps unless X is copied as is.
-  static constexpr bool kXformA = (AMODE != A_TMA_F32);
+  // The A operand is built by the transform warps unless X is copied as is:
+  // K-major (X), or MN-major for the weight gradient's X^T (X [M][K] read as
+  // [contraction][tile rows], a TF32 operand in the 128-byte swizzle with
+  // 32-byte atoms).
+  static constexpr bool kXformA = (AMODE != A_TMA_F32 && AMODE != A_TRANS_F32);
   static constexpr bool kTransA = (AMODE == A_TRANS_F32 || AMODE == A_TRANS_SWIGLU_F32);  // A = X^T
+  static constexpr bool kAmn = (AMODE == A_TRANS_F32);   // A copied MN-major
   // W [K,N] (N contiguous) is consumed MN-major straight from TMA: binary16
   // in the 128-byte swizzle, f32 (TF32) in the 128-byte swizzle with 32-byte
   // atoms (the layout an MN-major TF32 operand needs).
@@ -118,7 +122,7 @@ struct GemmTraits {
 
   static constexpr uint32_t TMEM_COLS = BN;
   static constexpr uint32_t IDESC =
-      umma_idesc(kF16 ? 0u : 2u, /*a_mn_major=*/false, /*b_mn_major=*/!BT, BM, BN);
+      umma_idesc(kF16 ? 0u : 2u, /*a_mn_major=*/kAmn, /*b_mn_major=*/!BT, BM, BN);
 
   static_assert(NS >= 2, "operand ring needs two stages");
   static_assert(NS * OP_STAGE_BYTES >= BM * BN * 4, "a cluster split's partial tile in the ring");
@@ -408,7 +412,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t full = bar(T::BAR_OP_TMA + st);
           mbar_arrive_expect_tx(full, T::OP_TMA_BYTES);
           const int kk = (kb0 + kb) * T::BK;
-          if constexpr (!T::kXformA) tma_load_2d(a_stage(st), &tm_a, kk, m0, full);
+          if constexpr (T::kAmn) {
+            // X^T: BM/32 boxes of [32 rows of the contraction][32 of the tile's rows]
+#pragma unroll
+            for (int j = 0; j < T::BM / 32; ++j)
+              tma_load_2d(a_stage(st) + j * 4096, &tm_a, m0 + j * 32, kk, full);
+          } else if constexpr (!T::kXformA) {
+            tma_load_2d(a_stage(st), &tm_a, kk, m0, full);
+          }
           if constexpr (T::kBT) {
             // W as [N][K]: the tile's BN rows, this k-block's 128 bytes
             tma_load_2d(b_stage(st), &tm_w, kk, n0, full);
@@ -439,7 +450,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after_sync();
 #pragma unroll
         for (int k = 0; k < T::NMMA; ++k) {
-          const uint64_t adesc = umma_desc_sw128(a_stage(st) + k * 32, 16, 1024);
+          // K-major A: a K step is 32 bytes along the row; MN-major X^T: KSTEP
+          // rows of 128 bytes, runs of 32 tile rows 4096 bytes apart
+          const uint64_t adesc =
+              T::kAmn ? umma_desc_sw128_atom32(a_stage(st) + k * T::KSTEP * 128, 4096, 512)
+                      : umma_desc_sw128(a_stage(st) + k * 32, 16, 1024);
           // W given as [N][K]: K-major. Else MN-major: a K step is KSTEP rows
           // of 128 bytes further; runs of W_ATOM columns B_ATOM_BYTES apart;
           // 8-row (binary16) or 4-row (TF32, 32-byte atoms) groups along K.

@@ -18,7 +18,7 @@ enum AMode : int {
   A_SWIGLU_F32 = 2,  // GATE, UP staged by TMA; silu(GATE) * UP written as f32 (TF32 MMA)
   A_SWIGLU_F16 = 3,  // GATE, UP staged by TMA; silu(GATE) * UP rounded to binary16
   A_TMA_F16 = 4,     // X rounded to binary16 by a pre-pass, copied by TMA (clustered kernels)
-  A_TRANS_F32 = 5,   // A = X^T (the weight gradient X^T dY): TMA-staged [32 m][32 k] tiles
+  A_TRANS_F32 = 5,   // A = X^T (the weight gradient X^T dY): MN-major TF32 operand by TMA
                      // of X transposed on chip into the K-major TF32 operand
   A_TRANS_SWIGLU_F32 = 6,  // A = (silu(GATE) * UP)^T, recomputed from staged GATE/UP tiles
                            // and transposed on chip (the weight gradient of W_down)
