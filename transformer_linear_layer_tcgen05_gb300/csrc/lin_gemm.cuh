@@ -255,57 +255,78 @@ __device__ __forceinline__ uint32_t csplit_off(int r, int c4) {
 }
 
 // The sum of a cluster split: CTA `rank` of the S takes its share of the
-// tile's 128 x BN/4 float4s (row-major, so that the 128 threads touch
+// tile's 128 x BN/4 float4s (row-major, so that consecutive threads touch
 // consecutive columns of a row) and adds the S partials in K order (rank 0
 // first, as the split sum kernel does), then the residual or the SwiGLU
-// backward, and writes Y (and Y2) with 16-byte global stores.
+// backward, and writes Y (and Y2) with 16-byte global stores. Every warp of
+// the CTA takes part (the roles are done by now), and each thread has two
+// outputs' partials and residual rows in flight before the first add: the
+// sum is a chain of distributed-shared-memory and global round trips, and
+// with four warps and one output at a time it took longer than the main
+// loop on the 512-token shapes.
 template <typename T>
 __device__ __forceinline__ void cluster_split_sum(uint32_t part, int S, int rank, int tid,
-                                                  int m0, int n0, const KernelArgs& args) {
+                                                  int nthreads, int m0, int n0,
+                                                  const KernelArgs& args) {
   constexpr int C4 = T::BN / 4;
   constexpr int TOTAL = T::BM * C4;
   const int beg = rank * TOTAL / S, end = (rank + 1) * TOTAL / S;
   const bool swb = (args.flags & KFLAG_SWIGLU_BWD) != 0;
-  for (int idx = beg + tid; idx < end; idx += 128) {
-    const int r = idx / C4, c4 = idx % C4;
-    const int row = m0 + r, col = n0 + 4 * c4;
-    if (row >= args.M || col >= args.N) continue;
-    const uint32_t off = part + csplit_off<T>(r, c4);
-    float4 v[kMaxClusterSplit];
+  for (int idx0 = beg + tid; idx0 < end; idx0 += 2 * nthreads) {
+    float4 v[2][kMaxClusterSplit];
+    float4 rv[2], gt[2], up[2];
+    bool live[2];
+    size_t o[2];
 #pragma unroll
-    for (int p = 0; p < kMaxClusterSplit; ++p)
-      if (p < S) v[p] = ld_cluster_v4f(mapa_shared(off, (uint32_t)p));
-    float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < 2; ++j) {
+      const int idx = idx0 + j * nthreads;
+      const int r = idx / C4, c4 = idx % C4;
+      const int row = m0 + r, col = n0 + 4 * c4;
+      live[j] = idx < end && row < args.M && col < args.N;
+      o[j] = live[j] ? (size_t)row * (size_t)args.N + (size_t)col : 0;
+      if (!live[j]) continue;
+      const uint32_t off = part + csplit_off<T>(r, c4);
 #pragma unroll
-    for (int p = 0; p < kMaxClusterSplit; ++p) {
-      if (p < S) {
-        sum.x += v[p].x;
-        sum.y += v[p].y;
-        sum.z += v[p].z;
-        sum.w += v[p].w;
+      for (int p = 0; p < kMaxClusterSplit; ++p)
+        if (p < S) v[j][p] = ld_cluster_v4f(mapa_shared(off, (uint32_t)p));
+      if (swb) {
+        gt[j] = *reinterpret_cast<const float4*>(args.G2 + o[j]);
+        up[j] = *reinterpret_cast<const float4*>(args.U2 + o[j]);
+      } else if constexpr (T::kResid) {
+        rv[j] = *reinterpret_cast<const float4*>(args.R + o[j]);
       }
     }
-    const size_t o = (size_t)row * (size_t)args.N + (size_t)col;
-    if (swb) {   // the SwiGLU backward of the summed dA
-      const float4 gt = *reinterpret_cast<const float4*>(args.G2 + o);
-      const float4 up = *reinterpret_cast<const float4*>(args.U2 + o);
-      float4 dg, du;
-      swiglu_backward(sum.x, gt.x, up.x, dg.x, du.x);
-      swiglu_backward(sum.y, gt.y, up.y, dg.y, du.y);
-      swiglu_backward(sum.z, gt.z, up.z, dg.z, du.z);
-      swiglu_backward(sum.w, gt.w, up.w, dg.w, du.w);
-      *reinterpret_cast<float4*>(args.Y + o) = dg;
-      *reinterpret_cast<float4*>(args.Y2 + o) = du;
-      continue;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      if (!live[j]) continue;
+      float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int p = 0; p < kMaxClusterSplit; ++p) {
+        if (p < S) {
+          sum.x += v[j][p].x;
+          sum.y += v[j][p].y;
+          sum.z += v[j][p].z;
+          sum.w += v[j][p].w;
+        }
+      }
+      if (swb) {   // the SwiGLU backward of the summed dA
+        float4 dg, du;
+        swiglu_backward(sum.x, gt[j].x, up[j].x, dg.x, du.x);
+        swiglu_backward(sum.y, gt[j].y, up[j].y, dg.y, du.y);
+        swiglu_backward(sum.z, gt[j].z, up[j].z, dg.z, du.z);
+        swiglu_backward(sum.w, gt[j].w, up[j].w, dg.w, du.w);
+        *reinterpret_cast<float4*>(args.Y + o[j]) = dg;
+        *reinterpret_cast<float4*>(args.Y2 + o[j]) = du;
+        continue;
+      }
+      if constexpr (T::kResid) {
+        sum.x += rv[j].x;
+        sum.y += rv[j].y;
+        sum.z += rv[j].z;
+        sum.w += rv[j].w;
+      }
+      *reinterpret_cast<float4*>(args.Y + o[j]) = sum;
     }
-    if constexpr (T::kResid) {
-      const float4 rv = *reinterpret_cast<const float4*>(args.R + o);
-      sum.x += rv.x;
-      sum.y += rv.y;
-      sum.z += rv.z;
-      sum.w += rv.w;
-    }
-    *reinterpret_cast<float4*>(args.Y + o) = sum;
   }
 }
 
@@ -723,9 +744,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before_sync();
   if (csplit) {
     cluster_sync_all();
-    if (warp >= 4 && !withhold)
-      cluster_split_sum<T>(sbase + T::OFF_OP, (int)gridDim.z, (int)blockIdx.z,
-                           (int)threadIdx.x - 128, m0, n0, args);
+    if (!withhold)
+      cluster_split_sum<T>(sbase + T::OFF_OP, (int)gridDim.z, (int)blockIdx.z, (int)threadIdx.x,
+                           (int)blockDim.x, m0, n0, args);
     cluster_sync_all();
   } else {
     __syncthreads();
