@@ -44,7 +44,7 @@ __device__ __forceinline__ float block_reduce(float v, float* sh) {
 
 }  // namespace
 
-__global__ void __launch_bounds__(kLossThreads)
+__global__ void __launch_bounds__(kLossThreads, 4)
     lin_cross_entropy_kernel(float* __restrict__ logits, const float2* __restrict__ stats,
                              int stats_cols, const int32_t* __restrict__ targets,
                              float* __restrict__ losses, int V, float alpha, float beta,
@@ -57,12 +57,28 @@ __global__ void __launch_bounds__(kLossThreads)
   float* row = logits + (size_t)s * (size_t)V;
   float4* row4 = reinterpret_cast<float4*>(row);
   const int V4 = V / 4;   // V % 4 == 0
+  // The thread's float4s of the row, kChunk at a time, in registers. The
+  // first chunk is requested with the target index, before anything else,
+  // so that its loads are in flight while the target logit and the row's
+  // statistics are fetched and combined. (kChunk = 8 keeps four of these
+  // CTAs resident per SM, so every row's CTA runs at once at M = 512.)
+  constexpr int kChunk = 8;
+  float4 l[kChunk];
+  auto load_chunk = [&](int v0) {
+#pragma unroll
+    for (int u = 0; u < kChunk; ++u) {
+      const int v = v0 + u * kLossThreads;
+      if (v < V4) l[u] = row4[v];
+    }
+  };
   const int tgt = targets[s];
+  load_chunk(tid);
   if (tgt < 0 || tgt >= V) {   // ignored row (padding): loss 0, dLogits 0
     for (int v = tid; v < V4; v += kLossThreads) row4[v] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (tid == 0) losses[s] = 0.0f;
     return;
   }
+  const float l_t = row[tgt];
   // phases 1 and 2a: row max and sum of exp(l - max)
   float row_max, denom;
   if (stats) {
@@ -91,7 +107,7 @@ __global__ void __launch_bounds__(kLossThreads)
     denom = block_reduce<false>(d, sh);
   }
   // phase 3 needs the target logit before phase 4 overwrites the row
-  const float l_t = row[tgt];
+  // (requested before the statistics were combined, above)
   __syncthreads();
   const float dg = fmaxf(denom, 1e-30f);
   const float inv_denom = 1.0f / dg;
@@ -99,20 +115,13 @@ __global__ void __launch_bounds__(kLossThreads)
   const float inv_V = 1.0f / (float)V;
   const float zl = 2.0f * beta * lse;
   const float smooth = alpha * inv_V;
-  // phase 4: dLogits in place (and the sum of the logits for smoothing);
-  // kUnroll of the thread's float4s are loaded before any is rewritten, so
-  // that as many loads are in flight
-  constexpr int kUnroll = 4;
+  // phase 4: dLogits in place (and the sum of the logits for smoothing),
+  // chunk by chunk from registers (every load of a chunk in flight at once)
   float sum_l = 0.0f;
-  for (int v0 = tid; v0 < V4; v0 += kUnroll * kLossThreads) {
-    float4 l[kUnroll];
+  for (int v0 = tid; v0 < V4; v0 += kChunk * kLossThreads) {
+    if (v0 != tid) load_chunk(v0);
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int v = v0 + u * kLossThreads;
-      if (v < V4) l[u] = row4[v];
-    }
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
+    for (int u = 0; u < kChunk; ++u) {
       const int v = v0 + u * kLossThreads;
       if (v >= V4) break;
       sum_l += (l[u].x + l[u].y) + (l[u].z + l[u].w);
