@@ -424,10 +424,15 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
   }
   if (resid) ok &= encode_2d(&maps.r, f32, p.R, N, M, N * 4, lin::kEpiCols, lin::kEpiRows);
   ok &= encode_2d(&maps.y, f32, p.Y, N, M, N * 4, lin::kEpiCols, lin::kEpiRows);
-  if (swb) {   // the SwiGLU-backward epilogue's GATE, UP in and dUP out
-    ok &= encode_2d(&maps.g2, f32, p.G2, N, M, N * 4, lin::kEpiCols, lin::kEpiRows);
-    ok &= encode_2d(&maps.u2, f32, p.U2, N, M, N * 4, lin::kEpiCols, lin::kEpiRows);
-    ok &= encode_2d(&maps.y2, f32, p.Y2, N, M, N * 4, lin::kEpiCols, lin::kEpiRows);
+  if (swb) {   // the SwiGLU-backward epilogue's GATE, UP in and dGATE, dUP out:
+    // [32 x 32] boxes (per-tile kernel), or [32 rows x 16] with the 64-byte
+    // swizzle (clustered kernel, four tiles per warp)
+    const uint32_t sc = cn > 0 ? (uint32_t)lin::kSwbCols : (uint32_t)lin::kEpiCols;
+    const CUtensorMapSwizzle sz = cn > 0 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
+    ok &= encode_2d(&maps.g2, f32, p.G2, N, M, N * 4, sc, lin::kEpiRows, sz);
+    ok &= encode_2d(&maps.u2, f32, p.U2, N, M, N * 4, sc, lin::kEpiRows, sz);
+    ok &= encode_2d(&maps.y2, f32, p.Y2, N, M, N * 4, sc, lin::kEpiRows, sz);
+    ok &= encode_2d(&maps.y, f32, p.Y, N, M, N * 4, sc, lin::kEpiRows, sz);
   }
   if (!ok) return cuda_fail(cudaErrorInvalidValue);
 

@@ -132,4 +132,12 @@ __device__ __forceinline__ uint32_t sw128(uint32_t r, uint32_t c) {
   return r * 128u + ((c ^ (r & 7u)) << 4);
 }
 
+// The same for a [rows][64 B] tile with the 64-byte swizzle (TMA
+// SWIZZLE_64B: 16-byte chunk index XOR address bits 7-8, i.e. (r / 2) mod 4).
+// A warp reading chunk c of 32 consecutive rows touches every bank once per
+// eight rows.
+__device__ __forceinline__ uint32_t sw64(uint32_t r, uint32_t c) {
+  return r * 64u + ((c ^ ((r >> 1) & 3u)) << 4);
+}
+
 }  // namespace lin

@@ -665,54 +665,75 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
                             __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
         }
       } else if (staged && NB == 2 && (args.flags & KFLAG_SWIGLU_BWD)) {
-        // dA -> dGATE, dUP: GATE and UP arrive by TMA in the two buffers,
-        // the gradients replace them there and leave by TMA store
-        const uint32_t bg = buf(0), bu = buf(1);
-        for (int c = 0; c < nc && ok; ++c) {
-          if (lane == 0) {
-            bulk_wait_group_read<0>();   // the last stores have read both buffers
-            mbar_arrive_expect_tx(ebar(0), 2 * T::EPI_BUF_BYTES);
-            tma_load_2d(bg, &tm_g2, n0 + c * kEpiCols, row0, ebar(0));
-            tma_load_2d(bu, &tm_u2, n0 + c * kEpiCols, row0, ebar(0));
-            ++sw_issued;
-            // the next chunk's GATE and UP on their way into L2, so that
-            // its loads, issued after this chunk's stores, hit there
-            // (16k-token shape: 640 -> 617 us; two chunks ahead 622, three
-            // 655)
-            if (c + 1 < nc) {
-              tma_prefetch_l2_2d(&tm_g2, n0 + (c + 1) * kEpiCols, row0);
-              tma_prefetch_l2_2d(&tm_u2, n0 + (c + 1) * kEpiCols, row0);
-            }
+        // dA -> dGATE, dUP in chunks of 16 columns. The warp's two 4 KB
+        // buffers hold four [32 rows][16 f32] tiles (64-byte swizzle): GATE
+        // and UP of a chunk land in the first two by TMA, the gradients leave
+        // from the other two by TMA store. The next chunk's GATE and UP are
+        // requested as soon as this chunk's are in registers, so they load
+        // while this chunk's gradients are stored (with one buffer pair
+        // doing both, every load waited for the previous chunk's stores).
+        constexpr int SC = kSwbCols;
+        constexpr uint32_t SB = (uint32_t)(kEpiRows * SC * 4);   // 2 KB
+        static_assert(2 * SB == T::EPI_BUF_BYTES, "four swizzled tiles in two buffers");
+        const uint32_t gin = buf(0), uin = buf(0) + SB, gout = buf(1), uout = buf(1) + SB;
+        int ns = n0 < args.N ? (args.N - n0 + SC - 1) / SC : 0;
+        if (ns > T::BNO / SC) ns = T::BNO / SC;
+        auto issue = [&](int c) {   // lane 0: GATE and UP of chunk c
+          mbar_arrive_expect_tx(ebar(0), 2 * SB);
+          tma_load_2d(gin, &tm_g2, n0 + c * SC, row0, ebar(0));
+          tma_load_2d(uin, &tm_u2, n0 + c * SC, row0, ebar(0));
+          ++sw_issued;
+          // the following chunk's GATE and UP on their way into L2
+          if (c + 1 < ns) {
+            tma_prefetch_l2_2d(&tm_g2, n0 + (c + 1) * SC, row0);
+            tma_prefetch_l2_2d(&tm_u2, n0 + (c + 1) * SC, row0);
           }
-          __syncwarp();
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(acc + (uint32_t)(c * kEpiCols), v);
+        };
+        if (lane == 0 && ns > 0) {
+          bulk_wait_group_read<0>();   // the last stores have read the input buffers too
+          issue(0);
+        }
+        __syncwarp();
+        for (int c = 0; c < ns && ok; ++c) {
+          uint32_t v[SC];
+          tmem_ld_32x32b_x16(acc + (uint32_t)(c * SC), v);
           tmem_wait_ld();
           if (!warp_wait_phase(ebar(0), sw_done & 1u, ctl)) {
             ok = false;
             break;
           }
           ++sw_done;
+          float4 dg[SC / 4], du[SC / 4];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint32_t off = sw128((uint32_t)lane, (uint32_t)j);
-            const float4 gt = ld_shared_v4f(bg + off);
-            const float4 up = ld_shared_v4f(bu + off);
-            float4 dg, du;
-            swiglu_backward(__uint_as_float(v[4 * j + 0]), gt.x, up.x, dg.x, du.x);
-            swiglu_backward(__uint_as_float(v[4 * j + 1]), gt.y, up.y, dg.y, du.y);
-            swiglu_backward(__uint_as_float(v[4 * j + 2]), gt.z, up.z, dg.z, du.z);
-            swiglu_backward(__uint_as_float(v[4 * j + 3]), gt.w, up.w, dg.w, du.w);
-            st_shared_v4(bg + off, __float_as_uint(dg.x), __float_as_uint(dg.y),
-                         __float_as_uint(dg.z), __float_as_uint(dg.w));
-            st_shared_v4(bu + off, __float_as_uint(du.x), __float_as_uint(du.y),
-                         __float_as_uint(du.z), __float_as_uint(du.w));
+          for (int j = 0; j < SC / 4; ++j) {
+            const uint32_t off = sw64((uint32_t)lane, (uint32_t)j);
+            const float4 gt = ld_shared_v4f(gin + off);
+            const float4 up = ld_shared_v4f(uin + off);
+            swiglu_backward(__uint_as_float(v[4 * j + 0]), gt.x, up.x, dg[j].x, du[j].x);
+            swiglu_backward(__uint_as_float(v[4 * j + 1]), gt.y, up.y, dg[j].y, du[j].y);
+            swiglu_backward(__uint_as_float(v[4 * j + 2]), gt.z, up.z, dg[j].z, du[j].z);
+            swiglu_backward(__uint_as_float(v[4 * j + 3]), gt.w, up.w, dg[j].w, du[j].w);
+          }
+          fence_proxy_async_smem();   // our reads of the inputs before the next loads land
+          __syncwarp();
+          if (lane == 0) {
+            if (c + 1 < ns) issue(c + 1);
+            bulk_wait_group_read<0>();   // the previous stores have read the output buffers
+          }
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < SC / 4; ++j) {
+            const uint32_t off = sw64((uint32_t)lane, (uint32_t)j);
+            st_shared_v4(gout + off, __float_as_uint(dg[j].x), __float_as_uint(dg[j].y),
+                         __float_as_uint(dg[j].z), __float_as_uint(dg[j].w));
+            st_shared_v4(uout + off, __float_as_uint(du[j].x), __float_as_uint(du[j].y),
+                         __float_as_uint(du[j].z), __float_as_uint(du[j].w));
           }
           fence_proxy_async_smem();   // staged gradients -> visible to the TMA stores
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(&tm_y, n0 + c * kEpiCols, row0, bg);
-            tma_store_2d(&tm_y2, n0 + c * kEpiCols, row0, bu);
+            tma_store_2d(&tm_y, n0 + c * SC, row0, gout);
+            tma_store_2d(&tm_y2, n0 + c * SC, row0, uout);
             bulk_commit_group();
           }
           __syncwarp();

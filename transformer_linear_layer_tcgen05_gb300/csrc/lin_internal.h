@@ -149,6 +149,10 @@ cudaError_t launch_gemm_f16(int amode, bool resid, int bn, bool bt, const Tensor
 // read X (or GATE and UP) through KernelArgs::A/U and W through its tensor
 // map; R and Y through KernelArgs.
 constexpr int kClusterBN = 256;
+// Columns per chunk of the clustered kernel's SwiGLU-backward epilogue
+// ([32 rows][16 f32] tiles, 64-byte swizzle: GATE, UP in and dGATE, dUP out
+// in four 2 KB buffers per warp).
+constexpr int kSwbCols = 16;
 cudaError_t launch_gemm_cluster_swiglu(int cn, const TensorMaps& maps, const KernelArgs& args,
                                        cudaStream_t stream);
 cudaError_t launch_gemm_cluster_cvt(int cn, bool resid, const TensorMaps& maps,
