@@ -237,6 +237,24 @@ bool f16_preconvert(int num_ng) {
   return num_ng >= 2;
 }
 
+// Whether the pre-converted forms (binary16 A copied by TMA) run as CTA
+// pairs along M -- one UMMA of M = 256 over two CTAs (tcgen05
+// .cta_group::2), each CTA loading half of the tile's W columns -- rather
+// than single CTAs: when the 256-row tiles make at least two rounds over the
+// SMs' pairs. Measured (cold / warm us, single CTAs -> pairs): the 16k-token
+// dX 405 / 396 -> 371 / 364, the 16k-token gate/up pair 821 -> 723; on the
+// 512-token shapes (under two rounds) no gain: lm_head_w16 18.95 -> 19.14
+// warm. LIN_F16_PAIR=0 / 1 forces it off / on (measurements).
+bool f16_pair(long long pair_tiles, int sms) {
+  static const int forced = [] {
+    const char* v = std::getenv("LIN_F16_PAIR");
+    if (!v) return -1;
+    return std::strcmp(v, "0") == 0 ? 0 : (std::strcmp(v, "1") == 0 ? 1 : -1);
+  }();
+  if (forced >= 0) return forced == 1;
+  return pair_tiles >= (long long)sms;
+}
+
 enum Form : int { F_MATMUL = 0, F_RESID = 1, F_SWIGLU = 2 };
 
 // In the kernels' terms: Y[M,N] = A[M,K] · B[K,N] (+ R), A = X or
@@ -512,18 +530,29 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
     // Persistent launch: split the K range of the last partial round when
     // that keeps idle clusters busy.
     cudaError_t ce = cudaSuccess;
-    const int num_m = (int)((M + lin::kBM - 1) / lin::kBM);
     const int num_ng = (int)((N + (uint64_t)lin::kClusterBN * cn - 1) / ((uint64_t)lin::kClusterBN * cn));
     const int nkb = (int)((K + 63) / 64);
     // binary16 X from a pre-pass, in the workspace after the partial tiles
     bool tma_a = !swiglu && !fixed && K % 8 == 0 && f16_preconvert(num_ng);
     // With A already binary16 in global memory a CTA copies its own A tiles
-    // by TMA and has nothing to share: single CTAs on every SM (152 rather
-    // than 144 in clusters of four) measured faster at every shape (the
-    // 16k-token dX 447 -> 417 us, the gate/up pair 868 -> 821 us, the
-    // 512-token dX 39.1 -> 35.6 us). Clusters stay for the forms whose A is
-    // built on chip; a forced cluster size applies to those only.
-    if (tma_a) cn = 1;
+    // by TMA and has nothing to share along N: single CTAs on every SM (152
+    // rather than 144 in clusters of four) measured faster at every shape
+    // than clusters along N (the 16k-token dX 447 -> 417 us, the gate/up
+    // pair 868 -> 821 us, the 512-token dX 39.1 -> 35.6 us), and CTA pairs
+    // along M, sharing the W tile between two SMs, faster again. Clusters
+    // along N stay for the forms whose A is built on chip; a forced cluster
+    // size applies to those only.
+    bool pair = false;
+    if (tma_a) {
+      const long long bno_p = dual ? lin::kClusterBN / 2 : lin::kClusterBN;
+      const long long pair_tiles = (long long)((M + 2 * lin::kBM - 1) / (2 * lin::kBM)) *
+                                   (long long)((N + bno_p - 1) / bno_p);
+      pair = f16_pair(pair_tiles, sm_count(dev));
+      cn = pair ? 2 : 1;
+    }
+    const int cn_n = pair ? 1 : cn;                           // CTAs along N
+    const int tile_rows = pair ? 2 * lin::kBM : lin::kBM;     // rows of a cluster tile
+    const int num_m = (int)((M + tile_rows - 1) / tile_rows);
     auto capacity = [&]() {
       if (dual) return lin::cluster_capacity_dual(tma_a, cn, &ce);
       if (p.bt) return lin::cluster_capacity_bt(tma_a, cn, resid, &ce);
@@ -537,14 +566,14 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
     // (the dual product's tiles are split nowhere either: the split sum
     // writes one output)
     const int bno = dual ? lin::kClusterBN / 2 : lin::kClusterBN;
-    const int num_ng_o = (int)((N + (uint64_t)bno * cn - 1) / ((uint64_t)bno * cn));
+    const int num_ng_o = (int)((N + (uint64_t)bno * cn_n - 1) / ((uint64_t)bno * cn_n));
     lin::SplitPlan plan = (p.row_stats || dual) ? lin::SplitPlan{0, 0, 1}
                                                 : lin::split_plan(num_m * num_ng_o, cap, nkb);
     // Bands of column groups whose weights stay in L2 (every cluster tile
     // reads K x cn x 256 binary16 weights, both halves of the dual form
     // included), when the whole W would not fit.
     {
-      const long long per_ng = (long long)K * cn * lin::kClusterBN * 2;
+      const long long per_ng = (long long)K * cn_n * lin::kClusterBN * 2;
       const long long band = per_ng > 0 ? lin::kBandWeightBytes / per_ng : 0;
       args.band_ng = band >= 1 && band < num_ng_o ? (int)band : 0;
     }
@@ -556,6 +585,8 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
     if (got < 0) return LIN_ERROR_UNSUPPORTED_SHAPE;
     if (got == 0 && tma_a) {   // no memory for the pre-pass: transform X in the GEMM
       tma_a = false;
+      pair = false;
+      cn = 1;
       cap = capacity();
       if (cap < 1) return cuda_fail(ce);
     }
@@ -568,6 +599,11 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
       uint16_t* xh = reinterpret_cast<uint16_t*>(reinterpret_cast<char*>(args.part) + xh_off);
       if (!encode_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT16, xh, K, M, K * 2, 64,
                      (uint32_t)lin::kBM))
+        e = cudaErrorInvalidValue;
+      // a pair's CTA loads half of the tile's rows of W as [N][K]
+      else if (pair && p.bt &&
+               !encode_2d(&maps.w, CU_TENSOR_MAP_DATA_TYPE_UINT16, p.W, K, N, K * 2, 64,
+                          (uint32_t)lin::kClusterBN / 2))
         e = cudaErrorInvalidValue;
       else
         e = lin::launch_cvt_f16(p.X, xh, M * K, sm_count(dev), stream);
@@ -586,8 +622,8 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
     }
     if (e == cudaSuccess && args.split_s >= 2) {
       const int clusters = args.split_r > 0 ? cap : args.split_rem * args.split_s;
-      e = lin::launch_split_reduce(args, resid, cn, lin::kClusterBN, args.split_r * clusters,
-                                   num_ng_o, stream);
+      e = lin::launch_split_reduce(args, resid, cn, pair, lin::kClusterBN,
+                                   args.split_r * clusters, num_ng_o, stream);
       kernels += 1;
     }
   } else {
@@ -629,7 +665,7 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
                                        : (p.at ? lin::A_TRANS_F32 : lin::A_TMA_F32),
                                 resid, bn, p.bt, maps, args, stream);
     if (e == cudaSuccess && args.split_s >= 2 && !(args.flags & lin::KFLAG_CLUSTER_SPLIT)) {
-      e = lin::launch_split_reduce(args, resid, 1, bn, 0, tiles_n, stream);
+      e = lin::launch_split_reduce(args, resid, 1, false, bn, 0, tiles_n, stream);
       kernels = 2;
     }
   }

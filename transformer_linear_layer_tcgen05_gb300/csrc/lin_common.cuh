@@ -66,6 +66,13 @@ __device__ __forceinline__ bool warp_wait_phase(uint32_t bar, uint32_t parity, c
   return __all_sync(0xffffffffu, ok);
 }
 
+// The same with cluster-scope acquire (a barrier that a peer's commit completes).
+__device__ __forceinline__ bool warp_wait_phase_cluster(uint32_t bar, uint32_t parity,
+                                                        const WaitCtl& c) {
+  const bool ok = wait_phase_cluster(bar, parity, c);
+  return __all_sync(0xffffffffu, ok);
+}
+
 // Lane 0 waits (it is the lane that issues the copies or UMMAs that follow);
 // the result is broadcast so the warp stays converged.
 __device__ __forceinline__ bool lane0_wait_phase(uint32_t bar, uint32_t parity, const WaitCtl& c,

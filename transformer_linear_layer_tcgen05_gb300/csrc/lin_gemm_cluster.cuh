@@ -64,12 +64,21 @@ struct ClusterTraits {
                 "binary16 forms only");
   static constexpr bool kSwiglu = (AMODE == A_SWIGLU_F16);
   // A already binary16 in global memory: the CTA copies every A k-block of
-  // its tile by TMA; no transform warps. Such a CTA has nothing to share with
-  // peers, so it runs alone (cluster size 1).
+  // its tile by TMA; no transform warps. Such a CTA has no A to share with
+  // peers: it runs alone (CN_ == 1) or as one of a CTA pair (CN_ == 2).
   static constexpr bool kTmaA = (AMODE == A_TMA_F16);
-  static constexpr int BM = kBM;
+  // CTA pair: the two CTAs of a cluster of two compute one 256 x BN tile
+  // with UMMAs of M = 256 (tcgen05 .cta_group::2), issued by the even CTA.
+  // Each CTA loads its 128 rows of A and half of the tile's W columns (the
+  // even CTA the first half), so that W's bytes per CTA and k-block halve,
+  // and keeps its 128 rows of the accumulator in its own TMEM.
+  static constexpr bool kPair = kTmaA && CN_ == 2;
+  static constexpr int BM = kBM;                  // rows of A and of the accumulator per CTA
+  static constexpr int TM = kPair ? 2 * kBM : kBM;   // rows of a tile
   static constexpr int BN = BN_;
-  static constexpr int CN = CN_;                  // CTAs per cluster, along N
+  static constexpr int CN = kPair ? 1 : CN_;      // CTAs per cluster along N
+  static constexpr int CS = CN_;                  // CTAs per cluster
+  static constexpr int BNB = kPair ? BN_ / 2 : BN_;   // W columns in this CTA's B stage
   static constexpr int BK = 64;                   // binary16 elements per k-block
   static constexpr int KSTEP = 16;
   static constexpr int NMMA = BK / KSTEP;
@@ -77,7 +86,7 @@ struct ClusterTraits {
   static constexpr bool kBT = BT_;
   static constexpr bool kDual = DUAL_;
   static constexpr int BNO = kDual ? BN_ / 2 : BN_;   // output columns per CTA and product
-  static constexpr int W_BOXES = kBT ? 1 : BN / W_ATOM;
+  static constexpr int W_BOXES = kBT ? 1 : BNB / W_ATOM;
   static constexpr int ROWS = BM / CN;            // A rows this CTA transforms
   static constexpr int INPUTS = kSwiglu ? 2 : 1;  // GATE and UP, or X
   static constexpr int XF_WARPS = kTmaA ? 0 : LIN_XF_WARPS;
@@ -114,7 +123,7 @@ struct ClusterTraits {
   static constexpr int PF = PF_FIT < 1 ? 1 : (PF_FIT > 4 ? 4 : PF_FIT);
 
   static constexpr uint32_t A_BYTES = BM * 128;
-  static constexpr uint32_t B_ATOM_BYTES = kBT ? BN * 128 : BK * 128;
+  static constexpr uint32_t B_ATOM_BYTES = kBT ? BNB * 128 : BK * 128;
   static constexpr uint32_t B_BYTES = W_BOXES * B_ATOM_BYTES;
 
   // Split rings: the SwiGLU form in clusters, whose A stage makes the
@@ -170,12 +179,14 @@ struct ClusterTraits {
   static constexpr uint32_t OFF_ABORT = OFF_TMEM_SLOT + 4;
 
   static constexpr uint32_t TMEM_COLS = 2 * BN;
-  static constexpr uint32_t IDESC = umma_idesc(0u, false, /*b_mn_major=*/!kBT, BM, BN);
-  static constexpr uint16_t CLUSTER_MASK = (uint16_t)((1u << CN) - 1u);
+  static constexpr uint32_t IDESC = umma_idesc(0u, false, /*b_mn_major=*/!kBT, TM, BN);
+  static constexpr uint16_t CLUSTER_MASK = (uint16_t)((1u << CS) - 1u);
   static constexpr int kThreadsC = (8 + XF_WARPS) * 32;
 
   static_assert(CN == 1 || CN == 2 || CN == 4 || CN == 8, "cluster size");
-  static_assert(!kTmaA || CN == 1, "a binary16 A from global memory is loaded by each CTA alone");
+  static_assert(!kTmaA || CS == 1 || kPair,
+                "a binary16 A from global memory: single CTAs or CTA pairs");
+  static_assert(!kPair || (!kDual || BN == 256), "pair: the dual form's halves are its two products");
   static_assert(kTmaA || XF_WARPS == 4 || XF_WARPS == 8 || XF_WARPS == 12, "transform warps");
   static_assert(XF_WARPS % XF_GROUPS == 0 && ROWS % XF_PER_GROUP == 0 &&
                     RW % ROWS_PER_LOAD == 0,
@@ -299,22 +310,25 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t crank = (CN > 1) ? cluster_ctarank() : 0u;
-  const int cid = blockIdx.x / CN;                  // cluster id
-  const int ncl = gridDim.x / CN;                   // clusters in the grid
-  const int num_m = (args.M + T::BM - 1) / T::BM;
-  const int num_ng = (args.N + T::BNO * CN - 1) / (T::BNO * CN);
+  const uint32_t crank = (T::CS > 1) ? cluster_ctarank() : 0u;
+  const int cid = blockIdx.x / T::CS;               // cluster id
+  const int ncl = gridDim.x / T::CS;                // clusters in the grid
+  const int num_m = (args.M + T::TM - 1) / T::TM;
+  const int num_ng = (args.N + T::BNO * T::CN - 1) / (T::BNO * T::CN);
   const int num_tiles = num_m * num_ng;
   const int nkb = (args.K + T::BK - 1) / T::BK;
   const WaitCtl ctl{args.timeout_ns, abort_flag, args.status};
 
   auto a_stage = [&](int s) -> uint32_t { return sbase + T::OFF_A + s * T::A_BYTES; };
   auto b_stage = [&](int s) -> uint32_t { return sbase + T::OFF_W + s * T::B_BYTES; };
+  // this CTA's first row and column of tile t (a pair's CTAs: rows apart)
   auto tile_m0 = [&](int t) -> int {
-    return tile_coords(t, num_m, num_ng, args.band_ng).m * T::BM;
+    return tile_coords(t, num_m, num_ng, args.band_ng).m * T::TM +
+           (T::kPair ? (int)crank * T::BM : 0);
   };
   auto tile_n0 = [&](int t) -> int {
-    return (tile_coords(t, num_m, num_ng, args.band_ng).ng * CN + (int)crank) * T::BNO;
+    return (tile_coords(t, num_m, num_ng, args.band_ng).ng * T::CN + (T::kPair ? 0 : (int)crank)) *
+           T::BNO;
   };
   // Work items of this cluster: whole tiles cid + i*ncl, round robin; with a
   // split tail (split_s >= 2), split_r whole tiles and then, for clusters
@@ -339,9 +353,11 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
   if (threadIdx.x == 0) {
     for (int s = 0; s < T::NA; ++s) {
       // the transform group's warps, and with one ring the producer (its
-      // W bytes, or a binary16 A and W from global memory)
+      // W bytes, or a binary16 A and W from global memory; a pair's stages
+      // fill on the even CTA's barrier, whose producer expects both CTAs'
+      // bytes)
       mbar_init(bar(T::BAR_AFULL + s), T::kTmaA ? 1 : (T::kSplit ? 0 : 1) + T::XF_PER_GROUP);
-      mbar_init(bar(T::BAR_AEMPTY + s), CN);       // every CTA's UMMA commit
+      mbar_init(bar(T::BAR_AEMPTY + s), T::CN);    // every UMMA-issuing CTA's commit
     }
     if constexpr (T::kSplit)
       for (int s = 0; s < T::NW; ++s) {
@@ -350,7 +366,8 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
       }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(T::BAR_ACC_FULL + b), 1);
-      mbar_init(bar(T::BAR_ACC_EMPTY + b), 4);
+      // the epilogue warps (a pair's: of both CTAs, on the even CTA's barrier)
+      mbar_init(bar(T::BAR_ACC_EMPTY + b), T::kPair ? 8 : 4);
     }
     for (int e = 0; e < 8; ++e) mbar_init(bar(T::BAR_EPI + e), 1);
     *abort_flag = 0;
@@ -371,8 +388,13 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
   }
   __syncwarp();
   if (warp == 2) {
-    tmem_alloc(smem_u32(tmem_slot), T::TMEM_COLS);
-    tmem_relinquish_alloc_permit();
+    if constexpr (T::kPair) {   // both CTAs together: the same columns in each
+      tmem_alloc_pair(smem_u32(tmem_slot), T::TMEM_COLS);
+      tmem_relinquish_alloc_permit_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_slot), T::TMEM_COLS);
+      tmem_relinquish_alloc_permit();
+    }
   }
   // Launched as a programmatic dependent: the set-up above overlapped the
   // previous kernel on the stream; nothing below touches global memory
@@ -381,7 +403,7 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
   tc_fence_before_sync();
   // Peers may arrive on our barriers and write our A stages only after every
   // CTA of the cluster initialised them.
-  if constexpr (CN > 1)
+  if constexpr (T::CS > 1)
     cluster_sync_all();
   else
     __syncthreads();
@@ -414,44 +436,91 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
           }
         }
         if (lane == 0) {
-          mbar_arrive_expect_tx(full, T::B_BYTES + (T::kTmaA ? T::A_BYTES : 0u));
+          constexpr uint32_t bytes = T::B_BYTES + (T::kTmaA ? T::A_BYTES : 0u);
+          // A pair's stage is full on the even CTA's barrier: its producer
+          // alone arrives, expecting both CTAs' bytes, and the odd CTA's
+          // loads complete there too. (Those may land before that arrival:
+          // the transaction count runs below zero for a while, but the
+          // phase cannot complete without the arrival. An arrival from the
+          // odd CTA as well -- a remote arrive with release at cluster
+          // scope -- took ~0.4 us per stage to issue and paced the ring.)
+          const uint32_t full0 = T::kPair ? mapa_shared(full, 0) : full;
+          if (!T::kPair)
+            mbar_arrive_expect_tx(full, bytes);
+          else if (crank == 0)
+            mbar_arrive_expect_tx(full, 2 * bytes);
+          auto load = [&](uint32_t dst, const CUtensorMap* map, int x, int y) {
+            if constexpr (T::kPair)
+              tma_load_2d_pair(dst, map, x, y, full0);
+            else
+              tma_load_2d(dst, map, x, y, full);
+          };
+          // this CTA's columns of the tile's B: all, or a pair's half
+          const int nb = T::kPair && !T::kDual ? n0 + (int)crank * T::BNB : n0;
           if constexpr (T::kBT) {
-            tma_load_2d(b_stage(s), &tm_w, kb * T::BK, n0, full);   // W as [N][K]
+            load(b_stage(s), &tm_w, kb * T::BK, nb);   // W as [N][K]
+          } else if constexpr (T::kDual && T::kPair) {
+            // the pair's B is [W tile | W2 tile]: the even CTA's half is W's
+#pragma unroll
+            for (int j = 0; j < T::W_BOXES; ++j)
+              load(b_stage(s) + j * T::B_ATOM_BYTES, crank == 0 ? &tm_w : &tm_w2,
+                   n0 + j * T::W_ATOM, kb * T::BK);
           } else if constexpr (T::kDual) {   // [W tile | W2 tile], BN/2 columns each
 #pragma unroll
             for (int j = 0; j < T::W_BOXES; ++j) {
               const int jj = j % (T::W_BOXES / 2);
-              tma_load_2d(b_stage(s) + j * T::B_ATOM_BYTES, j < T::W_BOXES / 2 ? &tm_w : &tm_w2,
-                          n0 + jj * T::W_ATOM, kb * T::BK, full);
+              load(b_stage(s) + j * T::B_ATOM_BYTES, j < T::W_BOXES / 2 ? &tm_w : &tm_w2,
+                   n0 + jj * T::W_ATOM, kb * T::BK);
             }
           } else {
 #pragma unroll
             for (int j = 0; j < T::W_BOXES; ++j)
-              tma_load_2d(b_stage(s) + j * T::B_ATOM_BYTES, &tm_w, n0 + j * T::W_ATOM, kb * T::BK,
-                          full);
+              load(b_stage(s) + j * T::B_ATOM_BYTES, &tm_w, nb + j * T::W_ATOM, kb * T::BK);
           }
-          if constexpr (T::kTmaA) tma_load_2d(a_stage(s), &tm_a, kb * T::BK, tile_m0(t), full);
+          if constexpr (T::kTmaA) load(a_stage(s), &tm_a, kb * T::BK, tile_m0(t));
         }
         __syncwarp();
       }
     }
-    // no TMA load of ours may still be in flight when the CTA leaves
-    if (lane == 0)
-      for (int x = (g > T::NW ? g - T::NW : 0); x < g; ++x)
-        wait_phase(bar((T::kSplit ? T::BAR_WFULL : T::BAR_AFULL) + x % T::NW), (x / T::NW) & 1,
-                   ctl, false);
+    // no TMA load of ours may still be in flight when the CTA leaves (a
+    // pair's odd CTA: its loads have landed once the UMMA that read them
+    // has released the stage)
+    if (lane == 0) {
+      for (int x = (g > T::NW ? g - T::NW : 0); x < g; ++x) {
+        if (T::kPair && crank != 0)
+          wait_phase_cluster(bar(T::BAR_AEMPTY + x % T::NW), (x / T::NW) & 1, ctl, false);
+        else
+          wait_phase(bar((T::kSplit ? T::BAR_WFULL : T::BAR_AFULL) + x % T::NW), (x / T::NW) & 1,
+                     ctl, false);
+      }
+    }
     __syncwarp();
-  } else if (warp == 1) {
-    // ---------------- UMMA issuer
+  } else if (warp == 1 && (!T::kPair || crank == 0)) {
+    // ---------------- UMMA issuer (a pair's: in the even CTA, for both)
+    // A pair's barriers here see the odd CTA's arrivals and bytes too: the
+    // waits acquire at cluster scope, and the commits reach both CTAs.
+    auto wait_local = [&](uint32_t b, uint32_t parity) -> bool {
+      return T::kPair ? wait_phase_cluster(b, parity, ctl) : wait_phase(b, parity, ctl);
+    };
+    auto commit_local = [&](uint32_t b) {
+      if constexpr (T::kPair)
+        umma_commit_pair(b, T::CLUSTER_MASK);
+      else
+        umma_commit(b);
+    };
     int g = 0;
     bool ok = true;
     int committed_tiles = 0;
     for (int i = 0; i < n_items && ok; ++i) {
       const int ab = i & 1;
       const uint32_t d_tmem = tmem + (uint32_t)(ab * T::BN);
-      if (i >= 2 && !lane0_wait_phase(bar(T::BAR_ACC_EMPTY + ab), ((i >> 1) - 1) & 1, ctl, lane)) {
-        ok = false;
-        break;
+      if (i >= 2) {
+        bool w = true;
+        if (lane == 0) w = wait_local(bar(T::BAR_ACC_EMPTY + ab), ((i >> 1) - 1) & 1);
+        if (!__shfl_sync(0xffffffffu, w ? 1 : 0, 0)) {
+          ok = false;
+          break;
+        }
       }
       const int kb0 = item_kb0(i), kb1 = item_kb1(i);
       for (int kb = kb0; kb < kb1; ++kb, ++g) {
@@ -459,7 +528,7 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
         const int s = g % T::NW;
         bool w = true;
         if (lane == 0) {
-          w = wait_phase(bar(T::BAR_AFULL + sa), (g / T::NA) & 1, ctl) &&
+          w = wait_local(bar(T::BAR_AFULL + sa), (g / T::NA) & 1) &&
               (!T::kSplit || wait_phase(bar(T::BAR_WFULL + s), (g / T::NW) & 1, ctl));
         }
         if (!__shfl_sync(0xffffffffu, w ? 1 : 0, 0)) {
@@ -474,18 +543,21 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
             const uint64_t bdesc =
                 T::kBT ? umma_desc_sw128(b_stage(s) + k * 32, 16, 1024)
                        : umma_desc_sw128(b_stage(s) + k * T::KSTEP * 128, T::B_ATOM_BYTES, 1024);
-            umma_f16(d_tmem, adesc, bdesc, T::IDESC, kb != kb0 || k != 0);
+            if constexpr (T::kPair)
+              umma_f16_pair(d_tmem, adesc, bdesc, T::IDESC, kb != kb0 || k != 0);
+            else
+              umma_f16(d_tmem, adesc, bdesc, T::IDESC, kb != kb0 || k != 0);
           }
-          if constexpr (CN > 1)
+          if constexpr (T::CN > 1)
             umma_commit_multicast(bar(T::BAR_AEMPTY + sa), T::CLUSTER_MASK);
           else
-            umma_commit(bar(T::BAR_AEMPTY + sa));
+            commit_local(bar(T::BAR_AEMPTY + sa));
           if constexpr (T::kSplit) umma_commit(bar(T::BAR_WEMPTY + s));
         }
         __syncwarp();
       }
       if (!ok) break;
-      if (lane == 0) umma_commit(bar(T::BAR_ACC_FULL + ab));
+      if (lane == 0) commit_local(bar(T::BAR_ACC_FULL + ab));
       __syncwarp();
       committed_tiles = i + 1;
     }
@@ -494,7 +566,7 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
       // commit on a buffer whose phase we can wait for.
       if (!ok) {
         const int ab = committed_tiles & 1;
-        umma_commit(bar(T::BAR_ACC_FULL + ab));
+        commit_local(bar(T::BAR_ACC_FULL + ab));
         wait_phase(bar(T::BAR_ACC_FULL + ab), (committed_tiles >> 1) & 1, ctl, false);
       } else if (committed_tiles > 0) {
         const int last = committed_tiles - 1;
@@ -566,7 +638,7 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
         __syncwarp();
         {
           const uint32_t full = bar(T::BAR_AFULL + s);
-          if constexpr (CN > 1) {
+          if constexpr (T::CN > 1) {
             // The peers' slices of this stage arrive as copy bytes on our
             // barrier; our slice goes to peer (crank + l) % CN from lane l,
             // so that the copies are issued side by side (measured faster
@@ -642,7 +714,9 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
         tma_load_2d(buf(ebuf(ec)), &tm_r, n0, row0, ebar(ebuf(ec)));
         ++r_issued;
       }
-      ok = warp_wait_phase(bar(T::BAR_ACC_FULL + ab), (i >> 1) & 1, ctl);
+      // (a pair's accumulator is complete when the even CTA's commit says so)
+      ok = T::kPair ? warp_wait_phase_cluster(bar(T::BAR_ACC_FULL + ab), (i >> 1) & 1, ctl)
+                    : warp_wait_phase(bar(T::BAR_ACC_FULL + ab), (i >> 1) & 1, ctl);
       tc_fence_after_sync();
       // last item's accumulator complete: a split sum may be scheduled
       if (i == n_items - 1 && q == 0 && lane == 0) pdl_launch_dependents();
@@ -653,7 +727,7 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
         // partial tile of this unit: [C4 float4 columns][128 rows], so that
         // the 32 lanes (rows) of a store write 512 consecutive bytes
         float4* part = reinterpret_cast<float4*>(args.part) +
-                       (size_t)(cid * CN + (int)crank) * C4 * T::BM + q * kEpiRows + lane;
+                       (size_t)(cid * T::CS + (int)crank) * C4 * T::BM + q * kEpiRows + lane;
         for (int c = 0; c < nc; ++c) {
           uint32_t v[32];
           tmem_ld_32x32b_x32(acc + (uint32_t)(c * kEpiCols), v);
@@ -828,10 +902,16 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
           args.row_stats[(size_t)(row0 + lane) * args.stats_cols + n0 / T::BN] =
               make_float2(rm, rs);
       }
-      // TMEM reads of this buffer are complete: hand it back to the UMMA warp.
+      // TMEM reads of this buffer are complete: hand it back to the UMMA warp
+      // (a pair's is in the even CTA).
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(T::BAR_ACC_EMPTY + ab));
+      if (lane == 0) {
+        if (T::kPair && crank != 0)
+          mbar_arrive_remote(mapa_shared(bar(T::BAR_ACC_EMPTY + ab), 0));
+        else
+          mbar_arrive(bar(T::BAR_ACC_EMPTY + ab));
+      }
     }
     if (lane == 0) {
       // Never leave with an R load in flight (only possible when a wait gave
@@ -848,13 +928,16 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
 
   // ---- teardown: no CTA leaves while a peer may still write to it
   tc_fence_before_sync();
-  if constexpr (CN > 1)
+  if constexpr (T::CS > 1)
     cluster_sync_all();
   else
     __syncthreads();
   if (warp == 2) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem, T::TMEM_COLS);
+    if constexpr (T::kPair)
+      tmem_dealloc_pair(tmem, T::TMEM_COLS);
+    else
+      tmem_dealloc(tmem, T::TMEM_COLS);
   }
 }
 
@@ -869,7 +952,7 @@ struct ClusterLaunch {
                                    bool dependent) {
     cudaLaunchConfig_t cfg = {};
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CN;
+    attr[0].val.clusterDim.x = T::CS;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -904,7 +987,7 @@ struct ClusterLaunch {
       }
       cudaLaunchAttribute attr[2];
       cudaLaunchConfig_t cfg = config(attr, nullptr, false);
-      cfg.gridDim = dim3(CN, 1, 1);
+      cfg.gridDim = dim3(T::CS, 1, 1);
       int n = 0;
       if (e == cudaSuccess) e = cudaOccupancyMaxActiveClusters(&n, (void*)kern, &cfg);
       if (e == cudaSuccess && n < 1) e = cudaErrorInvalidConfiguration;
@@ -923,8 +1006,8 @@ struct ClusterLaunch {
     cudaError_t e = cudaSuccess;
     const int cap = capacity(&e);
     if (cap < 1) return e;
-    const int num_m = (args.M + T::BM - 1) / T::BM;
-    const int num_ng = (args.N + T::BNO * CN - 1) / (T::BNO * CN);
+    const int num_m = (args.M + T::TM - 1) / T::TM;
+    const int num_ng = (args.N + T::BNO * T::CN - 1) / (T::BNO * T::CN);
     int clusters;
     if (args.split_s >= 2)
       clusters = args.split_r > 0 ? cap : args.split_rem * args.split_s;
@@ -933,7 +1016,7 @@ struct ClusterLaunch {
     if (clusters > cap) return cudaErrorInvalidConfiguration;
     cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = config(attr, stream, true);
-    cfg.gridDim = dim3((unsigned)(clusters * CN), 1, 1);
+    cfg.gridDim = dim3((unsigned)(clusters * T::CS), 1, 1);
     if constexpr (!T::kTmaA) {
       if (args.flags & KFLAG_A_V8)
         return cudaLaunchKernelEx(&cfg,
@@ -949,14 +1032,16 @@ struct ClusterLaunch {
 // float4 column c4 = (x / 128) % C4 of CTA `crank` of tile j, with
 // x / (128 * C4) = j * cn + crank: the order of the partial tiles
 // [unit][cta][C4][128 rows], so that consecutive threads load consecutive
-// partial float4s. Y = sum over the s K ranges in K order (+ R):
-// independent of timing, so bitwise reproducible.
+// partial float4s. The cn CTAs of a tile sit side by side along N, or
+// (pair) one above the other in a tile of 256 rows. Y = sum over the s K
+// ranges in K order (+ R): independent of timing, so bitwise reproducible.
 template <bool RESID, bool SWB>
 __global__ void __launch_bounds__(256)
     lin_split_reduce_kernel(const float4* __restrict__ part, const float* __restrict__ R,
-                            float* __restrict__ Y, int M, int N, int cn, int bn, int tile0,
-                            int num_ng, int band, int rem, int s, const float* __restrict__ G2,
-                            const float* __restrict__ U2, float* __restrict__ Y2) {
+                            float* __restrict__ Y, int M, int N, int cn, int pair, int bn,
+                            int tile0, int num_ng, int band, int rem, int s,
+                            const float* __restrict__ G2, const float* __restrict__ U2,
+                            float* __restrict__ Y2) {
   const int c4n = bn / 4;
   const long long per_cta = 128LL * c4n;
   const long long x = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -966,9 +1051,10 @@ __global__ void __launch_bounds__(256)
   const int c4 = (int)((x / 128) % c4n);
   const int r = (int)(x % 128);
   const int t = tile0 + j;
-  const TileRC rc = tile_coords(t, (M + 127) / 128, num_ng, band);
-  const int row = rc.m * 128 + r;
-  const int col = (rc.ng * cn + crank) * bn + 4 * c4;
+  const int tile_rows = pair ? 256 : 128;
+  const TileRC rc = tile_coords(t, (M + tile_rows - 1) / tile_rows, num_ng, band);
+  const int row = rc.m * tile_rows + (pair ? crank * 128 : 0) + r;
+  const int col = (pair ? rc.ng : rc.ng * cn + crank) * bn + 4 * c4;
   // The next kernel on the stream may be scheduled now: it waits for this
   // grid's completion itself before it touches memory.
   pdl_launch_dependents();

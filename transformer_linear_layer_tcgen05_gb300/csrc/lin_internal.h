@@ -163,12 +163,15 @@ int cluster_capacity_swiglu(int cn, cudaError_t* err);
 int cluster_capacity_cvt(int cn, bool resid, cudaError_t* err);
 // matmul_w16 / matmul_residual_w16 with A = binary16 X already in global
 // memory (tensor map `a`, boxes of 64 x 128): each CTA copies every A
-// k-block of its tile by TMA. Single CTAs only (cn must be 1).
+// k-block of its tile by TMA. cn 1: single CTAs (tiles of 128 rows); cn 2:
+// CTA pairs (tiles of 256 rows, UMMAs of M = 256 over the two CTAs, each
+// CTA loading half of the tile's W columns).
 cudaError_t launch_gemm_cluster_tma(int cn, bool resid, const TensorMaps& maps,
                                     const KernelArgs& args, cudaStream_t stream);
 int cluster_capacity_tma(int cn, bool resid, cudaError_t* err);
 // The transposed product dY · W^T (binary16 W given as [N][K]): A rounded by
-// the transform warps, or (tma_a) copied by TMA from the pre-pass's output.
+// the transform warps, or (tma_a) copied by TMA from the pre-pass's output
+// (then cn 2 means CTA pairs, as above; the W box is then 128 rows).
 cudaError_t launch_gemm_cluster_bt(bool tma_a, int cn, bool resid, const TensorMaps& maps,
                                    const KernelArgs& args, cudaStream_t stream);
 int cluster_capacity_bt(bool tma_a, int cn, bool resid, cudaError_t* err);
@@ -189,10 +192,11 @@ cudaError_t launch_cross_entropy(float* logits, const float2* row_stats, int sta
                                  int V, float alpha, float beta, float inv_norm,
                                  cudaStream_t stream);
 // Y (+ R) from the partial tiles of a split: tiles tile0 .. tile0 +
-// split_rem - 1 of width `bn` (cluster tiles of `cn` CTAs, `num_ng` of them
-// per row block), each summed over its split_s K ranges.
-cudaError_t launch_split_reduce(const KernelArgs& args, bool resid, int cn, int bn, int tile0,
-                                int num_ng, cudaStream_t stream);
+// split_rem - 1 of width `bn` (cluster tiles of `cn` CTAs along N, `num_ng`
+// of them per row block; or, `pair`, tiles of 256 rows whose two CTAs hold
+// 128 rows each), each summed over its split_s K ranges.
+cudaError_t launch_split_reduce(const KernelArgs& args, bool resid, int cn, bool pair, int bn,
+                                int tile0, int num_ng, cudaStream_t stream);
 
 // A caller-provided split-tail workspace: returns its base and size on
 // device `dev`, or an error status.

@@ -1,8 +1,8 @@
 // lin_kernels_cluster_cvt.cu -- instantiations of the clustered persistent
 // GEMM for matmul_w16 and matmul_residual_w16 (A rounded to binary16 by
 // the transform warps in clusters of 1, 2 or 4 CTAs, or by a pre-pass and
-// then copied by TMA into single CTAs), the pre-pass, and the split-tail sum
-// shared by every clustered form.
+// then copied by TMA into single CTAs or CTA pairs), the pre-pass, and the
+// split-tail sum shared by every clustered form.
 #include "lin_gemm_cluster.cuh"
 
 namespace lin {
@@ -13,19 +13,26 @@ using CvtLaunch = ClusterLaunch<A_CVT_F16, RESID, 256, CN>;
 template <bool RESID, int CN>
 using TmaLaunch = ClusterLaunch<A_TMA_F16, RESID, 256, CN>;
 
+// cn: 1 (single CTAs) or 2 (CTA pairs along M)
 cudaError_t launch_gemm_cluster_tma(int cn, bool resid, const TensorMaps& maps,
                                     const KernelArgs& args, cudaStream_t stream) {
-  if (cn != 1) return cudaErrorInvalidValue;
-  return resid ? TmaLaunch<true, 1>::launch(maps, args, stream)
-               : TmaLaunch<false, 1>::launch(maps, args, stream);
+  switch (cn * 2 + (resid ? 1 : 0)) {
+    case 2: return TmaLaunch<false, 1>::launch(maps, args, stream);
+    case 3: return TmaLaunch<true, 1>::launch(maps, args, stream);
+    case 4: return TmaLaunch<false, 2>::launch(maps, args, stream);
+    case 5: return TmaLaunch<true, 2>::launch(maps, args, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 int cluster_capacity_tma(int cn, bool resid, cudaError_t* err) {
-  if (cn != 1) {
-    *err = cudaErrorInvalidValue;
-    return 0;
+  switch (cn * 2 + (resid ? 1 : 0)) {
+    case 2: return TmaLaunch<false, 1>::capacity(err);
+    case 3: return TmaLaunch<true, 1>::capacity(err);
+    case 4: return TmaLaunch<false, 2>::capacity(err);
+    case 5: return TmaLaunch<true, 2>::capacity(err);
+    default: *err = cudaErrorInvalidValue; return 0;
   }
-  return resid ? TmaLaunch<true, 1>::capacity(err) : TmaLaunch<false, 1>::capacity(err);
 }
 
 // X -> binary16, four elements per thread and step (one 16-byte load, one
@@ -90,8 +97,8 @@ int cluster_capacity_cvt(int cn, bool resid, cudaError_t* err) {
   }
 }
 
-cudaError_t launch_split_reduce(const KernelArgs& args, bool resid, int cn, int bn, int tile0,
-                                int num_ng, cudaStream_t stream) {
+cudaError_t launch_split_reduce(const KernelArgs& args, bool resid, int cn, bool pair, int bn,
+                                int tile0, int num_ng, cudaStream_t stream) {
   const long long threads = (long long)args.split_rem * cn * 128 * (bn / 4);
   // Programmatic dependent launch: the sum is scheduled while the GEMM still
   // runs and waits for it in griddepcontrol.wait, hiding the launch gap.
@@ -107,14 +114,17 @@ cudaError_t launch_split_reduce(const KernelArgs& args, bool resid, int cn, int 
   const float4* part = reinterpret_cast<const float4*>(args.part);
   if (args.flags & KFLAG_SWIGLU_BWD)
     return cudaLaunchKernelEx(&cfg, lin_split_reduce_kernel<false, true>, part, args.R, args.Y,
-                              args.M, args.N, cn, bn, tile0, num_ng, args.band_ng, args.split_rem, args.split_s,
+                              args.M, args.N, cn, pair ? 1 : 0, bn, tile0, num_ng, args.band_ng,
+                              args.split_rem, args.split_s,
                               args.G2, args.U2, args.Y2);
   if (resid)
     return cudaLaunchKernelEx(&cfg, lin_split_reduce_kernel<true, false>, part, args.R, args.Y,
-                              args.M, args.N, cn, bn, tile0, num_ng, args.band_ng, args.split_rem, args.split_s,
+                              args.M, args.N, cn, pair ? 1 : 0, bn, tile0, num_ng, args.band_ng,
+                              args.split_rem, args.split_s,
                               args.G2, args.U2, args.Y2);
   return cudaLaunchKernelEx(&cfg, lin_split_reduce_kernel<false, false>, part, args.R, args.Y,
-                            args.M, args.N, cn, bn, tile0, num_ng, args.band_ng, args.split_rem, args.split_s,
+                            args.M, args.N, cn, pair ? 1 : 0, bn, tile0, num_ng, args.band_ng,
+                              args.split_rem, args.split_s,
                             args.G2, args.U2, args.Y2);
 }
 

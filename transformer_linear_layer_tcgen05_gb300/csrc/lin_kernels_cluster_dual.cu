@@ -9,13 +9,14 @@ namespace lin {
 template <int AMODE, int CN>
 using DualLaunch = ClusterLaunch<AMODE, false, 256, CN, /*BT=*/false, /*DUAL=*/true>;
 
-// The rounded-by-the-transform form in clusters of 1, 2 or 4 CTAs; the
-// pre-converted form (TMA-loaded A) in single CTAs only.
+// The rounded-by-the-transform form in clusters of 1, 2 or 4 CTAs along N;
+// the pre-converted form (TMA-loaded A) in single CTAs or CTA pairs (cn 2;
+// the even CTA loads the W tile, the odd one the W2 tile).
 template <int AMODE>
 cudaError_t dual_launch(int cn, const TensorMaps& m, const KernelArgs& a, cudaStream_t s) {
   if (cn == 1) return DualLaunch<AMODE, 1>::launch(m, a, s);
   if constexpr (AMODE == A_TMA_F16) {
-    return cudaErrorInvalidValue;
+    return cn == 2 ? DualLaunch<AMODE, 2>::launch(m, a, s) : cudaErrorInvalidValue;
   } else {
     switch (cn) {
       case 2: return DualLaunch<AMODE, 2>::launch(m, a, s);
@@ -29,6 +30,7 @@ template <int AMODE>
 int dual_capacity(int cn, cudaError_t* err) {
   if (cn == 1) return DualLaunch<AMODE, 1>::capacity(err);
   if constexpr (AMODE == A_TMA_F16) {
+    if (cn == 2) return DualLaunch<AMODE, 2>::capacity(err);
     *err = cudaErrorInvalidValue;
     return 0;
   } else {

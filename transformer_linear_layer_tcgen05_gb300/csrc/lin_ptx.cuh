@@ -386,6 +386,72 @@ __device__ __forceinline__ void umma_commit_multicast(uint32_t bar, uint16_t mas
       : "memory");
 }
 
+// ------------------------------------------------------------------ CTA pairs
+//
+// tcgen05 with .cta_group::2: the two CTAs of a cluster of two act as one
+// UMMA of M = 256. Each CTA holds 128 rows of A and half the columns of B
+// (the even CTA the first half) at the same shared-memory offsets, and its
+// 128 rows of the accumulator in its own TMEM at the same column; one thread
+// of the even CTA issues the UMMAs. A kernel uses one .cta_group throughout,
+// so TMEM is allocated and released by a warp of each CTA together.
+
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst),
+               "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_alloc_permit_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void umma_f16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive once on the mbarrier at offset `bar` in each CTA of `mask` when
+// every pair UMMA this thread issued so far is done.
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(mask)
+      : "memory");
+}
+
+// tma_load_2d into this CTA's shared memory whose bytes complete on an
+// mbarrier of either CTA of the pair (`bar_cluster` from mapa).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int32_t x,
+                                                 int32_t y, uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster)
+      : "memory");
+}
+
+// Arrive on an mbarrier of another CTA of the cluster and raise its
+// transaction count by `bytes` (address from mapa).
+__device__ __forceinline__ void mbar_arrive_expect_tx_remote(uint32_t cluster_addr,
+                                                             uint32_t bytes) {
+  asm volatile(
+      "mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(
+          cluster_addr),
+      "r"(bytes)
+      : "memory");
+}
+
 // ------------------------------------------------------------------ descriptors
 
 // UMMA shared-memory matrix descriptor for a 128-byte-swizzled operand.
