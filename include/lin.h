@@ -283,11 +283,13 @@ lin_status lin_matmul_t_swiglu_backward_w16(const float *DY, const uint16_t *W16
  * LSE = max + log(max(sum exp(l - max), 1e-30)), and *loss_sum = the sum of
  * the M losses (a fixed-order, reproducible sum). A target outside [0, V)
  * (padding) gives loss 0 and a zero dLogits row. The GEMM's epilogue keeps
- * per-row online-softmax partials (max, sum of exponentials over each 256
- * columns), so the loss kernel reads each logits row once instead of three
- * times. targets: int32 [M]; losses: f32 [M]; loss_sum: one f32. V % 8 == 0,
- * K % 4 == 0; DLOGITS, losses and loss_sum overlap no input or each other.
- * Kernels: the GEMM (and its binary16 pre-pass), the loss, the sum. */
+ * per-row partials (max, sum of exponentials and sum of the logits over each
+ * 256 columns), so the loss kernel reads each logits row once instead of
+ * three times. targets: int32 [M]; losses: f32 [M]; loss_sum: one f32.
+ * V % 8 == 0, K % 4 == 0; DLOGITS, losses and loss_sum overlap no input or
+ * each other. Kernels: the GEMM (and its binary16 pre-pass) and the loss,
+ * whose last CTA adds the losses (a separate sum kernel only when the call
+ * could not get its 16-byte-per-partial workspace). */
 lin_status lin_lm_head_cross_entropy_w16(const float *X, const uint16_t *W16,
                                          const int32_t *targets, float *DLOGITS, float *losses,
                                          float *loss_sum, int64_t M, int64_t V, int64_t K,

@@ -56,8 +56,11 @@ def _fused(X, W16, t, alpha, beta, inv_norm):
 
 
 # (M, V, K): ragged rows, a vocabulary that is not a multiple of 256 or of a
-# cluster's 1024 columns, and the lm_head shape of the pages (512 x 16384 x 768)
-SHAPES = [(129, 1032, 64), (300, 2048, 768), (64, 4096, 256), (512, 16384, 768)]
+# cluster's 1024 columns, the lm_head shape of the pages (512 x 16384 x 768),
+# and rows longer than the loss kernel stages at once (16384 logits: the
+# rest is read chunk by chunk)
+SHAPES = [(129, 1032, 64), (300, 2048, 768), (64, 4096, 256), (512, 16384, 768),
+          (64, 20488, 128)]
 PARAMS = [(0.0, 0.0, 1.0), (0.1, 0.0, 1.0 / 300), (0.0, 1e-4, 0.5), (0.05, 1e-3, 1.0)]
 
 
@@ -114,4 +117,6 @@ def test_no_contraction_gives_uniform_softmax():
     want = np.full(M, math.log(V))
     want[5] = 0.0
     np.testing.assert_allclose(losses.cpu().numpy(), want, rtol=1e-6)
-    assert lin.lin_last_launch_info()[0] == 2   # the loss and the sum (the GEMM only zeroes)
+    # one kernel: the loss, whose last CTA also adds the losses (the GEMM
+    # only zeroes the logits, and a memset the loss kernel's count of rows)
+    assert lin.lin_last_launch_info()[0] == 1

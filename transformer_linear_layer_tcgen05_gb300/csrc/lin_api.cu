@@ -279,8 +279,9 @@ struct Problem {
   const float* U2 = nullptr;
   float* Y2 = nullptr;
   // online-softmax partials of every output row (clustered kernel, no split)
-  float2* row_stats = nullptr;
+  float4* row_stats = nullptr;
   int stats_cols = 0;
+  uint32_t* zero_word = nullptr;   // the clustered GEMM zeroes it (a dependent kernel's counter)
   // dual GEMM: Y2 = A · W2 beside Y = A · W (binary16 W2 [K,N]; Y2 [M,N])
   const void* W2 = nullptr;
   // every buffer is a piece of one of the library's own device allocations
@@ -475,6 +476,7 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
   if (p.row_stats) {
     args.flags |= lin::KFLAG_ROW_STATS;
     args.row_stats = p.row_stats;
+    args.zero_word = p.zero_word;
     args.stats_cols = p.stats_cols;
   }
   if (swb) {
@@ -734,41 +736,48 @@ lin_status lm_head_cross_entropy(const float* X, const uint16_t* W16, const int3
   // capture), freed after the loss kernel; without it the loss kernel reads
   // each row three times instead of once
   const int cols = (int)((V + lin::kClusterBN - 1) / lin::kClusterBN);
-  const size_t stats_bytes = (size_t)M * cols * sizeof(float2);
+  const size_t stats_bytes = (size_t)M * cols * sizeof(float4);
+  // after the partials: the loss kernel's count of finished rows (zeroed by
+  // the GEMM, or by a memset when there is no GEMM)
+  const size_t ws_bytes = stats_bytes + 16;
   void* ws = nullptr;
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
   if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) cudaGetLastError();
   if (cs == cudaStreamCaptureStatusActive) {
-    if (cudaMallocAsync(&ws, stats_bytes, stream) != cudaSuccess) {
+    if (cudaMallocAsync(&ws, ws_bytes, stream) != cudaSuccess) {
       cudaGetLastError();
       ws = nullptr;
     }
   } else if (cs == cudaStreamCaptureStatusNone) {
     cudaMemPool_t pool = workspace_pool(dev);
-    if (!pool || cudaMallocFromPoolAsync(&ws, stats_bytes, pool, stream) != cudaSuccess) {
+    if (!pool || cudaMallocFromPoolAsync(&ws, ws_bytes, pool, stream) != cudaSuccess) {
       cudaGetLastError();
       ws = nullptr;
     }
   }
   Problem p{F_MATMUL, true, X, nullptr, nullptr, W16, nullptr, dlogits, M, V, K};
   // (with K == 0 the GEMM only zeroes the logits and leaves no partials)
-  p.row_stats = K > 0 ? static_cast<float2*>(ws) : nullptr;
+  p.row_stats = K > 0 ? static_cast<float4*>(ws) : nullptr;
   p.stats_cols = cols;
+  unsigned* done =
+      ws ? reinterpret_cast<unsigned*>(static_cast<char*>(ws) + stats_bytes) : nullptr;
+  p.zero_word = K > 0 ? done : nullptr;
   st = run(p, stream);
   const int gemm_kernels = t_last_kernels;
   const uint64_t gemm_ws = t_last_workspace;
   cudaError_t e = cudaSuccess;
-  if (st == LIN_SUCCESS)
+  if (st == LIN_SUCCESS && done && K == 0) e = cudaMemsetAsync(done, 0, 4, stream);
+  if (st == LIN_SUCCESS && e == cudaSuccess)
     e = lin::launch_cross_entropy(dlogits, p.row_stats, cols, targets, losses, loss_sum,
-                                  (int)M, (int)V, alpha, beta, inv_norm, stream);
+                                  (int)M, (int)V, alpha, beta, inv_norm, done, stream);
   if (ws) {
     const cudaError_t ef = cudaFreeAsync(ws, stream);
     if (e == cudaSuccess) e = ef;
   }
   if (st != LIN_SUCCESS) return st;
   if (e != cudaSuccess) return cuda_fail(e);
-  t_last_kernels = gemm_kernels + 2;
-  t_last_workspace = gemm_ws + (ws ? stats_bytes : 0);
+  t_last_kernels = gemm_kernels + (done ? 1 : 2);
+  t_last_workspace = gemm_ws + (ws ? ws_bytes : 0);
   return LIN_SUCCESS;
 }
 

@@ -400,6 +400,7 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
   // previous kernel on the stream; nothing below touches global memory
   // before that kernel has completed.
   pdl_wait();
+  if (args.zero_word && blockIdx.x == 0 && threadIdx.x == 0) *args.zero_word = 0u;
   tc_fence_before_sync();
   // Peers may arrive on our barriers and write our A stages only after every
   // CTA of the cluster initialised them.
@@ -813,9 +814,10 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
           __syncwarp();
         }
       } else if (staged) {
-        // online-softmax partials of this lane's row over the tile's columns
+        // online-softmax partials of this lane's row over the tile's columns,
+        // and the row's sum over them
         const bool stats = !T::kDual && (args.flags & KFLAG_ROW_STATS) != 0;
-        float rm = -INFINITY, rs = 0.0f;
+        float rm = -INFINITY, rs = 0.0f, rsum = 0.0f;
         for (int c = 0; c < nct && ok; ++c) {
           const uint32_t e = ec + (uint32_t)c;
           const uint32_t b = ebuf(e);
@@ -849,12 +851,15 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
             bulk_wait_group_read<0>();   // this buffer's last store has read it
           }
           __syncwarp();
-          if (stats) {   // (max, sum exp(y - max)) over the columns below N
+          if (stats) {   // (max, sum exp(y - max), sum y) over the columns below N
             const int col = n0 + c * kEpiCols;
             float cm = -INFINITY;
 #pragma unroll
             for (int i = 0; i < 32; ++i)
-              if (col + i < args.N) cm = fmaxf(cm, __uint_as_float(v[i]));
+              if (col + i < args.N) {
+                cm = fmaxf(cm, __uint_as_float(v[i]));
+                rsum += __uint_as_float(v[i]);
+              }
             const float mn = fmaxf(rm, cm);
             float sum = (rm == -INFINITY) ? 0.0f : rs * __expf(rm - mn);
             if (mn != -INFINITY) {
@@ -900,7 +905,7 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
         ec += (uint32_t)nct;
         if (stats && ok && row0 + lane < args.M)
           args.row_stats[(size_t)(row0 + lane) * args.stats_cols + n0 / T::BN] =
-              make_float2(rm, rs);
+              make_float4(rm, rs, rsum, 0.0f);
       }
       // TMEM reads of this buffer are complete: hand it back to the UMMA warp
       // (a pair's is in the even CTA).

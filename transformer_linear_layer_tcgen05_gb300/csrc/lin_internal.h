@@ -37,7 +37,8 @@ enum : uint32_t {
   KFLAG_SWIGLU_BWD = 1u << 2,
   // Epilogue (clustered kernels): also the online-softmax partials of each
   // output row over this CTA's columns of a tile -- (max, sum of exp(y -
-  // max)) -- into row_stats[row][n0 / BN] (cross-entropy of the lm_head).
+  // max), sum of y, 0) -- into row_stats[row][n0 / BN] (cross-entropy of
+  // the lm_head: the row's log-sum-exp and, for label smoothing, its sum).
   KFLAG_ROW_STATS = 1u << 3,
   // Split K of the per-tile kernel within a cluster (gridDim.z CTAs of one
   // tile, cluster dims (1, 1, split_s)): each CTA leaves its partial tile in
@@ -67,9 +68,11 @@ struct KernelArgs {
   const float* G2;      // GATE [M,N] of the SwiGLU-backward epilogue
   const float* U2;      // UP [M,N] of the SwiGLU-backward epilogue
   float* Y2;            // dUP [M,N] of the SwiGLU-backward epilogue (dGATE goes to Y)
-  float2* row_stats;    // [M][stats_cols] (max, sum exp) partials (KFLAG_ROW_STATS)
+  float4* row_stats;    // [M][stats_cols] (max, sum exp, sum, 0) partials (KFLAG_ROW_STATS)
   int32_t stats_cols;
   int32_t band_ng;      // column groups per band of the clustered tile order (0: one band)
+  uint32_t* zero_word;  // (clustered kernels) set to 0 once the kernel may touch memory: the
+                        // counter of a dependent kernel (null: none)
 };
 
 // Order of the clustered kernels' tiles: tile t of a grid of num_m row
@@ -185,11 +188,13 @@ int cluster_capacity_dual(bool tma_a, int cn, cudaError_t* err);
 cudaError_t launch_cvt_f16(const float* X, uint16_t* Xh, int64_t n, int sms, cudaStream_t stream);
 // Cross-entropy of page 07_loss on logits [M,V] in place (dLogits), one CTA
 // per row; with row_stats (stats_cols partials per row from the GEMM) the
-// row max and the sum of exponentials come from them, else from two passes
-// over the row. Then the deterministic sum of the M losses into *loss_sum.
-cudaError_t launch_cross_entropy(float* logits, const float2* row_stats, int stats_cols,
+// row max, the sum of exponentials and the row sum come from them, else from
+// two passes over the row. Then the deterministic sum of the M losses into
+// *loss_sum: by the loss kernel's last CTA when `done` (a counter that is
+// zero when the loss kernel starts) is given, else by a second kernel.
+cudaError_t launch_cross_entropy(float* logits, const float4* row_stats, int stats_cols,
                                  const int32_t* targets, float* losses, float* loss_sum, int M,
-                                 int V, float alpha, float beta, float inv_norm,
+                                 int V, float alpha, float beta, float inv_norm, unsigned* done,
                                  cudaStream_t stream);
 // Y (+ R) from the partial tiles of a split: tiles tile0 .. tile0 +
 // split_rem - 1 of width `bn` (cluster tiles of `cn` CTAs along N, `num_ng`

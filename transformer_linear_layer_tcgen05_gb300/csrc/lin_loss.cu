@@ -3,11 +3,11 @@
 // lm_head GEMM has just written, and the sum of the losses.
 //
 // One CTA per row, as on the page. The page's phases 1 and 2a (row max, sum
-// of exponentials) read the row twice; when the GEMM's epilogue has left
-// online-softmax partials per row (max and sum of exp(l - max) over each
-// CTA's 256 columns), they are combined here instead and the row is read
-// once, in phase 4, which also forms the sum of the logits that label
-// smoothing needs and writes dLogits in place.
+// of exponentials) read the row twice, and label smoothing needs the row's
+// sum; when the GEMM's epilogue has left partials per row (max, sum of
+// exp(l - max) and sum of l over each CTA's 256 columns), they are combined
+// here instead, and the row is read once, for phase 4, which writes dLogits
+// in place.
 #include "lin_common.cuh"
 
 namespace lin {
@@ -44,12 +44,62 @@ __device__ __forceinline__ float block_reduce(float v, float* sh) {
 
 }  // namespace
 
+// sum_losses, by the CTA that counts itself last: each CTA, once its loss is
+// written, counts itself done (its thread 0 fences the write first); in the
+// one that takes the count to M, all threads add the M losses in a fixed
+// order (a strided sum, then the fixed-order block reduction), so the total
+// has the same bits whichever CTA that is. `done` is zero when the grid
+// starts; without it (null) a separate kernel adds the losses. (Measured on
+// one GB300, cold / warm us of the lm_head shape: a separate sum kernel
+// 44.3 / 36.3, this 43.7 / 34.8; warp 0 alone counting with a release
+// atomic while the other warps went on, 44.7 / 36.5.)
+__device__ __forceinline__ void sum_if_last(const float* losses, int M, unsigned* done,
+                                            float* loss_sum, float* sh) {
+  if (!done) return;
+  __shared__ int last;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    last = atomicAdd(done, 1u) == (unsigned)(M - 1);
+  }
+  __syncthreads();
+  if (!last) return;
+  __threadfence();   // the other CTAs' losses, visible before their counts
+  float v = 0.0f;
+  for (int i = threadIdx.x; i < M; i += kLossThreads) v += __ldcg(losses + i);
+  v = block_reduce<false>(v, sh);
+  if (threadIdx.x == 0) *loss_sum = v;
+}
+
+// Online-softmax partials (max m, sum s of exp(l - m)) merged: the pair for
+// the union of both column sets. -inf maxima (no columns) merge as no-ops.
+__device__ __forceinline__ void merge_softmax(float& m, float& s, float m2, float s2) {
+  const float mx = fmaxf(m, m2);
+  if (mx == -INFINITY) return;
+  s = (m == -INFINITY ? 0.0f : s * __expf(m - mx)) + (m2 == -INFINITY ? 0.0f : s2 * __expf(m2 - mx));
+  m = mx;
+}
+
+// A CTA's first kRegF4 float4s of its row are loaded into registers
+// (kChunk per thread) and the next kSmemF4 copied into shared memory by
+// cp.async, all requested together with the target index before anything
+// else, so that the whole row (V <= 16384) is in flight at once; the rest of
+// a longer row is read in further register chunks during phase 4.
+constexpr int kChunk = 8;
+constexpr int kRegF4 = kChunk * kLossThreads;      // 2048 float4s: 32 KB
+constexpr int kSmemF4 = kChunk * kLossThreads;     // the next 32 KB
+constexpr size_t kLossSmemBytes = (size_t)kSmemF4 * 16;
+
 __global__ void __launch_bounds__(kLossThreads, 4)
-    lin_cross_entropy_kernel(float* __restrict__ logits, const float2* __restrict__ stats,
+    lin_cross_entropy_kernel(float* __restrict__ logits, const float4* __restrict__ stats,
                              int stats_cols, const int32_t* __restrict__ targets,
                              float* __restrict__ losses, int V, float alpha, float beta,
-                             float inv_norm) {
+                             float inv_norm, unsigned* __restrict__ done,
+                             float* __restrict__ loss_sum) {
+  extern __shared__ float4 staged[];   // kSmemF4 float4s of the row
   __shared__ float sh[kLossThreads / 32];
+  __shared__ float4 part[kLossThreads / 32];
+  __shared__ float3 row_sums;          // row max, sum of exp(l - max), sum of l
   const int s = blockIdx.x;
   const int tid = threadIdx.x;
   // Launched as a programmatic dependent of the GEMM: wait for its logits.
@@ -57,12 +107,7 @@ __global__ void __launch_bounds__(kLossThreads, 4)
   float* row = logits + (size_t)s * (size_t)V;
   float4* row4 = reinterpret_cast<float4*>(row);
   const int V4 = V / 4;   // V % 4 == 0
-  // The thread's float4s of the row, kChunk at a time, in registers. The
-  // first chunk is requested with the target index, before anything else,
-  // so that its loads are in flight while the target logit and the row's
-  // statistics are fetched and combined. (kChunk = 8 keeps four of these
-  // CTAs resident per SM, so every row's CTA runs at once at M = 512.)
-  constexpr int kChunk = 8;
+  const int tgt = targets[s];
   float4 l[kChunk];
   auto load_chunk = [&](int v0) {
 #pragma unroll
@@ -71,74 +116,127 @@ __global__ void __launch_bounds__(kLossThreads, 4)
       if (v < V4) l[u] = row4[v];
     }
   };
-  const int tgt = targets[s];
   load_chunk(tid);
+  // thread t's shared-memory float4s are t + u * kLossThreads, which it
+  // alone copies and later reads: its own cp_async_wait_all suffices
+  const uint32_t st0 = smem_u32(staged);
+#pragma unroll
+  for (int u = 0; u < kChunk; ++u) {
+    const int v = kRegF4 + tid + u * kLossThreads;
+    if (v < V4) cp_async_16(st0 + 16u * (uint32_t)(tid + u * kLossThreads), row4 + v);
+  }
   if (tgt < 0 || tgt >= V) {   // ignored row (padding): loss 0, dLogits 0
+    cp_async_wait_all();       // no copy may still write our shared memory
     for (int v = tid; v < V4; v += kLossThreads) row4[v] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (tid == 0) losses[s] = 0.0f;
+    sum_if_last(losses, gridDim.x, done, loss_sum, sh);
     return;
   }
-  const float l_t = row[tgt];
-  // phases 1 and 2a: row max and sum of exp(l - max)
-  float row_max, denom;
+  const float l_t = tid == 0 ? row[tgt] : 0.0f;   // phase 3 needs it before phase 4 overwrites it
+  // phases 1 and 2a (row max and sum of exp(l - max)) and the row sum that
+  // label smoothing needs
   if (stats) {
-    const float2* st = stats + (size_t)s * stats_cols;
-    float m = -INFINITY;
-    for (int i = tid; i < stats_cols; i += kLossThreads) m = fmaxf(m, st[i].x);
-    row_max = block_reduce<true>(m, sh);
-    float d = 0.0f;
-    if (row_max != -INFINITY)
-      for (int i = tid; i < stats_cols; i += kLossThreads)
-        if (st[i].x != -INFINITY) d += st[i].y * __expf(st[i].x - row_max);
-    denom = block_reduce<false>(d, sh);
-  } else {
+    // merge the GEMM's partials: each thread its columns in order, then
+    // the warps' shuffle trees, then warp 0 over the warps in order
+    const float4* st = stats + (size_t)s * stats_cols;
+    float m = -INFINITY, e = 0.0f, sum = 0.0f;
+    for (int i = tid; i < stats_cols; i += kLossThreads) {
+      const float4 p = st[i];
+      merge_softmax(m, e, p.x, p.y);
+      sum += p.z;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+      const float e2 = __shfl_xor_sync(0xffffffffu, e, o);
+      sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      merge_softmax(m, e, m2, e2);
+    }
+    if ((tid & 31) == 0) part[tid >> 5] = make_float4(m, e, sum, 0.0f);
+    __syncthreads();
+    if (tid == 0) {
+      float4 a = part[0];
+      for (int w = 1; w < kLossThreads / 32; ++w) {
+        merge_softmax(a.x, a.y, part[w].x, part[w].y);
+        a.z += part[w].z;
+      }
+      row_sums = make_float3(a.x, a.y, a.z);
+    }
+    __syncthreads();
+  } else {   // no partials: read the row from global memory for them
     float m = -INFINITY;
     for (int v = tid; v < V4; v += kLossThreads) {
-      const float4 l = row4[v];
-      m = fmaxf(fmaxf(m, fmaxf(l.x, l.y)), fmaxf(l.z, l.w));
+      const float4 x = row4[v];
+      m = fmaxf(m, fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w)));
     }
-    row_max = block_reduce<true>(m, sh);
-    float d = 0.0f;
+    const float row_max = block_reduce<true>(m, sh);
+    float d = 0.0f, sum = 0.0f;
     for (int v = tid; v < V4; v += kLossThreads) {
-      const float4 l = row4[v];
-      d += __expf(l.x - row_max) + __expf(l.y - row_max) + __expf(l.z - row_max) +
-           __expf(l.w - row_max);
+      const float4 x = row4[v];
+      d += __expf(x.x - row_max) + __expf(x.y - row_max) + __expf(x.z - row_max) +
+           __expf(x.w - row_max);
+      sum += (x.x + x.y) + (x.z + x.w);
     }
-    denom = block_reduce<false>(d, sh);
+    const float denom = block_reduce<false>(d, sh);
+    const float total = block_reduce<false>(sum, sh);
+    if (tid == 0) row_sums = make_float3(row_max, denom, total);
+    __syncthreads();
   }
-  // phase 3 needs the target logit before phase 4 overwrites the row
-  // (requested before the statistics were combined, above)
-  __syncthreads();
-  const float dg = fmaxf(denom, 1e-30f);
-  const float inv_denom = 1.0f / dg;
+  const float row_max = row_sums.x;
+  const float dg = fmaxf(row_sums.y, 1e-30f);
   const float lse = row_max + logf(dg);
   const float inv_V = 1.0f / (float)V;
   const float zl = 2.0f * beta * lse;
   const float smooth = alpha * inv_V;
-  // phase 4: dLogits in place (and the sum of the logits for smoothing),
-  // chunk by chunk from registers (every load of a chunk in flight at once)
-  float sum_l = 0.0f;
-  for (int v0 = tid; v0 < V4; v0 += kChunk * kLossThreads) {
-    if (v0 != tid) load_chunk(v0);
+  // Phase 4 per logit l: p = exp(l - lse) = 2^(l log2(e) - lse log2(e)), and
+  // dLogit = ((p - target share) + zl p) * inv_norm = p c_scale - c_off,
+  // less (1 - alpha) inv_norm at the target: two FMAs and one ex2 a logit.
+  constexpr float kLog2e = 1.4426950408889634f;
+  const float c_shift = lse * kLog2e;
+  const float c_scale = (1.0f + zl) * inv_norm;
+  const float c_off = smooth * inv_norm;
+  const float c_hit = (1.0f - alpha) * inv_norm;
+  const int tv = tgt >> 2;   // the float4 holding the target
+  // phase 3: the loss
+  if (tid == 0) {
+    const float ce = lse - (1.0f - alpha) * l_t - (alpha > 0.0f ? alpha * (row_sums.z * inv_V) : 0.0f);
+    losses[s] = ce + beta * lse * lse;
+  }
+  // (counted before phase 4, so that the count's fence has only the loss to
+  // wait for, not this CTA's dLogits stores)
+  sum_if_last(losses, gridDim.x, done, loss_sum, sh);
+  // phase 4: dLogits in place, from registers, then from shared memory, then
+  // (longer rows) register chunk by chunk
+  auto g1 = [&](float l) { return fmaf(ex2_approx(fmaf(l, kLog2e, -c_shift)), c_scale, -c_off); };
+  auto grad = [&](const float4 x, int v) -> float4 {
+    float4 y = make_float4(g1(x.x), g1(x.y), g1(x.z), g1(x.w));
+    if (v == tv) {
+      const int j = tgt & 3;
+      y.x -= j == 0 ? c_hit : 0.0f;
+      y.y -= j == 1 ? c_hit : 0.0f;
+      y.z -= j == 2 ? c_hit : 0.0f;
+      y.w -= j == 3 ? c_hit : 0.0f;
+    }
+    return y;
+  };
+#pragma unroll
+  for (int u = 0; u < kChunk; ++u) {
+    const int v = tid + u * kLossThreads;
+    if (v < V4) row4[v] = grad(l[u], v);
+  }
+  cp_async_wait_all();
+#pragma unroll
+  for (int u = 0; u < kChunk; ++u) {
+    const int v = kRegF4 + tid + u * kLossThreads;
+    if (v < V4) row4[v] = grad(staged[tid + u * kLossThreads], v);
+  }
+  for (int v0 = kRegF4 + kSmemF4 + tid; v0 < V4; v0 += kChunk * kLossThreads) {
+    load_chunk(v0);
 #pragma unroll
     for (int u = 0; u < kChunk; ++u) {
       const int v = v0 + u * kLossThreads;
-      if (v >= V4) break;
-      sum_l += (l[u].x + l[u].y) + (l[u].z + l[u].w);
-      float* e = &l[u].x;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float p = __expf(e[i] - row_max) * inv_denom;
-        const float tgt_dist = (4 * v + i == tgt ? 1.0f - alpha : 0.0f) + smooth;
-        e[i] = ((p - tgt_dist) + zl * p) * inv_norm;
-      }
-      row4[v] = l[u];
+      if (v < V4) row4[v] = grad(l[u], v);
     }
-  }
-  if (alpha > 0.0f) sum_l = block_reduce<false>(sum_l, sh);
-  if (tid == 0) {
-    const float ce = lse - (1.0f - alpha) * l_t - (alpha > 0.0f ? alpha * (sum_l * inv_V) : 0.0f);
-    losses[s] = ce + beta * lse * lse;
   }
 }
 
@@ -153,9 +251,9 @@ __global__ void __launch_bounds__(kLossThreads)
   if (threadIdx.x == 0) *out = v;
 }
 
-cudaError_t launch_cross_entropy(float* logits, const float2* row_stats, int stats_cols,
+cudaError_t launch_cross_entropy(float* logits, const float4* row_stats, int stats_cols,
                                  const int32_t* targets, float* losses, float* loss_sum, int M,
-                                 int V, float alpha, float beta, float inv_norm,
+                                 int V, float alpha, float beta, float inv_norm, unsigned* done,
                                  cudaStream_t stream) {
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -163,13 +261,16 @@ cudaError_t launch_cross_entropy(float* logits, const float2* row_stats, int sta
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)M, 1, 1);
   cfg.blockDim = dim3(kLossThreads, 1, 1);
+  cfg.dynamicSmemBytes = kLossSmemBytes;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, lin_cross_entropy_kernel, logits, row_stats,
-                                     stats_cols, targets, losses, V, alpha, beta, inv_norm);
-  if (e != cudaSuccess) return e;
+                                     stats_cols, targets, losses, V, alpha, beta, inv_norm, done,
+                                     loss_sum);
+  if (e != cudaSuccess || done) return e;
   cfg.gridDim = dim3(1, 1, 1);
+  cfg.dynamicSmemBytes = 0;
   return cudaLaunchKernelEx(&cfg, lin_sum_losses_kernel, (const float*)losses, M, loss_sum);
 }
 

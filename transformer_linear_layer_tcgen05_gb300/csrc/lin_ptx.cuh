@@ -100,6 +100,17 @@ __device__ __forceinline__ float4 ld_shared_v4f(uint32_t addr) {
   return v;
 }
 
+// 16-byte asynchronous copy global -> shared that bypasses the registers
+// (cached in L2 only); this thread's copies are complete after
+// cp_async_wait_all.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ mbarrier
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
@@ -438,17 +449,6 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster)
-      : "memory");
-}
-
-// Arrive on an mbarrier of another CTA of the cluster and raise its
-// transaction count by `bytes` (address from mapa).
-__device__ __forceinline__ void mbar_arrive_expect_tx_remote(uint32_t cluster_addr,
-                                                             uint32_t bytes) {
-  asm volatile(
-      "mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(
-          cluster_addr),
-      "r"(bytes)
       : "memory");
 }
 
