@@ -1,0 +1,48 @@
+"""The forward f32 SwiGLU form in the per-tile kernel with both tile widths
+(128 and 256 columns; the library takes 256 when N > 256), bit-exact against
+the oracle on small-integer inputs: ragged rows and columns (a last column
+tile of 8), and the K split through the workspace and the split-sum kernel.
+Each width runs in a child process of its own (LIN_F32_SWIGLU_BN is read
+once per process). A child also fails on a device status other than
+success."""
+
+import os
+import subprocess
+import sys
+
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+CHILD = r"""
+import sys
+import numpy as np
+sys.path.insert(0, sys.argv[1])
+import oracle
+from tests.gpu_util import integer_inputs, require_gpu, run_device, to_device
+from transformer_linear_layer_tcgen05_gb300 import lin
+require_gpu()
+bad = 0
+form = "matmul_residual_swiglu_a"
+for (M, N, K) in [(300, 264, 68), (128, 392, 256), (129, 520, 1028), (512, 768, 3072),
+                  (1, 1032, 64)]:
+    d = integer_inputs(form, M, N, K, seed=M + N + K)
+    Y = run_device(form, to_device(d), M, N).cpu().numpy().astype(np.float64)
+    Yref, _ = oracle.reference(form, d)
+    st = lin.lin_get_device_status()
+    nd = int(np.sum(Y != Yref))
+    if nd or st != lin.LIN_SUCCESS:
+        print(f"{M}x{N}x{K}: status {st}, {nd} mismatches", flush=True)
+    bad += nd + (st != lin.LIN_SUCCESS)
+sys.exit(1 if bad else 0)
+"""
+
+
+@pytest.mark.parametrize("bn", ["128", "256"])
+def test_f32_swiglu_tile_widths_exact(bn):
+    env = dict(os.environ, LIN_F32_SWIGLU_BN=bn)
+    r = subprocess.run([sys.executable, "-c", CHILD, ROOT], env=env, cwd=ROOT,
+                       stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout[-4000:]

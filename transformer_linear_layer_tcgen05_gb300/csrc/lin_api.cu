@@ -255,6 +255,22 @@ bool f16_pair(long long pair_tiles, int sms) {
   return pair_tiles >= (long long)sms;
 }
 
+// Tile width of the per-tile kernel for the forward f32 SwiGLU form, whose
+// transform warps build each row block's A once per column tile: 256
+// columns (half the rebuilds) when N spans more than one such tile, else
+// 128. Measured on 512 x 768 x 3072 (cold / warm us): 30.4 / 22.5 with 128,
+// 25.3 / 17.2 with 256. LIN_F32_SWIGLU_BN=128 / 256 forces it
+// (measurements).
+int f32_swiglu_bn(uint64_t N) {
+  static const int forced = [] {
+    const char* v = std::getenv("LIN_F32_SWIGLU_BN");
+    if (!v) return -1;
+    return std::strcmp(v, "128") == 0 ? 128 : (std::strcmp(v, "256") == 0 ? 256 : -1);
+  }();
+  if (forced > 0) return forced;
+  return N > 256 ? 256 : 128;
+}
+
 enum Form : int { F_MATMUL = 0, F_RESID = 1, F_SWIGLU = 2 };
 
 // In the kernels' terms: Y[M,N] = A[M,K] · B[K,N] (+ R), A = X or
@@ -406,7 +422,7 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
   }
 
   // 8. tensor maps and launch
-  const int bn = 128;
+  const int bn = (swiglu && !p.w16 && !p.at && !p.bt) ? f32_swiglu_bn(N) : 128;
   int cn = (p.w16 && !p.at) ? f16_cluster_size(N) : 0;   // 0: the per-tile kernel
   // the row partials and the dual product exist in the clustered kernel only
   if ((p.row_stats || p.W2) && cn == 0) cn = 1;
@@ -682,9 +698,9 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
 }
 
 // lm_head (logits = X @ W16 into DLOGITS) and the fused cross-entropy of
-// page 07_loss on them: the GEMM's epilogue leaves online-softmax partials
-// per row, the loss kernel turns the logits into dLogits in place and
-// writes the per-row losses, and a last kernel their sum.
+// page 07_loss on them: the GEMM's epilogue leaves per-row partials, the
+// loss kernel turns the logits into dLogits in place, writes the per-row
+// losses, and its last CTA their sum.
 lin_status lm_head_cross_entropy(const float* X, const uint16_t* W16, const int32_t* targets,
                                  float* dlogits, float* losses, float* loss_sum, int64_t M,
                                  int64_t V, int64_t K, float alpha, float beta, float inv_norm,

@@ -124,8 +124,11 @@ struct GemmTraits {
   static constexpr uint32_t IDESC =
       umma_idesc(kF16 ? 0u : 2u, /*a_mn_major=*/kAmn, /*b_mn_major=*/!BT, BM, BN);
 
+  // A cluster split keeps the partial tile in the operand ring; the forward
+  // SwiGLU form (a workspace split only) may have a smaller ring.
+  static constexpr bool kClusterSplitOK = NS * OP_STAGE_BYTES >= BM * BN * 4;
   static_assert(NS >= 2, "operand ring needs two stages");
-  static_assert(NS * OP_STAGE_BYTES >= BM * BN * 4, "a cluster split's partial tile in the ring");
+  static_assert(kClusterSplitOK || (kSwiglu && !kTransA), "a cluster split's partial tile in the ring");
   static_assert(NR <= 4 && NS <= 8, "barrier slots");
   static_assert(!kXform || NR * RAW_STAGE_BYTES >= EPI_BYTES, "epilogue aliasing");
   static_assert(OFF_ABORT + 4 <= BAR_REGION, "barrier region");
@@ -363,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool split = gridDim.z > 1;
   // ... or, with KFLAG_CLUSTER_SPLIT, keeps it in shared memory for the
   // cluster's sum (cluster dims (1, 1, gridDim.z): CTA rank = blockIdx.z).
-  const bool csplit = split && (args.flags & KFLAG_CLUSTER_SPLIT) != 0;
+  const bool csplit = T::kClusterSplitOK && split && (args.flags & KFLAG_CLUSTER_SPLIT) != 0;
   const int kb0 = (int)blockIdx.z * nkb_all / (int)gridDim.z;
   const int nkb = ((int)blockIdx.z + 1) * nkb_all / (int)gridDim.z - kb0;
   const bool withhold = (args.flags & KFLAG_WITHHOLD_PRODUCER) != 0;
@@ -777,7 +780,8 @@ cudaError_t launch_instance(const TensorMaps& m, const KernelArgs& args, cudaStr
             (unsigned)(args.split_s > 1 ? args.split_s : 1));
   if (args.flags & KFLAG_WITHHOLD_PRODUCER) grid = dim3(1, 1, 1);
   const bool csplit = grid.z > 1 && (args.flags & KFLAG_CLUSTER_SPLIT) != 0;
-  if (csplit && grid.z > (unsigned)kMaxClusterSplit) return cudaErrorInvalidValue;
+  if (csplit && (grid.z > (unsigned)kMaxClusterSplit || !T::kClusterSplitOK))
+    return cudaErrorInvalidValue;
   if (csplit && dev < 64) {
     // The largest split up to the one asked for whose clusters are all
     // resident at once (clusters of S CTAs of this size per GPC set the

@@ -12,6 +12,10 @@ cudaError_t launch_gemm_tf32(int amode, bool resid, int bn, bool bt, const Tenso
     return resid ? launch_instance<A_TMA_F32, true, 128, true>(maps, args, stream)
                  : launch_instance<A_TMA_F32, false, 128, true>(maps, args, stream);
   }
+  // the forward SwiGLU form also in 256-column tiles (each row block's
+  // SwiGLU A built half as often)
+  if (amode == A_SWIGLU_F32 && resid && bn == 256)
+    return launch_instance<A_SWIGLU_F32, true, 256>(maps, args, stream);
   if (bn != 128) return cudaErrorInvalidValue;
   if (amode == A_TMA_F32)
     return resid ? launch_instance<A_TMA_F32, true, 128>(maps, args, stream)
