@@ -103,6 +103,17 @@
  * lin_get_device_status() call reports and clears it. This is never expected
  * on a correct build; it exists so a scheduling bug cannot hang the GPU.
  *
+ * Checked build. The same sources compiled with LIN_DEVICE_CHECKS=1 (the
+ * library liblin_checked.so, built beside liblin.so) check, inside the
+ * kernels, every shared-memory stage and buffer index, TMEM column range,
+ * TMA coordinate alignment, cluster peer rank, and every global index that
+ * is not a TMA access (partial tiles, row partials, transform and loss
+ * loads) against its buffer. A failed check skips the access and records
+ * LIN_ERROR_DEVICE_CHECK with the site and the offending value (a skipped
+ * load then makes a bounded wait run out: the kernel still exits cleanly);
+ * lin_get_device_status() reports it and lin_last_device_check() tells
+ * which. In liblin.so the checks compile away.
+ *
  * Thread safety: every entry point may be called from several host threads.
  */
 #ifndef LIN_H
@@ -125,7 +136,8 @@ typedef enum lin_status {
   LIN_ERROR_ALIASING = 4,
   LIN_ERROR_UNSUPPORTED_DEVICE = 5,
   LIN_ERROR_CUDA = 6,
-  LIN_ERROR_TIMEOUT = 7
+  LIN_ERROR_TIMEOUT = 7,
+  LIN_ERROR_DEVICE_CHECK = 8
 } lin_status;
 
 /* Y[M,N] = X[M,K] @ W[K,N]; X, W, Y binary32.
@@ -379,9 +391,19 @@ int lin_last_cuda_error(void);
 void lin_last_launch_info(int* kernels, uint64_t* workspace_bytes);
 
 /* Waits for `stream`, then returns and clears the current device's status
- * word: LIN_SUCCESS, or LIN_ERROR_TIMEOUT if a kernel gave up on a wait since
- * the last call. Returns LIN_ERROR_CUDA if the synchronisation itself fails. */
+ * word: LIN_SUCCESS, LIN_ERROR_TIMEOUT if a kernel gave up on a wait since
+ * the last call, or LIN_ERROR_DEVICE_CHECK if a check of the checked build
+ * failed first (the first failure is the one kept). Returns LIN_ERROR_CUDA if
+ * the synchronisation itself fails. */
 lin_status lin_get_device_status(lin_stream_t stream);
+
+/* The check behind the calling thread's last LIN_ERROR_DEVICE_CHECK from
+ * lin_get_device_status(): its site (1 TMA coordinate alignment, 2 operand
+ * stage, 3 epilogue or staging buffer, 4 TMEM column, 5 partial-tile index,
+ * 6 row-partial index, 7 other global index, 8 cluster peer rank, 9 barrier
+ * slot, 99 the self-test) and the offending value; 0 and 0 if none. Either
+ * pointer may be NULL. */
+void lin_last_device_check(int *site, int64_t *value);
 
 /* Self-test of the bounded waits: enqueues one small kernel whose data
  * producer is told never to start, so every consumer's wait runs out after
@@ -390,6 +412,14 @@ lin_status lin_get_device_status(lin_stream_t stream);
  * status word (then cleared): LIN_ERROR_TIMEOUT when the mechanism works.
  * No memory is touched. */
 lin_status lin_selftest_wait_timeout(int64_t timeout_us, lin_stream_t stream);
+
+/* Self-test of the device-check record: enqueues one single-thread kernel
+ * that reports a failed check (site 99, value `value`) the way every check
+ * of the checked build does, without touching any other memory. Waits for
+ * `stream` and returns the status word (then cleared): LIN_ERROR_DEVICE_CHECK
+ * when the mechanism works, after which lin_last_device_check() gives 99 and
+ * `value`. Works in either build. */
+lin_status lin_selftest_device_check(int64_t value, lin_stream_t stream);
 
 /* Library version: major * 10000 + minor * 100 + patch. */
 int lin_version(void);

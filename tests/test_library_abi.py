@@ -42,6 +42,18 @@ def test_every_declared_symbol_is_exported(L):
         assert hasattr(L, name), name
 
 
+def test_checked_build_exports_the_same_symbols():
+    # the checked build (device checks on) is the same ABI in another file
+    import ctypes
+    path = build.build_library(checked=True)
+    assert path.endswith("liblin_checked.so") and path != build.LIB_PATH
+    C = ctypes.CDLL(path)
+    for name in declared_functions():
+        assert hasattr(C, name), name
+    C.lin_status_string.restype = ctypes.c_char_p
+    assert C.lin_status_string(8) == b"LIN_ERROR_DEVICE_CHECK"
+
+
 def test_binding_covers_every_compute_entry_point():
     for name in declared_functions():
         if name.startswith("lin_matmul"):

@@ -5,6 +5,11 @@ Every translation unit is compiled for sm_103a only
 shared library next to this file. Object files go to ``_build/`` at the
 repository root. A rebuild happens only when a source or header is newer than
 the library.
+
+``build_library(checked=True)`` builds the same sources with
+``-DLIN_DEVICE_CHECKS=1`` into ``liblin_checked.so`` (objects in
+``_build/checked/``): the checked build, whose kernels check their shared
+memory, TMEM, TMA-coordinate and global indices (include/lin.h).
 """
 
 from __future__ import annotations
@@ -20,6 +25,7 @@ CSRC = os.path.join(PKG_DIR, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "liblin.so")
+CHECKED_LIB_PATH = os.path.join(PKG_DIR, "liblin_checked.so")
 
 SOURCES = ["lin_api.cu", "lin_kernels_tf32.cu", "lin_kernels_f16.cu",
            "lin_kernels_cluster_swiglu.cu", "lin_kernels_cluster_cvt.cu",
@@ -45,23 +51,30 @@ def _inputs() -> list[str]:
     return files
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH):
+def up_to_date(checked: bool = False) -> bool:
+    lib = CHECKED_LIB_PATH if checked else LIB_PATH
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(f) <= t for f in _inputs())
 
 
-def build_library(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile and link liblin.so; return its path. Raises on any failure."""
-    if not force and up_to_date():
-        return LIB_PATH
+def build_library(force: bool = False, verbose: bool = False, extra_flags=(),
+                  checked: bool = False) -> str:
+    """Compile and link liblin.so (or, ``checked``, liblin_checked.so); return
+    its path. Raises on any failure."""
+    lib_path = CHECKED_LIB_PATH if checked else LIB_PATH
+    if not force and up_to_date(checked):
+        return lib_path
     nvcc = _nvcc()
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    build_dir = os.path.join(BUILD_DIR, "checked") if checked else BUILD_DIR
+    os.makedirs(build_dir, exist_ok=True)
+    if checked:
+        extra_flags = (*extra_flags, "-DLIN_DEVICE_CHECKS=1")
     procs = []
     objs = []
     for src in SOURCES:
-        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
+        obj = os.path.join(build_dir, src.replace(".cu", ".o"))
         objs.append(obj)
         cmd = [nvcc, *ARCH, *CFLAGS, *extra_flags, *os.environ.get("LIN_NVCC_FLAGS", "").split(),
                "-c", os.path.join(CSRC, src), "-o", obj]
@@ -78,16 +91,17 @@ def build_library(force: bool = False, verbose: bool = False, extra_flags=()) ->
             failed.append(f"{src}:\n{out}")
     if failed:
         raise RuntimeError("nvcc failed:\n" + "\n".join(failed))
-    tmp = LIB_PATH + ".tmp"
+    tmp = lib_path + ".tmp"
     link = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
     if verbose:
         print(" ".join(link), file=sys.stderr)
     r = subprocess.run(link, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n" + r.stdout)
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
-    print(build_library(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build_library(force="--force" in sys.argv, verbose="-v" in sys.argv,
+                        checked="--checked" in sys.argv))

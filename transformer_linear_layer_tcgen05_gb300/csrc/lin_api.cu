@@ -15,13 +15,17 @@
 
 namespace lin_detail {
 
-// Per-device status word written by kernels whose bounded waits ran out.
-__device__ int g_status_word;
+// Per-device status record written by kernels whose bounded waits ran out
+// or (checked build) whose device checks failed: [status, check site, check
+// value as int64].
+__device__ __align__(16) int g_status_word[4];
 
 constexpr uint64_t kDefaultTimeoutNs = 1000ull * 1000ull * 1000ull;   // 1 s per wait
 constexpr int kMaxDevices = 64;
 
 thread_local int t_last_cuda_error = 0;
+thread_local int t_last_check_site = 0;         // lin_last_device_check
+thread_local int64_t t_last_check_value = 0;
 thread_local int t_last_kernels = 0;            // lin_last_launch_info
 thread_local uint64_t t_last_workspace = 0;
 
@@ -600,6 +604,7 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
     const size_t xh_bytes = tma_a ? (size_t)M * (size_t)K * 2 : 0;
     const size_t need = xh_bytes ? xh_off + xh_bytes : part_bytes;
     const int got = need ? take_workspace(need) : 0;
+    args.part_f4 = got > 0 ? (int64_t)(part_bytes / 16) : 0;
     if (got < 0) return LIN_ERROR_UNSUPPORTED_SHAPE;
     if (got == 0 && tma_a) {   // no memory for the pre-pass: transform X in the GEMM
       tma_a = false;
@@ -668,6 +673,7 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
     } else if (split >= 2) {
       const size_t bytes = (size_t)tiles * split * lin::kBM * bn * sizeof(float);
       const int got = take_workspace(bytes);
+      args.part_f4 = got > 0 ? (int64_t)(bytes / 16) : 0;
       if (got < 0) return LIN_ERROR_UNSUPPORTED_SHAPE;
       if (got > 0) {
         args.split_r = 0;
@@ -785,7 +791,7 @@ lin_status lm_head_cross_entropy(const float* X, const uint16_t* W16, const int3
   if (st == LIN_SUCCESS && done && K == 0) e = cudaMemsetAsync(done, 0, 4, stream);
   if (st == LIN_SUCCESS && e == cudaSuccess)
     e = lin::launch_cross_entropy(dlogits, p.row_stats, cols, targets, losses, loss_sum,
-                                  (int)M, (int)V, alpha, beta, inv_norm, done, stream);
+                                  (int)M, (int)V, alpha, beta, inv_norm, done, word, stream);
   if (ws) {
     const cudaError_t ef = cudaFreeAsync(ws, stream);
     if (e == cudaSuccess) e = ef;
@@ -840,13 +846,20 @@ lin_status read_and_clear_status(cudaStream_t stream) {
   if (st != LIN_SUCCESS) return st;
   cudaError_t e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) return cuda_fail(e);
-  int v = 0;
-  e = cudaMemcpyFromSymbol(&v, g_status_word, sizeof(int));
+  int v[4] = {0, 0, 0, 0};
+  e = cudaMemcpyFromSymbol(v, g_status_word, sizeof(v));
   if (e != cudaSuccess) return cuda_fail(e);
-  const int zero = 0;
-  e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof(int));
+  const int zero[4] = {0, 0, 0, 0};
+  e = cudaMemcpyToSymbol(g_status_word, zero, sizeof(zero));
   if (e != cudaSuccess) return cuda_fail(e);
-  return v == lin::KSTATUS_TIMEOUT ? LIN_ERROR_TIMEOUT : LIN_SUCCESS;
+  if (v[0] == lin::KSTATUS_CHECK) {
+    t_last_check_site = v[1];
+    int64_t value = 0;
+    std::memcpy(&value, v + 2, sizeof(value));
+    t_last_check_value = value;
+    return LIN_ERROR_DEVICE_CHECK;
+  }
+  return v[0] == lin::KSTATUS_TIMEOUT ? LIN_ERROR_TIMEOUT : LIN_SUCCESS;
 }
 
 }  // namespace lin_detail
@@ -1022,6 +1035,7 @@ const char* lin_status_string(lin_status status) {
     case LIN_ERROR_UNSUPPORTED_DEVICE: return "LIN_ERROR_UNSUPPORTED_DEVICE";
     case LIN_ERROR_CUDA: return "LIN_ERROR_CUDA";
     case LIN_ERROR_TIMEOUT: return "LIN_ERROR_TIMEOUT";
+    case LIN_ERROR_DEVICE_CHECK: return "LIN_ERROR_DEVICE_CHECK";
   }
   return "LIN_ERROR_UNKNOWN";
 }
@@ -1035,6 +1049,22 @@ void lin_last_launch_info(int* kernels, uint64_t* workspace_bytes) {
 
 lin_status lin_get_device_status(lin_stream_t stream) {
   return read_and_clear_status(reinterpret_cast<cudaStream_t>(stream));
+}
+
+void lin_last_device_check(int* site, int64_t* value) {
+  if (site) *site = t_last_check_site;
+  if (value) *value = t_last_check_value;
+}
+
+lin_status lin_selftest_device_check(int64_t value, lin_stream_t stream) {
+  int dev = 0;
+  int* word = nullptr;
+  lin_status st = current_device(&dev, &word);
+  if (st != LIN_SUCCESS) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = lin::launch_selftest_check(word, (long long)value, s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return read_and_clear_status(s);
 }
 
 lin_status lin_selftest_wait_timeout(int64_t timeout_us, lin_stream_t stream) {

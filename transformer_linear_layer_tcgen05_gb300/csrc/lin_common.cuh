@@ -8,7 +8,38 @@
 #include "lin_internal.h"
 #include "lin_ptx.cuh"
 
+#ifndef LIN_DEVICE_CHECKS
+#define LIN_DEVICE_CHECKS 0
+#endif
+
 namespace lin {
+
+// ---------------------------------------------------------------- checks
+
+// Record a failed check in the status record [status, site, value]: the
+// first failure of any kind keeps the record.
+__device__ __forceinline__ void report_check(int* status, int site, long long value) {
+  if (status && atomicCAS(status, KSTATUS_OK, KSTATUS_CHECK) == KSTATUS_OK) {
+    status[1] = site;
+    *reinterpret_cast<long long*>(status + 2) = value;
+  }
+}
+
+// Checked build (LIN_DEVICE_CHECKS=1): true when the access guarded by `ok`
+// may go ahead; otherwise the failure is recorded and the caller skips the
+// access. In the default build it is true and compiles away.
+__device__ __forceinline__ bool dcheck(bool ok, int* status, int site, long long value) {
+#if LIN_DEVICE_CHECKS
+  if (!ok) report_check(status, site, value);
+  return ok;
+#else
+  (void)ok;
+  (void)status;
+  (void)site;
+  (void)value;
+  return true;
+#endif
+}
 
 // ---------------------------------------------------------------- waiting
 

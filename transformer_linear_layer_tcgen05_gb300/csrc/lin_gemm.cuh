@@ -289,6 +289,11 @@ __device__ __forceinline__ void cluster_split_sum(uint32_t part, int S, int rank
       o[j] = live[j] ? (size_t)row * (size_t)args.N + (size_t)col : 0;
       if (!live[j]) continue;
       const uint32_t off = part + csplit_off<T>(r, c4);
+      if (!dcheck(csplit_off<T>(r, c4) + 16 <= T::NS * T::OP_STAGE_BYTES && S <= kMaxClusterSplit,
+                  args.status, CHK_BUFFER, csplit_off<T>(r, c4))) {
+        live[j] = false;
+        continue;
+      }
 #pragma unroll
       for (int p = 0; p < kMaxClusterSplit; ++p)
         if (p < S) v[j][p] = ld_cluster_v4f(mapa_shared(off, (uint32_t)p));
@@ -371,6 +376,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nkb = ((int)blockIdx.z + 1) * nkb_all / (int)gridDim.z - kb0;
   const bool withhold = (args.flags & KFLAG_WITHHOLD_PRODUCER) != 0;
   const WaitCtl ctl{args.timeout_ns, abort_flag, args.status};
+  // Checked build: a TMA copy's innermost coordinate x (elements of esz
+  // bytes) on a 16-byte boundary; a ring slot inside its ring.
+  auto x_ok = [&](int x, int esz) -> bool {
+    return dcheck((x * esz) % 16 == 0, args.status, CHK_TMA_X, x);
+  };
+  auto slot_ok = [&](int slot, int n) -> bool {
+    return dcheck(slot >= 0 && slot < n, args.status, CHK_STAGE, slot);
+  };
 
   auto a_stage = [&](int s) -> uint32_t { return sbase + T::OFF_OP + s * T::OP_STAGE_BYTES; };
   auto b_stage = [&](int s) -> uint32_t { return a_stage(s) + T::A_BYTES; };
@@ -432,26 +445,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n = kb / T::NS;
         if (kb >= T::NS && !lane0_wait_phase(bar(T::BAR_OP_EMPTY + st), (n - 1) & 1, ctl, lane))
           break;
+        const int kk = (kb0 + kb) * T::BK;
+        // (x of every copy below: kk along K, m0 + j*32 or n0 + j*W_ATOM along
+        // M or N, all multiples of 16 bytes; a skipped copy makes the
+        // stage's wait run out)
+        const bool go = slot_ok(st, T::NS) && x_ok(kk, T::kBT ? T::ESZ : 4) && x_ok(m0, 4) &&
+                        x_ok(n0, T::ESZ);
         if (lane == 0) {
           const uint32_t full = bar(T::BAR_OP_TMA + st);
           mbar_arrive_expect_tx(full, T::OP_TMA_BYTES);
-          const int kk = (kb0 + kb) * T::BK;
-          if constexpr (T::kAmn) {
-            // X^T: BM/32 boxes of [32 rows of the contraction][32 of the tile's rows]
+          if (go) {
+            if constexpr (T::kAmn) {
+              // X^T: BM/32 boxes of [32 rows of the contraction][32 of the tile's rows]
 #pragma unroll
-            for (int j = 0; j < T::BM / 32; ++j)
-              tma_load_2d(a_stage(st) + j * 4096, &tm_a, m0 + j * 32, kk, full);
-          } else if constexpr (!T::kXformA) {
-            tma_load_2d(a_stage(st), &tm_a, kk, m0, full);
-          }
-          if constexpr (T::kBT) {
-            // W as [N][K]: the tile's BN rows, this k-block's 128 bytes
-            tma_load_2d(b_stage(st), &tm_w, kk, n0, full);
-          } else {
-            // W as [K][N]: 128-byte runs of W_ATOM columns, BK rows each
+              for (int j = 0; j < T::BM / 32; ++j)
+                tma_load_2d(a_stage(st) + j * 4096, &tm_a, m0 + j * 32, kk, full);
+            } else if constexpr (!T::kXformA) {
+              tma_load_2d(a_stage(st), &tm_a, kk, m0, full);
+            }
+            if constexpr (T::kBT) {
+              // W as [N][K]: the tile's BN rows, this k-block's 128 bytes
+              tma_load_2d(b_stage(st), &tm_w, kk, n0, full);
+            } else {
+              // W as [K][N]: 128-byte runs of W_ATOM columns, BK rows each
 #pragma unroll
-            for (int j = 0; j < T::W_BOXES; ++j)
-              tma_load_2d(b_stage(st) + j * T::B_ATOM_BYTES, &tm_w, n0 + j * T::W_ATOM, kk, full);
+              for (int j = 0; j < T::W_BOXES; ++j)
+                tma_load_2d(b_stage(st) + j * T::B_ATOM_BYTES, &tm_w, n0 + j * T::W_ATOM, kk,
+                            full);
+            }
           }
         }
         __syncwarp();
@@ -470,10 +491,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t ph = (kb / T::NS) & 1;
       if (T::OP_TMA_BYTES > 0 && !lane0_wait_phase(bar(T::BAR_OP_TMA + st), ph, ctl, lane)) break;
       if (T::kXform && !lane0_wait_phase(bar(T::BAR_OP_XF + st), ph, ctl, lane)) break;
+      const bool mma_ok = slot_ok(st, T::NS);   // (checked build; skipped UMMAs, not the commit)
       if (lane == 0) {
         tc_fence_after_sync();
 #pragma unroll
         for (int k = 0; k < T::NMMA; ++k) {
+          if (!mma_ok) break;
           // K-major A: a K step is 32 bytes along the row; MN-major X^T: KSTEP
           // rows of 128 bytes, runs of 32 tile rows 4096 bytes apart
           const uint64_t adesc =
@@ -513,11 +536,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n = t / T::NR;
         if (t >= T::NR && !lane0_wait_phase(bar(T::BAR_RAW_EMPTY + r), (n - 1) & 1, ctl, lane))
           break;
+        const int kk = (kb0 * T::RAW_PER_KB + t) * 32;   // f32 column of this raw stage
+        const bool go = slot_ok(r, T::NR) && x_ok(kk, 4) && x_ok(m0, 4);
         if (lane == 0) {
           const uint32_t full = bar(T::BAR_RAW_FULL + r);
           mbar_arrive_expect_tx(full, T::RAW_STAGE_BYTES);
-          const int kk = (kb0 * T::RAW_PER_KB + t) * 32;   // f32 column of this raw stage
-          if constexpr (T::kTransA) {
+          if (!go) {
+            // (checked build: the stage's wait runs out)
+          } else if constexpr (T::kTransA) {
             // X^T: BM/32 boxes of [32 rows of the contraction][32 of the tile's rows]
 #pragma unroll
             for (int j = 0; j < T::BM / 32; ++j) {
@@ -580,6 +606,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int row0 = m0 + q * kEpiRows;
     const bool rows_in = row0 < args.M;      // a box starting past M would store nothing
+    // checked build: chunk c's TMEM columns inside the accumulator
+    auto tcol_ok = [&](int c) -> bool {
+      return dcheck(c >= 0 && (c + 1) * kEpiCols <= BN, args.status, CHK_TMEM, c * kEpiCols);
+    };
     const uint32_t buf0 = sbase + T::OFF_EPI + (uint32_t)(q * 2) * T::EPI_BUF_BYTES;
     const uint32_t ebar0 = bar(T::BAR_EPI + q * 2);
     constexpr int NC = BN / kEpiCols;
@@ -599,21 +629,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = q * kEpiRows + lane;
         for (int c = 0; c < nc; ++c) {
           uint32_t v[32];
+          if (!tcol_ok(c)) break;
           tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * kEpiCols), v);
           tmem_wait_ld();
 #pragma unroll
           for (int j = 0; j < 8; ++j)
-            st_shared_v4(sbase + T::OFF_OP + csplit_off<T>(r, c * 8 + j), v[4 * j + 0],
-                         v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+            if (dcheck(csplit_off<T>(r, c * 8 + j) + 16 <= T::NS * T::OP_STAGE_BYTES, args.status,
+                       CHK_BUFFER, csplit_off<T>(r, c * 8 + j)))
+              st_shared_v4(sbase + T::OFF_OP + csplit_off<T>(r, c * 8 + j), v[4 * j + 0],
+                           v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
         }
       } else if (ok) {
         const size_t tile = (size_t)blockIdx.y * gridDim.x + blockIdx.x;
         float4* part = reinterpret_cast<float4*>(args.part) +
                        (tile * gridDim.z + blockIdx.z) * (BN / 4) * T::BM + q * kEpiRows + lane;
+        const long long part_at = (long long)(tile * gridDim.z + blockIdx.z) * (BN / 4) * T::BM +
+                                  q * kEpiRows + lane;
         for (int c = 0; c < nc; ++c) {
           uint32_t v[32];
+          if (!tcol_ok(c)) break;
           tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * kEpiCols), v);
           tmem_wait_ld();
+          if (!dcheck(part_at + (long long)(c * 8 + 7) * T::BM < args.part_f4, args.status,
+                      CHK_PART, part_at + (long long)(c * 8 + 7) * T::BM))
+            break;
 #pragma unroll
           for (int j = 0; j < 8; ++j)
             part[(size_t)(c * 8 + j) * T::BM] =
@@ -625,7 +664,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (!split && RESID && rows_in && !withhold && lane == 0 && nc > 0) {
       mbar_arrive_expect_tx(ebar0, T::EPI_BUF_BYTES);
-      tma_load_2d(buf0, &tm_r, n0, row0, ebar0);
+      if (x_ok(n0, 4)) tma_load_2d(buf0, &tm_r, n0, row0, ebar0);
       r_issued = 1;
     }
     if (!split) {
@@ -645,8 +684,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
           bulk_wait_group_read<0>();   // the last stores have read both buffers
           mbar_arrive_expect_tx(ebar0, 2 * T::EPI_BUF_BYTES);
-          tma_load_2d(bg, &tm_g2, n0 + c * kEpiCols, row0, ebar0);
-          tma_load_2d(bu, &tm_u2, n0 + c * kEpiCols, row0, ebar0);
+          if (x_ok(n0 + c * kEpiCols, 4)) {
+            tma_load_2d(bg, &tm_g2, n0 + c * kEpiCols, row0, ebar0);
+            tma_load_2d(bu, &tm_u2, n0 + c * kEpiCols, row0, ebar0);
+          }
           sw_issued = c + 1;
           if (c + 1 < nc) {   // the next chunk's GATE and UP into L2
             tma_prefetch_l2_2d(&tm_g2, n0 + (c + 1) * kEpiCols, row0);
@@ -655,7 +696,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         uint32_t v[32];
-        tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * kEpiCols), v);
+        if (tcol_ok(c))
+          tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * kEpiCols), v);
         tmem_wait_ld();
         if (!warp_wait_phase(ebar0, c & 1, ctl)) break;
         sw_done = c + 1;
@@ -677,8 +719,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_store_2d(&tm_y, n0 + c * kEpiCols, row0, bg);
-          tma_store_2d(&tm_y2, n0 + c * kEpiCols, row0, bu);
+          if (x_ok(n0 + c * kEpiCols, 4)) {
+            tma_store_2d(&tm_y, n0 + c * kEpiCols, row0, bg);
+            tma_store_2d(&tm_y2, n0 + c * kEpiCols, row0, bu);
+          }
           bulk_commit_group();
         }
       }
@@ -692,14 +736,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           if constexpr (RESID) {
             const uint32_t nb = ebar0 + 8u * (uint32_t)(b ^ 1);
             mbar_arrive_expect_tx(nb, T::EPI_BUF_BYTES);
-            tma_load_2d(buf0 + (b ^ 1) * T::EPI_BUF_BYTES, &tm_r, n0 + (c + 1) * kEpiCols, row0,
-                        nb);
+            if (x_ok(n0 + (c + 1) * kEpiCols, 4))
+              tma_load_2d(buf0 + (b ^ 1) * T::EPI_BUF_BYTES, &tm_r, n0 + (c + 1) * kEpiCols, row0,
+                          nb);
             r_issued = c + 2;
           }
         }
         __syncwarp();
         uint32_t v[32];
-        tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * kEpiCols), v);
+        if (tcol_ok(c))
+          tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * kEpiCols), v);
         tmem_wait_ld();
         if constexpr (RESID) {
           if (!warp_wait_phase(ebar0 + 8u * (uint32_t)b, (c >> 1) & 1, ctl)) break;
@@ -725,7 +771,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_store_2d(&tm_y, n0 + c * kEpiCols, row0, buf);
+          if (x_ok(n0 + c * kEpiCols, 4)) tma_store_2d(&tm_y, n0 + c * kEpiCols, row0, buf);
           bulk_commit_group();
         }
       }

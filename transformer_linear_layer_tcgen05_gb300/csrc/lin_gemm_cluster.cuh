@@ -221,9 +221,10 @@ struct Staged {
 template <typename T>
 __device__ __forceinline__ void stage_load(Staged<T>& st, const float* __restrict__ a,
                                            const float* __restrict__ u, int row0, int k0,
-                                           int M, int K, int tw, int lane) {
+                                           int M, int K, int tw, int lane, int* status) {
   const int col = k0 + T::CHUNK * (lane % T::LANES_PER_ROW);
-  const bool col_in = col < K;
+  // (K is a multiple of CHUNK on each path: a load is wholly in or out)
+  const bool col_in = col < K && dcheck(col + T::CHUNK <= K, status, CHK_GLOBAL, col);
   const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
   for (int q = 0; q < T::LPI; ++q) {
@@ -275,12 +276,14 @@ __device__ __forceinline__ void stage_compute(const Staged<T>& st,
 // rows. Either way each row's bytes spread over all 32 banks once.
 template <typename T>
 __device__ __forceinline__ void stage_store(uint32_t a_stage, uint32_t crank, int tw, int lane,
-                                            const uint32_t (&out)[T::LPI][T::CHUNK / 2]) {
+                                            const uint32_t (&out)[T::LPI][T::CHUNK / 2],
+                                            int* status) {
   const uint32_t c = (uint32_t)(lane % T::LANES_PER_ROW);
 #pragma unroll
   for (int q = 0; q < T::LPI; ++q) {
     const uint32_t r = crank * (uint32_t)T::ROWS +
                        (uint32_t)(tw * T::RW + q * T::ROWS_PER_LOAD + lane / T::LANES_PER_ROW);
+    if (!dcheck(r < (uint32_t)T::BM, status, CHK_STAGE, r)) continue;
     if constexpr (T::V8)
       st_shared_v4(a_stage + sw128(r, c), out[q][0], out[q][1], out[q][2], out[q][3]);
     else
@@ -451,6 +454,11 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
           else if (crank == 0)
             mbar_arrive_expect_tx(full, 2 * bytes);
           auto load = [&](uint32_t dst, const CUtensorMap* map, int x, int y) {
+            // every map here holds binary16: x a multiple of 8 elements
+            if (!dcheck((x & 7) == 0, args.status, CHK_TMA_X, x)) return;
+            if (!dcheck(dst >= sbase + T::OFF_A && dst < sbase + T::OFF_EPI, args.status,
+                        CHK_STAGE, (long long)(dst - sbase)))
+              return;
             if constexpr (T::kPair)
               tma_load_2d_pair(dst, map, x, y, full0);
             else
@@ -536,10 +544,16 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
           ok = false;
           break;
         }
+        // (checked build: the stages and the accumulator's columns in range;
+        // a failed check skips the UMMAs, not the commit)
+        const bool mma_ok =
+            dcheck(sa < T::NA && s < T::NW, args.status, CHK_STAGE, g) &&
+            dcheck((ab + 1) * T::BN <= (int)T::TMEM_COLS, args.status, CHK_TMEM, ab * T::BN);
         if (lane == 0) {
           tc_fence_after_sync();
 #pragma unroll
           for (int k = 0; k < T::NMMA; ++k) {
+            if (!mma_ok) break;
             const uint64_t adesc = umma_desc_sw128(a_stage(sa) + k * 32, 16, 1024);
             const uint64_t bdesc =
                 T::kBT ? umma_desc_sw128(b_stage(s) + k * 32, 16, 1024)
@@ -606,7 +620,7 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
       if (g < total) {
         int row0, k0;
         coords(g, row0, k0);
-        stage_load<T>(buf[d], args.A, args.U, row0, k0, args.M, args.K, tw, lane);
+        stage_load<T>(buf[d], args.A, args.U, row0, k0, args.M, args.K, tw, lane, args.status);
       }
     }
     bool ok = true;
@@ -622,7 +636,7 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
         if (gn < total) {
           int row0, k0;
           coords(gn, row0, k0);
-          stage_load<T>(buf[d], args.A, args.U, row0, k0, args.M, args.K, tw, lane);
+          stage_load<T>(buf[d], args.A, args.U, row0, k0, args.M, args.K, tw, lane, args.status);
         }
         const int s = g % T::NA;
         if (g >= T::NA) {
@@ -634,7 +648,7 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
             break;
           }
         }
-        stage_store<T>(a_stage(s), crank, tw, lane, vals);
+        stage_store<T>(a_stage(s), crank, tw, lane, vals, args.status);
         fence_proxy_async_smem();   // our rows -> visible to UMMA and to the copy engine
         __syncwarp();
         {
@@ -648,8 +662,9 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
             if (lane >= 1 && lane < CN) {
               const uint32_t dst = (crank + (uint32_t)lane) % (uint32_t)CN;
               const uint32_t src = a_stage(s) + slice_off;
-              bulk_copy_s2cluster(mapa_shared(src, dst), src, T::SLICE_BYTES,
-                                  mapa_shared(full, dst));
+              if (dcheck(dst < (uint32_t)T::CS && dst != crank, args.status, CHK_PEER, dst))
+                bulk_copy_s2cluster(mapa_shared(src, dst), src, T::SLICE_BYTES,
+                                    mapa_shared(full, dst));
             }
           } else {
             if (lane == 0) mbar_arrive(full);
@@ -689,6 +704,17 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
     // on; with one, after chunk e's store has read the buffer.
     auto ebuf = [&](uint32_t e) -> uint32_t { return e % NB; };
     auto ephase = [&](uint32_t e) -> uint32_t { return (e / NB) & 1u; };
+    // Checked build: an f32 TMA box at a column x that is a multiple of 4,
+    // staged inside this warp's buffers; TMEM columns inside the item's
+    // accumulator buffer.
+    auto epi_ok = [&](int x, uint32_t smem, uint32_t bytes) -> bool {
+      return dcheck((x & 3) == 0, args.status, CHK_TMA_X, x) &&
+             dcheck(smem >= buf0 && smem + bytes <= buf0 + NB * T::EPI_BUF_BYTES, args.status,
+                    CHK_BUFFER, (long long)(smem - sbase));
+    };
+    auto tcols_ok = [&](int col, int width) -> bool {
+      return dcheck(col >= 0 && col + width <= T::BN, args.status, CHK_TMEM, col);
+    };
     uint32_t ec = 0, r_issued = 0, r_done = 0, e_wait = 0;
     // SwiGLU-backward epilogue (two buffers): GATE and UP of a chunk land in
     // this warp's two buffers together (barrier BAR_EPI + 2q, one phase per
@@ -712,7 +738,8 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
         // R of the first chunk, into a buffer whose last store has read it
         bulk_wait_group_read<0>();
         mbar_arrive_expect_tx(ebar(ebuf(ec)), T::EPI_BUF_BYTES);
-        tma_load_2d(buf(ebuf(ec)), &tm_r, n0, row0, ebar(ebuf(ec)));
+        if (epi_ok(n0, buf(ebuf(ec)), T::EPI_BUF_BYTES))
+          tma_load_2d(buf(ebuf(ec)), &tm_r, n0, row0, ebar(ebuf(ec)));
         ++r_issued;
       }
       // (a pair's accumulator is complete when the even CTA's commit says so)
@@ -729,10 +756,16 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
         // the 32 lanes (rows) of a store write 512 consecutive bytes
         float4* part = reinterpret_cast<float4*>(args.part) +
                        (size_t)(cid * T::CS + (int)crank) * C4 * T::BM + q * kEpiRows + lane;
+        const long long part_end =
+            (long long)(cid * T::CS + (int)crank) * C4 * T::BM + q * kEpiRows + lane;
         for (int c = 0; c < nc; ++c) {
           uint32_t v[32];
+          if (!tcols_ok(c * kEpiCols, kEpiCols)) break;
           tmem_ld_32x32b_x32(acc + (uint32_t)(c * kEpiCols), v);
           tmem_wait_ld();
+          if (!dcheck(part_end + (long long)(c * 8 + 7) * T::BM < args.part_f4, args.status,
+                      CHK_PART, part_end + (long long)(c * 8 + 7) * T::BM))
+            break;
 #pragma unroll
           for (int j = 0; j < 8; ++j)
             part[(size_t)(c * 8 + j) * T::BM] =
@@ -755,8 +788,10 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
         if (ns > T::BNO / SC) ns = T::BNO / SC;
         auto issue = [&](int c) {   // lane 0: GATE and UP of chunk c
           mbar_arrive_expect_tx(ebar(0), 2 * SB);
-          tma_load_2d(gin, &tm_g2, n0 + c * SC, row0, ebar(0));
-          tma_load_2d(uin, &tm_u2, n0 + c * SC, row0, ebar(0));
+          if (epi_ok(n0 + c * SC, gin, 2 * SB)) {
+            tma_load_2d(gin, &tm_g2, n0 + c * SC, row0, ebar(0));
+            tma_load_2d(uin, &tm_u2, n0 + c * SC, row0, ebar(0));
+          }
           ++sw_issued;
           // the following chunk's GATE and UP on their way into L2
           if (c + 1 < ns) {
@@ -771,7 +806,7 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
         __syncwarp();
         for (int c = 0; c < ns && ok; ++c) {
           uint32_t v[SC];
-          tmem_ld_32x32b_x16(acc + (uint32_t)(c * SC), v);
+          if (tcols_ok(c * SC, SC)) tmem_ld_32x32b_x16(acc + (uint32_t)(c * SC), v);
           tmem_wait_ld();
           if (!warp_wait_phase(ebar(0), sw_done & 1u, ctl)) {
             ok = false;
@@ -807,8 +842,10 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
           fence_proxy_async_smem();   // staged gradients -> visible to the TMA stores
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(&tm_y, n0 + c * SC, row0, gout);
-            tma_store_2d(&tm_y2, n0 + c * SC, row0, uout);
+            if (epi_ok(n0 + c * SC, gout, 2 * SB)) {
+              tma_store_2d(&tm_y, n0 + c * SC, row0, gout);
+              tma_store_2d(&tm_y2, n0 + c * SC, row0, uout);
+            }
             bulk_commit_group();
           }
           __syncwarp();
@@ -832,13 +869,15 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
             bulk_wait_group_read<0>();
             if constexpr (RESID) {
               mbar_arrive_expect_tx(ebar(b ^ 1u), T::EPI_BUF_BYTES);
-              tma_load_2d(buf(b ^ 1u), &tm_r, n0 + (c + 1) * kEpiCols, row0, ebar(b ^ 1u));
+              if (epi_ok(n0 + (c + 1) * kEpiCols, buf(b ^ 1u), T::EPI_BUF_BYTES))
+                tma_load_2d(buf(b ^ 1u), &tm_r, n0 + (c + 1) * kEpiCols, row0, ebar(b ^ 1u));
               ++r_issued;
             }
           }
           __syncwarp();
           uint32_t v[32];
-          tmem_ld_32x32b_x32(acc + (uint32_t)(tc * kEpiCols), v);
+          if (tcols_ok(tc * kEpiCols, kEpiCols))
+            tmem_ld_32x32b_x32(acc + (uint32_t)(tc * kEpiCols), v);
           tmem_wait_ld();
           if constexpr (RESID) {
             if (!warp_wait_phase(ebar(b), ephase(e), ctl)) {
@@ -890,20 +929,23 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
           fence_proxy_async_smem();   // staged Y -> visible to the TMA store
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(second ? &tm_y2 : &tm_y, n0 + oc * kEpiCols, row0, buf(b));
+            if (epi_ok(n0 + oc * kEpiCols, buf(b), T::EPI_BUF_BYTES))
+              tma_store_2d(second ? &tm_y2 : &tm_y, n0 + oc * kEpiCols, row0, buf(b));
             bulk_commit_group();
             if (RESID && NB == 1 && c + 1 < nct) {
               // the single buffer: the next chunk's R once this store has read it
               bulk_wait_group_read<0>();
               mbar_arrive_expect_tx(ebar(0), T::EPI_BUF_BYTES);
-              tma_load_2d(buf(0), &tm_r, n0 + (c + 1) * kEpiCols, row0, ebar(0));
+              if (epi_ok(n0 + (c + 1) * kEpiCols, buf(0), T::EPI_BUF_BYTES))
+                tma_load_2d(buf(0), &tm_r, n0 + (c + 1) * kEpiCols, row0, ebar(0));
               ++r_issued;
             }
           }
           __syncwarp();
         }
         ec += (uint32_t)nct;
-        if (stats && ok && row0 + lane < args.M)
+        if (stats && ok && row0 + lane < args.M &&
+            dcheck(n0 / T::BN < args.stats_cols, args.status, CHK_STATS, n0 / T::BN))
           args.row_stats[(size_t)(row0 + lane) * args.stats_cols + n0 / T::BN] =
               make_float4(rm, rs, rsum, 0.0f);
       }
@@ -1046,7 +1088,7 @@ __global__ void __launch_bounds__(256)
                             float* __restrict__ Y, int M, int N, int cn, int pair, int bn,
                             int tile0, int num_ng, int band, int rem, int s,
                             const float* __restrict__ G2, const float* __restrict__ U2,
-                            float* __restrict__ Y2) {
+                            float* __restrict__ Y2, long long part_f4, int* status) {
   const int c4n = bn / 4;
   const long long per_cta = 128LL * c4n;
   const long long x = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -1068,8 +1110,12 @@ __global__ void __launch_bounds__(256)
   // GEMM's partial tiles are complete and visible.
   pdl_wait();
   // Up to 8 partials in flight per thread, added in K order.
-  const float4* src = part + ((long long)(j * s * cn + crank) * c4n + c4) * 128 + r;
+  const long long first = ((long long)(j * s * cn + crank) * c4n + c4) * 128 + r;
+  const float4* src = part + first;
   const long long stride = (long long)cn * c4n * 128;   // next K range
+  if (!dcheck(first + (long long)(s - 1) * stride < part_f4, status, CHK_PART,
+              first + (long long)(s - 1) * stride))
+    return;
   float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int p0 = 0; p0 < s; p0 += 8) {
     float4 v[8];

@@ -50,8 +50,23 @@ enum : uint32_t {
 // Largest split of the per-tile kernel: the portable cluster size.
 constexpr int kMaxClusterSplit = 8;
 
-// Device status word values (mirror lin_status).
-enum : int { KSTATUS_OK = 0, KSTATUS_TIMEOUT = 7 };
+// Device status word values (mirror lin_status). The status word is the
+// first int of a 16-byte record: [status, check site, check value (int64)].
+enum : int { KSTATUS_OK = 0, KSTATUS_TIMEOUT = 7, KSTATUS_CHECK = 8 };
+
+// Sites of the checked build's device checks (lin_last_device_check).
+enum CheckSite : int {
+  CHK_TMA_X = 1,         // a TMA copy's innermost coordinate not 16-byte aligned
+  CHK_STAGE = 2,         // an operand stage outside the ring
+  CHK_BUFFER = 3,        // an epilogue or staging buffer outside its region
+  CHK_TMEM = 4,          // a TMEM column range outside the allocation
+  CHK_PART = 5,          // a partial-tile index outside the workspace
+  CHK_STATS = 6,         // a row-partial index outside the workspace
+  CHK_GLOBAL = 7,        // another global index outside its tensor
+  CHK_PEER = 8,          // a cluster peer rank outside the cluster
+  CHK_BARRIER = 9,       // a barrier slot outside the barrier region
+  CHK_SELFTEST = 99,
+};
 
 struct KernelArgs {
   int32_t M, N, K;
@@ -73,6 +88,7 @@ struct KernelArgs {
   int32_t band_ng;      // column groups per band of the clustered tile order (0: one band)
   uint32_t* zero_word;  // (clustered kernels) set to 0 once the kernel may touch memory: the
                         // counter of a dependent kernel (null: none)
+  int64_t part_f4;      // float4s of args.part (checked build: partial-tile indices)
 };
 
 // Order of the clustered kernels' tiles: tile t of a grid of num_m row
@@ -195,13 +211,17 @@ cudaError_t launch_cvt_f16(const float* X, uint16_t* Xh, int64_t n, int sms, cud
 cudaError_t launch_cross_entropy(float* logits, const float4* row_stats, int stats_cols,
                                  const int32_t* targets, float* losses, float* loss_sum, int M,
                                  int V, float alpha, float beta, float inv_norm, unsigned* done,
-                                 cudaStream_t stream);
+                                 int* status, cudaStream_t stream);
 // Y (+ R) from the partial tiles of a split: tiles tile0 .. tile0 +
 // split_rem - 1 of width `bn` (cluster tiles of `cn` CTAs along N, `num_ng`
 // of them per row block; or, `pair`, tiles of 256 rows whose two CTAs hold
 // 128 rows each), each summed over its split_s K ranges.
 cudaError_t launch_split_reduce(const KernelArgs& args, bool resid, int cn, bool pair, int bn,
                                 int tile0, int num_ng, cudaStream_t stream);
+
+// One single-thread kernel that reports a failed check (site CHK_SELFTEST,
+// `value`) into the status record `status`; it touches no other memory.
+cudaError_t launch_selftest_check(int* status, long long value, cudaStream_t stream);
 
 // A caller-provided split-tail workspace: returns its base and size on
 // device `dev`, or an error status.

@@ -62,6 +62,15 @@ cudaError_t launch_cvt_f16(const float* X, uint16_t* Xh, int64_t n, int sms, cud
                             reinterpret_cast<uint2*>(Xh), n4);
 }
 
+__global__ void lin_selftest_check_kernel(int* status, long long value) {
+  report_check(status, CHK_SELFTEST, value);
+}
+
+cudaError_t launch_selftest_check(int* status, long long value, cudaStream_t stream) {
+  lin_selftest_check_kernel<<<1, 1, 0, stream>>>(status, value);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_gemm_cluster_cvt(int cn, bool resid, const TensorMaps& maps,
                                     const KernelArgs& args, cudaStream_t stream) {
   if (resid) {
@@ -116,16 +125,19 @@ cudaError_t launch_split_reduce(const KernelArgs& args, bool resid, int cn, bool
     return cudaLaunchKernelEx(&cfg, lin_split_reduce_kernel<false, true>, part, args.R, args.Y,
                               args.M, args.N, cn, pair ? 1 : 0, bn, tile0, num_ng, args.band_ng,
                               args.split_rem, args.split_s,
-                              args.G2, args.U2, args.Y2);
+                              args.G2, args.U2, args.Y2, (long long)args.part_f4,
+                              args.status);
   if (resid)
     return cudaLaunchKernelEx(&cfg, lin_split_reduce_kernel<true, false>, part, args.R, args.Y,
                               args.M, args.N, cn, pair ? 1 : 0, bn, tile0, num_ng, args.band_ng,
                               args.split_rem, args.split_s,
-                              args.G2, args.U2, args.Y2);
+                              args.G2, args.U2, args.Y2, (long long)args.part_f4,
+                              args.status);
   return cudaLaunchKernelEx(&cfg, lin_split_reduce_kernel<false, false>, part, args.R, args.Y,
                             args.M, args.N, cn, pair ? 1 : 0, bn, tile0, num_ng, args.band_ng,
                               args.split_rem, args.split_s,
-                            args.G2, args.U2, args.Y2);
+                            args.G2, args.U2, args.Y2, (long long)args.part_f4,
+                              args.status);
 }
 
 }  // namespace lin

@@ -95,7 +95,7 @@ __global__ void __launch_bounds__(kLossThreads, 4)
                              int stats_cols, const int32_t* __restrict__ targets,
                              float* __restrict__ losses, int V, float alpha, float beta,
                              float inv_norm, unsigned* __restrict__ done,
-                             float* __restrict__ loss_sum) {
+                             float* __restrict__ loss_sum, int* status) {
   extern __shared__ float4 staged[];   // kSmemF4 float4s of the row
   __shared__ float sh[kLossThreads / 32];
   __shared__ float4 part[kLossThreads / 32];
@@ -123,7 +123,9 @@ __global__ void __launch_bounds__(kLossThreads, 4)
 #pragma unroll
   for (int u = 0; u < kChunk; ++u) {
     const int v = kRegF4 + tid + u * kLossThreads;
-    if (v < V4) cp_async_16(st0 + 16u * (uint32_t)(tid + u * kLossThreads), row4 + v);
+    if (v < V4 &&
+        dcheck(tid + u * kLossThreads < kSmemF4, status, CHK_BUFFER, tid + u * kLossThreads))
+      cp_async_16(st0 + 16u * (uint32_t)(tid + u * kLossThreads), row4 + v);
   }
   if (tgt < 0 || tgt >= V) {   // ignored row (padding): loss 0, dLogits 0
     cp_async_wait_all();       // no copy may still write our shared memory
@@ -140,7 +142,8 @@ __global__ void __launch_bounds__(kLossThreads, 4)
     // the warps' shuffle trees, then warp 0 over the warps in order
     const float4* st = stats + (size_t)s * stats_cols;
     float m = -INFINITY, e = 0.0f, sum = 0.0f;
-    for (int i = tid; i < stats_cols; i += kLossThreads) {
+    const bool row_ok = dcheck(s < (int)gridDim.x, status, CHK_STATS, s);
+    for (int i = tid; row_ok && i < stats_cols; i += kLossThreads) {
       const float4 p = st[i];
       merge_softmax(m, e, p.x, p.y);
       sum += p.z;
@@ -254,7 +257,7 @@ __global__ void __launch_bounds__(kLossThreads)
 cudaError_t launch_cross_entropy(float* logits, const float4* row_stats, int stats_cols,
                                  const int32_t* targets, float* losses, float* loss_sum, int M,
                                  int V, float alpha, float beta, float inv_norm, unsigned* done,
-                                 cudaStream_t stream) {
+                                 int* status, cudaStream_t stream) {
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -267,7 +270,7 @@ cudaError_t launch_cross_entropy(float* logits, const float4* row_stats, int sta
   cfg.numAttrs = 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, lin_cross_entropy_kernel, logits, row_stats,
                                      stats_cols, targets, losses, V, alpha, beta, inv_norm, done,
-                                     loss_sum);
+                                     loss_sum, status);
   if (e != cudaSuccess || done) return e;
   cfg.gridDim = dim3(1, 1, 1);
   cfg.dynamicSmemBytes = 0;

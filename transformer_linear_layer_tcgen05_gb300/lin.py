@@ -22,7 +22,10 @@ from __future__ import annotations
 import ctypes
 import os
 
-LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "liblin.so")
+# LIN_CHECKED=1 loads the checked build (liblin_checked.so: the kernels check
+# their indices and report LIN_ERROR_DEVICE_CHECK; see include/lin.h).
+_LIB_NAME = "liblin_checked.so" if os.environ.get("LIN_CHECKED") == "1" else "liblin.so"
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), _LIB_NAME)
 
 STATUS = {
     0: "LIN_SUCCESS",
@@ -33,6 +36,7 @@ STATUS = {
     5: "LIN_ERROR_UNSUPPORTED_DEVICE",
     6: "LIN_ERROR_CUDA",
     7: "LIN_ERROR_TIMEOUT",
+    8: "LIN_ERROR_DEVICE_CHECK",
 }
 LIN_SUCCESS = 0
 LIN_ERROR_INVALID_VALUE = 1
@@ -42,6 +46,7 @@ LIN_ERROR_ALIASING = 4
 LIN_ERROR_UNSUPPORTED_DEVICE = 5
 LIN_ERROR_CUDA = 6
 LIN_ERROR_TIMEOUT = 7
+LIN_ERROR_DEVICE_CHECK = 8
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int64
@@ -58,6 +63,7 @@ SIGNATURES = {
     "lin_matmul_residual_swiglu_a_w16": [_P, _P, _P, _P, _P, _I, _I, _I, _S],
     "lin_get_device_status": [_S],
     "lin_selftest_wait_timeout": [_I, _S],
+    "lin_selftest_device_check": [_I, _S],
     "lin_matmul_residual_swiglu_a_w16_noalloc": [_P, _P, _P, _P, _P, _I, _I, _I, _S],
     "lin_matmul_t": [_P, _P, _P, _I, _I, _I, _S],
     "lin_matmul_t_acc": [_P, _P, _P, _I, _I, _I, _S],
@@ -117,6 +123,9 @@ def lib() -> ctypes.CDLL:
         L.lin_last_launch_info.argtypes = [ctypes.POINTER(ctypes.c_int),
                                            ctypes.POINTER(ctypes.c_uint64)]
         L.lin_last_launch_info.restype = None
+        L.lin_last_device_check.argtypes = [ctypes.POINTER(ctypes.c_int),
+                                            ctypes.POINTER(ctypes.c_int64)]
+        L.lin_last_device_check.restype = None
         _lib = L
     return _lib
 
@@ -397,6 +406,20 @@ def lin_get_device_status(stream=None) -> int:
 def lin_selftest_wait_timeout(timeout_us: int, stream=None) -> int:
     """Run the bounded-wait self-test; LIN_ERROR_TIMEOUT means it works."""
     return lib().lin_selftest_wait_timeout(int(timeout_us), _stream_handle(stream))
+
+
+def lin_selftest_device_check(value: int, stream=None) -> int:
+    """Run the device-check record self-test; LIN_ERROR_DEVICE_CHECK means it
+    works (lin_last_device_check() then gives (99, value))."""
+    return lib().lin_selftest_device_check(int(value), _stream_handle(stream))
+
+
+def lin_last_device_check() -> tuple:
+    """(site, value) of the calling thread's last LIN_ERROR_DEVICE_CHECK."""
+    site = ctypes.c_int(0)
+    value = ctypes.c_int64(0)
+    lib().lin_last_device_check(ctypes.byref(site), ctypes.byref(value))
+    return site.value, value.value
 
 
 # ------------------------------------------------- host-operand forms (CPU tensors)
