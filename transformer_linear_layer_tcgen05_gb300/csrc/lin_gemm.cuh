@@ -436,54 +436,66 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Every role below runs with its whole warp converged: lane 0 waits and
   // issues, the other lanes follow it loop by loop, and no lane reaches the
   // final CTA barrier while a lane of its warp still has work in flight.
-  if (warp == 0) {
-    // ---------------- operand-stage TMA producer (X for TF32, W for binary16)
-    if (T::OP_TMA_BYTES > 0 && !withhold) {
-      int filled = 0;
-      for (int kb = 0; kb < nkb; ++kb) {
-        const int st = kb % T::NS;
-        const int n = kb / T::NS;
-        if (kb >= T::NS && !lane0_wait_phase(bar(T::BAR_OP_EMPTY + st), (n - 1) & 1, ctl, lane))
-          break;
-        const int kk = (kb0 + kb) * T::BK;
-        // (x of every copy below: kk along K, m0 + j*32 or n0 + j*W_ATOM along
-        // M or N, all multiples of 16 bytes; a skipped copy makes the
-        // stage's wait run out)
-        const bool go = slot_ok(st, T::NS) && x_ok(kk, T::kBT ? T::ESZ : 4) && x_ok(m0, 4) &&
-                        x_ok(n0, T::ESZ);
-        if (lane == 0) {
-          const uint32_t full = bar(T::BAR_OP_TMA + st);
-          mbar_arrive_expect_tx(full, T::OP_TMA_BYTES);
-          if (go) {
-            if constexpr (T::kAmn) {
-              // X^T: BM/32 boxes of [32 rows of the contraction][32 of the tile's rows]
+  // Operand-stage TMA producer (X for TF32, W for binary16): the stage's
+  // boxes, A's and then W's, are issued by `nroles` warps, box i by role
+  // i % nroles, and role 0 also announces the stage's bytes. Issuing a box
+  // costs its thread about 70-120 cycles; the weight gradient's stage
+  // (four boxes of X^T, four of W) paced its ring with one issuing thread,
+  // and warp 3, free in that form, takes half (ffn_up_dw_f32 17.1 / 10.7 ->
+  // 15.0 / 9.35 us cold / warm; the five-box stages of the forms that read
+  // X gained nothing and keep one issuer).
+  constexpr bool kIssueSplit = T::kAmn;
+  auto produce = [&](int role, int nroles) {
+    int filled = 0;
+    for (int kb = 0; kb < nkb; ++kb) {
+      const int st = kb % T::NS;
+      const int n = kb / T::NS;
+      if (kb >= T::NS && !lane0_wait_phase(bar(T::BAR_OP_EMPTY + st), (n - 1) & 1, ctl, lane))
+        break;
+      const int kk = (kb0 + kb) * T::BK;
+      // (x of every copy below: kk along K, m0 + j*32 or n0 + j*W_ATOM along
+      // M or N, all multiples of 16 bytes; a skipped copy makes the
+      // stage's wait run out)
+      const bool go = slot_ok(st, T::NS) && x_ok(kk, T::kBT ? T::ESZ : 4) && x_ok(m0, 4) &&
+                      x_ok(n0, T::ESZ);
+      if (lane == 0) {
+        const uint32_t full = bar(T::BAR_OP_TMA + st);
+        if (role == 0) mbar_arrive_expect_tx(full, T::OP_TMA_BYTES);
+        int box = 0;
+        auto issue = [&](uint32_t dst, const CUtensorMap* map, int x, int y) {
+          if (box++ % nroles == role) tma_load_2d(dst, map, x, y, full);
+        };
+        if (go) {
+          if constexpr (T::kAmn) {
+            // X^T: BM/32 boxes of [32 rows of the contraction][32 of the tile's rows]
 #pragma unroll
-              for (int j = 0; j < T::BM / 32; ++j)
-                tma_load_2d(a_stage(st) + j * 4096, &tm_a, m0 + j * 32, kk, full);
-            } else if constexpr (!T::kXformA) {
-              tma_load_2d(a_stage(st), &tm_a, kk, m0, full);
-            }
-            if constexpr (T::kBT) {
-              // W as [N][K]: the tile's BN rows, this k-block's 128 bytes
-              tma_load_2d(b_stage(st), &tm_w, kk, n0, full);
-            } else {
-              // W as [K][N]: 128-byte runs of W_ATOM columns, BK rows each
+            for (int j = 0; j < T::BM / 32; ++j) issue(a_stage(st) + j * 4096, &tm_a, m0 + j * 32, kk);
+          } else if constexpr (!T::kXformA) {
+            issue(a_stage(st), &tm_a, kk, m0);
+          }
+          if constexpr (T::kBT) {
+            // W as [N][K]: the tile's BN rows, this k-block's 128 bytes
+            issue(b_stage(st), &tm_w, kk, n0);
+          } else {
+            // W as [K][N]: 128-byte runs of W_ATOM columns, BK rows each
 #pragma unroll
-              for (int j = 0; j < T::W_BOXES; ++j)
-                tma_load_2d(b_stage(st) + j * T::B_ATOM_BYTES, &tm_w, n0 + j * T::W_ATOM, kk,
-                            full);
-            }
+            for (int j = 0; j < T::W_BOXES; ++j)
+              issue(b_stage(st) + j * T::B_ATOM_BYTES, &tm_w, n0 + j * T::W_ATOM, kk);
           }
         }
-        __syncwarp();
-        filled = kb + 1;
       }
-      // Never leave with copies in flight: wait for the last fill of each slot.
-      if (lane == 0)
-        for (int kb = (filled > T::NS ? filled - T::NS : 0); kb < filled; ++kb)
-          wait_phase(bar(T::BAR_OP_TMA + kb % T::NS), (kb / T::NS) & 1, ctl, false);
       __syncwarp();
+      filled = kb + 1;
     }
+    // Never leave with copies in flight: wait for the last fill of each slot.
+    if (lane == 0)
+      for (int kb = (filled > T::NS ? filled - T::NS : 0); kb < filled; ++kb)
+        wait_phase(bar(T::BAR_OP_TMA + kb % T::NS), (kb / T::NS) & 1, ctl, false);
+    __syncwarp();
+  };
+
+  if (warp == 0) {
+    if (T::OP_TMA_BYTES > 0 && !withhold) produce(0, kIssueSplit ? 2 : 1);
   } else if (warp == 1) {
     // ---------------- UMMA issuer
     for (int kb = 0; kb < nkb; ++kb) {
@@ -527,7 +539,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else if (warp == 3) {
-    // ---------------- raw-stage TMA producer (inputs of the transform warps)
+    // ---------------- raw-stage TMA producer (inputs of the transform warps),
+    // or the second issuer of the operand stages
+    if (kIssueSplit && T::OP_TMA_BYTES > 0 && !withhold) produce(1, 2);
     if (T::kXform && !withhold) {
       const int nraw = nkb * T::RAW_PER_KB;
       int filled = 0;
