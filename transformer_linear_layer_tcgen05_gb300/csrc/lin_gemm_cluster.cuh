@@ -890,25 +890,6 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
             bulk_wait_group_read<0>();   // this buffer's last store has read it
           }
           __syncwarp();
-          if (stats) {   // (max, sum exp(y - max), sum y) over the columns below N
-            const int col = n0 + c * kEpiCols;
-            float cm = -INFINITY;
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (col + i < args.N) {
-                cm = fmaxf(cm, __uint_as_float(v[i]));
-                rsum += __uint_as_float(v[i]);
-              }
-            const float mn = fmaxf(rm, cm);
-            float sum = (rm == -INFINITY) ? 0.0f : rs * __expf(rm - mn);
-            if (mn != -INFINITY) {
-#pragma unroll
-              for (int i = 0; i < 32; ++i)
-                if (col + i < args.N) sum += __expf(__uint_as_float(v[i]) - mn);
-            }
-            rm = mn;
-            rs = sum;
-          }
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const uint32_t addr = buf(b) + sw128((uint32_t)lane, (uint32_t)j);
@@ -942,6 +923,42 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
             }
           }
           __syncwarp();
+          if (stats) {
+            // (max, sum exp(y - max), sum y) over the chunk's columns below N,
+            // merged into the lane's running pair; computed while the chunk's
+            // store is in flight. Four partial maxima and sums per quantity,
+            // so that no chain is 32 operations long; a column at or past N
+            // enters as -inf (exp 0) and adds 0 to the sum.
+            constexpr float kLog2e = 1.4426950408889634f;
+            const int nv = args.N - (n0 + c * kEpiCols);   // columns in range (>= 1)
+            float y[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) y[i] = i < nv ? __uint_as_float(v[i]) : -INFINITY;
+            float m4[4], s4[4];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              m4[q4] = y[q4];
+              s4[q4] = q4 < nv ? y[q4] : 0.0f;
+            }
+#pragma unroll
+            for (int i = 4; i < 32; ++i) {
+              m4[i & 3] = fmaxf(m4[i & 3], y[i]);
+              s4[i & 3] += i < nv ? y[i] : 0.0f;
+            }
+            const float cm = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+            rsum += (s4[0] + s4[1]) + (s4[2] + s4[3]);
+            const float mn = fmaxf(rm, cm);
+            float sum = (rm == -INFINITY) ? 0.0f : rs * ex2_approx((rm - mn) * kLog2e);
+            if (mn != -INFINITY) {
+              const float off = mn * kLog2e;
+              float e4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+              for (int i = 0; i < 32; ++i) e4[i & 3] += ex2_approx(fmaf(y[i], kLog2e, -off));
+              sum += (e4[0] + e4[1]) + (e4[2] + e4[3]);
+            }
+            rm = mn;
+            rs = sum;
+          }
         }
         ec += (uint32_t)nct;
         if (stats && ok && row0 + lane < args.M &&

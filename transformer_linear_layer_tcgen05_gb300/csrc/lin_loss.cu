@@ -44,31 +44,28 @@ __device__ __forceinline__ float block_reduce(float v, float* sh) {
 
 }  // namespace
 
-// sum_losses, by the CTA that counts itself last: each CTA, once its loss is
-// written, counts itself done (its thread 0 fences the write first); in the
-// one that takes the count to M, all threads add the M losses in a fixed
-// order (a strided sum, then the fixed-order block reduction), so the total
-// has the same bits whichever CTA that is. `done` is zero when the grid
-// starts; without it (null) a separate kernel adds the losses. (Measured on
-// one GB300, cold / warm us of the lm_head shape: a separate sum kernel
-// 44.3 / 36.3, this 43.7 / 34.8; warp 0 alone counting with a release
-// atomic while the other warps went on, 44.7 / 36.5.)
-__device__ __forceinline__ void sum_if_last(const float* losses, int M, unsigned* done,
-                                            float* loss_sum, float* sh) {
+// sum_losses, by the CTA that counts itself last. Warp 0 alone: its lane 0
+// has written the CTA's loss, fences it and counts the CTA done; in the CTA
+// whose count reaches M, warp 0 adds the M losses in a fixed order (a
+// strided sum per lane, then a shuffle tree), so the total has the same bits
+// whichever CTA that is. The other warps never wait for it. `done` is zero
+// when the grid starts; without it (null) a separate kernel adds the losses.
+__device__ __forceinline__ void count_and_sum_warp(const float* losses, int M, unsigned* done,
+                                                   float* loss_sum, int lane) {
   if (!done) return;
-  __shared__ int last;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    last = atomicAdd(done, 1u) == (unsigned)(M - 1);
+  unsigned last = 0;
+  if (lane == 0) {
+    __threadfence();   // this CTA's loss, visible before its count
+    last = atomicAdd(done, 1u) == (unsigned)(M - 1) ? 1u : 0u;
   }
-  __syncthreads();
+  last = __shfl_sync(0xffffffffu, last, 0);
   if (!last) return;
   __threadfence();   // the other CTAs' losses, visible before their counts
   float v = 0.0f;
-  for (int i = threadIdx.x; i < M; i += kLossThreads) v += __ldcg(losses + i);
-  v = block_reduce<false>(v, sh);
-  if (threadIdx.x == 0) *loss_sum = v;
+  for (int i = lane; i < M; i += 32) v += __ldcg(losses + i);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  if (lane == 0) *loss_sum = v;
 }
 
 // Online-softmax partials (max m, sum s of exp(l - m)) merged: the pair for
@@ -98,10 +95,9 @@ __global__ void __launch_bounds__(kLossThreads, 4)
                              float* __restrict__ loss_sum, int* status) {
   extern __shared__ float4 staged[];   // kSmemF4 float4s of the row
   __shared__ float sh[kLossThreads / 32];
-  __shared__ float4 part[kLossThreads / 32];
-  __shared__ float3 row_sums;          // row max, sum of exp(l - max), sum of l
   const int s = blockIdx.x;
   const int tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
   // Launched as a programmatic dependent of the GEMM: wait for its logits.
   pdl_wait();
   float* row = logits + (size_t)s * (size_t)V;
@@ -130,20 +126,24 @@ __global__ void __launch_bounds__(kLossThreads, 4)
   if (tgt < 0 || tgt >= V) {   // ignored row (padding): loss 0, dLogits 0
     cp_async_wait_all();       // no copy may still write our shared memory
     for (int v = tid; v < V4; v += kLossThreads) row4[v] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (tid == 0) losses[s] = 0.0f;
-    sum_if_last(losses, gridDim.x, done, loss_sum, sh);
+    if (warp == 0) {
+      if (lane == 0) losses[s] = 0.0f;
+      count_and_sum_warp(losses, gridDim.x, done, loss_sum, lane);
+    }
     return;
   }
   const float l_t = tid == 0 ? row[tgt] : 0.0f;   // phase 3 needs it before phase 4 overwrites it
   // phases 1 and 2a (row max and sum of exp(l - max)) and the row sum that
   // label smoothing needs
+  float row_max, denom, total;
   if (stats) {
-    // merge the GEMM's partials: each thread its columns in order, then
-    // the warps' shuffle trees, then warp 0 over the warps in order
+    // Every warp merges the GEMM's partials of the row by itself (lane i
+    // takes partials i, i + 32, ..., then a shuffle tree whose every lane
+    // ends with the same value), so no warp waits for another.
     const float4* st = stats + (size_t)s * stats_cols;
     float m = -INFINITY, e = 0.0f, sum = 0.0f;
     const bool row_ok = dcheck(s < (int)gridDim.x, status, CHK_STATS, s);
-    for (int i = tid; row_ok && i < stats_cols; i += kLossThreads) {
+    for (int i = lane; row_ok && i < stats_cols; i += 32) {
       const float4 p = st[i];
       merge_softmax(m, e, p.x, p.y);
       sum += p.z;
@@ -155,24 +155,16 @@ __global__ void __launch_bounds__(kLossThreads, 4)
       sum += __shfl_xor_sync(0xffffffffu, sum, o);
       merge_softmax(m, e, m2, e2);
     }
-    if ((tid & 31) == 0) part[tid >> 5] = make_float4(m, e, sum, 0.0f);
-    __syncthreads();
-    if (tid == 0) {
-      float4 a = part[0];
-      for (int w = 1; w < kLossThreads / 32; ++w) {
-        merge_softmax(a.x, a.y, part[w].x, part[w].y);
-        a.z += part[w].z;
-      }
-      row_sums = make_float3(a.x, a.y, a.z);
-    }
-    __syncthreads();
+    row_max = m;
+    denom = e;
+    total = sum;
   } else {   // no partials: read the row from global memory for them
     float m = -INFINITY;
     for (int v = tid; v < V4; v += kLossThreads) {
       const float4 x = row4[v];
       m = fmaxf(m, fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w)));
     }
-    const float row_max = block_reduce<true>(m, sh);
+    row_max = block_reduce<true>(m, sh);
     float d = 0.0f, sum = 0.0f;
     for (int v = tid; v < V4; v += kLossThreads) {
       const float4 x = row4[v];
@@ -180,13 +172,10 @@ __global__ void __launch_bounds__(kLossThreads, 4)
            __expf(x.w - row_max);
       sum += (x.x + x.y) + (x.z + x.w);
     }
-    const float denom = block_reduce<false>(d, sh);
-    const float total = block_reduce<false>(sum, sh);
-    if (tid == 0) row_sums = make_float3(row_max, denom, total);
-    __syncthreads();
+    denom = block_reduce<false>(d, sh);
+    total = block_reduce<false>(sum, sh);
   }
-  const float row_max = row_sums.x;
-  const float dg = fmaxf(row_sums.y, 1e-30f);
+  const float dg = fmaxf(denom, 1e-30f);
   const float lse = row_max + logf(dg);
   const float inv_V = 1.0f / (float)V;
   const float zl = 2.0f * beta * lse;
@@ -200,14 +189,15 @@ __global__ void __launch_bounds__(kLossThreads, 4)
   const float c_off = smooth * inv_norm;
   const float c_hit = (1.0f - alpha) * inv_norm;
   const int tv = tgt >> 2;   // the float4 holding the target
-  // phase 3: the loss
-  if (tid == 0) {
-    const float ce = lse - (1.0f - alpha) * l_t - (alpha > 0.0f ? alpha * (row_sums.z * inv_V) : 0.0f);
-    losses[s] = ce + beta * lse * lse;
+  // phase 3: the loss, and the count of sum_losses (warp 0; before its
+  // phase 4, so that the count's fence has only the loss to wait for)
+  if (warp == 0) {
+    if (lane == 0) {
+      const float ce = lse - (1.0f - alpha) * l_t - (alpha > 0.0f ? alpha * (total * inv_V) : 0.0f);
+      losses[s] = ce + beta * lse * lse;
+    }
+    count_and_sum_warp(losses, gridDim.x, done, loss_sum, lane);
   }
-  // (counted before phase 4, so that the count's fence has only the loss to
-  // wait for, not this CTA's dLogits stores)
-  sum_if_last(losses, gridDim.x, done, loss_sum, sh);
   // phase 4: dLogits in place, from registers, then from shared memory, then
   // (longer rows) register chunk by chunk
   auto g1 = [&](float l) { return fmaf(ex2_approx(fmaf(l, kLog2e, -c_shift)), c_scale, -c_off); };
