@@ -611,6 +611,20 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
       row0 = tile_m0(item_tile(i)) + (int)crank * T::ROWS;
       k0 = kb * T::BK;
     };
+    // The group loads its k-blocks in order, XF_GROUPS apart: a cursor steps
+    // to the next one within its work item, and only crossing into the next
+    // item takes the divisions of `coords` (they would otherwise sit on the
+    // path to every load's issue).
+    int cur_g = -1, cur_row0 = 0, cur_k0 = 0, cur_kend = 0;
+    auto cursor_to = [&](int g) {
+      if (cur_g >= 0 && g - cur_g == T::XF_GROUPS && cur_k0 + T::XF_GROUPS * T::BK < cur_kend) {
+        cur_k0 += T::XF_GROUPS * T::BK;
+      } else {
+        coords(g, cur_row0, cur_k0);
+        cur_kend = (g < n_full * nkb ? nkb : unit_kb1) * T::BK;
+      }
+      cur_g = g;
+    };
     // This group's k-blocks are g = grp + XF_GROUPS * j; buffer j % PF holds
     // the inputs of k-block j, loaded PF of the group's k-blocks ahead.
     Staged<T> buf[T::PF];
@@ -618,9 +632,9 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
     for (int d = 0; d < T::PF; ++d) {
       const int g = grp + T::XF_GROUPS * d;
       if (g < total) {
-        int row0, k0;
-        coords(g, row0, k0);
-        stage_load<T>(buf[d], args.A, args.U, row0, k0, args.M, args.K, tw, lane, args.status);
+        cursor_to(g);
+        stage_load<T>(buf[d], args.A, args.U, cur_row0, cur_k0, args.M, args.K, tw, lane,
+                      args.status);
       }
     }
     bool ok = true;
@@ -634,9 +648,9 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
         stage_compute<T>(buf[d], vals);
         const int gn = g + T::XF_GROUPS * T::PF;
         if (gn < total) {
-          int row0, k0;
-          coords(gn, row0, k0);
-          stage_load<T>(buf[d], args.A, args.U, row0, k0, args.M, args.K, tw, lane, args.status);
+          cursor_to(gn);
+          stage_load<T>(buf[d], args.A, args.U, cur_row0, cur_k0, args.M, args.K, tw, lane,
+                        args.status);
         }
         const int s = g % T::NA;
         if (g >= T::NA) {
