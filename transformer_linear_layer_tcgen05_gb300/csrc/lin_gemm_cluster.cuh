@@ -121,6 +121,10 @@ struct ClusterTraits {
   static constexpr int STAGE_REGS = XF_WARPS > 8 ? 32 : 64;   // per lane, for staged input
   static constexpr int PF_FIT = STAGE_REGS / (4 * LOADS);
   static constexpr int PF = PF_FIT < 1 ? 1 : (PF_FIT > 4 ? 4 : PF_FIT);
+  // The transform's cursor and the lane's load addresses are kept from one
+  // k-block to the next (LaneRows) where the staged registers leave room
+  // for them; elsewhere they are computed per k-block.
+  static constexpr bool kLaneRows = LOADS <= 8;
 
   static constexpr uint32_t A_BYTES = BM * 128;
   static constexpr uint32_t B_ATOM_BYTES = kBT ? BNB * 128 : BK * 128;
@@ -231,6 +235,54 @@ __device__ __forceinline__ void stage_load(Staged<T>& st, const float* __restric
     const int row = row0 + tw * T::RW + q * T::ROWS_PER_LOAD + lane / T::LANES_PER_ROW;
     const bool in = col_in && row < M;
     const size_t off = (size_t)(in ? row : 0) * (size_t)K + (size_t)(in ? col : 0);
+#pragma unroll
+    for (int i = 0; i < T::INPUTS; ++i) {
+      const float* src = (i == 0 ? a : u) + off;
+      if constexpr (T::V8) {
+        if (in)
+          ldg_stream_v8f(src, st.v[i][q][0], st.v[i][q][1]);
+        else
+          st.v[i][q][0] = st.v[i][q][1] = zero;
+      } else {
+        st.v[i][q][0] = in ? ldg_stream_v4f(src) : zero;
+      }
+    }
+  }
+}
+
+// The same loads with this lane's first row offset (row * K + its first
+// column), the row stride of its loads and the rows left before M computed
+// once per work item: per k-block only k0 is added.
+template <typename T>
+struct LaneRows {
+  size_t off0;      // first load's row * K + column (row 0 when past M)
+  size_t stride;    // ROWS_PER_LOAD * K
+  int rows_left;    // M - the first load's row
+  int col;          // this lane's first column within a k-block
+};
+
+template <typename T>
+__device__ __forceinline__ void lane_rows(LaneRows<T>& lr, int row0, int M, int K, int tw,
+                                          int lane) {
+  lr.col = T::CHUNK * (lane % T::LANES_PER_ROW);
+  const int row = row0 + tw * T::RW + lane / T::LANES_PER_ROW;
+  lr.rows_left = M - row;
+  lr.off0 = (size_t)row * (size_t)K + (size_t)lr.col;
+  lr.stride = (size_t)T::ROWS_PER_LOAD * (size_t)K;
+}
+
+template <typename T>
+__device__ __forceinline__ void stage_load_at(Staged<T>& st, const float* __restrict__ a,
+                                              const float* __restrict__ u, const LaneRows<T>& lr,
+                                              int k0, int K, int* status) {
+  const int col = k0 + lr.col;
+  // (K is a multiple of CHUNK on each path: a load is wholly in or out)
+  const bool col_in = col < K && dcheck(col + T::CHUNK <= K, status, CHK_GLOBAL, col);
+  const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int q = 0; q < T::LPI; ++q) {
+    const bool in = col_in && q * T::ROWS_PER_LOAD < lr.rows_left;
+    const size_t off = in ? lr.off0 + (size_t)q * lr.stride + (size_t)k0 : 0;
 #pragma unroll
     for (int i = 0; i < T::INPUTS; ++i) {
       const float* src = (i == 0 ? a : u) + off;
@@ -616,14 +668,30 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
     // item takes the divisions of `coords` (they would otherwise sit on the
     // path to every load's issue).
     int cur_g = -1, cur_row0 = 0, cur_k0 = 0, cur_kend = 0;
+    LaneRows<T> cur_rows;
     auto cursor_to = [&](int g) {
       if (cur_g >= 0 && g - cur_g == T::XF_GROUPS && cur_k0 + T::XF_GROUPS * T::BK < cur_kend) {
         cur_k0 += T::XF_GROUPS * T::BK;
       } else {
+        const int row0_before = cur_row0;
         coords(g, cur_row0, cur_k0);
         cur_kend = (g < n_full * nkb ? nkb : unit_kb1) * T::BK;
+        if (cur_g < 0 || cur_row0 != row0_before)
+          lane_rows<T>(cur_rows, cur_row0, args.M, args.K, tw, lane);
       }
       cur_g = g;
+    };
+    // the inputs of k-block g into b (instances whose staged registers leave
+    // no room for the cursor compute the coordinates every time)
+    auto load_kblock = [&](Staged<T>& b, int g) {
+      if constexpr (T::kLaneRows) {
+        cursor_to(g);
+        stage_load_at<T>(b, args.A, args.U, cur_rows, cur_k0, args.K, args.status);
+      } else {
+        int row0, k0;
+        coords(g, row0, k0);
+        stage_load<T>(b, args.A, args.U, row0, k0, args.M, args.K, tw, lane, args.status);
+      }
     };
     // This group's k-blocks are g = grp + XF_GROUPS * j; buffer j % PF holds
     // the inputs of k-block j, loaded PF of the group's k-blocks ahead.
@@ -632,9 +700,7 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
     for (int d = 0; d < T::PF; ++d) {
       const int g = grp + T::XF_GROUPS * d;
       if (g < total) {
-        cursor_to(g);
-        stage_load<T>(buf[d], args.A, args.U, cur_row0, cur_k0, args.M, args.K, tw, lane,
-                      args.status);
+        load_kblock(buf[d], g);
       }
     }
     bool ok = true;
@@ -648,9 +714,7 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
         stage_compute<T>(buf[d], vals);
         const int gn = g + T::XF_GROUPS * T::PF;
         if (gn < total) {
-          cursor_to(gn);
-          stage_load<T>(buf[d], args.A, args.U, cur_row0, cur_k0, args.M, args.K, tw, lane,
-                        args.status);
+          load_kblock(buf[d], gn);
         }
         const int s = g % T::NA;
         if (g >= T::NA) {
