@@ -8,7 +8,7 @@
 // exp(l - max) and sum of l over each CTA's 256 columns), they are combined
 // here instead, and the row is read once, for phase 4, which writes dLogits
 // in place.
-#include "lin_common.cuh"
+#include "lin_ce.cuh"
 
 namespace lin {
 
@@ -44,47 +44,17 @@ __device__ __forceinline__ float block_reduce(float v, float* sh) {
 
 }  // namespace
 
-// sum_losses, by the CTA that counts itself last. Warp 0 alone: its lane 0
-// has written the CTA's loss, fences it and counts the CTA done; in the CTA
-// whose count reaches M, warp 0 adds the M losses in a fixed order (a
-// strided sum per lane, then a shuffle tree), so the total has the same bits
-// whichever CTA that is. The other warps never wait for it. `done` is zero
-// when the grid starts; without it (null) a separate kernel adds the losses.
-__device__ __forceinline__ void count_and_sum_warp(const float* losses, int M, unsigned* done,
-                                                   float* loss_sum, int lane) {
-  if (!done) return;
-  unsigned last = 0;
-  if (lane == 0) {
-    __threadfence();   // this CTA's loss, visible before its count
-    last = atomicAdd(done, 1u) == (unsigned)(M - 1) ? 1u : 0u;
-  }
-  last = __shfl_sync(0xffffffffu, last, 0);
-  if (!last) return;
-  __threadfence();   // the other CTAs' losses, visible before their counts
-  float v = 0.0f;
-  for (int i = lane; i < M; i += 32) v += __ldcg(losses + i);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  if (lane == 0) *loss_sum = v;
-}
-
-// Online-softmax partials (max m, sum s of exp(l - m)) merged: the pair for
-// the union of both column sets. -inf maxima (no columns) merge as no-ops.
-__device__ __forceinline__ void merge_softmax(float& m, float& s, float m2, float s2) {
-  const float mx = fmaxf(m, m2);
-  if (mx == -INFINITY) return;
-  s = (m == -INFINITY ? 0.0f : s * __expf(m - mx)) + (m2 == -INFINITY ? 0.0f : s2 * __expf(m2 - mx));
-  m = mx;
-}
-
 // A CTA's first kRegF4 float4s of its row are loaded into registers
-// (kChunk per thread) and the next kSmemF4 copied into shared memory by
-// cp.async, all requested together with the target index before anything
-// else, so that the whole row (V <= 16384) is in flight at once; the rest of
-// a longer row is read in further register chunks during phase 4.
-constexpr int kChunk = 8;
-constexpr int kRegF4 = kChunk * kLossThreads;      // 2048 float4s: 32 KB
-constexpr int kSmemF4 = kChunk * kLossThreads;     // the next 32 KB
+// (kChunk per thread) and the next kSmemF4 (kSmemChunk per thread) copied
+// into shared memory by cp.async, all requested together with the target
+// index before anything else, so that the whole row (V <= 16384) is in
+// flight at once; the rest of a longer row is read in further register
+// chunks during phase 4. (Six register float4s a thread keep the kernel
+// within the 64 registers of four CTAs per SM.)
+constexpr int kChunk = 6;
+constexpr int kSmemChunk = 10;
+constexpr int kRegF4 = kChunk * kLossThreads;           // 1536 float4s: 24 KB
+constexpr int kSmemF4 = kSmemChunk * kLossThreads;      // the next 40 KB
 constexpr size_t kLossSmemBytes = (size_t)kSmemF4 * 16;
 
 __global__ void __launch_bounds__(kLossThreads, 4)
@@ -117,7 +87,7 @@ __global__ void __launch_bounds__(kLossThreads, 4)
   // alone copies and later reads: its own cp_async_wait_all suffices
   const uint32_t st0 = smem_u32(staged);
 #pragma unroll
-  for (int u = 0; u < kChunk; ++u) {
+  for (int u = 0; u < kSmemChunk; ++u) {
     const int v = kRegF4 + tid + u * kLossThreads;
     if (v < V4 &&
         dcheck(tid + u * kLossThreads < kSmemF4, status, CHK_BUFFER, tid + u * kLossThreads))
@@ -137,27 +107,15 @@ __global__ void __launch_bounds__(kLossThreads, 4)
   // label smoothing needs
   float row_max, denom, total;
   if (stats) {
-    // Every warp merges the GEMM's partials of the row by itself (lane i
-    // takes partials i, i + 32, ..., then a shuffle tree whose every lane
-    // ends with the same value), so no warp waits for another.
+    // Every warp merges the GEMM's partials of the row by itself, so no
+    // warp waits for another.
     const float4* st = stats + (size_t)s * stats_cols;
-    float m = -INFINITY, e = 0.0f, sum = 0.0f;
     const bool row_ok = dcheck(s < (int)gridDim.x, status, CHK_STATS, s);
-    for (int i = lane; row_ok && i < stats_cols; i += 32) {
-      const float4 p = st[i];
-      merge_softmax(m, e, p.x, p.y);
-      sum += p.z;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-      const float e2 = __shfl_xor_sync(0xffffffffu, e, o);
-      sum += __shfl_xor_sync(0xffffffffu, sum, o);
-      merge_softmax(m, e, m2, e2);
-    }
-    row_max = m;
-    denom = e;
-    total = sum;
+    const float3 rs = warp_merge_partials([&](int i) { return st[i]; }, row_ok ? stats_cols : 0,
+                                          lane);
+    row_max = rs.x;
+    denom = rs.y;
+    total = rs.z;
   } else {   // no partials: read the row from global memory for them
     float m = -INFINITY;
     for (int v = tid; v < V4; v += kLossThreads) {
@@ -175,43 +133,17 @@ __global__ void __launch_bounds__(kLossThreads, 4)
     denom = block_reduce<false>(d, sh);
     total = block_reduce<false>(sum, sh);
   }
-  const float dg = fmaxf(denom, 1e-30f);
-  const float lse = row_max + logf(dg);
-  const float inv_V = 1.0f / (float)V;
-  const float zl = 2.0f * beta * lse;
-  const float smooth = alpha * inv_V;
-  // Phase 4 per logit l: p = exp(l - lse) = 2^(l log2(e) - lse log2(e)), and
-  // dLogit = ((p - target share) + zl p) * inv_norm = p c_scale - c_off,
-  // less (1 - alpha) inv_norm at the target: two FMAs and one ex2 a logit.
-  constexpr float kLog2e = 1.4426950408889634f;
-  const float c_shift = lse * kLog2e;
-  const float c_scale = (1.0f + zl) * inv_norm;
-  const float c_off = smooth * inv_norm;
-  const float c_hit = (1.0f - alpha) * inv_norm;
-  const int tv = tgt >> 2;   // the float4 holding the target
+  const CeRow cr = ce_row(row_max, denom, V, alpha, beta, inv_norm);
+  const int tv = tgt >> 2, tj = tgt & 3;   // the float4 holding the target, and its lane
   // phase 3: the loss, and the count of sum_losses (warp 0; before its
   // phase 4, so that the count's fence has only the loss to wait for)
   if (warp == 0) {
-    if (lane == 0) {
-      const float ce = lse - (1.0f - alpha) * l_t - (alpha > 0.0f ? alpha * (total * inv_V) : 0.0f);
-      losses[s] = ce + beta * lse * lse;
-    }
+    if (lane == 0) losses[s] = ce_loss(cr, l_t, total, V, alpha, beta);
     count_and_sum_warp(losses, gridDim.x, done, loss_sum, lane);
   }
   // phase 4: dLogits in place, from registers, then from shared memory, then
   // (longer rows) register chunk by chunk
-  auto g1 = [&](float l) { return fmaf(ex2_approx(fmaf(l, kLog2e, -c_shift)), c_scale, -c_off); };
-  auto grad = [&](const float4 x, int v) -> float4 {
-    float4 y = make_float4(g1(x.x), g1(x.y), g1(x.z), g1(x.w));
-    if (v == tv) {
-      const int j = tgt & 3;
-      y.x -= j == 0 ? c_hit : 0.0f;
-      y.y -= j == 1 ? c_hit : 0.0f;
-      y.z -= j == 2 ? c_hit : 0.0f;
-      y.w -= j == 3 ? c_hit : 0.0f;
-    }
-    return y;
-  };
+  auto grad = [&](const float4 x, int v) -> float4 { return ce_grad4(cr, x, v, tv, tj); };
 #pragma unroll
   for (int u = 0; u < kChunk; ++u) {
     const int v = tid + u * kLossThreads;
@@ -219,7 +151,7 @@ __global__ void __launch_bounds__(kLossThreads, 4)
   }
   cp_async_wait_all();
 #pragma unroll
-  for (int u = 0; u < kChunk; ++u) {
+  for (int u = 0; u < kSmemChunk; ++u) {
     const int v = kRegF4 + tid + u * kLossThreads;
     if (v < V4) row4[v] = grad(staged[tid + u * kLossThreads], v);
   }
