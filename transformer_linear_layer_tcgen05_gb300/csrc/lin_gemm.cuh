@@ -120,7 +120,8 @@ struct GemmTraits {
   static constexpr uint32_t OFF_TMEM_SLOT = BAR_COUNT * 8;
   static constexpr uint32_t OFF_ABORT = OFF_TMEM_SLOT + 4;
 
-  static constexpr uint32_t TMEM_COLS = BN;
+  // (TMEM is allocated in powers of two of at least 32 columns)
+  static constexpr uint32_t TMEM_COLS = BN <= 32 ? 32 : BN <= 64 ? 64 : BN <= 128 ? 128 : 256;
   static constexpr uint32_t IDESC =
       umma_idesc(kF16 ? 0u : 2u, /*a_mn_major=*/kAmn, /*b_mn_major=*/!BT, BM, BN);
 
@@ -133,7 +134,8 @@ struct GemmTraits {
   static_assert(!kXform || NR * RAW_STAGE_BYTES >= EPI_BYTES, "epilogue aliasing");
   static_assert(OFF_ABORT + 4 <= BAR_REGION, "barrier region");
   static_assert(SMEM_BYTES <= SMEM_CAP, "shared memory");
-  static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256 && (BN & (BN - 1)) == 0, "tile width");
+  static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "tile width");
+  static_assert((BN / 4) % 8 == 0, "a cluster split's swizzle groups of eight 16-byte columns");
   static_assert(BN % W_ATOM == 0, "W runs per tile");
 };
 

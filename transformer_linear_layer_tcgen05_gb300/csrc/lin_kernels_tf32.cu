@@ -16,6 +16,11 @@ cudaError_t launch_gemm_tf32(int amode, bool resid, int bn, bool bt, const Tenso
   // SwiGLU A built half as often)
   if (amode == A_SWIGLU_F32 && resid && bn == 256)
     return launch_instance<A_SWIGLU_F32, true, 256>(maps, args, stream);
+  // X copied as is, in 96-column tiles: 4/3 as many tiles as 128 columns
+  // give, for shapes whose 128-column tiles leave SMs idle
+  if (amode == A_TMA_F32 && bn == 96)
+    return resid ? launch_instance<A_TMA_F32, true, 96>(maps, args, stream)
+                 : launch_instance<A_TMA_F32, false, 96>(maps, args, stream);
   if (bn != 128) return cudaErrorInvalidValue;
   if (amode == A_TMA_F32)
     return resid ? launch_instance<A_TMA_F32, true, 128>(maps, args, stream)
