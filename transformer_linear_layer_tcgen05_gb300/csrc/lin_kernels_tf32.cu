@@ -8,7 +8,10 @@ namespace lin {
 cudaError_t launch_gemm_tf32(int amode, bool resid, int bn, bool bt, const TensorMaps& maps,
                              const KernelArgs& args, cudaStream_t stream) {
   if (bt) {   // dY · W^T: both operands copied by TMA, nothing to transform
-    if (amode != A_TMA_F32 || bn != 128) return cudaErrorInvalidValue;
+    if (amode != A_TMA_F32 || (bn != 128 && bn != 96)) return cudaErrorInvalidValue;
+    if (bn == 96)
+      return resid ? launch_instance<A_TMA_F32, true, 96, true>(maps, args, stream)
+                   : launch_instance<A_TMA_F32, false, 96, true>(maps, args, stream);
     return resid ? launch_instance<A_TMA_F32, true, 128, true>(maps, args, stream)
                  : launch_instance<A_TMA_F32, false, 128, true>(maps, args, stream);
   }
