@@ -542,23 +542,29 @@ def time_gate_up(iters: int, flush_buf, peaks: dict, M: int = 16384) -> dict:
         lin.lin_matmul_w16(X, WG, G)
         lin.lin_matmul_w16(X, WU, U)
 
-    def median_us(fn):
-        for _ in range(3):
-            fn()
-        torch.cuda.synchronize()
-        times = []
-        for _ in range(max(5, iters // 5)):
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            fn()
-            e1.record(stream)
-            e1.synchronize()
-            times.append(e0.elapsed_time(e1) * 1e3)
-        assert lin.lin_get_device_status() == lin.LIN_SUCCESS
-        return statistics.median(times)
-    sep_us = median_us(separate)
-    us = median_us(call)
+    def timed_us(fn):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1) * 1e3
+
+    # The two ways alternate call by call (medians of each), so that neither
+    # runs in a later, hotter part of the table than the other: under the
+    # power cap the clock falls as the 16k-token tables go on.
+    for _ in range(3):
+        separate()
+        call()
+    torch.cuda.synchronize()
+    sep_times, times = [], []
+    for _ in range(max(5, iters // 5)):
+        sep_times.append(timed_us(separate))
+        times.append(timed_us(call))
+    assert lin.lin_get_device_status() == lin.LIN_SUCCESS
+    sep_us = statistics.median(sep_times)
+    us = statistics.median(times)
     flops = 2 * 2 * M * N * K
     nbytes = M * K * 4 + 2 * K * N * 2 + 2 * M * N * 4
     bf16 = peaks["bf16_tflops"]

@@ -108,3 +108,21 @@ def test_matches_two_single_products():
     lin.lin_matmul_w16(t(d["X"]), t(WU), Y)
     torch.cuda.synchronize()
     assert np.array_equal(Y.cpu().numpy().astype(np.float64), U)
+
+
+def test_pairs_run_as_the_two_single_products():
+    # where the products run as CTA pairs the call is the binary16 pre-pass
+    # and the single-product kernel once per weight matrix, so it equals the
+    # two lin_matmul_w16 calls bit for bit
+    import torch
+    M, N, K = 513, 8192, 512
+    d = wl.generate("matmul_w16", M, N, K, seed=5)
+    WU = wl.generate("matmul_w16", M, N, K, seed=6)["W16"]
+    G, U = _run(d["X"], d["W16"], WU)
+    assert lin.lin_last_launch_info()[0] == 3
+    t = lambda a: torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).cuda()
+    Y = torch.empty((M, N), device="cuda")
+    for W, ref in ((d["W16"], G), (WU, U)):
+        lin.lin_matmul_w16(t(d["X"]), t(W), Y)
+        torch.cuda.synchronize()
+        assert np.array_equal(Y.cpu().numpy().astype(np.float64), ref)

@@ -654,11 +654,34 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
         e = cudaErrorInvalidValue;
       else
         e = lin::launch_cvt_f16(p.X, xh, M * K, sm_count(dev), stream);
-      if (e == cudaSuccess)
+      kernels = 2;
+      if (e == cudaSuccess && dual && pair) {
+        // The gate and up products as CTA pairs: two launches of the
+        // single-product kernel on the one binary16 X, each in its own tile
+        // order (its W alone stays in L2), rather than the dual kernel,
+        // whose tiles hold both products' columns and whose W and W2 need
+        // two bands: at 16k tokens 794 against 883 us (one GB300, the two
+        // ways alternating), and 2 x 100.7 against 226.8 us with 140
+        // against 166 MB of DRAM reads at 4k tokens.
+        lin::KernelArgs a = args;
+        const long long per_ng = (long long)K * lin::kClusterBN * 2;
+        const long long band = per_ng > 0 ? lin::kBandWeightBytes / per_ng : 0;
+        const long long ng = (long long)((N + lin::kClusterBN - 1) / lin::kClusterBN);
+        a.band_ng = band >= 1 && band < ng ? (int)band : 0;
+        e = lin::launch_gemm_cluster_tma(cn, false, maps, a, stream);
+        if (e == cudaSuccess) {
+          lin::TensorMaps m2 = maps;
+          m2.w = maps.w2;
+          m2.y = maps.y2;
+          a.Y = p.Y2;
+          e = lin::launch_gemm_cluster_tma(cn, false, m2, a, stream);
+        }
+        kernels = 3;
+      } else if (e == cudaSuccess) {
         e = dual   ? lin::launch_gemm_cluster_dual(true, cn, maps, args, stream)
             : p.bt ? lin::launch_gemm_cluster_bt(true, cn, resid, maps, args, stream)
                    : lin::launch_gemm_cluster_tma(cn, resid, maps, args, stream);
-      kernels = 2;
+      }
     } else if (dual) {
       e = lin::launch_gemm_cluster_dual(false, cn, maps, args, stream);
     } else if (p.bt) {
