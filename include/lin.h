@@ -308,12 +308,15 @@ lin_status lin_lm_head_cross_entropy_w16(const float *X, const uint16_t *W16,
                                          float alpha, float beta, float inv_norm,
                                          lin_stream_t stream);
 
-/* The SwiGLU FFN's gate and up projections in one launch: GATE[M,N] =
+/* The SwiGLU FFN's gate and up projections from one read of X: GATE[M,N] =
  * X[M,K] @ WG16[K,N] and UP[M,N] = X[M,K] @ WU16[K,N] (binary16 weights, X
  * rounded to binary16 once for both), the producer of lin_matmul_residual_swiglu_a's
  * GATE and UP (N = d_ff). The pages do not describe it (03_linear_forward
  * lists the forward GEMMs only); it is the two matmul_w16 products computed
- * from one read of X. N % 8 == 0, K % 4 == 0; GATE and UP overlap nothing. */
+ * from one read of X: one launch over both products' tiles, or, for shapes
+ * that run as CTA pairs, the binary16 pre-pass and one launch per product
+ * (the results are the same bits as lin_matmul_w16's). N % 8 == 0,
+ * K % 4 == 0; GATE and UP overlap nothing. */
 lin_status lin_gate_up_w16(const float *X, const uint16_t *WG16, const uint16_t *WU16,
                            float *GATE, float *UP, int64_t M, int64_t N, int64_t K,
                            lin_stream_t stream);
