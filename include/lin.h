@@ -315,8 +315,9 @@ lin_status lin_lm_head_cross_entropy_w16(const float *X, const uint16_t *W16,
  * lists the forward GEMMs only); it is the two matmul_w16 products computed
  * from one read of X: one launch over both products' tiles, or, for shapes
  * that run as CTA pairs, the binary16 pre-pass and one launch per product
- * (the results are the same bits as lin_matmul_w16's). N % 8 == 0,
- * K % 4 == 0; GATE and UP overlap nothing. */
+ * (the same rounding of X and the same K order as lin_matmul_w16 where that
+ * runs without a split tail). N % 8 == 0, K % 4 == 0; GATE and UP overlap
+ * nothing. */
 lin_status lin_gate_up_w16(const float *X, const uint16_t *WG16, const uint16_t *WU16,
                            float *GATE, float *UP, int64_t M, int64_t N, int64_t K,
                            lin_stream_t stream);
