@@ -56,6 +56,11 @@ struct GemmTraits {
   // atoms (the layout an MN-major TF32 operand needs).
   static constexpr bool kBT = BT;
   static constexpr bool kXform = kXformA;
+  // Transform warps: warps 4-7 (then the epilogue), and for the forward f32
+  // SwiGLU form, whose transform (two MUFU operations an element) paces its
+  // k-loop, warps 8-11 as well (transform only).
+  static constexpr int XF_WARPS = (AMODE == A_SWIGLU_F32) ? 8 : 4;
+  static constexpr int kThreadsT = (4 + XF_WARPS) * 32;
 
   static constexpr int BM = kBM;
   static constexpr int BN = BN_;
@@ -142,15 +147,16 @@ struct GemmTraits {
 // Build part of one A k-block from one raw stage (32 f32 columns of X or of
 // GATE and UP). `half` selects which 32 columns of the k-block this raw stage
 // holds (always 0 for the f32 operand). tid in [0, 128).
-template <int AMODE>
+template <int AMODE, int NT>
 __device__ __forceinline__ void transform_raw_stage(uint32_t a_stage, uint32_t raw, int half,
                                                     int tid) {
   constexpr uint32_t BOX = kBM * 128;
   if constexpr (AMODE == A_SWIGLU_F32) {
-    // f32 operand: chunk c of row r <- silu(G) * U of the same chunk.
+    // f32 operand: chunk c of row r <- silu(G) * U of the same chunk; the
+    // stage's 1024 chunks over the transform warps' NT threads.
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const uint32_t idx = i * 128 + tid;
+    for (int i = 0; i < 1024 / NT; ++i) {
+      const uint32_t idx = i * NT + tid;
       const uint32_t r = (idx >> 6) * 8 + (idx & 7);
       const uint32_t c = (idx >> 3) & 7;
       const uint32_t off = sw128(r, c);
@@ -343,7 +349,7 @@ __device__ __forceinline__ void cluster_split_sum(uint32_t part, int S, int rank
 // ---------------------------------------------------------------- kernel
 
 template <int AMODE, bool RESID, int BN, bool BT>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(GemmTraits<AMODE, RESID, BN, BT>::kThreadsT, 1)
     lin_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                     const __grid_constant__ CUtensorMap tm_u,
                     const __grid_constant__ CUtensorMap tm_w,
@@ -395,12 +401,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int st = 0; st < T::NS; ++st) {
       mbar_init(bar(T::BAR_OP_TMA + st), 1);
-      mbar_init(bar(T::BAR_OP_XF + st), 4);       // one arrive per transform warp
+      mbar_init(bar(T::BAR_OP_XF + st), T::XF_WARPS);   // one arrive per transform warp
       mbar_init(bar(T::BAR_OP_EMPTY + st), 1);    // tcgen05.commit
     }
     for (int r = 0; r < T::NR; ++r) {
       mbar_init(bar(T::BAR_RAW_FULL + r), 1);
-      mbar_init(bar(T::BAR_RAW_EMPTY + r), 4);
+      mbar_init(bar(T::BAR_RAW_EMPTY + r), T::XF_WARPS);
     }
     mbar_init(bar(T::BAR_ACC_FULL), 1);
     for (int e = 0; e < 8; ++e) mbar_init(bar(T::BAR_EPI + e), 1);
@@ -583,9 +589,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
     }
   } else if (warp >= 4) {
-    // ---------------- warps 4-7: transform, then epilogue
-    const int q = warp - 4;                 // TMEM lane quadrant of this warp
-    const int tid = threadIdx.x - 128;      // 0..127
+    // ---------------- warps 4-7: transform, then epilogue (warps 8-11 of the
+    // f32 SwiGLU form: transform only)
+    const int q = warp - 4;                 // TMEM lane quadrant of this warp (warps 4-7)
+    const int tid = threadIdx.x - 128;      // 0 .. 32 * XF_WARPS - 1
     bool ok = true;
     int t = 0;
     for (int kb = 0; kb < (T::kXform ? nkb : 0) && ok; ++kb) {
@@ -607,7 +614,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                        raw_stage(r) + T::RAW_BOX_BYTES, q, lane);
         else if constexpr (T::kTransA)
           transpose_tile<T::BM>(a_stage(st), raw_stage(r), q, lane);
-        else if constexpr (T::kXformA) transform_raw_stage<AMODE>(a_stage(st), raw_stage(r), h, tid);
+        else if constexpr (T::kXformA)
+          transform_raw_stage<AMODE, 32 * T::XF_WARPS>(a_stage(st), raw_stage(r), h, tid);
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(T::BAR_RAW_EMPTY + r));
       }
@@ -616,9 +624,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(T::BAR_OP_XF + st));
     }
-    // The epilogue buffers alias the raw ring: all four warps must be done
-    // reading it first.
-    named_bar_sync(1, 128);
+    // The epilogue buffers alias the raw ring: every transform warp must be
+    // done reading it first.
+    named_bar_sync(1, 32 * T::XF_WARPS);
+    if (warp < 8) {
 
     const int row0 = m0 + q * kEpiRows;
     const bool rows_in = row0 < args.M;      // a box starting past M would store nothing
@@ -801,6 +810,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (lane == 0) bulk_wait_group_all();
     __syncwarp();
+    }
   }
 
   // ---- teardown (a cluster split first sums the partials: every CTA's is
@@ -860,7 +870,7 @@ cudaError_t launch_instance(const TensorMaps& m, const KernelArgs& args, cudaStr
         ca[0].val.clusterDim.z = grid.z;
         cudaLaunchConfig_t q = {};
         q.gridDim = dim3(1, 1, grid.z);
-        q.blockDim = dim3(kThreads, 1, 1);
+        q.blockDim = dim3(T::kThreadsT, 1, 1);
         q.dynamicSmemBytes = T::SMEM_BYTES;
         q.attrs = ca;
         q.numAttrs = 1;
@@ -885,7 +895,7 @@ cudaError_t launch_instance(const TensorMaps& m, const KernelArgs& args, cudaStr
   attr[1].val.clusterDim.z = grid.z;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(T::kThreadsT, 1, 1);
   cfg.dynamicSmemBytes = T::SMEM_BYTES;
   cfg.stream = stream;
   cfg.attrs = attr;
