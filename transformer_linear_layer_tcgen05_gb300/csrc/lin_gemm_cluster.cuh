@@ -253,16 +253,15 @@ __device__ __forceinline__ void stage_load(Staged<T>& st, const float* __restric
 // The same loads with this lane's first row offset (row * K + its first
 // column), the row stride of its loads and the rows left before M computed
 // once per work item: per k-block only k0 is added.
-template <typename T>
 struct LaneRows {
-  size_t off0;      // first load's row * K + column (row 0 when past M)
+  size_t off0;      // first load's row * K + column
   size_t stride;    // ROWS_PER_LOAD * K
   int rows_left;    // M - the first load's row
   int col;          // this lane's first column within a k-block
 };
 
 template <typename T>
-__device__ __forceinline__ void lane_rows(LaneRows<T>& lr, int row0, int M, int K, int tw,
+__device__ __forceinline__ void lane_rows(LaneRows& lr, int row0, int M, int K, int tw,
                                           int lane) {
   lr.col = T::CHUNK * (lane % T::LANES_PER_ROW);
   const int row = row0 + tw * T::RW + lane / T::LANES_PER_ROW;
@@ -273,7 +272,7 @@ __device__ __forceinline__ void lane_rows(LaneRows<T>& lr, int row0, int M, int 
 
 template <typename T>
 __device__ __forceinline__ void stage_load_at(Staged<T>& st, const float* __restrict__ a,
-                                              const float* __restrict__ u, const LaneRows<T>& lr,
+                                              const float* __restrict__ u, const LaneRows& lr,
                                               int k0, int K, int* status) {
   const int col = k0 + lr.col;
   // (K is a multiple of CHUNK on each path: a load is wholly in or out)
@@ -668,7 +667,7 @@ __global__ void __launch_bounds__(ClusterTraits<AMODE, RESID, BN, CN, V8, BT, DU
     // item takes the divisions of `coords` (they would otherwise sit on the
     // path to every load's issue).
     int cur_g = -1, cur_row0 = 0, cur_k0 = 0, cur_kend = 0;
-    LaneRows<T> cur_rows;
+    LaneRows cur_rows;
     auto cursor_to = [&](int g) {
       if (cur_g >= 0 && g - cur_g == T::XF_GROUPS && cur_k0 + T::XF_GROUPS * T::BK < cur_kend) {
         cur_k0 += T::XF_GROUPS * T::BK;
