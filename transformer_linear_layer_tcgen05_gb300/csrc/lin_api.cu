@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
 #include <cstdlib>
@@ -276,15 +277,18 @@ int f32_swiglu_bn(uint64_t N) {
 }
 
 // Tile width of the per-tile kernel for the f32 forms that copy X (or dY) as
-// is (matmul, matmul_residual, and matmul_t, whose W tile is K-major): 96
-// columns while the 96-column tiles fit one wave on the SMs (the 512-token
-// shapes: more SMs busy, or a smaller K split), else 128; for matmul_t only
-// where 128-column tiles would split K. Measured on one GB300 (warm µs,
-// 128 -> 96 columns): ffn_up_residual_f32 12.8 -> 12.25, attn_proj_f32
-// 7.46 -> 7.14 (K split 5 -> 4), attn_proj_dx_f32 7.44 -> 7.11; but
-// ffn_up_dx_f32 (no split either way) 12.3 -> 12.85. Cold unchanged.
+// is (matmul, matmul_residual, and matmul_t, whose W tile is K-major), for
+// the 512-token shapes: where 128-column tiles leave the SMs to a K split,
+// 96 columns (a smaller split, a smaller partial tile to sum) when the
+// contraction is short (at most 32 k-blocks), else 128 (the longer K
+// ranges of the smaller split cost more than the sum saves); where they do
+// not split, 96 columns while the 96-column tiles fit one wave (more SMs
+// busy). Measured on one GB300 (warm µs, 128 -> 96 columns):
+// attn_proj_f32 7.46 -> 7.14 and attn_proj_dx_f32 7.44 -> 7.11 (contraction
+// 768, split 6 -> 4), ffn_up_dx_f32 12.3 -> 12.85 (contraction 3072: kept at
+// 128), ffn_up_residual_f32 12.8 -> 12.25 (no split; 96 -> 128 tiles).
 // LIN_F32_BN=96 / 128 forces it (measurements).
-int f32_x_bn(uint64_t M, uint64_t N, bool bt, int sms) {
+int f32_x_bn(uint64_t M, uint64_t N, uint64_t K, int sms) {
   static const int forced = [] {
     const char* v = std::getenv("LIN_F32_BN");
     if (!v) return -1;
@@ -293,8 +297,11 @@ int f32_x_bn(uint64_t M, uint64_t N, bool bt, int sms) {
   if (forced > 0) return forced;
   const uint64_t rows = (M + lin::kBM - 1) / lin::kBM;
   const uint64_t t96 = rows * ((N + 95) / 96), t128 = rows * ((N + 127) / 128);
+  const uint64_t nkb = (K + 31) / 32;
   if (t96 > (uint64_t)sms) return 128;
-  return (!bt || 2 * t128 <= (uint64_t)sms) ? 96 : 128;
+  const uint64_t split128 = std::min<uint64_t>((uint64_t)sms / t128, nkb / 4);
+  if (split128 >= 2) return nkb <= 32 ? 96 : 128;
+  return 96;
 }
 
 enum Form : int { F_MATMUL = 0, F_RESID = 1, F_SWIGLU = 2 };
@@ -449,7 +456,7 @@ lin_status run(const Problem& p, cudaStream_t stream, lin::WorkspaceGetter fixed
 
   // 8. tensor maps and launch
   const int bn = (swiglu && !p.w16 && !p.at && !p.bt) ? f32_swiglu_bn(N)
-                 : (!swiglu && !p.w16 && !p.at) ? f32_x_bn(M, N, p.bt, sm_count(dev))
+                 : (!swiglu && !p.w16 && !p.at) ? f32_x_bn(M, N, K, sm_count(dev))
                                                          : 128;
   int cn = (p.w16 && !p.at) ? f16_cluster_size(N) : 0;   // 0: the per-tile kernel
   // the row partials and the dual product exist in the clustered kernel only
